@@ -1,0 +1,119 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module only draws random numbers and lays them out; it holds none of
+the product's arithmetic, so both the CUDA path (tests, benchmark) and the
+CPU oracle can be fed from it.
+
+Operand rounding follows the Phobos "@tensorcore" page, section "The
+forms" (operands are rounded to f16 before the tensor cores see them):
+values are drawn in fp32 and rounded once, round-to-nearest-even, by
+``Tensor.half()`` / ``Tensor.bfloat16()``.  Storage is row-major; A is
+stored [M, K] (or [K, M] when transposed), B [K, N] (or [N, K]), C and D
+[M, N].
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+@dataclasses.dataclass(frozen=True)
+class GemmCase:
+    """One synthetic GEMM workload: shapes, value distributions, scalars."""
+    name: str
+    M: int
+    N: int
+    K: int
+    in_dtype: str = "f16"          # dtype of A and B
+    out_dtype: str = "f32"         # dtype of C and D
+    dist: str = "normal"           # "normal" (mean 0, std) or "uniform" on [-1, 1]
+    std: float = 1.0
+    transA: int = 0
+    transB: int = 0
+    alpha: float = 1.0
+    beta: float = 0.0
+    c_dist: str = "normal"         # distribution of C when beta != 0
+    seed: int = 0
+
+    @property
+    def a_shape(self):
+        return (self.K, self.M) if self.transA else (self.M, self.K)
+
+    @property
+    def b_shape(self):
+        return (self.N, self.K) if self.transB else (self.K, self.N)
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Each operand read once, C read once when beta != 0, D written once."""
+        isz = 2
+        osz = 4 if self.out_dtype == "f32" else 2
+        return isz * (self.M * self.K + self.K * self.N) + osz * self.M * self.N * (1 + (self.beta != 0))
+
+
+def _draw(gen, shape, dist, std):
+    if dist == "uniform":
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * 2.0 - 1.0
+    if dist == "normal":
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        return x * std if std != 1.0 else x
+    raise ValueError(dist)
+
+
+def make_inputs(case: GemmCase):
+    """CPU tensors (A, B, C) for ``case``; C is None when beta == 0.
+
+    The generator is ``torch.Generator().manual_seed(case.seed)``; A, B
+    and C are drawn from it in that order.
+    """
+    gen = torch.Generator().manual_seed(case.seed)
+    dt = _TORCH_DTYPE[case.in_dtype]
+    A = _draw(gen, case.a_shape, case.dist, case.std).to(dt)
+    B = _draw(gen, case.b_shape, case.dist, case.std).to(dt)
+    C = None
+    if case.beta != 0.0:
+        C = _draw(gen, (case.M, case.N), case.c_dist, 1.0).to(_TORCH_DTYPE[case.out_dtype])
+    return A, B, C
+
+
+def integer_matrix(shape, lo, hi, seed, dtype="f16"):
+    """Integer-valued matrix with entries uniform on [lo, hi], seeded."""
+    gen = torch.Generator().manual_seed(seed)
+    x = torch.randint(lo, hi + 1, shape, generator=gen, dtype=torch.int32)
+    return x.to(_TORCH_DTYPE[dtype])
+
+
+# The workloads the benchmark and the parity tests run, in a fixed order; the
+# seed of the i-th entry (1-based) is 1000 + i.
+def _cases():
+    k8192 = 8192
+    rows = [
+        # single m16n8k16 atom: TIRx "gemm" page, "Demonstration program"
+        GemmCase("single_atom_16x8x16_f16", 16, 8, 16, "f16", dist="uniform"),
+        GemmCase("gemm_512_f16_alpha1.5_beta0.5", 512, 512, 512, "f16", dist="normal",
+                 alpha=1.5, beta=0.5, c_dist="normal"),
+        GemmCase("gemm_4096_bf16_transB_beta1", 4096, 4096, 4096, "bf16", dist="uniform",
+                 transB=1, alpha=1.0, beta=1.0, c_dist="uniform"),
+        GemmCase("gemm_8192_f16", k8192, k8192, k8192, "f16", dist="normal",
+                 std=1.0 / math.sqrt(k8192)),
+        GemmCase("sweep_8192x8192_K256_f16", 8192, 8192, 256, "f16"),
+        GemmCase("sweep_8192x8192_K1024_f16", 8192, 8192, 1024, "f16"),
+        GemmCase("sweep_8192x8192_K4096_f16", 8192, 8192, 4096, "f16"),
+        GemmCase("sweep_8192x8192_K16384_f16", 8192, 8192, 16384, "f16"),
+        GemmCase("tall_skinny_32768x256x4096_f16", 32768, 256, 4096, "f16"),
+        GemmCase("unaligned_1000_f16", 1000, 1000, 1000, "f16"),
+    ]
+    return [dataclasses.replace(c, seed=1000 + i + 1) for i, c in enumerate(rows)]
+
+
+CASES = _cases()
+CASE_BY_NAME = {c.name: c for c in CASES}
+HEADLINE = CASE_BY_NAME["gemm_8192_f16"]

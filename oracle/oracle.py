@@ -1,0 +1,210 @@
+"""Python face of the CPU oracle (``oracle_gemm.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's ``cpu_baseline`` / reference leg are the only callers.  Nothing
+here imports the product package, and the product package never imports
+this module.
+
+The oracle computes ``D = alpha * op(A) @ op(B) + beta * C`` by the plain
+definition in binary64 (TVM TIRx "gemm" page, opening paragraph and the
+"What it accepts" table; Phobos "@tensorcore" page, the
+gemm_fp16tc_fp32acc.ph epilogue), and the per-element error bound
+``|alpha| * sum_k |a_ik * b_kj| + |beta| * |c_ij|``.
+
+Inputs are numpy arrays or torch CPU tensors: A and B hold fp16 / bf16
+bits, C holds fp32 (or fp16 / bf16 bits when the output is 16-bit).
+Row-major with explicit leading dimensions.
+"""
+from __future__ import annotations
+
+import concurrent.futures as _cf
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+F16, BF16, F32 = 0, 1, 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "oracle_gemm.c")
+LIBRARY = os.path.join(_HERE, "liboracle_gemm.so")
+CFLAGS = ["-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC"]
+
+
+def compile_library(src: str, out: str) -> str:
+    """gcc ``src`` into the shared library ``out`` (atomically replaced)."""
+    tmp = out + ".tmp.%d" % os.getpid()
+    subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, src, "-lm", "-lpthread"])
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle_gemm.c`` into ``liboracle_gemm.so`` beside it."""
+    if force or not os.path.exists(LIBRARY) or os.path.getmtime(LIBRARY) < os.path.getmtime(SOURCE):
+        compile_library(SOURCE, LIBRARY)
+    return LIBRARY
+
+
+def _bits16(x):
+    """A 2-D uint16 array of fp16 / bf16 bit patterns."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):                      # torch tensor
+        import torch
+        x = x.detach().cpu().contiguous().view(torch.int16).numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float16:
+        x = x.view(np.uint16)
+    if x.dtype not in (np.uint16, np.int16):
+        raise TypeError("16-bit operand expected, got %s" % x.dtype)
+    return x.view(np.uint16)
+
+
+def _c_array(c, c_dtype):
+    if c is None:
+        return None
+    if hasattr(c, "detach"):
+        import torch
+        c = c.detach().cpu().contiguous()
+        c = c.numpy() if c.dtype == torch.float32 else c.view(torch.int16).numpy()
+    c = np.ascontiguousarray(c)
+    if c_dtype == F32:
+        if c.dtype != np.float32:
+            raise TypeError("fp32 C expected, got %s" % c.dtype)
+        return c
+    return _bits16(c)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _ld(arr, default):
+    return arr.shape[1] if arr is not None and arr.ndim == 2 else default
+
+
+class Oracle:
+    """One loaded build of the oracle library."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        i64, i32, dbl, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+        lib.oracle_decode_f16.restype = dbl
+        lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
+        lib.oracle_decode_bf16.restype = dbl
+        lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
+        lib.oracle_gemm.restype = i32
+        lib.oracle_gemm.argtypes = [vp, vp, i64, vp, vp, vp, i64, i64, i64, i64, i64, i64,
+                                    i32, i32, dbl, dbl, i32, i32, i64, i64]
+        lib.oracle_gemm_entries.restype = i32
+        lib.oracle_gemm_entries.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, i64, i64, i64,
+                                            i64, i64, i64, i32, i32, dbl, dbl, i32, i32]
+        self.lib = lib
+        self.path = path
+
+    def decode_f16(self, bits: int) -> float:
+        return self.lib.oracle_decode_f16(int(bits))
+
+    def decode_bf16(self, bits: int) -> float:
+        return self.lib.oracle_decode_bf16(int(bits))
+
+    def gemm(self, A, B, C, M, N, K, *, transA=0, transB=0, alpha=1.0, beta=0.0,
+             in_dtype=F16, c_dtype=F32, lda=None, ldb=None, ldc=None,
+             rows=None, threads=1):
+        """Full rows of D (all rows unless ``rows=(begin, end)``).
+
+        Returns ``(D, bound)``: float64 arrays of shape [M, N]; rows outside
+        the requested range stay NaN.  ``threads > 1`` runs disjoint row
+        blocks of the same single-threaded C loop concurrently.
+        """
+        A16, B16 = _bits16(A), _bits16(B)
+        C_ = _c_array(C, c_dtype) if beta != 0.0 else None
+        lda = lda if lda is not None else _ld(A16, M if transA else K)
+        ldb = ldb if ldb is not None else _ld(B16, K if transB else N)
+        ldc = ldc if ldc is not None else _ld(C_, N)
+        D = np.full((M, N), np.nan)
+        bound = np.full((M, N), np.nan)
+        r0, r1 = rows if rows is not None else (0, M)
+        lib = self.lib
+
+        def run(a, b):
+            rc = lib.oracle_gemm(D.ctypes.data, bound.ctypes.data, N, _ptr(A16), _ptr(B16),
+                                 _ptr(C_), M, N, K, lda, ldb, ldc, int(transA), int(transB),
+                                 float(alpha), float(beta), int(in_dtype), int(c_dtype), a, b)
+            if rc != 0:
+                raise ValueError("oracle_gemm rejected its arguments")
+
+        if threads <= 1 or r1 - r0 < 2:
+            run(r0, r1)
+        else:
+            step = max(1, (r1 - r0 + threads * 4 - 1) // (threads * 4))
+            with _cf.ThreadPoolExecutor(threads) as ex:
+                list(ex.map(lambda a: run(a, min(a + step, r1)), range(r0, r1, step)))
+        return D, bound
+
+    def gemm_entries(self, A, B, C, M, N, K, rows, cols, *, transA=0, transB=0, alpha=1.0,
+                     beta=0.0, in_dtype=F16, c_dtype=F32, lda=None, ldb=None, ldc=None,
+                     threads=1):
+        """D and bound at the listed (rows[e], cols[e]) positions only."""
+        A16, B16 = _bits16(A), _bits16(B)
+        C_ = _c_array(C, c_dtype) if beta != 0.0 else None
+        lda = lda if lda is not None else _ld(A16, M if transA else K)
+        ldb = ldb if ldb is not None else _ld(B16, K if transB else N)
+        ldc = ldc if ldc is not None else _ld(C_, N)
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        cols = np.ascontiguousarray(cols, dtype=np.int64)
+        n = rows.shape[0]
+        D = np.empty(n)
+        bound = np.empty(n)
+        lib = self.lib
+
+        def run(a, b):
+            rc = lib.oracle_gemm_entries(D[a:].ctypes.data, bound[a:].ctypes.data,
+                                         rows[a:].ctypes.data, cols[a:].ctypes.data, b - a,
+                                         _ptr(A16), _ptr(B16), _ptr(C_), M, N, K, lda, ldb, ldc,
+                                         int(transA), int(transB), float(alpha), float(beta),
+                                         int(in_dtype), int(c_dtype))
+            if rc != 0:
+                raise ValueError("oracle_gemm_entries rejected its arguments")
+
+        if n == 0:
+            return D, bound
+        if threads <= 1 or n < 2:
+            run(0, n)
+        else:
+            step = max(1, (n + threads * 4 - 1) // (threads * 4))
+            with _cf.ThreadPoolExecutor(threads) as ex:
+                list(ex.map(lambda a: run(a, min(a + step, n)), range(0, n, step)))
+        return D, bound
+
+
+_default = None
+_default_lock = threading.Lock()
+
+
+def default() -> Oracle:
+    """The oracle built from ``oracle_gemm.c`` (compiled on first use)."""
+    global _default
+    with _default_lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def gemm(*args, **kwargs):
+    return default().gemm(*args, **kwargs)
+
+
+def gemm_entries(*args, **kwargs):
+    return default().gemm_entries(*args, **kwargs)
+
+
+def decode_f16(bits):
+    return default().decode_f16(bits)
+
+
+def decode_bf16(bits):
+    return default().decode_bf16(bits)

@@ -1,0 +1,235 @@
+/*
+ * CPU oracle for the dense matrix product  D = alpha * op(A) @ op(B) + beta * C.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may load, link or
+ * call this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg do.  It shares no code, header, table or constant with the
+ * CUDA path; the two meet only through the seeded inputs they are handed.
+ *
+ * What it computes (the plain definition, written out):
+ *
+ *   TVM TIRx "gemm" page, opening paragraph and the "What it accepts" table
+ *   (rows "dtype" and "alpha / beta"); the TIRx gemm guide, section 一
+ *   ("语义定义"); Phobos "@tensorcore" page, example gemm_fp16tc_fp32acc.ph
+ *   (epilogue  alpha * acc + beta * c_old):
+ *
+ *     D[i][j] = alpha * sum_{k=0}^{K-1} Ahat[i][k] * Bhat[k][j]  +  beta * C[i][j]
+ *
+ *   Ahat = A   (transA = 0, A stored M x K)  or  A^T (transA = 1, stored K x M)
+ *   Bhat = B   (transB = 0, B stored K x N)  or  B^T (transB = 1, stored N x K)
+ *
+ *   The transpose flags only name the logical orientation; the operation is
+ *   normalised to A = [M,K], B = [K,N], C = D = [M,N] (TIRx gemm guide,
+ *   section 二, "维度一致性").  Storage is row-major; a leading dimension is
+ *   the row stride in elements (the demonstration program on the TIRx
+ *   "gemm" page indexes A_g[m, k], B_g[k, n], D_g[m, n]).
+ *
+ *   beta == 0 means "D zero-initialised": C is never read, so a NaN in C
+ *   cannot reach D ("What it accepts" table, alpha / beta row; the
+ *   "How inputs change the algorithm" table, beta row).
+ *
+ * Precision: every fp16 / bf16 / fp32 element is decoded exactly to a
+ * double by the decoders below, products and sums are taken in double
+ * (binary64), in increasing k order, one output element at a time.  The
+ * sum of |products| is kept alongside, so the caller can form the
+ * per-element error bound  |alpha| * sum|a*b| + |beta| * |c|.
+ *
+ * Build: a plain C99 compiler, -O2, -ffp-contract=off (no fused
+ * multiply-add, no fast-math), so that x86-64 and aarch64 give the same
+ * bits.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <string.h>
+
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2 };
+
+/* ---- exact element decoders -------------------------------------------- */
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+double oracle_decode_f16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);               /* subnormal: f * 2^-14 * 2^-10 */
+    else if (e == 31)
+        v = (f == 0) ? INFINITY : NAN;
+    else
+        v = ldexp((double)(1024 + f), e - 25);   /* 1.f * 2^(e-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper half of an IEEE 754 binary32 (8 exponent bits, bias
+ * 127, 7 fraction bits). */
+double oracle_decode_bf16(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 7) & 0xff;
+    int f = h & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);              /* subnormal: f * 2^-126 * 2^-7 */
+    else if (e == 255)
+        v = (f == 0) ? INFINITY : NAN;
+    else
+        v = ldexp((double)(128 + f), e - 134);   /* 1.f * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+/* binary32 -> binary64 is exact. */
+static double decode_f32(const void* p)
+{
+    float x;
+    memcpy(&x, p, sizeof x);
+    return (double)x;
+}
+
+/* The 16-bit decoders above are memoised in two 2^16-entry tables, filled
+ * once by calling them on every bit pattern (pthread_once: the tests call
+ * the oracle from several threads at a time). */
+static double g_f16_table[65536];
+static double g_bf16_table[65536];
+static pthread_once_t g_tables_once = PTHREAD_ONCE_INIT;
+
+static void fill_tables(void)
+{
+    for (uint32_t h = 0; h < 65536u; ++h) {
+        g_f16_table[h] = oracle_decode_f16((uint16_t)h);
+        g_bf16_table[h] = oracle_decode_bf16((uint16_t)h);
+    }
+}
+
+static const double* table_for(int dtype)
+{
+    pthread_once(&g_tables_once, fill_tables);
+    return dtype == ORACLE_F16 ? g_f16_table : g_bf16_table;
+}
+
+/* ---- operand access ------------------------------------------------------ */
+
+typedef struct {
+    const uint16_t* A;
+    const uint16_t* B;
+    const void* C;
+    int64_t M, N, K, lda, ldb, ldc;
+    int transA, transB;
+    double alpha, beta;
+    const double* in_table;   /* decoder for A and B */
+    int c_dtype;
+} problem_t;
+
+/* Ahat[i][k] */
+static double a_hat(const problem_t* p, int64_t i, int64_t k)
+{
+    uint16_t bits = p->transA ? p->A[k * p->lda + i] : p->A[i * p->lda + k];
+    return p->in_table[bits];
+}
+
+/* Bhat[k][j] */
+static double b_hat(const problem_t* p, int64_t k, int64_t j)
+{
+    uint16_t bits = p->transB ? p->B[j * p->ldb + k] : p->B[k * p->ldb + j];
+    return p->in_table[bits];
+}
+
+static double c_elem(const problem_t* p, int64_t i, int64_t j)
+{
+    int64_t off = i * p->ldc + j;
+    if (p->c_dtype == ORACLE_F32)
+        return decode_f32((const char*)p->C + 4 * off);
+    const uint16_t bits = ((const uint16_t*)p->C)[off];
+    return p->c_dtype == ORACLE_F16 ? oracle_decode_f16(bits) : oracle_decode_bf16(bits);
+}
+
+/* One output element by the definition; *bound gets
+ * |alpha| * sum_k |Ahat[i][k] * Bhat[k][j]| + |beta| * |C[i][j]|. */
+static double one_element(const problem_t* p, int64_t i, int64_t j, double* bound)
+{
+    double s = 0.0, sa = 0.0;
+    for (int64_t k = 0; k < p->K; ++k) {
+        double prod = a_hat(p, i, k) * b_hat(p, k, j);
+        s += prod;
+        sa += fabs(prod);
+    }
+    double d = p->alpha * s;
+    double b = fabs(p->alpha) * sa;
+    if (p->beta != 0.0) {             /* beta == 0: C is not read */
+        double c = c_elem(p, i, j);
+        d += p->beta * c;
+        b += fabs(p->beta) * fabs(c);
+    }
+    *bound = b;
+    return d;
+}
+
+static int setup(problem_t* p, const void* A, const void* B, const void* C,
+                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc,
+                 int transA, int transB, double alpha, double beta,
+                 int in_dtype, int c_dtype)
+{
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if (in_dtype != ORACLE_F16 && in_dtype != ORACLE_BF16) return -1;
+    if (c_dtype != ORACLE_F16 && c_dtype != ORACLE_BF16 && c_dtype != ORACLE_F32) return -1;
+    if ((M > 0 && K > 0 && A == NULL) || (K > 0 && N > 0 && B == NULL)) return -1;
+    if (beta != 0.0 && M > 0 && N > 0 && C == NULL) return -1;
+    /* the stored row length must fit in the leading dimension */
+    if (K > 0 && lda < (transA ? M : K)) return -1;
+    if (K > 0 && ldb < (transB ? K : N)) return -1;
+    if (beta != 0.0 && ldc < N) return -1;
+    p->A = (const uint16_t*)A;
+    p->B = (const uint16_t*)B;
+    p->C = C;
+    p->M = M; p->N = N; p->K = K;
+    p->lda = lda; p->ldb = ldb; p->ldc = ldc;
+    p->transA = transA != 0; p->transB = transB != 0;
+    p->alpha = alpha; p->beta = beta;
+    p->in_table = table_for(in_dtype);
+    p->c_dtype = c_dtype;
+    return 0;
+}
+
+/* Full rows [row_begin, row_end) of D.  D and bound are dense [M, N]
+ * double arrays with row stride ldo; only the requested rows are written.
+ * Returns 0, or -1 on a malformed argument. */
+int oracle_gemm(double* D, double* bound, int64_t ldo,
+                const void* A, const void* B, const void* C,
+                int64_t M, int64_t N, int64_t K,
+                int64_t lda, int64_t ldb, int64_t ldc,
+                int transA, int transB, double alpha, double beta,
+                int in_dtype, int c_dtype,
+                int64_t row_begin, int64_t row_end)
+{
+    problem_t p;
+    if (setup(&p, A, B, C, M, N, K, lda, ldb, ldc, transA, transB, alpha, beta,
+              in_dtype, c_dtype) != 0)
+        return -1;
+    if (row_begin < 0 || row_end > M || row_begin > row_end || ldo < N) return -1;
+    for (int64_t i = row_begin; i < row_end; ++i)
+        for (int64_t j = 0; j < N; ++j)
+            D[i * ldo + j] = one_element(&p, i, j, &bound[i * ldo + j]);
+    return 0;
+}
+
+/* The listed elements (rows[e], cols[e]) only, e < count: D[e], bound[e]. */
+int oracle_gemm_entries(double* D, double* bound,
+                        const int64_t* rows, const int64_t* cols, int64_t count,
+                        const void* A, const void* B, const void* C,
+                        int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldc,
+                        int transA, int transB, double alpha, double beta,
+                        int in_dtype, int c_dtype)
+{
+    problem_t p;
+    if (setup(&p, A, B, C, M, N, K, lda, ldb, ldc, transA, transB, alpha, beta,
+              in_dtype, c_dtype) != 0)
+        return -1;
+    for (int64_t e = 0; e < count; ++e)
+        if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
+    for (int64_t e = 0; e < count; ++e)
+        D[e] = one_element(&p, rows[e], cols[e], &bound[e]);
+    return 0;
+}

@@ -1,0 +1,313 @@
+"""Pins for the CPU oracle: checks against facts fixed outside the oracle.
+
+Each ``pin_*`` function takes a loaded ``Oracle`` and raises
+``AssertionError`` when the oracle disagrees with something the pages or
+plain mathematics fix:
+
+* exact decoding of every fp16 / bf16 bit pattern (numpy's IEEE binary16,
+  and bfloat16 defined as the upper half of binary32);
+* brute force in Python integers on integer-valued inputs, with padded
+  leading dimensions and all four transpose forms (exact);
+* numpy's float64 matmul on random inputs (a library routine);
+* identity and permutation operands, beta = 0 vs beta = 1 semantics (TIRx
+  "gemm" page, "What it accepts" table, alpha / beta row: 0 -> D = A@B,
+  1 -> D = A@B + C), transpose equivalence (the flags only name the
+  logical orientation), linearity in alpha and beta, a closed-form sum and
+  the error bound's own identities.
+
+``tests/test_oracle_mutants.py`` runs the same pins against deliberately
+broken builds of the oracle and requires each break to be caught.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle.oracle import BF16, F16, F32
+
+F16_NAN = 0x7E00
+BF16_NAN = 0x7FC0
+_TD = {F16: torch.float16, BF16: torch.bfloat16}
+
+
+def _same(a, b):
+    """Bitwise-equal doubles, NaN equal to NaN."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    both_nan = np.isnan(a) & np.isnan(b)
+    eq = (a == b) & (np.signbit(a) == np.signbit(b))
+    return bool(np.all(both_nan | eq))
+
+
+def _int_tensor(rng, shape, lo, hi, dtype):
+    return torch.from_numpy(rng.integers(lo, hi + 1, size=shape).astype(np.float32)).to(_TD[dtype])
+
+
+def _padded(x16: torch.Tensor, pad: int, dtype):
+    """Copy of a 2-D 16-bit tensor into a buffer with `pad` extra NaN columns.
+
+    Returns (buffer as uint16 numpy, leading dimension)."""
+    bits = x16.contiguous().view(torch.int16).numpy().view(np.uint16)
+    rows, cols = bits.shape
+    buf = np.full((rows, cols + pad), F16_NAN if dtype == F16 else BF16_NAN, dtype=np.uint16)
+    buf[:, :cols] = bits
+    return buf, cols + pad
+
+
+def _as_int_lists(x: torch.Tensor):
+    return x.to(torch.int64).tolist()
+
+
+def pin_decoders(orc):
+    h = np.arange(65536, dtype=np.uint32)
+    ref16 = h.astype(np.uint16).view(np.float16).astype(np.float64)
+    refbf = (h << 16).view(np.float32).astype(np.float64)
+    got16 = np.array([orc.decode_f16(x) for x in range(65536)])
+    gotbf = np.array([orc.decode_bf16(x) for x in range(65536)])
+    assert _same(got16, ref16), "fp16 decoder disagrees with IEEE binary16"
+    assert _same(gotbf, refbf), "bf16 decoder disagrees with the upper half of binary32"
+
+
+def _brute(A, B, C, transA, transB, alpha, beta):
+    """Exact integer D by the definition, Python ints only."""
+    a = _as_int_lists(A)
+    b = _as_int_lists(B)
+    c = _as_int_lists(C) if C is not None else None
+    M = len(a[0]) if transA else len(a)
+    K = len(a) if transA else len(a[0])
+    N = len(b) if transB else len(b[0])
+    D = [[0] * N for _ in range(M)]
+    for i in range(M):
+        for j in range(N):
+            s = 0
+            for k in range(K):
+                aik = a[k][i] if transA else a[i][k]
+                bkj = b[j][k] if transB else b[k][j]
+                s += aik * bkj
+            D[i][j] = alpha * s + (beta * c[i][j] if beta != 0 else 0)
+    return D
+
+
+def pin_brute_force_integers(orc):
+    rng = np.random.default_rng(7)
+    shapes = [(16, 8, 16), (3, 5, 7), (1, 1, 1), (17, 9, 33), (5, 2, 40)]
+    for dtype in (F16, BF16):
+        for (M, N, K) in shapes:
+            for transA in (0, 1):
+                for transB in (0, 1):
+                    for alpha, beta in ((1, 0), (1, 1), (-3, 1), (2, 0)):
+                        A = _int_tensor(rng, (K, M) if transA else (M, K), -8, 8, dtype)
+                        B = _int_tensor(rng, (N, K) if transB else (K, N), -8, 8, dtype)
+                        C = torch.from_numpy(rng.integers(-100, 101, size=(M, N)).astype(np.float32))
+                        Ab, lda = _padded(A, 3, dtype)
+                        Bb, ldb = _padded(B, 5, dtype)
+                        Cb = np.full((M, N + 2), np.nan, dtype=np.float32)
+                        Cb[:, :N] = C.numpy()
+                        D, _ = orc.gemm(Ab, Bb, Cb, M, N, K, transA=transA, transB=transB,
+                                        alpha=alpha, beta=beta, in_dtype=dtype, c_dtype=F32,
+                                        lda=lda, ldb=ldb, ldc=N + 2)
+                        ref = _brute(A, B, C if beta else None, transA, transB, alpha, beta)
+                        assert np.array_equal(D, np.array(ref, dtype=np.float64)), \
+                            "brute force mismatch M,N,K=%s trans=%d%d alpha=%s beta=%s dtype=%d" % (
+                                (M, N, K), transA, transB, alpha, beta, dtype)
+
+
+def _op(x64, trans):
+    return x64.T if trans else x64
+
+
+def pin_numpy_float64(orc):
+    rng = np.random.default_rng(11)
+    M, N, K = 37, 29, 53
+    for dtype in (F16, BF16):
+        for transA in (0, 1):
+            for transB in (0, 1):
+                A = torch.from_numpy(rng.standard_normal((K, M) if transA else (M, K)).astype(np.float32)).to(_TD[dtype])
+                B = torch.from_numpy(rng.standard_normal((N, K) if transB else (K, N)).astype(np.float32)).to(_TD[dtype])
+                C = rng.standard_normal((M, N)).astype(np.float32)
+                D, bound = orc.gemm(A, B, C, M, N, K, transA=transA, transB=transB,
+                                    alpha=1.5, beta=0.5, in_dtype=dtype)
+                a64 = _op(A.double().numpy(), transA)
+                b64 = _op(B.double().numpy(), transB)
+                ref = 1.5 * (a64 @ b64) + 0.5 * C.astype(np.float64)
+                assert np.all(np.abs(D - ref) <= 1e-12 * bound + 1e-300), \
+                    "numpy float64 matmul mismatch (trans=%d%d dtype=%d)" % (transA, transB, dtype)
+
+
+def pin_identity(orc):
+    rng = np.random.default_rng(13)
+    K, N = 24, 19
+    for dtype in (F16, BF16):
+        for transB in (0, 1):
+            eye = torch.eye(K, dtype=_TD[dtype])
+            B = torch.from_numpy(rng.standard_normal((N, K) if transB else (K, N)).astype(np.float32)).to(_TD[dtype])
+            C = rng.standard_normal((K, N)).astype(np.float32)
+            D, _ = orc.gemm(eye, B, C, K, N, K, transB=transB, alpha=1.5, beta=0.5, in_dtype=dtype)
+            ref = 1.5 * _op(B.double().numpy(), transB) + 0.5 * C.astype(np.float64)
+            assert _same(D, ref), "identity operand: D != alpha*B + beta*C"
+
+
+def pin_permutation(orc):
+    rng = np.random.default_rng(17)
+    K, N = 21, 13
+    perm = rng.permutation(K)
+    P = torch.zeros((K, K), dtype=torch.float16)
+    P[torch.arange(K), torch.from_numpy(perm)] = 1.0
+    B = torch.from_numpy(rng.standard_normal((K, N)).astype(np.float32)).half()
+    for transA in (0, 1):
+        A = P.T.contiguous() if transA else P
+        D, _ = orc.gemm(A, B, None, K, N, K, transA=transA)
+        assert _same(D, B.double().numpy()[perm, :]), "permutation operand: rows not permuted"
+
+
+def pin_beta_semantics(orc):
+    rng = np.random.default_rng(19)
+    M, N, K = 9, 11, 14
+    A = _int_tensor(rng, (M, K), -8, 8, F16)
+    B = _int_tensor(rng, (K, N), -8, 8, F16)
+    C = rng.integers(-50, 51, size=(M, N)).astype(np.float32)
+    D0, _ = orc.gemm(A, B, C, M, N, K, beta=0.0)
+    D1, _ = orc.gemm(A, B, C, M, N, K, beta=1.0)
+    assert np.array_equal(D1 - D0, C.astype(np.float64)), "D(beta=1) - D(beta=0) != C"
+    Cnan = np.full((M, N), np.nan, dtype=np.float32)
+    Dn, bn = orc.gemm(A, B, Cnan, M, N, K, beta=0.0)
+    assert np.all(np.isfinite(Dn)) and np.all(np.isfinite(bn)), "beta=0 read C"
+    assert np.array_equal(Dn, D0)
+    # K = 0: the sum is empty, D = beta * C
+    Dk, bk = orc.gemm(None, None, C, M, N, 0, alpha=2.0, beta=0.5, lda=1, ldb=N)
+    assert np.array_equal(Dk, 0.5 * C.astype(np.float64)) and np.array_equal(bk, np.abs(0.5 * C.astype(np.float64)))
+
+
+def pin_transpose_equivalence(orc):
+    rng = np.random.default_rng(23)
+    M, N, K = 13, 10, 27
+    for dtype in (F16, BF16):
+        A = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(_TD[dtype])
+        B = torch.from_numpy(rng.standard_normal((K, N)).astype(np.float32)).to(_TD[dtype])
+        base, _ = orc.gemm(A, B, None, M, N, K, in_dtype=dtype)
+        for transA in (0, 1):
+            for transB in (0, 1):
+                As = A.T.contiguous() if transA else A
+                Bs = B.T.contiguous() if transB else B
+                D, _ = orc.gemm(As, Bs, None, M, N, K, transA=transA, transB=transB, in_dtype=dtype)
+                assert _same(D, base), "transpose forms disagree (trans=%d%d)" % (transA, transB)
+
+
+def pin_linearity(orc):
+    rng = np.random.default_rng(29)
+    M, N, K = 12, 15, 31
+    A = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).half()
+    B = torch.from_numpy(rng.standard_normal((K, N)).astype(np.float32)).half()
+    C = rng.standard_normal((M, N)).astype(np.float32)
+    D10, b10 = orc.gemm(A, B, C, M, N, K, alpha=1.0, beta=0.0)
+    for alpha, beta in ((1.5, 0.5), (-2.0, 3.0), (0.25, -1.0)):
+        D, bound = orc.gemm(A, B, C, M, N, K, alpha=alpha, beta=beta)
+        ref = alpha * D10 + beta * C.astype(np.float64)
+        assert np.all(np.abs(D - ref) <= 1e-14 * bound), "not linear in alpha, beta"
+
+
+def pin_closed_form(orc):
+    """A[i][k] = i + 2k + 1, B[k][j] = 3k - j + 1:
+    D[i][j] = K(i+1)(1-j) + (3(i+1) + 2(1-j)) K(K-1)/2 + 6 (K-1)K(2K-1)/6."""
+    M, N, K = 7, 6, 37
+    i = np.arange(M)[:, None]
+    k = np.arange(K)[None, :]
+    A = torch.from_numpy((i + 2 * k + 1).astype(np.float32)).half()
+    kk = np.arange(K)[:, None]
+    j = np.arange(N)[None, :]
+    B = torch.from_numpy((3 * kk - j + 1).astype(np.float32)).half()
+    s1 = K * (K - 1) // 2
+    s2 = (K - 1) * K * (2 * K - 1) // 6
+    ii, jj = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    ref = K * (ii + 1) * (1 - jj) + (3 * (ii + 1) + 2 * (1 - jj)) * s1 + 6 * s2
+    for transA in (0, 1):
+        for transB in (0, 1):
+            As = A.T.contiguous() if transA else A
+            Bs = B.T.contiguous() if transB else B
+            D, _ = orc.gemm(As, Bs, None, M, N, K, transA=transA, transB=transB)
+            assert np.array_equal(D, ref.astype(np.float64)), "closed-form sum mismatch"
+
+
+def pin_bound(orc):
+    rng = np.random.default_rng(31)
+    M, N, K = 8, 9, 20
+    # all terms non-negative: the bound equals D
+    A = _int_tensor(rng, (M, K), 0, 8, F16)
+    B = _int_tensor(rng, (K, N), 0, 8, F16)
+    C = rng.integers(0, 40, size=(M, N)).astype(np.float32)
+    D, bound = orc.gemm(A, B, C, M, N, K, alpha=2.0, beta=1.0)
+    assert np.array_equal(D, bound), "bound != D for non-negative terms"
+    # ones @ (-ones): D = -alpha*K, bound = |alpha|*K (+ |beta||C|)
+    A = torch.ones((M, K), dtype=torch.float16)
+    B = -torch.ones((K, N), dtype=torch.float16)
+    D, bound = orc.gemm(A, B, C, M, N, K, alpha=-1.5, beta=-0.5)
+    assert np.array_equal(D, 1.5 * K - 0.5 * C.astype(np.float64))
+    assert np.array_equal(bound, 1.5 * K + 0.5 * np.abs(C.astype(np.float64)))
+    # mixed signs: |D| <= bound
+    A = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).half()
+    B = torch.from_numpy(rng.standard_normal((K, N)).astype(np.float32)).half()
+    D, bound = orc.gemm(A, B, C, M, N, K, alpha=0.7, beta=-1.3)
+    assert np.all(np.abs(D) <= bound * (1 + 1e-12)), "|D| exceeds its bound"
+
+
+def pin_entries_match_rows(orc):
+    rng = np.random.default_rng(37)
+    M, N, K = 23, 17, 29
+    for transA, transB in ((0, 0), (1, 1)):
+        A = torch.from_numpy(rng.standard_normal((K, M) if transA else (M, K)).astype(np.float32)).bfloat16()
+        B = torch.from_numpy(rng.standard_normal((N, K) if transB else (K, N)).astype(np.float32)).bfloat16()
+        C = rng.standard_normal((M, N)).astype(np.float32)
+        kw = dict(transA=transA, transB=transB, alpha=1.25, beta=-0.75, in_dtype=BF16)
+        D, bound = orc.gemm(A, B, C, M, N, K, **kw)
+        r = rng.integers(0, M, size=50)
+        c = rng.integers(0, N, size=50)
+        De, be = orc.gemm_entries(A, B, C, M, N, K, r, c, **kw)
+        assert _same(De, D[r, c]) and _same(be, bound[r, c]), "entry path disagrees with row path"
+        # a second row-range call fills only its rows
+        Dp, _ = orc.gemm(A, B, C, M, N, K, rows=(5, 9), **kw)
+        assert _same(Dp[5:9], D[5:9]) and np.all(np.isnan(Dp[:5]))
+
+
+def pin_16bit_c(orc):
+    """C in fp16 / bf16 (16-bit outputs) is decoded like the operands."""
+    rng = np.random.default_rng(41)
+    M, N, K = 6, 5, 4
+    A = _int_tensor(rng, (M, K), -4, 4, F16)
+    B = _int_tensor(rng, (K, N), -4, 4, F16)
+    for cd in (F16, BF16):
+        C = _int_tensor(rng, (M, N), -30, 30, cd)
+        D, _ = orc.gemm(A, B, C, M, N, K, beta=1.0, c_dtype=cd)
+        ref = _brute(A, B, C, 0, 0, 1, 1)
+        assert np.array_equal(D, np.array(ref, dtype=np.float64)), "16-bit C decoded wrongly"
+
+
+def pin_rejects_bad_arguments(orc):
+    A = torch.zeros((4, 4), dtype=torch.float16)
+    bad = [
+        dict(lda=3),                      # row longer than the leading dimension
+        dict(ldb=2),
+        dict(in_dtype=F32),               # operands must be 16-bit
+    ]
+    for kw in bad:
+        try:
+            orc.gemm(A, A, None, 4, 4, 4, **kw)
+        except ValueError:
+            continue
+        raise AssertionError("oracle accepted malformed arguments %s" % kw)
+
+
+ALL_PINS = [
+    pin_decoders,
+    pin_brute_force_integers,
+    pin_numpy_float64,
+    pin_identity,
+    pin_permutation,
+    pin_beta_semantics,
+    pin_transpose_equivalence,
+    pin_linearity,
+    pin_closed_form,
+    pin_bound,
+    pin_entries_match_rows,
+    pin_16bit_c,
+    pin_rejects_bad_arguments,
+]
