@@ -1,0 +1,424 @@
+"""Throughput of D = alpha * op(A) @ op(B) + beta * C on GB300, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--case NAME] [--no-e2e] [--no-cpu-baseline]
+
+A step is one GEMM call through the C ABI over the resident, seeded
+synthetic inputs of the workload (default: M = N = K = 8192, fp16
+operands drawn N(0, 1/sqrt(K)), alpha = 1, beta = 0, fp32 D).  The timed
+region is exactly K steps between CUDA events on the launching stream,
+bracketed by a barrier and a device synchronisation; with N > 1 (torchrun)
+every rank runs its own replica and the slowest rank's time is used.
+
+--impl reference times the CPU oracle instead (the only other
+implementation of this operation in the repository), on bounded samples
+of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense fp16/bf16 tensor-core peak"
+UNIT = "TFLOP/s"
+NOMINAL_DENSE_TFLOPS = 2250.0        # GB300 dense fp16/bf16, NVIDIA's figure
+FLOP_PER_CLK_PER_SM = 8192           # dense f16/bf16 tcgen05 rate per SM
+KERNEL_SOURCES = ["dense_tensor_core_02_gb300/csrc/gemm_sm103.cu",
+                  "dense_tensor_core_02_gb300/csrc/ptx.cuh",
+                  "dense_tensor_core_02_gb300/csrc/gemm_params.h"]
+
+
+def _rank_info():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def _measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(case_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s.txt" % case_name)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, util_sm, reasons, power = [], [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                clk, cmax, pw, util = float(parts[1]), float(parts[2]), float(parts[3]), float(parts[4])
+            except ValueError:
+                continue
+            sm.append(clk)
+            smax.append(cmax)
+            power.append(pw)
+            if util >= 50:
+                util_sm.append(clk)
+            for name, flag in zip(names, parts[6:10]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        pick = util_sm or sm
+        return {"sm_mhz": statistics.median(pick) if pick else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons),
+                "samples": len(sm), "samples_under_load": len(util_sm),
+                "power_w_max": max(power) if power else None}
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--case", default=None, help="workload name (default: the 8192^3 fp16 headline)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def _workload_config(case, n_gpus):
+    from dense_tensor_core_02_gb300.inputs import CASES
+    dist = ("N(0,%g)" % case.std) if case.dist == "normal" else "U[-1,1]"
+    return {
+        "workload": "%s: M=%d N=%d K=%d, %s A/B %s, %s D, alpha=%g beta=%g, transA=%d transB=%d" % (
+            case.name, case.M, case.N, case.K, case.in_dtype, dist, case.out_dtype, case.alpha, case.beta,
+            case.transA, case.transB),
+        "M": case.M, "N": case.N, "K": case.K, "accumulate": "f32", "out_dtype": case.out_dtype,
+        "seed": case.seed, "workload_index": CASES.index(case) + 1,
+        "l2": "inputs larger than L2 (A+B+D = %.0f MiB > 129 MB), no flush" % (case.algorithmic_bytes / 2 ** 20)
+        if case.algorithmic_bytes > 129e6 else "working set fits in L2; L2 flushed between steps",
+        "parallelism": "replicas x%d (each GPU its own full GEMM)" % n_gpus,
+    }
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+
+
+def _oracle_sampler(case):
+    """Returns (run(n_entries) -> seconds, threads): the oracle, as it stands,
+    on n_entries output elements of the workload spread over all threads."""
+    import numpy as np
+
+    import oracle.oracle as oracle
+    from dense_tensor_core_02_gb300.inputs import make_inputs
+
+    A, B, C = make_inputs(case)
+    threads = len(os.sched_getaffinity(0))
+    rng = np.random.default_rng(case.seed)
+    code = {"f16": 0, "bf16": 1, "f32": 2}
+
+    def run(n):
+        rows = rng.integers(0, case.M, size=n)
+        cols = rng.integers(0, case.N, size=n)
+        t0 = time.perf_counter()
+        oracle.gemm_entries(A, B, C, case.M, case.N, case.K, rows, cols, transA=case.transA,
+                            transB=case.transB, alpha=case.alpha, beta=case.beta,
+                            in_dtype=code[case.in_dtype], c_dtype=code[case.out_dtype], threads=threads)
+        return time.perf_counter() - t0
+
+    return run, threads
+
+
+def _calibrate(run, threads, target_s):
+    n = threads * 2
+    while True:
+        t = run(n)
+        if t >= 0.25 or n >= 1 << 24:
+            return max(threads, int(n * target_s / max(t, 1e-9))), t
+        n *= 4
+
+
+def cpu_baseline(case, target_s):
+    run, threads = _oracle_sampler(case)
+    n, _ = _calibrate(run, threads, target_s)
+    t = run(n)
+    flops = 2.0 * case.K * n
+    return {"value": flops / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d output elements of %s (random positions, each the full K=%d dot product), "
+                      "%.1f s on %d threads" % (n, case.name, case.K, t, threads)}
+
+
+def run_reference(args, case):
+    rank, world, _ = _rank_info()
+    if rank != 0:
+        return 0
+    run, threads = _oracle_sampler(case)
+    per_step_s = min(0.25, 90.0 / max(1, args.steps + args.warmup))
+    n, _ = _calibrate(run, threads, per_step_s)
+    for _ in range(args.warmup):
+        run(n)
+    total = 0.0
+    for _ in range(args.steps):
+        total += run(n)
+    flops = 2.0 * case.K * n * args.steps
+    value = flops / total / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": _workload_config(case, args.gpus),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "each step: %d output elements of %s (full K=%d dot products)" % (
+                             n, case.name, case.K)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------
+# the CUDA path
+
+
+def run_ours(args, case):
+    import torch
+
+    from dense_tensor_core_02_gb300 import binding
+    from dense_tensor_core_02_gb300.inputs import make_inputs
+
+    rank, world, local_rank = _rank_info()
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    binding.load_library()
+
+    code = {"f16": binding.F16, "bf16": binding.BF16, "f32": binding.F32}
+    A, B, C = make_inputs(case)
+    Ad, Bd = A.to(dev), B.to(dev)
+    Cd = C.to(dev) if C is not None else None
+    otype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[case.out_dtype]
+    Dd = torch.empty((case.M, case.N), dtype=otype, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+    ldc = Cd.stride(0) if Cd is not None else case.N
+    small = case.algorithmic_bytes <= 129e6
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if small else None
+
+    def step():
+        if flush is not None:
+            flush.zero_()
+        rc = binding.gemm(Dd, Ad, Bd, Cd, case.M, case.N, case.K, Ad.stride(0), Bd.stride(0), ldc,
+                          Dd.stride(0), case.transA, case.transB, case.alpha, case.beta,
+                          code[case.in_dtype], code[case.out_dtype], sptr)
+        if rc != 0:
+            raise RuntimeError("gemm: %s" % binding.gemm_status_string(rc))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    status, info = binding.gemm_poll_device_error(stream)
+    if status != 0:
+        raise RuntimeError("device status after warm-up: %s %s" % (binding.gemm_status_string(status), info))
+
+    sampler = ClockSampler(local_rank).start() if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    elapsed_ms = e0.elapsed_time(e1)
+    status, info = binding.gemm_poll_device_error(stream)
+    if status != 0:
+        raise RuntimeError("device status after timing: %s %s" % (binding.gemm_status_string(status), info))
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    per_launch_ms = elapsed_ms / args.steps
+    value = world * case.flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    # end to end through the same C ABI: pinned host inputs in, host result out
+    e2e = None
+    if not args.no_e2e:
+        hA = A.pin_memory()
+        hB = B.pin_memory()
+        hC = C.pin_memory() if C is not None else None
+        hD = torch.empty((case.M, case.N), dtype=otype).pin_memory()
+
+        def e2e_step():
+            Ad.copy_(hA, non_blocking=True)
+            Bd.copy_(hB, non_blocking=True)
+            if hC is not None:
+                Cd.copy_(hC, non_blocking=True)
+            rc = binding.gemm(Dd, Ad, Bd, Cd, case.M, case.N, case.K, Ad.stride(0), Bd.stride(0), ldc,
+                              Dd.stride(0), case.transA, case.transB, case.alpha, case.beta,
+                              code[case.in_dtype], code[case.out_dtype], sptr)
+            if rc != 0:
+                raise RuntimeError("gemm: %s" % binding.gemm_status_string(rc))
+            hD.copy_(Dd, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.e2e_steps):
+                e2e_step()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        e2e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        h2d = A.numel() * A.element_size() + B.numel() * B.element_size() + (
+            C.numel() * C.element_size() if C is not None else 0)
+        d2h = Dd.numel() * Dd.element_size()
+        e2e = {"value": world * case.flops * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+               "ms_per_step": e2e_ms / args.e2e_steps}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = _measured_peaks()
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    achieved = case.flops / (per_launch_ms * 1e-3) / 1e12
+    peak = float(peaks["bf16_tflops"])
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                "frac": achieved / peak, "traffic": _profiled_traffic(case.name),
+                "peak_source": "%s bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json); f16 runs at the bf16 rate"
+                               % peak_src,
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "frac_of_nominal_2250": achieved / NOMINAL_DENSE_TFLOPS,
+                "algorithmic_flops_per_launch": case.flops,
+                "algorithmic_bytes_per_launch": case.algorithmic_bytes,
+                "achieved_gbs": case.algorithmic_bytes / (per_launch_ms * 1e-3) / 1e9}
+    if clocks and clocks.get("sm_mhz"):
+        clk_peak = num_sms * FLOP_PER_CLK_PER_SM * clocks["sm_mhz"] * 1e6 / 1e12
+        roofline["frac_of_clock_peak"] = achieved / clk_peak
+        roofline["clock_peak_tflops"] = clk_peak
+    roofline["max_clock_peak_tflops"] = num_sms * FLOP_PER_CLK_PER_SM * 2070e6 / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": per_launch_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": case.in_dtype, "data": "synthetic",
+        "config": _workload_config(case, world), "roofline": roofline,
+        "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps, "num_sms": num_sms,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = _args()
+    from dense_tensor_core_02_gb300.inputs import CASE_BY_NAME, HEADLINE
+    case = CASE_BY_NAME[args.case] if args.case else HEADLINE
+    if args.impl == "reference":
+        return run_reference(args, case)
+    return run_ours(args, case)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

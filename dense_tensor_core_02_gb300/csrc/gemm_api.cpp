@@ -1,0 +1,421 @@
+// C-ABI entry points of libgemm_gb300.so (declared in include/gemm_gb300.h).
+//
+// Host side of the boundary: argument validation (every rejection happens
+// before anything is enqueued), per-device state, TMA descriptor encoding,
+// kernel selection and launch.  Nothing here synchronises the caller's
+// stream except gemm_poll_device_error().
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm_gb300.h"
+#include "gemm_internal.h"
+#include "gemm_params.h"
+
+namespace {
+
+using gb300::DeviceStatus;
+using gb300::GemmParams;
+using gb300::TcgenLaunch;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxDim = 2147483647;           // TMA coordinates are signed 32-bit
+constexpr int64_t kMaxStrideBytes = 1ll << 40;    // TMA global stride limit
+
+struct DeviceState {
+    bool ready = false;
+    int status = GEMM_OK;     // sticky result of the set-up
+    int num_sms = 0;
+    DeviceStatus* d_status = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+
+bool log_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("GEMM_LOG");
+        return v && *v && std::strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
+#define GEMM_LOGF(...)                                \
+    do {                                              \
+        if (log_enabled()) {                          \
+            std::fprintf(stderr, "[gemm_gb300] " __VA_ARGS__); \
+            std::fputc('\n', stderr);                 \
+        }                                             \
+    } while (0)
+
+int reject(int code, const char* why) {
+    GEMM_LOGF("rejected (%s): %s", gemm_status_string(code), why);
+    return code;
+}
+
+// Bound on every in-kernel wait (GEMM_WAIT_TIMEOUT_NS, default 2 s).
+uint64_t wait_timeout_ns() {
+    const char* v = std::getenv("GEMM_WAIT_TIMEOUT_NS");
+    if (v && *v) {
+        unsigned long long x = std::strtoull(v, nullptr, 10);
+        if (x > 0) return (uint64_t)x;
+    }
+    return (uint64_t)2000000000ull;
+}
+
+// Test hook (GEMM_TEST_SKIP_FIRST_STAGE=1): the producer leaves stage 0 of
+// the first tile empty, so the MMA's wait for it runs out after the time
+// bound and the kernel reports GEMM_ERR_DEVICE_TIMEOUT without faulting.
+int skip_first_stage_setting() {
+    const char* v = std::getenv("GEMM_TEST_SKIP_FIRST_STAGE");
+    return (v && std::strcmp(v, "1") == 0) ? 1 : 0;
+}
+
+// Kernel variant: "pair" (2-SM tiles), "single" or automatic.
+int variant_override() {
+    const char* v = std::getenv("GEMM_VARIANT");
+    if (!v) return -1;
+    if (std::strcmp(v, "pair") == 0) return 1;
+    if (std::strcmp(v, "single") == 0) return 0;
+    return -1;
+}
+
+int group_m_setting() {
+    const char* v = std::getenv("GEMM_GROUP_M");
+    if (v && *v) {
+        int g = std::atoi(v);
+        if (g >= 1 && g <= 4096) return g;
+    }
+    return 8;
+}
+
+int elem_size(int dtype) { return dtype == GEMM_F32 ? 4 : 2; }
+
+// Byte range [lo, hi) covered by a row-major rows x cols matrix.
+void byte_range(const void* p, int64_t rows, int64_t cols, int64_t ld, int esz, uintptr_t* lo, uintptr_t* hi) {
+    *lo = reinterpret_cast<uintptr_t>(p);
+    *hi = *lo + (uintptr_t)(((rows - 1) * ld + cols) * esz);
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+int device_state(int dev, DeviceState** out) {
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& st = g_devices[dev];
+    if (!st.ready) {
+        st.ready = true;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            st.status = GEMM_ERR_CUDA;
+        } else if (major != 10 || minor != 3) {
+            GEMM_LOGF("device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
+            st.status = GEMM_ERR_ARCH;
+        } else if (gb300::prepare_kernels_on_current_device() != cudaSuccess) {
+            st.status = GEMM_ERR_CUDA;
+        } else if (cudaMalloc(&st.d_status, sizeof(DeviceStatus)) != cudaSuccess ||
+                   cudaMemset(st.d_status, 0, sizeof(DeviceStatus)) != cudaSuccess) {
+            st.status = GEMM_ERR_CUDA;
+        }
+        if (st.status != GEMM_OK) cudaGetLastError();   // do not leave a sticky-free error behind
+    }
+    *out = &st;
+    return st.status;
+}
+
+int get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        else
+            cudaGetLastError();
+    });
+    return g_encode ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+CUtensorMapDataType tma_dtype(int dt) {
+    return dt == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                          : dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
+// A 2-D row-major matrix: dim0 = contiguous extent, dim1 = rows; the box is
+// box0 x box1 elements, staged with 128-byte swizzling, zero fill outside.
+int encode_2d(CUtensorMap* map, int dt, const void* ptr, int64_t dim0, int64_t dim1, int64_t ld, uint32_t box0,
+              uint32_t box1) {
+    cuuint64_t dims[2] = {(cuuint64_t)dim0, (cuuint64_t)dim1};
+    cuuint64_t strides[1] = {(cuuint64_t)(ld * elem_size(dt))};
+    cuuint32_t box[2] = {box0, box1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, tma_dtype(dt), 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        GEMM_LOGF("cuTensorMapEncodeTiled failed (%d): dims %lld x %lld, ld %lld, box %u x %u", (int)r,
+                  (long long)dim0, (long long)dim1, (long long)ld, box0, box1);
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+struct Plan {
+    int pair;
+    int tile_m, tile_n;
+    int num_m, num_n, num_tiles;
+    int grid;
+    int smem;
+};
+
+Plan make_plan(int64_t M, int64_t N, int num_sms) {
+    Plan pl{};
+    int ov = variant_override();
+    pl.pair = ov >= 0 ? ov : (M > gb300::tcgen05_tile_m(0) ? 1 : 0);
+    pl.tile_m = gb300::tcgen05_tile_m(pl.pair);
+    pl.tile_n = gb300::tcgen05_tile_n();
+    pl.num_m = (int)((M + pl.tile_m - 1) / pl.tile_m);
+    pl.num_n = (int)((N + pl.tile_n - 1) / pl.tile_n);
+    pl.num_tiles = pl.num_m * pl.num_n;
+    const int units = pl.pair ? num_sms / 2 : num_sms;   // clusters that fit at once
+    int clusters = pl.num_tiles < units ? pl.num_tiles : units;
+    if (clusters < 1) clusters = 1;
+    pl.grid = pl.pair ? 2 * clusters : clusters;
+    pl.smem = gb300::tcgen05_smem_bytes(pl.pair);
+    return pl;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gemm_status_string(int status) {
+    switch (status) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG";
+        case GEMM_ERR_UNSUPPORTED_DTYPE: return "GEMM_ERR_UNSUPPORTED_DTYPE";
+        case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED";
+        case GEMM_ERR_ALIAS: return "GEMM_ERR_ALIAS";
+        case GEMM_ERR_ARCH: return "GEMM_ERR_ARCH";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
+        case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT";
+        case GEMM_ERR_TOO_LARGE: return "GEMM_ERR_TOO_LARGE";
+        default: return "GEMM_ERR_UNKNOWN";
+    }
+}
+
+int gemm_tile_coords(int tile, int num_m, int num_n, int group_m, int* m_blk, int* n_blk) {
+    if (num_m < 1 || num_n < 1 || group_m < 1 || tile < 0 || !m_blk || !n_blk) return GEMM_ERR_INVALID_ARG;
+    if ((int64_t)num_m * num_n > kMaxDim || tile >= num_m * num_n) return GEMM_ERR_INVALID_ARG;
+    gb300::tile_coords(tile, num_m, num_n, group_m, m_blk, n_blk);
+    return GEMM_OK;
+}
+
+int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out) {
+    if (M < 1 || N < 1 || K < 0 || num_sms < 2 || !out) return GEMM_ERR_INVALID_ARG;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_TOO_LARGE;
+    Plan pl = make_plan(M, N, num_sms);
+    out[0] = pl.pair;
+    out[1] = pl.tile_m;
+    out[2] = pl.tile_n;
+    out[3] = pl.num_tiles;
+    out[4] = pl.grid;
+    out[5] = pl.smem;
+    return GEMM_OK;
+}
+
+int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+         int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float alpha, float beta, int in_dtype,
+         int out_dtype, struct CUstream_st* stream) {
+    // ---- arguments (host only, nothing touches the device) ----
+    if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16) return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "in_dtype");
+    if (out_dtype != GEMM_F32 && out_dtype != GEMM_F16 && out_dtype != GEMM_BF16)
+        return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "out_dtype");
+    if (M < 0 || N < 0 || K < 0) return reject(GEMM_ERR_INVALID_ARG, "negative size");
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
+        return reject(GEMM_ERR_INVALID_ARG, "transpose flag not 0/1");
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return reject(GEMM_ERR_TOO_LARGE, "dimension");
+    const bool has_c = beta != 0.0f;
+    const int osz = elem_size(out_dtype);
+    if (!D) return reject(GEMM_ERR_INVALID_ARG, "D is NULL");
+    if (ldd < N) return reject(GEMM_ERR_INVALID_ARG, "ldd < N");
+    if (has_c) {
+        if (!C) return reject(GEMM_ERR_INVALID_ARG, "C is NULL with beta != 0");
+        if (ldc < N) return reject(GEMM_ERR_INVALID_ARG, "ldc < N");
+    }
+    if (K > 0) {
+        if (!A || !B) return reject(GEMM_ERR_INVALID_ARG, "A or B is NULL");
+        if (lda < (transA ? M : K)) return reject(GEMM_ERR_INVALID_ARG, "lda too small");
+        if (ldb < (transB ? K : N)) return reject(GEMM_ERR_INVALID_ARG, "ldb too small");
+        if (lda * 2 >= kMaxStrideBytes || ldb * 2 >= kMaxStrideBytes) return reject(GEMM_ERR_TOO_LARGE, "stride");
+        if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u)
+            return reject(GEMM_ERR_MISALIGNED, "A or B not 16-byte aligned");
+        if (((lda * 2) | (ldb * 2)) & 15) return reject(GEMM_ERR_MISALIGNED, "lda*2 or ldb*2 not a multiple of 16");
+    }
+    if (ldd * osz >= kMaxStrideBytes || (has_c && ldc * osz >= kMaxStrideBytes))
+        return reject(GEMM_ERR_TOO_LARGE, "stride");
+    if (reinterpret_cast<uintptr_t>(D) & 15u) return reject(GEMM_ERR_MISALIGNED, "D not 16-byte aligned");
+    if ((ldd * osz) & 15) return reject(GEMM_ERR_MISALIGNED, "ldd*sizeof(out) not a multiple of 16");
+    if (has_c) {
+        if (reinterpret_cast<uintptr_t>(C) & 15u) return reject(GEMM_ERR_MISALIGNED, "C not 16-byte aligned");
+        if ((ldc * osz) & 15) return reject(GEMM_ERR_MISALIGNED, "ldc*sizeof(out) not a multiple of 16");
+    }
+    {
+        uintptr_t d0, d1;
+        byte_range(D, M, N, ldd, osz, &d0, &d1);
+        if (K > 0) {
+            uintptr_t a0, a1, b0, b1;
+            byte_range(A, transA ? K : M, transA ? M : K, lda, 2, &a0, &a1);
+            byte_range(B, transB ? N : K, transB ? K : N, ldb, 2, &b0, &b1);
+            if (overlaps(d0, d1, a0, a1) || overlaps(d0, d1, b0, b1))
+                return reject(GEMM_ERR_ALIAS, "D overlaps A or B");
+        }
+        if (has_c && !(C == D && ldc == ldd)) {
+            uintptr_t c0, c1;
+            byte_range(C, M, N, ldc, osz, &c0, &c1);
+            if (overlaps(d0, d1, c0, c1)) return reject(GEMM_ERR_ALIAS, "D overlaps C (other than C == D, ldc == ldd)");
+        }
+    }
+
+    // ---- device ----
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return reject(GEMM_ERR_CUDA, "cudaGetDevice");
+    }
+    DeviceState* ds = nullptr;
+    int rc = device_state(dev, &ds);
+    if (rc != GEMM_OK) return reject(rc, "device set-up");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    const int out_kind = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
+    if (K == 0) {
+        GEMM_LOGF("M=%lld N=%lld K=0: epilogue-only kernel", (long long)M, (long long)N);
+        cudaError_t e = gb300::launch_k0(out_kind, D, has_c ? C : nullptr, (int)M, (int)N, ldc, ldd, alpha, beta,
+                                         has_c ? 1 : 0, ds->num_sms, s);
+        if (e != cudaSuccess) return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+        return GEMM_OK;
+    }
+
+    if ((rc = get_encoder()) != GEMM_OK) return reject(rc, "cuTensorMapEncodeTiled unavailable");
+    const Plan pl = make_plan(M, N, ds->num_sms);
+    TcgenLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const uint32_t bk = (uint32_t)gb300::tcgen05_block_k();
+    // A: K-major (transA = 0) as [M rows][K], else MN-major as [K rows][M]
+    if (!transA)
+        rc = encode_2d(&L.a, in_dtype, A, K, M, lda, bk, (uint32_t)gb300::tcgen05_load_rows_a());
+    else
+        rc = encode_2d(&L.a, in_dtype, A, M, K, lda, 64, bk);
+    if (rc != GEMM_OK) return reject(rc, "tensor map A");
+    // B: K-major (transB = 1) as [N rows][K], else MN-major as [K rows][N]
+    if (transB)
+        rc = encode_2d(&L.b, in_dtype, B, K, N, ldb, bk, (uint32_t)gb300::tcgen05_load_rows_b(pl.pair));
+    else
+        rc = encode_2d(&L.b, in_dtype, B, N, K, ldb, 64, bk);
+    if (rc != GEMM_OK) return reject(rc, "tensor map B");
+    const uint32_t chunk_cols = 128u / (uint32_t)osz;
+    // TMA stores write whole 16-byte pieces of a row, even past the tensor's
+    // last column: D's map stops at the last whole piece (n_tma) and the
+    // kernel stores columns [n_tma, N) element by element.
+    const int64_t vec = 16 / osz;
+    const int64_t n_tma = (N / vec) * vec;
+    if ((rc = encode_2d(&L.d, out_dtype, D, n_tma > 0 ? n_tma : N, M, ldd, chunk_cols, 32)) != GEMM_OK)
+        return reject(rc, "tensor map D");
+    if (has_c && (rc = encode_2d(&L.c, out_dtype, C, N, M, ldc, chunk_cols, 32)) != GEMM_OK)
+        return reject(rc, "tensor map C");
+
+    GemmParams& p = L.p;
+    p.M = (int32_t)M;
+    p.N = (int32_t)N;
+    p.K = (int32_t)K;
+    p.num_m_tiles = pl.num_m;
+    p.num_n_tiles = pl.num_n;
+    p.num_k_blocks = (int32_t)((K + bk - 1) / bk);
+    p.num_tiles = pl.num_tiles;
+    p.group_m = group_m_setting();
+    p.alpha = alpha;
+    p.beta = beta;
+    p.a_mn_major = transA ? 1 : 0;
+    p.b_mn_major = transB ? 0 : 1;
+    p.has_c = has_c ? 1 : 0;
+    p.timeout_ns = wait_timeout_ns();
+    p.skip_first_stage = skip_first_stage_setting();
+    p.n_tma = (int32_t)n_tma;
+    p.d_ptr = D;
+    p.ldd = ldd;
+    p.status = ds->d_status;
+    // tcgen05 instruction descriptor, kind::f16: D format f32 (bits 4-5 = 1),
+    // A / B format (bits 7-9, 10-12: 0 = f16, 1 = bf16), A / B major
+    // (bits 15, 16: 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
+    const uint32_t fmt = in_dtype == GEMM_BF16 ? 1u : 0u;
+    const uint32_t mma_m = (uint32_t)pl.tile_m;   // 128 (one SM) or 256 (CTA pair)
+    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)p.a_mn_major << 15) |
+              ((uint32_t)p.b_mn_major << 16) | (((uint32_t)pl.tile_n >> 3) << 17) | ((mma_m >> 4) << 24);
+    L.pair = pl.pair;
+    L.out = out_kind;
+    L.grid = pl.grid;
+
+    GEMM_LOGF("M=%lld N=%lld K=%lld trans=%d%d in=%d out=%d beta%s0: %s tiles %dx%d (%d), grid %d, smem %d",
+              (long long)M, (long long)N, (long long)K, transA, transB, in_dtype, out_dtype, has_c ? "!=" : "==",
+              pl.pair ? "cta-pair" : "1-cta", pl.tile_m, pl.tile_n, pl.num_tiles, pl.grid, pl.smem);
+    cudaError_t e = gb300::launch_tcgen05(L, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+    }
+    return GEMM_OK;
+}
+
+int gemm_poll_device_error(struct CUstream_st* stream, int* info) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    DeviceState* ds = nullptr;
+    int rc = device_state(dev, &ds);
+    if (rc != GEMM_OK) return rc;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    DeviceStatus st{};
+    if (cudaMemcpy(&st, ds->d_status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (info) {
+        info[0] = st.code;
+        info[1] = st.block;
+        info[2] = st.site;
+        info[3] = st.detail;
+    }
+    if (st.code != 0) {
+        if (cudaMemset(ds->d_status, 0, sizeof(DeviceStatus)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        return st.code;
+    }
+    return GEMM_OK;
+}
+
+}  // extern "C"

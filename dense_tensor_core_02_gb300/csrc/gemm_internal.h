@@ -1,0 +1,39 @@
+// Internal interface between the C-ABI host code (gemm_api.cpp) and the
+// sm_103a kernels (gemm_sm103.cu).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gemm_params.h"
+
+namespace gb300 {
+
+// Output (C and D) element types, in the kernels' template vocabulary.
+enum OutKind : int { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
+
+// Device status code written by a wait that gave up (= GEMM_ERR_DEVICE_TIMEOUT).
+constexpr int kDeviceErrTimeout = -8;
+
+struct TcgenLaunch {
+    CUtensorMap a, b, c, d;   // TMA descriptors (c unused when beta == 0)
+    GemmParams p;
+    int pair;                 // 1: CTA-pair (cta_group::2) kernel
+    int out;                  // OutKind
+    int grid;                 // CTAs (a multiple of 2 for the pair kernel)
+};
+
+cudaError_t prepare_kernels_on_current_device();
+cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream);
+cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,
+                      float beta, int has_c, int num_sms, cudaStream_t stream);
+
+int tcgen05_tile_m(int pair);      // D rows per tile
+int tcgen05_tile_n();              // D columns per tile
+int tcgen05_block_k();             // K per pipeline stage
+int tcgen05_load_rows_a();         // A rows (M) one CTA stages per stage
+int tcgen05_load_rows_b(int pair); // B rows (N) one CTA stages per stage
+int tcgen05_smem_bytes(int pair);
+
+}  // namespace gb300

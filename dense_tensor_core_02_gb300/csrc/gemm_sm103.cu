@@ -1,0 +1,563 @@
+// sm_103a kernels for D = alpha * op(A) @ op(B) + beta * C.
+//
+// The contraction is the one of the TVM TIRx "gemm" page (opening paragraph
+// and "What it accepts": f16/bf16 operands, f32 accumulator, D initialised
+// to 0 for beta = 0 or from C for beta = 1) with the general epilogue
+// alpha * acc + beta * c_old of the Phobos "@tensorcore" page
+// (gemm_fp16tc_fp32acc.ph).  The pages lower it to warp-level mma.sync
+// fragments in registers; here it is re-designed for Blackwell:
+//
+//  * operand staging: TMA 2-D tile loads into 128-byte-swizzled shared
+//    memory, an S-stage full/empty mbarrier ring (replaces the pages'
+//    swizzled cp.async staging, Phobos "@tensorcore" page, section
+//    "Interactions", @pipeline);
+//  * main loop: tcgen05.mma kind::f16 issued by one thread, accumulator in
+//    tensor memory (TMEM), the first K step with the accumulate flag off
+//    (the TIRx "Algorithm" step 3 "initialise D, then accumulate over K in
+//    place" becomes "overwrite, then accumulate");
+//  * warp specialisation: warp 0 = TMA producer, warp 1 = TMEM allocator
+//    and MMA issuer, warps 2..5 = epilogue (one TMEM lane quadrant each);
+//  * two accumulators in TMEM (2 x 256 columns) so the epilogue of tile i
+//    overlaps the main loop of tile i+1;
+//  * persistent grid with grouped (L2-friendly) tile order;
+//  * optional CTA pair (cta_group::2): a 256 x 256 tile per cluster of two
+//    SMs, each SM loading its half of A and its half of B;
+//  * epilogue: tcgen05.ld TMEM -> registers, alpha/beta (C fetched by TMA
+//    only when beta != 0), conversion, swizzled shared staging, TMA store;
+//  * masked edges: TMA zero-fills out-of-range operand elements and clips
+//    out-of-range stores, so ragged M, N, K need no separate path;
+//  * every wait is bounded by the global timer; a wait that gives up records
+//    itself in a device status block and the kernel unwinds cleanly.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "gemm_internal.h"
+#include "gemm_params.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+
+constexpr int kBM = 128;             // accumulator rows per CTA (= TMEM lanes)
+constexpr int kBN = 256;             // accumulator columns per tile
+constexpr int kBK = 64;              // K per stage: one 128-byte swizzle row of 16-bit elements
+constexpr int kUK = 16;              // K per tcgen05.mma kind::f16
+constexpr int kNumThreads = 192;     // 6 warps
+constexpr int kEpiWarps = 4;
+constexpr int kEpiBufBytes = 4096;   // one epilogue staging box: 32 rows x 128 bytes
+constexpr int kTmemCols = 512;       // two 128 x 256 fp32 accumulators
+constexpr int kAtomBytes = 1024;     // 8 rows x 128 bytes: one 128B-swizzle atom
+constexpr int kMnChunkBytes = 64 * kBK * 2;   // one 64-wide MN-major box (64 x 64 x 2 B)
+
+template <bool kPair>
+struct Cfg {
+    static constexpr int kCtaGroup = kPair ? 2 : 1;
+    static constexpr int kTileM = kPair ? 2 * kBM : kBM;   // D rows per tile
+    static constexpr int kLoadN = kPair ? kBN / 2 : kBN;   // B rows (N) each CTA stages
+    static constexpr int kStages = kPair ? 6 : 4;
+    static constexpr int kABytes = kBM * kBK * 2;
+    static constexpr int kBBytes = kLoadN * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kOffA = 0;
+    static constexpr int kOffB = kOffA + kStages * kABytes;
+    static constexpr int kOffEpi = kOffB + kStages * kBBytes;
+    static constexpr int kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBufBytes;
+    // full[S], empty[S], tmem_full[2], tmem_empty[2], c_ready[4 warps][2]
+    static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps;
+    static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+    static constexpr int kOffAbort = kOffTmemSlot + 4;
+    static constexpr int kSmemBytes = kOffAbort + 4 + 1024;   // + base alignment slack
+};
+
+static_assert(Cfg<false>::kSmemBytes <= 232448, "shared memory budget (1-CTA)");
+static_assert(Cfg<true>::kSmemBytes <= 232448, "shared memory budget (CTA pair)");
+
+// tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand:
+// start address, leading / stride byte offsets (all >> 4), the fixed
+// descriptor version 0b001 at bits 46-48, base offset 0, swizzle mode 2
+// (128 B) at bits 61-63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Descriptor of the kk-th K=16 slice of a staged operand tile.
+//  K-major (K contiguous): rows of 128 B, 8-row atoms 1024 B apart (SBO);
+//    a K step of 16 elements is +32 B inside the swizzle row.
+//  MN-major (M or N contiguous): boxes of 64 MN x 64 K, each K row 128 B;
+//    8-K-row atoms 1024 B apart (SBO), 64-wide MN boxes 8 KiB apart (LBO);
+//    a K step of 16 rows is +2 KiB.
+__device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int mn_major, int kk) {
+    return mn_major ? sw128_desc(tile + kk * (kUK * 128), kMnChunkBytes, kAtomBytes)
+                    : sw128_desc(tile + kk * (kUK * 2), 16, kAtomBytes);
+}
+
+__device__ __noinline__ void report_timeout(const GemmParams& p, int site, int detail) {
+    if (atomicCAS(&p.status->code, 0, kDeviceErrTimeout) == 0) {
+        p.status->block = blockIdx.x;
+        p.status->site = site;
+        p.status->detail = detail;
+        __threadfence();
+    }
+}
+
+// Wait for the phase of `bar` with parity `parity`; gives up (returns false)
+// when another thread of the CTA has aborted or the time bound has passed.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
+                                             const GemmParams& p, int site, int detail) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t n = 1;; ++n) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((n & 15u) == 0) {
+            if (*abort) return false;
+            if (ptx::globaltimer_ns() - t0 > p.timeout_ns) {
+                *abort = 1;
+                report_timeout(p, site, detail);
+                return false;
+            }
+        }
+    }
+}
+
+// Stage one operand tile of `rows` (M or N) x kBK (K).
+template <bool kPair>
+__device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, int mn_major,
+                                             int row0, int rows, int k0, uint32_t bar) {
+    if (mn_major) {
+        for (int j = 0; j < rows / 64; ++j) {
+            if constexpr (kPair)
+                ptx::tma_load_2d_pair(dst + j * kMnChunkBytes, map, row0 + 64 * j, k0, bar);
+            else
+                ptx::tma_load_2d(dst + j * kMnChunkBytes, map, row0 + 64 * j, k0, bar);
+        }
+    } else {
+        if constexpr (kPair)
+            ptx::tma_load_2d_pair(dst, map, k0, row0, bar);
+        else
+            ptx::tma_load_2d(dst, map, k0, row0, bar);
+    }
+}
+
+template <int kOut>
+struct OutTraits;
+template <>
+struct OutTraits<kOutF32> {
+    static constexpr int kBytes = 4;
+};
+template <>
+struct OutTraits<kOutF16> {
+    static constexpr int kBytes = 2;
+};
+template <>
+struct OutTraits<kOutBF16> {
+    static constexpr int kBytes = 2;
+};
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int out) {
+    if (out == kOutF16) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack2(uint32_t u, int out) {
+    if (out == kOutF16) {
+        __half2 h = *reinterpret_cast<__half2*>(&u);
+        return __half22float2(h);
+    }
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
+    return __bfloat1622float2(h);
+}
+
+template <bool kPair, int kOut>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                        const GemmParams p) {
+    using Cf = Cfg<kPair>;
+    constexpr int kCG = Cf::kCtaGroup;
+    constexpr int kOutBytes = OutTraits<kOut>::kBytes;
+    constexpr int kChunkCols = 128 / kOutBytes;   // columns per 128-byte staging row
+    constexpr int kChunks = kBN / kChunkCols;
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // 128B-swizzle atoms need 1024-B alignment
+    uint8_t* smem = smem_raw + (base - raw);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = kPair ? ptx::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+
+    const uint32_t bars = base + Cf::kOffBar;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (Cf::kStages + s); };
+    auto tfull_bar = [&](int a) { return bars + 8u * (2 * Cf::kStages + a); };
+    auto tempty_bar = [&](int a) { return bars + 8u * (2 * Cf::kStages + 2 + a); };
+    auto c_bar = [&](int w, int b) { return bars + 8u * (2 * Cf::kStages + 4 + 2 * w + b); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cf::kOffAbort);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Cf::kOffTmemSlot);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cf::kStages; ++s) {
+            ptx::mbar_init(full_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(tfull_bar(a), 1);
+            ptx::mbar_init(tempty_bar(a), (kPair ? 2 : 1) * kEpiWarps * 32);
+        }
+        for (int w = 0; w < kEpiWarps; ++w)
+            for (int b = 0; b < 2; ++b) ptx::mbar_init(c_bar(w, b), 1);
+        *abort_flag = 0;
+        ptx::fence_mbarrier_init();
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmD);
+        if (p.has_c) ptx::prefetch_tensormap(&tmC);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<kCG>(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
+        ptx::tmem_relinquish<kCG>();
+    }
+    ptx::tc_fence_before_sync();
+    if constexpr (kPair)
+        ptx::cluster_sync();
+    else
+        __syncthreads();
+    ptx::tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int cluster_id = kPair ? blockIdx.x / 2 : blockIdx.x;
+    const int num_clusters = kPair ? gridDim.x / 2 : gridDim.x;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            const uint32_t stage_tx = (kPair ? 2 : 1) * Cf::kStageBytes;
+            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+                int mb, nb;
+                tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, &mb, &nb);
+                const int a_row0 = mb * Cf::kTileM + (int)rank * kBM;
+                const int b_row0 = nb * kBN + (int)rank * Cf::kLoadN;
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p, kSiteProducerEmpty, t)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool skip = p.skip_first_stage && t == cluster_id && kb == 0;
+                    if (!skip) {
+                        const uint32_t fb = kPair ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
+                        if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), stage_tx);
+                        const int k0 = kb * kBK;
+                        load_operand<kPair>(base + Cf::kOffA + stage * Cf::kABytes, &tmA, p.a_mn_major,
+                                            a_row0, kBM, k0, fb);
+                        load_operand<kPair>(base + Cf::kOffB + stage * Cf::kBBytes, &tmB, p.b_mn_major,
+                                            b_row0, Cf::kLoadN, k0, fb);
+                    }
+                    if (++stage == Cf::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // Drain: wait until the MMA has released every stage, so that no
+            // completion signal is still on its way to this CTA at exit.
+            for (int i = 0; ok && i < Cf::kStages; ++i) {
+                if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p, kSiteProducerTail, i)) break;
+                if (++stage == Cf::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------- MMA issuer (the pair's leader CTA only) ----------------
+        if (leader && lane == 0) {
+            const uint32_t idesc = p.idesc;
+            int stage = 0;
+            uint32_t phase = 0;
+            int it = 0;
+            bool ok = true;
+            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++it) {
+                const int acc = it & 1;
+                const uint32_t acc_phase = (it >> 1) & 1;
+                if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p, kSiteMmaTmemEmpty, t)) break;
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                    if (!wait_bounded(full_bar(stage), phase, abort_flag, p, kSiteMmaFull, t)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after_sync();
+                    const uint32_t sa = base + Cf::kOffA + stage * Cf::kABytes;
+                    const uint32_t sb = base + Cf::kOffB + stage * Cf::kBBytes;
+#pragma unroll
+                    for (int kk = 0; kk < kBK / kUK; ++kk) {
+                        ptx::mma_f16<kCG>(d_tmem, operand_desc(sa, p.a_mn_major, kk),
+                                          operand_desc(sb, p.b_mn_major, kk), idesc, (kb | kk) != 0);
+                    }
+                    if constexpr (kPair)
+                        ptx::mma_commit_pair(empty_bar(stage), 0x3);
+                    else
+                        ptx::mma_commit(empty_bar(stage));
+                    if (++stage == Cf::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if constexpr (kPair)
+                    ptx::mma_commit_pair(tfull_bar(acc), 0x3);
+                else
+                    ptx::mma_commit(tfull_bar(acc));
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue warps 2..5 ----------------
+        const int ew = warp - 2;   // staging buffers and C barriers of this warp
+        const int q = warp & 3;    // the TMEM lane quadrant this warp may read
+        const uint32_t epi = base + Cf::kOffEpi + ew * 2 * kEpiBufBytes;
+        const float alpha = p.alpha;
+        const float beta = p.beta;
+        const bool has_c = p.has_c != 0;
+        constexpr int kVec = 16 / kOutBytes;   // elements per 16-byte piece
+        uint32_t chunk_iter = 0;
+        bool prev_stored = false;   // lane 0: the previous chunk committed a TMA store
+        int it = 0;
+        bool ok = true;
+        for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++it) {
+            int mb, nb;
+            tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, &mb, &nb);
+            const int acc = it & 1;
+            const uint32_t acc_phase = (it >> 1) & 1;
+            ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p, kSiteEpilogueTmemFull, t);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after_sync();
+            const int row0 = mb * Cf::kTileM + (int)rank * kBM + q * 32;
+            const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN);
+            for (int c = 0; c < kChunks; ++c, ++chunk_iter) {
+                const uint32_t buf = chunk_iter & 1u;
+                const uint32_t sbuf = epi + buf * kEpiBufBytes;
+                const int col0 = nb * kBN + c * kChunkCols;
+                if (col0 >= p.N) break;   // the rest of this tile lies beyond the last column
+                // the store issued from this buffer two chunks ago must have read it
+                if (lane == 0) {
+                    if (prev_stored)
+                        ptx::bulk_wait_group_read<1>();
+                    else
+                        ptx::bulk_wait_group_read<0>();
+                }
+                __syncwarp();
+                if (has_c && lane == 0) {
+                    ptx::mbar_arrive_expect_tx(c_bar(ew, buf), kEpiBufBytes);
+                    ptx::tma_load_2d(sbuf, &tmC, col0, row0, c_bar(ew, buf));
+                }
+                uint32_t v[kChunkCols];
+                ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(c * kChunkCols),
+                                        *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                if constexpr (kChunkCols == 64)
+                    ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(c * kChunkCols + 32),
+                                            *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                ptx::tmem_wait_ld();
+                if (has_c) {
+                    ok = wait_bounded(c_bar(ew, buf), (chunk_iter >> 1) & 1u, abort_flag, p, kSiteEpilogueC, t);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
+                const uint32_t row_addr = sbuf + (uint32_t)lane * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t addr = row_addr + ((uint32_t)(j ^ (lane & 7)) << 4);
+                    uint32_t w[4];
+                    if constexpr (kOutBytes == 4) {
+                        float o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) o[e] = alpha * __uint_as_float(v[4 * j + e]);
+                        if (has_c) {
+                            uint32_t cv[4];
+                            ptx::ld_shared_v4(addr, cv[0], cv[1], cv[2], cv[3]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                o[e] = fmaf(alpha, __uint_as_float(v[4 * j + e]), beta * __uint_as_float(cv[e]));
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) w[e] = __float_as_uint(o[e]);
+                    } else {
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = alpha * __uint_as_float(v[8 * j + e]);
+                        if (has_c) {
+                            uint32_t cv[4];
+                            ptx::ld_shared_v4(addr, cv[0], cv[1], cv[2], cv[3]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 cf = unpack2(cv[e], kOut);
+                                o[2 * e] = fmaf(alpha, __uint_as_float(v[8 * j + 2 * e]), beta * cf.x);
+                                o[2 * e + 1] = fmaf(alpha, __uint_as_float(v[8 * j + 2 * e + 1]), beta * cf.y);
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) w[e] = pack2(o[2 * e], o[2 * e + 1], kOut);
+                    }
+                    ptx::st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                const bool tma_part = col0 < p.n_tma;
+                if (lane == 0) {
+                    if (tma_part) {
+                        ptx::tma_store_2d(&tmD, sbuf, col0, row0);
+                        ptx::bulk_commit_group();
+                    }
+                    prev_stored = tma_part;
+                }
+                // columns [n_tma, N) of this row, one element at a time
+                if (col0 + kChunkCols > p.n_tma && row0 + lane < p.M) {
+                    const int c_begin = col0 > p.n_tma ? col0 : p.n_tma;
+                    const int c_end = col0 + kChunkCols < p.N ? col0 + kChunkCols : p.N;
+                    char* drow = static_cast<char*>(p.d_ptr) + ((int64_t)(row0 + lane) * p.ldd) * kOutBytes;
+                    for (int col = c_begin; col < c_end; ++col) {
+                        const int cc = col - col0;
+                        const uint32_t addr =
+                            row_addr + ((uint32_t)((cc / kVec) ^ (lane & 7)) << 4) + (uint32_t)((cc % kVec) * kOutBytes);
+                        if constexpr (kOutBytes == 4)
+                            *reinterpret_cast<uint32_t*>(drow + (int64_t)col * 4) = ptx::ld_shared_u32(addr);
+                        else
+                            *reinterpret_cast<uint16_t*>(drow + (int64_t)col * 2) = ptx::ld_shared_u16(addr);
+                    }
+                }
+            }
+            if (!ok) break;
+            // every TMEM read of this accumulator has completed (wait::ld)
+            ptx::tc_fence_before_sync();
+            if constexpr (kPair)
+                ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
+            else
+                ptx::mbar_arrive(tempty_bar(acc));
+        }
+        if (lane == 0) ptx::bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before_sync();
+    if constexpr (kPair)
+        ptx::cluster_sync();
+    else
+        __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after_sync();
+        ptx::tmem_dealloc<kCG>(tmem_base, kTmemCols);
+    }
+}
+
+// K = 0: the sum is empty, D = alpha * 0 + beta * C (C not read when beta = 0).
+template <int kOut>
+__global__ void gemm_k0_kernel(void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,
+                               float beta, int has_c) {
+    const int64_t total = (int64_t)M * N;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t i = idx / N, j = idx - (idx / N) * N;
+        const float acc = 0.0f;
+        float d = alpha * acc;
+        if (kOut == kOutF32) {
+            if (has_c) d = fmaf(alpha, acc, beta * static_cast<const float*>(C)[i * ldc + j]);
+            static_cast<float*>(D)[i * ldd + j] = d;
+        } else if (kOut == kOutF16) {
+            if (has_c) d = fmaf(alpha, acc, beta * __half2float(static_cast<const __half*>(C)[i * ldc + j]));
+            static_cast<__half*>(D)[i * ldd + j] = __float2half_rn(d);
+        } else {
+            if (has_c)
+                d = fmaf(alpha, acc, beta * __bfloat162float(static_cast<const __nv_bfloat16*>(C)[i * ldc + j]));
+            static_cast<__nv_bfloat16*>(D)[i * ldd + j] = __float2bfloat16_rn(d);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host-side launch helpers (called from gemm_api.cpp)
+
+template <bool kPair, int kOut>
+static cudaError_t prepare_one() {
+    return cudaFuncSetAttribute(gemm_tcgen05_kernel<kPair, kOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<kPair>::kSmemBytes);
+}
+
+cudaError_t prepare_kernels_on_current_device() {
+    cudaError_t e;
+    if ((e = prepare_one<false, kOutF32>()) != cudaSuccess) return e;
+    if ((e = prepare_one<false, kOutF16>()) != cudaSuccess) return e;
+    if ((e = prepare_one<false, kOutBF16>()) != cudaSuccess) return e;
+    if ((e = prepare_one<true, kOutF32>()) != cudaSuccess) return e;
+    if ((e = prepare_one<true, kOutF16>()) != cudaSuccess) return e;
+    if ((e = prepare_one<true, kOutBF16>()) != cudaSuccess) return e;
+    return cudaSuccess;
+}
+
+int tcgen05_tile_m(int pair) { return pair ? Cfg<true>::kTileM : Cfg<false>::kTileM; }
+int tcgen05_tile_n() { return kBN; }
+int tcgen05_block_k() { return kBK; }
+int tcgen05_load_rows_b(int pair) { return pair ? Cfg<true>::kLoadN : Cfg<false>::kLoadN; }
+int tcgen05_load_rows_a() { return kBM; }
+int tcgen05_smem_bytes(int pair) { return pair ? Cfg<true>::kSmemBytes : Cfg<false>::kSmemBytes; }
+
+template <bool kPair, int kOut>
+static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.grid, 1, 1);
+    cfg.blockDim = dim3(kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<kPair>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (kPair) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut>, L.a, L.b, L.c, L.d, L.p);
+}
+
+cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream) {
+    if (L.pair) {
+        if (L.out == kOutF32) return launch_one<true, kOutF32>(L, stream);
+        if (L.out == kOutF16) return launch_one<true, kOutF16>(L, stream);
+        return launch_one<true, kOutBF16>(L, stream);
+    }
+    if (L.out == kOutF32) return launch_one<false, kOutF32>(L, stream);
+    if (L.out == kOutF16) return launch_one<false, kOutF16>(L, stream);
+    return launch_one<false, kOutBF16>(L, stream);
+}
+
+cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,
+                      float beta, int has_c, int num_sms, cudaStream_t stream) {
+    const int64_t total = (int64_t)M * N;
+    int64_t blocks = (total + 255) / 256;
+    const int64_t cap = (int64_t)num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    if (out == kOutF32)
+        gemm_k0_kernel<kOutF32><<<(unsigned)blocks, 256, 0, stream>>>(D, C, M, N, ldc, ldd, alpha, beta, has_c);
+    else if (out == kOutF16)
+        gemm_k0_kernel<kOutF16><<<(unsigned)blocks, 256, 0, stream>>>(D, C, M, N, ldc, ldd, alpha, beta, has_c);
+    else
+        gemm_k0_kernel<kOutBF16><<<(unsigned)blocks, 256, 0, stream>>>(D, C, M, N, ldc, ldd, alpha, beta, has_c);
+    return cudaGetLastError();
+}
+
+}  // namespace gb300

@@ -1,0 +1,138 @@
+/*
+ * gemm_gb300.h -- C ABI of the GB300 (sm_103a) dense GEMM library
+ * (libgemm_gb300.so).
+ *
+ *   D = alpha * op(A) @ op(B) + beta * C
+ *
+ * The operation is the tile-level contraction of the TVM TIRx "gemm" page
+ * (opening paragraph: "D = alpha*A@B + beta*C"; table "What it accepts":
+ * float16 / bfloat16 operands, float32 accumulator; beta 0 -> D = A@B,
+ * beta 1 -> D = A@B + C) with the general epilogue alpha * acc + beta * c_old
+ * of the Phobos "@tensorcore" page (example gemm_fp16tc_fp32acc.ph), for
+ * whole row-major matrices in GPU memory.
+ *
+ * Layout (TIRx gemm guide, section 二, dimension consistency: the
+ * transpose flags only name the logical orientation, the operation is
+ * normalised to A = [M,K], B = [K,N], C = D = [M,N]):
+ *   A  row-major [M, K] (transA = 0) or [K, M] (transA = 1), lda = its row stride
+ *   B  row-major [K, N] (transB = 0) or [N, K] (transB = 1), ldb = its row stride
+ *   C  row-major [M, N], ldc = row stride (read only when beta != 0)
+ *   D  row-major [M, N], ldd = row stride
+ * Leading dimensions are in elements.
+ *
+ * Precision: A and B are both in_dtype (GEMM_F16 or GEMM_BF16; one dtype
+ * for both, so mixed operand types cannot be expressed); products are
+ * accumulated in fp32 on the tensor cores; the epilogue computes
+ * fmaf(alpha, acc, beta * c) in fp32 (alpha * acc when beta == 0) and
+ * rounds to out_dtype (round-to-nearest-even for 16-bit outputs).  C has
+ * out_dtype.  beta == 0 means "D zero-initialised": C is not read and may
+ * be NULL, and NaNs in C do not reach D.
+ *
+ * Ownership and ordering: the caller owns every buffer; all four pointers
+ * are device pointers valid on the current device.  gemm() enqueues its
+ * work on `stream` and returns without synchronising.  The library keeps
+ * one small device status block per device (allocated on the first call on
+ * that device) and no per-call device memory.  Calls are thread-safe.
+ *
+ * Errors: gemm() returns GEMM_OK or a negative GEMM_ERR_* code.  Every
+ * argument error is detected before anything is enqueued, and D is then
+ * untouched.  A failure inside the kernel (a pipeline wait that exceeded
+ * its time bound) is reported by gemm_poll_device_error().
+ */
+#ifndef GEMM_GB300_H
+#define GEMM_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_API __attribute__((visibility("default")))
+#else
+#define GEMM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* = cudaStream_t; NULL is the legacy default stream */
+
+typedef enum {
+    GEMM_F16 = 0,  /* IEEE binary16 */
+    GEMM_BF16 = 1, /* bfloat16 */
+    GEMM_F32 = 2   /* IEEE binary32 (outputs only) */
+} gemm_dtype_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1,       /* negative size, flag not 0/1, ld too small, NULL buffer */
+    GEMM_ERR_UNSUPPORTED_DTYPE = -2, /* in_dtype not F16/BF16, or out_dtype not F32/F16/BF16 */
+    GEMM_ERR_MISALIGNED = -3,        /* a buffer not 16-byte aligned, or ld * element size not a multiple of 16 */
+    GEMM_ERR_ALIAS = -4,             /* D overlaps A or B, or overlaps C other than C == D with ldc == ldd */
+    GEMM_ERR_ARCH = -5,              /* the current device is not an sm_103 (GB300) GPU */
+    GEMM_ERR_LAUNCH = -6,            /* the kernel launch was refused */
+    GEMM_ERR_CUDA = -7,              /* another CUDA runtime / driver error */
+    GEMM_ERR_DEVICE_TIMEOUT = -8,    /* (gemm_poll_device_error) an in-kernel wait gave up */
+    GEMM_ERR_TOO_LARGE = -9          /* a dimension above 2^31 - 1, or a stride above 2^40 bytes */
+} gemm_status_t;
+
+/*
+ * D = alpha * op(A) @ op(B) + beta * C on the current device, enqueued on
+ * `stream`.
+ *
+ *   M, N, K          sizes, >= 0.  M == 0 or N == 0: nothing to do, GEMM_OK.
+ *                    K == 0: the sum is empty, D = alpha * 0 + beta * C.
+ *   lda, ldb         >= the stored row length of A / B (K or M, N or K) when
+ *                    K > 0; ignored when K == 0.
+ *   ldc              >= N when beta != 0; ignored otherwise.
+ *   ldd              >= N.
+ *   transA, transB   0 or 1 (see the layout above).
+ *   alpha, beta      any float; beta == 0.0f selects "C not read".
+ *   in_dtype         GEMM_F16 or GEMM_BF16 (A and B).
+ *   out_dtype        GEMM_F32, GEMM_F16 or GEMM_BF16 (C and D).
+ *   stream           CUDA stream of the current device.
+ *
+ * Alignment: A, B, C, D must be 16-byte aligned and lda*2, ldb*2,
+ * ldc*sizeof(out), ldd*sizeof(out) multiples of 16 bytes (TMA's rule).
+ * Returns GEMM_OK or a GEMM_ERR_* code (see gemm_status_t).
+ * Setting the environment variable GEMM_LOG=1 prints each call's plan or
+ * rejection reason to stderr.
+ */
+GEMM_API int gemm(void* D, const void* A, const void* B, const void* C,
+         int64_t M, int64_t N, int64_t K,
+         int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd,
+         int transA, int transB, float alpha, float beta,
+         int in_dtype, int out_dtype, struct CUstream_st* stream);
+
+/* A static, human-readable name for a gemm_status_t value (never NULL). */
+GEMM_API const char* gemm_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * block.  Returns GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT when a kernel's pipeline
+ * wait exceeded its bound (GEMM_WAIT_TIMEOUT_NS, default 2 s) since the last
+ * poll, or GEMM_ERR_CUDA when the stream reports a CUDA error.  When
+ * `info` is not NULL it receives four ints: code, block, wait site, detail.
+ */
+GEMM_API int gemm_poll_device_error(struct CUstream_st* stream, int* info);
+
+/*
+ * Host-only query (no GPU needed): the persistent kernel's tile order.
+ * For a grid of num_m x num_n output tiles rasterised in groups of group_m
+ * tile rows, writes the (m, n) tile coordinates of tile index `tile`.
+ * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for out-of-range arguments.
+ */
+GEMM_API int gemm_tile_coords(int tile, int num_m, int num_n, int group_m, int* m_blk, int* n_blk);
+
+/*
+ * Host-only query (no GPU needed): the kernel configuration gemm() would
+ * choose for these sizes on a GPU with num_sms SMs.  out[0..5] receive:
+ * cta_pair (1 = 2-SM tiles), tile_m, tile_n, number of tiles, grid size
+ * (CTAs), dynamic shared memory bytes.  Returns GEMM_OK or an error code.
+ */
+GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_GB300_H */
