@@ -51,6 +51,8 @@ def load_library():
             lib.gemm_tile_coords.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
             lib.gemm_plan.restype = i32
             lib.gemm_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64)]
+            lib.gemm_noalloc.restype = i32
+            lib.gemm_noalloc.argtypes = list(lib.gemm.argtypes)
             _lib = lib
     return _lib
 
@@ -83,6 +85,17 @@ def gemm(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
     return lib.gemm(_addr(D), _addr(A), _addr(B), _addr(C), int(M), int(N), int(K), int(lda), int(ldb),
                     int(ldc), int(ldd), int(transA), int(transB), float(alpha), float(beta),
                     int(in_dtype), int(out_dtype), _stream(stream))
+
+
+def gemm_noalloc(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
+                 in_dtype, out_dtype, stream=None) -> int:
+    """The C entry point ``gemm_noalloc``: what ``gemm`` computes, for callers
+    that cannot allocate device memory (the library then uses a fixed static
+    scratch record instead of a cudaMalloc'd one).  Returns its status."""
+    lib = load_library()
+    return lib.gemm_noalloc(_addr(D), _addr(A), _addr(B), _addr(C), int(M), int(N), int(K), int(lda),
+                            int(ldb), int(ldc), int(ldd), int(transA), int(transB), float(alpha),
+                            float(beta), int(in_dtype), int(out_dtype), _stream(stream))
 
 
 def gemm_status_string(status: int) -> str:

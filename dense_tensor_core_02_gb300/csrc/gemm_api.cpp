@@ -419,3 +419,199 @@ int gemm_poll_device_error(struct CUstream_st* stream, int* info) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// gemm_noalloc(): the same computation for callers that must not allocate
+// device memory.  Its set-up (once per device) only queries attributes, sets
+// the kernels' shared-memory limit and looks up the static scratch's device
+// address; each call then validates, encodes the TMA maps on the host
+// stack, clears the status record with a stream-ordered memset and
+// launches.  Nothing on this path calls cudaMalloc, cudaFree or any other
+// allocating routine.
+
+namespace {
+
+struct NoAllocState {
+    bool ready = false;
+    int status = GEMM_OK;
+    int num_sms = 0;
+    DeviceStatus* scratch_status = nullptr;   // device address of the static scratch
+};
+
+NoAllocState g_noalloc[kMaxDevices];
+
+int noalloc_device_state(int dev, NoAllocState** out) {
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    NoAllocState& st = g_noalloc[dev];
+    if (!st.ready) {
+        st.ready = true;
+        int major = 0, minor = 0;
+        void* scratch = nullptr;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            st.status = GEMM_ERR_CUDA;
+        } else if (major != 10 || minor != 3) {
+            st.status = GEMM_ERR_ARCH;
+        } else if (gb300::prepare_kernels_on_current_device() != cudaSuccess) {
+            st.status = GEMM_ERR_CUDA;
+        } else if (gb300::noalloc_scratch_address(&scratch) != cudaSuccess || scratch == nullptr) {
+            st.status = GEMM_ERR_CUDA;
+        } else {
+            st.scratch_status = static_cast<DeviceStatus*>(scratch);
+        }
+        if (st.status != GEMM_OK) cudaGetLastError();
+    }
+    *out = &st;
+    return st.status;
+}
+
+// The argument rules of gemm(), checked without touching the device.
+int noalloc_validate(const void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float beta,
+                     int in_dtype, int out_dtype) {
+    if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16) return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "in_dtype");
+    if (out_dtype != GEMM_F32 && out_dtype != GEMM_F16 && out_dtype != GEMM_BF16)
+        return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "out_dtype");
+    if (M < 0 || N < 0 || K < 0) return reject(GEMM_ERR_INVALID_ARG, "negative size");
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
+        return reject(GEMM_ERR_INVALID_ARG, "transpose flag not 0/1");
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return reject(GEMM_ERR_TOO_LARGE, "dimension");
+    const bool has_c = beta != 0.0f;
+    const int osz = elem_size(out_dtype);
+    if (!D) return reject(GEMM_ERR_INVALID_ARG, "D is NULL");
+    if (ldd < N) return reject(GEMM_ERR_INVALID_ARG, "ldd < N");
+    if (has_c) {
+        if (!C) return reject(GEMM_ERR_INVALID_ARG, "C is NULL with beta != 0");
+        if (ldc < N) return reject(GEMM_ERR_INVALID_ARG, "ldc < N");
+    }
+    if (K > 0) {
+        if (!A || !B) return reject(GEMM_ERR_INVALID_ARG, "A or B is NULL");
+        if (lda < (transA ? M : K)) return reject(GEMM_ERR_INVALID_ARG, "lda too small");
+        if (ldb < (transB ? K : N)) return reject(GEMM_ERR_INVALID_ARG, "ldb too small");
+        if (lda * 2 >= kMaxStrideBytes || ldb * 2 >= kMaxStrideBytes) return reject(GEMM_ERR_TOO_LARGE, "stride");
+        if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u)
+            return reject(GEMM_ERR_MISALIGNED, "A or B not 16-byte aligned");
+        if (((lda * 2) | (ldb * 2)) & 15) return reject(GEMM_ERR_MISALIGNED, "lda*2 or ldb*2 not a multiple of 16");
+    }
+    if (ldd * osz >= kMaxStrideBytes || (has_c && ldc * osz >= kMaxStrideBytes))
+        return reject(GEMM_ERR_TOO_LARGE, "stride");
+    if (reinterpret_cast<uintptr_t>(D) & 15u) return reject(GEMM_ERR_MISALIGNED, "D not 16-byte aligned");
+    if ((ldd * osz) & 15) return reject(GEMM_ERR_MISALIGNED, "ldd*sizeof(out) not a multiple of 16");
+    if (has_c) {
+        if (reinterpret_cast<uintptr_t>(C) & 15u) return reject(GEMM_ERR_MISALIGNED, "C not 16-byte aligned");
+        if ((ldc * osz) & 15) return reject(GEMM_ERR_MISALIGNED, "ldc*sizeof(out) not a multiple of 16");
+    }
+    uintptr_t d0, d1;
+    byte_range(D, M, N, ldd, osz, &d0, &d1);
+    if (K > 0) {
+        uintptr_t a0, a1, b0, b1;
+        byte_range(A, transA ? K : M, transA ? M : K, lda, 2, &a0, &a1);
+        byte_range(B, transB ? N : K, transB ? K : N, ldb, 2, &b0, &b1);
+        if (overlaps(d0, d1, a0, a1) || overlaps(d0, d1, b0, b1)) return reject(GEMM_ERR_ALIAS, "D overlaps A or B");
+    }
+    if (has_c && !(C == D && ldc == ldd)) {
+        uintptr_t c0, c1;
+        byte_range(C, M, N, ldc, osz, &c0, &c1);
+        if (overlaps(d0, d1, c0, c1)) return reject(GEMM_ERR_ALIAS, "D overlaps C (other than C == D, ldc == ldd)");
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N,
+                                     int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA,
+                                     int transB, float alpha, float beta, int in_dtype, int out_dtype,
+                                     struct CUstream_st* stream) {
+    int rc = noalloc_validate(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, beta, in_dtype, out_dtype);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    // The only scratch is the 16-byte status record, whatever the sizes;
+    // refuse anything that would not fit the static array.
+    if ((int)sizeof(DeviceStatus) > gb300::noalloc_scratch_bytes())
+        return reject(GEMM_ERR_TOO_LARGE, "scratch larger than the static array");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return reject(GEMM_ERR_CUDA, "cudaGetDevice");
+    }
+    NoAllocState* ns = nullptr;
+    if ((rc = noalloc_device_state(dev, &ns)) != GEMM_OK) return reject(rc, "device set-up (no-alloc)");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    const bool has_c = beta != 0.0f;
+    const int osz = elem_size(out_dtype);
+    if (K == 0) {   // epilogue-only kernel: no scratch at all
+        const int ok = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
+        cudaError_t e = gb300::launch_k0(ok, D, has_c ? C : nullptr, (int)M, (int)N, ldc, ldd, alpha, beta,
+                                         has_c ? 1 : 0, ns->num_sms, s);
+        if (e != cudaSuccess) return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+        return GEMM_OK;
+    }
+    if ((rc = get_encoder()) != GEMM_OK) return reject(rc, "cuTensorMapEncodeTiled unavailable");
+    const Plan pl = make_plan(M, N, ns->num_sms);
+    TcgenLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    const uint32_t bk = (uint32_t)gb300::tcgen05_block_k();
+    if (!transA)
+        rc = encode_2d(&L.a, in_dtype, A, K, M, lda, bk, (uint32_t)gb300::tcgen05_load_rows_a());
+    else
+        rc = encode_2d(&L.a, in_dtype, A, M, K, lda, 64, bk);
+    if (rc != GEMM_OK) return reject(rc, "tensor map A");
+    if (transB)
+        rc = encode_2d(&L.b, in_dtype, B, K, N, ldb, bk, (uint32_t)gb300::tcgen05_load_rows_b(pl.pair));
+    else
+        rc = encode_2d(&L.b, in_dtype, B, N, K, ldb, 64, bk);
+    if (rc != GEMM_OK) return reject(rc, "tensor map B");
+    const uint32_t chunk_cols = 128u / (uint32_t)osz;
+    const int64_t vec = 16 / osz;
+    const int64_t n_tma = (N / vec) * vec;
+    if ((rc = encode_2d(&L.d, out_dtype, D, n_tma > 0 ? n_tma : N, M, ldd, chunk_cols, 32)) != GEMM_OK)
+        return reject(rc, "tensor map D");
+    if (has_c && (rc = encode_2d(&L.c, out_dtype, C, N, M, ldc, chunk_cols, 32)) != GEMM_OK)
+        return reject(rc, "tensor map C");
+
+    GemmParams& p = L.p;
+    p.M = (int32_t)M;
+    p.N = (int32_t)N;
+    p.K = (int32_t)K;
+    p.num_m_tiles = pl.num_m;
+    p.num_n_tiles = pl.num_n;
+    p.num_k_blocks = (int32_t)((K + bk - 1) / bk);
+    p.num_tiles = pl.num_tiles;
+    p.group_m = group_m_setting();
+    p.alpha = alpha;
+    p.beta = beta;
+    p.a_mn_major = transA ? 1 : 0;
+    p.b_mn_major = transB ? 0 : 1;
+    p.has_c = has_c ? 1 : 0;
+    p.timeout_ns = wait_timeout_ns();
+    p.skip_first_stage = 0;
+    p.status = ns->scratch_status;
+    p.n_tma = (int32_t)n_tma;
+    p.d_ptr = D;
+    p.ldd = ldd;
+    const uint32_t fmt = in_dtype == GEMM_BF16 ? 1u : 0u;
+    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)p.a_mn_major << 15) |
+              ((uint32_t)p.b_mn_major << 16) | (((uint32_t)pl.tile_n >> 3) << 17) | (((uint32_t)pl.tile_m >> 4) << 24);
+    L.pair = pl.pair;
+    L.out = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
+    L.grid = pl.grid;
+
+    // The status record must start each call at zero (the kernel records
+    // only the first wait that gives up); stream-ordered, allocates nothing.
+    if (cudaMemsetAsync(p.status, 0, sizeof(DeviceStatus), s) != cudaSuccess) {
+        cudaGetLastError();
+        return reject(GEMM_ERR_CUDA, "clearing the static status record");
+    }
+    GEMM_LOGF("no-alloc: M=%lld N=%lld K=%lld: %s tiles %dx%d (%d), grid %d", (long long)M, (long long)N,
+              (long long)K, pl.pair ? "cta-pair" : "1-cta", pl.tile_m, pl.tile_n, pl.num_tiles, pl.grid);
+    cudaError_t e = gb300::launch_tcgen05(L, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+    }
+    return GEMM_OK;
+}

@@ -29,6 +29,11 @@ cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream);
 cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,
                       float beta, int has_c, int num_sms, cudaStream_t stream);
 
+// Static scratch of gemm_noalloc(): its device address on the current
+// device (cudaGetSymbolAddress) and its size in bytes.
+cudaError_t noalloc_scratch_address(void** ptr);
+int noalloc_scratch_bytes();
+
 int tcgen05_tile_m(int pair);      // D rows per tile
 int tcgen05_tile_n();              // D columns per tile
 int tcgen05_block_k();             // K per pipeline stage

@@ -488,6 +488,24 @@ __global__ void gemm_k0_kernel(void* D, const void* C, int M, int N, int64_t ldc
 }
 
 // ---------------------------------------------------------------------------
+// Scratch of the allocation-free entry point gemm_noalloc(): the device
+// status record its launches write lives in this fixed module array (zeroed
+// when the module loads, kept by every GPU that loads the library until the
+// process exits) instead of in a cudaMalloc'd block.  Every gemm_noalloc()
+// call on a device shares it.
+
+constexpr int kNoAllocScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+static_assert(sizeof(DeviceStatus) <= kNoAllocScratchBytes, "the status record must fit the static scratch");
+
+// Device address of the static scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address must come
+// from the runtime; call with the target device current.
+cudaError_t noalloc_scratch_address(void** ptr) { return cudaGetSymbolAddress(ptr, g_noalloc_scratch); }
+
+int noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+// ---------------------------------------------------------------------------
 // host-side launch helpers (called from gemm_api.cpp)
 
 template <bool kPair, int kOut>

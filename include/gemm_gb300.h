@@ -131,6 +131,41 @@ GEMM_API int gemm_tile_coords(int tile, int num_m, int num_n, int group_m, int* 
  */
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out);
 
+/*
+ * gemm_noalloc -- gemm() for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart of this call; it exists for users of this
+ * library.  gemm() obtains its device status record with cudaMalloc the
+ * first time it runs on a device.  Some callers cannot allow that: code
+ * that owns all of the device's memory through its own pool or budget,
+ * code running where CUDA allocation calls are not permitted (for example
+ * from a stream callback), or code that must not add allocations to a
+ * process it does not own.  gemm_noalloc() computes exactly what gemm()
+ * computes, with the same arguments, rules and return codes, through the
+ * same kernel, but never calls cudaMalloc, cudaFree or any other allocating
+ * routine: the kernel's scratch (its 16-byte status record) lives in a
+ * fixed 256-byte array inside the library, which every GPU that loads the
+ * library holds until the process exits.  The scratch does not grow with
+ * the problem, so no problem size exceeds it; a build whose record did not
+ * fit the array would return GEMM_ERR_TOO_LARGE.
+ *
+ *   - The first call on each device does a one-time set-up (device queries,
+ *     the kernels' shared-memory limit, and the device address of the
+ *     static array via cudaGetSymbolAddress).  Make that first call before
+ *     any stream capture.
+ *   - All gemm_noalloc() calls on a device share the one status record; each
+ *     call clears it (a stream-ordered memset) before its kernel starts.
+ *     Calls whose kernels overlap on the GPU (different streams) race on it.
+ *   - A pipeline wait that exceeds its time bound stops the kernel early and
+ *     is recorded only in that static record: gemm_poll_device_error()
+ *     reports the errors of gemm(), not of this call.
+ */
+GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, const void* C,
+                          int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd,
+                          int transA, int transB, float alpha, float beta,
+                          int in_dtype, int out_dtype, struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif
