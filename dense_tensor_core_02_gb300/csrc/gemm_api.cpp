@@ -101,6 +101,35 @@ int group_m_setting() {
     return 8;
 }
 
+// Memory-system tuning of a launch (needs p.num_k_blocks set).
+//  * L2 eviction priorities of the A, B loads and D stores (0 normal, 1
+//    evict-first, 2 evict-last).  Operand panels are re-read by the other
+//    tiles of their row / column group, D is written once and never re-read:
+//    A and B default to evict-last, D to evict-first.  GEMM_L2_HINTS="a,b,d"
+//    overrides.
+//  * Epilogue pacing (GEMM_EPI_PACE_NS overrides): the persistent CTAs run
+//    their tiles nearly in step, so without a pause every SM would store its
+//    finished tile at the same moment.
+void tuning(GemmParams& p) {
+    p.hint_a = 2;
+    p.hint_b = 2;
+    p.hint_d = 1;
+    const char* v = std::getenv("GEMM_L2_HINTS");
+    int a, b, d;
+    if (v && std::sscanf(v, "%d,%d,%d", &a, &b, &d) == 3 && a >= 0 && a <= 2 && b >= 0 && b <= 2 && d >= 0 &&
+        d <= 2) {
+        p.hint_a = a;
+        p.hint_b = b;
+        p.hint_d = d;
+    }
+    p.epi_pace_ns = 0;
+    const char* pv = std::getenv("GEMM_EPI_PACE_NS");
+    if (pv && *pv) {
+        const int ns = std::atoi(pv);
+        if (ns >= 0 && ns <= 100000) p.epi_pace_ns = ns;
+    }
+}
+
 int elem_size(int dtype) { return dtype == GEMM_F32 ? 4 : 2; }
 
 // Byte range [lo, hi) covered by a row-major rows x cols matrix.
@@ -348,7 +377,8 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     p.K = (int32_t)K;
     p.num_m_tiles = pl.num_m;
     p.num_n_tiles = pl.num_n;
-    p.num_k_blocks = (int32_t)((K + bk - 1) / bk);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair);
+    p.num_k_blocks = (int32_t)((K + stage_k - 1) / stage_k);   // pipeline stages per tile
     p.num_tiles = pl.num_tiles;
     p.group_m = group_m_setting();
     p.alpha = alpha;
@@ -361,6 +391,7 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     p.n_tma = (int32_t)n_tma;
     p.d_ptr = D;
     p.ldd = ldd;
+    tuning(p);
     p.status = ds->d_status;
     // tcgen05 instruction descriptor, kind::f16: D format f32 (bits 4-5 = 1),
     // A / B format (bits 7-9, 10-12: 0 = f16, 1 = bf16), A / B major
@@ -579,7 +610,8 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
     p.K = (int32_t)K;
     p.num_m_tiles = pl.num_m;
     p.num_n_tiles = pl.num_n;
-    p.num_k_blocks = (int32_t)((K + bk - 1) / bk);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair);
+    p.num_k_blocks = (int32_t)((K + stage_k - 1) / stage_k);   // pipeline stages per tile
     p.num_tiles = pl.num_tiles;
     p.group_m = group_m_setting();
     p.alpha = alpha;
@@ -593,6 +625,7 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
     p.n_tma = (int32_t)n_tma;
     p.d_ptr = D;
     p.ldd = ldd;
+    tuning(p);
     const uint32_t fmt = in_dtype == GEMM_BF16 ? 1u : 0u;
     p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)p.a_mn_major << 15) |
               ((uint32_t)p.b_mn_major << 16) | (((uint32_t)pl.tile_n >> 3) << 17) | (((uint32_t)pl.tile_m >> 4) << 24);

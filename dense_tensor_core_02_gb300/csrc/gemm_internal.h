@@ -36,7 +36,8 @@ int noalloc_scratch_bytes();
 
 int tcgen05_tile_m(int pair);      // D rows per tile
 int tcgen05_tile_n();              // D columns per tile
-int tcgen05_block_k();             // K per pipeline stage
+int tcgen05_block_k();             // K of one TMA operand box (one 128-byte swizzle row)
+int tcgen05_stage_k(int pair);     // K per pipeline stage
 int tcgen05_load_rows_a();         // A rows (M) one CTA stages per stage
 int tcgen05_load_rows_b(int pair); // B rows (N) one CTA stages per stage
 int tcgen05_smem_bytes(int pair);

@@ -49,6 +49,13 @@ struct GemmParams {
     int32_t pad0;
     void* d_ptr;
     int64_t ldd;            // D row stride in elements
+    // L2 eviction priority of the TMA copies of A, B (loads) and D (stores):
+    // 0 normal, 1 evict-first, 2 evict-last.
+    int32_t hint_a, hint_b, hint_d;
+    // Pause (ns) after each epilogue store chunk, except on a CTA's last
+    // tile: spreads the D writes of all SMs over the next tile's main loop
+    // instead of a simultaneous burst that stalls the operand loads.
+    int32_t epi_pace_ns;
 };
 
 // Persistent-tile order with L2-friendly grouping: tiles run down a group of

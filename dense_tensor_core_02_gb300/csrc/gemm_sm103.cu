@@ -49,15 +49,23 @@ constexpr int kEpiBufBytes = 4096;   // one epilogue staging box: 32 rows x 128 
 constexpr int kTmemCols = 512;       // two 128 x 256 fp32 accumulators
 constexpr int kAtomBytes = 1024;     // 8 rows x 128 bytes: one 128B-swizzle atom
 constexpr int kMnChunkBytes = 64 * kBK * 2;   // one 64-wide MN-major box (64 x 64 x 2 B)
+static_assert(kBK / kUK == 4, "the MMA loop issues four K slices per stage");
 
 template <bool kPair>
 struct Cfg {
     static constexpr int kCtaGroup = kPair ? 2 : 1;
     static constexpr int kTileM = kPair ? 2 * kBM : kBM;   // D rows per tile
     static constexpr int kLoadN = kPair ? kBN / 2 : kBN;   // B rows (N) each CTA stages
-    static constexpr int kStages = kPair ? 6 : 4;
-    static constexpr int kABytes = kBM * kBK * 2;
-    static constexpr int kBBytes = kLoadN * kBK * 2;
+    // A pipeline stage holds kSub 64-wide K sub-blocks.  The MMA issuer pays a
+    // fixed cost per stage (barrier wait, release commit) while the tensor
+    // core queues only a few MMAs, so the pair kernel puts 8 MMAs (2 sub-
+    // blocks) behind each wait: 3 stages x 64 KiB instead of 6 x 32 KiB.
+    static constexpr int kSub = kPair ? 2 : 1;
+    static constexpr int kStages = kPair ? 3 : 4;
+    static constexpr int kASubBytes = kBM * kBK * 2;
+    static constexpr int kBSubBytes = kLoadN * kBK * 2;
+    static constexpr int kABytes = kSub * kASubBytes;
+    static constexpr int kBBytes = kSub * kBSubBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
@@ -124,19 +132,19 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 // Stage one operand tile of `rows` (M or N) x kBK (K).
 template <bool kPair>
 __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* map, int mn_major,
-                                             int row0, int rows, int k0, uint32_t bar) {
+                                             int row0, int rows, int k0, uint32_t bar, uint64_t policy) {
     if (mn_major) {
         for (int j = 0; j < rows / 64; ++j) {
             if constexpr (kPair)
-                ptx::tma_load_2d_pair(dst + j * kMnChunkBytes, map, row0 + 64 * j, k0, bar);
+                ptx::tma_load_2d_pair_hint(dst + j * kMnChunkBytes, map, row0 + 64 * j, k0, bar, policy);
             else
-                ptx::tma_load_2d(dst + j * kMnChunkBytes, map, row0 + 64 * j, k0, bar);
+                ptx::tma_load_2d_hint(dst + j * kMnChunkBytes, map, row0 + 64 * j, k0, bar, policy);
         }
     } else {
         if constexpr (kPair)
-            ptx::tma_load_2d_pair(dst, map, k0, row0, bar);
+            ptx::tma_load_2d_pair_hint(dst, map, k0, row0, bar, policy);
         else
-            ptx::tma_load_2d(dst, map, k0, row0, bar);
+            ptx::tma_load_2d_hint(dst, map, k0, row0, bar, policy);
     }
 }
 
@@ -243,6 +251,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             const uint32_t stage_tx = (kPair ? 2 : 1) * Cf::kStageBytes;
+            const uint64_t pol_a = ptx::l2_policy(p.hint_a);
+            const uint64_t pol_b = ptx::l2_policy(p.hint_b);
             for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
                 int mb, nb;
                 tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, &mb, &nb);
@@ -257,11 +267,14 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     if (!skip) {
                         const uint32_t fb = kPair ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
                         if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), stage_tx);
-                        const int k0 = kb * kBK;
-                        load_operand<kPair>(base + Cf::kOffA + stage * Cf::kABytes, &tmA, p.a_mn_major,
-                                            a_row0, kBM, k0, fb);
-                        load_operand<kPair>(base + Cf::kOffB + stage * Cf::kBBytes, &tmB, p.b_mn_major,
-                                            b_row0, Cf::kLoadN, k0, fb);
+#pragma unroll
+                        for (int sub = 0; sub < Cf::kSub; ++sub) {
+                            const int k0 = (kb * Cf::kSub + sub) * kBK;
+                            load_operand<kPair>(base + Cf::kOffA + stage * Cf::kABytes + sub * Cf::kASubBytes, &tmA,
+                                                p.a_mn_major, a_row0, kBM, k0, fb, pol_a);
+                            load_operand<kPair>(base + Cf::kOffB + stage * Cf::kBBytes + sub * Cf::kBSubBytes, &tmB,
+                                                p.b_mn_major, b_row0, Cf::kLoadN, k0, fb, pol_b);
+                        }
                     }
                     if (++stage == Cf::kStages) {
                         stage = 0;
@@ -284,6 +297,15 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         // ---------------- MMA issuer (the pair's leader CTA only) ----------------
         if (leader && lane == 0) {
             const uint32_t idesc = p.idesc;
+            // Descriptors of stage 0, K slice 0.  A stage or a K slice moves
+            // only the 14-bit start-address field (address >> 4), which cannot
+            // carry out of its field: shared addresses stay below 256 KiB.  So
+            // the loop advances them with plain adds; this single thread must
+            // issue a stage's four MMAs faster than the tensor core runs them.
+            const uint64_t a_desc0 = operand_desc(base + Cf::kOffA, p.a_mn_major, 0);
+            const uint64_t b_desc0 = operand_desc(base + Cf::kOffB, p.b_mn_major, 0);
+            const uint64_t a_kstep = (uint64_t)((p.a_mn_major ? kUK * 128 : kUK * 2) >> 4);
+            const uint64_t b_kstep = (uint64_t)((p.b_mn_major ? kUK * 128 : kUK * 2) >> 4);
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
@@ -300,12 +322,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint32_t sa = base + Cf::kOffA + stage * Cf::kABytes;
-                    const uint32_t sb = base + Cf::kOffB + stage * Cf::kBBytes;
+                    const uint64_t ad = a_desc0 + (uint64_t)(stage * (Cf::kABytes >> 4));
+                    const uint64_t bd = b_desc0 + (uint64_t)(stage * (Cf::kBBytes >> 4));
 #pragma unroll
-                    for (int kk = 0; kk < kBK / kUK; ++kk) {
-                        ptx::mma_f16<kCG>(d_tmem, operand_desc(sa, p.a_mn_major, kk),
-                                          operand_desc(sb, p.b_mn_major, kk), idesc, (kb | kk) != 0);
+                    for (int sub = 0; sub < Cf::kSub; ++sub) {
+                        const uint64_t as = ad + (uint64_t)(sub * (Cf::kASubBytes >> 4));
+                        const uint64_t bs = bd + (uint64_t)(sub * (Cf::kBSubBytes >> 4));
+#pragma unroll
+                        for (int kk = 0; kk < kBK / kUK; ++kk)
+                            ptx::mma_f16<kCG>(d_tmem, as + kk * a_kstep, bs + kk * b_kstep, idesc,
+                                              (kb | sub | kk) != 0);
                     }
                     if constexpr (kPair)
                         ptx::mma_commit_pair(empty_bar(stage), 0x3);
@@ -333,6 +359,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         const float beta = p.beta;
         const bool has_c = p.has_c != 0;
         constexpr int kVec = 16 / kOutBytes;   // elements per 16-byte piece
+        const uint64_t pol_d = ptx::l2_policy(p.hint_d);
         uint32_t chunk_iter = 0;
         bool prev_stored = false;   // lane 0: the previous chunk committed a TMA store
         int it = 0;
@@ -348,6 +375,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::tc_fence_after_sync();
             const int row0 = mb * Cf::kTileM + (int)rank * kBM + q * 32;
             const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN);
+            const bool pace = p.epi_pace_ns > 0 && t + num_clusters < p.num_tiles;
             for (int c = 0; c < kChunks; ++c, ++chunk_iter) {
                 const uint32_t buf = chunk_iter & 1u;
                 const uint32_t sbuf = epi + buf * kEpiBufBytes;
@@ -419,7 +447,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 const bool tma_part = col0 < p.n_tma;
                 if (lane == 0) {
                     if (tma_part) {
-                        ptx::tma_store_2d(&tmD, sbuf, col0, row0);
+                        ptx::tma_store_2d_hint(&tmD, sbuf, col0, row0, pol_d);
                         ptx::bulk_commit_group();
                     }
                     prev_stored = tma_part;
@@ -439,6 +467,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                             *reinterpret_cast<uint16_t*>(drow + (int64_t)col * 2) = ptx::ld_shared_u16(addr);
                     }
                 }
+                if (pace) __nanosleep((unsigned)p.epi_pace_ns);
             }
             if (!ok) break;
             // every TMEM read of this accumulator has completed (wait::ld)
@@ -528,6 +557,7 @@ cudaError_t prepare_kernels_on_current_device() {
 int tcgen05_tile_m(int pair) { return pair ? Cfg<true>::kTileM : Cfg<false>::kTileM; }
 int tcgen05_tile_n() { return kBN; }
 int tcgen05_block_k() { return kBK; }
+int tcgen05_stage_k(int pair) { return kBK * (pair ? Cfg<true>::kSub : Cfg<false>::kSub); }
 int tcgen05_load_rows_b(int pair) { return pair ? Cfg<true>::kLoadN : Cfg<false>::kLoadN; }
 int tcgen05_load_rows_a() { return kBM; }
 int tcgen05_smem_bytes(int pair) { return pair ? Cfg<true>::kSmemBytes : Cfg<false>::kSmemBytes; }
