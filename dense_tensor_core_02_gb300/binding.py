@@ -120,11 +120,11 @@ def gemm_tile_coords(tile, num_m, num_n, group_m):
 
 
 def gemm_plan(M, N, K, num_sms):
-    out = (ctypes.c_int64 * 6)()
+    out = (ctypes.c_int64 * 8)()
     rc = load_library().gemm_plan(int(M), int(N), int(K), int(num_sms), out)
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_plan")
-    keys = ("cta_pair", "tile_m", "tile_n", "num_tiles", "grid", "smem_bytes")
+    keys = ("cta_pair", "tile_m", "tile_n", "num_tiles", "grid", "smem_bytes", "epi_warps", "stages")
     return dict(zip(keys, list(out)))
 
 

@@ -210,9 +210,20 @@ struct Plan {
     int num_m, num_n, num_tiles;
     int grid;
     int smem;
+    int epi_warps;
+    int stages;
 };
 
-Plan make_plan(int64_t M, int64_t N, int num_sms) {
+// Epilogue warps: 8 when a tile's main loop is short (few K stages), so the
+// time goes into storing D; 4 otherwise.  GEMM_EPI_WARPS=4|8 overrides.
+int epi_warps_for(int64_t K, int pair) {
+    const char* v = std::getenv("GEMM_EPI_WARPS");
+    if (v && (std::strcmp(v, "4") == 0 || std::strcmp(v, "8") == 0)) return std::atoi(v);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pair);
+    return (K + stage_k - 1) / stage_k <= 4 ? 8 : 4;
+}
+
+Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms) {
     Plan pl{};
     int ov = variant_override();
     pl.pair = ov >= 0 ? ov : (M > gb300::tcgen05_tile_m(0) ? 1 : 0);
@@ -225,7 +236,9 @@ Plan make_plan(int64_t M, int64_t N, int num_sms) {
     int clusters = pl.num_tiles < units ? pl.num_tiles : units;
     if (clusters < 1) clusters = 1;
     pl.grid = pl.pair ? 2 * clusters : clusters;
-    pl.smem = gb300::tcgen05_smem_bytes(pl.pair);
+    pl.epi_warps = epi_warps_for(K, pl.pair);
+    pl.smem = gb300::tcgen05_smem_bytes(pl.pair, pl.epi_warps);
+    pl.stages = gb300::tcgen05_stages(pl.pair, pl.epi_warps);
     return pl;
 }
 
@@ -259,13 +272,15 @@ int gemm_tile_coords(int tile, int num_m, int num_n, int group_m, int* m_blk, in
 int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out) {
     if (M < 1 || N < 1 || K < 0 || num_sms < 2 || !out) return GEMM_ERR_INVALID_ARG;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_TOO_LARGE;
-    Plan pl = make_plan(M, N, num_sms);
+    Plan pl = make_plan(M, N, K, num_sms);
     out[0] = pl.pair;
     out[1] = pl.tile_m;
     out[2] = pl.tile_n;
     out[3] = pl.num_tiles;
     out[4] = pl.grid;
     out[5] = pl.smem;
+    out[6] = pl.epi_warps;
+    out[7] = pl.stages;
     return GEMM_OK;
 }
 
@@ -344,7 +359,7 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     }
 
     if ((rc = get_encoder()) != GEMM_OK) return reject(rc, "cuTensorMapEncodeTiled unavailable");
-    const Plan pl = make_plan(M, N, ds->num_sms);
+    const Plan pl = make_plan(M, N, K, ds->num_sms);
     TcgenLaunch L;
     std::memset(&L, 0, sizeof(L));
     const uint32_t bk = (uint32_t)gb300::tcgen05_block_k();
@@ -403,10 +418,13 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     L.pair = pl.pair;
     L.out = out_kind;
     L.grid = pl.grid;
+    L.epi_warps = pl.epi_warps;
 
-    GEMM_LOGF("M=%lld N=%lld K=%lld trans=%d%d in=%d out=%d beta%s0: %s tiles %dx%d (%d), grid %d, smem %d",
+    GEMM_LOGF("M=%lld N=%lld K=%lld trans=%d%d in=%d out=%d beta%s0: %s tiles %dx%d (%d), grid %d, smem %d, "
+              "%d epilogue warps, %d stages",
               (long long)M, (long long)N, (long long)K, transA, transB, in_dtype, out_dtype, has_c ? "!=" : "==",
-              pl.pair ? "cta-pair" : "1-cta", pl.tile_m, pl.tile_n, pl.num_tiles, pl.grid, pl.smem);
+              pl.pair ? "cta-pair" : "1-cta", pl.tile_m, pl.tile_n, pl.num_tiles, pl.grid, pl.smem, pl.epi_warps,
+              pl.stages);
     cudaError_t e = gb300::launch_tcgen05(L, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -582,7 +600,7 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
         return GEMM_OK;
     }
     if ((rc = get_encoder()) != GEMM_OK) return reject(rc, "cuTensorMapEncodeTiled unavailable");
-    const Plan pl = make_plan(M, N, ns->num_sms);
+    const Plan pl = make_plan(M, N, K, ns->num_sms);
     TcgenLaunch L;
     std::memset(&L, 0, sizeof(L));
     const uint32_t bk = (uint32_t)gb300::tcgen05_block_k();
@@ -632,6 +650,7 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
     L.pair = pl.pair;
     L.out = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
     L.grid = pl.grid;
+    L.epi_warps = pl.epi_warps;
 
     // The status record must start each call at zero (the kernel records
     // only the first wait that gives up); stream-ordered, allocates nothing.

@@ -22,6 +22,7 @@ struct TcgenLaunch {
     int pair;                 // 1: CTA-pair (cta_group::2) kernel
     int out;                  // OutKind
     int grid;                 // CTAs (a multiple of 2 for the pair kernel)
+    int epi_warps;            // 4 or 8 epilogue warps
 };
 
 cudaError_t prepare_kernels_on_current_device();
@@ -40,6 +41,7 @@ int tcgen05_block_k();             // K of one TMA operand box (one 128-byte swi
 int tcgen05_stage_k(int pair);     // K per pipeline stage
 int tcgen05_load_rows_a();         // A rows (M) one CTA stages per stage
 int tcgen05_load_rows_b(int pair); // B rows (N) one CTA stages per stage
-int tcgen05_smem_bytes(int pair);
+int tcgen05_smem_bytes(int pair, int epi_warps);
+int tcgen05_stages(int pair, int epi_warps);
 
 }  // namespace gb300

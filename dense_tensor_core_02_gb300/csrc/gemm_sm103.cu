@@ -43,43 +43,52 @@ constexpr int kBM = 128;             // accumulator rows per CTA (= TMEM lanes)
 constexpr int kBN = 256;             // accumulator columns per tile
 constexpr int kBK = 64;              // K per stage: one 128-byte swizzle row of 16-bit elements
 constexpr int kUK = 16;              // K per tcgen05.mma kind::f16
-constexpr int kNumThreads = 192;     // 6 warps
-constexpr int kEpiWarps = 4;
 constexpr int kEpiBufBytes = 4096;   // one epilogue staging box: 32 rows x 128 bytes
 constexpr int kTmemCols = 512;       // two 128 x 256 fp32 accumulators
 constexpr int kAtomBytes = 1024;     // 8 rows x 128 bytes: one 128B-swizzle atom
 constexpr int kMnChunkBytes = 64 * kBK * 2;   // one 64-wide MN-major box (64 x 64 x 2 B)
+constexpr int kSmemBudget = 232448;  // dynamic shared memory per CTA on sm_103
 static_assert(kBK / kUK == 4, "the MMA loop issues four K slices per stage");
 
-template <bool kPair>
+// kEpiW epilogue warps: 4 (one per TMEM lane quadrant, each storing all 256
+// columns of its 32 rows) for K-heavy shapes, or 8 (two per quadrant, 128
+// columns each) for shapes whose time goes into storing D; the operand ring
+// gets whatever shared memory the staging boxes leave.
+template <bool kPair, int kEpiW>
 struct Cfg {
     static constexpr int kCtaGroup = kPair ? 2 : 1;
     static constexpr int kTileM = kPair ? 2 * kBM : kBM;   // D rows per tile
     static constexpr int kLoadN = kPair ? kBN / 2 : kBN;   // B rows (N) each CTA stages
+    static constexpr int kEpiWarps = kEpiW;
+    static constexpr int kNumThreads = 64 + 32 * kEpiW;    // producer, MMA, epilogue warps
+    static constexpr int kEpiCols = kBN / (kEpiW / 4);     // accumulator columns per epilogue warp
     // A pipeline stage holds kSub 64-wide K sub-blocks.  The MMA issuer pays a
     // fixed cost per stage (barrier wait, release commit) while the tensor
     // core queues only a few MMAs, so the pair kernel puts 8 MMAs (2 sub-
-    // blocks) behind each wait: 3 stages x 64 KiB instead of 6 x 32 KiB.
+    // blocks) behind each wait: 64 KiB stages instead of 32 KiB ones.
     static constexpr int kSub = kPair ? 2 : 1;
-    static constexpr int kStages = kPair ? 3 : 4;
     static constexpr int kASubBytes = kBM * kBK * 2;
     static constexpr int kBSubBytes = kLoadN * kBK * 2;
     static constexpr int kABytes = kSub * kASubBytes;
     static constexpr int kBBytes = kSub * kBSubBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;
+    // staging boxes per epilogue warp: the store-bound configuration keeps
+    // more D bytes in flight per SM
+    static constexpr int kEpiBufs = kEpiW == 8 ? 3 : 2;
+    static constexpr int kEpiBytes = kEpiW * kEpiBufs * kEpiBufBytes;
+    static constexpr int kStages = (kSmemBudget - kEpiBytes - 2048) / kStageBytes;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
     static constexpr int kOffEpi = kOffB + kStages * kBBytes;
-    static constexpr int kOffBar = kOffEpi + kEpiWarps * 2 * kEpiBufBytes;
-    // full[S], empty[S], tmem_full[2], tmem_empty[2], c_ready[4 warps][2]
-    static constexpr int kNumBars = 2 * kStages + 4 + 2 * kEpiWarps;
+    static constexpr int kOffBar = kOffEpi + kEpiBytes;
+    // full[S], empty[S], tmem_full[2], tmem_empty[2], c_ready[epilogue warps][kEpiBufs]
+    static constexpr int kNumBars = 2 * kStages + 4 + kEpiBufs * kEpiW;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kSmemBytes = kOffAbort + 4 + 1024;   // + base alignment slack
+    static_assert(kStages >= 2, "at least two operand stages");
+    static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
 };
-
-static_assert(Cfg<false>::kSmemBytes <= 232448, "shared memory budget (1-CTA)");
-static_assert(Cfg<true>::kSmemBytes <= 232448, "shared memory budget (CTA pair)");
 
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand:
 // start address, leading / stride byte offsets (all >> 4), the fixed
@@ -181,16 +190,17 @@ __device__ __forceinline__ float2 unpack2(uint32_t u, int out) {
     return __bfloat1622float2(h);
 }
 
-template <bool kPair, int kOut>
-__global__ void __launch_bounds__(kNumThreads, 1)
+template <bool kPair, int kOut, int kEpiW>
+__global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const GemmParams p) {
-    using Cf = Cfg<kPair>;
+    using Cf = Cfg<kPair, kEpiW>;
     constexpr int kCG = Cf::kCtaGroup;
+    constexpr int kEpiWarps = Cf::kEpiWarps;
     constexpr int kOutBytes = OutTraits<kOut>::kBytes;
     constexpr int kChunkCols = 128 / kOutBytes;   // columns per 128-byte staging row
-    constexpr int kChunks = kBN / kChunkCols;
+    constexpr int kChunks = Cf::kEpiCols / kChunkCols;   // staging chunks per warp and tile
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -207,7 +217,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     auto empty_bar = [&](int s) { return bars + 8u * (Cf::kStages + s); };
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * Cf::kStages + a); };
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * Cf::kStages + 2 + a); };
-    auto c_bar = [&](int w, int b) { return bars + 8u * (2 * Cf::kStages + 4 + 2 * w + b); };
+    auto c_bar = [&](int w, int b) { return bars + 8u * (2 * Cf::kStages + 4 + Cf::kEpiBufs * w + b); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cf::kOffAbort);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Cf::kOffTmemSlot);
 
@@ -221,7 +231,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             ptx::mbar_init(tempty_bar(a), (kPair ? 2 : 1) * kEpiWarps * 32);
         }
         for (int w = 0; w < kEpiWarps; ++w)
-            for (int b = 0; b < 2; ++b) ptx::mbar_init(c_bar(w, b), 1);
+            for (int b = 0; b < Cf::kEpiBufs; ++b) ptx::mbar_init(c_bar(w, b), 1);
         *abort_flag = 0;
         ptx::fence_mbarrier_init();
         ptx::prefetch_tensormap(&tmA);
@@ -351,17 +361,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue warps 2..5 ----------------
+        // ---------------- epilogue warps 2 .. 2 + kEpiW - 1 ----------------
         const int ew = warp - 2;   // staging buffers and C barriers of this warp
         const int q = warp & 3;    // the TMEM lane quadrant this warp may read
-        const uint32_t epi = base + Cf::kOffEpi + ew * 2 * kEpiBufBytes;
+        const int col_begin = (ew / 4) * Cf::kEpiCols;   // this warp's first column in the tile
+        const uint32_t epi = base + Cf::kOffEpi + ew * Cf::kEpiBufs * kEpiBufBytes;
         const float alpha = p.alpha;
         const float beta = p.beta;
         const bool has_c = p.has_c != 0;
         constexpr int kVec = 16 / kOutBytes;   // elements per 16-byte piece
         const uint64_t pol_d = ptx::l2_policy(p.hint_d);
         uint32_t chunk_iter = 0;
-        bool prev_stored = false;   // lane 0: the previous chunk committed a TMA store
         int it = 0;
         bool ok = true;
         for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++it) {
@@ -374,36 +384,54 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             if (!ok) break;
             ptx::tc_fence_after_sync();
             const int row0 = mb * Cf::kTileM + (int)rank * kBM + q * 32;
-            const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN);
+            const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN + col_begin);
             const bool pace = p.epi_pace_ns > 0 && t + num_clusters < p.num_tiles;
-            for (int c = 0; c < kChunks; ++c, ++chunk_iter) {
-                const uint32_t buf = chunk_iter & 1u;
-                const uint32_t sbuf = epi + buf * kEpiBufBytes;
-                const int col0 = nb * kBN + c * kChunkCols;
-                if (col0 >= p.N) break;   // the rest of this tile lies beyond the last column
-                // the store issued from this buffer two chunks ago must have read it
-                if (lane == 0) {
-                    if (prev_stored)
-                        ptx::bulk_wait_group_read<1>();
-                    else
-                        ptx::bulk_wait_group_read<0>();
-                }
-                __syncwarp();
-                if (has_c && lane == 0) {
-                    ptx::mbar_arrive_expect_tx(c_bar(ew, buf), kEpiBufBytes);
-                    ptx::tma_load_2d(sbuf, &tmC, col0, row0, c_bar(ew, buf));
-                }
-                uint32_t v[kChunkCols];
-                ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(c * kChunkCols),
-                                        *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            // Accumulator chunks come out of TMEM one ahead of their use: the
+            // load of chunk c+1 is in flight while chunk c is converted and
+            // staged.  Two named register arrays alternate (chunks are taken
+            // in pairs), so the asynchronously written registers are never
+            // copied or indexed at run time before their wait.
+            uint32_t va[kChunkCols], vb[kChunkCols];
+            auto tmem_load = [&](int c, uint32_t(&v)[kChunkCols]) {
+                ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(c * kChunkCols), *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
                 if constexpr (kChunkCols == 64)
                     ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(c * kChunkCols + 32),
                                             *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-                ptx::tmem_wait_ld();
+            };
+            bool stop = false;
+            auto chunk = [&](int c, uint32_t(&v)[kChunkCols], uint32_t(&next)[kChunkCols]) {
+                if (stop) return;
+                // tcgen05.ld / wait::ld are .sync.aligned: the previous chunk
+                // ended in lane-dependent code (the ragged-column stores), so
+                // the warp reconverges explicitly first.
+                __syncwarp();
+                ptx::tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                if constexpr (kChunkCols == 64) ptx::tmem_wait_ld(*reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                const uint32_t buf = chunk_iter % Cf::kEpiBufs;
+                const uint32_t sbuf = epi + buf * kEpiBufBytes;
+                const int col0 = nb * kBN + col_begin + c * kChunkCols;
+                if (col0 >= p.N) {   // the rest of this tile lies beyond the last column
+                    stop = true;
+                    return;
+                }
+                if (c + 1 < kChunks) tmem_load(c + 1, next);
+                // Every chunk commits one bulk group (empty when it stores
+                // nothing), so allowing kEpiBufs - 1 groups in flight means the
+                // store that last used this buffer has finished reading it.
+                if (lane == 0) ptx::bulk_wait_group_read<Cf::kEpiBufs - 1>();
+                __syncwarp();
                 if (has_c) {
-                    ok = wait_bounded(c_bar(ew, buf), (chunk_iter >> 1) & 1u, abort_flag, p, kSiteEpilogueC, t);
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(c_bar(ew, buf), kEpiBufBytes);
+                        ptx::tma_load_2d(sbuf, &tmC, col0, row0, c_bar(ew, buf));
+                    }
+                    ok = wait_bounded(c_bar(ew, buf), (chunk_iter / Cf::kEpiBufs) & 1u, abort_flag, p,
+                                      kSiteEpilogueC, t);
                     ok = __all_sync(0xffffffffu, ok);
-                    if (!ok) break;
+                    if (!ok) {
+                        stop = true;
+                        return;
+                    }
                 }
                 const uint32_t row_addr = sbuf + (uint32_t)lane * 128u;
 #pragma unroll
@@ -446,11 +474,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                 __syncwarp();
                 const bool tma_part = col0 < p.n_tma;
                 if (lane == 0) {
-                    if (tma_part) {
-                        ptx::tma_store_2d_hint(&tmD, sbuf, col0, row0, pol_d);
-                        ptx::bulk_commit_group();
-                    }
-                    prev_stored = tma_part;
+                    if (tma_part) ptx::tma_store_2d_hint(&tmD, sbuf, col0, row0, pol_d);
+                    ptx::bulk_commit_group();
                 }
                 // columns [n_tma, N) of this row, one element at a time
                 if (col0 + kChunkCols > p.n_tma && row0 + lane < p.M) {
@@ -468,7 +493,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
                     }
                 }
                 if (pace) __nanosleep((unsigned)p.epi_pace_ns);
+                ++chunk_iter;
+            };
+            static_assert(kChunks % 2 == 0, "chunks are taken in pairs");
+            tmem_load(0, va);
+#pragma unroll
+            for (int c = 0; c < kChunks; c += 2) {
+                chunk(c, va, vb);
+                chunk(c + 1, vb, va);
             }
+            __syncwarp();
+            ptx::tmem_wait_ld();   // a prefetch cut short by `stop` must land before the release
             if (!ok) break;
             // every TMEM read of this accumulator has completed (wait::ld)
             ptx::tc_fence_before_sync();
@@ -537,37 +572,50 @@ int noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 // ---------------------------------------------------------------------------
 // host-side launch helpers (called from gemm_api.cpp)
 
-template <bool kPair, int kOut>
+template <bool kPair, int kOut, int kEpiW>
 static cudaError_t prepare_one() {
-    return cudaFuncSetAttribute(gemm_tcgen05_kernel<kPair, kOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg<kPair>::kSmemBytes);
+    return cudaFuncSetAttribute(gemm_tcgen05_kernel<kPair, kOut, kEpiW>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kPair, kEpiW>::kSmemBytes);
+}
+
+template <bool kPair, int kEpiW>
+static cudaError_t prepare_outs() {
+    cudaError_t e;
+    if ((e = prepare_one<kPair, kOutF32, kEpiW>()) != cudaSuccess) return e;
+    if ((e = prepare_one<kPair, kOutF16, kEpiW>()) != cudaSuccess) return e;
+    return prepare_one<kPair, kOutBF16, kEpiW>();
 }
 
 cudaError_t prepare_kernels_on_current_device() {
     cudaError_t e;
-    if ((e = prepare_one<false, kOutF32>()) != cudaSuccess) return e;
-    if ((e = prepare_one<false, kOutF16>()) != cudaSuccess) return e;
-    if ((e = prepare_one<false, kOutBF16>()) != cudaSuccess) return e;
-    if ((e = prepare_one<true, kOutF32>()) != cudaSuccess) return e;
-    if ((e = prepare_one<true, kOutF16>()) != cudaSuccess) return e;
-    if ((e = prepare_one<true, kOutBF16>()) != cudaSuccess) return e;
-    return cudaSuccess;
+    if ((e = prepare_outs<false, 4>()) != cudaSuccess) return e;
+    if ((e = prepare_outs<false, 8>()) != cudaSuccess) return e;
+    if ((e = prepare_outs<true, 4>()) != cudaSuccess) return e;
+    return prepare_outs<true, 8>();
 }
 
-int tcgen05_tile_m(int pair) { return pair ? Cfg<true>::kTileM : Cfg<false>::kTileM; }
+int tcgen05_tile_m(int pair) { return pair ? Cfg<true, 4>::kTileM : Cfg<false, 4>::kTileM; }
 int tcgen05_tile_n() { return kBN; }
 int tcgen05_block_k() { return kBK; }
-int tcgen05_stage_k(int pair) { return kBK * (pair ? Cfg<true>::kSub : Cfg<false>::kSub); }
-int tcgen05_load_rows_b(int pair) { return pair ? Cfg<true>::kLoadN : Cfg<false>::kLoadN; }
+int tcgen05_stage_k(int pair) { return kBK * (pair ? Cfg<true, 4>::kSub : Cfg<false, 4>::kSub); }
+int tcgen05_load_rows_b(int pair) { return pair ? Cfg<true, 4>::kLoadN : Cfg<false, 4>::kLoadN; }
 int tcgen05_load_rows_a() { return kBM; }
-int tcgen05_smem_bytes(int pair) { return pair ? Cfg<true>::kSmemBytes : Cfg<false>::kSmemBytes; }
+int tcgen05_smem_bytes(int pair, int epi_warps) {
+    if (pair) return epi_warps == 8 ? Cfg<true, 8>::kSmemBytes : Cfg<true, 4>::kSmemBytes;
+    return epi_warps == 8 ? Cfg<false, 8>::kSmemBytes : Cfg<false, 4>::kSmemBytes;
+}
+int tcgen05_stages(int pair, int epi_warps) {
+    if (pair) return epi_warps == 8 ? Cfg<true, 8>::kStages : Cfg<true, 4>::kStages;
+    return epi_warps == 8 ? Cfg<false, 8>::kStages : Cfg<false, 4>::kStages;
+}
 
-template <bool kPair, int kOut>
+template <bool kPair, int kOut, int kEpiW>
 static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
+    using Cf = Cfg<kPair, kEpiW>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.grid, 1, 1);
-    cfg.blockDim = dim3(kNumThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<kPair>::kSmemBytes;
+    cfg.blockDim = dim3(Cf::kNumThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cf::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     if (kPair) {
@@ -578,18 +626,19 @@ static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut>, L.a, L.b, L.c, L.d, L.p);
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW>, L.a, L.b, L.c, L.d, L.p);
+}
+
+template <bool kPair, int kEpiW>
+static cudaError_t launch_out(const TcgenLaunch& L, cudaStream_t stream) {
+    if (L.out == kOutF32) return launch_one<kPair, kOutF32, kEpiW>(L, stream);
+    if (L.out == kOutF16) return launch_one<kPair, kOutF16, kEpiW>(L, stream);
+    return launch_one<kPair, kOutBF16, kEpiW>(L, stream);
 }
 
 cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream) {
-    if (L.pair) {
-        if (L.out == kOutF32) return launch_one<true, kOutF32>(L, stream);
-        if (L.out == kOutF16) return launch_one<true, kOutF16>(L, stream);
-        return launch_one<true, kOutBF16>(L, stream);
-    }
-    if (L.out == kOutF32) return launch_one<false, kOutF32>(L, stream);
-    if (L.out == kOutF16) return launch_one<false, kOutF16>(L, stream);
-    return launch_one<false, kOutBF16>(L, stream);
+    if (L.pair) return L.epi_warps == 8 ? launch_out<true, 8>(L, stream) : launch_out<true, 4>(L, stream);
+    return L.epi_warps == 8 ? launch_out<false, 8>(L, stream) : launch_out<false, 4>(L, stream);
 }
 
 cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,

@@ -125,9 +125,10 @@ GEMM_API int gemm_tile_coords(int tile, int num_m, int num_n, int group_m, int* 
 
 /*
  * Host-only query (no GPU needed): the kernel configuration gemm() would
- * choose for these sizes on a GPU with num_sms SMs.  out[0..5] receive:
+ * choose for these sizes on a GPU with num_sms SMs.  out[0..7] receive:
  * cta_pair (1 = 2-SM tiles), tile_m, tile_n, number of tiles, grid size
- * (CTAs), dynamic shared memory bytes.  Returns GEMM_OK or an error code.
+ * (CTAs), dynamic shared memory bytes, epilogue warps, operand pipeline
+ * stages.  Returns GEMM_OK or an error code.
  */
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out);
 
