@@ -53,6 +53,8 @@ def load_library():
             lib.gemm_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64)]
             lib.gemm_noalloc.restype = i32
             lib.gemm_noalloc.argtypes = list(lib.gemm.argtypes)
+            lib.gemm_schedule_units.restype = i32
+            lib.gemm_schedule_units.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(i32), i32]
             _lib = lib
     return _lib
 
@@ -120,12 +122,24 @@ def gemm_tile_coords(tile, num_m, num_n, group_m):
 
 
 def gemm_plan(M, N, K, num_sms):
-    out = (ctypes.c_int64 * 8)()
+    out = (ctypes.c_int64 * 10)()
     rc = load_library().gemm_plan(int(M), int(N), int(K), int(num_sms), out)
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_plan")
-    keys = ("cta_pair", "tile_m", "tile_n", "num_tiles", "grid", "smem_bytes", "epi_warps", "stages")
+    keys = ("cta_pair", "tile_m", "tile_n", "num_tiles", "grid", "smem_bytes", "epi_warps", "stages",
+            "sk_tiles", "workspace_bytes")
     return dict(zip(keys, list(out)))
+
+
+def gemm_schedule_units(num_tiles, iters, workers, sk_tiles, worker):
+    """The work units of one worker: list of (tile, kb, ke, sk, ci, nc)."""
+    lib = load_library()
+    n = lib.gemm_schedule_units(int(num_tiles), int(iters), int(workers), int(sk_tiles), int(worker), None, 0)
+    if n < 0:
+        raise GemmError(n, "gemm_schedule_units")
+    buf = (ctypes.c_int * (6 * max(n, 1)))()
+    lib.gemm_schedule_units(int(num_tiles), int(iters), int(workers), int(sk_tiles), int(worker), buf, n)
+    return [tuple(buf[6 * i:6 * i + 6]) for i in range(n)]
 
 
 _DT = {}

@@ -12,7 +12,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include "../../include/gemm_gb300.h"
 #include "gemm_internal.h"
@@ -212,18 +214,47 @@ struct Plan {
     int smem;
     int epi_warps;
     int stages;
+    int iters;         // pipeline stages per tile
+    int sk_tiles;      // trailing tiles split along K (stream-K), 0 = data-parallel
+    int max_nc;        // most contributors any stream-K tile has
+    int64_t ws_bytes;  // workspace the stream-K fixup needs
 };
 
+// Stream-K policy: GEMM_STREAMK=0 never, 1 whenever the tiles do not fill
+// whole waves; the default does the same.  A stream-K range shorter than
+// GEMM_SK_MIN_ITERS stages (default 4) is not worth a partial: for small
+// problems fewer clusters are used instead.
+int streamk_setting() {
+    const char* v = std::getenv("GEMM_STREAMK");
+    return (v && std::strcmp(v, "0") == 0) ? 0 : 1;
+}
+
+// Measured on GB300: splitting pays only when each worker's stream-K share is
+// long (8192^3: ~30 stages per worker, +1.3 %); short shares (4096^3: ~12)
+// and memory-bound shapes lose more to the partial-tile traffic than they gain.
+int sk_min_iters_setting() {
+    const char* v = std::getenv("GEMM_SK_MIN_ITERS");
+    if (v && *v) {
+        const int n = std::atoi(v);
+        if (n >= 1 && n <= 1 << 20) return n;
+    }
+    return 24;
+}
+
+constexpr int64_t kPartialBytes = 128 * 256 * 4;   // one CTA's 128 x 256 fp32 accumulator
+
 // Epilogue warps: 8 when a tile's main loop is short (few K stages), so the
-// time goes into storing D; 4 otherwise.  GEMM_EPI_WARPS=4|8 overrides.
-int epi_warps_for(int64_t K, int pair) {
+// time goes into storing D; 4 otherwise.  The 8-warp kernels exist for f32
+// output only.  GEMM_EPI_WARPS=4|8 overrides (f32 output).
+int epi_warps_for(int64_t K, int pair, int out_dtype) {
+    if (out_dtype != GEMM_F32) return 4;
     const char* v = std::getenv("GEMM_EPI_WARPS");
     if (v && (std::strcmp(v, "4") == 0 || std::strcmp(v, "8") == 0)) return std::atoi(v);
     const int64_t stage_k = gb300::tcgen05_stage_k(pair);
     return (K + stage_k - 1) / stage_k <= 4 ? 8 : 4;
 }
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms) {
+Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk, int out_dtype) {
     Plan pl{};
     int ov = variant_override();
     pl.pair = ov >= 0 ? ov : (M > gb300::tcgen05_tile_m(0) ? 1 : 0);
@@ -232,14 +263,84 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms) {
     pl.num_m = (int)((M + pl.tile_m - 1) / pl.tile_m);
     pl.num_n = (int)((N + pl.tile_n - 1) / pl.tile_n);
     pl.num_tiles = pl.num_m * pl.num_n;
+    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair);
+    pl.iters = (int)((K + stage_k - 1) / stage_k);
     const int units = pl.pair ? num_sms / 2 : num_sms;   // clusters that fit at once
     int clusters = pl.num_tiles < units ? pl.num_tiles : units;
     if (clusters < 1) clusters = 1;
+    // Stream-K when the whole tiles leave the last wave partly empty.
+    if (allow_streamk && streamk_setting() && pl.iters > 0 && pl.num_tiles % units != 0) {
+        const int min_iters = sk_min_iters_setting();
+        if (pl.num_tiles > units) {
+            const int rem = pl.num_tiles % units;
+            if ((int64_t)rem * pl.iters / units >= min_iters) {
+                clusters = units;
+                pl.sk_tiles = rem;
+            }
+        } else {
+            const int64_t total = (int64_t)pl.num_tiles * pl.iters;
+            const int64_t workers = std::min<int64_t>(units, total / min_iters);
+            if (workers > pl.num_tiles) {
+                clusters = (int)workers;
+                pl.sk_tiles = pl.num_tiles;
+            }
+        }
+    }
     pl.grid = pl.pair ? 2 * clusters : clusters;
-    pl.epi_warps = epi_warps_for(K, pl.pair);
+    if (pl.sk_tiles > 0) {
+        const gb300::Schedule s{pl.num_tiles, pl.iters, clusters, pl.sk_tiles};
+        for (int t = 0; t < pl.sk_tiles; ++t) {
+            const int nc = s.worker_of((int64_t)(t + 1) * pl.iters - 1) - s.worker_of((int64_t)t * pl.iters) + 1;
+            pl.max_nc = std::max(pl.max_nc, nc);
+        }
+        const int64_t counters = ((int64_t)pl.sk_tiles * 2 * 4 + 255) / 256 * 256;
+        pl.ws_bytes = counters + (int64_t)pl.sk_tiles * pl.max_nc * 2 * kPartialBytes;
+    }
+    pl.epi_warps = epi_warps_for(K, pl.pair, out_dtype);
     pl.smem = gb300::tcgen05_smem_bytes(pl.pair, pl.epi_warps);
     pl.stages = gb300::tcgen05_stages(pl.pair, pl.epi_warps);
     return pl;
+}
+
+// Stream-K workspace, one per (device, stream): calls on one stream run in
+// order, so they can share it; calls on different streams get different
+// ones.  Grown on demand (freeing the old one synchronises the device) and
+// kept until the process exits.  `epoch` numbers the launches that use it.
+struct Workspace {
+    int dev;
+    cudaStream_t stream;
+    void* base;
+    int64_t bytes;
+    uint32_t epoch;
+};
+std::vector<Workspace> g_workspaces;
+
+int workspace_for(int dev, cudaStream_t s, int64_t bytes, void** base, uint32_t* epoch) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    Workspace* w = nullptr;
+    for (auto& x : g_workspaces)
+        if (x.dev == dev && x.stream == s) w = &x;
+    if (!w) {
+        g_workspaces.push_back(Workspace{dev, s, nullptr, 0, 0});
+        w = &g_workspaces.back();
+    }
+    if (w->bytes < bytes) {
+        if (w->base && cudaFree(w->base) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        w->base = nullptr;
+        w->bytes = 0;
+        if (cudaMalloc(&w->base, (size_t)bytes) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        w->bytes = bytes;
+    }
+    w->epoch = (w->epoch + 1) & 0xFFFFFFu;
+    *base = w->base;
+    *epoch = w->epoch;
+    return GEMM_OK;
 }
 
 }  // namespace
@@ -269,10 +370,34 @@ int gemm_tile_coords(int tile, int num_m, int num_n, int group_m, int* m_blk, in
     return GEMM_OK;
 }
 
+int gemm_schedule_units(int num_tiles, int iters, int workers, int sk_tiles, int worker, int* out, int max_units) {
+    if (num_tiles < 1 || iters < 1 || workers < 1 || sk_tiles < 0 || sk_tiles > num_tiles || worker < 0 ||
+        worker >= workers || max_units < 0 || (max_units > 0 && !out))
+        return GEMM_ERR_INVALID_ARG;
+    const gb300::Schedule s{num_tiles, iters, workers, sk_tiles};
+    gb300::UnitIter it;
+    it.start(s, worker);
+    gb300::WorkUnit u;
+    int n = 0;
+    while (it.next(s, worker, &u)) {
+        if (n < max_units) {
+            int* r = out + 6 * n;
+            r[0] = u.tile;
+            r[1] = u.kb;
+            r[2] = u.ke;
+            r[3] = u.sk;
+            r[4] = u.ci;
+            r[5] = u.nc;
+        }
+        ++n;
+    }
+    return n;
+}
+
 int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out) {
     if (M < 1 || N < 1 || K < 0 || num_sms < 2 || !out) return GEMM_ERR_INVALID_ARG;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_TOO_LARGE;
-    Plan pl = make_plan(M, N, K, num_sms);
+    Plan pl = make_plan(M, N, K, num_sms, true, GEMM_F32);
     out[0] = pl.pair;
     out[1] = pl.tile_m;
     out[2] = pl.tile_n;
@@ -281,6 +406,8 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out) {
     out[5] = pl.smem;
     out[6] = pl.epi_warps;
     out[7] = pl.stages;
+    out[8] = pl.sk_tiles;
+    out[9] = pl.ws_bytes;
     return GEMM_OK;
 }
 
@@ -359,7 +486,7 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     }
 
     if ((rc = get_encoder()) != GEMM_OK) return reject(rc, "cuTensorMapEncodeTiled unavailable");
-    const Plan pl = make_plan(M, N, K, ds->num_sms);
+    const Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype);
     TcgenLaunch L;
     std::memset(&L, 0, sizeof(L));
     const uint32_t bk = (uint32_t)gb300::tcgen05_block_k();
@@ -385,7 +512,6 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
         return reject(rc, "tensor map D");
     if (has_c && (rc = encode_2d(&L.c, out_dtype, C, N, M, ldc, chunk_cols, 32)) != GEMM_OK)
         return reject(rc, "tensor map C");
-
     GemmParams& p = L.p;
     p.M = (int32_t)M;
     p.N = (int32_t)N;
@@ -408,6 +534,17 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     p.ldd = ldd;
     tuning(p);
     p.status = ds->d_status;
+    if (pl.sk_tiles > 0) {
+        void* ws = nullptr;
+        uint32_t epoch = 0;
+        if ((rc = workspace_for(dev, s, pl.ws_bytes, &ws, &epoch)) != GEMM_OK)
+            return reject(rc, "stream-K workspace");
+        p.sk_tiles = pl.sk_tiles;
+        p.ws_max_nc = pl.max_nc;
+        p.ws_epoch = epoch;
+        p.ws_counters = static_cast<uint32_t*>(ws);
+        p.ws_partials = static_cast<char*>(ws) + ((int64_t)pl.sk_tiles * 2 * 4 + 255) / 256 * 256;
+    }
     // tcgen05 instruction descriptor, kind::f16: D format f32 (bits 4-5 = 1),
     // A / B format (bits 7-9, 10-12: 0 = f16, 1 = bf16), A / B major
     // (bits 15, 16: 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
@@ -421,10 +558,10 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     L.epi_warps = pl.epi_warps;
 
     GEMM_LOGF("M=%lld N=%lld K=%lld trans=%d%d in=%d out=%d beta%s0: %s tiles %dx%d (%d), grid %d, smem %d, "
-              "%d epilogue warps, %d stages",
+              "%d epilogue warps, %d stages, %d stream-K tiles (<= %d contributors)",
               (long long)M, (long long)N, (long long)K, transA, transB, in_dtype, out_dtype, has_c ? "!=" : "==",
               pl.pair ? "cta-pair" : "1-cta", pl.tile_m, pl.tile_n, pl.num_tiles, pl.grid, pl.smem, pl.epi_warps,
-              pl.stages);
+              pl.stages, pl.sk_tiles, pl.max_nc);
     cudaError_t e = gb300::launch_tcgen05(L, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -600,7 +737,7 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
         return GEMM_OK;
     }
     if ((rc = get_encoder()) != GEMM_OK) return reject(rc, "cuTensorMapEncodeTiled unavailable");
-    const Plan pl = make_plan(M, N, K, ns->num_sms);
+    const Plan pl = make_plan(M, N, K, ns->num_sms, false, out_dtype);   // no workspace: data-parallel
     TcgenLaunch L;
     std::memset(&L, 0, sizeof(L));
     const uint32_t bk = (uint32_t)gb300::tcgen05_block_k();
@@ -621,7 +758,6 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
         return reject(rc, "tensor map D");
     if (has_c && (rc = encode_2d(&L.c, out_dtype, C, N, M, ldc, chunk_cols, 32)) != GEMM_OK)
         return reject(rc, "tensor map C");
-
     GemmParams& p = L.p;
     p.M = (int32_t)M;
     p.N = (int32_t)N;

@@ -26,6 +26,7 @@ enum WaitSite : int {
     kSiteMmaFull = 4,
     kSiteEpilogueTmemFull = 5,
     kSiteEpilogueC = 6,
+    kSiteStreamK = 7,   // the stream-K arrival counter could not be updated
 };
 
 struct GemmParams {
@@ -56,6 +57,93 @@ struct GemmParams {
     // tile: spreads the D writes of all SMs over the next tile's main loop
     // instead of a simultaneous burst that stalls the operand loads.
     int32_t epi_pace_ns;
+    // Stream-K (see Schedule): the trailing sk_tiles tiles are split along K.
+    int32_t sk_tiles;
+    int32_t ws_max_nc;        // partial slots per stream-K tile
+    uint32_t ws_epoch;        // tags this launch's arrivals on the counters (24 bits used)
+    int32_t pad2;
+    uint32_t* ws_counters;    // [sk_tiles][2 CTA ranks] arrival counters
+    void* ws_partials;        // [sk_tiles][ws_max_nc][2 ranks] x 128x256 fp32 partials
+};
+
+// ---------------------------------------------------------------------------
+// Work schedule (host and device).  A tile's K loop has `iters` pipeline
+// stages.  The first `num_tiles - sk_tiles` tiles (in raster order) are
+// whole units, dealt round-robin to the `workers` persistent clusters; the
+// last `sk_tiles` tiles ("stream-K" tiles) are cut along K so that every
+// worker gets the same number of stages: worker w owns the positions
+// [bound(w), bound(w+1)) of the sk_tiles * iters stream-K stages.  A tile
+// cut between several workers is finished by whichever of them arrives last
+// (it adds the others' partial accumulators), so no worker ever waits for
+// another.
+
+struct WorkUnit {
+    int tile;   // tile index in raster order
+    int kb;     // first pipeline stage of the unit
+    int ke;     // one past its last stage
+    int sk;     // index among the stream-K tiles, or -1 for a whole tile
+    int ci;     // this worker's contributor index for the tile (0 = lowest K)
+    int nc;     // number of contributors (1: no partials to combine)
+};
+
+struct Schedule {
+    int num_tiles;
+    int iters;      // pipeline stages per tile
+    int workers;    // persistent clusters
+    int sk_tiles;   // trailing tiles split along K (0: plain data-parallel)
+
+    GB300_HD int dp_tiles() const { return num_tiles - sk_tiles; }
+    GB300_HD int64_t sk_total() const { return (int64_t)sk_tiles * iters; }
+    GB300_HD int64_t bound(int w) const { return sk_total() * w / workers; }
+    // The worker whose stream-K range holds position pos (0 <= pos < sk_total).
+    GB300_HD int worker_of(int64_t pos) const {
+        int w = (int)(pos * workers / sk_total());
+        while (w + 1 < workers && bound(w + 1) <= pos) ++w;
+        while (w > 0 && bound(w) > pos) --w;
+        return w;
+    }
+};
+
+// Iterates the units of one worker: its stream-K segments first, then its
+// whole tiles.
+struct UnitIter {
+    int64_t pos, end;   // remaining stream-K positions
+    int dp_next;        // next whole tile
+
+    GB300_HD void start(const Schedule& s, int w) {
+        pos = s.sk_tiles ? s.bound(w) : 0;
+        end = s.sk_tiles ? s.bound(w + 1) : 0;
+        dp_next = w;
+    }
+    GB300_HD bool next(const Schedule& s, int w, WorkUnit* u) {
+        if (pos < end) {
+            const int t = (int)(pos / s.iters);
+            const int64_t t0 = (int64_t)t * s.iters;
+            const int64_t t1 = t0 + s.iters;
+            const int64_t stop = end < t1 ? end : t1;
+            const int first = s.worker_of(t0);
+            const int last = s.worker_of(t1 - 1);
+            u->tile = s.dp_tiles() + t;
+            u->kb = (int)(pos - t0);
+            u->ke = (int)(stop - t0);
+            u->sk = t;
+            u->ci = w - first;
+            u->nc = last - first + 1;
+            pos = stop;
+            return true;
+        }
+        if (dp_next < s.dp_tiles()) {
+            u->tile = dp_next;
+            u->kb = 0;
+            u->ke = s.iters;
+            u->sk = -1;
+            u->ci = 0;
+            u->nc = 1;
+            dp_next += s.workers;
+            return true;
+        }
+        return false;
+    }
 };
 
 // Persistent-tile order with L2-friendly grouping: tiles run down a group of

@@ -85,7 +85,8 @@ struct Cfg {
     static constexpr int kNumBars = 2 * kStages + 4 + kEpiBufs * kEpiW;
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
-    static constexpr int kSmemBytes = kOffAbort + 4 + 1024;   // + base alignment slack
+    static constexpr int kOffSkFlag = kOffAbort + 4;    // "this CTA finishes the stream-K tile"
+    static constexpr int kSmemBytes = kOffSkFlag + 4 + 1024;   // + base alignment slack
     static_assert(kStages >= 2, "at least two operand stages");
     static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
 };
@@ -136,6 +137,37 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
             }
         }
     }
+}
+
+// Barrier among the epilogue warps only (named barrier 1; barrier 0 is
+// __syncthreads).
+template <int kEpiW>
+__device__ __forceinline__ void epi_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kEpiW * 32) : "memory");
+}
+
+// Counts one contributor into a stream-K tile and tells whether it is the
+// last of `nc`.  The counter word holds (launch epoch << 8) | count, so a
+// word left behind by an earlier or interrupted launch restarts at 1 instead
+// of being trusted.  The retry loop is bounded (each failure means another
+// contributor succeeded); if it runs out the CTA aborts.
+__device__ __noinline__ bool arrive_is_last(uint32_t* counter, uint32_t epoch, int nc, volatile int* abort,
+                                            const GemmParams& p, int detail) {
+    const uint32_t tag = epoch & 0xFFFFFFu;
+    uint32_t old = atomicAdd(counter, 0u);
+    for (int tries = 0; tries < (1 << 20); ++tries) {
+        const uint32_t count = ((old >> 8) == tag ? (old & 0xFFu) : 0u) + 1u;
+        const uint32_t prev = atomicCAS(counter, old, (tag << 8) | count);
+        if (prev == old) {
+            if (count != (uint32_t)nc) return false;
+            atomicExch(counter, 0u);   // every contributor is in: the word is free again
+            return true;
+        }
+        old = prev;
+    }
+    *abort = 1;
+    report_timeout(p, kSiteStreamK, detail);
+    return false;
 }
 
 // Stage one operand tile of `rows` (M or N) x kBK (K).
@@ -190,7 +222,7 @@ __device__ __forceinline__ float2 unpack2(uint32_t u, int out) {
     return __bfloat1622float2(h);
 }
 
-template <bool kPair, int kOut, int kEpiW>
+template <bool kPair, int kOut, int kEpiW, bool kHasC>
 __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
@@ -219,6 +251,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * Cf::kStages + 2 + a); };
     auto c_bar = [&](int w, int b) { return bars + 8u * (2 * Cf::kStages + 4 + Cf::kEpiBufs * w + b); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cf::kOffAbort);
+    volatile int* sk_flag = reinterpret_cast<volatile int*>(smem + Cf::kOffSkFlag);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Cf::kOffTmemSlot);
 
     if (threadIdx.x == 0) {
@@ -237,7 +270,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
         ptx::prefetch_tensormap(&tmD);
-        if (p.has_c) ptx::prefetch_tensormap(&tmC);
+        if constexpr (kHasC) ptx::prefetch_tensormap(&tmC);
     }
     if (warp == 1) {
         ptx::tmem_alloc<kCG>(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
@@ -253,6 +286,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
 
     const int cluster_id = kPair ? blockIdx.x / 2 : blockIdx.x;
     const int num_clusters = kPair ? gridDim.x / 2 : gridDim.x;
+    const Schedule sched{p.num_tiles, p.num_k_blocks, num_clusters, p.sk_tiles};
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -263,17 +297,22 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
             const uint32_t stage_tx = (kPair ? 2 : 1) * Cf::kStageBytes;
             const uint64_t pol_a = ptx::l2_policy(p.hint_a);
             const uint64_t pol_b = ptx::l2_policy(p.hint_b);
-            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+            UnitIter units;
+            units.start(sched, cluster_id);
+            WorkUnit u;
+            bool first_unit = true;
+            while (ok && units.next(sched, cluster_id, &u)) {
+                const int t = u.tile;
                 int mb, nb;
                 tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, &mb, &nb);
                 const int a_row0 = mb * Cf::kTileM + (int)rank * kBM;
                 const int b_row0 = nb * kBN + (int)rank * Cf::kLoadN;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = u.kb; kb < u.ke; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p, kSiteProducerEmpty, t)) {
                         ok = false;
                         break;
                     }
-                    const bool skip = p.skip_first_stage && t == cluster_id && kb == 0;
+                    const bool skip = p.skip_first_stage && first_unit && kb == u.kb;
                     if (!skip) {
                         const uint32_t fb = kPair ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
                         if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), stage_tx);
@@ -291,6 +330,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
                         phase ^= 1u;
                     }
                 }
+                first_unit = false;
             }
             // Drain: wait until the MMA has released every stage, so that no
             // completion signal is still on its way to this CTA at exit.
@@ -320,13 +360,17 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++it) {
+            UnitIter units;
+            units.start(sched, cluster_id);
+            WorkUnit u;
+            for (; ok && units.next(sched, cluster_id, &u); ++it) {
+                const int t = u.tile;
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p, kSiteMmaTmemEmpty, t)) break;
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = u.kb; kb < u.ke; ++kb) {
                     if (!wait_bounded(full_bar(stage), phase, abort_flag, p, kSiteMmaFull, t)) {
                         ok = false;
                         break;
@@ -341,7 +385,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < kBK / kUK; ++kk)
                             ptx::mma_f16<kCG>(d_tmem, as + kk * a_kstep, bs + kk * b_kstep, idesc,
-                                              (kb | sub | kk) != 0);
+                                              ((kb - u.kb) | sub | kk) != 0);
                     }
                     if constexpr (kPair)
                         ptx::mma_commit_pair(empty_bar(stage), 0x3);
@@ -368,13 +412,16 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
         const uint32_t epi = base + Cf::kOffEpi + ew * Cf::kEpiBufs * kEpiBufBytes;
         const float alpha = p.alpha;
         const float beta = p.beta;
-        const bool has_c = p.has_c != 0;
         constexpr int kVec = 16 / kOutBytes;   // elements per 16-byte piece
         const uint64_t pol_d = ptx::l2_policy(p.hint_d);
         uint32_t chunk_iter = 0;
         int it = 0;
         bool ok = true;
-        for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters, ++it) {
+        UnitIter units;
+        units.start(sched, cluster_id);
+        WorkUnit u;
+        for (; ok && units.next(sched, cluster_id, &u); ++it) {
+            const int t = u.tile;
             int mb, nb;
             tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, &mb, &nb);
             const int acc = it & 1;
@@ -385,7 +432,100 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
             ptx::tc_fence_after_sync();
             const int row0 = mb * Cf::kTileM + (int)rank * kBM + q * 32;
             const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN + col_begin);
-            const bool pace = p.epi_pace_ns > 0 && t + num_clusters < p.num_tiles;
+            bool more = false;
+            if (p.epi_pace_ns > 0) {
+                UnitIter peek = units;
+                WorkUnit nu;
+                more = peek.next(sched, cluster_id, &nu);
+            }
+            const bool pace = more;
+
+            // Stream-K: a unit that covers only part of its tile's K range
+            // stores its partial accumulator, then counts itself in; only the
+            // last contributor to arrive goes on to finish the tile (adding
+            // every contributor's partial in contributor order, so the result
+            // does not depend on who arrives last).
+            const bool partial = u.nc > 1;
+            const float4* ws = static_cast<const float4*>(p.ws_partials);
+            auto partial_at = [&](int contributor, int unit32, int j) -> int64_t {
+                const int64_t slot = (int64_t)u.sk * p.ws_max_nc + contributor;
+                return (slot * 2 + rank) * (kBM * kBN / 4) + ((q * (kBN / 32) + unit32) * 8 + j) * 32 + lane;
+            };
+            if (partial) {
+                __syncwarp();
+#pragma unroll 1
+                for (int g = 0; g < Cf::kEpiCols / 32; ++g) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(g * 32), r);
+                    ptx::tmem_wait_ld(r);
+                    float4* dst = static_cast<float4*>(p.ws_partials);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        __stcg(&dst[partial_at(u.ci, col_begin / 32 + g, j)],
+                               make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                           __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+                }
+                __threadfence();
+                epi_bar_sync<kEpiWarps>();
+                if (ew == 0 && lane == 0)
+                    *sk_flag = arrive_is_last(p.ws_counters + (u.sk * 2 + rank), p.ws_epoch, u.nc, abort_flag, p, t)
+                                   ? 1
+                                   : 0;
+                epi_bar_sync<kEpiWarps>();
+                const bool last = *sk_flag != 0;
+                if (!last) {
+                    ptx::tc_fence_before_sync();
+                    if constexpr (kPair)
+                        ptx::mbar_arrive_cluster(ptx::map_to_rank(tempty_bar(acc), 0));
+                    else
+                        ptx::mbar_arrive(tempty_bar(acc));
+                    continue;
+                }
+                __threadfence();
+                // Last to arrive: replace this CTA's accumulator in TMEM by the
+                // sum of every contributor's partial, in contributor order (its
+                // own term read back from TMEM), then finish the tile as usual.
+                __syncwarp();   // the tcgen05 loads / stores below are .sync.aligned
+#pragma unroll 1
+                for (int g = 0; g < Cf::kEpiCols / 32; ++g) {
+                    uint32_t r[32];
+                    ptx::tmem_ld_32x32b_x32(t_row + (uint32_t)(g * 32), r);
+                    ptx::tmem_wait_ld(r);
+                    const int unit32 = col_begin / 32 + g;
+                    float4 s[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) s[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int k = 0; k < u.nc; ++k) {
+                        float4 x[8];
+                        if (k == u.ci) {
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                x[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                   __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                        } else {
+                            // the eight loads are independent: all in flight together
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) x[j] = __ldcg(&ws[partial_at(k, unit32, j)]);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            s[j].x += x[j].x;
+                            s[j].y += x[j].y;
+                            s[j].z += x[j].z;
+                            s[j].w += x[j].w;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        r[4 * j] = __float_as_uint(s[j].x);
+                        r[4 * j + 1] = __float_as_uint(s[j].y);
+                        r[4 * j + 2] = __float_as_uint(s[j].z);
+                        r[4 * j + 3] = __float_as_uint(s[j].w);
+                    }
+                    ptx::tmem_st_32x32b_x32(t_row + (uint32_t)(g * 32), r);
+                }
+                ptx::tmem_wait_st();
+            }
             // Accumulator chunks come out of TMEM one ahead of their use: the
             // load of chunk c+1 is in flight while chunk c is converted and
             // staged.  Two named register arrays alternate (chunks are taken
@@ -420,7 +560,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
                 // store that last used this buffer has finished reading it.
                 if (lane == 0) ptx::bulk_wait_group_read<Cf::kEpiBufs - 1>();
                 __syncwarp();
-                if (has_c) {
+                if constexpr (kHasC) {   // this chunk of C, by TMA, into the staging box
                     if (lane == 0) {
                         ptx::mbar_arrive_expect_tx(c_bar(ew, buf), kEpiBufBytes);
                         ptx::tma_load_2d(sbuf, &tmC, col0, row0, c_bar(ew, buf));
@@ -442,12 +582,12 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
                         float o[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) o[e] = alpha * __uint_as_float(v[4 * j + e]);
-                        if (has_c) {
-                            uint32_t cv[4];
-                            ptx::ld_shared_v4(addr, cv[0], cv[1], cv[2], cv[3]);
+                        if constexpr (kHasC) {
+                            uint32_t c4[4];
+                            ptx::ld_shared_v4(addr, c4[0], c4[1], c4[2], c4[3]);
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                o[e] = fmaf(alpha, __uint_as_float(v[4 * j + e]), beta * __uint_as_float(cv[e]));
+                                o[e] = fmaf(alpha, __uint_as_float(v[4 * j + e]), beta * __uint_as_float(c4[e]));
                         }
 #pragma unroll
                         for (int e = 0; e < 4; ++e) w[e] = __float_as_uint(o[e]);
@@ -455,12 +595,12 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
                         float o[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) o[e] = alpha * __uint_as_float(v[8 * j + e]);
-                        if (has_c) {
-                            uint32_t cv[4];
-                            ptx::ld_shared_v4(addr, cv[0], cv[1], cv[2], cv[3]);
+                        if constexpr (kHasC) {
+                            uint32_t c4[4];
+                            ptx::ld_shared_v4(addr, c4[0], c4[1], c4[2], c4[3]);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
-                                const float2 cf = unpack2(cv[e], kOut);
+                                const float2 cf = unpack2(c4[e], kOut);
                                 o[2 * e] = fmaf(alpha, __uint_as_float(v[8 * j + 2 * e]), beta * cf.x);
                                 o[2 * e + 1] = fmaf(alpha, __uint_as_float(v[8 * j + 2 * e + 1]), beta * cf.y);
                             }
@@ -496,6 +636,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
                 ++chunk_iter;
             };
             static_assert(kChunks % 2 == 0, "chunks are taken in pairs");
+            __syncwarp();
             tmem_load(0, va);
 #pragma unroll
             for (int c = 0; c < kChunks; c += 2) {
@@ -572,26 +713,30 @@ int noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 // ---------------------------------------------------------------------------
 // host-side launch helpers (called from gemm_api.cpp)
 
-template <bool kPair, int kOut, int kEpiW>
+// Instantiated configurations: every (pair, beta != 0) combination with 4
+// epilogue warps for each output type, and with 8 epilogue warps for f32
+// output (the store-bound configuration).
+template <bool kPair, int kOut, int kEpiW, bool kHasC>
 static cudaError_t prepare_one() {
-    return cudaFuncSetAttribute(gemm_tcgen05_kernel<kPair, kOut, kEpiW>,
+    return cudaFuncSetAttribute(gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kPair, kEpiW>::kSmemBytes);
 }
 
-template <bool kPair, int kEpiW>
-static cudaError_t prepare_outs() {
+template <bool kPair, bool kHasC>
+static cudaError_t prepare_group() {
     cudaError_t e;
-    if ((e = prepare_one<kPair, kOutF32, kEpiW>()) != cudaSuccess) return e;
-    if ((e = prepare_one<kPair, kOutF16, kEpiW>()) != cudaSuccess) return e;
-    return prepare_one<kPair, kOutBF16, kEpiW>();
+    if ((e = prepare_one<kPair, kOutF32, 4, kHasC>()) != cudaSuccess) return e;
+    if ((e = prepare_one<kPair, kOutF32, 8, kHasC>()) != cudaSuccess) return e;
+    if ((e = prepare_one<kPair, kOutF16, 4, kHasC>()) != cudaSuccess) return e;
+    return prepare_one<kPair, kOutBF16, 4, kHasC>();
 }
 
 cudaError_t prepare_kernels_on_current_device() {
     cudaError_t e;
-    if ((e = prepare_outs<false, 4>()) != cudaSuccess) return e;
-    if ((e = prepare_outs<false, 8>()) != cudaSuccess) return e;
-    if ((e = prepare_outs<true, 4>()) != cudaSuccess) return e;
-    return prepare_outs<true, 8>();
+    if ((e = prepare_group<false, false>()) != cudaSuccess) return e;
+    if ((e = prepare_group<false, true>()) != cudaSuccess) return e;
+    if ((e = prepare_group<true, false>()) != cudaSuccess) return e;
+    return prepare_group<true, true>();
 }
 
 int tcgen05_tile_m(int pair) { return pair ? Cfg<true, 4>::kTileM : Cfg<false, 4>::kTileM; }
@@ -609,7 +754,7 @@ int tcgen05_stages(int pair, int epi_warps) {
     return epi_warps == 8 ? Cfg<false, 8>::kStages : Cfg<false, 4>::kStages;
 }
 
-template <bool kPair, int kOut, int kEpiW>
+template <bool kPair, int kOut, int kEpiW, bool kHasC>
 static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
     using Cf = Cfg<kPair, kEpiW>;
     cudaLaunchConfig_t cfg = {};
@@ -626,19 +771,22 @@ static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW>, L.a, L.b, L.c, L.d, L.p);
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC>, L.a, L.b, L.c, L.d, L.p);
 }
 
-template <bool kPair, int kEpiW>
-static cudaError_t launch_out(const TcgenLaunch& L, cudaStream_t stream) {
-    if (L.out == kOutF32) return launch_one<kPair, kOutF32, kEpiW>(L, stream);
-    if (L.out == kOutF16) return launch_one<kPair, kOutF16, kEpiW>(L, stream);
-    return launch_one<kPair, kOutBF16, kEpiW>(L, stream);
+template <bool kPair, bool kHasC>
+static cudaError_t launch_group(const TcgenLaunch& L, cudaStream_t stream) {
+    if (L.out == kOutF32)
+        return L.epi_warps == 8 ? launch_one<kPair, kOutF32, 8, kHasC>(L, stream)
+                                : launch_one<kPair, kOutF32, 4, kHasC>(L, stream);
+    if (L.out == kOutF16) return launch_one<kPair, kOutF16, 4, kHasC>(L, stream);
+    return launch_one<kPair, kOutBF16, 4, kHasC>(L, stream);
 }
 
 cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream) {
-    if (L.pair) return L.epi_warps == 8 ? launch_out<true, 8>(L, stream) : launch_out<true, 4>(L, stream);
-    return L.epi_warps == 8 ? launch_out<false, 8>(L, stream) : launch_out<false, 4>(L, stream);
+    const bool has_c = L.p.has_c != 0;
+    if (L.pair) return has_c ? launch_group<true, true>(L, stream) : launch_group<true, false>(L, stream);
+    return has_c ? launch_group<false, true>(L, stream) : launch_group<false, false>(L, stream);
 }
 
 cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,

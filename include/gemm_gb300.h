@@ -125,12 +125,27 @@ GEMM_API int gemm_tile_coords(int tile, int num_m, int num_n, int group_m, int* 
 
 /*
  * Host-only query (no GPU needed): the kernel configuration gemm() would
- * choose for these sizes on a GPU with num_sms SMs.  out[0..7] receive:
+ * choose for these sizes on a GPU with num_sms SMs.  out[0..9] receive:
  * cta_pair (1 = 2-SM tiles), tile_m, tile_n, number of tiles, grid size
  * (CTAs), dynamic shared memory bytes, epilogue warps, operand pipeline
- * stages.  Returns GEMM_OK or an error code.
+ * stages, stream-K tiles (trailing tiles split along K; 0 = every tile
+ * whole), and the bytes of the per-stream workspace the stream-K tiles
+ * need.  Returns GEMM_OK or an error code.
  */
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out);
+
+/*
+ * Host-only query (no GPU needed): the work of one persistent worker
+ * (cluster) under the kernel's schedule.  num_tiles tiles of `iters`
+ * pipeline stages each; the last sk_tiles tiles are split along K evenly
+ * across the `workers` workers; the others are dealt whole, round-robin.
+ * Writes up to max_units records of 6 ints (tile, first stage, end stage,
+ * stream-K tile index or -1, contributor index, number of contributors) to
+ * `out` and returns the number of units of this worker (possibly more than
+ * max_units), or GEMM_ERR_INVALID_ARG.
+ */
+GEMM_API int gemm_schedule_units(int num_tiles, int iters, int workers, int sk_tiles, int worker, int* out,
+                                 int max_units);
 
 /*
  * gemm_noalloc -- gemm() for callers that cannot allocate device memory.

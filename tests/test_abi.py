@@ -154,9 +154,81 @@ def test_plan(lib, M, N, K):
     assert p["tile_m"] * ((M + p["tile_m"] - 1) // p["tile_m"]) >= M
     assert p["num_tiles"] == ((M + p["tile_m"] - 1) // p["tile_m"]) * ((N + p["tile_n"] - 1) // p["tile_n"])
     assert p["grid"] <= sms
+    units = sms // 2 if p["cta_pair"] else sms
+    workers = p["grid"] // 2 if p["cta_pair"] else p["grid"]
     if p["cta_pair"]:
         assert p["grid"] % 2 == 0 and p["tile_m"] == 256
-        assert p["grid"] == 2 * min(p["num_tiles"], sms // 2)
+    if p["sk_tiles"] == 0:
+        assert workers == min(p["num_tiles"], units)
     else:
-        assert p["grid"] == min(p["num_tiles"], sms)
+        assert workers <= units and p["workspace_bytes"] > 0
     assert p["smem_bytes"] <= 232448
+
+
+SCHEDULES = [
+    # (num_tiles, iters, workers, sk_tiles)
+    (1024, 64, 76, 36),      # 8192^3 on 76 clusters: 13 whole rounds + 36 split tiles
+    (256, 32, 76, 28),       # 4096^3
+    (128, 32, 76, 52),       # 32768 x 256 x 4096
+    (16, 8, 32, 16),         # 1000^3: every tile split, 2 contributors each
+    (16, 8, 76, 16),         # more workers than stages per tile: empty ranges
+    (4, 4, 8, 4),
+    (7, 3, 5, 2),
+    (10, 1, 4, 10),
+    (300, 17, 76, 0),        # data-parallel only
+    (1, 1, 1, 1),
+]
+
+
+@pytest.mark.parametrize("num_tiles,iters,workers,sk_tiles", SCHEDULES)
+def test_schedule_covers_every_stage_once(lib, num_tiles, iters, workers, sk_tiles):
+    """Every (tile, stage) is done by exactly one worker; a split tile's
+    contributors are numbered 0..nc-1 in K order with one agreed nc."""
+    seen = {}
+    per_worker = []
+    contrib = {}
+    for w in range(workers):
+        units = binding.gemm_schedule_units(num_tiles, iters, workers, sk_tiles, w)
+        total = 0
+        for (tile, kb, ke, sk, ci, nc) in units:
+            assert 0 <= tile < num_tiles and 0 <= kb < ke <= iters
+            assert (sk >= 0) == (tile >= num_tiles - sk_tiles)
+            if sk >= 0:
+                assert tile == num_tiles - sk_tiles + sk
+            if nc == 1:
+                assert (kb, ke, ci) == (0, iters, 0)
+            for k in range(kb, ke):
+                assert (tile, k) not in seen
+                seen[(tile, k)] = w
+            contrib.setdefault(tile, []).append((kb, ci, nc, w))
+            total += ke - kb
+        per_worker.append(total)
+    assert len(seen) == num_tiles * iters
+    for tile, lst in contrib.items():
+        lst.sort()
+        ncs = {c[2] for c in lst}
+        assert ncs == {len(lst)}, (tile, lst)
+        assert [c[1] for c in lst] == list(range(len(lst)))          # K order = contributor order
+        assert [c[3] for c in lst] == sorted(c[3] for c in lst)      # consecutive workers
+    if sk_tiles:
+        # stream-K balances the work: every worker within one tile's stages of the mean
+        assert max(per_worker) - min(per_worker) <= iters + 1
+
+
+def test_plan_streamk_choices(lib):
+    p = binding.gemm_plan(8192, 8192, 8192, 152)
+    assert p["sk_tiles"] == 1024 % 76 and p["grid"] == 152 and p["workspace_bytes"] > 0
+    p = binding.gemm_plan(8192, 8192, 256, 152)          # 2 stages per tile: too short to split
+    assert p["sk_tiles"] == 0 and p["workspace_bytes"] == 0
+    p = binding.gemm_plan(1000, 1000, 1000, 152)         # shares too short to split: whole tiles
+    assert p["sk_tiles"] == 0 and p["grid"] == 32
+    p = binding.gemm_plan(4096, 4096, 4096, 152)         # ~12 stages per worker: not split
+    assert p["sk_tiles"] == 0
+    p = binding.gemm_plan(8192, 8192, 16384, 152)        # ~60 stages per worker
+    assert p["sk_tiles"] == 1024 % 76
+
+
+def test_schedule_rejects_bad_arguments(lib):
+    for args in [(0, 1, 1, 0, 0), (4, 0, 1, 0, 0), (4, 4, 2, 5, 0), (4, 4, 2, 1, 2)]:
+        with pytest.raises(binding.GemmError):
+            binding.gemm_schedule_units(*args)
