@@ -243,6 +243,56 @@ int sk_min_iters_setting() {
 
 constexpr int64_t kPartialBytes = 128 * 256 * 4;   // one CTA's 128 x 256 fp32 accumulator
 
+// TMA (the tcgen05 kernel) needs 16-byte-aligned bases and row strides.
+bool tma_layout_ok(const void* D, const void* A, const void* B, const void* C, int64_t K, int64_t lda, int64_t ldb,
+                   int64_t ldc, int64_t ldd, int osz, bool has_c) {
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    bool ok = a16(D) && ((ldd * osz) & 15) == 0;
+    if (has_c) ok = ok && a16(C) && ((ldc * osz) & 15) == 0;
+    if (K > 0) ok = ok && a16(A) && a16(B) && (((lda * 2) | (ldb * 2)) & 15) == 0;
+    return ok;
+}
+
+// Which kernel: the warp-level mma.sync kernel when TMA cannot describe the
+// layout, or when the problem is so small that the tcgen05 kernel's set-up
+// dominates (M*N*K <= GEMM_SYNC_MAX_WORK, default 2^15 = 32^3);
+// GEMM_PATH=tcgen05|mma_sync forces one (tcgen05 only where TMA can).
+bool use_mma_sync(bool tma_ok, int64_t M, int64_t N, int64_t K) {
+    if (!tma_ok) return true;
+    const char* v = std::getenv("GEMM_PATH");
+    if (v && std::strcmp(v, "mma_sync") == 0) return true;
+    if (v && std::strcmp(v, "tcgen05") == 0) return false;
+    int64_t limit = 1 << 15;
+    const char* w = std::getenv("GEMM_SYNC_MAX_WORK");
+    if (w && *w) limit = std::strtoll(w, nullptr, 10);
+    return M * N * K <= limit;
+}
+
+cudaError_t launch_sync(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                        int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float alpha,
+                        float beta, int in_dtype, int out_kind, bool has_c, cudaStream_t s) {
+    gb300::SyncParams sp;
+    sp.A = A;
+    sp.B = B;
+    sp.C = has_c ? C : nullptr;
+    sp.D = D;
+    sp.M = M;
+    sp.N = N;
+    sp.K = K;
+    sp.lda = lda;
+    sp.ldb = ldb;
+    sp.ldc = has_c ? ldc : 0;
+    sp.ldd = ldd;
+    sp.transA = transA;
+    sp.transB = transB;
+    sp.alpha = alpha;
+    sp.beta = beta;
+    sp.in_bf16 = in_dtype == GEMM_BF16 ? 1 : 0;
+    sp.out = out_kind;
+    sp.has_c = has_c ? 1 : 0;
+    return gb300::launch_mma_sync(sp, s);
+}
+
 // Epilogue warps: 8 when a tile's main loop is short (few K stages), so the
 // time goes into storing D; 4 otherwise.  The 8-warp kernels exist for f32
 // output only.  GEMM_EPI_WARPS=4|8 overrides (f32 output).
@@ -436,18 +486,14 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
         if (lda < (transA ? M : K)) return reject(GEMM_ERR_INVALID_ARG, "lda too small");
         if (ldb < (transB ? K : N)) return reject(GEMM_ERR_INVALID_ARG, "ldb too small");
         if (lda * 2 >= kMaxStrideBytes || ldb * 2 >= kMaxStrideBytes) return reject(GEMM_ERR_TOO_LARGE, "stride");
-        if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u)
-            return reject(GEMM_ERR_MISALIGNED, "A or B not 16-byte aligned");
-        if (((lda * 2) | (ldb * 2)) & 15) return reject(GEMM_ERR_MISALIGNED, "lda*2 or ldb*2 not a multiple of 16");
+        if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u)
+            return reject(GEMM_ERR_MISALIGNED, "A or B not 2-byte aligned");
     }
     if (ldd * osz >= kMaxStrideBytes || (has_c && ldc * osz >= kMaxStrideBytes))
         return reject(GEMM_ERR_TOO_LARGE, "stride");
-    if (reinterpret_cast<uintptr_t>(D) & 15u) return reject(GEMM_ERR_MISALIGNED, "D not 16-byte aligned");
-    if ((ldd * osz) & 15) return reject(GEMM_ERR_MISALIGNED, "ldd*sizeof(out) not a multiple of 16");
-    if (has_c) {
-        if (reinterpret_cast<uintptr_t>(C) & 15u) return reject(GEMM_ERR_MISALIGNED, "C not 16-byte aligned");
-        if ((ldc * osz) & 15) return reject(GEMM_ERR_MISALIGNED, "ldc*sizeof(out) not a multiple of 16");
-    }
+    if (reinterpret_cast<uintptr_t>(D) & (uintptr_t)(osz - 1)) return reject(GEMM_ERR_MISALIGNED, "D not element-aligned");
+    if (has_c && (reinterpret_cast<uintptr_t>(C) & (uintptr_t)(osz - 1)))
+        return reject(GEMM_ERR_MISALIGNED, "C not element-aligned");
     {
         uintptr_t d0, d1;
         byte_range(D, M, N, ldd, osz, &d0, &d1);
@@ -482,6 +528,18 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
         cudaError_t e = gb300::launch_k0(out_kind, D, has_c ? C : nullptr, (int)M, (int)N, ldc, ldd, alpha, beta,
                                          has_c ? 1 : 0, ds->num_sms, s);
         if (e != cudaSuccess) return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+        return GEMM_OK;
+    }
+    const bool tma_ok = tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, osz, has_c);
+    if (use_mma_sync(tma_ok, M, N, K)) {
+        GEMM_LOGF("M=%lld N=%lld K=%lld trans=%d%d: mma.sync kernel (%s)", (long long)M, (long long)N, (long long)K,
+                  transA, transB, tma_ok ? "small problem" : "layout not 16-byte aligned");
+        cudaError_t e = launch_sync(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype,
+                                    out_kind, has_c, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+        }
         return GEMM_OK;
     }
 
@@ -678,18 +736,14 @@ int noalloc_validate(const void* D, const void* A, const void* B, const void* C,
         if (lda < (transA ? M : K)) return reject(GEMM_ERR_INVALID_ARG, "lda too small");
         if (ldb < (transB ? K : N)) return reject(GEMM_ERR_INVALID_ARG, "ldb too small");
         if (lda * 2 >= kMaxStrideBytes || ldb * 2 >= kMaxStrideBytes) return reject(GEMM_ERR_TOO_LARGE, "stride");
-        if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 15u)
-            return reject(GEMM_ERR_MISALIGNED, "A or B not 16-byte aligned");
-        if (((lda * 2) | (ldb * 2)) & 15) return reject(GEMM_ERR_MISALIGNED, "lda*2 or ldb*2 not a multiple of 16");
+        if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u)
+            return reject(GEMM_ERR_MISALIGNED, "A or B not 2-byte aligned");
     }
     if (ldd * osz >= kMaxStrideBytes || (has_c && ldc * osz >= kMaxStrideBytes))
         return reject(GEMM_ERR_TOO_LARGE, "stride");
-    if (reinterpret_cast<uintptr_t>(D) & 15u) return reject(GEMM_ERR_MISALIGNED, "D not 16-byte aligned");
-    if ((ldd * osz) & 15) return reject(GEMM_ERR_MISALIGNED, "ldd*sizeof(out) not a multiple of 16");
-    if (has_c) {
-        if (reinterpret_cast<uintptr_t>(C) & 15u) return reject(GEMM_ERR_MISALIGNED, "C not 16-byte aligned");
-        if ((ldc * osz) & 15) return reject(GEMM_ERR_MISALIGNED, "ldc*sizeof(out) not a multiple of 16");
-    }
+    if (reinterpret_cast<uintptr_t>(D) & (uintptr_t)(osz - 1)) return reject(GEMM_ERR_MISALIGNED, "D not element-aligned");
+    if (has_c && (reinterpret_cast<uintptr_t>(C) & (uintptr_t)(osz - 1)))
+        return reject(GEMM_ERR_MISALIGNED, "C not element-aligned");
     uintptr_t d0, d1;
     byte_range(D, M, N, ldd, osz, &d0, &d1);
     if (K > 0) {
@@ -734,6 +788,16 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
         cudaError_t e = gb300::launch_k0(ok, D, has_c ? C : nullptr, (int)M, (int)N, ldc, ldd, alpha, beta,
                                          has_c ? 1 : 0, ns->num_sms, s);
         if (e != cudaSuccess) return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+        return GEMM_OK;
+    }
+    if (use_mma_sync(tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, osz, has_c), M, N, K)) {   // no scratch
+        const int ok = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
+        cudaError_t e = launch_sync(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype, ok,
+                                    has_c, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+        }
         return GEMM_OK;
     }
     if ((rc = get_encoder()) != GEMM_OK) return reject(rc, "cuTensorMapEncodeTiled unavailable");

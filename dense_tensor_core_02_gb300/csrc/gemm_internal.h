@@ -25,6 +25,23 @@ struct TcgenLaunch {
     int epi_warps;            // 4 or 8 epilogue warps
 };
 
+// Arguments of the warp-level mma.sync path (gemm_mma_sync.cu): any
+// element-aligned layout; K > 0.
+struct SyncParams {
+    const void* A;
+    const void* B;
+    const void* C;
+    void* D;
+    int64_t M, N, K, lda, ldb, ldc, ldd;
+    int transA, transB;
+    float alpha, beta;
+    int in_bf16;   // A and B are bf16 (else f16)
+    int out;       // OutKind of C and D
+    int has_c;     // beta != 0
+};
+
+cudaError_t launch_mma_sync(const SyncParams& p, cudaStream_t stream);
+
 cudaError_t prepare_kernels_on_current_device();
 cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream);
 cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,

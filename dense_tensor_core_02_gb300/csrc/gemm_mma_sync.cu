@@ -1,0 +1,229 @@
+// Warp-level tensor-core path: mma.sync.aligned.m16n8k16 with register
+// fragments, the lowering the TVM TIRx "gemm" page describes (sections
+// "Demonstration program", "Algorithm" and "Generated CUDA"), used for the
+// cases the TMA / tcgen05 kernel cannot take or does not pay off for:
+//
+//  * operands or outputs whose addresses or row strides are not 16-byte
+//    multiples (TMA cannot describe them; this path loads element by
+//    element, so any element-aligned layout works);
+//  * tiny problems, where the tcgen05 kernel's set-up (tensor memory,
+//    barriers, TMA descriptors) costs more than the arithmetic.
+//
+// Fragment layout of one m16n8k16 atom, lane = 4 g + t (g = lane / 4,
+// t = lane % 4), exactly as the demonstration program stages it:
+//   A (16 x 16): slot s = 4 kHi + 2 rM + kp holds A[g + 8 rM][2 t + kp + 8 kHi]
+//                (the slot order of the TIRx gemm guide, section 三; the
+//                 operand registers a0..a3 pack slot pairs (kp = 0, 1))
+//   B (16 x 8):  slot s = 2 kHi + kp holds B[2 t + kp + 8 kHi][g]
+//   D (16 x 8):  slot s = 2 rM + rN holds D[g + 8 rM][2 t + rN]
+// D is initialised to 0 and accumulated over K in place (TIRx "Algorithm",
+// step 3); alpha and beta are applied in the epilogue like the tcgen05 path.
+// K is covered by k16 atoms; a remainder of at most 8 takes one m16n8k8
+// atom, as the lowering does for K = 8 (mod 16).  Staged columns past K are
+// zero, so the last k16 atom of a ragged K adds nothing for them.
+//
+// CTA tile 64 x 64, 4 warps in a 2 x 2 grid of 32 x 32 warp tiles
+// (2 x 4 atoms each), K slabs of 32 staged in shared memory with padded rows.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gemm_internal.h"
+
+namespace gb300 {
+
+namespace {
+
+constexpr int kSBM = 64, kSBN = 64, kSBK = 32;
+constexpr int kSThreads = 128;
+constexpr int kPad = 8;   // halves of padding per shared row (conflict-free fragment loads)
+
+template <int kIn>
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    if constexpr (kIn == 0)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+            "{%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// m16n8k8: the atom for a K remainder of 8 (the lowering's k8 shape).  Its
+// A fragment is the kHi = 0 half of the k16 one (slots rM = 0, 1), its B
+// fragment the kHi = 0 register.
+template <int kIn>
+__device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    if constexpr (kIn == 0)
+        asm volatile(
+            "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(b0));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, {%0, %1, %2, %3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(a1), "r"(b0));
+}
+
+__device__ __forceinline__ uint32_t pack_halves(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
+
+template <int kOut>
+__device__ __forceinline__ float load_out(const void* p, int64_t i) {
+    if constexpr (kOut == kOutF32) return static_cast<const float*>(p)[i];
+    if constexpr (kOut == kOutF16) return __half2float(static_cast<const __half*>(p)[i]);
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(p)[i]);
+}
+
+template <int kOut>
+__device__ __forceinline__ void store_out(void* p, int64_t i, float v) {
+    if constexpr (kOut == kOutF32)
+        static_cast<float*>(p)[i] = v;
+    else if constexpr (kOut == kOutF16)
+        static_cast<__half*>(p)[i] = __float2half_rn(v);
+    else
+        static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
+}
+
+// One 64 x 64 tile of D at (m0, n0).
+template <int kIn, int kOut, bool kHasC>
+__device__ __forceinline__ void sync_tile(const SyncParams& p, int64_t m0, int64_t n0, uint16_t (*As)[kSBK + kPad],
+                                          uint16_t (*Bs)[kSBK + kPad]) {
+    const int tid = threadIdx.x;
+    const int lane = tid % 32;
+    const int warp = tid / 32;
+    const int g = lane / 4, tq = lane % 4;
+    const int wm = (warp / 2) * 32, wn = (warp % 2) * 32;   // warp tile origin in the CTA tile
+    const uint16_t* A = static_cast<const uint16_t*>(p.A);
+    const uint16_t* B = static_cast<const uint16_t*>(p.B);
+
+    float acc[2][4][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) acc[i][j][s] = 0.0f;
+
+    for (int64_t k0 = 0; k0 < p.K; k0 += kSBK) {
+        // stage A[m0.., k0..] and B[k0.., n0..] (out of range -> 0)
+        // consecutive threads walk the operand's contiguous dimension
+        for (int e = tid; e < kSBM * kSBK; e += kSThreads) {
+            const int r = p.transA ? e % kSBM : e / kSBK;
+            const int c = p.transA ? e / kSBM : e % kSBK;
+            const int64_t m = m0 + r, k = k0 + c;
+            uint16_t v = 0;
+            if (m < p.M && k < p.K) v = p.transA ? A[k * p.lda + m] : A[m * p.lda + k];
+            As[r][c] = v;
+        }
+        for (int e = tid; e < kSBN * kSBK; e += kSThreads) {
+            const int r = p.transB ? e / kSBK : e % kSBN;
+            const int c = p.transB ? e % kSBK : e / kSBN;
+            const int64_t n = n0 + r, k = k0 + c;
+            uint16_t v = 0;
+            if (n < p.N && k < p.K) v = p.transB ? B[n * p.ldb + k] : B[k * p.ldb + n];
+            Bs[r][c] = v;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int ks = 0; ks < kSBK; ks += 16) {
+            const int64_t k_left = p.K - (k0 + ks);   // same for the whole CTA
+            if (k_left <= 0) break;
+            uint32_t af[2][4], bf[4][2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int r = wm + 16 * i + g;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {   // w = 2 kHi + rM: slots 2w, 2w + 1 (kp = 0, 1)
+                    const int rM = w % 2, kHi = w / 2;
+                    const int c = ks + 2 * tq + 8 * kHi;
+                    af[i][w] = pack_halves(As[r + 8 * rM][c], As[r + 8 * rM][c + 1]);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r = wn + 8 * j + g;
+#pragma unroll
+                for (int kHi = 0; kHi < 2; ++kHi) {   // slots 2 kHi, 2 kHi + 1
+                    const int c = ks + 2 * tq + 8 * kHi;
+                    bf[j][kHi] = pack_halves(Bs[r][c], Bs[r][c + 1]);
+                }
+            }
+            if (k_left > 8) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_16816<kIn>(acc[i][j], af[i], bf[j]);
+            } else {   // at most 8 columns of K left: one k8 atom
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) mma_1688<kIn>(acc[i][j], af[i][0], af[i][1], bf[j][0]);
+            }
+        }
+        __syncthreads();
+    }
+
+    // epilogue: D = alpha * acc (+ beta * C), element by element with bounds
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int rM = s / 2, rN = s % 2;
+                const int64_t m = m0 + wm + 16 * i + g + 8 * rM;
+                const int64_t n = n0 + wn + 8 * j + 2 * tq + rN;
+                if (m < p.M && n < p.N) {
+                    float d;
+                    if constexpr (kHasC)
+                        d = fmaf(p.alpha, acc[i][j][s], p.beta * load_out<kOut>(p.C, m * p.ldc + n));
+                    else
+                        d = p.alpha * acc[i][j][s];
+                    store_out<kOut>(p.D, m * p.ldd + n, d);
+                }
+            }
+}
+
+template <int kIn, int kOut, bool kHasC>
+__global__ void __launch_bounds__(kSThreads) gemm_mma_sync_kernel(SyncParams p) {
+    // As[m][k] and Bs[n][k]: both K-contiguous, so A and B fragments are read
+    // the same way (pairs of consecutive k).
+    __shared__ uint16_t As[kSBM][kSBK + kPad];
+    __shared__ uint16_t Bs[kSBN][kSBK + kPad];
+    const int64_t num_m_tiles = (p.M + kSBM - 1) / kSBM;
+    // grid.y is capped at 65535: CTAs step through the M tiles by gridDim.y
+    for (int64_t mt = blockIdx.y; mt < num_m_tiles; mt += gridDim.y)
+        sync_tile<kIn, kOut, kHasC>(p, mt * kSBM, (int64_t)blockIdx.x * kSBN, As, Bs);
+}
+
+template <int kIn, int kOut, bool kHasC>
+cudaError_t launch_sync_one(const SyncParams& p, cudaStream_t stream) {
+    const int64_t m_tiles = (p.M + kSBM - 1) / kSBM;
+    const dim3 grid((unsigned)((p.N + kSBN - 1) / kSBN), (unsigned)(m_tiles < 65535 ? m_tiles : 65535));
+    gemm_mma_sync_kernel<kIn, kOut, kHasC><<<grid, kSThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int kIn, bool kHasC>
+cudaError_t launch_sync_out(const SyncParams& p, cudaStream_t stream) {
+    if (p.out == kOutF32) return launch_sync_one<kIn, kOutF32, kHasC>(p, stream);
+    if (p.out == kOutF16) return launch_sync_one<kIn, kOutF16, kHasC>(p, stream);
+    return launch_sync_one<kIn, kOutBF16, kHasC>(p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_mma_sync(const SyncParams& p, cudaStream_t stream) {
+    if (p.in_bf16) return p.has_c ? launch_sync_out<1, true>(p, stream) : launch_sync_out<1, false>(p, stream);
+    return p.has_c ? launch_sync_out<0, true>(p, stream) : launch_sync_out<0, false>(p, stream);
+}
+
+}  // namespace gb300

@@ -66,7 +66,7 @@ typedef enum {
     GEMM_OK = 0,
     GEMM_ERR_INVALID_ARG = -1,       /* negative size, flag not 0/1, ld too small, NULL buffer */
     GEMM_ERR_UNSUPPORTED_DTYPE = -2, /* in_dtype not F16/BF16, or out_dtype not F32/F16/BF16 */
-    GEMM_ERR_MISALIGNED = -3,        /* a buffer not 16-byte aligned, or ld * element size not a multiple of 16 */
+    GEMM_ERR_MISALIGNED = -3,        /* a buffer not aligned to its element size */
     GEMM_ERR_ALIAS = -4,             /* D overlaps A or B, or overlaps C other than C == D with ldc == ldd */
     GEMM_ERR_ARCH = -5,              /* the current device is not an sm_103 (GB300) GPU */
     GEMM_ERR_LAUNCH = -6,            /* the kernel launch was refused */
@@ -91,8 +91,16 @@ typedef enum {
  *   out_dtype        GEMM_F32, GEMM_F16 or GEMM_BF16 (C and D).
  *   stream           CUDA stream of the current device.
  *
- * Alignment: A, B, C, D must be 16-byte aligned and lda*2, ldb*2,
- * ldc*sizeof(out), ldd*sizeof(out) multiples of 16 bytes (TMA's rule).
+ * Alignment: each buffer must be aligned to its element size.  Two kernels
+ * compute the product: the tcgen05 kernel (TMA copies, tensor-memory
+ * accumulators) when A, B, C, D are 16-byte aligned and lda*2, ldb*2,
+ * ldc*sizeof(out), ldd*sizeof(out) are multiples of 16 bytes (TMA's rule),
+ * and a warp-level mma.sync kernel (element-wise loads) for any other
+ * layout and for problems with M*N*K <= 2^15, where the tcgen05 kernel's
+ * set-up outweighs the arithmetic.  Both accumulate in fp32 and give the
+ * same results within the documented tolerance.  GEMM_PATH=tcgen05 or
+ * mma_sync forces one (tcgen05 only where TMA's rule holds);
+ * GEMM_SYNC_MAX_WORK sets the size threshold.
  * Returns GEMM_OK or a GEMM_ERR_* code (see gemm_status_t).
  * Setting the environment variable GEMM_LOG=1 prints each call's plan or
  * rejection reason to stderr.
@@ -158,7 +166,10 @@ GEMM_API int gemm_schedule_units(int num_tiles, int iters, int workers, int sk_t
  * from a stream callback), or code that must not add allocations to a
  * process it does not own.  gemm_noalloc() computes exactly what gemm()
  * computes, with the same arguments, rules and return codes, through the
- * same kernel, but never calls cudaMalloc, cudaFree or any other allocating
+ * same kernels (the tcgen05 kernel without stream-K splitting, whose
+ * partial sums would need a workspace; the mma.sync kernel, which needs no
+ * scratch, for the layouts and sizes gemm() sends there), but never calls
+ * cudaMalloc, cudaFree or any other allocating
  * routine: the kernel's scratch (its 16-byte status record) lives in a
  * fixed 256-byte array inside the library, which every GPU that loads the
  * library holds until the process exits.  The scratch does not grow with

@@ -14,7 +14,10 @@ from tests import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ["pair", "single"]
+# "pair" / "single": the tcgen05 kernel with 2-SM or 1-SM tiles (forced even
+# where the size rule would pick the mma.sync kernel); "mma_sync": the
+# warp-level kernel.
+VARIANTS = ["pair", "single", "mma_sync"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -29,7 +32,17 @@ def _device():
 
 @pytest.fixture(params=VARIANTS)
 def variant(request):
-    with H.env(GEMM_VARIANT=request.param):
+    if request.param == "mma_sync":
+        with H.env(GEMM_PATH="mma_sync", GEMM_VARIANT=None):
+            yield request.param
+    else:
+        with H.env(GEMM_PATH="tcgen05", GEMM_VARIANT=request.param):
+            yield request.param
+
+
+@pytest.fixture(params=["tcgen05", "mma_sync"])
+def path(request):
+    with H.env(GEMM_PATH=request.param):
         yield request.param
 
 
@@ -58,7 +71,7 @@ PAGE_SHAPES = [(16, 8, 16), (32, 8, 16), (16, 16, 16), (16, 8, 32), (64, 8, 16),
 @pytest.mark.parametrize("shape", PAGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("beta", [0.0, 1.0])
-def test_page_matrix_integers_exact(shape, dtype, beta):
+def test_page_matrix_integers_exact(path, shape, dtype, beta):
     M, N, K = shape
     seed = M * 10007 + N * 101 + K + 7 * (dtype == "bf16") + 13 * int(beta)
     A = H.int_matrix((M, K), -8, 8, dtype, seed)
@@ -272,7 +285,7 @@ def test_wait_bound_reports_and_recovers():
     A = H.int_matrix((M, K), -4, 4, "f16", 61)
     B = H.int_matrix((K, N), -4, 4, "f16", 62)
     assert H.poll()[0] == 0
-    with H.env(GEMM_TEST_SKIP_FIRST_STAGE="1", GEMM_WAIT_TIMEOUT_NS="300000000"):
+    with H.env(GEMM_TEST_SKIP_FIRST_STAGE="1", GEMM_WAIT_TIMEOUT_NS="300000000", GEMM_PATH="tcgen05"):
         _, rc = H.run_gemm(A, B, None, M, N, K)
     assert rc == 0
     status, info = H.poll()

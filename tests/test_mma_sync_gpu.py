@@ -1,0 +1,215 @@
+"""GPU parity of the warp-level mma.sync kernel against the CPU oracle.
+
+This kernel takes what TMA cannot describe -- operand or output addresses
+and row strides that are element-aligned but not 16-byte multiples -- and
+tiny problems.  The tests here cover those layouts through the default
+routing (no environment override) and, with GEMM_PATH=mma_sync, the
+workloads the tcgen05 kernel is tested on.  The shared parity cases
+(golden atom, page test matrix, transposes, ragged canaries, in place,
+16-bit outputs, alpha/beta) run on this kernel through the "mma_sync"
+variant of the main GPU test module.
+"""
+import numpy as np
+import pytest
+import torch
+
+from dense_tensor_core_02_gb300 import binding
+from dense_tensor_core_02_gb300.inputs import CASES, make_inputs
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load_library()
+    yield
+    rc, info = H.poll()
+    assert rc == 0, ("device status after the module", rc, info)
+
+
+def _strided(host, offset, ld, dtype, fill=float("nan")):
+    """Copy a CPU matrix [rows, cols] into a device buffer at element
+    `offset` with row stride `ld`; return (flat buffer, view)."""
+    rows, cols = host.shape
+    dev = torch.device("cuda", 0)
+    n = offset + (rows - 1) * ld + cols + 8 if rows else offset + 8
+    buf = torch.full((n,), fill, dtype=H.TORCH[dtype], device=dev)
+    view = buf.as_strided((rows, cols), (ld, 1), offset)
+    view.copy_(host.to(dev))
+    return buf, view
+
+
+def _run(A, B, C, M, N, K, *, offs=(0, 0, 0, 0), lds=None, transA=0, transB=0, alpha=1.0, beta=0.0,
+         in_dtype="f16", out_dtype="f32", fn=None):
+    """Call the C ABI with A, B, C, D placed at element offsets `offs` and
+    row strides `lds` (default: the densest legal stride); return D on the
+    CPU, the whole D buffer (for canary checks), the status and (offset, ldd)."""
+    fn = fn or binding.gemm
+    ra, ca = (K, M) if transA else (M, K)
+    rb, cb = (N, K) if transB else (K, N)
+    lda, ldb, ldc, ldd = lds or (ca, cb, N, N)
+    _, Av = _strided(A, offs[0], lda, in_dtype)
+    _, Bv = _strided(B, offs[1], ldb, in_dtype)
+    Cv = _strided(C, offs[2], ldc, out_dtype)[1] if C is not None else None
+    Dbuf, Dv = _strided(torch.full((M, N), float("nan")), offs[3], ldd, out_dtype)
+    rc = fn(Dv, Av, Bv, Cv, M, N, K, lda, ldb, ldc if C is not None else N, ldd, transA, transB, alpha, beta,
+            H.CODE[in_dtype], H.CODE[out_dtype], None)
+    torch.cuda.synchronize()
+    return Dv.cpu(), Dbuf.cpu(), rc
+
+
+def _check_canaries(Dbuf, M, N, off, ldd):
+    """Everything in the D buffer outside the M x N view is still NaN."""
+    flat = Dbuf.double().numpy()
+    mask = np.ones(flat.shape, dtype=bool)
+    for r in range(M):
+        mask[off + r * ldd: off + r * ldd + N] = False
+    assert np.isnan(flat[mask]).all(), "elements outside D written"
+
+
+# (M, N, K, element offsets of A, B, C, D, strides lda, ldb, ldc, ldd or None)
+ODD_LAYOUTS = [
+    (300, 200, 1001, (0, 0, 0, 0), None),                  # K = 1001: lda = 1001 (2002 bytes)
+    (129, 77, 65, (1, 3, 1, 1), None),                     # every base off the 16-byte grid
+    (64, 64, 64, (0, 0, 0, 0), (65, 67, 66, 69)),          # odd strides, aligned bases
+    (257, 130, 33, (5, 0, 2, 3), (41, 133, 131, 135)),
+    (1, 1, 7, (1, 1, 1, 1), None),
+    (17, 9, 3, (0, 1, 0, 1), None),
+    (520, 392, 264, (2, 0, 0, 0), None),                   # only A off the grid
+]
+
+
+@pytest.mark.parametrize("transA", [0, 1])
+@pytest.mark.parametrize("transB", [0, 1])
+@pytest.mark.parametrize("layout", ODD_LAYOUTS, ids=lambda l: "%dx%dx%d_o%s" % (l[0], l[1], l[2],
+                                                                               "".join(map(str, l[3]))))
+def test_odd_layouts_integers_exact(layout, transA, transB):
+    """Layouts TMA cannot take, through the default routing; integer-valued
+    inputs, so the fp32 result is exact."""
+    M, N, K, offs, lds = layout
+    if lds is not None:
+        ra, ca = (K, M) if transA else (M, K)
+        rb, cb = (N, K) if transB else (K, N)
+        lds = (max(lds[0], ca), max(lds[1], cb), lds[2], lds[3])
+    seed = M * 31 + N * 7 + K + 2 * transA + transB
+    A = H.int_matrix((K, M) if transA else (M, K), -8, 8, "f16", seed)
+    B = H.int_matrix((N, K) if transB else (K, N), -8, 8, "f16", seed + 1)
+    C = H.int_matrix((M, N), -100, 100, "f32", seed + 2)
+    with H.env(GEMM_PATH=None):
+        D, Dbuf, rc = _run(A, B, C, M, N, K, offs=offs, lds=lds, transA=transA, transB=transB, beta=1.0)
+    assert rc == 0
+    ref, _ = H.oracle_full(A, B, C, M, N, K, transA=transA, transB=transB, beta=1.0)
+    H.assert_exact(D.numpy(), ref, "odd layout %s" % (layout,))
+    ldd = lds[3] if lds else N
+    _check_canaries(Dbuf, M, N, offs[3], ldd)
+
+
+@pytest.mark.parametrize("in_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("out_dtype", ["f32", "f16", "bf16"])
+def test_odd_layouts_random(in_dtype, out_dtype):
+    M, N, K = 333, 250, 517
+    seed = 7 + 3 * (in_dtype == "bf16") + ["f32", "f16", "bf16"].index(out_dtype)
+    A = H.normal_matrix((K, M), in_dtype, seed)
+    B = H.normal_matrix((K, N), in_dtype, seed + 1)
+    C = H.normal_matrix((M, N), out_dtype, seed + 2)
+    kw = dict(transA=1, alpha=-1.25, beta=0.5, in_dtype=in_dtype, out_dtype=out_dtype)
+    with H.env(GEMM_PATH=None):
+        D, Dbuf, rc = _run(A, B, C, M, N, K, offs=(1, 1, 1, 1), lds=(M + 1, N + 3, N + 1, N + 5), **kw)
+    assert rc == 0
+    ref, bound = H.oracle_full(A, B, C, M, N, K, **kw)
+    H.assert_close(D.double().numpy(), ref, bound, out_dtype, "odd random %s->%s" % (in_dtype, out_dtype))
+    _check_canaries(Dbuf, M, N, 1, N + 5)
+
+
+def test_in_place_odd_layout():
+    """C == D (same pointer, same stride) off the 16-byte grid."""
+    M, N, K = 130, 90, 77
+    A = H.normal_matrix((M, K), "bf16", 91)
+    B = H.normal_matrix((N, K), "bf16", 92)
+    C = H.normal_matrix((M, N), "f32", 93)
+    dev = torch.device("cuda", 0)
+    _, Av = _strided(A, 1, K, "bf16")
+    _, Bv = _strided(B, 1, K, "bf16")
+    _, CD = _strided(C, 3, N + 1, "f32")
+    rc = binding.gemm(CD, Av, Bv, CD, M, N, K, K, K, N + 1, N + 1, 0, 1, 0.75, -1.5, 1, 2, None)
+    assert rc == 0
+    torch.cuda.synchronize()
+    ref, bound = H.oracle_full(A, B, C, M, N, K, transB=1, alpha=0.75, beta=-1.5, in_dtype="bf16")
+    H.assert_close(CD.cpu().numpy(), ref, bound, what="in place, odd layout")
+
+
+def test_beta_zero_never_reads_c_odd_layout():
+    M, N, K = 40, 24, 9
+    A = H.normal_matrix((M, K), "f16", 94)
+    B = H.normal_matrix((K, N), "f16", 95)
+    C = torch.full((M, N), float("nan"))
+    D, _, rc = _run(A, B, C, M, N, K, offs=(1, 1, 1, 1), beta=0.0)
+    assert rc == 0 and torch.isfinite(D).all()
+    ref, bound = H.oracle_full(A, B, None, M, N, K)
+    H.assert_close(D.numpy(), ref, bound, what="beta 0, NaN C, odd layout")
+
+
+TINY = [(1, 1, 1), (16, 8, 16), (8, 16, 8), (63, 65, 17), (64, 64, 64), (5, 300, 3), (100, 7, 250)]
+
+
+@pytest.mark.parametrize("shape", TINY, ids=lambda s: "x".join(map(str, s)))
+def test_tiny_problems_default_routing(shape):
+    """Tiny problems through the default routing (the smallest take the
+    mma.sync kernel, the rest the tcgen05 kernel): exact on integers."""
+    M, N, K = shape
+    A = H.int_matrix((M, K), -8, 8, "bf16", M + N + K)
+    B = H.int_matrix((N, K), -8, 8, "bf16", M * N + K)
+    with H.env(GEMM_PATH=None, GEMM_SYNC_MAX_WORK=None):
+        D, rc = H.run_gemm(A, B, None, M, N, K, transB=1, in_dtype="bf16", alpha=2.0)
+    assert rc == 0
+    ref, _ = H.oracle_full(A, B, None, M, N, K, transB=1, in_dtype="bf16", alpha=2.0)
+    H.assert_exact(D.numpy(), ref, "tiny %s" % (shape,))
+
+
+SMALL_CASES = [c for c in CASES if c.M * c.N * c.K <= 1024 ** 3]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: c.name)
+def test_workloads_forced_mma_sync(case):
+    """The small workloads, every element, on the mma.sync kernel."""
+    A, B, C = make_inputs(case)
+    kw = dict(transA=case.transA, transB=case.transB, alpha=case.alpha, beta=case.beta,
+              in_dtype=case.in_dtype, out_dtype=case.out_dtype)
+    with H.env(GEMM_PATH="mma_sync"):
+        D, rc = H.run_gemm(A, B, C, case.M, case.N, case.K, **kw)
+    assert rc == 0
+    ref, bound = H.oracle_full(A, B, C, case.M, case.N, case.K, **kw)
+    H.assert_close(D.numpy(), ref, bound, case.out_dtype, case.name)
+
+
+def test_large_odd_stride_sampled():
+    """A large problem whose K (4097) keeps it off TMA: sampled positions in
+    every 128 x 128 block against the oracle."""
+    M, N, K = 2048, 1536, 4097
+    A = H.normal_matrix((M, K), "f16", 101)
+    B = H.normal_matrix((N, K), "f16", 102)
+    with H.env(GEMM_PATH=None):
+        D, rc = H.run_gemm(A, B, None, M, N, K, transB=1)
+    assert rc == 0
+    assert not torch.isnan(D).any()
+    rows, cols = H.sample_positions(M, N, per_block=4, seed=5)
+    ref, bound = H.oracle_at(A, B, None, M, N, K, rows, cols, transB=1)
+    H.assert_close(D.numpy()[rows, cols], ref, bound, what="large odd stride")
+
+
+def test_paths_agree_on_integers():
+    """On integer-valued inputs both kernels are exact, so they agree bit for bit."""
+    M, N, K = 264, 200, 136
+    A = H.int_matrix((M, K), -8, 8, "f16", 111)
+    B = H.int_matrix((K, N), -8, 8, "f16", 112)
+    C = H.int_matrix((M, N), -50, 50, "f32", 113)
+    out = []
+    for path in ("tcgen05", "mma_sync"):
+        with H.env(GEMM_PATH=path):
+            D, rc = H.run_gemm(A, B, C, M, N, K, beta=-1.0)
+        assert rc == 0
+        out.append(D)
+    assert torch.equal(out[0], out[1])

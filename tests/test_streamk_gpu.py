@@ -22,7 +22,7 @@ def _device():
 
 @pytest.fixture(params=["pair", "single"])
 def variant(request):
-    with H.env(GEMM_VARIANT=request.param):
+    with H.env(GEMM_PATH="tcgen05", GEMM_VARIANT=request.param):
         yield request.param
 
 
