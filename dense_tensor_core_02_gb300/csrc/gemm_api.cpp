@@ -85,13 +85,16 @@ int skip_first_stage_setting() {
     return (v && std::strcmp(v, "1") == 0) ? 1 : 0;
 }
 
-// Kernel variant: "pair" (2-SM tiles), "single" or automatic.
+// Kernel variant: "pair" (256 x 256 tiles on 2 SMs), "single" (128 x 256),
+// "narrow" (128 x 64) or automatic.
+enum Variant { kAuto = -1, kSingle = 0, kPairV = 1, kNarrow = 2 };
 int variant_override() {
     const char* v = std::getenv("GEMM_VARIANT");
-    if (!v) return -1;
-    if (std::strcmp(v, "pair") == 0) return 1;
-    if (std::strcmp(v, "single") == 0) return 0;
-    return -1;
+    if (!v) return kAuto;
+    if (std::strcmp(v, "pair") == 0) return kPairV;
+    if (std::strcmp(v, "single") == 0) return kSingle;
+    if (std::strcmp(v, "narrow") == 0) return kNarrow;
+    return kAuto;
 }
 
 int group_m_setting() {
@@ -296,8 +299,8 @@ cudaError_t launch_sync(void* D, const void* A, const void* B, const void* C, in
 // Epilogue warps: 8 when a tile's main loop is short (few K stages), so the
 // time goes into storing D; 4 otherwise.  The 8-warp kernels exist for f32
 // output only.  GEMM_EPI_WARPS=4|8 overrides (f32 output).
-int epi_warps_for(int64_t K, int pair, int out_dtype) {
-    if (out_dtype != GEMM_F32) return 4;
+int epi_warps_for(int64_t K, int pair, int out_dtype, int tile_n) {
+    if (out_dtype != GEMM_F32 || tile_n == gb300::tcgen05_narrow_n()) return 4;
     const char* v = std::getenv("GEMM_EPI_WARPS");
     if (v && (std::strcmp(v, "4") == 0 || std::strcmp(v, "8") == 0)) return std::atoi(v);
     const int64_t stage_k = gb300::tcgen05_stage_k(pair);
@@ -306,10 +309,19 @@ int epi_warps_for(int64_t K, int pair, int out_dtype) {
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk, int out_dtype) {
     Plan pl{};
-    int ov = variant_override();
-    pl.pair = ov >= 0 ? ov : (M > gb300::tcgen05_tile_m(0) ? 1 : 0);
+    const int ov = variant_override();
+    pl.pair = ov == kPairV || (ov == kAuto && M > gb300::tcgen05_tile_m(0)) ? 1 : 0;
     pl.tile_m = gb300::tcgen05_tile_m(pl.pair);
-    pl.tile_n = gb300::tcgen05_tile_n();
+    pl.tile_n = gb300::tcgen05_wide_n();
+    // Narrow 128 x 64 tiles when the wide ones would keep at most a quarter
+    // of the SMs busy (the time then goes into latency and into each CTA's
+    // epilogue, which a narrow tile cuts by four), or when N fits one.
+    const int64_t wide_ctas = ((M + pl.tile_m - 1) / pl.tile_m) * ((N + pl.tile_n - 1) / pl.tile_n) * (pl.pair + 1);
+    if (ov == kNarrow || (ov == kAuto && (wide_ctas * 4 <= num_sms || N <= gb300::tcgen05_narrow_n()))) {
+        pl.pair = 0;
+        pl.tile_m = gb300::tcgen05_tile_m(0);
+        pl.tile_n = gb300::tcgen05_narrow_n();
+    }
     pl.num_m = (int)((M + pl.tile_m - 1) / pl.tile_m);
     pl.num_n = (int)((N + pl.tile_n - 1) / pl.tile_n);
     pl.num_tiles = pl.num_m * pl.num_n;
@@ -346,9 +358,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
         const int64_t counters = ((int64_t)pl.sk_tiles * 2 * 4 + 255) / 256 * 256;
         pl.ws_bytes = counters + (int64_t)pl.sk_tiles * pl.max_nc * 2 * kPartialBytes;
     }
-    pl.epi_warps = epi_warps_for(K, pl.pair, out_dtype);
-    pl.smem = gb300::tcgen05_smem_bytes(pl.pair, pl.epi_warps);
-    pl.stages = gb300::tcgen05_stages(pl.pair, pl.epi_warps);
+    pl.epi_warps = epi_warps_for(K, pl.pair, out_dtype, pl.tile_n);
+    pl.smem = gb300::tcgen05_smem_bytes(pl.pair, pl.epi_warps, pl.tile_n);
+    pl.stages = gb300::tcgen05_stages(pl.pair, pl.epi_warps, pl.tile_n);
     return pl;
 }
 
@@ -556,7 +568,7 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     if (rc != GEMM_OK) return reject(rc, "tensor map A");
     // B: K-major (transB = 1) as [N rows][K], else MN-major as [K rows][N]
     if (transB)
-        rc = encode_2d(&L.b, in_dtype, B, K, N, ldb, bk, (uint32_t)gb300::tcgen05_load_rows_b(pl.pair));
+        rc = encode_2d(&L.b, in_dtype, B, K, N, ldb, bk, (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n));
     else
         rc = encode_2d(&L.b, in_dtype, B, N, K, ldb, 64, bk);
     if (rc != GEMM_OK) return reject(rc, "tensor map B");
@@ -611,6 +623,7 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)p.a_mn_major << 15) |
               ((uint32_t)p.b_mn_major << 16) | (((uint32_t)pl.tile_n >> 3) << 17) | ((mma_m >> 4) << 24);
     L.pair = pl.pair;
+    L.tile_n = pl.tile_n;
     L.out = out_kind;
     L.grid = pl.grid;
     L.epi_warps = pl.epi_warps;
@@ -811,7 +824,7 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
         rc = encode_2d(&L.a, in_dtype, A, M, K, lda, 64, bk);
     if (rc != GEMM_OK) return reject(rc, "tensor map A");
     if (transB)
-        rc = encode_2d(&L.b, in_dtype, B, K, N, ldb, bk, (uint32_t)gb300::tcgen05_load_rows_b(pl.pair));
+        rc = encode_2d(&L.b, in_dtype, B, K, N, ldb, bk, (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n));
     else
         rc = encode_2d(&L.b, in_dtype, B, N, K, ldb, 64, bk);
     if (rc != GEMM_OK) return reject(rc, "tensor map B");
@@ -848,6 +861,7 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
     p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)p.a_mn_major << 15) |
               ((uint32_t)p.b_mn_major << 16) | (((uint32_t)pl.tile_n >> 3) << 17) | (((uint32_t)pl.tile_m >> 4) << 24);
     L.pair = pl.pair;
+    L.tile_n = pl.tile_n;
     L.out = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
     L.grid = pl.grid;
     L.epi_warps = pl.epi_warps;

@@ -23,6 +23,7 @@ struct TcgenLaunch {
     int out;                  // OutKind
     int grid;                 // CTAs (a multiple of 2 for the pair kernel)
     int epi_warps;            // 4 or 8 epilogue warps
+    int tile_n;               // 256, or 64 for the narrow single-CTA tiles
 };
 
 // Arguments of the warp-level mma.sync path (gemm_mma_sync.cu): any
@@ -53,12 +54,13 @@ cudaError_t noalloc_scratch_address(void** ptr);
 int noalloc_scratch_bytes();
 
 int tcgen05_tile_m(int pair);      // D rows per tile
-int tcgen05_tile_n();              // D columns per tile
+int tcgen05_wide_n();              // D columns per throughput tile
+int tcgen05_narrow_n();            // D columns per narrow tile (single CTA, 4 epilogue warps)
 int tcgen05_block_k();             // K of one TMA operand box (one 128-byte swizzle row)
 int tcgen05_stage_k(int pair);     // K per pipeline stage
 int tcgen05_load_rows_a();         // A rows (M) one CTA stages per stage
-int tcgen05_load_rows_b(int pair); // B rows (N) one CTA stages per stage
-int tcgen05_smem_bytes(int pair, int epi_warps);
-int tcgen05_stages(int pair, int epi_warps);
+int tcgen05_load_rows_b(int pair, int tile_n);   // B rows (N) one CTA stages per stage
+int tcgen05_smem_bytes(int pair, int epi_warps, int tile_n);
+int tcgen05_stages(int pair, int epi_warps, int tile_n);
 
 }  // namespace gb300

@@ -40,28 +40,36 @@
 namespace gb300 {
 
 constexpr int kBM = 128;             // accumulator rows per CTA (= TMEM lanes)
-constexpr int kBN = 256;             // accumulator columns per tile
+constexpr int kBNMax = 256;          // accumulator columns of the throughput tiles
+constexpr int kNarrowN = 64;         // accumulator columns of the narrow (small-problem) tiles
 constexpr int kBK = 64;              // K per stage: one 128-byte swizzle row of 16-bit elements
 constexpr int kUK = 16;              // K per tcgen05.mma kind::f16
 constexpr int kEpiBufBytes = 4096;   // one epilogue staging box: 32 rows x 128 bytes
-constexpr int kTmemCols = 512;       // two 128 x 256 fp32 accumulators
+constexpr int kTmemCols = 512;       // two accumulators of up to 128 x 256 fp32
 constexpr int kAtomBytes = 1024;     // 8 rows x 128 bytes: one 128B-swizzle atom
 constexpr int kMnChunkBytes = 64 * kBK * 2;   // one 64-wide MN-major box (64 x 64 x 2 B)
 constexpr int kSmemBudget = 232448;  // dynamic shared memory per CTA on sm_103
 static_assert(kBK / kUK == 4, "the MMA loop issues four K slices per stage");
 
-// kEpiW epilogue warps: 4 (one per TMEM lane quadrant, each storing all 256
-// columns of its 32 rows) for K-heavy shapes, or 8 (two per quadrant, 128
-// columns each) for shapes whose time goes into storing D; the operand ring
-// gets whatever shared memory the staging boxes leave.
-template <bool kPair, int kEpiW>
+// kEpiW epilogue warps: 4 (one per TMEM lane quadrant, each storing all
+// columns of its 32 rows) for K-heavy shapes, or 8 (two per quadrant, half
+// the columns each) for shapes whose time goes into storing D; the operand
+// ring gets whatever shared memory the staging boxes leave.
+// kTileN: 256 (the throughput tiles: 256 x 256 per CTA pair, 128 x 256 per
+// single CTA) or 64 (128 x 64 single-CTA tiles for problems too small to
+// fill the GPU with wide tiles: four times as many CTAs, each with a
+// quarter of the epilogue).
+template <bool kPair, int kEpiW, int kTileN_ = kBNMax>
 struct Cfg {
+    static constexpr int kTileN = kTileN_;                 // D columns per tile
     static constexpr int kCtaGroup = kPair ? 2 : 1;
     static constexpr int kTileM = kPair ? 2 * kBM : kBM;   // D rows per tile
-    static constexpr int kLoadN = kPair ? kBN / 2 : kBN;   // B rows (N) each CTA stages
+    static constexpr int kLoadN = kPair ? kTileN / 2 : kTileN;   // B rows (N) each CTA stages
     static constexpr int kEpiWarps = kEpiW;
     static constexpr int kNumThreads = 64 + 32 * kEpiW;    // producer, MMA, epilogue warps
-    static constexpr int kEpiCols = kBN / (kEpiW / 4);     // accumulator columns per epilogue warp
+    static constexpr int kEpiCols = kTileN / (kEpiW / 4);  // accumulator columns per epilogue warp
+    static_assert(kLoadN % 64 == 0, "MN-major operand boxes are 64 wide");
+    static_assert(kTileN <= kBNMax && kTileN % 64 == 0, "tile width");
     // A pipeline stage holds kSub 64-wide K sub-blocks.  The MMA issuer pays a
     // fixed cost per stage (barrier wait, release commit) while the tensor
     // core queues only a few MMAs, so the pair kernel puts 8 MMAs (2 sub-
@@ -222,12 +230,13 @@ __device__ __forceinline__ float2 unpack2(uint32_t u, int out) {
     return __bfloat1622float2(h);
 }
 
-template <bool kPair, int kOut, int kEpiW, bool kHasC>
-__global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
+template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN>
+__global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN>::kNumThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const GemmParams p) {
-    using Cf = Cfg<kPair, kEpiW>;
+    using Cf = Cfg<kPair, kEpiW, kTileN>;
+    constexpr int kBN = kTileN;
     constexpr int kCG = Cf::kCtaGroup;
     constexpr int kEpiWarps = Cf::kEpiWarps;
     constexpr int kOutBytes = OutTraits<kOut>::kBytes;
@@ -426,11 +435,29 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
             tile_coords(t, p.num_m_tiles, p.num_n_tiles, p.group_m, &mb, &nb);
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
+            const int row0 = mb * Cf::kTileM + (int)rank * kBM + q * 32;
+            // C does not depend on the main loop: for a whole tile, the C
+            // boxes of the first kEpiBufs chunks are fetched before the
+            // accumulator is ready, so their latency hides behind the MMAs.
+            // (A stream-K contributor learns only later whether it stores.)
+            constexpr int kPrefetchC = kHasC ? (Cf::kEpiBufs < kChunks ? Cf::kEpiBufs : kChunks) : 0;
+            const bool prefetch_c = kPrefetchC > 0 && u.nc == 1;
+            if (prefetch_c && lane == 0) {
+                ptx::bulk_wait_group_read<0>();   // every staging box of this warp is free
+#pragma unroll
+                for (int c = 0; c < kPrefetchC; ++c) {
+                    const int col0 = nb * kBN + col_begin + c * kChunkCols;
+                    if (col0 < p.N) {
+                        const uint32_t buf = (chunk_iter + c) % Cf::kEpiBufs;
+                        ptx::mbar_arrive_expect_tx(c_bar(ew, buf), kEpiBufBytes);
+                        ptx::tma_load_2d(epi + buf * kEpiBufBytes, &tmC, col0, row0, c_bar(ew, buf));
+                    }
+                }
+            }
             ok = wait_bounded(tfull_bar(acc), acc_phase, abort_flag, p, kSiteEpilogueTmemFull, t);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after_sync();
-            const int row0 = mb * Cf::kTileM + (int)rank * kBM + q * 32;
             const uint32_t t_row = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kBN + col_begin);
             bool more = false;
             if (p.epi_pace_ns > 0) {
@@ -561,7 +588,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
                 if (lane == 0) ptx::bulk_wait_group_read<Cf::kEpiBufs - 1>();
                 __syncwarp();
                 if constexpr (kHasC) {   // this chunk of C, by TMA, into the staging box
-                    if (lane == 0) {
+                    if (lane == 0 && !(prefetch_c && c < kPrefetchC)) {
                         ptx::mbar_arrive_expect_tx(c_bar(ew, buf), kEpiBufBytes);
                         ptx::tma_load_2d(sbuf, &tmC, col0, row0, c_bar(ew, buf));
                     }
@@ -635,13 +662,13 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW>::kNumThreads, 1)
                 if (pace) __nanosleep((unsigned)p.epi_pace_ns);
                 ++chunk_iter;
             };
-            static_assert(kChunks % 2 == 0, "chunks are taken in pairs");
+            static_assert(kChunks % 2 == 0 || kChunks == 1, "chunks are taken in pairs");
             __syncwarp();
             tmem_load(0, va);
 #pragma unroll
             for (int c = 0; c < kChunks; c += 2) {
                 chunk(c, va, vb);
-                chunk(c + 1, vb, va);
+                if constexpr (kChunks > 1) chunk(c + 1, vb, va);
             }
             __syncwarp();
             ptx::tmem_wait_ld();   // a prefetch cut short by `stop` must land before the release
@@ -713,22 +740,32 @@ int noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 // ---------------------------------------------------------------------------
 // host-side launch helpers (called from gemm_api.cpp)
 
-// Instantiated configurations: every (pair, beta != 0) combination with 4
-// epilogue warps for each output type, and with 8 epilogue warps for f32
-// output (the store-bound configuration).
-template <bool kPair, int kOut, int kEpiW, bool kHasC>
+// Instantiated configurations: every (pair, beta != 0) combination of the
+// 256-wide tiles with 4 epilogue warps for each output type, and with 8
+// epilogue warps for f32 output (the store-bound configuration); the 64-wide
+// single-CTA tiles with 4 epilogue warps for each output type.
+template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN>
 static cudaError_t prepare_one() {
-    return cudaFuncSetAttribute(gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<kPair, kEpiW>::kSmemBytes);
+    return cudaFuncSetAttribute(gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC, kTileN>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg<kPair, kEpiW, kTileN>::kSmemBytes);
 }
 
 template <bool kPair, bool kHasC>
 static cudaError_t prepare_group() {
     cudaError_t e;
-    if ((e = prepare_one<kPair, kOutF32, 4, kHasC>()) != cudaSuccess) return e;
-    if ((e = prepare_one<kPair, kOutF32, 8, kHasC>()) != cudaSuccess) return e;
-    if ((e = prepare_one<kPair, kOutF16, 4, kHasC>()) != cudaSuccess) return e;
-    return prepare_one<kPair, kOutBF16, 4, kHasC>();
+    if ((e = prepare_one<kPair, kOutF32, 4, kHasC, kBNMax>()) != cudaSuccess) return e;
+    if ((e = prepare_one<kPair, kOutF32, 8, kHasC, kBNMax>()) != cudaSuccess) return e;
+    if ((e = prepare_one<kPair, kOutF16, 4, kHasC, kBNMax>()) != cudaSuccess) return e;
+    return prepare_one<kPair, kOutBF16, 4, kHasC, kBNMax>();
+}
+
+template <bool kHasC>
+static cudaError_t prepare_narrow() {
+    cudaError_t e;
+    if ((e = prepare_one<false, kOutF32, 4, kHasC, kNarrowN>()) != cudaSuccess) return e;
+    if ((e = prepare_one<false, kOutF16, 4, kHasC, kNarrowN>()) != cudaSuccess) return e;
+    return prepare_one<false, kOutBF16, 4, kHasC, kNarrowN>();
 }
 
 cudaError_t prepare_kernels_on_current_device() {
@@ -736,27 +773,32 @@ cudaError_t prepare_kernels_on_current_device() {
     if ((e = prepare_group<false, false>()) != cudaSuccess) return e;
     if ((e = prepare_group<false, true>()) != cudaSuccess) return e;
     if ((e = prepare_group<true, false>()) != cudaSuccess) return e;
-    return prepare_group<true, true>();
+    if ((e = prepare_group<true, true>()) != cudaSuccess) return e;
+    if ((e = prepare_narrow<false>()) != cudaSuccess) return e;
+    return prepare_narrow<true>();
 }
 
 int tcgen05_tile_m(int pair) { return pair ? Cfg<true, 4>::kTileM : Cfg<false, 4>::kTileM; }
-int tcgen05_tile_n() { return kBN; }
+int tcgen05_wide_n() { return kBNMax; }
+int tcgen05_narrow_n() { return kNarrowN; }
 int tcgen05_block_k() { return kBK; }
 int tcgen05_stage_k(int pair) { return kBK * (pair ? Cfg<true, 4>::kSub : Cfg<false, 4>::kSub); }
-int tcgen05_load_rows_b(int pair) { return pair ? Cfg<true, 4>::kLoadN : Cfg<false, 4>::kLoadN; }
+int tcgen05_load_rows_b(int pair, int tile_n) { return pair ? tile_n / 2 : tile_n; }
 int tcgen05_load_rows_a() { return kBM; }
-int tcgen05_smem_bytes(int pair, int epi_warps) {
+int tcgen05_smem_bytes(int pair, int epi_warps, int tile_n) {
+    if (tile_n == kNarrowN) return Cfg<false, 4, kNarrowN>::kSmemBytes;
     if (pair) return epi_warps == 8 ? Cfg<true, 8>::kSmemBytes : Cfg<true, 4>::kSmemBytes;
     return epi_warps == 8 ? Cfg<false, 8>::kSmemBytes : Cfg<false, 4>::kSmemBytes;
 }
-int tcgen05_stages(int pair, int epi_warps) {
+int tcgen05_stages(int pair, int epi_warps, int tile_n) {
+    if (tile_n == kNarrowN) return Cfg<false, 4, kNarrowN>::kStages;
     if (pair) return epi_warps == 8 ? Cfg<true, 8>::kStages : Cfg<true, 4>::kStages;
     return epi_warps == 8 ? Cfg<false, 8>::kStages : Cfg<false, 4>::kStages;
 }
 
-template <bool kPair, int kOut, int kEpiW, bool kHasC>
+template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN = kBNMax>
 static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
-    using Cf = Cfg<kPair, kEpiW>;
+    using Cf = Cfg<kPair, kEpiW, kTileN>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.grid, 1, 1);
     cfg.blockDim = dim3(Cf::kNumThreads, 1, 1);
@@ -771,7 +813,8 @@ static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC>, L.a, L.b, L.c, L.d, L.p);
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC, kTileN>, L.a, L.b, L.c, L.d,
+                              L.p);
 }
 
 template <bool kPair, bool kHasC>
@@ -783,8 +826,16 @@ static cudaError_t launch_group(const TcgenLaunch& L, cudaStream_t stream) {
     return launch_one<kPair, kOutBF16, 4, kHasC>(L, stream);
 }
 
+template <bool kHasC>
+static cudaError_t launch_narrow(const TcgenLaunch& L, cudaStream_t stream) {
+    if (L.out == kOutF32) return launch_one<false, kOutF32, 4, kHasC, kNarrowN>(L, stream);
+    if (L.out == kOutF16) return launch_one<false, kOutF16, 4, kHasC, kNarrowN>(L, stream);
+    return launch_one<false, kOutBF16, 4, kHasC, kNarrowN>(L, stream);
+}
+
 cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream) {
     const bool has_c = L.p.has_c != 0;
+    if (L.tile_n == kNarrowN) return has_c ? launch_narrow<true>(L, stream) : launch_narrow<false>(L, stream);
     if (L.pair) return has_c ? launch_group<true, true>(L, stream) : launch_group<true, false>(L, stream);
     return has_c ? launch_group<false, true>(L, stream) : launch_group<false, false>(L, stream);
 }

@@ -231,12 +231,24 @@ def test_plan_streamk_choices(lib):
     assert p["sk_tiles"] == 1024 % 76 and p["grid"] == 152 and p["workspace_bytes"] > 0
     p = binding.gemm_plan(8192, 8192, 256, 152)          # 2 stages per tile: too short to split
     assert p["sk_tiles"] == 0 and p["workspace_bytes"] == 0
-    p = binding.gemm_plan(1000, 1000, 1000, 152)         # shares too short to split: whole tiles
-    assert p["sk_tiles"] == 0 and p["grid"] == 32
+    p = binding.gemm_plan(1000, 1000, 1000, 152)         # 16 wide tiles: narrow ones instead, whole
+    assert p["sk_tiles"] == 0 and p["tile_n"] == 64 and p["cta_pair"] == 0 and p["grid"] == 128
     p = binding.gemm_plan(4096, 4096, 4096, 152)         # ~12 stages per worker: not split
     assert p["sk_tiles"] == 0
     p = binding.gemm_plan(8192, 8192, 16384, 152)        # ~60 stages per worker
     assert p["sk_tiles"] == 1024 % 76
+
+
+@pytest.mark.parametrize("M,N,K,tile_n", [(512, 512, 512, 64), (16, 8, 16, 64), (8192, 64, 4096, 64),
+                                          (2048, 2048, 2048, 256), (32768, 256, 4096, 256),
+                                          (1024, 1024, 4096, 64), (8192, 8192, 256, 256)])
+def test_plan_tile_width(lib, M, N, K, tile_n):
+    """Narrow 128 x 64 tiles exactly when the wide tiles would occupy at
+    most a quarter of the SMs, or N fits one narrow tile."""
+    p = binding.gemm_plan(M, N, K, 152)
+    assert p["tile_n"] == tile_n
+    if tile_n == 64:
+        assert p["cta_pair"] == 0 and p["tile_m"] == 128 and p["epi_warps"] == 4
 
 
 def test_schedule_rejects_bad_arguments(lib):

@@ -14,10 +14,10 @@ from tests import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
 
-# "pair" / "single": the tcgen05 kernel with 2-SM or 1-SM tiles (forced even
-# where the size rule would pick the mma.sync kernel); "mma_sync": the
-# warp-level kernel.
-VARIANTS = ["pair", "single", "mma_sync"]
+# "pair" / "single" / "narrow": the tcgen05 kernel with 256 x 256 tiles on
+# 2 SMs, 128 x 256 or 128 x 64 tiles on one SM (forced even where the size
+# rule would pick another); "mma_sync": the warp-level kernel.
+VARIANTS = ["pair", "single", "narrow", "mma_sync"]
 
 
 @pytest.fixture(scope="module", autouse=True)

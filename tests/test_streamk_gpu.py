@@ -20,7 +20,7 @@ def _device():
     assert H.poll()[0] == 0
 
 
-@pytest.fixture(params=["pair", "single"])
+@pytest.fixture(params=["pair", "single", "narrow"])
 def variant(request):
     with H.env(GEMM_PATH="tcgen05", GEMM_VARIANT=request.param):
         yield request.param
