@@ -225,7 +225,7 @@ struct Plan {
 
 // Stream-K policy: GEMM_STREAMK=0 never, 1 whenever the tiles do not fill
 // whole waves; the default does the same.  A stream-K range shorter than
-// GEMM_SK_MIN_ITERS stages (default 4) is not worth a partial: for small
+// GEMM_SK_MIN_ITERS stages (default 24) is not worth a partial: for small
 // problems fewer clusters are used instead.
 int streamk_setting() {
     const char* v = std::getenv("GEMM_STREAMK");
@@ -256,19 +256,31 @@ bool tma_layout_ok(const void* D, const void* A, const void* B, const void* C, i
     return ok;
 }
 
-// Which kernel: the warp-level mma.sync kernel when TMA cannot describe the
-// layout, or when the problem is so small that the tcgen05 kernel's set-up
-// dominates (M*N*K <= GEMM_SYNC_MAX_WORK, default 2^15 = 32^3);
-// GEMM_PATH=tcgen05|mma_sync forces one (tcgen05 only where TMA can).
-bool use_mma_sync(bool tma_ok, int64_t M, int64_t N, int64_t K) {
-    if (!tma_ok) return true;
+int64_t env_int64(const char* name, int64_t dflt) {
+    const char* v = std::getenv(name);
+    return (v && *v) ? std::strtoll(v, nullptr, 10) : dflt;
+}
+
+// Which kernel:
+//  * the tcgen05 kernel on the caller's buffers when TMA can describe them,
+//    except for problems so small that its set-up dominates
+//    (M*N*K <= GEMM_SYNC_MAX_WORK, default 2^15 = 32^3);
+//  * otherwise, when the caller may allocate and the problem pays for the
+//    copies (M*N*K > GEMM_REPACK_MIN_WORK, default 2^22), the tcgen05 kernel
+//    on repacked copies (see gemm_repacked);
+//  * else the warp-level mma.sync kernel, which takes any element-aligned
+//    layout as it is.
+// GEMM_PATH=tcgen05|mma_sync forces a kernel (tcgen05 through the repacking
+// when TMA cannot describe the layout and allocation is allowed).
+enum Route { kRouteTcgen05, kRouteRepack, kRouteSync };
+Route route_for(bool tma_ok, bool can_allocate, int64_t M, int64_t N, int64_t K) {
     const char* v = std::getenv("GEMM_PATH");
-    if (v && std::strcmp(v, "mma_sync") == 0) return true;
-    if (v && std::strcmp(v, "tcgen05") == 0) return false;
-    int64_t limit = 1 << 15;
-    const char* w = std::getenv("GEMM_SYNC_MAX_WORK");
-    if (w && *w) limit = std::strtoll(w, nullptr, 10);
-    return M * N * K <= limit;
+    const int64_t work = M * N * K;
+    if (v && std::strcmp(v, "mma_sync") == 0) return kRouteSync;
+    const bool force_tc = v && std::strcmp(v, "tcgen05") == 0;
+    if (tma_ok) return (!force_tc && work <= env_int64("GEMM_SYNC_MAX_WORK", 1 << 15)) ? kRouteSync : kRouteTcgen05;
+    if (can_allocate && (force_tc || work > env_int64("GEMM_REPACK_MIN_WORK", 1 << 22))) return kRouteRepack;
+    return kRouteSync;
 }
 
 cudaError_t launch_sync(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
@@ -364,11 +376,15 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
     return pl;
 }
 
-// Stream-K workspace, one per (device, stream): calls on one stream run in
-// order, so they can share it; calls on different streams get different
+// Device workspaces, one per (kind, device, stream): calls on one stream run
+// in order, so they can share one; calls on different streams get different
 // ones.  Grown on demand (freeing the old one synchronises the device) and
 // kept until the process exits.  `epoch` numbers the launches that use it.
+// Kinds: the stream-K partial sums and arrival counters, and the repacked
+// operands / outputs of gemm_repacked.
+enum WorkspaceKind { kWsStreamK = 0, kWsRepack = 1 };
 struct Workspace {
+    int kind;
     int dev;
     cudaStream_t stream;
     void* base;
@@ -377,13 +393,13 @@ struct Workspace {
 };
 std::vector<Workspace> g_workspaces;
 
-int workspace_for(int dev, cudaStream_t s, int64_t bytes, void** base, uint32_t* epoch) {
+int workspace_for(int kind, int dev, cudaStream_t s, int64_t bytes, void** base, uint32_t* epoch) {
     std::lock_guard<std::mutex> lock(g_mutex);
     Workspace* w = nullptr;
     for (auto& x : g_workspaces)
-        if (x.dev == dev && x.stream == s) w = &x;
+        if (x.kind == kind && x.dev == dev && x.stream == s) w = &x;
     if (!w) {
-        g_workspaces.push_back(Workspace{dev, s, nullptr, 0, 0});
+        g_workspaces.push_back(Workspace{kind, dev, s, nullptr, 0, 0});
         w = &g_workspaces.back();
     }
     if (w->bytes < bytes) {
@@ -402,6 +418,79 @@ int workspace_for(int dev, cudaStream_t s, int64_t bytes, void** base, uint32_t*
     w->epoch = (w->epoch + 1) & 0xFFFFFFu;
     *base = w->base;
     *epoch = w->epoch;
+    return GEMM_OK;
+}
+
+// Layouts TMA cannot describe, on the tcgen05 kernel.  Each operand or
+// output whose address or row stride is off the 16-byte grid is copied to
+// (for D: computed in) workspace rows padded to 16 bytes; the call then runs
+// on the aligned buffers, and a repacked D is copied back.
+//  * A, B: copied when misaligned.
+//  * D misaligned: the kernel writes a workspace D'.  C, when read, is read
+//    where it is if it is aligned and is not D; otherwise it is copied into
+//    D' first and the kernel runs in place on D'.
+//  * D aligned, C misaligned: C is copied into D, and the kernel runs in place.
+// Returns kNoWorkspace (before enqueuing anything) when the workspace cannot
+// be had, else GEMM_OK or the inner call's error.
+constexpr int kNoWorkspace = 1;
+int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                  int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float alpha,
+                  float beta, int in_dtype, int out_dtype, int dev, cudaStream_t s) {
+    const int osz = elem_size(out_dtype);
+    const bool has_c = beta != 0.0f;
+    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    auto round_up = [](int64_t x, int64_t m) { return (x + m - 1) / m * m; };
+    const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
+    const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
+    const bool a_ok = a16(A) && (lda * 2) % 16 == 0;
+    const bool b_ok = a16(B) && (ldb * 2) % 16 == 0;
+    const bool d_ok = a16(D) && (ldd * osz) % 16 == 0;
+    const bool c_ok = !has_c || (a16(C) && (ldc * osz) % 16 == 0);
+    const int64_t lda2 = a_ok ? lda : round_up(a_cols, 8);
+    const int64_t ldb2 = b_ok ? ldb : round_up(b_cols, 8);
+    const int64_t ldd2 = d_ok ? ldd : round_up(N, 16 / osz);
+    const int64_t a_bytes = a_ok ? 0 : round_up(a_rows * lda2 * 2, 256);
+    const int64_t b_bytes = b_ok ? 0 : round_up(b_rows * ldb2 * 2, 256);
+    const int64_t d_bytes = d_ok ? 0 : round_up(M * ldd2 * osz, 256);
+    void* ws = nullptr;
+    uint32_t epoch = 0;
+    if (workspace_for(kWsRepack, dev, s, a_bytes + b_bytes + d_bytes, &ws, &epoch) != GEMM_OK) return kNoWorkspace;
+    char* w = static_cast<char*>(ws);
+    const void* A2 = A;
+    const void* B2 = B;
+    void* D2 = D;
+    const void* C2 = C;
+    int64_t ldc2 = ldc;
+    cudaError_t e = cudaSuccess;
+    if (!a_ok) {
+        A2 = w;
+        e = gb300::launch_copy2d(w, lda2, A, lda, a_rows, a_cols, 2, s);
+        w += a_bytes;
+    }
+    if (e == cudaSuccess && !b_ok) {
+        B2 = w;
+        e = gb300::launch_copy2d(w, ldb2, B, ldb, b_rows, b_cols, 2, s);
+        w += b_bytes;
+    }
+    if (!d_ok) D2 = w;
+    if (e == cudaSuccess && has_c && !(c_ok && C != D)) {
+        if (!(c_ok && d_ok)) {   // (C == D, both aligned: already in place)
+            e = gb300::launch_copy2d(D2, ldd2, C, ldc, M, N, osz, s);
+            C2 = D2;
+            ldc2 = ldd2;
+        }
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    const int rc = gemm(D2, A2, B2, C2, M, N, K, lda2, ldb2, ldc2, ldd2, transA, transB, alpha, beta, in_dtype,
+                        out_dtype, s);
+    if (rc != GEMM_OK || d_ok) return rc;
+    if (gb300::launch_copy2d(D, ldd, D2, ldd2, M, N, osz, s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
     return GEMM_OK;
 }
 
@@ -543,7 +632,16 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
         return GEMM_OK;
     }
     const bool tma_ok = tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, osz, has_c);
-    if (use_mma_sync(tma_ok, M, N, K)) {
+    Route route = route_for(tma_ok, true, M, N, K);
+    if (route == kRouteRepack) {
+        GEMM_LOGF("M=%lld N=%lld K=%lld: layout not 16-byte aligned, repacked for the tcgen05 kernel", (long long)M,
+                  (long long)N, (long long)K);
+        rc = gemm_repacked(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype, out_dtype,
+                           dev, s);
+        if (rc != kNoWorkspace) return rc == GEMM_OK ? GEMM_OK : reject(rc, "repacked call");
+        route = kRouteSync;   // no workspace to be had: the kernel that needs none
+    }
+    if (route == kRouteSync) {
         GEMM_LOGF("M=%lld N=%lld K=%lld trans=%d%d: mma.sync kernel (%s)", (long long)M, (long long)N, (long long)K,
                   transA, transB, tma_ok ? "small problem" : "layout not 16-byte aligned");
         cudaError_t e = launch_sync(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype,
@@ -607,7 +705,7 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     if (pl.sk_tiles > 0) {
         void* ws = nullptr;
         uint32_t epoch = 0;
-        if ((rc = workspace_for(dev, s, pl.ws_bytes, &ws, &epoch)) != GEMM_OK)
+        if ((rc = workspace_for(kWsStreamK, dev, s, pl.ws_bytes, &ws, &epoch)) != GEMM_OK)
             return reject(rc, "stream-K workspace");
         p.sk_tiles = pl.sk_tiles;
         p.ws_max_nc = pl.max_nc;
@@ -803,7 +901,7 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
         if (e != cudaSuccess) return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
         return GEMM_OK;
     }
-    if (use_mma_sync(tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, osz, has_c), M, N, K)) {   // no scratch
+    if (route_for(tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, osz, has_c), false, M, N, K) == kRouteSync) {
         const int ok = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
         cudaError_t e = launch_sync(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype, ok,
                                     has_c, s);

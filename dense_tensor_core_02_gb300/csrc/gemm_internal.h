@@ -43,6 +43,11 @@ struct SyncParams {
 
 cudaError_t launch_mma_sync(const SyncParams& p, cudaStream_t stream);
 
+// dst[r * ldd + c] = src[r * lds + c] for r < rows, c < cols; elements of
+// elem_bytes (2 or 4) bytes, any element-aligned strides.
+cudaError_t launch_copy2d(void* dst, int64_t ldd, const void* src, int64_t lds, int64_t rows, int64_t cols,
+                          int elem_bytes, cudaStream_t stream);
+
 cudaError_t prepare_kernels_on_current_device();
 cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream);
 cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,

@@ -145,6 +145,47 @@ def normal_matrix(shape, dtype, seed, std=1.0):
     return (torch.randn(shape, generator=g) * std).to(TORCH[dtype])
 
 
+def strided(host, offset, ld, dtype, fill=float("nan")):
+    """Copy a CPU matrix [rows, cols] into a device buffer at element
+    `offset` with row stride `ld`; return (flat buffer, view)."""
+    rows, cols = host.shape
+    dev = torch.device("cuda", 0)
+    n = offset + (rows - 1) * ld + cols + 8 if rows else offset + 8
+    buf = torch.full((n,), fill, dtype=TORCH[dtype], device=dev)
+    view = buf.as_strided((rows, cols), (ld, 1), offset)
+    view.copy_(host.to(dev))
+    return buf, view
+
+
+def run_layout(A, B, C, M, N, K, *, offs=(0, 0, 0, 0), lds=None, transA=0, transB=0, alpha=1.0, beta=0.0,
+               in_dtype="f16", out_dtype="f32", fn=None):
+    """Call the C ABI (gemm, or `fn`) with A, B, C, D placed at element
+    offsets `offs` and row strides `lds` (default: the densest legal
+    strides); return D on the CPU, the whole D buffer (for canary checks)
+    and the status."""
+    fn = fn or binding.gemm
+    ra, ca = (K, M) if transA else (M, K)
+    rb, cb = (N, K) if transB else (K, N)
+    lda, ldb, ldc, ldd = lds or (ca, cb, N, N)
+    _, Av = strided(A, offs[0], lda, in_dtype)
+    _, Bv = strided(B, offs[1], ldb, in_dtype)
+    Cv = strided(C, offs[2], ldc, out_dtype)[1] if C is not None else None
+    Dbuf, Dv = strided(torch.full((M, N), float("nan")), offs[3], ldd, out_dtype)
+    rc = fn(Dv, Av, Bv, Cv, M, N, K, lda, ldb, ldc if C is not None else N, ldd, transA, transB, alpha, beta,
+            CODE[in_dtype], CODE[out_dtype], None)
+    torch.cuda.synchronize()
+    return Dv.cpu(), Dbuf.cpu(), rc
+
+
+def check_canaries(Dbuf, M, N, off, ldd):
+    """Everything in the D buffer outside the M x N view is still NaN."""
+    flat = Dbuf.double().numpy()
+    mask = np.ones(flat.shape, dtype=bool)
+    for r in range(M):
+        mask[off + r * ldd: off + r * ldd + N] = False
+    assert np.isnan(flat[mask]).all(), "elements outside D written"
+
+
 def tflops(M, N, K, ms):
     return 2.0 * M * N * K / (ms * 1e-3) / 1e12
 

@@ -1,13 +1,15 @@
 """GPU parity of the warp-level mma.sync kernel against the CPU oracle.
 
-This kernel takes what TMA cannot describe -- operand or output addresses
-and row strides that are element-aligned but not 16-byte multiples -- and
-tiny problems.  The tests here cover those layouts through the default
-routing (no environment override) and, with GEMM_PATH=mma_sync, the
-workloads the tcgen05 kernel is tested on.  The shared parity cases
-(golden atom, page test matrix, transposes, ragged canaries, in place,
-16-bit outputs, alpha/beta) run on this kernel through the "mma_sync"
-variant of the main GPU test module.
+This kernel takes any element-aligned layout as it is -- operand or output
+addresses and row strides that are not 16-byte multiples, which TMA cannot
+describe -- and tiny problems.  It runs every layout that gemm_noalloc()
+receives off the 16-byte grid, and gemm()'s small ones (larger ones are
+repacked for the tcgen05 kernel; see test_repack_gpu.py).  The tests here
+force it (GEMM_PATH=mma_sync) on those layouts and on the workloads the
+tcgen05 kernel is tested on.  The shared parity cases (golden atom, page
+test matrix, transposes, ragged canaries, in place, 16-bit outputs,
+alpha/beta) run on it through the "mma_sync" variant of the main GPU test
+module.
 """
 import numpy as np
 import pytest
@@ -30,46 +32,6 @@ def _device():
     assert rc == 0, ("device status after the module", rc, info)
 
 
-def _strided(host, offset, ld, dtype, fill=float("nan")):
-    """Copy a CPU matrix [rows, cols] into a device buffer at element
-    `offset` with row stride `ld`; return (flat buffer, view)."""
-    rows, cols = host.shape
-    dev = torch.device("cuda", 0)
-    n = offset + (rows - 1) * ld + cols + 8 if rows else offset + 8
-    buf = torch.full((n,), fill, dtype=H.TORCH[dtype], device=dev)
-    view = buf.as_strided((rows, cols), (ld, 1), offset)
-    view.copy_(host.to(dev))
-    return buf, view
-
-
-def _run(A, B, C, M, N, K, *, offs=(0, 0, 0, 0), lds=None, transA=0, transB=0, alpha=1.0, beta=0.0,
-         in_dtype="f16", out_dtype="f32", fn=None):
-    """Call the C ABI with A, B, C, D placed at element offsets `offs` and
-    row strides `lds` (default: the densest legal stride); return D on the
-    CPU, the whole D buffer (for canary checks), the status and (offset, ldd)."""
-    fn = fn or binding.gemm
-    ra, ca = (K, M) if transA else (M, K)
-    rb, cb = (N, K) if transB else (K, N)
-    lda, ldb, ldc, ldd = lds or (ca, cb, N, N)
-    _, Av = _strided(A, offs[0], lda, in_dtype)
-    _, Bv = _strided(B, offs[1], ldb, in_dtype)
-    Cv = _strided(C, offs[2], ldc, out_dtype)[1] if C is not None else None
-    Dbuf, Dv = _strided(torch.full((M, N), float("nan")), offs[3], ldd, out_dtype)
-    rc = fn(Dv, Av, Bv, Cv, M, N, K, lda, ldb, ldc if C is not None else N, ldd, transA, transB, alpha, beta,
-            H.CODE[in_dtype], H.CODE[out_dtype], None)
-    torch.cuda.synchronize()
-    return Dv.cpu(), Dbuf.cpu(), rc
-
-
-def _check_canaries(Dbuf, M, N, off, ldd):
-    """Everything in the D buffer outside the M x N view is still NaN."""
-    flat = Dbuf.double().numpy()
-    mask = np.ones(flat.shape, dtype=bool)
-    for r in range(M):
-        mask[off + r * ldd: off + r * ldd + N] = False
-    assert np.isnan(flat[mask]).all(), "elements outside D written"
-
-
 # (M, N, K, element offsets of A, B, C, D, strides lda, ldb, ldc, ldd or None)
 ODD_LAYOUTS = [
     (300, 200, 1001, (0, 0, 0, 0), None),                  # K = 1001: lda = 1001 (2002 bytes)
@@ -87,8 +49,8 @@ ODD_LAYOUTS = [
 @pytest.mark.parametrize("layout", ODD_LAYOUTS, ids=lambda l: "%dx%dx%d_o%s" % (l[0], l[1], l[2],
                                                                                "".join(map(str, l[3]))))
 def test_odd_layouts_integers_exact(layout, transA, transB):
-    """Layouts TMA cannot take, through the default routing; integer-valued
-    inputs, so the fp32 result is exact."""
+    """Layouts TMA cannot take; integer-valued inputs, so the fp32 result is
+    exact."""
     M, N, K, offs, lds = layout
     if lds is not None:
         ra, ca = (K, M) if transA else (M, K)
@@ -98,13 +60,13 @@ def test_odd_layouts_integers_exact(layout, transA, transB):
     A = H.int_matrix((K, M) if transA else (M, K), -8, 8, "f16", seed)
     B = H.int_matrix((N, K) if transB else (K, N), -8, 8, "f16", seed + 1)
     C = H.int_matrix((M, N), -100, 100, "f32", seed + 2)
-    with H.env(GEMM_PATH=None):
-        D, Dbuf, rc = _run(A, B, C, M, N, K, offs=offs, lds=lds, transA=transA, transB=transB, beta=1.0)
+    with H.env(GEMM_PATH="mma_sync"):
+        D, Dbuf, rc = H.run_layout(A, B, C, M, N, K, offs=offs, lds=lds, transA=transA, transB=transB, beta=1.0)
     assert rc == 0
     ref, _ = H.oracle_full(A, B, C, M, N, K, transA=transA, transB=transB, beta=1.0)
     H.assert_exact(D.numpy(), ref, "odd layout %s" % (layout,))
     ldd = lds[3] if lds else N
-    _check_canaries(Dbuf, M, N, offs[3], ldd)
+    H.check_canaries(Dbuf, M, N, offs[3], ldd)
 
 
 @pytest.mark.parametrize("in_dtype", ["f16", "bf16"])
@@ -116,12 +78,12 @@ def test_odd_layouts_random(in_dtype, out_dtype):
     B = H.normal_matrix((K, N), in_dtype, seed + 1)
     C = H.normal_matrix((M, N), out_dtype, seed + 2)
     kw = dict(transA=1, alpha=-1.25, beta=0.5, in_dtype=in_dtype, out_dtype=out_dtype)
-    with H.env(GEMM_PATH=None):
-        D, Dbuf, rc = _run(A, B, C, M, N, K, offs=(1, 1, 1, 1), lds=(M + 1, N + 3, N + 1, N + 5), **kw)
+    with H.env(GEMM_PATH="mma_sync"):
+        D, Dbuf, rc = H.run_layout(A, B, C, M, N, K, offs=(1, 1, 1, 1), lds=(M + 1, N + 3, N + 1, N + 5), **kw)
     assert rc == 0
     ref, bound = H.oracle_full(A, B, C, M, N, K, **kw)
     H.assert_close(D.double().numpy(), ref, bound, out_dtype, "odd random %s->%s" % (in_dtype, out_dtype))
-    _check_canaries(Dbuf, M, N, 1, N + 5)
+    H.check_canaries(Dbuf, M, N, 1, N + 5)
 
 
 def test_in_place_odd_layout():
@@ -131,10 +93,11 @@ def test_in_place_odd_layout():
     B = H.normal_matrix((N, K), "bf16", 92)
     C = H.normal_matrix((M, N), "f32", 93)
     dev = torch.device("cuda", 0)
-    _, Av = _strided(A, 1, K, "bf16")
-    _, Bv = _strided(B, 1, K, "bf16")
-    _, CD = _strided(C, 3, N + 1, "f32")
-    rc = binding.gemm(CD, Av, Bv, CD, M, N, K, K, K, N + 1, N + 1, 0, 1, 0.75, -1.5, 1, 2, None)
+    _, Av = H.strided(A, 1, K, "bf16")
+    _, Bv = H.strided(B, 1, K, "bf16")
+    _, CD = H.strided(C, 3, N + 1, "f32")
+    with H.env(GEMM_PATH="mma_sync"):
+        rc = binding.gemm(CD, Av, Bv, CD, M, N, K, K, K, N + 1, N + 1, 0, 1, 0.75, -1.5, 1, 2, None)
     assert rc == 0
     torch.cuda.synchronize()
     ref, bound = H.oracle_full(A, B, C, M, N, K, transB=1, alpha=0.75, beta=-1.5, in_dtype="bf16")
@@ -146,7 +109,8 @@ def test_beta_zero_never_reads_c_odd_layout():
     A = H.normal_matrix((M, K), "f16", 94)
     B = H.normal_matrix((K, N), "f16", 95)
     C = torch.full((M, N), float("nan"))
-    D, _, rc = _run(A, B, C, M, N, K, offs=(1, 1, 1, 1), beta=0.0)
+    with H.env(GEMM_PATH="mma_sync"):
+        D, _, rc = H.run_layout(A, B, C, M, N, K, offs=(1, 1, 1, 1), beta=0.0)
     assert rc == 0 and torch.isfinite(D).all()
     ref, bound = H.oracle_full(A, B, None, M, N, K)
     H.assert_close(D.numpy(), ref, bound, what="beta 0, NaN C, odd layout")
@@ -186,12 +150,12 @@ def test_workloads_forced_mma_sync(case):
 
 
 def test_large_odd_stride_sampled():
-    """A large problem whose K (4097) keeps it off TMA: sampled positions in
-    every 128 x 128 block against the oracle."""
+    """A large problem whose K (4097) keeps it off TMA, on this kernel:
+    sampled positions in every 128 x 128 block against the oracle."""
     M, N, K = 2048, 1536, 4097
     A = H.normal_matrix((M, K), "f16", 101)
     B = H.normal_matrix((N, K), "f16", 102)
-    with H.env(GEMM_PATH=None):
+    with H.env(GEMM_PATH="mma_sync"):
         D, rc = H.run_gemm(A, B, None, M, N, K, transB=1)
     assert rc == 0
     assert not torch.isnan(D).any()
