@@ -1,3 +1,6 @@
+// Kernels for layouts the TMA / tcgen05 kernel cannot take as they are:
+// the repacking copy (below) and, first, the warp-level tensor-core path.
+//
 // Warp-level tensor-core path: mma.sync.aligned.m16n8k16 with register
 // fragments, the lowering the TVM TIRx "gemm" page describes (sections
 // "Demonstration program", "Algorithm" and "Generated CUDA"), used for the
@@ -219,11 +222,40 @@ cudaError_t launch_sync_out(const SyncParams& p, cudaStream_t stream) {
     return launch_sync_one<kIn, kOutBF16, kHasC>(p, stream);
 }
 
+// Row-major 2-D copy between element-aligned layouts with any row strides:
+// the repacking step that gives the tcgen05 kernel's TMA copies 16-byte-
+// aligned operands and outputs.  Consecutive threads take consecutive
+// elements of a row.
+template <typename T>
+__global__ void copy2d_kernel(T* dst, int64_t ldd, const T* src, int64_t lds, int64_t rows, int64_t cols) {
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
+        for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols;
+             c += (int64_t)gridDim.x * blockDim.x)
+            dst[r * ldd + c] = src[r * lds + c];
+}
+
 }  // namespace
 
 cudaError_t launch_mma_sync(const SyncParams& p, cudaStream_t stream) {
     if (p.in_bf16) return p.has_c ? launch_sync_out<1, true>(p, stream) : launch_sync_out<1, false>(p, stream);
     return p.has_c ? launch_sync_out<0, true>(p, stream) : launch_sync_out<0, false>(p, stream);
+}
+
+cudaError_t launch_copy2d(void* dst, int64_t ldd, const void* src, int64_t lds, int64_t rows, int64_t cols,
+                          int elem_bytes, cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    constexpr int kThreads = 256;
+    int64_t gx = (cols + kThreads - 1) / kThreads;
+    if (gx > 64) gx = 64;
+    const int64_t gy = rows < 65535 ? rows : 65535;
+    const dim3 grid((unsigned)gx, (unsigned)gy);
+    if (elem_bytes == 4)
+        copy2d_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(static_cast<uint32_t*>(dst), ldd,
+                                                               static_cast<const uint32_t*>(src), lds, rows, cols);
+    else
+        copy2d_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(static_cast<uint16_t*>(dst), ldd,
+                                                               static_cast<const uint16_t*>(src), lds, rows, cols);
+    return cudaGetLastError();
 }
 
 }  // namespace gb300

@@ -719,18 +719,6 @@ __global__ void gemm_k0_kernel(void* D, const void* C, int M, int N, int64_t ldc
     }
 }
 
-// Row-major 2-D copy between element-aligned layouts with any row strides:
-// the repacking step that gives the tcgen05 kernel's TMA copies 16-byte-
-// aligned operands and outputs.  Consecutive threads take consecutive
-// elements of a row.
-template <typename T>
-__global__ void copy2d_kernel(T* dst, int64_t ldd, const T* src, int64_t lds, int64_t rows, int64_t cols) {
-    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
-        for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols;
-             c += (int64_t)gridDim.x * blockDim.x)
-            dst[r * ldd + c] = src[r * lds + c];
-}
-
 // ---------------------------------------------------------------------------
 // Scratch of the allocation-free entry point gemm_noalloc(): the device
 // status record its launches write lives in this fixed module array (zeroed
@@ -850,23 +838,6 @@ cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream) {
     if (L.tile_n == kNarrowN) return has_c ? launch_narrow<true>(L, stream) : launch_narrow<false>(L, stream);
     if (L.pair) return has_c ? launch_group<true, true>(L, stream) : launch_group<true, false>(L, stream);
     return has_c ? launch_group<false, true>(L, stream) : launch_group<false, false>(L, stream);
-}
-
-cudaError_t launch_copy2d(void* dst, int64_t ldd, const void* src, int64_t lds, int64_t rows, int64_t cols,
-                          int elem_bytes, cudaStream_t stream) {
-    if (rows <= 0 || cols <= 0) return cudaSuccess;
-    constexpr int kThreads = 256;
-    int64_t gx = (cols + kThreads - 1) / kThreads;
-    if (gx > 64) gx = 64;
-    const int64_t gy = rows < 65535 ? rows : 65535;
-    const dim3 grid((unsigned)gx, (unsigned)gy);
-    if (elem_bytes == 4)
-        copy2d_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(static_cast<uint32_t*>(dst), ldd,
-                                                               static_cast<const uint32_t*>(src), lds, rows, cols);
-    else
-        copy2d_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(static_cast<uint16_t*>(dst), ldd,
-                                                               static_cast<const uint16_t*>(src), lds, rows, cols);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,
