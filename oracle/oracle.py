@@ -12,8 +12,10 @@ gemm_fp16tc_fp32acc.ph epilogue), and the per-element error bound
 ``|alpha| * sum_k |a_ik * b_kj| + |beta| * |c_ij|``.
 
 Inputs are numpy arrays or torch CPU tensors: A and B hold fp16 / bf16
-bits, C holds fp32 (or fp16 / bf16 bits when the output is 16-bit).
-Row-major with explicit leading dimensions.
+bits, or E4M3 / E5M2 bits (one byte each; the 8-bit precisions of the
+tcgen05 path the TIRx gemm guide lists in section 七); C holds fp32 (or
+fp16 / bf16 bits when the output is 16-bit).  Row-major with explicit
+leading dimensions.
 """
 from __future__ import annotations
 
@@ -25,7 +27,8 @@ import threading
 
 import numpy as np
 
-F16, BF16, F32 = 0, 1, 2
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
+FP8 = (E4M3, E5M2)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "oracle_gemm.c")
@@ -63,6 +66,23 @@ def _bits16(x):
     return x.view(np.uint16)
 
 
+def _bits8(x):
+    """A 2-D uint8 array of E4M3 / E5M2 bit patterns."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):                      # torch tensor (float8 or uint8)
+        import torch
+        x = x.detach().cpu().contiguous().view(torch.uint8).numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype not in (np.uint8, np.int8):
+        raise TypeError("8-bit operand expected, got %s" % x.dtype)
+    return x.view(np.uint8)
+
+
+def _operand(x, in_dtype):
+    return _bits8(x) if in_dtype in FP8 else _bits16(x)
+
+
 def _c_array(c, c_dtype):
     if c is None:
         return None
@@ -96,6 +116,10 @@ class Oracle:
         lib.oracle_decode_f16.argtypes = [ctypes.c_uint16]
         lib.oracle_decode_bf16.restype = dbl
         lib.oracle_decode_bf16.argtypes = [ctypes.c_uint16]
+        lib.oracle_decode_e4m3.restype = dbl
+        lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
+        lib.oracle_decode_e5m2.restype = dbl
+        lib.oracle_decode_e5m2.argtypes = [ctypes.c_uint8]
         lib.oracle_gemm.restype = i32
         lib.oracle_gemm.argtypes = [vp, vp, i64, vp, vp, vp, i64, i64, i64, i64, i64, i64,
                                     i32, i32, dbl, dbl, i32, i32, i64, i64]
@@ -111,6 +135,12 @@ class Oracle:
     def decode_bf16(self, bits: int) -> float:
         return self.lib.oracle_decode_bf16(int(bits))
 
+    def decode_e4m3(self, bits: int) -> float:
+        return self.lib.oracle_decode_e4m3(int(bits))
+
+    def decode_e5m2(self, bits: int) -> float:
+        return self.lib.oracle_decode_e5m2(int(bits))
+
     def gemm(self, A, B, C, M, N, K, *, transA=0, transB=0, alpha=1.0, beta=0.0,
              in_dtype=F16, c_dtype=F32, lda=None, ldb=None, ldc=None,
              rows=None, threads=1):
@@ -120,10 +150,10 @@ class Oracle:
         the requested range stay NaN.  ``threads > 1`` runs disjoint row
         blocks of the same single-threaded C loop concurrently.
         """
-        A16, B16 = _bits16(A), _bits16(B)
+        Ab, Bb = _operand(A, in_dtype), _operand(B, in_dtype)
         C_ = _c_array(C, c_dtype) if beta != 0.0 else None
-        lda = lda if lda is not None else _ld(A16, M if transA else K)
-        ldb = ldb if ldb is not None else _ld(B16, K if transB else N)
+        lda = lda if lda is not None else _ld(Ab, M if transA else K)
+        ldb = ldb if ldb is not None else _ld(Bb, K if transB else N)
         ldc = ldc if ldc is not None else _ld(C_, N)
         D = np.full((M, N), np.nan)
         bound = np.full((M, N), np.nan)
@@ -131,7 +161,7 @@ class Oracle:
         lib = self.lib
 
         def run(a, b):
-            rc = lib.oracle_gemm(D.ctypes.data, bound.ctypes.data, N, _ptr(A16), _ptr(B16),
+            rc = lib.oracle_gemm(D.ctypes.data, bound.ctypes.data, N, _ptr(Ab), _ptr(Bb),
                                  _ptr(C_), M, N, K, lda, ldb, ldc, int(transA), int(transB),
                                  float(alpha), float(beta), int(in_dtype), int(c_dtype), a, b)
             if rc != 0:
@@ -149,10 +179,10 @@ class Oracle:
                      beta=0.0, in_dtype=F16, c_dtype=F32, lda=None, ldb=None, ldc=None,
                      threads=1):
         """D and bound at the listed (rows[e], cols[e]) positions only."""
-        A16, B16 = _bits16(A), _bits16(B)
+        Ab, Bb = _operand(A, in_dtype), _operand(B, in_dtype)
         C_ = _c_array(C, c_dtype) if beta != 0.0 else None
-        lda = lda if lda is not None else _ld(A16, M if transA else K)
-        ldb = ldb if ldb is not None else _ld(B16, K if transB else N)
+        lda = lda if lda is not None else _ld(Ab, M if transA else K)
+        ldb = ldb if ldb is not None else _ld(Bb, K if transB else N)
         ldc = ldc if ldc is not None else _ld(C_, N)
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         cols = np.ascontiguousarray(cols, dtype=np.int64)
@@ -164,7 +194,7 @@ class Oracle:
         def run(a, b):
             rc = lib.oracle_gemm_entries(D[a:].ctypes.data, bound[a:].ctypes.data,
                                          rows[a:].ctypes.data, cols[a:].ctypes.data, b - a,
-                                         _ptr(A16), _ptr(B16), _ptr(C_), M, N, K, lda, ldb, ldc,
+                                         _ptr(Ab), _ptr(Bb), _ptr(C_), M, N, K, lda, ldb, ldc,
                                          int(transA), int(transB), float(alpha), float(beta),
                                          int(in_dtype), int(c_dtype))
             if rc != 0:
@@ -208,3 +238,11 @@ def decode_f16(bits):
 
 def decode_bf16(bits):
     return default().decode_bf16(bits)
+
+
+def decode_e4m3(bits):
+    return default().decode_e4m3(bits)
+
+
+def decode_e5m2(bits):
+    return default().decode_e5m2(bits)

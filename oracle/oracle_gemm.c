@@ -28,7 +28,14 @@
  *   cannot reach D ("What it accepts" table, alpha / beta row; the
  *   "How inputs change the algorithm" table, beta row).
  *
- * Precision: every fp16 / bf16 / fp32 element is decoded exactly to a
+ * Operand types: fp16 and bf16 (the TIRx "gemm" page, "What it accepts",
+ * dtype row), and the 8-bit floating-point types E4M3 and E5M2 that the
+ * TIRx gemm guide lists among the asynchronous (tcgen05) path's precisions
+ * (section 七, "精度与指令族").  The pages do not define the 8-bit formats;
+ * they are the OCP 8-bit floating-point formats the PTX ISA calls .e4m3 and
+ * .e5m2 (decoders below).  A and B always have the same type.
+ *
+ * Precision: every fp16 / bf16 / fp8 / fp32 element is decoded exactly to a
  * double by the decoders below, products and sums are taken in double
  * (binary64), in increasing k order, one output element at a time.  The
  * sum of |products| is kept alongside, so the caller can form the
@@ -43,7 +50,7 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2 };
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2, ORACLE_E4M3 = 3, ORACLE_E5M2 = 4 };
 
 /* ---- exact element decoders -------------------------------------------- */
 
@@ -80,6 +87,41 @@ double oracle_decode_bf16(uint16_t h)
     return sign ? -v : v;
 }
 
+/* E4M3: 1 sign bit, 4 exponent bits (bias 7), 3 fraction bits; no
+ * infinities; S.1111.111 is NaN, so the largest finite value is
+ * 1.75 * 2^8 = 448. */
+double oracle_decode_e4m3(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xf;
+    int f = b & 0x7;
+    double v;
+    if (e == 15 && f == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);                /* subnormal: f * 2^-6 * 2^-3 */
+    else
+        v = ldexp((double)(8 + f), e - 10);      /* 1.f * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* E5M2: 1 sign bit, 5 exponent bits (bias 15), 2 fraction bits, with
+ * binary16's infinities and NaNs (exponent 31). */
+double oracle_decode_e5m2(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 2) & 0x1f;
+    int f = b & 0x3;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -16);               /* subnormal: f * 2^-14 * 2^-2 */
+    else if (e == 31)
+        v = (f == 0) ? INFINITY : NAN;
+    else
+        v = ldexp((double)(4 + f), e - 17);      /* 1.f * 2^(e-15) */
+    return sign ? -v : v;
+}
+
 /* binary32 -> binary64 is exact. */
 static double decode_f32(const void* p)
 {
@@ -88,11 +130,13 @@ static double decode_f32(const void* p)
     return (double)x;
 }
 
-/* The 16-bit decoders above are memoised in two 2^16-entry tables, filled
- * once by calling them on every bit pattern (pthread_once: the tests call
- * the oracle from several threads at a time). */
+/* The operand decoders above are memoised in tables indexed by the bit
+ * pattern, filled once by calling them on every pattern (pthread_once: the
+ * tests call the oracle from several threads at a time). */
 static double g_f16_table[65536];
 static double g_bf16_table[65536];
+static double g_e4m3_table[256];
+static double g_e5m2_table[256];
 static pthread_once_t g_tables_once = PTHREAD_ONCE_INIT;
 
 static void fill_tables(void)
@@ -101,39 +145,55 @@ static void fill_tables(void)
         g_f16_table[h] = oracle_decode_f16((uint16_t)h);
         g_bf16_table[h] = oracle_decode_bf16((uint16_t)h);
     }
+    for (uint32_t b = 0; b < 256u; ++b) {
+        g_e4m3_table[b] = oracle_decode_e4m3((uint8_t)b);
+        g_e5m2_table[b] = oracle_decode_e5m2((uint8_t)b);
+    }
 }
 
 static const double* table_for(int dtype)
 {
     pthread_once(&g_tables_once, fill_tables);
-    return dtype == ORACLE_F16 ? g_f16_table : g_bf16_table;
+    switch (dtype) {
+    case ORACLE_F16: return g_f16_table;
+    case ORACLE_BF16: return g_bf16_table;
+    case ORACLE_E4M3: return g_e4m3_table;
+    default: return g_e5m2_table;
+    }
 }
 
 /* ---- operand access ------------------------------------------------------ */
 
 typedef struct {
-    const uint16_t* A;
-    const uint16_t* B;
+    const void* A;
+    const void* B;
     const void* C;
     int64_t M, N, K, lda, ldb, ldc;
     int transA, transB;
     double alpha, beta;
     const double* in_table;   /* decoder for A and B */
+    int in_bytes;             /* bytes per A / B element: 2 (fp16, bf16) or 1 (fp8) */
     int c_dtype;
 } problem_t;
+
+/* The bit pattern of operand element `idx` (elements of in_bytes bytes). */
+static unsigned operand_bits(const problem_t* p, const void* X, int64_t idx)
+{
+    return p->in_bytes == 1 ? ((const uint8_t*)X)[idx] : ((const uint16_t*)X)[idx];
+}
 
 /* Ahat[i][k] */
 static double a_hat(const problem_t* p, int64_t i, int64_t k)
 {
-    uint16_t bits = p->transA ? p->A[k * p->lda + i] : p->A[i * p->lda + k];
-    return p->in_table[bits];
+    int64_t idx = p->transA ? k * p->lda + i : i * p->lda + k;
+    return p->in_table[operand_bits(p, p->A, idx)];
 }
 
 /* Bhat[k][j] */
 static double b_hat(const problem_t* p, int64_t k, int64_t j)
 {
-    uint16_t bits = p->transB ? p->B[j * p->ldb + k] : p->B[k * p->ldb + j];
-    return p->in_table[bits];
+    int64_t idx = p->transB ? j * p->ldb + k : k * p->ldb + j;
+    return p->in_table[operand_bits(p, p->B, idx)];
 }
 
 static double c_elem(const problem_t* p, int64_t i, int64_t j)
@@ -172,7 +232,9 @@ static int setup(problem_t* p, const void* A, const void* B, const void* C,
                  int in_dtype, int c_dtype)
 {
     if (M < 0 || N < 0 || K < 0) return -1;
-    if (in_dtype != ORACLE_F16 && in_dtype != ORACLE_BF16) return -1;
+    if (in_dtype != ORACLE_F16 && in_dtype != ORACLE_BF16 && in_dtype != ORACLE_E4M3 &&
+        in_dtype != ORACLE_E5M2)
+        return -1;
     if (c_dtype != ORACLE_F16 && c_dtype != ORACLE_BF16 && c_dtype != ORACLE_F32) return -1;
     if ((M > 0 && K > 0 && A == NULL) || (K > 0 && N > 0 && B == NULL)) return -1;
     if (beta != 0.0 && M > 0 && N > 0 && C == NULL) return -1;
@@ -180,14 +242,15 @@ static int setup(problem_t* p, const void* A, const void* B, const void* C,
     if (K > 0 && lda < (transA ? M : K)) return -1;
     if (K > 0 && ldb < (transB ? K : N)) return -1;
     if (beta != 0.0 && ldc < N) return -1;
-    p->A = (const uint16_t*)A;
-    p->B = (const uint16_t*)B;
+    p->A = A;
+    p->B = B;
     p->C = C;
     p->M = M; p->N = N; p->K = K;
     p->lda = lda; p->ldb = ldb; p->ldc = ldc;
     p->transA = transA != 0; p->transB = transB != 0;
     p->alpha = alpha; p->beta = beta;
     p->in_table = table_for(in_dtype);
+    p->in_bytes = (in_dtype == ORACLE_E4M3 || in_dtype == ORACLE_E5M2) ? 1 : 2;
     p->c_dtype = c_dtype;
     return 0;
 }

@@ -5,7 +5,11 @@ Each ``pin_*`` function takes a loaded ``Oracle`` and raises
 plain mathematics fix:
 
 * exact decoding of every fp16 / bf16 bit pattern (numpy's IEEE binary16,
-  and bfloat16 defined as the upper half of binary32);
+  and bfloat16 defined as the upper half of binary32) and of every E4M3 /
+  E5M2 pattern (torch's float8_e4m3fn / float8_e5m2 conversions, and the
+  formats' fixed points: largest finite values 448 and 57344, smallest
+  subnormals 2^-9 and 2^-16, E4M3's single NaN pattern per sign, E5M2's
+  infinities);
 * brute force in Python integers on integer-valued inputs, with padded
   leading dimensions and all four transpose forms (exact);
 * numpy's float64 matmul on random inputs (a library routine);
@@ -23,11 +27,11 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from oracle.oracle import BF16, F16, F32
+from oracle.oracle import BF16, E4M3, E5M2, F16, F32
 
 F16_NAN = 0x7E00
 BF16_NAN = 0x7FC0
-_TD = {F16: torch.float16, BF16: torch.bfloat16}
+_TD = {F16: torch.float16, BF16: torch.bfloat16, E4M3: torch.float8_e4m3fn, E5M2: torch.float8_e5m2}
 
 
 def _same(a, b):
@@ -66,6 +70,68 @@ def pin_decoders(orc):
     gotbf = np.array([orc.decode_bf16(x) for x in range(65536)])
     assert _same(got16, ref16), "fp16 decoder disagrees with IEEE binary16"
     assert _same(gotbf, refbf), "bf16 decoder disagrees with the upper half of binary32"
+
+
+def pin_fp8_decoders(orc):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    for dtype, decode in ((E4M3, orc.decode_e4m3), (E5M2, orc.decode_e5m2)):
+        ref = codes.view(_TD[dtype]).to(torch.float64).numpy()
+        got = np.array([decode(x) for x in range(256)])
+        assert _same(got, ref), "fp8 decoder %d disagrees with torch's conversion" % dtype
+    # fixed points of the formats
+    assert orc.decode_e4m3(0x7E) == 448.0 and orc.decode_e4m3(0xFE) == -448.0
+    assert orc.decode_e4m3(0x01) == 2.0 ** -9 and orc.decode_e4m3(0x08) == 2.0 ** -6
+    assert orc.decode_e4m3(0x38) == 1.0 and orc.decode_e4m3(0x78) == 256.0
+    nan4 = [b for b in range(256) if np.isnan(orc.decode_e4m3(b))]
+    assert nan4 == [0x7F, 0xFF], "E4M3 has exactly one NaN pattern per sign"
+    assert orc.decode_e5m2(0x7B) == 57344.0 and orc.decode_e5m2(0x01) == 2.0 ** -16
+    assert orc.decode_e5m2(0x3C) == 1.0 and orc.decode_e5m2(0x04) == 2.0 ** -14
+    assert orc.decode_e5m2(0x7C) == np.inf and orc.decode_e5m2(0xFC) == -np.inf
+    assert all(np.isnan(orc.decode_e5m2(b)) for b in (0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF))
+
+
+def _padded8(x8: torch.Tensor, pad: int):
+    """Copy of a 2-D fp8 tensor into a byte buffer with `pad` extra NaN columns
+    (0x7F is NaN in both formats).  Returns (buffer, leading dimension)."""
+    bits = x8.contiguous().view(torch.uint8).numpy()
+    rows, cols = bits.shape
+    buf = np.full((rows, cols + pad), 0x7F, dtype=np.uint8)
+    buf[:, :cols] = bits
+    return buf, cols + pad
+
+
+def pin_fp8_brute_force_integers(orc):
+    """Integers in [-8, 8] are exact in both formats: D is exact."""
+    rng = np.random.default_rng(43)
+    for dtype in (E4M3, E5M2):
+        for (M, N, K) in ((16, 8, 32), (5, 3, 9), (1, 1, 1), (9, 17, 40)):
+            for transA in (0, 1):
+                for transB in (0, 1):
+                    A = torch.from_numpy(rng.integers(-8, 9, size=(K, M) if transA else (M, K)).astype(np.float32)).to(_TD[dtype])
+                    B = torch.from_numpy(rng.integers(-8, 9, size=(N, K) if transB else (K, N)).astype(np.float32)).to(_TD[dtype])
+                    C = torch.from_numpy(rng.integers(-100, 101, size=(M, N)).astype(np.float32))
+                    Ab, lda = _padded8(A, 5)
+                    Bb, ldb = _padded8(B, 3)
+                    for alpha, beta in ((1, 0), (1, 1), (-2, 1)):
+                        D, _ = orc.gemm(Ab, Bb, C.numpy(), M, N, K, transA=transA, transB=transB,
+                                        alpha=alpha, beta=beta, in_dtype=dtype, lda=lda, ldb=ldb)
+                        ref = _brute(A.float(), B.float(), C if beta else None, transA, transB, alpha, beta)
+                        assert np.array_equal(D, np.array(ref, dtype=np.float64)), \
+                            "fp8 brute force mismatch %s trans=%d%d dtype=%d" % ((M, N, K), transA, transB, dtype)
+
+
+def pin_fp8_numpy_float64(orc):
+    rng = np.random.default_rng(47)
+    M, N, K = 21, 19, 67
+    for dtype in (E4M3, E5M2):
+        for transA, transB in ((0, 1), (1, 0)):
+            A = torch.from_numpy(rng.standard_normal((K, M) if transA else (M, K)).astype(np.float32)).to(_TD[dtype])
+            B = torch.from_numpy(rng.standard_normal((N, K) if transB else (K, N)).astype(np.float32)).to(_TD[dtype])
+            C = rng.standard_normal((M, N)).astype(np.float32)
+            D, bound = orc.gemm(A, B, C, M, N, K, transA=transA, transB=transB, alpha=0.75, beta=-1.5,
+                                in_dtype=dtype)
+            ref = 0.75 * (_op(A.double().numpy(), transA) @ _op(B.double().numpy(), transB)) - 1.5 * C.astype(np.float64)
+            assert np.all(np.abs(D - ref) <= 1e-12 * bound + 1e-300), "fp8 numpy float64 mismatch (dtype=%d)" % dtype
 
 
 def _brute(A, B, C, transA, transB, alpha, beta):
@@ -286,7 +352,8 @@ def pin_rejects_bad_arguments(orc):
     bad = [
         dict(lda=3),                      # row longer than the leading dimension
         dict(ldb=2),
-        dict(in_dtype=F32),               # operands must be 16-bit
+        dict(in_dtype=F32),               # operands must be 16- or 8-bit floating point
+        dict(in_dtype=7),
     ]
     for kw in bad:
         try:
@@ -298,6 +365,9 @@ def pin_rejects_bad_arguments(orc):
 
 ALL_PINS = [
     pin_decoders,
+    pin_fp8_decoders,
+    pin_fp8_brute_force_integers,
+    pin_fp8_numpy_float64,
     pin_brute_force_integers,
     pin_numpy_float64,
     pin_identity,

@@ -16,11 +16,11 @@ import oracle.oracle as oracle
 from tests import oracle_pins
 
 MUTANTS = {
-    "transA_ignored": ("p->transA ? p->A[k * p->lda + i] : p->A[i * p->lda + k]",
-                       "p->transA ? p->A[i * p->lda + k] : p->A[i * p->lda + k]"),
-    "transB_swapped": ("p->transB ? p->B[j * p->ldb + k] : p->B[k * p->ldb + j]",
-                       "p->transB ? p->B[k * p->ldb + j] : p->B[j * p->ldb + k]"),
-    "lda_replaced_by_K": ("p->A[i * p->lda + k]", "p->A[i * p->K + k]"),
+    "transA_ignored": ("int64_t idx = p->transA ? k * p->lda + i : i * p->lda + k;",
+                       "int64_t idx = p->transA ? i * p->lda + k : i * p->lda + k;"),
+    "transB_swapped": ("int64_t idx = p->transB ? j * p->ldb + k : k * p->ldb + j;",
+                       "int64_t idx = p->transB ? k * p->ldb + j : j * p->ldb + k;"),
+    "lda_replaced_by_K": ("i * p->lda + k;", "i * p->K + k;"),
     "ldc_replaced_by_N": ("int64_t off = i * p->ldc + j;", "int64_t off = i * p->N + j;"),
     "beta_dropped": ("d += p->beta * c;", "d += c;"),
     "beta0_reads_C": ("if (p->beta != 0.0) {             /* beta == 0: C is not read */",
@@ -42,6 +42,14 @@ MUTANTS = {
     "c16_decoded_as_bf16": ("return p->c_dtype == ORACLE_F16 ? oracle_decode_f16(bits) : oracle_decode_bf16(bits);",
                             "return oracle_decode_bf16(bits);"),
     "ld_check_missing": ("if (K > 0 && lda < (transA ? M : K)) return -1;", ""),
+    "e4m3_nan_missing": ("if (e == 15 && f == 7)\n        v = NAN;", "if (0)\n        v = NAN;"),
+    "e4m3_exponent_bias": ("v = ldexp((double)(8 + f), e - 10);", "v = ldexp((double)(8 + f), e - 9);"),
+    "e4m3_subnormal_scale": ("v = ldexp((double)f, -9);", "v = ldexp((double)f, -10);"),
+    "e5m2_subnormal_scale": ("v = ldexp((double)f, -16);", "v = ldexp((double)f, -15);"),
+    "e5m2_no_infinity": ("v = (f == 0) ? INFINITY : NAN;\n    else\n        v = ldexp((double)(4 + f), e - 17);",
+                         "v = ldexp((double)(4 + f), e - 17);\n    else\n        v = ldexp((double)(4 + f), e - 17);"),
+    "fp8_read_as_16bit": ("return p->in_bytes == 1 ?", "return p->in_bytes == 0 ?"),
+    "fp8_table_swapped": ("case ORACLE_E4M3: return g_e4m3_table;", "case ORACLE_E4M3: return g_e5m2_table;"),
     "entries_use_col_as_row": ("D[e] = one_element(&p, rows[e], cols[e], &bound[e]);",
                                "D[e] = one_element(&p, rows[e], cols[e] % (p.N > 1 ? p.N - 1 : 1), &bound[e]);"),
 }
