@@ -34,7 +34,9 @@ METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense fp16/bf16 tensor-core peak"
 UNIT = "TFLOP/s"
 NOMINAL_DENSE_TFLOPS = 2250.0        # GB300 dense fp16/bf16, NVIDIA's figure
 FLOP_PER_CLK_PER_SM = 8192           # dense f16/bf16 tcgen05 rate per SM
-KERNEL_SOURCES = ["dense_tensor_core_02_gb300/csrc/gemm_sm103.cu",
+FP8_RATE = 2.0                       # nominal dense fp8 rate / fp16 rate (4.5 / 2.25 PFLOP/s)
+KERNEL_SOURCES = ["dense_tensor_core_02_gb300/csrc/gemm_tcgen05.cuh",
+                  "dense_tensor_core_02_gb300/csrc/gemm_sm103.cu",
                   "dense_tensor_core_02_gb300/csrc/ptx.cuh",
                   "dense_tensor_core_02_gb300/csrc/gemm_params.h"]
 
@@ -187,7 +189,7 @@ def _oracle_sampler(case):
     A, B, C = make_inputs(case)
     threads = len(os.sched_getaffinity(0))
     rng = np.random.default_rng(case.seed)
-    code = {"f16": 0, "bf16": 1, "f32": 2}
+    code = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4}
 
     def run(n):
         rows = rng.integers(0, case.M, size=n)
@@ -269,7 +271,8 @@ def run_ours(args, case):
     torch.cuda.set_device(dev)
     binding.load_library()
 
-    code = {"f16": binding.F16, "bf16": binding.BF16, "f32": binding.F32}
+    code = {"f16": binding.F16, "bf16": binding.BF16, "f32": binding.F32, "e4m3": binding.E4M3,
+            "e5m2": binding.E5M2}
     A, B, C = make_inputs(case)
     Ad, Bd = A.to(dev), B.to(dev)
     Cd = C.to(dev) if C is not None else None
@@ -381,21 +384,26 @@ def run_ours(args, case):
     peaks, peak_src = _measured_peaks()
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     achieved = case.flops / (per_launch_ms * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops"])
+    # 8-bit operands: no measured fp8 peak exists, so the measured bf16 figures
+    # are scaled by the nominal dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s).
+    rate = FP8_RATE if case.in_dtype in ("e4m3", "e5m2") else 1.0
+    peak = float(peaks["bf16_tflops"]) * rate
+    src = ("%s bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json); f16 runs at the bf16 rate" % peak_src
+           if rate == 1.0 else
+           "%s bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json) x 2, the nominal dense fp8 / bf16 ratio" % peak_src)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                 "frac": achieved / peak, "traffic": _profiled_traffic(case.name),
-                "peak_source": "%s bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json); f16 runs at the bf16 rate"
-                               % peak_src,
-                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
-                "frac_of_nominal_2250": achieved / NOMINAL_DENSE_TFLOPS,
+                "peak_source": src,
+                "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak / rate)) * rate),
+                "frac_of_nominal": achieved / (NOMINAL_DENSE_TFLOPS * rate),
                 "algorithmic_flops_per_launch": case.flops,
                 "algorithmic_bytes_per_launch": case.algorithmic_bytes,
                 "achieved_gbs": case.algorithmic_bytes / (per_launch_ms * 1e-3) / 1e9}
     if clocks and clocks.get("sm_mhz"):
-        clk_peak = num_sms * FLOP_PER_CLK_PER_SM * clocks["sm_mhz"] * 1e6 / 1e12
+        clk_peak = num_sms * FLOP_PER_CLK_PER_SM * rate * clocks["sm_mhz"] * 1e6 / 1e12
         roofline["frac_of_clock_peak"] = achieved / clk_peak
         roofline["clock_peak_tflops"] = clk_peak
-    roofline["max_clock_peak_tflops"] = num_sms * FLOP_PER_CLK_PER_SM * 2070e6 / 1e12
+    roofline["max_clock_peak_tflops"] = num_sms * FLOP_PER_CLK_PER_SM * rate * 2070e6 / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per_launch_ms, "higher_is_better": True,

@@ -13,9 +13,10 @@ import ctypes
 import os
 import threading
 
-F16, BF16, F32 = 0, 1, 2
+F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
 GEMM_OK = 0
 GEMM_ERR_DEVICE_TIMEOUT = -8
+GEMM_ERR_UNSUPPORTED_LAYOUT = -10
 
 LIBRARY_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgemm_gb300.so")
 

@@ -135,7 +135,11 @@ void tuning(GemmParams& p) {
     }
 }
 
-int elem_size(int dtype) { return dtype == GEMM_F32 ? 4 : 2; }
+bool is_f8(int dtype) { return dtype == GEMM_E4M3 || dtype == GEMM_E5M2; }
+int elem_size(int dtype) { return dtype == GEMM_F32 ? 4 : is_f8(dtype) ? 1 : 2; }
+int out_kind_of(int out_dtype) {
+    return out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
+}
 
 // Byte range [lo, hi) covered by a row-major rows x cols matrix.
 void byte_range(const void* p, int64_t rows, int64_t cols, int64_t ld, int esz, uintptr_t* lo, uintptr_t* hi) {
@@ -185,9 +189,14 @@ int get_encoder() {
     return g_encode ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// TMA moves bits: 8-bit floating-point operands travel as bytes.
 CUtensorMapDataType tma_dtype(int dt) {
-    return dt == GEMM_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                          : dt == GEMM_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    switch (dt) {
+        case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+        case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        case GEMM_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    }
 }
 
 // A 2-D row-major matrix: dim0 = contiguous extent, dim1 = rows; the box is
@@ -248,13 +257,17 @@ constexpr int64_t kPartialBytes = 128 * 256 * 4;   // one CTA's 128 x 256 fp32 a
 
 // TMA (the tcgen05 kernel) needs 16-byte-aligned bases and row strides.
 bool tma_layout_ok(const void* D, const void* A, const void* B, const void* C, int64_t K, int64_t lda, int64_t ldb,
-                   int64_t ldc, int64_t ldd, int osz, bool has_c) {
+                   int64_t ldc, int64_t ldd, int isz, int osz, bool has_c) {
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     bool ok = a16(D) && ((ldd * osz) & 15) == 0;
     if (has_c) ok = ok && a16(C) && ((ldc * osz) & 15) == 0;
-    if (K > 0) ok = ok && a16(A) && a16(B) && (((lda * 2) | (ldb * 2)) & 15) == 0;
+    if (K > 0) ok = ok && a16(A) && a16(B) && (((lda * isz) | (ldb * isz)) & 15) == 0;
     return ok;
 }
+
+// The tcgen05 kernel stages 8-bit operands K-major only: A stored [M, K]
+// (transA = 0) and B stored [N, K] (transB = 1).
+bool operand_majors_ok(int in_dtype, int transA, int transB) { return !is_f8(in_dtype) || (!transA && transB); }
 
 int64_t env_int64(const char* name, int64_t dflt) {
     const char* v = std::getenv(name);
@@ -262,25 +275,27 @@ int64_t env_int64(const char* name, int64_t dflt) {
 }
 
 // Which kernel:
-//  * the tcgen05 kernel on the caller's buffers when TMA can describe them,
-//    except for problems so small that its set-up dominates
+//  * the tcgen05 kernel on the caller's buffers when it can take them as
+//    they are (TMA's alignment rule; 8-bit operands K-major), except for
+//    fp16 / bf16 problems so small that its set-up dominates
 //    (M*N*K <= GEMM_SYNC_MAX_WORK, default 2^15 = 32^3);
 //  * otherwise, when the caller may allocate and the problem pays for the
-//    copies (M*N*K > GEMM_REPACK_MIN_WORK, default 2^22), the tcgen05 kernel
-//    on repacked copies (see gemm_repacked);
+//    copies (M*N*K > GEMM_REPACK_MIN_WORK, default 2^22; always for 8-bit
+//    operands), the tcgen05 kernel on repacked copies (gemm_repacked);
 //  * else the warp-level mma.sync kernel, which takes any element-aligned
-//    layout as it is.
-// GEMM_PATH=tcgen05|mma_sync forces a kernel (tcgen05 through the repacking
-// when TMA cannot describe the layout and allocation is allowed).
-enum Route { kRouteTcgen05, kRouteRepack, kRouteSync };
-Route route_for(bool tma_ok, bool can_allocate, int64_t M, int64_t N, int64_t K) {
+//    fp16 / bf16 layout as it is; 8-bit operands have no such kernel.
+// GEMM_PATH=tcgen05|mma_sync forces a kernel where one can run (tcgen05
+// through the repacking when it cannot take the buffers as they are).
+enum Route { kRouteTcgen05, kRouteRepack, kRouteSync, kRouteNone };
+Route route_for(bool direct_ok, bool f8, bool can_allocate, int64_t M, int64_t N, int64_t K) {
     const char* v = std::getenv("GEMM_PATH");
     const int64_t work = M * N * K;
-    if (v && std::strcmp(v, "mma_sync") == 0) return kRouteSync;
+    if (!f8 && v && std::strcmp(v, "mma_sync") == 0) return kRouteSync;
     const bool force_tc = v && std::strcmp(v, "tcgen05") == 0;
-    if (tma_ok) return (!force_tc && work <= env_int64("GEMM_SYNC_MAX_WORK", 1 << 15)) ? kRouteSync : kRouteTcgen05;
-    if (can_allocate && (force_tc || work > env_int64("GEMM_REPACK_MIN_WORK", 1 << 22))) return kRouteRepack;
-    return kRouteSync;
+    if (direct_ok)
+        return (!f8 && !force_tc && work <= env_int64("GEMM_SYNC_MAX_WORK", 1 << 15)) ? kRouteSync : kRouteTcgen05;
+    if (can_allocate && (f8 || force_tc || work > env_int64("GEMM_REPACK_MIN_WORK", 1 << 22))) return kRouteRepack;
+    return f8 ? kRouteNone : kRouteSync;
 }
 
 cudaError_t launch_sync(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
@@ -311,15 +326,15 @@ cudaError_t launch_sync(void* D, const void* A, const void* B, const void* C, in
 // Epilogue warps: 8 when a tile's main loop is short (few K stages), so the
 // time goes into storing D; 4 otherwise.  The 8-warp kernels exist for f32
 // output only.  GEMM_EPI_WARPS=4|8 overrides (f32 output).
-int epi_warps_for(int64_t K, int pair, int out_dtype, int tile_n) {
+int epi_warps_for(int64_t K, int pair, int out_dtype, int tile_n, int f8) {
     if (out_dtype != GEMM_F32 || tile_n == gb300::tcgen05_narrow_n()) return 4;
     const char* v = std::getenv("GEMM_EPI_WARPS");
     if (v && (std::strcmp(v, "4") == 0 || std::strcmp(v, "8") == 0)) return std::atoi(v);
-    const int64_t stage_k = gb300::tcgen05_stage_k(pair);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pair, f8);
     return (K + stage_k - 1) / stage_k <= 4 ? 8 : 4;
 }
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk, int out_dtype) {
+Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk, int out_dtype, int f8) {
     Plan pl{};
     const int ov = variant_override();
     pl.pair = ov == kPairV || (ov == kAuto && M > gb300::tcgen05_tile_m(0)) ? 1 : 0;
@@ -337,7 +352,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
     pl.num_m = (int)((M + pl.tile_m - 1) / pl.tile_m);
     pl.num_n = (int)((N + pl.tile_n - 1) / pl.tile_n);
     pl.num_tiles = pl.num_m * pl.num_n;
-    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8);
     pl.iters = (int)((K + stage_k - 1) / stage_k);
     const int units = pl.pair ? num_sms / 2 : num_sms;   // clusters that fit at once
     int clusters = pl.num_tiles < units ? pl.num_tiles : units;
@@ -370,7 +385,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
         const int64_t counters = ((int64_t)pl.sk_tiles * 2 * 4 + 255) / 256 * 256;
         pl.ws_bytes = counters + (int64_t)pl.sk_tiles * pl.max_nc * 2 * kPartialBytes;
     }
-    pl.epi_warps = epi_warps_for(K, pl.pair, out_dtype, pl.tile_n);
+    pl.epi_warps = epi_warps_for(K, pl.pair, out_dtype, pl.tile_n, f8);
     pl.smem = gb300::tcgen05_smem_bytes(pl.pair, pl.epi_warps, pl.tile_n);
     pl.stages = gb300::tcgen05_stages(pl.pair, pl.epi_warps, pl.tile_n);
     return pl;
@@ -421,11 +436,168 @@ int workspace_for(int kind, int dev, cudaStream_t s, int64_t bytes, void** base,
     return GEMM_OK;
 }
 
-// Layouts TMA cannot describe, on the tcgen05 kernel.  Each operand or
-// output whose address or row stride is off the 16-byte grid is copied to
-// (for D: computed in) workspace rows padded to 16 bytes; the call then runs
-// on the aligned buffers, and a repacked D is copied back.
-//  * A, B: copied when misaligned.
+// The argument rules shared by gemm() and gemm_noalloc(), checked on the
+// host without touching the device.
+int validate(const void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+             int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float beta, int in_dtype,
+             int out_dtype) {
+    if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16 && !is_f8(in_dtype))
+        return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "in_dtype");
+    if (out_dtype != GEMM_F32 && out_dtype != GEMM_F16 && out_dtype != GEMM_BF16)
+        return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "out_dtype");
+    if (M < 0 || N < 0 || K < 0) return reject(GEMM_ERR_INVALID_ARG, "negative size");
+    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
+        return reject(GEMM_ERR_INVALID_ARG, "transpose flag not 0/1");
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return reject(GEMM_ERR_TOO_LARGE, "dimension");
+    const bool has_c = beta != 0.0f;
+    const int isz = elem_size(in_dtype);
+    const int osz = elem_size(out_dtype);
+    if (!D) return reject(GEMM_ERR_INVALID_ARG, "D is NULL");
+    if (ldd < N) return reject(GEMM_ERR_INVALID_ARG, "ldd < N");
+    if (has_c) {
+        if (!C) return reject(GEMM_ERR_INVALID_ARG, "C is NULL with beta != 0");
+        if (ldc < N) return reject(GEMM_ERR_INVALID_ARG, "ldc < N");
+    }
+    if (K > 0) {
+        if (!A || !B) return reject(GEMM_ERR_INVALID_ARG, "A or B is NULL");
+        if (lda < (transA ? M : K)) return reject(GEMM_ERR_INVALID_ARG, "lda too small");
+        if (ldb < (transB ? K : N)) return reject(GEMM_ERR_INVALID_ARG, "ldb too small");
+        if (lda * isz >= kMaxStrideBytes || ldb * isz >= kMaxStrideBytes) return reject(GEMM_ERR_TOO_LARGE, "stride");
+        if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & (uintptr_t)(isz - 1))
+            return reject(GEMM_ERR_MISALIGNED, "A or B not element-aligned");
+    }
+    if (ldd * osz >= kMaxStrideBytes || (has_c && ldc * osz >= kMaxStrideBytes))
+        return reject(GEMM_ERR_TOO_LARGE, "stride");
+    if (reinterpret_cast<uintptr_t>(D) & (uintptr_t)(osz - 1)) return reject(GEMM_ERR_MISALIGNED, "D not element-aligned");
+    if (has_c && (reinterpret_cast<uintptr_t>(C) & (uintptr_t)(osz - 1)))
+        return reject(GEMM_ERR_MISALIGNED, "C not element-aligned");
+    uintptr_t d0, d1;
+    byte_range(D, M, N, ldd, osz, &d0, &d1);
+    if (K > 0) {
+        uintptr_t a0, a1, b0, b1;
+        byte_range(A, transA ? K : M, transA ? M : K, lda, isz, &a0, &a1);
+        byte_range(B, transB ? N : K, transB ? K : N, ldb, isz, &b0, &b1);
+        if (overlaps(d0, d1, a0, a1) || overlaps(d0, d1, b0, b1)) return reject(GEMM_ERR_ALIAS, "D overlaps A or B");
+    }
+    if (has_c && !(C == D && ldc == ldd)) {
+        uintptr_t c0, c1;
+        byte_range(C, M, N, ldc, osz, &c0, &c1);
+        if (overlaps(d0, d1, c0, c1)) return reject(GEMM_ERR_ALIAS, "D overlaps C (other than C == D, ldc == ldd)");
+    }
+    return GEMM_OK;
+}
+
+// Tensor maps, kernel parameters and instruction descriptor of one tcgen05
+// launch over buffers it can take as they are; the caller adds the status
+// record and, for stream-K, the workspace.
+int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, const void* B, const void* C,
+                     int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA,
+                     int transB, float alpha, float beta, int in_dtype, int out_dtype) {
+    const bool has_c = beta != 0.0f;
+    const bool f8 = is_f8(in_dtype);
+    const int osz = elem_size(out_dtype);
+    int rc;
+    if ((rc = get_encoder()) != GEMM_OK) return rc;
+    std::memset(L, 0, sizeof(*L));
+    const uint32_t bk = (uint32_t)gb300::tcgen05_block_k(f8);   // K elements per 128-byte row
+    // A: K-major (transA = 0) as [M rows][K], else MN-major as [K rows][M]
+    if (!transA)
+        rc = encode_2d(&L->a, in_dtype, A, K, M, lda, bk, (uint32_t)gb300::tcgen05_load_rows_a());
+    else
+        rc = encode_2d(&L->a, in_dtype, A, M, K, lda, 64, bk);
+    if (rc != GEMM_OK) return rc;
+    // B: K-major (transB = 1) as [N rows][K], else MN-major as [K rows][N]
+    if (transB)
+        rc = encode_2d(&L->b, in_dtype, B, K, N, ldb, bk, (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n));
+    else
+        rc = encode_2d(&L->b, in_dtype, B, N, K, ldb, 64, bk);
+    if (rc != GEMM_OK) return rc;
+    const uint32_t chunk_cols = 128u / (uint32_t)osz;
+    // TMA stores write whole 16-byte pieces of a row, even past the tensor's
+    // last column: D's map stops at the last whole piece (n_tma) and the
+    // kernel stores columns [n_tma, N) element by element.
+    const int64_t vec = 16 / osz;
+    const int64_t n_tma = (N / vec) * vec;
+    if ((rc = encode_2d(&L->d, out_dtype, D, n_tma > 0 ? n_tma : N, M, ldd, chunk_cols, 32)) != GEMM_OK) return rc;
+    if (has_c && (rc = encode_2d(&L->c, out_dtype, C, N, M, ldc, chunk_cols, 32)) != GEMM_OK) return rc;
+    GemmParams& p = L->p;
+    p.M = (int32_t)M;
+    p.N = (int32_t)N;
+    p.K = (int32_t)K;
+    p.num_m_tiles = pl.num_m;
+    p.num_n_tiles = pl.num_n;
+    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8);
+    p.num_k_blocks = (int32_t)((K + stage_k - 1) / stage_k);   // pipeline stages per tile
+    p.num_tiles = pl.num_tiles;
+    p.group_m = group_m_setting();
+    p.alpha = alpha;
+    p.beta = beta;
+    p.a_mn_major = transA ? 1 : 0;
+    p.b_mn_major = transB ? 0 : 1;
+    p.has_c = has_c ? 1 : 0;
+    p.timeout_ns = wait_timeout_ns();
+    p.n_tma = (int32_t)n_tma;
+    p.d_ptr = D;
+    p.ldd = ldd;
+    tuning(p);
+    // tcgen05 instruction descriptor (kind::f16 or kind::f8f6f4, chosen by the
+    // kernel instantiation): D format f32 (bits 4-5 = 1); A / B format (bits
+    // 7-9, 10-12): kind::f16 0 = f16, 1 = bf16; kind::f8f6f4 0 = E4M3, 1 = E5M2;
+    // A / B major (bits 15, 16: 1 = MN-major); N >> 3 (bits 17-22); M >> 4
+    // (bits 24-28).
+    const uint32_t fmt = (in_dtype == GEMM_BF16 || in_dtype == GEMM_E5M2) ? 1u : 0u;
+    const uint32_t mma_m = (uint32_t)pl.tile_m;   // 128 (one SM) or 256 (CTA pair)
+    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)p.a_mn_major << 15) |
+              ((uint32_t)p.b_mn_major << 16) | (((uint32_t)pl.tile_n >> 3) << 17) | ((mma_m >> 4) << 24);
+    L->pair = pl.pair;
+    L->tile_n = pl.tile_n;
+    L->f8 = f8 ? 1 : 0;
+    L->out = out_kind_of(out_dtype);
+    L->grid = pl.grid;
+    L->epi_warps = pl.epi_warps;
+    return GEMM_OK;
+}
+
+int launch_described(const TcgenLaunch& L, cudaStream_t s) {
+    cudaError_t e = gb300::launch_tcgen05(L, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+    }
+    return GEMM_OK;
+}
+
+int launch_k0_or_reject(int out_dtype, void* D, const void* C, int64_t M, int64_t N, int64_t ldc, int64_t ldd,
+                        float alpha, float beta, int num_sms, cudaStream_t s) {
+    const bool has_c = beta != 0.0f;
+    cudaError_t e = gb300::launch_k0(out_kind_of(out_dtype), D, has_c ? C : nullptr, (int)M, (int)N, ldc, ldd, alpha,
+                                     beta, has_c ? 1 : 0, num_sms, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+    }
+    return GEMM_OK;
+}
+
+int launch_sync_or_reject(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                          int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float alpha,
+                          float beta, int in_dtype, int out_dtype, cudaStream_t s) {
+    cudaError_t e = launch_sync(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype,
+                                out_kind_of(out_dtype), beta != 0.0f, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+    }
+    return GEMM_OK;
+}
+
+// Layouts the tcgen05 kernel cannot take as they are, made so.  Each operand
+// or output whose address or row stride is off the 16-byte grid is copied
+// to (for D: computed in) workspace rows padded to 16 bytes; an 8-bit operand
+// stored MN-major (A with transA, B without transB) is transposed into a
+// K-major workspace copy.  The call then runs on the prepared buffers, and a
+// workspace D is copied back.
 //  * D misaligned: the kernel writes a workspace D'.  C, when read, is read
 //    where it is if it is aligned and is not D; otherwise it is copied into
 //    D' first and the kernel runs in place on D'.
@@ -436,21 +608,30 @@ constexpr int kNoWorkspace = 1;
 int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
                   int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float alpha,
                   float beta, int in_dtype, int out_dtype, int dev, cudaStream_t s) {
+    const int isz = elem_size(in_dtype);
     const int osz = elem_size(out_dtype);
     const bool has_c = beta != 0.0f;
+    const bool f8 = is_f8(in_dtype);
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     auto round_up = [](int64_t x, int64_t m) { return (x + m - 1) / m * m; };
     const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
     const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
-    const bool a_ok = a16(A) && (lda * 2) % 16 == 0;
-    const bool b_ok = a16(B) && (ldb * 2) % 16 == 0;
+    // 8-bit operands end up K-major: A as [M, K] (transA2 = 0), B as [N, K] (transB2 = 1)
+    const int transA2 = f8 ? 0 : transA;
+    const int transB2 = f8 ? 1 : transB;
+    const bool a_turn = transA2 != transA, b_turn = transB2 != transB;
+    const bool a_ok = !a_turn && a16(A) && (lda * isz) % 16 == 0;
+    const bool b_ok = !b_turn && a16(B) && (ldb * isz) % 16 == 0;
     const bool d_ok = a16(D) && (ldd * osz) % 16 == 0;
     const bool c_ok = !has_c || (a16(C) && (ldc * osz) % 16 == 0);
-    const int64_t lda2 = a_ok ? lda : round_up(a_cols, 8);
-    const int64_t ldb2 = b_ok ? ldb : round_up(b_cols, 8);
+    const int64_t per16 = 16 / isz;   // elements per 16 bytes
+    const int64_t a_rows2 = a_turn ? a_cols : a_rows, a_cols2 = a_turn ? a_rows : a_cols;
+    const int64_t b_rows2 = b_turn ? b_cols : b_rows, b_cols2 = b_turn ? b_rows : b_cols;
+    const int64_t lda2 = a_ok ? lda : round_up(a_cols2, per16);
+    const int64_t ldb2 = b_ok ? ldb : round_up(b_cols2, per16);
     const int64_t ldd2 = d_ok ? ldd : round_up(N, 16 / osz);
-    const int64_t a_bytes = a_ok ? 0 : round_up(a_rows * lda2 * 2, 256);
-    const int64_t b_bytes = b_ok ? 0 : round_up(b_rows * ldb2 * 2, 256);
+    const int64_t a_bytes = a_ok ? 0 : round_up(a_rows2 * lda2 * isz, 256);
+    const int64_t b_bytes = b_ok ? 0 : round_up(b_rows2 * ldb2 * isz, 256);
     const int64_t d_bytes = d_ok ? 0 : round_up(M * ldd2 * osz, 256);
     void* ws = nullptr;
     uint32_t epoch = 0;
@@ -464,12 +645,14 @@ int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t 
     cudaError_t e = cudaSuccess;
     if (!a_ok) {
         A2 = w;
-        e = gb300::launch_copy2d(w, lda2, A, lda, a_rows, a_cols, 2, s);
+        e = a_turn ? gb300::launch_transpose2d(w, lda2, A, lda, a_rows, a_cols, isz, s)
+                   : gb300::launch_copy2d(w, lda2, A, lda, a_rows, a_cols, isz, s);
         w += a_bytes;
     }
     if (e == cudaSuccess && !b_ok) {
         B2 = w;
-        e = gb300::launch_copy2d(w, ldb2, B, ldb, b_rows, b_cols, 2, s);
+        e = b_turn ? gb300::launch_transpose2d(w, ldb2, B, ldb, b_rows, b_cols, isz, s)
+                   : gb300::launch_copy2d(w, ldb2, B, ldb, b_rows, b_cols, isz, s);
         w += b_bytes;
     }
     if (!d_ok) D2 = w;
@@ -484,7 +667,7 @@ int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t 
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
-    const int rc = gemm(D2, A2, B2, C2, M, N, K, lda2, ldb2, ldc2, ldd2, transA, transB, alpha, beta, in_dtype,
+    const int rc = gemm(D2, A2, B2, C2, M, N, K, lda2, ldb2, ldc2, ldd2, transA2, transB2, alpha, beta, in_dtype,
                         out_dtype, s);
     if (rc != GEMM_OK || d_ok) return rc;
     if (gb300::launch_copy2d(D, ldd, D2, ldd2, M, N, osz, s) != cudaSuccess) {
@@ -498,6 +681,7 @@ int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t 
 
 extern "C" {
 
+
 const char* gemm_status_string(int status) {
     switch (status) {
         case GEMM_OK: return "GEMM_OK";
@@ -510,6 +694,7 @@ const char* gemm_status_string(int status) {
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA";
         case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT";
         case GEMM_ERR_TOO_LARGE: return "GEMM_ERR_TOO_LARGE";
+        case GEMM_ERR_UNSUPPORTED_LAYOUT: return "GEMM_ERR_UNSUPPORTED_LAYOUT";
         default: return "GEMM_ERR_UNKNOWN";
     }
 }
@@ -548,7 +733,7 @@ int gemm_schedule_units(int num_tiles, int iters, int workers, int sk_tiles, int
 int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out) {
     if (M < 1 || N < 1 || K < 0 || num_sms < 2 || !out) return GEMM_ERR_INVALID_ARG;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_TOO_LARGE;
-    Plan pl = make_plan(M, N, K, num_sms, true, GEMM_F32);
+    Plan pl = make_plan(M, N, K, num_sms, true, GEMM_F32, 0);
     out[0] = pl.pair;
     out[1] = pl.tile_m;
     out[2] = pl.tile_n;
@@ -565,52 +750,8 @@ int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out) {
 int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
          int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float alpha, float beta, int in_dtype,
          int out_dtype, struct CUstream_st* stream) {
-    // ---- arguments (host only, nothing touches the device) ----
-    if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16) return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "in_dtype");
-    if (out_dtype != GEMM_F32 && out_dtype != GEMM_F16 && out_dtype != GEMM_BF16)
-        return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "out_dtype");
-    if (M < 0 || N < 0 || K < 0) return reject(GEMM_ERR_INVALID_ARG, "negative size");
-    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
-        return reject(GEMM_ERR_INVALID_ARG, "transpose flag not 0/1");
-    if (M == 0 || N == 0) return GEMM_OK;
-    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return reject(GEMM_ERR_TOO_LARGE, "dimension");
-    const bool has_c = beta != 0.0f;
-    const int osz = elem_size(out_dtype);
-    if (!D) return reject(GEMM_ERR_INVALID_ARG, "D is NULL");
-    if (ldd < N) return reject(GEMM_ERR_INVALID_ARG, "ldd < N");
-    if (has_c) {
-        if (!C) return reject(GEMM_ERR_INVALID_ARG, "C is NULL with beta != 0");
-        if (ldc < N) return reject(GEMM_ERR_INVALID_ARG, "ldc < N");
-    }
-    if (K > 0) {
-        if (!A || !B) return reject(GEMM_ERR_INVALID_ARG, "A or B is NULL");
-        if (lda < (transA ? M : K)) return reject(GEMM_ERR_INVALID_ARG, "lda too small");
-        if (ldb < (transB ? K : N)) return reject(GEMM_ERR_INVALID_ARG, "ldb too small");
-        if (lda * 2 >= kMaxStrideBytes || ldb * 2 >= kMaxStrideBytes) return reject(GEMM_ERR_TOO_LARGE, "stride");
-        if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u)
-            return reject(GEMM_ERR_MISALIGNED, "A or B not 2-byte aligned");
-    }
-    if (ldd * osz >= kMaxStrideBytes || (has_c && ldc * osz >= kMaxStrideBytes))
-        return reject(GEMM_ERR_TOO_LARGE, "stride");
-    if (reinterpret_cast<uintptr_t>(D) & (uintptr_t)(osz - 1)) return reject(GEMM_ERR_MISALIGNED, "D not element-aligned");
-    if (has_c && (reinterpret_cast<uintptr_t>(C) & (uintptr_t)(osz - 1)))
-        return reject(GEMM_ERR_MISALIGNED, "C not element-aligned");
-    {
-        uintptr_t d0, d1;
-        byte_range(D, M, N, ldd, osz, &d0, &d1);
-        if (K > 0) {
-            uintptr_t a0, a1, b0, b1;
-            byte_range(A, transA ? K : M, transA ? M : K, lda, 2, &a0, &a1);
-            byte_range(B, transB ? N : K, transB ? K : N, ldb, 2, &b0, &b1);
-            if (overlaps(d0, d1, a0, a1) || overlaps(d0, d1, b0, b1))
-                return reject(GEMM_ERR_ALIAS, "D overlaps A or B");
-        }
-        if (has_c && !(C == D && ldc == ldd)) {
-            uintptr_t c0, c1;
-            byte_range(C, M, N, ldc, osz, &c0, &c1);
-            if (overlaps(d0, d1, c0, c1)) return reject(GEMM_ERR_ALIAS, "D overlaps C (other than C == D, ldc == ldd)");
-        }
-    }
+    int rc = validate(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, beta, in_dtype, out_dtype);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
 
     // ---- device ----
     int dev = 0;
@@ -619,89 +760,42 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
         return reject(GEMM_ERR_CUDA, "cudaGetDevice");
     }
     DeviceState* ds = nullptr;
-    int rc = device_state(dev, &ds);
-    if (rc != GEMM_OK) return reject(rc, "device set-up");
+    if ((rc = device_state(dev, &ds)) != GEMM_OK) return reject(rc, "device set-up");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-
-    const int out_kind = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
+    const bool has_c = beta != 0.0f;
     if (K == 0) {
         GEMM_LOGF("M=%lld N=%lld K=0: epilogue-only kernel", (long long)M, (long long)N);
-        cudaError_t e = gb300::launch_k0(out_kind, D, has_c ? C : nullptr, (int)M, (int)N, ldc, ldd, alpha, beta,
-                                         has_c ? 1 : 0, ds->num_sms, s);
-        if (e != cudaSuccess) return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
-        return GEMM_OK;
+        return launch_k0_or_reject(out_dtype, D, C, M, N, ldc, ldd, alpha, beta, ds->num_sms, s);
     }
-    const bool tma_ok = tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, osz, has_c);
-    Route route = route_for(tma_ok, true, M, N, K);
+    const bool f8 = is_f8(in_dtype);
+    const bool direct_ok =
+        tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, elem_size(in_dtype), elem_size(out_dtype), has_c) &&
+        operand_majors_ok(in_dtype, transA, transB);
+    Route route = route_for(direct_ok, f8, true, M, N, K);
     if (route == kRouteRepack) {
-        GEMM_LOGF("M=%lld N=%lld K=%lld: layout not 16-byte aligned, repacked for the tcgen05 kernel", (long long)M,
+        GEMM_LOGF("M=%lld N=%lld K=%lld: layout the tcgen05 kernel cannot take as it is, repacked", (long long)M,
                   (long long)N, (long long)K);
         rc = gemm_repacked(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype, out_dtype,
                            dev, s);
         if (rc != kNoWorkspace) return rc == GEMM_OK ? GEMM_OK : reject(rc, "repacked call");
-        route = kRouteSync;   // no workspace to be had: the kernel that needs none
+        route = f8 ? kRouteNone : kRouteSync;   // no workspace to be had
     }
+    if (route == kRouteNone) return reject(GEMM_ERR_UNSUPPORTED_LAYOUT, "8-bit operands: no workspace for repacking");
     if (route == kRouteSync) {
         GEMM_LOGF("M=%lld N=%lld K=%lld trans=%d%d: mma.sync kernel (%s)", (long long)M, (long long)N, (long long)K,
-                  transA, transB, tma_ok ? "small problem" : "layout not 16-byte aligned");
-        cudaError_t e = launch_sync(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype,
-                                    out_kind, has_c, s);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
-        }
-        return GEMM_OK;
+                  transA, transB, direct_ok ? "small problem" : "layout not 16-byte aligned");
+        return launch_sync_or_reject(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype,
+                                     out_dtype, s);
     }
 
-    if ((rc = get_encoder()) != GEMM_OK) return reject(rc, "cuTensorMapEncodeTiled unavailable");
-    const Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype);
+    const Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, f8 ? 1 : 0);
     TcgenLaunch L;
-    std::memset(&L, 0, sizeof(L));
-    const uint32_t bk = (uint32_t)gb300::tcgen05_block_k();
-    // A: K-major (transA = 0) as [M rows][K], else MN-major as [K rows][M]
-    if (!transA)
-        rc = encode_2d(&L.a, in_dtype, A, K, M, lda, bk, (uint32_t)gb300::tcgen05_load_rows_a());
-    else
-        rc = encode_2d(&L.a, in_dtype, A, M, K, lda, 64, bk);
-    if (rc != GEMM_OK) return reject(rc, "tensor map A");
-    // B: K-major (transB = 1) as [N rows][K], else MN-major as [K rows][N]
-    if (transB)
-        rc = encode_2d(&L.b, in_dtype, B, K, N, ldb, bk, (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n));
-    else
-        rc = encode_2d(&L.b, in_dtype, B, N, K, ldb, 64, bk);
-    if (rc != GEMM_OK) return reject(rc, "tensor map B");
-    const uint32_t chunk_cols = 128u / (uint32_t)osz;
-    // TMA stores write whole 16-byte pieces of a row, even past the tensor's
-    // last column: D's map stops at the last whole piece (n_tma) and the
-    // kernel stores columns [n_tma, N) element by element.
-    const int64_t vec = 16 / osz;
-    const int64_t n_tma = (N / vec) * vec;
-    if ((rc = encode_2d(&L.d, out_dtype, D, n_tma > 0 ? n_tma : N, M, ldd, chunk_cols, 32)) != GEMM_OK)
-        return reject(rc, "tensor map D");
-    if (has_c && (rc = encode_2d(&L.c, out_dtype, C, N, M, ldc, chunk_cols, 32)) != GEMM_OK)
-        return reject(rc, "tensor map C");
+    if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
+                               in_dtype, out_dtype)) != GEMM_OK)
+        return reject(rc, "tensor maps");
     GemmParams& p = L.p;
-    p.M = (int32_t)M;
-    p.N = (int32_t)N;
-    p.K = (int32_t)K;
-    p.num_m_tiles = pl.num_m;
-    p.num_n_tiles = pl.num_n;
-    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair);
-    p.num_k_blocks = (int32_t)((K + stage_k - 1) / stage_k);   // pipeline stages per tile
-    p.num_tiles = pl.num_tiles;
-    p.group_m = group_m_setting();
-    p.alpha = alpha;
-    p.beta = beta;
-    p.a_mn_major = transA ? 1 : 0;
-    p.b_mn_major = transB ? 0 : 1;
-    p.has_c = has_c ? 1 : 0;
-    p.timeout_ns = wait_timeout_ns();
-    p.skip_first_stage = skip_first_stage_setting();
-    p.n_tma = (int32_t)n_tma;
-    p.d_ptr = D;
-    p.ldd = ldd;
-    tuning(p);
     p.status = ds->d_status;
+    p.skip_first_stage = skip_first_stage_setting();
     if (pl.sk_tiles > 0) {
         void* ws = nullptr;
         uint32_t epoch = 0;
@@ -713,30 +807,12 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
         p.ws_counters = static_cast<uint32_t*>(ws);
         p.ws_partials = static_cast<char*>(ws) + ((int64_t)pl.sk_tiles * 2 * 4 + 255) / 256 * 256;
     }
-    // tcgen05 instruction descriptor, kind::f16: D format f32 (bits 4-5 = 1),
-    // A / B format (bits 7-9, 10-12: 0 = f16, 1 = bf16), A / B major
-    // (bits 15, 16: 1 = MN-major), N >> 3 (bits 17-22), M >> 4 (bits 24-28).
-    const uint32_t fmt = in_dtype == GEMM_BF16 ? 1u : 0u;
-    const uint32_t mma_m = (uint32_t)pl.tile_m;   // 128 (one SM) or 256 (CTA pair)
-    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)p.a_mn_major << 15) |
-              ((uint32_t)p.b_mn_major << 16) | (((uint32_t)pl.tile_n >> 3) << 17) | ((mma_m >> 4) << 24);
-    L.pair = pl.pair;
-    L.tile_n = pl.tile_n;
-    L.out = out_kind;
-    L.grid = pl.grid;
-    L.epi_warps = pl.epi_warps;
-
     GEMM_LOGF("M=%lld N=%lld K=%lld trans=%d%d in=%d out=%d beta%s0: %s tiles %dx%d (%d), grid %d, smem %d, "
               "%d epilogue warps, %d stages, %d stream-K tiles (<= %d contributors)",
               (long long)M, (long long)N, (long long)K, transA, transB, in_dtype, out_dtype, has_c ? "!=" : "==",
               pl.pair ? "cta-pair" : "1-cta", pl.tile_m, pl.tile_n, pl.num_tiles, pl.grid, pl.smem, pl.epi_warps,
               pl.stages, pl.sk_tiles, pl.max_nc);
-    cudaError_t e = gb300::launch_tcgen05(L, s);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
-    }
-    return GEMM_OK;
+    return launch_described(L, s);
 }
 
 int gemm_poll_device_error(struct CUstream_st* stream, int* info) {
@@ -822,63 +898,22 @@ int noalloc_device_state(int dev, NoAllocState** out) {
     return st.status;
 }
 
-// The argument rules of gemm(), checked without touching the device.
-int noalloc_validate(const void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
-                     int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float beta,
-                     int in_dtype, int out_dtype) {
-    if (in_dtype != GEMM_F16 && in_dtype != GEMM_BF16) return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "in_dtype");
-    if (out_dtype != GEMM_F32 && out_dtype != GEMM_F16 && out_dtype != GEMM_BF16)
-        return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "out_dtype");
-    if (M < 0 || N < 0 || K < 0) return reject(GEMM_ERR_INVALID_ARG, "negative size");
-    if ((transA != 0 && transA != 1) || (transB != 0 && transB != 1))
-        return reject(GEMM_ERR_INVALID_ARG, "transpose flag not 0/1");
-    if (M == 0 || N == 0) return GEMM_OK;
-    if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return reject(GEMM_ERR_TOO_LARGE, "dimension");
-    const bool has_c = beta != 0.0f;
-    const int osz = elem_size(out_dtype);
-    if (!D) return reject(GEMM_ERR_INVALID_ARG, "D is NULL");
-    if (ldd < N) return reject(GEMM_ERR_INVALID_ARG, "ldd < N");
-    if (has_c) {
-        if (!C) return reject(GEMM_ERR_INVALID_ARG, "C is NULL with beta != 0");
-        if (ldc < N) return reject(GEMM_ERR_INVALID_ARG, "ldc < N");
-    }
-    if (K > 0) {
-        if (!A || !B) return reject(GEMM_ERR_INVALID_ARG, "A or B is NULL");
-        if (lda < (transA ? M : K)) return reject(GEMM_ERR_INVALID_ARG, "lda too small");
-        if (ldb < (transB ? K : N)) return reject(GEMM_ERR_INVALID_ARG, "ldb too small");
-        if (lda * 2 >= kMaxStrideBytes || ldb * 2 >= kMaxStrideBytes) return reject(GEMM_ERR_TOO_LARGE, "stride");
-        if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B)) & 1u)
-            return reject(GEMM_ERR_MISALIGNED, "A or B not 2-byte aligned");
-    }
-    if (ldd * osz >= kMaxStrideBytes || (has_c && ldc * osz >= kMaxStrideBytes))
-        return reject(GEMM_ERR_TOO_LARGE, "stride");
-    if (reinterpret_cast<uintptr_t>(D) & (uintptr_t)(osz - 1)) return reject(GEMM_ERR_MISALIGNED, "D not element-aligned");
-    if (has_c && (reinterpret_cast<uintptr_t>(C) & (uintptr_t)(osz - 1)))
-        return reject(GEMM_ERR_MISALIGNED, "C not element-aligned");
-    uintptr_t d0, d1;
-    byte_range(D, M, N, ldd, osz, &d0, &d1);
-    if (K > 0) {
-        uintptr_t a0, a1, b0, b1;
-        byte_range(A, transA ? K : M, transA ? M : K, lda, 2, &a0, &a1);
-        byte_range(B, transB ? N : K, transB ? K : N, ldb, 2, &b0, &b1);
-        if (overlaps(d0, d1, a0, a1) || overlaps(d0, d1, b0, b1)) return reject(GEMM_ERR_ALIAS, "D overlaps A or B");
-    }
-    if (has_c && !(C == D && ldc == ldd)) {
-        uintptr_t c0, c1;
-        byte_range(C, M, N, ldc, osz, &c0, &c1);
-        if (overlaps(d0, d1, c0, c1)) return reject(GEMM_ERR_ALIAS, "D overlaps C (other than C == D, ldc == ldd)");
-    }
-    return GEMM_OK;
-}
-
 }  // namespace
 
 extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N,
                                      int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA,
                                      int transB, float alpha, float beta, int in_dtype, int out_dtype,
                                      struct CUstream_st* stream) {
-    int rc = noalloc_validate(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, beta, in_dtype, out_dtype);
+    int rc = validate(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, beta, in_dtype, out_dtype);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    const bool has_c = beta != 0.0f;
+    const bool f8 = is_f8(in_dtype);
+    const bool direct_ok =
+        tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, elem_size(in_dtype), elem_size(out_dtype), has_c) &&
+        operand_majors_ok(in_dtype, transA, transB);
+    const Route route = K == 0 ? kRouteTcgen05 : route_for(direct_ok, f8, false, M, N, K);
+    if (route == kRouteNone)   // decided on the host: nothing enqueued
+        return reject(GEMM_ERR_UNSUPPORTED_LAYOUT, "8-bit operands must be K-major and 16-byte aligned here");
     // The only scratch is the 16-byte status record, whatever the sizes;
     // refuse anything that would not fit the static array.
     if ((int)sizeof(DeviceStatus) > gb300::noalloc_scratch_bytes())
@@ -891,91 +926,25 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
     NoAllocState* ns = nullptr;
     if ((rc = noalloc_device_state(dev, &ns)) != GEMM_OK) return reject(rc, "device set-up (no-alloc)");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-
-    const bool has_c = beta != 0.0f;
-    const int osz = elem_size(out_dtype);
-    if (K == 0) {   // epilogue-only kernel: no scratch at all
-        const int ok = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
-        cudaError_t e = gb300::launch_k0(ok, D, has_c ? C : nullptr, (int)M, (int)N, ldc, ldd, alpha, beta,
-                                         has_c ? 1 : 0, ns->num_sms, s);
-        if (e != cudaSuccess) return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
-        return GEMM_OK;
-    }
-    if (route_for(tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, osz, has_c), false, M, N, K) == kRouteSync) {
-        const int ok = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
-        cudaError_t e = launch_sync(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype, ok,
-                                    has_c, s);
-        if (e != cudaSuccess) {
-            cudaGetLastError();
-            return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
-        }
-        return GEMM_OK;
-    }
-    if ((rc = get_encoder()) != GEMM_OK) return reject(rc, "cuTensorMapEncodeTiled unavailable");
-    const Plan pl = make_plan(M, N, K, ns->num_sms, false, out_dtype);   // no workspace: data-parallel
+    if (K == 0)   // epilogue-only kernel: no scratch at all
+        return launch_k0_or_reject(out_dtype, D, C, M, N, ldc, ldd, alpha, beta, ns->num_sms, s);
+    if (route == kRouteSync)   // needs no scratch either
+        return launch_sync_or_reject(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype,
+                                     out_dtype, s);
+    const Plan pl = make_plan(M, N, K, ns->num_sms, false, out_dtype, f8 ? 1 : 0);   // no workspace: data-parallel
     TcgenLaunch L;
-    std::memset(&L, 0, sizeof(L));
-    const uint32_t bk = (uint32_t)gb300::tcgen05_block_k();
-    if (!transA)
-        rc = encode_2d(&L.a, in_dtype, A, K, M, lda, bk, (uint32_t)gb300::tcgen05_load_rows_a());
-    else
-        rc = encode_2d(&L.a, in_dtype, A, M, K, lda, 64, bk);
-    if (rc != GEMM_OK) return reject(rc, "tensor map A");
-    if (transB)
-        rc = encode_2d(&L.b, in_dtype, B, K, N, ldb, bk, (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n));
-    else
-        rc = encode_2d(&L.b, in_dtype, B, N, K, ldb, 64, bk);
-    if (rc != GEMM_OK) return reject(rc, "tensor map B");
-    const uint32_t chunk_cols = 128u / (uint32_t)osz;
-    const int64_t vec = 16 / osz;
-    const int64_t n_tma = (N / vec) * vec;
-    if ((rc = encode_2d(&L.d, out_dtype, D, n_tma > 0 ? n_tma : N, M, ldd, chunk_cols, 32)) != GEMM_OK)
-        return reject(rc, "tensor map D");
-    if (has_c && (rc = encode_2d(&L.c, out_dtype, C, N, M, ldc, chunk_cols, 32)) != GEMM_OK)
-        return reject(rc, "tensor map C");
-    GemmParams& p = L.p;
-    p.M = (int32_t)M;
-    p.N = (int32_t)N;
-    p.K = (int32_t)K;
-    p.num_m_tiles = pl.num_m;
-    p.num_n_tiles = pl.num_n;
-    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair);
-    p.num_k_blocks = (int32_t)((K + stage_k - 1) / stage_k);   // pipeline stages per tile
-    p.num_tiles = pl.num_tiles;
-    p.group_m = group_m_setting();
-    p.alpha = alpha;
-    p.beta = beta;
-    p.a_mn_major = transA ? 1 : 0;
-    p.b_mn_major = transB ? 0 : 1;
-    p.has_c = has_c ? 1 : 0;
-    p.timeout_ns = wait_timeout_ns();
-    p.skip_first_stage = 0;
-    p.status = ns->scratch_status;
-    p.n_tma = (int32_t)n_tma;
-    p.d_ptr = D;
-    p.ldd = ldd;
-    tuning(p);
-    const uint32_t fmt = in_dtype == GEMM_BF16 ? 1u : 0u;
-    p.idesc = (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)p.a_mn_major << 15) |
-              ((uint32_t)p.b_mn_major << 16) | (((uint32_t)pl.tile_n >> 3) << 17) | (((uint32_t)pl.tile_m >> 4) << 24);
-    L.pair = pl.pair;
-    L.tile_n = pl.tile_n;
-    L.out = out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
-    L.grid = pl.grid;
-    L.epi_warps = pl.epi_warps;
-
+    if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
+                               in_dtype, out_dtype)) != GEMM_OK)
+        return reject(rc, "tensor maps");
+    L.p.status = ns->scratch_status;
+    L.p.skip_first_stage = 0;
     // The status record must start each call at zero (the kernel records
     // only the first wait that gives up); stream-ordered, allocates nothing.
-    if (cudaMemsetAsync(p.status, 0, sizeof(DeviceStatus), s) != cudaSuccess) {
+    if (cudaMemsetAsync(L.p.status, 0, sizeof(DeviceStatus), s) != cudaSuccess) {
         cudaGetLastError();
         return reject(GEMM_ERR_CUDA, "clearing the static status record");
     }
     GEMM_LOGF("no-alloc: M=%lld N=%lld K=%lld: %s tiles %dx%d (%d), grid %d", (long long)M, (long long)N,
               (long long)K, pl.pair ? "cta-pair" : "1-cta", pl.tile_m, pl.tile_n, pl.num_tiles, pl.grid);
-    cudaError_t e = gb300::launch_tcgen05(L, s);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
-    }
-    return GEMM_OK;
+    return launch_described(L, s);
 }

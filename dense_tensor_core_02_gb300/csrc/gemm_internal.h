@@ -1,5 +1,6 @@
 // Internal interface between the C-ABI host code (gemm_api.cpp) and the
-// sm_103a kernels (gemm_sm103.cu).
+// sm_103a kernels (gemm_tcgen05.cuh instantiated by gemm_sm103.cu and
+// gemm_sm103_f8.cu; gemm_mma_sync.cu).
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -24,6 +25,7 @@ struct TcgenLaunch {
     int grid;                 // CTAs (a multiple of 2 for the pair kernel)
     int epi_warps;            // 4 or 8 epilogue warps
     int tile_n;               // 256, or 64 for the narrow single-CTA tiles
+    int f8;                   // 1: E4M3 / E5M2 operands (kind::f8f6f4), K-major only
 };
 
 // Arguments of the warp-level mma.sync path (gemm_mma_sync.cu): any
@@ -44,12 +46,18 @@ struct SyncParams {
 cudaError_t launch_mma_sync(const SyncParams& p, cudaStream_t stream);
 
 // dst[r * ldd + c] = src[r * lds + c] for r < rows, c < cols; elements of
-// elem_bytes (2 or 4) bytes, any element-aligned strides.
+// elem_bytes (1, 2 or 4) bytes, any element-aligned strides.
 cudaError_t launch_copy2d(void* dst, int64_t ldd, const void* src, int64_t lds, int64_t rows, int64_t cols,
                           int elem_bytes, cudaStream_t stream);
+// dst[c * ldd + r] = src[r * lds + c] (dst holds the cols x rows transpose);
+// elements of 1 or 2 bytes.
+cudaError_t launch_transpose2d(void* dst, int64_t ldd, const void* src, int64_t lds, int64_t rows, int64_t cols,
+                               int elem_bytes, cudaStream_t stream);
 
 cudaError_t prepare_kernels_on_current_device();
 cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream);
+cudaError_t prepare_kernels_f8();                                          // gemm_sm103_f8.cu
+cudaError_t launch_tcgen05_f8(const TcgenLaunch& L, cudaStream_t stream);  // gemm_sm103_f8.cu
 cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,
                       float beta, int has_c, int num_sms, cudaStream_t stream);
 
@@ -61,8 +69,8 @@ int noalloc_scratch_bytes();
 int tcgen05_tile_m(int pair);      // D rows per tile
 int tcgen05_wide_n();              // D columns per throughput tile
 int tcgen05_narrow_n();            // D columns per narrow tile (single CTA, 4 epilogue warps)
-int tcgen05_block_k();             // K of one TMA operand box (one 128-byte swizzle row)
-int tcgen05_stage_k(int pair);     // K per pipeline stage
+int tcgen05_block_k(int f8);       // K of one TMA operand box (one 128-byte swizzle row)
+int tcgen05_stage_k(int pair, int f8);   // K per pipeline stage
 int tcgen05_load_rows_a();         // A rows (M) one CTA stages per stage
 int tcgen05_load_rows_b(int pair, int tile_n);   // B rows (N) one CTA stages per stage
 int tcgen05_smem_bytes(int pair, int epi_warps, int tile_n);

@@ -234,6 +234,31 @@ __global__ void copy2d_kernel(T* dst, int64_t ldd, const T* src, int64_t lds, in
             dst[r * ldd + c] = src[r * lds + c];
 }
 
+// dst[c * ldd + r] = src[r * lds + c] for r < rows, c < cols: the
+// repacking step that turns an 8-bit operand stored MN-major into the
+// K-major copy the tcgen05 kernel stages.  32 x 32 tiles through shared
+// memory, so that both the reads and the writes walk rows.
+constexpr int kTT = 32;
+template <typename T>
+__global__ void transpose2d_kernel(T* dst, int64_t ldd, const T* src, int64_t lds, int64_t rows, int64_t cols) {
+    __shared__ T tile[kTT][kTT + 1];
+    const int64_t tiles_r = (rows + kTT - 1) / kTT, tiles_c = (cols + kTT - 1) / kTT;
+    for (int64_t br = blockIdx.y; br < tiles_r; br += gridDim.y)
+        for (int64_t bc = blockIdx.x; bc < tiles_c; bc += gridDim.x) {
+            const int64_t r0 = br * kTT, c0 = bc * kTT;
+            for (int i = threadIdx.y; i < kTT; i += blockDim.y) {
+                const int64_t r = r0 + i, c = c0 + threadIdx.x;
+                if (r < rows && c < cols) tile[i][threadIdx.x] = src[r * lds + c];
+            }
+            __syncthreads();
+            for (int i = threadIdx.y; i < kTT; i += blockDim.y) {
+                const int64_t c = c0 + i, r = r0 + threadIdx.x;   // dst row c, column r
+                if (r < rows && c < cols) dst[c * ldd + r] = tile[threadIdx.x][i];
+            }
+            __syncthreads();
+        }
+}
+
 }  // namespace
 
 cudaError_t launch_mma_sync(const SyncParams& p, cudaStream_t stream) {
@@ -252,9 +277,27 @@ cudaError_t launch_copy2d(void* dst, int64_t ldd, const void* src, int64_t lds, 
     if (elem_bytes == 4)
         copy2d_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(static_cast<uint32_t*>(dst), ldd,
                                                                static_cast<const uint32_t*>(src), lds, rows, cols);
-    else
+    else if (elem_bytes == 2)
         copy2d_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(static_cast<uint16_t*>(dst), ldd,
                                                                static_cast<const uint16_t*>(src), lds, rows, cols);
+    else
+        copy2d_kernel<uint8_t><<<grid, kThreads, 0, stream>>>(static_cast<uint8_t*>(dst), ldd,
+                                                              static_cast<const uint8_t*>(src), lds, rows, cols);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose2d(void* dst, int64_t ldd, const void* src, int64_t lds, int64_t rows, int64_t cols,
+                               int elem_bytes, cudaStream_t stream) {
+    if (rows <= 0 || cols <= 0) return cudaSuccess;
+    const int64_t tr = (rows + kTT - 1) / kTT, tc = (cols + kTT - 1) / kTT;
+    const dim3 grid((unsigned)(tc < 65535 ? tc : 65535), (unsigned)(tr < 65535 ? tr : 65535));
+    const dim3 block(kTT, kTT / 4);
+    if (elem_bytes == 2)
+        transpose2d_kernel<uint16_t><<<grid, block, 0, stream>>>(static_cast<uint16_t*>(dst), ldd,
+                                                                 static_cast<const uint16_t*>(src), lds, rows, cols);
+    else
+        transpose2d_kernel<uint8_t><<<grid, block, 0, stream>>>(static_cast<uint8_t*>(dst), ldd,
+                                                                static_cast<const uint8_t*>(src), lds, rows, cols);
     return cudaGetLastError();
 }
 

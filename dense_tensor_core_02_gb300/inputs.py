@@ -7,7 +7,8 @@ CPU oracle can be fed from it.
 Operand rounding follows the Phobos "@tensorcore" page, section "The
 forms" (operands are rounded to f16 before the tensor cores see them):
 values are drawn in fp32 and rounded once, round-to-nearest-even, by
-``Tensor.half()`` / ``Tensor.bfloat16()``.  Storage is row-major; A is
+``Tensor.half()`` / ``Tensor.bfloat16()`` (``Tensor.to(torch.float8_*)``,
+saturating to the largest finite value, for the 8-bit operands).  Storage is row-major; A is
 stored [M, K] (or [K, M] when transposed), B [K, N] (or [N, K]), C and D
 [M, N].
 """
@@ -18,7 +19,9 @@ import math
 
 import torch
 
-_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+_TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+                "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+_ELEM_BYTES = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -54,8 +57,8 @@ class GemmCase:
     @property
     def algorithmic_bytes(self) -> int:
         """Each operand read once, C read once when beta != 0, D written once."""
-        isz = 2
-        osz = 4 if self.out_dtype == "f32" else 2
+        isz = _ELEM_BYTES[self.in_dtype]
+        osz = _ELEM_BYTES[self.out_dtype]
         return isz * (self.M * self.K + self.K * self.N) + osz * self.M * self.N * (1 + (self.beta != 0))
 
 
@@ -88,7 +91,7 @@ def integer_matrix(shape, lo, hi, seed, dtype="f16"):
     """Integer-valued matrix with entries uniform on [lo, hi], seeded."""
     gen = torch.Generator().manual_seed(seed)
     x = torch.randint(lo, hi + 1, shape, generator=gen, dtype=torch.int32)
-    return x.to(_TORCH_DTYPE[dtype])
+    return x.float().to(_TORCH_DTYPE[dtype])
 
 
 # The workloads the benchmark and the parity tests run, in a fixed order; the
@@ -110,6 +113,11 @@ def _cases():
         GemmCase("sweep_8192x8192_K16384_f16", 8192, 8192, 16384, "f16"),
         GemmCase("tall_skinny_32768x256x4096_f16", 32768, 256, 4096, "f16"),
         GemmCase("unaligned_1000_f16", 1000, 1000, 1000, "f16"),
+        # 8-bit operands (the tcgen05 path's fp8 precisions, TIRx gemm guide
+        # section 七), K-major as the kind::f8f6f4 kernel reads them in place
+        GemmCase("gemm_8192_e4m3_transB", k8192, k8192, k8192, "e4m3", transB=1),
+        GemmCase("gemm_4096_e5m2_transB_beta1", 4096, 4096, 4096, "e5m2", dist="uniform",
+                 transB=1, alpha=1.0, beta=1.0, c_dist="uniform"),
     ]
     return [dataclasses.replace(c, seed=1000 + i + 1) for i, c in enumerate(rows)]
 

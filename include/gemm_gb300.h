@@ -20,8 +20,10 @@
  *   D  row-major [M, N], ldd = row stride
  * Leading dimensions are in elements.
  *
- * Precision: A and B are both in_dtype (GEMM_F16 or GEMM_BF16; one dtype
- * for both, so mixed operand types cannot be expressed); products are
+ * Precision: A and B are both in_dtype (GEMM_F16, GEMM_BF16, or the 8-bit
+ * GEMM_E4M3 / GEMM_E5M2 that the TIRx gemm guide lists among the tcgen05
+ * path's precisions, section 七; one dtype for both, so mixed operand types
+ * cannot be expressed); products are
  * accumulated in fp32 on the tensor cores; the epilogue computes
  * fmaf(alpha, acc, beta * c) in fp32 (alpha * acc when beta == 0) and
  * rounds to out_dtype (round-to-nearest-even for 16-bit outputs).  C has
@@ -32,7 +34,10 @@
  * are device pointers valid on the current device.  gemm() enqueues its
  * work on `stream` and returns without synchronising.  The library keeps
  * one small device status block per device (allocated on the first call on
- * that device) and no per-call device memory.  Calls are thread-safe.
+ * that device) and, per (device, stream), workspaces for stream-K partial
+ * sums and repacked operands, allocated when a call first needs them and
+ * grown on demand (growing one synchronises the device).  Calls are
+ * thread-safe.
  *
  * Errors: gemm() returns GEMM_OK or a negative GEMM_ERR_* code.  Every
  * argument error is detected before anything is enqueued, and D is then
@@ -59,7 +64,9 @@ struct CUstream_st; /* = cudaStream_t; NULL is the legacy default stream */
 typedef enum {
     GEMM_F16 = 0,  /* IEEE binary16 */
     GEMM_BF16 = 1, /* bfloat16 */
-    GEMM_F32 = 2   /* IEEE binary32 (outputs only) */
+    GEMM_F32 = 2,  /* IEEE binary32 (outputs only) */
+    GEMM_E4M3 = 3, /* 8-bit float, 1-4-3, bias 7, no infinities, S.1111.111 = NaN (operands only) */
+    GEMM_E5M2 = 4  /* 8-bit float, 1-5-2, bias 15, with infinities and NaNs (operands only) */
 } gemm_dtype_t;
 
 typedef enum {
@@ -72,7 +79,8 @@ typedef enum {
     GEMM_ERR_LAUNCH = -6,            /* the kernel launch was refused */
     GEMM_ERR_CUDA = -7,              /* another CUDA runtime / driver error */
     GEMM_ERR_DEVICE_TIMEOUT = -8,    /* (gemm_poll_device_error) an in-kernel wait gave up */
-    GEMM_ERR_TOO_LARGE = -9          /* a dimension above 2^31 - 1, or a stride above 2^40 bytes */
+    GEMM_ERR_TOO_LARGE = -9,         /* a dimension above 2^31 - 1, or a stride above 2^40 bytes */
+    GEMM_ERR_UNSUPPORTED_LAYOUT = -10 /* 8-bit operands in a layout the call cannot take (see gemm_noalloc) */
 } gemm_status_t;
 
 /*
@@ -87,20 +95,27 @@ typedef enum {
  *   ldd              >= N.
  *   transA, transB   0 or 1 (see the layout above).
  *   alpha, beta      any float; beta == 0.0f selects "C not read".
- *   in_dtype         GEMM_F16 or GEMM_BF16 (A and B).
+ *   in_dtype         GEMM_F16, GEMM_BF16, GEMM_E4M3 or GEMM_E5M2 (A and B).
  *   out_dtype        GEMM_F32, GEMM_F16 or GEMM_BF16 (C and D).
  *   stream           CUDA stream of the current device.
  *
- * Alignment: each buffer must be aligned to its element size.  Two kernels
- * compute the product: the tcgen05 kernel (TMA copies, tensor-memory
- * accumulators) when A, B, C, D are 16-byte aligned and lda*2, ldb*2,
- * ldc*sizeof(out), ldd*sizeof(out) are multiples of 16 bytes (TMA's rule),
- * and a warp-level mma.sync kernel (element-wise loads) for any other
- * layout and for problems with M*N*K <= 2^15, where the tcgen05 kernel's
- * set-up outweighs the arithmetic.  Both accumulate in fp32 and give the
- * same results within the documented tolerance.  GEMM_PATH=tcgen05 or
- * mma_sync forces one (tcgen05 only where TMA's rule holds);
- * GEMM_SYNC_MAX_WORK sets the size threshold.
+ * Alignment: each buffer must be aligned to its element size; any such
+ * layout is computed.  Kernels:
+ *   - the tcgen05 kernel (TMA copies, tensor-memory accumulators) on the
+ *     caller's buffers when A, B, C, D are 16-byte aligned and lda, ldb,
+ *     ldc, ldd times their element sizes are multiples of 16 bytes (TMA's
+ *     rule), and 8-bit operands are K-major (A stored [M, K], transA = 0;
+ *     B stored [N, K], transB = 1);
+ *   - fp16 / bf16 problems with M*N*K <= 2^15 (GEMM_SYNC_MAX_WORK): a
+ *     warp-level mma.sync kernel, whose set-up is cheaper;
+ *   - other layouts with M*N*K > 2^22 (GEMM_REPACK_MIN_WORK), and every
+ *     other 8-bit layout: the tcgen05 kernel on workspace copies (operands
+ *     copied into 16-byte-aligned rows, 8-bit MN-major operands transposed
+ *     to K-major, a misaligned D computed in workspace and copied back);
+ *   - the remaining fp16 / bf16 layouts: the mma.sync kernel, which reads
+ *     and writes element by element.
+ * All accumulate in fp32 and agree within the documented tolerance.
+ * GEMM_PATH=tcgen05 or mma_sync forces a kernel where it can run.
  * Returns GEMM_OK or a GEMM_ERR_* code (see gemm_status_t).
  * Setting the environment variable GEMM_LOG=1 prints each call's plan or
  * rejection reason to stderr.
@@ -164,13 +179,14 @@ GEMM_API int gemm_schedule_units(int num_tiles, int iters, int workers, int sk_t
  * that owns all of the device's memory through its own pool or budget,
  * code running where CUDA allocation calls are not permitted (for example
  * from a stream callback), or code that must not add allocations to a
- * process it does not own.  gemm_noalloc() computes exactly what gemm()
- * computes, with the same arguments, rules and return codes, through the
- * same kernels (the tcgen05 kernel without stream-K splitting, whose
- * partial sums would need a workspace; the mma.sync kernel, which needs no
- * scratch, for the layouts and sizes gemm() sends there), but never calls
- * cudaMalloc, cudaFree or any other allocating
- * routine: the kernel's scratch (its 16-byte status record) lives in a
+ * process it does not own.  gemm_noalloc() computes what gemm() computes,
+ * with the same arguments, rules and return codes, through the same
+ * kernels, but never calls cudaMalloc, cudaFree or any other allocating
+ * routine.  Without workspace it does not split tiles along K (stream-K)
+ * and does not repack: fp16 / bf16 layouts off TMA's 16-byte grid run on
+ * the mma.sync kernel whatever their size, and 8-bit operands must already
+ * be K-major and 16-byte aligned (else GEMM_ERR_UNSUPPORTED_LAYOUT, before
+ * anything is enqueued).  The kernel's scratch (its 16-byte status record) lives in a
  * fixed 256-byte array inside the library, which every GPU that loads the
  * library holds until the process exits.  The scratch does not grow with
  * the problem, so no problem size exceeds it; a build whose record did not

@@ -18,8 +18,9 @@ import torch
 import oracle.oracle as oracle
 from dense_tensor_core_02_gb300 import binding
 
-CODE = {"f16": 0, "bf16": 1, "f32": 2}
-TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+CODE = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4}
+TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.float8_e4m3fn,
+         "e5m2": torch.float8_e5m2}
 ORACLE_THREADS = max(1, min(16, len(os.sched_getaffinity(0))))
 
 
@@ -137,7 +138,7 @@ def assert_exact(d_gpu, d_ref, what=""):
 
 def int_matrix(shape, lo, hi, dtype, seed):
     g = torch.Generator().manual_seed(seed)
-    return torch.randint(lo, hi + 1, shape, generator=g, dtype=torch.int32).to(TORCH[dtype])
+    return torch.randint(lo, hi + 1, shape, generator=g, dtype=torch.int32).float().to(TORCH[dtype])
 
 
 def normal_matrix(shape, dtype, seed, std=1.0):

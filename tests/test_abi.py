@@ -45,7 +45,7 @@ def test_status_strings(lib):
     names = {0: "GEMM_OK", -1: "GEMM_ERR_INVALID_ARG", -2: "GEMM_ERR_UNSUPPORTED_DTYPE",
              -3: "GEMM_ERR_MISALIGNED", -4: "GEMM_ERR_ALIAS", -5: "GEMM_ERR_ARCH",
              -6: "GEMM_ERR_LAUNCH", -7: "GEMM_ERR_CUDA", -8: "GEMM_ERR_DEVICE_TIMEOUT",
-             -9: "GEMM_ERR_TOO_LARGE"}
+             -9: "GEMM_ERR_TOO_LARGE", -10: "GEMM_ERR_UNSUPPORTED_LAYOUT"}
     for code, name in names.items():
         assert binding.gemm_status_string(code) == name
     assert binding.gemm_status_string(12345) == "GEMM_ERR_UNKNOWN"
@@ -72,6 +72,7 @@ def _call(**kw):
 REJECTIONS = [
     (dict(in_dtype=2), -2),                 # fp32 operands
     (dict(in_dtype=7), -2),
+    (dict(in_dtype=5), -2),
     (dict(out_dtype=9), -2),
     (dict(M=-1), -1),
     (dict(K=-3), -1),
@@ -127,6 +128,30 @@ def test_element_aligned_layouts_pass_validation(lib, kw):
     # call proceeds to the device and fails on a CPU-only box.
     rc = _call(**kw)
     assert rc in (0, -7, -5), rc
+
+
+@pytest.mark.parametrize("kw", [dict(in_dtype=3, A=A_ + 1, lda=65), dict(in_dtype=4, transB=0, ldb=64),
+                                dict(in_dtype=3, transA=1, B=B_ + 7)])
+def test_fp8_layouts_pass_validation(lib, kw):
+    # 8-bit operands need only byte alignment: gemm() repacks what the
+    # tcgen05 kernel cannot read in place, so these reach the device.
+    rc = _call(**kw)
+    assert rc in (0, -7, -5), rc
+
+
+def _call_noalloc(**kw):
+    a = dict(OK_ARGS)
+    a.update(kw)
+    return binding.gemm_noalloc(a["D"], a["A"], a["B"], a["C"], a["M"], a["N"], a["K"], a["lda"], a["ldb"],
+                                a["ldc"], a["ldd"], a["transA"], a["transB"], a["alpha"], a["beta"],
+                                a["in_dtype"], a["out_dtype"], 0)
+
+
+@pytest.mark.parametrize("kw", [dict(in_dtype=3, transB=0), dict(in_dtype=4, transA=1, transB=1),
+                                dict(in_dtype=3, transB=1, A=A_ + 8), dict(in_dtype=4, transB=1, lda=72)])
+def test_noalloc_fp8_needs_k_major_aligned_operands(lib, kw):
+    """Without workspace nothing can be repacked: rejected on the host."""
+    assert _call_noalloc(**kw) == -10
 
 
 def test_k0_needs_no_operands(lib):
