@@ -54,6 +54,8 @@ def load_library():
             lib.gemm_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64)]
             lib.gemm_noalloc.restype = i32
             lib.gemm_noalloc.argtypes = list(lib.gemm.argtypes)
+            lib.gemm_host.restype = i32
+            lib.gemm_host.argtypes = list(lib.gemm.argtypes)
             lib.gemm_schedule_units.restype = i32
             lib.gemm_schedule_units.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(i32), i32]
             _lib = lib
@@ -99,6 +101,17 @@ def gemm_noalloc(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha,
     return lib.gemm_noalloc(_addr(D), _addr(A), _addr(B), _addr(C), int(M), int(N), int(K), int(lda),
                             int(ldb), int(ldc), int(ldd), int(transA), int(transB), float(alpha),
                             float(beta), int(in_dtype), int(out_dtype), _stream(stream))
+
+
+def gemm_host(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
+              in_dtype, out_dtype, stream=None) -> int:
+    """The C entry point ``gemm_host``: what ``gemm`` computes, with A, B, C
+    and D in host memory (pinned for asynchronous copies); D is complete
+    once ``stream`` has completed the call.  Returns its status."""
+    lib = load_library()
+    return lib.gemm_host(_addr(D), _addr(A), _addr(B), _addr(C), int(M), int(N), int(K), int(lda), int(ldb),
+                         int(ldc), int(ldd), int(transA), int(transB), float(alpha), float(beta), int(in_dtype),
+                         int(out_dtype), _stream(stream))
 
 
 def gemm_status_string(status: int) -> str:

@@ -209,6 +209,37 @@ GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, const void* C,
                           int transA, int transB, float alpha, float beta,
                           int in_dtype, int out_dtype, struct CUstream_st* stream);
 
+/*
+ * gemm_host -- gemm() with A, B, C and D in host memory.
+ *
+ * The pages have no counterpart of this call; it is the entry point for
+ * callers whose matrices live on the host.  Same arguments, layouts, rules
+ * and results as gemm(), except that the four pointers are host pointers
+ * (pinned memory -- cudaMallocHost / cudaHostAlloc / cudaHostRegister --
+ * lets the copies run asynchronously at full speed; pageable memory works,
+ * with copies that block the calling thread).
+ *
+ *   - The library stages the operands in device buffers it owns (one set
+ *     per (device, stream), grown on demand, kept until the process exits)
+ *     and pipelines the work over row panels of D on three streams: the
+ *     host-to-device copies of later panels, the products of earlier ones
+ *     (on `stream`, through gemm()) and the device-to-host copies of
+ *     finished ones overlap.
+ *   - Stream order: the copies of A, B and C start after the work already
+ *     enqueued on `stream`, and D is complete on the host when `stream`
+ *     has completed this call (for example after cudaStreamSynchronize).
+ *     The host buffers must stay unchanged until then.
+ *   - Consecutive calls on one stream are ordered; calls on one stream from
+ *     several threads must be serialised by the caller.
+ * Returns GEMM_OK or a GEMM_ERR_* code; argument errors (including host
+ * buffers that overlap) are detected before anything is enqueued.
+ */
+GEMM_API int gemm_host(void* D, const void* A, const void* B, const void* C,
+                       int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd,
+                       int transA, int transB, float alpha, float beta,
+                       int in_dtype, int out_dtype, struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -154,6 +154,26 @@ def test_noalloc_fp8_needs_k_major_aligned_operands(lib, kw):
     assert _call_noalloc(**kw) == -10
 
 
+def _call_host(**kw):
+    a = dict(OK_ARGS)
+    a.update(kw)
+    return binding.gemm_host(a["D"], a["A"], a["B"], a["C"], a["M"], a["N"], a["K"], a["lda"], a["ldb"],
+                             a["ldc"], a["ldd"], a["transA"], a["transB"], a["alpha"], a["beta"],
+                             a["in_dtype"], a["out_dtype"], 0)
+
+
+@pytest.mark.parametrize("kw,code", [(dict(in_dtype=2), -2), (dict(out_dtype=3), -2), (dict(M=-1), -1),
+                                     (dict(ldd=63), -1), (dict(C=0), -1), (dict(lda=63), -1),
+                                     (dict(A=A_ + 1), -3), (dict(D=A_), -4), (dict(C=D_ + 4), -4),
+                                     (dict(C=D_, ldc=72), -4), (dict(transB=3), -1)])
+def test_host_entry_rejects_before_any_copy(lib, kw, code):
+    assert _call_host(**kw) == code
+
+
+def test_host_entry_empty_is_a_no_op(lib):
+    assert _call_host(M=0) == 0 and _call_host(N=0, D=0) == 0
+
+
 def test_k0_needs_no_operands(lib):
     rc = _call(K=0, A=0, B=0, lda=0, ldb=0)
     assert rc in (0, -7, -5), rc
