@@ -46,6 +46,22 @@ def _rank_info():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def slowest_rank_ms(elapsed_ms, dist=None, device="cpu"):
+    """The job's time: the maximum over ranks of each rank's time (every
+    rank runs its own replica; the job is done when the slowest is)."""
+    if dist is None:
+        return elapsed_ms
+    import torch
+    t = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_step, steps, elapsed_ms):
+    """Whole-job throughput: the flops of all ranks' steps over the job's time."""
+    return world * flops_per_step * steps / (elapsed_ms * 1e-3) / 1e12
+
+
 def _measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -323,13 +339,10 @@ def run_ours(args, case):
     status, info = binding.gemm_poll_device_error(stream)
     if status != 0:
         raise RuntimeError("device status after timing: %s %s" % (binding.gemm_status_string(status), info))
-    if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = slowest_rank_ms(elapsed_ms, dist, dev)
 
     per_launch_ms = elapsed_ms / args.steps
-    value = world * case.flops * args.steps / (elapsed_ms * 1e-3) / 1e12
+    value = job_tflops(world, case.flops, args.steps, elapsed_ms)
 
     # end to end through the C ABI's host-buffer entry point gemm_host():
     # pinned host inputs in, host result out, every copy inside the timed
@@ -364,14 +377,11 @@ def run_ours(args, case):
         torch.cuda.synchronize(dev)
         barrier()
         e2e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([e2e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = slowest_rank_ms(e2e_ms, dist, dev)
         h2d = A.numel() * A.element_size() + B.numel() * B.element_size() + (
             C.numel() * C.element_size() if C is not None else 0)
         d2h = Dd.numel() * Dd.element_size()
-        e2e = {"value": world * case.flops * args.e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e2e = {"value": job_tflops(world, case.flops, args.e2e_steps, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": e2e_ms / args.e2e_steps,
                "api": "gemm_host (pinned host buffers; copies pipelined with the products over row panels)"}
