@@ -25,8 +25,9 @@
 // atom, as the lowering does for K = 8 (mod 16).  Staged columns past K are
 // zero, so the last k16 atom of a ragged K adds nothing for them.
 //
-// CTA tile 64 x 64, 4 warps in a 2 x 2 grid of 32 x 32 warp tiles
-// (2 x 4 atoms each), K slabs of 32 staged in shared memory with padded rows.
+// CTA tile 128 x 128, 8 warps in a 2 x 4 grid of 64 x 32 warp tiles
+// (4 x 4 atoms each); K slabs of 32 double-buffered in shared memory with
+// padded rows, the next slab's loads in flight during the current MMAs.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -39,9 +40,13 @@ namespace gb300 {
 
 namespace {
 
-constexpr int kSBM = 64, kSBN = 64, kSBK = 32;
-constexpr int kSThreads = 128;
+constexpr int kSBM = 128, kSBN = 128, kSBK = 32;   // CTA tile and K slab
+constexpr int kSThreads = 256;                     // 8 warps in a 2 (M) x 4 (N) grid
+constexpr int kWarpsN = 4;
+constexpr int kWarpM = 64, kWarpN = 32;            // warp tile
+constexpr int kAtomsM = kWarpM / 16, kAtomsN = kWarpN / 8;
 constexpr int kPad = 8;   // halves of padding per shared row (conflict-free fragment loads)
+static_assert(kSBM / kWarpM * (kSBN / kWarpN) == kSThreads / 32, "one warp tile per warp");
 
 template <int kIn>
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
@@ -95,90 +100,125 @@ __device__ __forceinline__ void store_out(void* p, int64_t i, float v) {
         static_cast<__nv_bfloat16*>(p)[i] = __float2bfloat16_rn(v);
 }
 
-// One 64 x 64 tile of D at (m0, n0).
+// Operand staging: the slab [rows, kSBK] of one operand, read element by
+// element (any element-aligned layout) with consecutive threads on the
+// operand's contiguous dimension, into registers; out-of-range -> 0.
+//   trans = 0: element (r, k) at X[(r0 + r) * ld + k0 + k]   (K contiguous)
+//   trans = 1: element (r, k) at X[(k0 + k) * ld + r0 + r]   (rows contiguous)
+template <int kRows>
+__device__ __forceinline__ void load_slab(uint16_t (&v)[kRows * kSBK / kSThreads], const uint16_t* X, int trans,
+                                          int64_t ld, int64_t r0, int64_t rows, int64_t k0, int64_t K) {
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < kRows * kSBK / kSThreads; ++i) {
+        const int e = tid + i * kSThreads;
+        const int r = trans ? e % kRows : e / kSBK;
+        const int c = trans ? e / kRows : e % kSBK;
+        const int64_t rr = r0 + r, kk = k0 + c;
+        v[i] = (rr < rows && kk < K) ? (trans ? X[kk * ld + rr] : X[rr * ld + kk]) : (uint16_t)0;
+    }
+}
+
+// ... and from registers into the K-contiguous shared slab S[r][k].
+template <int kRows>
+__device__ __forceinline__ void store_slab(uint16_t (*S)[kSBK + kPad], const uint16_t (&v)[kRows * kSBK / kSThreads],
+                                           int trans) {
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < kRows * kSBK / kSThreads; ++i) {
+        const int e = tid + i * kSThreads;
+        const int r = trans ? e % kRows : e / kSBK;
+        const int c = trans ? e / kRows : e % kSBK;
+        S[r][c] = v[i];
+    }
+}
+
+// One kSBM x kSBN tile of D at (m0, n0).  The K loop is software-pipelined:
+// the next slab's global loads are in flight (in registers) while the
+// current slab, double-buffered in shared memory, feeds the MMAs.
 template <int kIn, int kOut, bool kHasC>
-__device__ __forceinline__ void sync_tile(const SyncParams& p, int64_t m0, int64_t n0, uint16_t (*As)[kSBK + kPad],
-                                          uint16_t (*Bs)[kSBK + kPad]) {
+__device__ __forceinline__ void sync_tile(const SyncParams& p, int64_t m0, int64_t n0,
+                                          uint16_t (*As)[kSBM][kSBK + kPad], uint16_t (*Bs)[kSBN][kSBK + kPad]) {
     const int tid = threadIdx.x;
     const int lane = tid % 32;
     const int warp = tid / 32;
     const int g = lane / 4, tq = lane % 4;
-    const int wm = (warp / 2) * 32, wn = (warp % 2) * 32;   // warp tile origin in the CTA tile
+    const int wm = (warp / kWarpsN) * kWarpM, wn = (warp % kWarpsN) * kWarpN;   // warp tile origin
     const uint16_t* A = static_cast<const uint16_t*>(p.A);
     const uint16_t* B = static_cast<const uint16_t*>(p.B);
+    // B as [N rows][K]: transB = 1 is K-contiguous, transB = 0 (stored [K, N]) rows-contiguous
+    const int b_trans = p.transB ? 0 : 1;
 
-    float acc[2][4][4];
+    float acc[kAtomsM][kAtomsN][4];
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < kAtomsM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < kAtomsN; ++j)
 #pragma unroll
             for (int s = 0; s < 4; ++s) acc[i][j][s] = 0.0f;
 
+    uint16_t ra[kSBM * kSBK / kSThreads], rb[kSBN * kSBK / kSThreads];
+    load_slab<kSBM>(ra, A, p.transA, p.lda, m0, p.M, 0, p.K);
+    load_slab<kSBN>(rb, B, b_trans, p.ldb, n0, p.N, 0, p.K);
+    store_slab<kSBM>(As[0], ra, p.transA);
+    store_slab<kSBN>(Bs[0], rb, b_trans);
+    __syncthreads();
+    int cur = 0;
     for (int64_t k0 = 0; k0 < p.K; k0 += kSBK) {
-        // stage A[m0.., k0..] and B[k0.., n0..] (out of range -> 0)
-        // consecutive threads walk the operand's contiguous dimension
-        for (int e = tid; e < kSBM * kSBK; e += kSThreads) {
-            const int r = p.transA ? e % kSBM : e / kSBK;
-            const int c = p.transA ? e / kSBM : e % kSBK;
-            const int64_t m = m0 + r, k = k0 + c;
-            uint16_t v = 0;
-            if (m < p.M && k < p.K) v = p.transA ? A[k * p.lda + m] : A[m * p.lda + k];
-            As[r][c] = v;
+        const bool more = k0 + kSBK < p.K;   // the same for the whole CTA
+        if (more) {
+            load_slab<kSBM>(ra, A, p.transA, p.lda, m0, p.M, k0 + kSBK, p.K);
+            load_slab<kSBN>(rb, B, b_trans, p.ldb, n0, p.N, k0 + kSBK, p.K);
         }
-        for (int e = tid; e < kSBN * kSBK; e += kSThreads) {
-            const int r = p.transB ? e / kSBK : e % kSBN;
-            const int c = p.transB ? e % kSBK : e / kSBN;
-            const int64_t n = n0 + r, k = k0 + c;
-            uint16_t v = 0;
-            if (n < p.N && k < p.K) v = p.transB ? B[n * p.ldb + k] : B[k * p.ldb + n];
-            Bs[r][c] = v;
-        }
-        __syncthreads();
 #pragma unroll
         for (int ks = 0; ks < kSBK; ks += 16) {
             const int64_t k_left = p.K - (k0 + ks);   // same for the whole CTA
             if (k_left <= 0) break;
-            uint32_t af[2][4], bf[4][2];
+            uint32_t af[kAtomsM][4], bf[kAtomsN][2];
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < kAtomsM; ++i) {
                 const int r = wm + 16 * i + g;
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {   // w = 2 kHi + rM: slots 2w, 2w + 1 (kp = 0, 1)
                     const int rM = w % 2, kHi = w / 2;
                     const int c = ks + 2 * tq + 8 * kHi;
-                    af[i][w] = pack_halves(As[r + 8 * rM][c], As[r + 8 * rM][c + 1]);
+                    af[i][w] = pack_halves(As[cur][r + 8 * rM][c], As[cur][r + 8 * rM][c + 1]);
                 }
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kAtomsN; ++j) {
                 const int r = wn + 8 * j + g;
 #pragma unroll
                 for (int kHi = 0; kHi < 2; ++kHi) {   // slots 2 kHi, 2 kHi + 1
                     const int c = ks + 2 * tq + 8 * kHi;
-                    bf[j][kHi] = pack_halves(Bs[r][c], Bs[r][c + 1]);
+                    bf[j][kHi] = pack_halves(Bs[cur][r][c], Bs[cur][r][c + 1]);
                 }
             }
             if (k_left > 8) {
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
+                for (int i = 0; i < kAtomsM; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) mma_16816<kIn>(acc[i][j], af[i], bf[j]);
+                    for (int j = 0; j < kAtomsN; ++j) mma_16816<kIn>(acc[i][j], af[i], bf[j]);
             } else {   // at most 8 columns of K left: one k8 atom
 #pragma unroll
-                for (int i = 0; i < 2; ++i)
+                for (int i = 0; i < kAtomsM; ++i)
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) mma_1688<kIn>(acc[i][j], af[i][0], af[i][1], bf[j][0]);
+                    for (int j = 0; j < kAtomsN; ++j) mma_1688<kIn>(acc[i][j], af[i][0], af[i][1], bf[j][0]);
             }
         }
+        if (more) {   // the other buffer was last read before the previous barrier
+            store_slab<kSBM>(As[cur ^ 1], ra, p.transA);
+            store_slab<kSBN>(Bs[cur ^ 1], rb, b_trans);
+        }
         __syncthreads();
+        cur ^= 1;
     }
 
     // epilogue: D = alpha * acc (+ beta * C), element by element with bounds
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < kAtomsM; ++i)
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < kAtomsN; ++j)
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
                 const int rM = s / 2, rN = s % 2;
@@ -197,14 +237,16 @@ __device__ __forceinline__ void sync_tile(const SyncParams& p, int64_t m0, int64
 
 template <int kIn, int kOut, bool kHasC>
 __global__ void __launch_bounds__(kSThreads) gemm_mma_sync_kernel(SyncParams p) {
-    // As[m][k] and Bs[n][k]: both K-contiguous, so A and B fragments are read
-    // the same way (pairs of consecutive k).
-    __shared__ uint16_t As[kSBM][kSBK + kPad];
-    __shared__ uint16_t Bs[kSBN][kSBK + kPad];
+    // As[buf][m][k] and Bs[buf][n][k]: both K-contiguous, so A and B
+    // fragments are read the same way (pairs of consecutive k).
+    __shared__ uint16_t As[2][kSBM][kSBK + kPad];
+    __shared__ uint16_t Bs[2][kSBN][kSBK + kPad];
     const int64_t num_m_tiles = (p.M + kSBM - 1) / kSBM;
     // grid.y is capped at 65535: CTAs step through the M tiles by gridDim.y
-    for (int64_t mt = blockIdx.y; mt < num_m_tiles; mt += gridDim.y)
+    for (int64_t mt = blockIdx.y; mt < num_m_tiles; mt += gridDim.y) {
         sync_tile<kIn, kOut, kHasC>(p, mt * kSBM, (int64_t)blockIdx.x * kSBN, As, Bs);
+        __syncthreads();   // the next tile's first stores must not overtake this tile's reads
+    }
 }
 
 template <int kIn, int kOut, bool kHasC>
