@@ -151,6 +151,23 @@ void byte_range(const void* p, int64_t rows, int64_t cols, int64_t ld, int esz, 
 
 bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
 
+// True while `s` is being captured into a CUDA graph: no allocation, no
+// synchronising call may happen then.
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return st != cudaStreamCaptureStatusNone;
+}
+
+bool device_ready(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    return g_devices[dev].ready;
+}
+
 int device_state(int dev, DeviceState** out) {
     if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -410,7 +427,10 @@ struct Workspace {
 };
 std::vector<Workspace> g_workspaces;
 
-int workspace_for(int kind, int dev, cudaStream_t s, int64_t bytes, void** base, uint32_t* epoch) {
+// `may_grow` false (the stream is being captured into a CUDA graph, where
+// allocating is not allowed): only an existing workspace that is large
+// enough is returned; otherwise GEMM_ERR_CUDA, with nothing changed.
+int workspace_for(int kind, int dev, cudaStream_t s, int64_t bytes, void** base, uint32_t* epoch, bool may_grow) {
     std::lock_guard<std::mutex> lock(g_mutex);
     Workspace* w = nullptr;
     for (auto& x : g_workspaces)
@@ -420,6 +440,7 @@ int workspace_for(int kind, int dev, cudaStream_t s, int64_t bytes, void** base,
         w = &g_workspaces.back();
     }
     if (w->bytes < bytes) {
+        if (!may_grow) return GEMM_ERR_CUDA;
         if (w->base && cudaFree(w->base) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
@@ -609,7 +630,7 @@ int launch_sync_or_reject(void* D, const void* A, const void* B, const void* C, 
 constexpr int kNoWorkspace = 1;
 int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
                   int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float alpha,
-                  float beta, int in_dtype, int out_dtype, int dev, cudaStream_t s) {
+                  float beta, int in_dtype, int out_dtype, int dev, cudaStream_t s, bool may_grow) {
     const int isz = elem_size(in_dtype);
     const int osz = elem_size(out_dtype);
     const bool has_c = beta != 0.0f;
@@ -637,7 +658,8 @@ int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t 
     const int64_t d_bytes = d_ok ? 0 : round_up(M * ldd2 * osz, 256);
     void* ws = nullptr;
     uint32_t epoch = 0;
-    if (workspace_for(kWsRepack, dev, s, a_bytes + b_bytes + d_bytes, &ws, &epoch) != GEMM_OK) return kNoWorkspace;
+    if (workspace_for(kWsRepack, dev, s, a_bytes + b_bytes + d_bytes, &ws, &epoch, may_grow) != GEMM_OK)
+        return kNoWorkspace;
     char* w = static_cast<char*>(ws);
     const void* A2 = A;
     const void* B2 = B;
@@ -761,9 +783,15 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
         cudaGetLastError();
         return reject(GEMM_ERR_CUDA, "cudaGetDevice");
     }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // Inside a CUDA graph capture nothing may be allocated: the device set-up
+    // (one allocation) must have happened before, and workspaces are used
+    // only where they already exist (see below).
+    const bool in_capture = capturing(s);
+    if (in_capture && !device_ready(dev))
+        return reject(GEMM_ERR_CUDA, "first call on this device inside a stream capture");
     DeviceState* ds = nullptr;
     if ((rc = device_state(dev, &ds)) != GEMM_OK) return reject(rc, "device set-up");
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool has_c = beta != 0.0f;
     if (K == 0) {
         GEMM_LOGF("M=%lld N=%lld K=0: epilogue-only kernel", (long long)M, (long long)N);
@@ -778,7 +806,7 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
         GEMM_LOGF("M=%lld N=%lld K=%lld: layout the tcgen05 kernel cannot take as it is, repacked", (long long)M,
                   (long long)N, (long long)K);
         rc = gemm_repacked(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype, out_dtype,
-                           dev, s);
+                           dev, s, !in_capture);
         if (rc != kNoWorkspace) return rc == GEMM_OK ? GEMM_OK : reject(rc, "repacked call");
         route = f8 ? kRouteNone : kRouteSync;   // no workspace to be had
     }
@@ -790,7 +818,13 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
                                      out_dtype, s);
     }
 
-    const Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, f8 ? 1 : 0);
+    Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, f8 ? 1 : 0);
+    void* ws = nullptr;
+    uint32_t epoch = 0;
+    if (pl.sk_tiles > 0 && workspace_for(kWsStreamK, dev, s, pl.ws_bytes, &ws, &epoch, !in_capture) != GEMM_OK) {
+        if (!in_capture) return reject(GEMM_ERR_CUDA, "stream-K workspace");
+        pl = make_plan(M, N, K, ds->num_sms, false, out_dtype, f8 ? 1 : 0);   // whole tiles: no workspace
+    }
     TcgenLaunch L;
     if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
                                in_dtype, out_dtype)) != GEMM_OK)
@@ -799,10 +833,6 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
     p.status = ds->d_status;
     p.skip_first_stage = skip_first_stage_setting();
     if (pl.sk_tiles > 0) {
-        void* ws = nullptr;
-        uint32_t epoch = 0;
-        if ((rc = workspace_for(kWsStreamK, dev, s, pl.ws_bytes, &ws, &epoch)) != GEMM_OK)
-            return reject(rc, "stream-K workspace");
         p.sk_tiles = pl.sk_tiles;
         p.ws_max_nc = pl.max_nc;
         p.ws_epoch = epoch;
@@ -925,9 +955,14 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
         cudaGetLastError();
         return reject(GEMM_ERR_CUDA, "cudaGetDevice");
     }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (capturing(s)) {   // the one-time set-up is not done inside a stream capture
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (dev < 0 || dev >= kMaxDevices || !g_noalloc[dev].ready)
+            return reject(GEMM_ERR_CUDA, "first call on this device inside a stream capture");
+    }
     NoAllocState* ns = nullptr;
     if ((rc = noalloc_device_state(dev, &ns)) != GEMM_OK) return reject(rc, "device set-up (no-alloc)");
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0)   // epilogue-only kernel: no scratch at all
         return launch_k0_or_reject(out_dtype, D, C, M, N, ldc, ldd, alpha, beta, ns->num_sms, s);
     if (route == kRouteSync)   // needs no scratch either

@@ -69,13 +69,25 @@ struct Pipe {
 std::mutex g_mutex;
 std::vector<Pipe*> g_pipes;
 
-int pipe_for(int dev, cudaStream_t user, Pipe** out) {
+// True while `s` is being captured into a CUDA graph: nothing may be
+// created or allocated then.
+bool capturing(cudaStream_t s) {
+    cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &st) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return st != cudaStreamCaptureStatusNone;
+}
+
+int pipe_for(int dev, cudaStream_t user, bool may_create, Pipe** out) {
     std::lock_guard<std::mutex> lock(g_mutex);
     for (Pipe* p : g_pipes)
         if (p->dev == dev && p->user == user) {
             *out = p;
             return p->ready ? GEMM_OK : GEMM_ERR_CUDA;
         }
+    if (!may_create) return GEMM_ERR_CUDA;
     Pipe* p = new Pipe;
     p->dev = dev;
     p->user = user;
@@ -95,8 +107,9 @@ int pipe_for(int dev, cudaStream_t user, Pipe** out) {
 
 // Grows the pipe's staging buffer.  Freeing the old one synchronises the
 // device, so no copy or product still uses it.
-int ensure_buffer(Pipe* p, int64_t bytes) {
+int ensure_buffer(Pipe* p, int64_t bytes, bool may_grow) {
     if (p->bytes >= bytes) return GEMM_OK;
+    if (!may_grow) return GEMM_ERR_CUDA;
     if (p->buf && cudaFree(p->buf) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
@@ -163,8 +176,11 @@ extern "C" GEMM_API int gemm_host(void* D, const void* A, const void* B, const v
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return copy_error();
     cudaStream_t user = reinterpret_cast<cudaStream_t>(stream);
+    // Inside a CUDA graph capture the staging streams and buffers must exist
+    // already (from an earlier call on this stream with at least these sizes).
+    const bool may_allocate = !capturing(user);
     Pipe* p = nullptr;
-    if ((rc = pipe_for(dev, user, &p)) != GEMM_OK) return rc;
+    if ((rc = pipe_for(dev, user, may_allocate, &p)) != GEMM_OK) return rc;
 
     const bool has_c = beta != 0.0f;
     const int isz = elem_bytes(in_dtype), osz = elem_bytes(out_dtype);
@@ -177,7 +193,7 @@ extern "C" GEMM_API int gemm_host(void* D, const void* A, const void* B, const v
     const int64_t a_bytes = round_up(a_rows * lda_d * isz, 256);
     const int64_t b_bytes = round_up(b_rows * ldb_d * isz, 256);
     const int64_t o_bytes = round_up(M * ldo_d * osz, 256);
-    if ((rc = ensure_buffer(p, a_bytes + b_bytes + o_bytes * (has_c ? 2 : 1))) != GEMM_OK) return rc;
+    if ((rc = ensure_buffer(p, a_bytes + b_bytes + o_bytes * (has_c ? 2 : 1), may_allocate)) != GEMM_OK) return rc;
     char* dA = p->buf;
     char* dB = dA + a_bytes;
     char* dD = dB + b_bytes;

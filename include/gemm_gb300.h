@@ -116,6 +116,11 @@ typedef enum {
  *     and writes element by element.
  * All accumulate in fp32 and agree within the documented tolerance.
  * GEMM_PATH=tcgen05 or mma_sync forces a kernel where it can run.
+ * CUDA graphs: gemm() may be called while `stream` is being captured, as
+ * long as an earlier call (outside the capture) has run on the device; it
+ * then allocates nothing: stream-K splitting and the repacking route are
+ * used only where this stream's workspace from earlier calls is large
+ * enough (otherwise whole tiles, respectively the mma.sync kernel).
  * Returns GEMM_OK or a GEMM_ERR_* code (see gemm_status_t).
  * Setting the environment variable GEMM_LOG=1 prints each call's plan or
  * rejection reason to stderr.
@@ -231,6 +236,10 @@ GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, const void* C,
  *     The host buffers must stay unchanged until then.
  *   - Consecutive calls on one stream are ordered; calls on one stream from
  *     several threads must be serialised by the caller.
+ *   - CUDA graphs: a call inside a capture of `stream` needs the staging
+ *     set up by an earlier call on that stream with at least these sizes
+ *     (else GEMM_ERR_CUDA); the captured copies then read and write the
+ *     same host buffers on every replay.
  * Returns GEMM_OK or a GEMM_ERR_* code; argument errors (including host
  * buffers that overlap) are detected before anything is enqueued.
  */

@@ -1,0 +1,117 @@
+"""gemm(), gemm_noalloc() and gemm_host() captured into CUDA graphs and
+replayed, against the CPU oracle.  Inside a capture the library allocates
+nothing: stream-K and the repacking route use only workspaces that earlier
+calls on the stream created, else the call falls back to whole tiles /
+the mma.sync kernel.  Replays read the buffers' current contents, so new
+inputs copied into the same buffers give new, correct results.
+"""
+import pytest
+import torch
+
+from dense_tensor_core_02_gb300 import binding
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load_library()
+    yield
+    rc, info = H.poll()
+    assert rc == 0, ("device status after the module", rc, info)
+
+
+def _problem(M, N, K, seed, dev):
+    A = H.int_matrix((M, K), -8, 8, "f16", seed)
+    B = H.int_matrix((K, N), -8, 8, "f16", seed + 1)
+    return A, B, A.to(dev), B.to(dev), torch.empty((M, N), device=dev)
+
+
+@pytest.mark.parametrize("warm", [True, False])
+def test_captured_gemm_replays(warm):
+    """A stream-K shape (forced fine split) and a narrow-tile shape in one
+    graph.  Without a warm-up call on this stream the stream-K workspace does
+    not exist yet, so the captured call plans whole tiles instead."""
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream()
+    shapes = [(1024, 768, 2080), (300, 200, 136)]
+    probs = [_problem(M, N, K, 10 * i + 1, dev) for i, (M, N, K) in enumerate(shapes)]
+    binding.gemm(probs[0][4], probs[0][2], probs[0][3], None, 16, 8, 16, 2080, 768, 768, 768, 0, 0, 1.0, 0.0, 0,
+                 2, s)   # the device's one-time set-up happens outside the capture
+    s.synchronize()
+
+    def calls():
+        for (A, B, Ad, Bd, Dd), (M, N, K) in zip(probs, shapes):
+            rc = binding.gemm(Dd, Ad, Bd, None, M, N, K, K, N, N, N, 0, 0, 1.0, 0.0, 0, 2, s)
+            assert rc == 0
+
+    with H.env(GEMM_SK_MIN_ITERS="1"):
+        if warm:
+            with torch.cuda.stream(s):
+                calls()
+            s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            calls()
+    for rep in range(2):
+        if rep == 1:   # new inputs in the same buffers
+            for i, (A, B, Ad, Bd, Dd) in enumerate(probs):
+                A2 = H.int_matrix(tuple(A.shape), -8, 8, "f16", 100 + i)
+                Ad.copy_(A2)
+                probs[i] = (A2, B, Ad, Bd, Dd)
+        for (_, _, _, _, Dd) in probs:
+            Dd.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for (A, B, _, _, Dd), (M, N, K) in zip(probs, shapes):
+            ref, _ = H.oracle_full(A, B, None, M, N, K)
+            H.assert_exact(Dd.cpu().numpy(), ref, "replay %d %s" % (rep, (M, N, K)))
+
+
+def test_captured_misaligned_call_without_workspace():
+    """A layout off the 16-byte grid, large enough for the repacking route,
+    captured on a fresh stream: no repack workspace exists, so the captured
+    call runs the mma.sync kernel instead."""
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream()
+    M, N, K = 520, 392, 1001
+    A = H.int_matrix((M, K), -8, 8, "bf16", 41)
+    B = H.int_matrix((K, N), -8, 8, "bf16", 42)
+    Ad, Bd, Dd = A.to(dev), B.to(dev), torch.empty((M, N), device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        assert binding.gemm(Dd, Ad, Bd, None, M, N, K, K, N, N, N, 0, 0, 1.0, 0.0, 1, 2, s) == 0
+    Dd.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    ref, _ = H.oracle_full(A, B, None, M, N, K, in_dtype="bf16")
+    H.assert_exact(Dd.cpu().numpy(), ref, "captured misaligned")
+
+
+def test_captured_noalloc_and_host():
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream()
+    M, N, K = 2048, 256, 192
+    A = H.int_matrix((M, K), -8, 8, "f16", 51)
+    B = H.int_matrix((K, N), -8, 8, "f16", 52)
+    Ad, Bd, Dd = A.to(dev), B.to(dev), torch.empty((M, N), device=dev)
+    hA, hB = A.pin_memory(), B.pin_memory()
+    hD = torch.empty((M, N)).pin_memory()
+    # warm-up outside the capture: one-time set-up and gemm_host staging
+    assert binding.gemm_noalloc(Dd, Ad, Bd, None, M, N, K, K, N, N, N, 0, 0, 1.0, 0.0, 0, 2, s) == 0
+    assert binding.gemm_host(hD, hA, hB, None, M, N, K, K, N, N, N, 0, 0, 1.0, 0.0, 0, 2, s) == 0
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        assert binding.gemm_noalloc(Dd, Ad, Bd, None, M, N, K, K, N, N, N, 0, 0, 2.0, 0.0, 0, 2, s) == 0
+        assert binding.gemm_host(hD, hA, hB, None, M, N, K, K, N, N, N, 0, 0, -1.0, 0.0, 0, 2, s) == 0
+    Dd.fill_(float("nan"))
+    hD.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    ref, _ = H.oracle_full(A, B, None, M, N, K)
+    H.assert_exact(Dd.cpu().numpy(), 2.0 * ref, "captured no-alloc")
+    H.assert_exact(hD.numpy(), -ref, "captured gemm_host")
