@@ -116,8 +116,14 @@ int group_m_setting() {
 //    +2.8 %).  GEMM_L2_HINTS="a,b,d" overrides.
 //  * Epilogue pacing (GEMM_EPI_PACE_NS overrides): the persistent CTAs run
 //    their tiles nearly in step, so without a pause every SM would store its
-//    finished tile at the same moment.
-void tuning(GemmParams& p) {
+//    finished tile at the same moment, and the D stores would crowd out the
+//    next tile's operand loads.  With two accumulators an epilogue has the
+//    whole next main loop to finish in, so for tiles with a long main loop
+//    (>= 24 stages, ~0.7 us each) each store chunk is followed by a pause of
+//    20 ns per stage (a quarter of the main loop spread over a warp's 8
+//    chunks), at most 2 us.  Measured (8192 x 8192, K = 4096 / 8192 / 16384):
+//    +2 % / +1 % / +0.7 %; shorter tiles are store-bound and get no pause.
+void tuning(GemmParams& p, int tile_n) {
     p.hint_a = p.num_n_tiles == 1 ? 1 : 2;
     p.hint_b = p.num_m_tiles == 1 ? 1 : 2;
     p.hint_d = 1;
@@ -130,6 +136,7 @@ void tuning(GemmParams& p) {
         p.hint_d = d;
     }
     p.epi_pace_ns = 0;
+    if (tile_n == 256 && p.num_k_blocks >= 24) p.epi_pace_ns = std::min(2000, p.num_k_blocks * 20);
     const char* pv = std::getenv("GEMM_EPI_PACE_NS");
     if (pv && *pv) {
         const int ns = std::atoi(pv);
@@ -563,7 +570,7 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     p.n_tma = (int32_t)n_tma;
     p.d_ptr = D;
     p.ldd = ldd;
-    tuning(p);
+    tuning(p, pl.tile_n);
     // tcgen05 instruction descriptor (kind::f16 or kind::f8f6f4, chosen by the
     // kernel instantiation): D format f32 (bits 4-5 = 1); A / B format (bits
     // 7-9, 10-12): kind::f16 0 = f16, 1 = bf16; kind::f8f6f4 0 = E4M3, 1 = E5M2;
