@@ -7,14 +7,16 @@
 // later panels, the products of earlier ones and the device->host copies of
 // finished ones overlap:
 //
-//   copy-in stream   B (whole) | A0 C0 | A1 C1 | A2 C2 | ...
-//   caller's stream            |  gemm(panel 0) | gemm(panel 1) | ...
-//   copy-out stream                             |  D0  |  D1  | ...
+//   copy-in stream   B0 | A0 C0 | B1 | B2 | B3 | A1 C1 | A2 C2 | ...
+//   caller's stream      | D00 | D01 | D02 | D03 |  gemm(panel 1) | ...
+//   copy-out stream            | D00 | D01 | D02 | D03 |  D1  | ...
 //
 // A row panel of D needs all of B and its own rows of A (for transA = 1,
-// its columns of the stored A, a strided copy) and C.  The staging buffers
-// have 16-byte-aligned row strides, so gemm() runs the tcgen05 kernel on
-// them directly.
+// its columns of the stored A, a strided copy) and C.  The first panel is
+// computed and copied out in column blocks, each as soon as its block of B
+// is in, so the copy-out stream starts long before all of B has crossed
+// the host link.  The staging buffers have 16-byte-aligned row strides, so
+// gemm() runs the tcgen05 kernel on them directly.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -30,6 +32,7 @@
 namespace {
 
 constexpr int kMaxPanels = 16;
+constexpr int kFirstBlocks = 4;   // column blocks of the first panel (N >= 1024)
 constexpr int64_t kMaxDim = 2147483647;
 
 int elem_bytes(int dtype) {
@@ -59,6 +62,8 @@ struct Pipe {
     cudaStream_t out = nullptr;   // device -> host copies
     cudaEvent_t loaded[kMaxPanels] = {};     // panel p's A (and C) are on the device
     cudaEvent_t computed[kMaxPanels] = {};   // panel p's D is on the device
+    cudaEvent_t b_loaded[kFirstBlocks] = {};    // column block j of B is on the device
+    cudaEvent_t b_computed[kFirstBlocks] = {};  // column block j of the first panel's D is on the device
     cudaEvent_t entry = nullptr;             // this call's place in the caller's stream
     cudaEvent_t copied_out = nullptr;        // this call's D is on the host
     char* buf = nullptr;
@@ -98,6 +103,9 @@ int pipe_for(int dev, cudaStream_t user, bool may_create, Pipe** out) {
     for (int i = 0; ok && i < kMaxPanels; ++i)
         ok = cudaEventCreateWithFlags(&p->loaded[i], cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&p->computed[i], cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; ok && i < kFirstBlocks; ++i)
+        ok = cudaEventCreateWithFlags(&p->b_loaded[i], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&p->b_computed[i], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) cudaGetLastError();
     p->ready = ok;
     g_pipes.push_back(p);   // kept until the process exits, like the device workspaces
@@ -204,37 +212,72 @@ extern "C" GEMM_API int gemm_host(void* D, const void* A, const void* B, const v
     // (see the end of this function), so the staging buffers are free.
     if (cudaEventRecord(p->entry, user) != cudaSuccess || cudaStreamWaitEvent(p->in, p->entry, 0) != cudaSuccess)
         return copy_error();
-    if (K > 0 && cudaMemcpy2DAsync(dB, ldb_d * isz, B, ldb * isz, b_cols * isz, b_rows, cudaMemcpyHostToDevice,
-                                   p->in) != cudaSuccess)
-        return copy_error();
     const int64_t rows = panel_rows(M);
     const int panels = (int)((M + rows - 1) / rows);
-    for (int q = 0; q < panels; ++q) {
+    // columns [n0, n0 + nc) of op(B): a column block of the stored [K, N] B
+    // (transB = 0), or a row block of the stored [N, K] B (transB = 1)
+    const int64_t bcols = (N >= 1024 && K > 0) ? round_up((N + kFirstBlocks - 1) / kFirstBlocks, 256) : N;
+    const int blocks = (int)((N + bcols - 1) / bcols);
+    auto copy_b = [&](int64_t n0, int64_t nc) {
+        if (transB)
+            return cudaMemcpy2DAsync(dB + n0 * ldb_d * isz, ldb_d * isz, static_cast<const char*>(B) + n0 * ldb * isz,
+                                     ldb * isz, K * isz, nc, cudaMemcpyHostToDevice, p->in);
+        return cudaMemcpy2DAsync(dB + n0 * isz, ldb_d * isz, static_cast<const char*>(B) + n0 * isz, ldb * isz,
+                                 nc * isz, K, cudaMemcpyHostToDevice, p->in);
+    };
+    auto b_block = [&](int64_t n0) -> const void* {
+        return K > 0 ? static_cast<const void*>(dB + (transB ? n0 * ldb_d : n0) * isz) : nullptr;
+    };
+    // the rows of op(A) and of C of panel q, then its "loaded" event
+    auto copy_panel_inputs = [&](int q) {
         const int64_t m0 = q * rows, mr = std::min(rows, M - m0);
-        // this panel's rows of op(A): rows m0.. of A, or columns m0.. of the stored [K, M] A
+        // rows m0.. of A, or columns m0.. of the stored [K, M] A
         const char* a_src = static_cast<const char*>(A) + (transA ? m0 : m0 * lda) * isz;
         char* a_dst = dA + (transA ? m0 : m0 * lda_d) * isz;
         if (K > 0 && cudaMemcpy2DAsync(a_dst, lda_d * isz, a_src, lda * isz, (transA ? mr : K) * isz,
                                        transA ? K : mr, cudaMemcpyHostToDevice, p->in) != cudaSuccess)
-            return copy_error();
+            return false;
         if (has_c && cudaMemcpy2DAsync(dC + m0 * ldo_d * osz, ldo_d * osz,
                                        static_cast<const char*>(C) + m0 * ldc * osz, ldc * osz, N * osz, mr,
                                        cudaMemcpyHostToDevice, p->in) != cudaSuccess)
+            return false;
+        return cudaEventRecord(p->loaded[q], p->in) == cudaSuccess;
+    };
+    // D[m0.., n0..] of the panel / block on the caller's stream, then its copy-out
+    auto compute_and_return = [&](int q, int64_t n0, int64_t nc, cudaEvent_t inputs, cudaEvent_t done) {
+        const int64_t m0 = q * rows, mr = std::min(rows, M - m0);
+        if (cudaStreamWaitEvent(user, inputs, 0) != cudaSuccess) return copy_error();
+        const void* a_panel = K > 0 ? static_cast<const void*>(dA + (transA ? m0 : m0 * lda_d) * isz) : nullptr;
+        const int64_t o = (m0 * ldo_d + n0) * osz;
+        int r = gemm(dD + o, a_panel, b_block(n0), has_c ? dC + o : nullptr, mr, nc, K, lda_d, ldb_d, ldo_d, ldo_d,
+                     transA, transB, alpha, beta, in_dtype, out_dtype, stream);
+        if (r != GEMM_OK) return r;
+        if (cudaEventRecord(done, user) != cudaSuccess || cudaStreamWaitEvent(p->out, done, 0) != cudaSuccess ||
+            cudaMemcpy2DAsync(static_cast<char*>(D) + (m0 * ldd + n0) * osz, ldd * osz, dD + o, ldo_d * osz,
+                              nc * osz, mr, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
             return copy_error();
-        if (cudaEventRecord(p->loaded[q], p->in) != cudaSuccess ||
-            cudaStreamWaitEvent(user, p->loaded[q], 0) != cudaSuccess)
+        return (int)GEMM_OK;
+    };
+
+    // copy-in: B's first column block, the first panel's A and C, B's other blocks
+    if (K > 0 && copy_b(0, std::min(bcols, N)) != cudaSuccess) return copy_error();
+    if (!copy_panel_inputs(0)) return copy_error();
+    for (int j = 1; j < blocks; ++j) {
+        const int64_t n0 = j * bcols;
+        if (copy_b(n0, std::min(bcols, N - n0)) != cudaSuccess || cudaEventRecord(p->b_loaded[j], p->in) != cudaSuccess)
             return copy_error();
-        const void* a_panel = transA ? static_cast<const void*>(dA + m0 * isz) : static_cast<const void*>(a_dst);
-        rc = gemm(dD + m0 * ldo_d * osz, K > 0 ? a_panel : nullptr, K > 0 ? dB : nullptr,
-                  has_c ? dC + m0 * ldo_d * osz : nullptr, mr, N, K, lda_d, ldb_d, ldo_d, ldo_d, transA, transB,
-                  alpha, beta, in_dtype, out_dtype, stream);
-        if (rc != GEMM_OK) return rc;
-        if (cudaEventRecord(p->computed[q], user) != cudaSuccess ||
-            cudaStreamWaitEvent(p->out, p->computed[q], 0) != cudaSuccess)
-            return copy_error();
-        if (cudaMemcpy2DAsync(static_cast<char*>(D) + m0 * ldd * osz, ldd * osz, dD + m0 * ldo_d * osz,
-                              ldo_d * osz, N * osz, mr, cudaMemcpyDeviceToHost, p->out) != cudaSuccess)
-            return copy_error();
+    }
+    // the first panel, block by block
+    for (int j = 0; j < blocks; ++j) {
+        const int64_t n0 = j * bcols;
+        if ((rc = compute_and_return(0, n0, std::min(bcols, N - n0), j == 0 ? p->loaded[0] : p->b_loaded[j],
+                                     p->b_computed[j])) != GEMM_OK)
+            return rc;
+    }
+    // the other panels, whole
+    for (int q = 1; q < panels; ++q) {
+        if (!copy_panel_inputs(q)) return copy_error();
+        if ((rc = compute_and_return(q, 0, N, p->loaded[q], p->computed[q])) != GEMM_OK) return rc;
     }
     // D is on the host when the caller's stream reaches this point.
     if (cudaEventRecord(p->copied_out, p->out) != cudaSuccess || cudaStreamWaitEvent(user, p->copied_out, 0) != cudaSuccess)

@@ -119,3 +119,20 @@ def test_host_alias_rejected():
     # D overlapping B (same host buffer viewed twice)
     rc = binding.gemm_host(buf, A, buf, None, 64, 64, 64, 64, 128, 64, 64, 0, 0, 1.0, 0.0, 0, 2, None)
     assert rc == -4
+
+
+@pytest.mark.parametrize("transB", [0, 1])
+@pytest.mark.parametrize("in_dtype", ["f16", "e4m3"])
+def test_first_panel_in_column_blocks(transB, in_dtype):
+    """N >= 1024: the first row panel is computed and copied out in column
+    blocks (a ragged last one here) while the rest of B is still arriving."""
+    M, N, K = 2300, 1100, 200
+    seed = 61 + transB + 2 * (in_dtype == "e4m3")
+    A = H.int_matrix((M, K), -8, 8, in_dtype, seed)
+    B = H.int_matrix((N, K) if transB else (K, N), -8, 8, in_dtype, seed + 1)
+    C = H.int_matrix((M, N), -50, 50, "f32", seed + 2)
+    kw = dict(transB=transB, beta=1.0, in_dtype=in_dtype)
+    D, rc = _run_host(A, B, C, M, N, K, pad=5, **kw)
+    assert rc == 0
+    ref, _ = H.oracle_full(A, B, C, M, N, K, **kw)
+    H.assert_exact(D.numpy(), ref, "column blocks transB=%d %s" % (transB, in_dtype))
