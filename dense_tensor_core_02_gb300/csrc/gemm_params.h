@@ -47,7 +47,7 @@ struct GemmParams {
     // columns [0, n_tma) (n_tma = N rounded down to 16 bytes); the last
     // N - n_tma columns of each row are stored element by element.
     int32_t n_tma;
-    int32_t pad0;
+    int32_t pad0;           // keeps d_ptr 8-byte aligned
     void* d_ptr;
     int64_t ldd;            // D row stride in elements
     // L2 eviction priority of the TMA copies of A, B (loads) and D (stores):
@@ -61,9 +61,9 @@ struct GemmParams {
     int32_t sk_tiles;
     int32_t ws_max_nc;        // partial slots per stream-K tile
     uint32_t ws_epoch;        // tags this launch's arrivals on the counters (24 bits used)
-    int32_t pad2;
+    int32_t pad2;           // keeps ws_counters 8-byte aligned
     uint32_t* ws_counters;    // [sk_tiles][2 CTA ranks] arrival counters
-    void* ws_partials;        // [sk_tiles][ws_max_nc][2 ranks] x 128x256 fp32 partials
+    void* ws_partials;        // [sk_tiles][ws_max_nc][2 ranks] x one CTA's fp32 accumulator (128 x tile N)
 };
 
 // ---------------------------------------------------------------------------
