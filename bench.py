@@ -36,6 +36,7 @@ NOMINAL_DENSE_TFLOPS = 2250.0        # GB300 dense fp16/bf16, NVIDIA's figure
 FLOP_PER_CLK_PER_SM = 8192           # dense f16/bf16 tcgen05 rate per SM
 FP8_RATE = 2.0                       # nominal dense fp8 rate / fp16 rate (4.5 / 2.25 PFLOP/s)
 E2E_STREAMS = 2                      # streams the end-to-end steps alternate between
+BURST_STEPS = 10                     # launches per burst measurement
 KERNEL_SOURCES = ["dense_tensor_core_02_gb300/csrc/gemm_tcgen05.cuh",
                   "dense_tensor_core_02_gb300/csrc/gemm_sm103.cu",
                   "dense_tensor_core_02_gb300/csrc/ptx.cuh",
@@ -322,10 +323,24 @@ def run_ours(args, case):
     if status != 0:
         raise RuntimeError("device status after warm-up: %s %s" % (binding.gemm_status_string(status), info))
 
-    sampler = ClockSampler(local_rank).start() if rank == 0 else None
-    time.sleep(0.3 if sampler else 0)
+    # burst: the best of three runs of BURST_STEPS launches, measured the way
+    # the burst peak is (a short run, before the power cap sets in); the
+    # headline is the long run below, reported against both peaks
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    burst_ms = None
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(BURST_STEPS):
+                step()
+            e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t = e0.elapsed_time(e1) / BURST_STEPS
+        burst_ms = t if burst_ms is None else min(burst_ms, t)
+
+    sampler = ClockSampler(local_rank).start() if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
     barrier()
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
@@ -423,6 +438,9 @@ def run_ours(args, case):
                 "algorithmic_flops_per_launch": case.flops,
                 "algorithmic_bytes_per_launch": case.algorithmic_bytes,
                 "achieved_gbs": case.algorithmic_bytes / (per_launch_ms * 1e-3) / 1e9}
+    burst_tflops = case.flops / (burst_ms * 1e-3) / 1e12
+    roofline["burst"] = {"launches": BURST_STEPS, "best_of": 3, "ms_per_launch": burst_ms,
+                         "achieved": burst_tflops, "frac": burst_tflops / peak}
     if clocks and clocks.get("sm_mhz"):
         clk_peak = num_sms * FLOP_PER_CLK_PER_SM * rate * clocks["sm_mhz"] * 1e6 / 1e12
         roofline["frac_of_clock_peak"] = achieved / clk_peak
