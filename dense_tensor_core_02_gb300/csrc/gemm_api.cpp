@@ -586,6 +586,10 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     L->out = out_kind_of(out_dtype);
     L->grid = pl.grid;
     L->epi_warps = pl.epi_warps;
+    // Programmatic dependent launch: the kernel's set-up overlaps the tail of
+    // the previous kernel on the stream (GEMM_PDL=0 turns it off).
+    const char* pdl = std::getenv("GEMM_PDL");
+    L->pdl = (pdl && std::strcmp(pdl, "0") == 0) ? 0 : 1;
     return GEMM_OK;
 }
 

@@ -26,6 +26,7 @@ struct TcgenLaunch {
     int epi_warps;            // 4 or 8 epilogue warps
     int tile_n;               // 256, or 64 for the narrow single-CTA tiles
     int f8;                   // 1: E4M3 / E5M2 operands (kind::f8f6f4), K-major only
+    int pdl;                  // 1: launch with programmatic stream serialisation
 };
 
 // Arguments of the warp-level mma.sync path (gemm_mma_sync.cu): any

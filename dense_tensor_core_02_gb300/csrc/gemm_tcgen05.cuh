@@ -303,6 +303,14 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN>::kNumThreads, 1)
         __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Launched with programmatic stream serialisation, this grid may start
+    // while the previous kernel on the stream is still finishing: the set-up
+    // above (barriers, tensor memory, descriptor prefetch) overlaps its tail,
+    // and every global access below waits for its completion here.  The next
+    // grid may be scheduled right away; it can occupy an SM only once this
+    // grid's CTA there has exited, and it waits for this grid in turn.
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
 
     const int cluster_id = kPair ? blockIdx.x / 2 : blockIdx.x;
     const int num_clusters = kPair ? gridDim.x / 2 : gridDim.x;
@@ -749,15 +757,22 @@ static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
     cfg.blockDim = dim3(Cf::kNumThreads, 1, 1);
     cfg.dynamicSmemBytes = Cf::kSmemBytes;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
     if (kPair) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
     }
+    if (L.pdl) {   // programmatic dependent launch (see grid_dependency_wait in the kernel)
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC, kTileN, kF8>, L.a, L.b, L.c, L.d,
                               L.p);
 }

@@ -348,6 +348,17 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+
+// Waits until the grids this one depends on (the previous kernel on the
+// stream, when launched with programmatic stream serialisation) have
+// completed and their memory operations are visible.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next grid on the stream be scheduled before this one completes
+// (its own grid_dependency_wait still waits for this grid's completion).
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- shared memory vector access ---------------------------------------------
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
