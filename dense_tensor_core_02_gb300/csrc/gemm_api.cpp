@@ -588,8 +588,7 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     L->epi_warps = pl.epi_warps;
     // Programmatic dependent launch: the kernel's set-up overlaps the tail of
     // the previous kernel on the stream (GEMM_PDL=0 turns it off).
-    const char* pdl = std::getenv("GEMM_PDL");
-    L->pdl = (pdl && std::strcmp(pdl, "0") == 0) ? 0 : 1;
+    L->pdl = gb300::pdl_setting();
     return GEMM_OK;
 }
 
@@ -714,8 +713,15 @@ int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t 
 
 }  // namespace
 
-extern "C" {
+int gb300::pdl_setting() {
+    static const int on = [] {
+        const char* v = std::getenv("GEMM_PDL");
+        return (v && std::strcmp(v, "0") == 0) ? 0 : 1;
+    }();
+    return on;
+}
 
+extern "C" {
 
 const char* gemm_status_string(int status) {
     switch (status) {

@@ -46,6 +46,29 @@ struct SyncParams {
 
 cudaError_t launch_mma_sync(const SyncParams& p, cudaStream_t stream);
 
+// 1 unless GEMM_PDL=0: launch kernels with programmatic stream serialisation
+// (each kernel waits for its predecessor with griddepcontrol.wait before its
+// first global access, so its set-up overlaps the predecessor's tail).
+int pdl_setting();
+
+#ifdef __CUDACC__
+// Launches `kernel` on `stream`, with programmatic stream serialisation
+// when pdl_setting() allows it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_with_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_setting() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+#endif
+
 // dst[r * ldd + c] = src[r * lds + c] for r < rows, c < cols; elements of
 // elem_bytes (1, 2 or 4) bytes, any element-aligned strides.
 cudaError_t launch_copy2d(void* dst, int64_t ldd, const void* src, int64_t lds, int64_t rows, int64_t cols,

@@ -35,6 +35,7 @@
 #include <cstdint>
 
 #include "gemm_internal.h"
+#include "ptx.cuh"
 
 namespace gb300 {
 
@@ -241,6 +242,8 @@ __global__ void __launch_bounds__(kSThreads) gemm_mma_sync_kernel(SyncParams p) 
     // fragments are read the same way (pairs of consecutive k).
     __shared__ uint16_t As[2][kSBM][kSBK + kPad];
     __shared__ uint16_t Bs[2][kSBN][kSBK + kPad];
+    ptx::grid_dependency_wait();   // the previous kernel's writes are visible (programmatic launch)
+    ptx::launch_dependents();
     const int64_t num_m_tiles = (p.M + kSBM - 1) / kSBM;
     // grid.y is capped at 65535: CTAs step through the M tiles by gridDim.y
     for (int64_t mt = blockIdx.y; mt < num_m_tiles; mt += gridDim.y) {
@@ -253,8 +256,7 @@ template <int kIn, int kOut, bool kHasC>
 cudaError_t launch_sync_one(const SyncParams& p, cudaStream_t stream) {
     const int64_t m_tiles = (p.M + kSBM - 1) / kSBM;
     const dim3 grid((unsigned)((p.N + kSBN - 1) / kSBN), (unsigned)(m_tiles < 65535 ? m_tiles : 65535));
-    gemm_mma_sync_kernel<kIn, kOut, kHasC><<<grid, kSThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_with_pdl(gemm_mma_sync_kernel<kIn, kOut, kHasC>, grid, dim3(kSThreads), stream, p);
 }
 
 template <int kIn, bool kHasC>
@@ -270,6 +272,8 @@ cudaError_t launch_sync_out(const SyncParams& p, cudaStream_t stream) {
 // elements of a row.
 template <typename T>
 __global__ void copy2d_kernel(T* dst, int64_t ldd, const T* src, int64_t lds, int64_t rows, int64_t cols) {
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
     for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
         for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < cols;
              c += (int64_t)gridDim.x * blockDim.x)
@@ -284,6 +288,8 @@ constexpr int kTT = 32;
 template <typename T>
 __global__ void transpose2d_kernel(T* dst, int64_t ldd, const T* src, int64_t lds, int64_t rows, int64_t cols) {
     __shared__ T tile[kTT][kTT + 1];
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
     const int64_t tiles_r = (rows + kTT - 1) / kTT, tiles_c = (cols + kTT - 1) / kTT;
     for (int64_t br = blockIdx.y; br < tiles_r; br += gridDim.y)
         for (int64_t bc = blockIdx.x; bc < tiles_c; bc += gridDim.x) {
@@ -317,15 +323,13 @@ cudaError_t launch_copy2d(void* dst, int64_t ldd, const void* src, int64_t lds, 
     const int64_t gy = rows < 65535 ? rows : 65535;
     const dim3 grid((unsigned)gx, (unsigned)gy);
     if (elem_bytes == 4)
-        copy2d_kernel<uint32_t><<<grid, kThreads, 0, stream>>>(static_cast<uint32_t*>(dst), ldd,
-                                                               static_cast<const uint32_t*>(src), lds, rows, cols);
-    else if (elem_bytes == 2)
-        copy2d_kernel<uint16_t><<<grid, kThreads, 0, stream>>>(static_cast<uint16_t*>(dst), ldd,
-                                                               static_cast<const uint16_t*>(src), lds, rows, cols);
-    else
-        copy2d_kernel<uint8_t><<<grid, kThreads, 0, stream>>>(static_cast<uint8_t*>(dst), ldd,
-                                                              static_cast<const uint8_t*>(src), lds, rows, cols);
-    return cudaGetLastError();
+        return launch_with_pdl(copy2d_kernel<uint32_t>, grid, dim3(kThreads), stream, static_cast<uint32_t*>(dst),
+                               ldd, static_cast<const uint32_t*>(src), lds, rows, cols);
+    if (elem_bytes == 2)
+        return launch_with_pdl(copy2d_kernel<uint16_t>, grid, dim3(kThreads), stream, static_cast<uint16_t*>(dst),
+                               ldd, static_cast<const uint16_t*>(src), lds, rows, cols);
+    return launch_with_pdl(copy2d_kernel<uint8_t>, grid, dim3(kThreads), stream, static_cast<uint8_t*>(dst), ldd,
+                           static_cast<const uint8_t*>(src), lds, rows, cols);
 }
 
 cudaError_t launch_transpose2d(void* dst, int64_t ldd, const void* src, int64_t lds, int64_t rows, int64_t cols,
@@ -335,12 +339,10 @@ cudaError_t launch_transpose2d(void* dst, int64_t ldd, const void* src, int64_t 
     const dim3 grid((unsigned)(tc < 65535 ? tc : 65535), (unsigned)(tr < 65535 ? tr : 65535));
     const dim3 block(kTT, kTT / 4);
     if (elem_bytes == 2)
-        transpose2d_kernel<uint16_t><<<grid, block, 0, stream>>>(static_cast<uint16_t*>(dst), ldd,
-                                                                 static_cast<const uint16_t*>(src), lds, rows, cols);
-    else
-        transpose2d_kernel<uint8_t><<<grid, block, 0, stream>>>(static_cast<uint8_t*>(dst), ldd,
-                                                                static_cast<const uint8_t*>(src), lds, rows, cols);
-    return cudaGetLastError();
+        return launch_with_pdl(transpose2d_kernel<uint16_t>, grid, block, stream, static_cast<uint16_t*>(dst), ldd,
+                               static_cast<const uint16_t*>(src), lds, rows, cols);
+    return launch_with_pdl(transpose2d_kernel<uint8_t>, grid, block, stream, static_cast<uint8_t*>(dst), ldd,
+                           static_cast<const uint8_t*>(src), lds, rows, cols);
 }
 
 }  // namespace gb300

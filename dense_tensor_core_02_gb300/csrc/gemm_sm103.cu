@@ -10,6 +10,8 @@ namespace gb300 {
 template <int kOut>
 __global__ void gemm_k0_kernel(void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,
                                float beta, int has_c) {
+    ptx::grid_dependency_wait();   // the previous kernel's writes are visible (programmatic launch)
+    ptx::launch_dependents();
     const int64_t total = (int64_t)M * N;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -87,13 +89,12 @@ cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc
     const int64_t cap = (int64_t)num_sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    const dim3 grid((unsigned)blocks), block(256);
     if (out == kOutF32)
-        gemm_k0_kernel<kOutF32><<<(unsigned)blocks, 256, 0, stream>>>(D, C, M, N, ldc, ldd, alpha, beta, has_c);
-    else if (out == kOutF16)
-        gemm_k0_kernel<kOutF16><<<(unsigned)blocks, 256, 0, stream>>>(D, C, M, N, ldc, ldd, alpha, beta, has_c);
-    else
-        gemm_k0_kernel<kOutBF16><<<(unsigned)blocks, 256, 0, stream>>>(D, C, M, N, ldc, ldd, alpha, beta, has_c);
-    return cudaGetLastError();
+        return launch_with_pdl(gemm_k0_kernel<kOutF32>, grid, block, stream, D, C, M, N, ldc, ldd, alpha, beta, has_c);
+    if (out == kOutF16)
+        return launch_with_pdl(gemm_k0_kernel<kOutF16>, grid, block, stream, D, C, M, N, ldc, ldd, alpha, beta, has_c);
+    return launch_with_pdl(gemm_k0_kernel<kOutBF16>, grid, block, stream, D, C, M, N, ldc, ldd, alpha, beta, has_c);
 }
 
 }  // namespace gb300
