@@ -187,7 +187,8 @@ def _workload_config(case, n_gpus):
         "M": case.M, "N": case.N, "K": case.K, "accumulate": "f32", "out_dtype": case.out_dtype,
         "seed": case.seed, "workload_index": CASES.index(case) + 1,
         "l2": "inputs larger than L2 (A+B+D = %.0f MiB > 129 MB), no flush" % (case.algorithmic_bytes / 2 ** 20)
-        if case.algorithmic_bytes > 129e6 else "working set fits in L2; L2 flushed between steps",
+        if case.algorithmic_bytes > 129e6 else
+        "working set fits in L2: a 256 MB write flushes L2 before every launch, outside the timed spans",
         "parallelism": "replicas x%d (each GPU its own full GEMM)" % n_gpus,
     }
 
@@ -303,8 +304,6 @@ def run_ours(args, case):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if small else None
 
     def step():
-        if flush is not None:
-            flush.zero_()
         rc = binding.gemm(Dd, Ad, Bd, Cd, case.M, case.N, case.K, Ad.stride(0), Bd.stride(0), ldc,
                           Dd.stride(0), case.transA, case.transB, case.alpha, case.beta,
                           code[case.in_dtype], code[case.out_dtype], sptr)
@@ -323,35 +322,41 @@ def run_ours(args, case):
     if status != 0:
         raise RuntimeError("device status after warm-up: %s %s" % (binding.gemm_status_string(status), info))
 
+    def timed(n):
+        """Device time (ms) of n launches on the stream.  Working sets that
+        fit in L2 get a flush (a 256 MB write) before every launch, outside
+        the timed spans: each launch is bracketed by its own event pair."""
+        with torch.cuda.stream(stream):
+            if flush is None:
+                e0.record(stream)
+                for _ in range(n):
+                    step()
+                e1.record(stream)
+            else:
+                spans = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                         for _ in range(n)]
+                for a, b in spans:
+                    flush.zero_()
+                    a.record(stream)
+                    step()
+                    b.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) if flush is None else sum(a.elapsed_time(b) for a, b in spans)
+
     # burst: the best of three runs of BURST_STEPS launches, measured the way
     # the burst peak is (a short run, before the power cap sets in); the
     # headline is the long run below, reported against both peaks
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    burst_ms = None
-    for _ in range(3):
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for _ in range(BURST_STEPS):
-                step()
-            e1.record(stream)
-        torch.cuda.synchronize(dev)
-        t = e0.elapsed_time(e1) / BURST_STEPS
-        burst_ms = t if burst_ms is None else min(burst_ms, t)
+    burst_ms = min(timed(BURST_STEPS) for _ in range(3)) / BURST_STEPS
 
     sampler = ClockSampler(local_rank).start() if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     barrier()
     torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-    torch.cuda.synchronize(dev)
+    elapsed_ms = timed(args.steps)
     barrier()
     clocks = sampler.stop() if sampler else None
-    elapsed_ms = e0.elapsed_time(e1)
     status, info = binding.gemm_poll_device_error(stream)
     if status != 0:
         raise RuntimeError("device status after timing: %s %s" % (binding.gemm_status_string(status), info))
@@ -430,18 +435,31 @@ def run_ours(args, case):
     src = ("%s bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json); f16 runs at the bf16 rate" % peak_src
            if rate == 1.0 else
            "%s bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json) x 2, the nominal dense fp8 / bf16 ratio" % peak_src)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": _profiled_traffic(case.name),
-                "peak_source": src,
-                "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak / rate)) * rate),
-                "frac_of_nominal": achieved / (NOMINAL_DENSE_TFLOPS * rate),
-                "algorithmic_flops_per_launch": case.flops,
-                "algorithmic_bytes_per_launch": case.algorithmic_bytes,
-                "achieved_gbs": case.algorithmic_bytes / (per_launch_ms * 1e-3) / 1e9}
+    achieved_gbs = case.algorithmic_bytes / (per_launch_ms * 1e-3) / 1e9
+    hbm = float(peaks["hbm_gbs"])
+    # the bound: below the ridge (peak flop/s / copy bandwidth) the algorithmic
+    # bytes limit the launch, above it the tensor cores do
+    intensity = case.flops / case.algorithmic_bytes
+    ridge = peak * 1e12 / (hbm * 1e9)
     burst_tflops = case.flops / (burst_ms * 1e-3) / 1e12
-    roofline["burst"] = {"launches": BURST_STEPS, "best_of": 3, "ms_per_launch": burst_ms,
-                         "achieved": burst_tflops, "frac": burst_tflops / peak}
-    if clocks and clocks.get("sm_mhz"):
+    if intensity >= ridge:
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                    "frac": achieved / peak, "peak_source": src,
+                    "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak / rate)) * rate),
+                    "frac_of_nominal": achieved / (NOMINAL_DENSE_TFLOPS * rate)}
+        burst = {"achieved": burst_tflops, "frac": burst_tflops / peak}
+    else:
+        roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
+                    "frac": achieved_gbs / hbm,
+                    "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_src,
+                    "achieved_tflops": achieved, "tensor_peak_tflops": peak}
+        burst_gbs = case.algorithmic_bytes / (burst_ms * 1e-3) / 1e9
+        burst = {"achieved": burst_gbs, "frac": burst_gbs / hbm}
+    roofline.update({"traffic": _profiled_traffic(case.name), "arithmetic_intensity": intensity,
+                     "ridge_flop_per_byte": ridge, "algorithmic_flops_per_launch": case.flops,
+                     "algorithmic_bytes_per_launch": case.algorithmic_bytes, "achieved_gbs": achieved_gbs})
+    roofline["burst"] = dict(burst, launches=BURST_STEPS, best_of=3, ms_per_launch=burst_ms)
+    if clocks and clocks.get("sm_mhz") and roofline["bound"] == "tensor":
         clk_peak = num_sms * FLOP_PER_CLK_PER_SM * rate * clocks["sm_mhz"] * 1e6 / 1e12
         roofline["frac_of_clock_peak"] = achieved / clk_peak
         roofline["clock_peak_tflops"] = clk_peak
