@@ -11,6 +11,13 @@ definition in binary64 (TVM TIRx "gemm" page, opening paragraph and the
 gemm_fp16tc_fp32acc.ph epilogue), and the per-element error bound
 ``|alpha| * sum_k |a_ik * b_kj| + |beta| * |c_ij|``.
 
+With ``sfa`` / ``sfb`` given, the 8-bit operands are MX block-scaled: every
+32 consecutive K elements of a row of op(A) share the UE8M0 scale
+``2^(sfa[i, k // 32] - 127)``, and of a column of op(B) the scale
+``2^(sfb[j, k // 32] - 127)`` (``sfa`` is [M, ceil(K/32)], ``sfb`` is
+[N, ceil(K/32)], uint8; 255 is NaN) -- the OCP Microscaling reading of the
+"block scaling (SFA / SFB)" the TIRx gemm guide lists in section 七.
+
 Inputs are numpy arrays or torch CPU tensors: A and B hold fp16 / bf16
 bits, or E4M3 / E5M2 bits (one byte each; the 8-bit precisions of the
 tcgen05 path the TIRx gemm guide lists in section 七); C holds fp32 (or
@@ -98,6 +105,19 @@ def _c_array(c, c_dtype):
     return _bits16(c)
 
 
+def _scales(x):
+    """A 2-D uint8 array of UE8M0 scale bytes."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().cpu().contiguous().view(torch.uint8).numpy()
+    x = np.ascontiguousarray(x)
+    if x.dtype not in (np.uint8, np.int8):
+        raise TypeError("uint8 scales expected, got %s" % x.dtype)
+    return x.view(np.uint8)
+
+
 def _ptr(a):
     return None if a is None else a.ctypes.data
 
@@ -126,6 +146,15 @@ class Oracle:
         lib.oracle_gemm_entries.restype = i32
         lib.oracle_gemm_entries.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, i64, i64, i64,
                                             i64, i64, i64, i32, i32, dbl, dbl, i32, i32]
+        lib.oracle_decode_ue8m0.restype = dbl
+        lib.oracle_decode_ue8m0.argtypes = [ctypes.c_uint8]
+        lib.oracle_gemm_mx.restype = i32
+        lib.oracle_gemm_mx.argtypes = [vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64,
+                                       i64, i64, i64, i32, i32, dbl, dbl, i32, i32, i64, i64]
+        lib.oracle_gemm_mx_entries.restype = i32
+        lib.oracle_gemm_mx_entries.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, i64, i64,
+                                               i64, i64, i64, i64, i64, i64, i32, i32, dbl, dbl,
+                                               i32, i32]
         self.lib = lib
         self.path = path
 
@@ -141,15 +170,20 @@ class Oracle:
     def decode_e5m2(self, bits: int) -> float:
         return self.lib.oracle_decode_e5m2(int(bits))
 
+    def decode_ue8m0(self, bits: int) -> float:
+        return self.lib.oracle_decode_ue8m0(int(bits))
+
     def gemm(self, A, B, C, M, N, K, *, transA=0, transB=0, alpha=1.0, beta=0.0,
              in_dtype=F16, c_dtype=F32, lda=None, ldb=None, ldc=None,
-             rows=None, threads=1):
+             rows=None, threads=1, sfa=None, sfb=None, ld_sfa=None, ld_sfb=None):
         """Full rows of D (all rows unless ``rows=(begin, end)``).
 
         Returns ``(D, bound)``: float64 arrays of shape [M, N]; rows outside
         the requested range stay NaN.  ``threads > 1`` runs disjoint row
-        blocks of the same single-threaded C loop concurrently.
+        blocks of the same single-threaded C loop concurrently.  ``sfa`` and
+        ``sfb`` (both or neither) make the 8-bit operands MX block-scaled.
         """
+        mx = _mx_args(sfa, sfb, ld_sfa, ld_sfb, K)
         Ab, Bb = _operand(A, in_dtype), _operand(B, in_dtype)
         C_ = _c_array(C, c_dtype) if beta != 0.0 else None
         lda = lda if lda is not None else _ld(Ab, M if transA else K)
@@ -161,9 +195,16 @@ class Oracle:
         lib = self.lib
 
         def run(a, b):
-            rc = lib.oracle_gemm(D.ctypes.data, bound.ctypes.data, N, _ptr(Ab), _ptr(Bb),
-                                 _ptr(C_), M, N, K, lda, ldb, ldc, int(transA), int(transB),
-                                 float(alpha), float(beta), int(in_dtype), int(c_dtype), a, b)
+            if mx is None:
+                rc = lib.oracle_gemm(D.ctypes.data, bound.ctypes.data, N, _ptr(Ab), _ptr(Bb),
+                                     _ptr(C_), M, N, K, lda, ldb, ldc, int(transA), int(transB),
+                                     float(alpha), float(beta), int(in_dtype), int(c_dtype), a, b)
+            else:
+                sa, sb, la, lb = mx
+                rc = lib.oracle_gemm_mx(D.ctypes.data, bound.ctypes.data, N, _ptr(Ab), _ptr(Bb),
+                                        _ptr(C_), _ptr(sa), _ptr(sb), M, N, K, lda, ldb, ldc, la, lb,
+                                        int(transA), int(transB), float(alpha), float(beta),
+                                        int(in_dtype), int(c_dtype), a, b)
             if rc != 0:
                 raise ValueError("oracle_gemm rejected its arguments")
 
@@ -177,8 +218,9 @@ class Oracle:
 
     def gemm_entries(self, A, B, C, M, N, K, rows, cols, *, transA=0, transB=0, alpha=1.0,
                      beta=0.0, in_dtype=F16, c_dtype=F32, lda=None, ldb=None, ldc=None,
-                     threads=1):
+                     threads=1, sfa=None, sfb=None, ld_sfa=None, ld_sfb=None):
         """D and bound at the listed (rows[e], cols[e]) positions only."""
+        mx = _mx_args(sfa, sfb, ld_sfa, ld_sfb, K)
         Ab, Bb = _operand(A, in_dtype), _operand(B, in_dtype)
         C_ = _c_array(C, c_dtype) if beta != 0.0 else None
         lda = lda if lda is not None else _ld(Ab, M if transA else K)
@@ -192,11 +234,20 @@ class Oracle:
         lib = self.lib
 
         def run(a, b):
-            rc = lib.oracle_gemm_entries(D[a:].ctypes.data, bound[a:].ctypes.data,
-                                         rows[a:].ctypes.data, cols[a:].ctypes.data, b - a,
-                                         _ptr(Ab), _ptr(Bb), _ptr(C_), M, N, K, lda, ldb, ldc,
-                                         int(transA), int(transB), float(alpha), float(beta),
-                                         int(in_dtype), int(c_dtype))
+            if mx is None:
+                rc = lib.oracle_gemm_entries(D[a:].ctypes.data, bound[a:].ctypes.data,
+                                             rows[a:].ctypes.data, cols[a:].ctypes.data, b - a,
+                                             _ptr(Ab), _ptr(Bb), _ptr(C_), M, N, K, lda, ldb, ldc,
+                                             int(transA), int(transB), float(alpha), float(beta),
+                                             int(in_dtype), int(c_dtype))
+            else:
+                sa, sb, la, lb = mx
+                rc = lib.oracle_gemm_mx_entries(D[a:].ctypes.data, bound[a:].ctypes.data,
+                                                rows[a:].ctypes.data, cols[a:].ctypes.data, b - a,
+                                                _ptr(Ab), _ptr(Bb), _ptr(C_), _ptr(sa), _ptr(sb),
+                                                M, N, K, lda, ldb, ldc, la, lb,
+                                                int(transA), int(transB), float(alpha),
+                                                float(beta), int(in_dtype), int(c_dtype))
             if rc != 0:
                 raise ValueError("oracle_gemm_entries rejected its arguments")
 
@@ -209,6 +260,18 @@ class Oracle:
             with _cf.ThreadPoolExecutor(threads) as ex:
                 list(ex.map(lambda a: run(a, min(a + step, n)), range(0, n, step)))
         return D, bound
+
+
+def _mx_args(sfa, sfb, ld_sfa, ld_sfb, K):
+    """(sfa, sfb, ld_sfa, ld_sfb) as the C oracle takes them, or None."""
+    if sfa is None and sfb is None:
+        return None
+    if sfa is None or sfb is None:
+        raise ValueError("block scaling needs both sfa and sfb")
+    sa, sb = _scales(sfa), _scales(sfb)
+    kb = (K + 31) // 32
+    return (sa, sb, ld_sfa if ld_sfa is not None else _ld(sa, kb),
+            ld_sfb if ld_sfb is not None else _ld(sb, kb))
 
 
 _default = None
@@ -246,3 +309,7 @@ def decode_e4m3(bits):
 
 def decode_e5m2(bits):
     return default().decode_e5m2(bits)
+
+
+def decode_ue8m0(bits):
+    return default().decode_ue8m0(bits)

@@ -41,6 +41,20 @@
  * sum of |products| is kept alongside, so the caller can form the
  * per-element error bound  |alpha| * sum|a*b| + |beta| * |c|.
  *
+ * Block-scaled 8-bit operands (oracle_gemm_mx*): the TIRx gemm guide lists
+ * block scaling with separate A and B scale factors ("SFA/SFB") among the
+ * asynchronous path's modes (section 七) without defining it.  The reading
+ * taken is the OCP Microscaling (MX) one: each run of 32 consecutive K
+ * elements of a row of Ahat shares one scale SFA[i][k / 32], and of a column
+ * of Bhat one scale SFB[j][k / 32]; a scale is a UE8M0 byte e standing for
+ * 2^(e - 127) (e = 255: NaN).  The definition becomes
+ *
+ *     D[i][j] = alpha * sum_k (SFA[i][k/32] * Ahat[i][k]) * (SFB[j][k/32] * Bhat[k][j])
+ *               + beta * C[i][j]
+ *
+ * with SFA stored [M, ceil(K/32)] and SFB stored [N, ceil(K/32)], row-major
+ * with row strides ld_sfa / ld_sfb, whatever transA / transB say.
+ *
  * Build: a plain C99 compiler, -O2, -ffp-contract=off (no fused
  * multiply-add, no fast-math), so that x86-64 and aarch64 give the same
  * bits.
@@ -122,6 +136,16 @@ double oracle_decode_e5m2(uint8_t b)
     return sign ? -v : v;
 }
 
+/* UE8M0, the MX shared scale: 8 exponent bits (bias 127), no sign and no
+ * fraction, so the value is 2^(e - 127); the all-ones pattern is NaN. */
+double oracle_decode_ue8m0(uint8_t e)
+{
+    return e == 0xFFu ? NAN : ldexp(1.0, (int)e - 127);
+}
+
+/* K elements per MX scale block */
+#define MX_BLOCK 32
+
 /* binary32 -> binary64 is exact. */
 static double decode_f32(const void* p)
 {
@@ -174,6 +198,9 @@ typedef struct {
     const double* in_table;   /* decoder for A and B */
     int in_bytes;             /* bytes per A / B element: 2 (fp16, bf16) or 1 (fp8) */
     int c_dtype;
+    const uint8_t* SFA;       /* MX scales of Ahat's rows, or NULL (no block scaling) */
+    const uint8_t* SFB;       /* MX scales of Bhat's columns */
+    int64_t ld_sfa, ld_sfb;
 } problem_t;
 
 /* The bit pattern of operand element `idx` (elements of in_bytes bytes). */
@@ -182,18 +209,22 @@ static unsigned operand_bits(const problem_t* p, const void* X, int64_t idx)
     return p->in_bytes == 1 ? ((const uint8_t*)X)[idx] : ((const uint16_t*)X)[idx];
 }
 
-/* Ahat[i][k] */
+/* Ahat[i][k], times its block's scale when the operands are block-scaled */
 static double a_hat(const problem_t* p, int64_t i, int64_t k)
 {
     int64_t idx = p->transA ? k * p->lda + i : i * p->lda + k;
-    return p->in_table[operand_bits(p, p->A, idx)];
+    double v = p->in_table[operand_bits(p, p->A, idx)];
+    if (p->SFA != NULL) v *= oracle_decode_ue8m0(p->SFA[i * p->ld_sfa + k / MX_BLOCK]);
+    return v;
 }
 
-/* Bhat[k][j] */
+/* Bhat[k][j], likewise */
 static double b_hat(const problem_t* p, int64_t k, int64_t j)
 {
     int64_t idx = p->transB ? j * p->ldb + k : k * p->ldb + j;
-    return p->in_table[operand_bits(p, p->B, idx)];
+    double v = p->in_table[operand_bits(p, p->B, idx)];
+    if (p->SFB != NULL) v *= oracle_decode_ue8m0(p->SFB[j * p->ld_sfb + k / MX_BLOCK]);
+    return v;
 }
 
 static double c_elem(const problem_t* p, int64_t i, int64_t j)
@@ -252,6 +283,46 @@ static int setup(problem_t* p, const void* A, const void* B, const void* C,
     p->in_table = table_for(in_dtype);
     p->in_bytes = (in_dtype == ORACLE_E4M3 || in_dtype == ORACLE_E5M2) ? 1 : 2;
     p->c_dtype = c_dtype;
+    p->SFA = NULL;
+    p->SFB = NULL;
+    p->ld_sfa = p->ld_sfb = 0;
+    return 0;
+}
+
+/* Block scales on top of setup(): 8-bit operands only, both scale arrays
+ * present whenever they are read, rows of ceil(K/32) scales. */
+static int setup_mx(problem_t* p, const void* SFA, const void* SFB, int64_t ld_sfa, int64_t ld_sfb)
+{
+    const int64_t kb = (p->K + MX_BLOCK - 1) / MX_BLOCK;
+    if (p->in_bytes != 1) return -1;
+    if ((p->M > 0 && p->K > 0 && SFA == NULL) || (p->N > 0 && p->K > 0 && SFB == NULL)) return -1;
+    if (p->K > 0 && (ld_sfa < kb || ld_sfb < kb)) return -1;
+    p->SFA = (const uint8_t*)SFA;
+    p->SFB = (const uint8_t*)SFB;
+    p->ld_sfa = ld_sfa;
+    p->ld_sfb = ld_sfb;
+    return 0;
+}
+
+/* Full rows [row_begin, row_end) of D into D and bound (row stride ldo). */
+static int rows_of(const problem_t* p, double* D, double* bound, int64_t ldo,
+                   int64_t row_begin, int64_t row_end)
+{
+    if (row_begin < 0 || row_end > p->M || row_begin > row_end || ldo < p->N) return -1;
+    for (int64_t i = row_begin; i < row_end; ++i)
+        for (int64_t j = 0; j < p->N; ++j)
+            D[i * ldo + j] = one_element(p, i, j, &bound[i * ldo + j]);
+    return 0;
+}
+
+/* The listed elements (rows[e], cols[e]), e < count, into D[e], bound[e]. */
+static int entries_of(const problem_t* p, double* D, double* bound,
+                      const int64_t* rows, const int64_t* cols, int64_t count)
+{
+    for (int64_t e = 0; e < count; ++e)
+        if (rows[e] < 0 || rows[e] >= p->M || cols[e] < 0 || cols[e] >= p->N) return -1;
+    for (int64_t e = 0; e < count; ++e)
+        D[e] = one_element(p, rows[e], cols[e], &bound[e]);
     return 0;
 }
 
@@ -270,11 +341,7 @@ int oracle_gemm(double* D, double* bound, int64_t ldo,
     if (setup(&p, A, B, C, M, N, K, lda, ldb, ldc, transA, transB, alpha, beta,
               in_dtype, c_dtype) != 0)
         return -1;
-    if (row_begin < 0 || row_end > M || row_begin > row_end || ldo < N) return -1;
-    for (int64_t i = row_begin; i < row_end; ++i)
-        for (int64_t j = 0; j < N; ++j)
-            D[i * ldo + j] = one_element(&p, i, j, &bound[i * ldo + j]);
-    return 0;
+    return rows_of(&p, D, bound, ldo, row_begin, row_end);
 }
 
 /* The listed elements (rows[e], cols[e]) only, e < count: D[e], bound[e]. */
@@ -290,9 +357,42 @@ int oracle_gemm_entries(double* D, double* bound,
     if (setup(&p, A, B, C, M, N, K, lda, ldb, ldc, transA, transB, alpha, beta,
               in_dtype, c_dtype) != 0)
         return -1;
-    for (int64_t e = 0; e < count; ++e)
-        if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N) return -1;
-    for (int64_t e = 0; e < count; ++e)
-        D[e] = one_element(&p, rows[e], cols[e], &bound[e]);
-    return 0;
+    return entries_of(&p, D, bound, rows, cols, count);
+}
+
+/* oracle_gemm with MX block-scaled 8-bit operands (scales SFA [M, ceil(K/32)]
+ * and SFB [N, ceil(K/32)], UE8M0 bytes). */
+int oracle_gemm_mx(double* D, double* bound, int64_t ldo,
+                   const void* A, const void* B, const void* C,
+                   const void* SFA, const void* SFB,
+                   int64_t M, int64_t N, int64_t K,
+                   int64_t lda, int64_t ldb, int64_t ldc, int64_t ld_sfa, int64_t ld_sfb,
+                   int transA, int transB, double alpha, double beta,
+                   int in_dtype, int c_dtype,
+                   int64_t row_begin, int64_t row_end)
+{
+    problem_t p;
+    if (setup(&p, A, B, C, M, N, K, lda, ldb, ldc, transA, transB, alpha, beta,
+              in_dtype, c_dtype) != 0 ||
+        setup_mx(&p, SFA, SFB, ld_sfa, ld_sfb) != 0)
+        return -1;
+    return rows_of(&p, D, bound, ldo, row_begin, row_end);
+}
+
+/* oracle_gemm_entries with MX block-scaled 8-bit operands. */
+int oracle_gemm_mx_entries(double* D, double* bound,
+                           const int64_t* rows, const int64_t* cols, int64_t count,
+                           const void* A, const void* B, const void* C,
+                           const void* SFA, const void* SFB,
+                           int64_t M, int64_t N, int64_t K,
+                           int64_t lda, int64_t ldb, int64_t ldc, int64_t ld_sfa, int64_t ld_sfb,
+                           int transA, int transB, double alpha, double beta,
+                           int in_dtype, int c_dtype)
+{
+    problem_t p;
+    if (setup(&p, A, B, C, M, N, K, lda, ldb, ldc, transA, transB, alpha, beta,
+              in_dtype, c_dtype) != 0 ||
+        setup_mx(&p, SFA, SFB, ld_sfa, ld_sfb) != 0)
+        return -1;
+    return entries_of(&p, D, bound, rows, cols, count);
 }

@@ -17,7 +17,14 @@ plain mathematics fix:
   "gemm" page, "What it accepts" table, alpha / beta row: 0 -> D = A@B,
   1 -> D = A@B + C), transpose equivalence (the flags only name the
   logical orientation), linearity in alpha and beta, a closed-form sum and
-  the error bound's own identities.
+  the error bound's own identities;
+* MX block scaling (the OCP Microscaling reading of the TIRx gemm guide's
+  "block scaling (SFA / SFB)", section 七): the UE8M0 decoder against
+  torch's float8_e8m0fnu conversion, exact rational brute force with scale
+  blocks of 32 along K (ragged last block, padded scale rows), unit scales
+  reducing to the unscaled product, exact doubling of a row / column when
+  its scales go up by one, invariance when a block's scale moves from A to
+  B, a closed form at a block boundary and NaN scales.
 
 ``tests/test_oracle_mutants.py`` runs the same pins against deliberately
 broken builds of the oracle and requires each break to be caught.
@@ -363,6 +370,204 @@ def pin_rejects_bad_arguments(orc):
         raise AssertionError("oracle accepted malformed arguments %s" % kw)
 
 
+# ---- MX block scaling ------------------------------------------------------
+
+UE8M0_NAN = 0xFF
+
+
+def pin_ue8m0_decoder(orc):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = np.array([orc.decode_ue8m0(x) for x in range(256)])
+    assert _same(got, ref), "UE8M0 decoder disagrees with torch's float8_e8m0fnu"
+    assert orc.decode_ue8m0(127) == 1.0 and orc.decode_ue8m0(128) == 2.0 and orc.decode_ue8m0(126) == 0.5
+    assert orc.decode_ue8m0(0) == 2.0 ** -127 and orc.decode_ue8m0(254) == 2.0 ** 127
+    assert np.isnan(orc.decode_ue8m0(UE8M0_NAN))
+
+
+def _mx_case(rng, M, N, K, transA, transB, dtype, lo=121, hi=133):
+    """Integer-valued 8-bit operands, scales in [lo, hi], scale rows padded
+    with NaN scales (so a scale read from the padding shows)."""
+    A = torch.from_numpy(rng.integers(-8, 9, size=(K, M) if transA else (M, K)).astype(np.float32)).to(_TD[dtype])
+    B = torch.from_numpy(rng.integers(-8, 9, size=(N, K) if transB else (K, N)).astype(np.float32)).to(_TD[dtype])
+    kb = (K + 31) // 32
+    sfa = np.full((M, kb + 3), UE8M0_NAN, dtype=np.uint8)
+    sfb = np.full((N, kb + 1), UE8M0_NAN, dtype=np.uint8)
+    sfa[:, :kb] = rng.integers(lo, hi + 1, size=(M, kb))
+    sfb[:, :kb] = rng.integers(lo, hi + 1, size=(N, kb))
+    return A, B, sfa, sfb
+
+
+def _mx_brute(A, B, sfa, sfb, C, transA, transB, alpha, beta):
+    """Exact D by the definition in Python rationals."""
+    from fractions import Fraction
+    a = _as_int_lists(A.float())
+    b = _as_int_lists(B.float())
+    M = len(a[0]) if transA else len(a)
+    K = len(a) if transA else len(a[0])
+    N = len(b) if transB else len(b[0])
+    out = []
+    for i in range(M):
+        row = []
+        for j in range(N):
+            acc = Fraction(0)
+            for k in range(K):
+                x = a[k][i] if transA else a[i][k]
+                y = b[j][k] if transB else b[k][j]
+                e = int(sfa[i, k // 32]) + int(sfb[j, k // 32]) - 254
+                acc += Fraction(x * y) * (Fraction(2) ** e)
+            d = Fraction(alpha) * acc
+            if beta != 0:
+                d += Fraction(beta) * Fraction(float(C[i, j]))
+            row.append(float(d))
+        out.append(row)
+    return np.array(out, dtype=np.float64)
+
+
+def pin_mx_brute_force(orc):
+    rng = np.random.default_rng(53)
+    for dtype in (E4M3, E5M2):
+        for (M, N, K) in ((3, 4, 70), (2, 5, 32), (4, 3, 33), (1, 1, 1), (5, 2, 96)):
+            for transA in (0, 1):
+                for transB in (0, 1):
+                    A, B, sfa, sfb = _mx_case(rng, M, N, K, transA, transB, dtype)
+                    Ab, lda = _padded8(A, 5)
+                    Bb, ldb = _padded8(B, 3)
+                    C = rng.integers(-50, 51, size=(M, N)).astype(np.float32)
+                    for alpha, beta in ((1, 0), (-0.5, 1)):
+                        D, _ = orc.gemm(Ab, Bb, C, M, N, K, transA=transA, transB=transB, alpha=alpha,
+                                        beta=beta, in_dtype=dtype, lda=lda, ldb=ldb, sfa=sfa, sfb=sfb)
+                        ref = _mx_brute(A, B, sfa, sfb, C, transA, transB, alpha, beta)
+                        assert np.array_equal(D, ref), "MX brute force mismatch %s trans=%d%d dtype=%d" % (
+                            (M, N, K), transA, transB, dtype)
+
+
+def pin_mx_unit_scales(orc):
+    """Scale 127 (= 1) everywhere: the unscaled 8-bit product, bit for bit."""
+    rng = np.random.default_rng(59)
+    M, N, K = 7, 9, 100
+    for dtype in (E4M3, E5M2):
+        A = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(_TD[dtype])
+        B = torch.from_numpy(rng.standard_normal((N, K)).astype(np.float32)).to(_TD[dtype])
+        ones_a = np.full((M, 4), 127, dtype=np.uint8)
+        ones_b = np.full((N, 4), 127, dtype=np.uint8)
+        D, bound = orc.gemm(A, B, None, M, N, K, transB=1, in_dtype=dtype, sfa=ones_a, sfb=ones_b)
+        D0, bound0 = orc.gemm(A, B, None, M, N, K, transB=1, in_dtype=dtype)
+        assert _same(D, D0) and _same(bound, bound0), "unit scales change the product"
+
+
+def pin_mx_row_column_scaling(orc):
+    """One more on every scale of row i of A doubles row i of D exactly; two
+    more on column j's scales of B quadruple column j; nothing else moves."""
+    rng = np.random.default_rng(61)
+    M, N, K = 6, 5, 80
+    A, B, sfa, sfb = _mx_case(rng, M, N, K, 0, 1, E4M3)
+    D, _ = orc.gemm(A, B, None, M, N, K, transB=1, in_dtype=E4M3, sfa=sfa, sfb=sfb)
+    kb = 3
+    sfa2 = sfa.copy()
+    sfa2[2, :kb] += 1
+    D2, _ = orc.gemm(A, B, None, M, N, K, transB=1, in_dtype=E4M3, sfa=sfa2, sfb=sfb)
+    ref = D.copy()
+    ref[2, :] *= 2
+    assert _same(D2, ref), "raising one row's scales must double that row only"
+    sfb2 = sfb.copy()
+    sfb2[4, :kb] += 2
+    D3, _ = orc.gemm(A, B, None, M, N, K, transB=1, in_dtype=E4M3, sfa=sfa, sfb=sfb2)
+    ref = D.copy()
+    ref[:, 4] *= 4
+    assert _same(D3, ref), "raising one column's scales must quadruple that column only"
+
+
+def pin_mx_block_exchange(orc):
+    """Moving a factor 2^e from A's scales of block kb to B's leaves D
+    unchanged; moving it into another block changes it."""
+    rng = np.random.default_rng(67)
+    M, N, K = 4, 6, 96
+    A, B, sfa, sfb = _mx_case(rng, M, N, K, 1, 0, E5M2)
+    D, _ = orc.gemm(A, B, None, M, N, K, transA=1, in_dtype=E5M2, sfa=sfa, sfb=sfb)
+    sfa2, sfb2 = sfa.copy(), sfb.copy()
+    sfa2[:, 1] += 3
+    sfb2[:, 1] -= 3
+    D2, _ = orc.gemm(A, B, None, M, N, K, transA=1, in_dtype=E5M2, sfa=sfa2, sfb=sfb2)
+    assert _same(D, D2), "a factor moved between A's and B's scales of one block changed D"
+    sfb3 = sfb.copy()
+    sfb3[:, 2] -= 3
+    D3, _ = orc.gemm(A, B, None, M, N, K, transA=1, in_dtype=E5M2, sfa=sfa2, sfb=sfb3)
+    assert not _same(D, D3), "scales of different blocks must not cancel"
+
+
+def pin_mx_block_boundary(orc):
+    """Elements k = 31 and k = 32 fall in blocks 0 and 1: closed form."""
+    K = 64
+    A = torch.zeros((1, K), dtype=torch.float8_e4m3fn)
+    B = torch.zeros((1, K), dtype=torch.float8_e4m3fn)
+    A[0, 31] = 3.0
+    A[0, 32] = 5.0
+    B[0, 31] = 2.0
+    B[0, 32] = 7.0
+    sfa = np.array([[130, 120]], dtype=np.uint8)   # 2^3, 2^-7
+    sfb = np.array([[125, 131]], dtype=np.uint8)   # 2^-2, 2^4
+    D, bound = orc.gemm(A, B, None, 1, 1, K, transB=1, in_dtype=E4M3, sfa=sfa, sfb=sfb)
+    want = 3 * 2 * 2.0 ** (3 - 2) + 5 * 7 * 2.0 ** (-7 + 4)
+    assert D[0, 0] == want and bound[0, 0] == want, "block boundary misplaced"
+
+
+def pin_mx_nan_scale(orc):
+    """A NaN scale (0xFF) makes its block NaN: every D element whose sum
+    takes a product from that block is NaN, the rest are finite."""
+    rng = np.random.default_rng(71)
+    M, N, K = 4, 3, 64
+    A, B, sfa, sfb = _mx_case(rng, M, N, K, 0, 0, E4M3)
+    sfa = np.ascontiguousarray(sfa[:, :2])
+    sfb = np.ascontiguousarray(sfb[:, :2])
+    sfa[1, 1] = UE8M0_NAN
+    sfb[2, 0] = UE8M0_NAN
+    D, _ = orc.gemm(A, B, None, M, N, K, in_dtype=E4M3, sfa=sfa, sfb=sfb)
+    expect_nan = np.zeros((M, N), dtype=bool)
+    expect_nan[1, :] = True
+    expect_nan[:, 2] = True
+    assert np.array_equal(np.isnan(D), expect_nan), "NaN scales propagate wrongly"
+
+
+def pin_mx_numpy_float64(orc):
+    rng = np.random.default_rng(73)
+    M, N, K = 13, 11, 150
+    kb = (K + 31) // 32
+    for dtype in (E4M3, E5M2):
+        A = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(_TD[dtype])
+        B = torch.from_numpy(rng.standard_normal((N, K)).astype(np.float32)).to(_TD[dtype])
+        sfa = rng.integers(110, 140, size=(M, kb)).astype(np.uint8)
+        sfb = rng.integers(110, 140, size=(N, kb)).astype(np.uint8)
+        C = rng.standard_normal((M, N)).astype(np.float32)
+        D, bound = orc.gemm(A, B, C, M, N, K, transB=1, alpha=1.25, beta=0.5, in_dtype=dtype,
+                            sfa=sfa, sfb=sfb)
+        ea = np.repeat(sfa.astype(np.float64) - 127.0, 32, axis=1)[:, :K]
+        eb = np.repeat(sfb.astype(np.float64) - 127.0, 32, axis=1)[:, :K]
+        a = A.double().numpy() * np.exp2(ea)
+        b = B.double().numpy() * np.exp2(eb)
+        ref = 1.25 * (a @ b.T) + 0.5 * C.astype(np.float64)
+        assert np.all(np.abs(D - ref) <= 1e-12 * bound), "MX numpy float64 mismatch (dtype=%d)" % dtype
+
+
+def pin_mx_rejects_bad_arguments(orc):
+    A8 = torch.zeros((4, 64), dtype=torch.float8_e4m3fn)
+    A16 = torch.zeros((4, 64), dtype=torch.float16)
+    s2 = np.zeros((4, 2), dtype=np.uint8)
+    s1 = np.zeros((4, 1), dtype=np.uint8)
+    bad = [
+        (A16, dict(in_dtype=F16, sfa=s2, sfb=s2)),       # block scaling is for 8-bit operands
+        (A8, dict(in_dtype=E4M3, sfa=s1, sfb=s2)),       # a scale row shorter than ceil(K/32)
+        (A8, dict(in_dtype=E4M3, sfa=s2, sfb=s1)),
+        (A8, dict(in_dtype=E4M3, sfa=s2, sfb=None)),     # both scale arrays or neither
+    ]
+    for A, kw in bad:
+        try:
+            orc.gemm(A, A, None, 4, 4, 64, transB=1, **kw)
+        except ValueError:
+            continue
+        raise AssertionError("oracle accepted malformed block-scaled arguments %s" % list(kw))
+
+
 ALL_PINS = [
     pin_decoders,
     pin_fp8_decoders,
@@ -380,4 +585,13 @@ ALL_PINS = [
     pin_entries_match_rows,
     pin_16bit_c,
     pin_rejects_bad_arguments,
+    pin_ue8m0_decoder,
+    pin_mx_brute_force,
+    pin_mx_unit_scales,
+    pin_mx_row_column_scaling,
+    pin_mx_block_exchange,
+    pin_mx_block_boundary,
+    pin_mx_nan_scale,
+    pin_mx_numpy_float64,
+    pin_mx_rejects_bad_arguments,
 ]

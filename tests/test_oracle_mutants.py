@@ -30,8 +30,8 @@ MUTANTS = {
     "first_k_dropped": ("for (int64_t k = 0; k < p->K; ++k) {", "for (int64_t k = 1; k < p->K; ++k) {"),
     "sign_of_product": ("double prod = a_hat(p, i, k) * b_hat(p, k, j);",
                         "double prod = fabs(a_hat(p, i, k)) * b_hat(p, k, j);"),
-    "output_transposed": ("D[i * ldo + j] = one_element(&p, i, j, &bound[i * ldo + j]);",
-                          "D[i * ldo + j] = one_element(&p, j % p.M, i % p.N, &bound[i * ldo + j]);"),
+    "output_transposed": ("D[i * ldo + j] = one_element(p, i, j, &bound[i * ldo + j]);",
+                          "D[i * ldo + j] = one_element(p, j % p->M, i % p->N, &bound[i * ldo + j]);"),
     "f16_exponent_bias": ("v = ldexp((double)(1024 + f), e - 25);", "v = ldexp((double)(1024 + f), e - 24);"),
     "f16_subnormal_scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
     "bf16_subnormal_scale": ("v = ldexp((double)f, -133);", "v = ldexp((double)f, -126);"),
@@ -50,8 +50,16 @@ MUTANTS = {
                          "v = ldexp((double)(4 + f), e - 17);\n    else\n        v = ldexp((double)(4 + f), e - 17);"),
     "fp8_read_as_16bit": ("return p->in_bytes == 1 ?", "return p->in_bytes == 0 ?"),
     "fp8_table_swapped": ("case ORACLE_E4M3: return g_e4m3_table;", "case ORACLE_E4M3: return g_e5m2_table;"),
-    "entries_use_col_as_row": ("D[e] = one_element(&p, rows[e], cols[e], &bound[e]);",
-                               "D[e] = one_element(&p, rows[e], cols[e] % (p.N > 1 ? p.N - 1 : 1), &bound[e]);"),
+    "mx_sfa_block_16": ("p->SFA[i * p->ld_sfa + k / MX_BLOCK]", "p->SFA[i * p->ld_sfa + k / 16]"),
+    "mx_sfb_block_64": ("p->SFB[j * p->ld_sfb + k / MX_BLOCK]", "p->SFB[j * p->ld_sfb + k / 64]"),
+    "mx_sfa_row_stride_of_sfb": ("p->SFA[i * p->ld_sfa + k / MX_BLOCK]", "p->SFA[i * p->ld_sfb + k / MX_BLOCK]"),
+    "mx_sfb_dropped": ("if (p->SFB != NULL) v *=", "if (0) v *="),
+    "mx_scale_bias_128": ("ldexp(1.0, (int)e - 127)", "ldexp(1.0, (int)e - 128)"),
+    "mx_nan_scale_missing": ("e == 0xFFu ? NAN :", "0 ? NAN :"),
+    "mx_scale_row_check_missing": ("if (p->K > 0 && (ld_sfa < kb || ld_sfb < kb)) return -1;", ""),
+    "mx_16bit_accepted": ("if (p->in_bytes != 1) return -1;", ""),
+    "entries_use_col_as_row": ("D[e] = one_element(p, rows[e], cols[e], &bound[e]);",
+                               "D[e] = one_element(p, rows[e], cols[e] % (p->N > 1 ? p->N - 1 : 1), &bound[e]);"),
 }
 
 
