@@ -180,9 +180,10 @@ def _args():
 def _workload_config(case, n_gpus):
     from dense_tensor_core_02_gb300.inputs import CASES
     dist = ("N(0,%g)" % case.std) if case.dist == "normal" else "U[-1,1]"
+    mx = (", MX block scales (UE8M0 per 32 K, bytes U{%d..%d})" % (case.sf_lo, case.sf_hi)) if case.mx else ""
     return {
-        "workload": "%s: M=%d N=%d K=%d, %s A/B %s, %s D, alpha=%g beta=%g, transA=%d transB=%d" % (
-            case.name, case.M, case.N, case.K, case.in_dtype, dist, case.out_dtype, case.alpha, case.beta,
+        "workload": "%s: M=%d N=%d K=%d, %s A/B %s%s, %s D, alpha=%g beta=%g, transA=%d transB=%d" % (
+            case.name, case.M, case.N, case.K, case.in_dtype, dist, mx, case.out_dtype, case.alpha, case.beta,
             case.transA, case.transB),
         "M": case.M, "N": case.N, "K": case.K, "accumulate": "f32", "out_dtype": case.out_dtype,
         "seed": case.seed, "workload_index": CASES.index(case) + 1,
@@ -203,9 +204,10 @@ def _oracle_sampler(case):
     import numpy as np
 
     import oracle.oracle as oracle
-    from dense_tensor_core_02_gb300.inputs import make_inputs
+    from dense_tensor_core_02_gb300.inputs import make_inputs, make_scales
 
     A, B, C = make_inputs(case)
+    sf = dict(zip(("sfa", "sfb"), (x.numpy() for x in make_scales(case)))) if case.mx else {}
     threads = len(os.sched_getaffinity(0))
     rng = np.random.default_rng(case.seed)
     code = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4}
@@ -216,7 +218,7 @@ def _oracle_sampler(case):
         t0 = time.perf_counter()
         oracle.gemm_entries(A, B, C, case.M, case.N, case.K, rows, cols, transA=case.transA,
                             transB=case.transB, alpha=case.alpha, beta=case.beta,
-                            in_dtype=code[case.in_dtype], c_dtype=code[case.out_dtype], threads=threads)
+                            in_dtype=code[case.in_dtype], c_dtype=code[case.out_dtype], threads=threads, **sf)
         return time.perf_counter() - t0
 
     return run, threads
@@ -278,7 +280,7 @@ def run_ours(args, case):
     import torch
 
     from dense_tensor_core_02_gb300 import binding
-    from dense_tensor_core_02_gb300.inputs import make_inputs
+    from dense_tensor_core_02_gb300.inputs import make_inputs, make_scales
 
     rank, world, local_rank = _rank_info()
     dist = None
@@ -295,6 +297,11 @@ def run_ours(args, case):
     A, B, C = make_inputs(case)
     Ad, Bd = A.to(dev), B.to(dev)
     Cd = C.to(dev) if C is not None else None
+    SFA, SFB = make_scales(case) if case.mx else (None, None)
+    SFAd = SFA.to(dev) if SFA is not None else None
+    SFBd = SFB.to(dev) if SFB is not None else None
+    # launches per step: gemm_mx rearranges each operand's scales first
+    launches_per_step = 3 if case.mx else 1
     otype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[case.out_dtype]
     Dd = torch.empty((case.M, case.N), dtype=otype, device=dev)
     stream = torch.cuda.Stream(dev)
@@ -303,12 +310,21 @@ def run_ours(args, case):
     small = case.algorithmic_bytes <= 129e6
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if small else None
 
-    def step():
-        rc = binding.gemm(Dd, Ad, Bd, Cd, case.M, case.N, case.K, Ad.stride(0), Bd.stride(0), ldc,
-                          Dd.stride(0), case.transA, case.transB, case.alpha, case.beta,
-                          code[case.in_dtype], code[case.out_dtype], sptr)
+    def call(D_, A_, B_, C_, SFA_, SFB_, s_ptr):
+        if case.mx:
+            rc = binding.gemm_mx(D_, A_, B_, C_, SFA_, SFB_, case.M, case.N, case.K, A_.stride(0), B_.stride(0),
+                                 C_.stride(0) if C_ is not None else case.N, D_.stride(0), SFA_.stride(0),
+                                 SFB_.stride(0), case.transA, case.transB, case.alpha, case.beta,
+                                 code[case.in_dtype], code[case.out_dtype], s_ptr)
+        else:
+            rc = binding.gemm(D_, A_, B_, C_, case.M, case.N, case.K, A_.stride(0), B_.stride(0),
+                              C_.stride(0) if C_ is not None else case.N, D_.stride(0), case.transA, case.transB,
+                              case.alpha, case.beta, code[case.in_dtype], code[case.out_dtype], s_ptr)
         if rc != 0:
             raise RuntimeError("gemm: %s" % binding.gemm_status_string(rc))
+
+    def step():
+        call(Dd, Ad, Bd, Cd, SFAd, SFBd, sptr)
 
     def barrier():
         if dist is not None:
@@ -380,9 +396,24 @@ def run_ours(args, case):
         hC = C.pin_memory() if C is not None else None
         streams = [torch.cuda.Stream(dev) for _ in range(E2E_STREAMS)]
         hDs = [torch.empty((case.M, case.N), dtype=otype).pin_memory() for _ in streams]
+        if case.mx:
+            # gemm_mx takes device buffers: each step copies its inputs in and
+            # its result out on its stream around the call (no panelling)
+            hSFA, hSFB = SFA.pin_memory(), SFB.pin_memory()
+            dbufs = [[torch.empty_like(x, device=dev) if x is not None else None
+                      for x in (hD, hA, hB, hC, hSFA, hSFB)] for hD in hDs]
 
         def e2e_step(i):
             s_i, hD = streams[i % len(streams)], hDs[i % len(streams)]
+            if case.mx:
+                dD, dA, dB, dC, dSA, dSB = dbufs[i % len(streams)]
+                with torch.cuda.stream(s_i):
+                    for d_, h_ in ((dA, hA), (dB, hB), (dC, hC), (dSA, hSFA), (dSB, hSFB)):
+                        if d_ is not None:
+                            d_.copy_(h_, non_blocking=True)
+                    call(dD, dA, dB, dC, dSA, dSB, s_i.cuda_stream)
+                    hD.copy_(dD, non_blocking=True)
+                return
             rc = binding.gemm_host(hD, hA, hB, hC, case.M, case.N, case.K, hA.stride(0), hB.stride(0),
                                    hC.stride(0) if hC is not None else case.N, hD.stride(0), case.transA,
                                    case.transB, case.alpha, case.beta, code[case.in_dtype],
@@ -412,13 +443,16 @@ def run_ours(args, case):
             if not torch.equal(hD, ref):
                 raise RuntimeError("end-to-end results differ between streams")
         h2d = A.numel() * A.element_size() + B.numel() * B.element_size() + (
-            C.numel() * C.element_size() if C is not None else 0)
+            C.numel() * C.element_size() if C is not None else 0) + (
+            SFA.numel() + SFB.numel() if case.mx else 0)
         d2h = Dd.numel() * Dd.element_size()
         e2e = {"value": job_tflops(world, case.flops, args.e2e_steps, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": e2e_ms / args.e2e_steps,
-               "api": "gemm_host (pinned host buffers; copies pipelined with the products over row panels; "
-                      "steps alternate between %d streams)" % len(streams)}
+               "api": ("gemm_mx between a copy of the inputs in and of D out (pinned host buffers), steps "
+                       "alternating between %d streams" if case.mx else
+                       "gemm_host (pinned host buffers; copies pipelined with the products over row panels; "
+                       "steps alternate between %d streams)") % len(streams)}
 
     if rank != 0:
         if dist is not None:
@@ -459,6 +493,9 @@ def run_ours(args, case):
                      "ridge_flop_per_byte": ridge, "algorithmic_flops_per_launch": case.flops,
                      "algorithmic_bytes_per_launch": case.algorithmic_bytes, "achieved_gbs": achieved_gbs})
     roofline["burst"] = dict(burst, launches=BURST_STEPS, best_of=3, ms_per_launch=burst_ms)
+    if case.mx:
+        roofline["note"] = ("block-scaled: the time per launch is that of the whole gemm_mx step, the two small "
+                            "scale-rearranging launches included")
     if clocks and clocks.get("sm_mhz") and roofline["bound"] == "tensor":
         clk_peak = num_sms * FLOP_PER_CLK_PER_SM * rate * clocks["sm_mhz"] * 1e6 / 1e12
         roofline["frac_of_clock_peak"] = achieved / clk_peak
@@ -469,7 +506,7 @@ def run_ours(args, case):
         "warmup": args.warmup, "ms_per_step": per_launch_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": case.in_dtype, "data": "synthetic",
         "config": _workload_config(case, world), "roofline": roofline,
-        "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps, "num_sms": num_sms,
+        "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps * launches_per_step, "num_sms": num_sms,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)

@@ -56,6 +56,9 @@ def load_library():
             lib.gemm_noalloc.argtypes = list(lib.gemm.argtypes)
             lib.gemm_host.restype = i32
             lib.gemm_host.argtypes = list(lib.gemm.argtypes)
+            lib.gemm_mx.restype = i32
+            lib.gemm_mx.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i64, i64,
+                                    i32, i32, f32, f32, i32, i32, vp]
             lib.gemm_schedule_units.restype = i32
             lib.gemm_schedule_units.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(i32), i32]
             _lib = lib
@@ -112,6 +115,18 @@ def gemm_host(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, be
     return lib.gemm_host(_addr(D), _addr(A), _addr(B), _addr(C), int(M), int(N), int(K), int(lda), int(ldb),
                          int(ldc), int(ldd), int(transA), int(transB), float(alpha), float(beta), int(in_dtype),
                          int(out_dtype), _stream(stream))
+
+
+def gemm_mx(D, A, B, C, SFA, SFB, M, N, K, lda, ldb, ldc, ldd, ld_sfa, ld_sfb, transA, transB, alpha, beta,
+            in_dtype, out_dtype, stream=None) -> int:
+    """The C entry point ``gemm_mx``: ``gemm`` with MX block-scaled E4M3 /
+    E5M2 operands (one UE8M0 scale byte per 32 K elements of each row of
+    op(A), SFA [M, ceil(K/32)], and of each column of op(B), SFB
+    [N, ceil(K/32)]).  Returns its status."""
+    lib = load_library()
+    return lib.gemm_mx(_addr(D), _addr(A), _addr(B), _addr(C), _addr(SFA), _addr(SFB), int(M), int(N), int(K),
+                       int(lda), int(ldb), int(ldc), int(ldd), int(ld_sfa), int(ld_sfb), int(transA), int(transB),
+                       float(alpha), float(beta), int(in_dtype), int(out_dtype), _stream(stream))
 
 
 def gemm_status_string(status: int) -> str:

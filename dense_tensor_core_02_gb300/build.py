@@ -22,7 +22,8 @@ INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", INCLUDE]
-SOURCES = ["gemm_sm103.cu", "gemm_sm103_f8.cu", "gemm_mma_sync.cu", "gemm_api.cpp", "gemm_host.cpp"]
+SOURCES = ["gemm_sm103.cu", "gemm_sm103_f8.cu", "gemm_sm103_mx.cu", "gemm_mma_sync.cu", "gemm_api.cpp",
+           "gemm_host.cpp"]
 HEADERS = ["ptx.cuh", "gemm_params.h", "gemm_internal.h", "gemm_tcgen05.cuh"]
 
 

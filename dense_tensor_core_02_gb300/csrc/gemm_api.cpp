@@ -360,17 +360,19 @@ int epi_warps_for(int64_t K, int pair, int out_dtype, int tile_n, int f8) {
     return (K + stage_k - 1) / stage_k <= 4 ? 8 : 4;
 }
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk, int out_dtype, int f8) {
+// mx: the block-scaled kernel, which has one tile shape (128 x 192 on one
+// SM, 4 epilogue warps); stream-K applies to it as to the others.
+Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk, int out_dtype, int f8, int mx = 0) {
     Plan pl{};
-    const int ov = variant_override();
+    const int ov = mx ? kSingle : variant_override();
     pl.pair = ov == kPairV || (ov == kAuto && M > gb300::tcgen05_tile_m(0)) ? 1 : 0;
     pl.tile_m = gb300::tcgen05_tile_m(pl.pair);
-    pl.tile_n = gb300::tcgen05_wide_n();
+    pl.tile_n = mx ? gb300::tcgen05_mx_tile_n() : gb300::tcgen05_wide_n();
     // Narrow 128 x 64 tiles when the wide ones would keep at most a quarter
     // of the SMs busy (the time then goes into latency and into each CTA's
     // epilogue, which a narrow tile cuts by four), or when N fits one.
     const int64_t wide_ctas = ((M + pl.tile_m - 1) / pl.tile_m) * ((N + pl.tile_n - 1) / pl.tile_n) * (pl.pair + 1);
-    if (ov == kNarrow || (ov == kAuto && (wide_ctas * 4 <= num_sms || N <= gb300::tcgen05_narrow_n()))) {
+    if (!mx && (ov == kNarrow || (ov == kAuto && (wide_ctas * 4 <= num_sms || N <= gb300::tcgen05_narrow_n())))) {
         pl.pair = 0;
         pl.tile_m = gb300::tcgen05_tile_m(0);
         pl.tile_n = gb300::tcgen05_narrow_n();
@@ -411,6 +413,12 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
         const int64_t counters = ((int64_t)pl.sk_tiles * 2 * 4 + 255) / 256 * 256;
         pl.ws_bytes = counters + (int64_t)pl.sk_tiles * pl.max_nc * 2 * kPartialBytes;
     }
+    if (mx) {
+        pl.epi_warps = 4;
+        pl.smem = gb300::tcgen05_mx_smem_bytes();
+        pl.stages = gb300::tcgen05_mx_stages();
+        return pl;
+    }
     pl.epi_warps = epi_warps_for(K, pl.pair, out_dtype, pl.tile_n, f8);
     pl.smem = gb300::tcgen05_smem_bytes(pl.pair, pl.epi_warps, pl.tile_n);
     pl.stages = gb300::tcgen05_stages(pl.pair, pl.epi_warps, pl.tile_n);
@@ -421,9 +429,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
 // in order, so they can share one; calls on different streams get different
 // ones.  Grown on demand (freeing the old one synchronises the device) and
 // kept until the process exits.  `epoch` numbers the launches that use it.
-// Kinds: the stream-K partial sums and arrival counters, and the repacked
-// operands / outputs of gemm_repacked.
-enum WorkspaceKind { kWsStreamK = 0, kWsRepack = 1 };
+// Kinds: the stream-K partial sums and arrival counters, the repacked
+// operands / outputs of gemm_repacked, and gemm_mx's rearranged scales.
+enum WorkspaceKind { kWsStreamK = 0, kWsRepack = 1, kWsScales = 2 };
 struct Workspace {
     int kind;
     int dev;
@@ -515,6 +523,23 @@ int validate(const void* D, const void* A, const void* B, const void* C, int64_t
         byte_range(C, M, N, ldc, osz, &c0, &c1);
         if (overlaps(d0, d1, c0, c1)) return reject(GEMM_ERR_ALIAS, "D overlaps C (other than C == D, ldc == ldd)");
     }
+    return GEMM_OK;
+}
+
+// gemm_mx's extra arguments: 8-bit operands; for K > 0 both scale arrays,
+// rows of at least ceil(K/32) scales, neither overlapping D.  Called after
+// validate() with M, N > 0.
+int validate_scales(const void* D, const void* SFA, const void* SFB, int64_t M, int64_t N, int64_t K,
+                    int64_t ld_sfa, int64_t ld_sfb, int64_t ldd, int out_dtype) {
+    if (K == 0) return GEMM_OK;
+    const int64_t kblocks = (K + 31) / 32;
+    if (!SFA || !SFB) return reject(GEMM_ERR_INVALID_ARG, "SFA or SFB is NULL");
+    if (ld_sfa < kblocks || ld_sfb < kblocks) return reject(GEMM_ERR_INVALID_ARG, "scale row shorter than ceil(K/32)");
+    uintptr_t d0, d1, a0, a1, b0, b1;
+    byte_range(D, M, N, ldd, elem_size(out_dtype), &d0, &d1);
+    byte_range(SFA, M, kblocks, ld_sfa, 1, &a0, &a1);
+    byte_range(SFB, N, kblocks, ld_sfb, 1, &b0, &b1);
+    if (overlaps(d0, d1, a0, a1) || overlaps(d0, d1, b0, b1)) return reject(GEMM_ERR_ALIAS, "D overlaps SFA or SFB");
     return GEMM_OK;
 }
 
@@ -638,9 +663,13 @@ int launch_sync_or_reject(void* D, const void* A, const void* B, const void* C, 
 // Returns kNoWorkspace (before enqueuing anything) when the workspace cannot
 // be had, else GEMM_OK or the inner call's error.
 constexpr int kNoWorkspace = 1;
+// With SFA / SFB (block-scaled operands) the inner call is gemm_mx(); the
+// scales are indexed by row of op(A) and column of op(B), so they need no
+// repacking here.
 int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
                   int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float alpha,
-                  float beta, int in_dtype, int out_dtype, int dev, cudaStream_t s, bool may_grow) {
+                  float beta, int in_dtype, int out_dtype, int dev, cudaStream_t s, bool may_grow,
+                  const void* SFA = nullptr, const void* SFB = nullptr, int64_t ld_sfa = 0, int64_t ld_sfb = 0) {
     const int isz = elem_size(in_dtype);
     const int osz = elem_size(out_dtype);
     const bool has_c = beta != 0.0f;
@@ -701,8 +730,10 @@ int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t 
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
-    const int rc = gemm(D2, A2, B2, C2, M, N, K, lda2, ldb2, ldc2, ldd2, transA2, transB2, alpha, beta, in_dtype,
-                        out_dtype, s);
+    const int rc = SFA ? gemm_mx(D2, A2, B2, C2, SFA, SFB, M, N, K, lda2, ldb2, ldc2, ldd2, ld_sfa, ld_sfb, transA2,
+                                 transB2, alpha, beta, in_dtype, out_dtype, s)
+                       : gemm(D2, A2, B2, C2, M, N, K, lda2, ldb2, ldc2, ldd2, transA2, transB2, alpha, beta,
+                              in_dtype, out_dtype, s);
     if (rc != GEMM_OK || d_ok) return rc;
     if (gb300::launch_copy2d(D, ldd, D2, ldd2, M, N, osz, s) != cudaSuccess) {
         cudaGetLastError();
@@ -861,6 +892,100 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
               (long long)M, (long long)N, (long long)K, transA, transB, in_dtype, out_dtype, has_c ? "!=" : "==",
               pl.pair ? "cta-pair" : "1-cta", pl.tile_m, pl.tile_n, pl.num_tiles, pl.grid, pl.smem, pl.epi_warps,
               pl.stages, pl.sk_tiles, pl.max_nc);
+    return launch_described(L, s);
+}
+
+int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SFA, const void* SFB, int64_t M,
+            int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int64_t ld_sfa, int64_t ld_sfb,
+            int transA, int transB, float alpha, float beta, int in_dtype, int out_dtype,
+            struct CUstream_st* stream) {
+    if (!is_f8(in_dtype)) return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "block scaling needs E4M3 / E5M2 operands");
+    int rc = validate(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, beta, in_dtype, out_dtype);
+    if (rc != GEMM_OK || M == 0 || N == 0) return rc;
+    if ((rc = validate_scales(D, SFA, SFB, M, N, K, ld_sfa, ld_sfb, ldd, out_dtype)) != GEMM_OK) return rc;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return reject(GEMM_ERR_CUDA, "cudaGetDevice");
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const bool in_capture = capturing(s);
+    if (in_capture && !device_ready(dev))
+        return reject(GEMM_ERR_CUDA, "first call on this device inside a stream capture");
+    DeviceState* ds = nullptr;
+    if ((rc = device_state(dev, &ds)) != GEMM_OK) return reject(rc, "device set-up");
+    const bool has_c = beta != 0.0f;
+    if (K == 0) return launch_k0_or_reject(out_dtype, D, C, M, N, ldc, ldd, alpha, beta, ds->num_sms, s);
+    const bool direct_ok =
+        tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, elem_size(in_dtype), elem_size(out_dtype), has_c) &&
+        operand_majors_ok(in_dtype, transA, transB);
+    if (!direct_ok) {
+        GEMM_LOGF("mx: M=%lld N=%lld K=%lld: layout the tcgen05 kernel cannot take as it is, repacked", (long long)M,
+                  (long long)N, (long long)K);
+        rc = gemm_repacked(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype, out_dtype,
+                           dev, s, !in_capture, SFA, SFB, ld_sfa, ld_sfb);
+        if (rc != kNoWorkspace) return rc == GEMM_OK ? GEMM_OK : reject(rc, "repacked call");
+        return reject(GEMM_ERR_UNSUPPORTED_LAYOUT, "8-bit operands: no workspace for repacking");
+    }
+
+    Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, 1, 1);
+    // The scales, rearranged into per-stage chunks (gemm_sm103_mx.cu).
+    const int64_t kblocks = (K + 31) / 32;
+    const int64_t sfa_bytes = gb300::sf_tiles_bytes(pl.tile_m, pl.num_m, pl.iters);
+    const int64_t sfb_bytes = gb300::sf_tiles_bytes(pl.tile_n, pl.num_n, pl.iters);
+    void* sws = nullptr;
+    uint32_t sepoch = 0;
+    if (workspace_for(kWsScales, dev, s, sfa_bytes + sfb_bytes, &sws, &sepoch, !in_capture) != GEMM_OK)
+        return reject(GEMM_ERR_CUDA, in_capture ? "scale workspace (a capture cannot allocate it; make one call of "
+                                                  "at least this size on the stream first)"
+                                                : "scale workspace");
+    uint8_t* sfa_tiles = static_cast<uint8_t*>(sws);
+    uint8_t* sfb_tiles = sfa_tiles + sfa_bytes;
+    void* ws = nullptr;
+    uint32_t epoch = 0;
+    if (pl.sk_tiles > 0 && workspace_for(kWsStreamK, dev, s, pl.ws_bytes, &ws, &epoch, !in_capture) != GEMM_OK) {
+        if (!in_capture) return reject(GEMM_ERR_CUDA, "stream-K workspace");
+        pl = make_plan(M, N, K, ds->num_sms, false, out_dtype, 1, 1);   // whole tiles: no workspace
+    }
+    TcgenLaunch L;
+    if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
+                               in_dtype, out_dtype)) != GEMM_OK)
+        return reject(rc, "tensor maps");
+    GemmParams& p = L.p;
+    // tcgen05 instruction descriptor, kind::mxf8f6f4: A / B format (bits 7-9,
+    // 10-12: 0 = E4M3, 1 = E5M2), both K-major (bits 15, 16 = 0), N >> 3
+    // (bits 17-22), scale type UE8M0 (bit 23), M >> 4 (bits 24-28); the
+    // kernel adds the scale-byte IDs of each K slice (bits 4-5 for B, 29-30
+    // for A).  The accumulator is f32 by definition of the kind.
+    const uint32_t fmt = in_dtype == GEMM_E5M2 ? 1u : 0u;
+    p.idesc = (fmt << 7) | (fmt << 10) | (((uint32_t)pl.tile_n >> 3) << 17) | (1u << 23) |
+              (((uint32_t)pl.tile_m >> 4) << 24);
+    p.sfa_tiles = sfa_tiles;
+    p.sfb_tiles = sfb_tiles;
+    L.mx = 1;
+    p.status = ds->d_status;
+    p.skip_first_stage = skip_first_stage_setting();
+    if (pl.sk_tiles > 0) {
+        p.sk_tiles = pl.sk_tiles;
+        p.ws_max_nc = pl.max_nc;
+        p.ws_epoch = epoch;
+        p.ws_counters = static_cast<uint32_t*>(ws);
+        p.ws_partials = static_cast<char*>(ws) + ((int64_t)pl.sk_tiles * 2 * 4 + 255) / 256 * 256;
+    }
+    cudaError_t e = gb300::launch_sf_tiles(sfa_tiles, static_cast<const uint8_t*>(SFA), ld_sfa, M, kblocks,
+                                           pl.tile_m, pl.num_m, pl.iters, s);
+    if (e == cudaSuccess)
+        e = gb300::launch_sf_tiles(sfb_tiles, static_cast<const uint8_t*>(SFB), ld_sfb, N, kblocks, pl.tile_n,
+                                   pl.num_n, pl.iters, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
+    }
+    GEMM_LOGF("mx: M=%lld N=%lld K=%lld in=%d out=%d beta%s0: tiles %dx%d (%d), grid %d, smem %d, %d stages, "
+              "%d stream-K tiles",
+              (long long)M, (long long)N, (long long)K, in_dtype, out_dtype, has_c ? "!=" : "==", pl.tile_m,
+              pl.tile_n, pl.num_tiles, pl.grid, pl.smem, pl.stages, pl.sk_tiles);
     return launch_described(L, s);
 }
 

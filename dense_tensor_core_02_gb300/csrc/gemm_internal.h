@@ -1,6 +1,6 @@
 // Internal interface between the C-ABI host code (gemm_api.cpp) and the
 // sm_103a kernels (gemm_tcgen05.cuh instantiated by gemm_sm103.cu and
-// gemm_sm103_f8.cu; gemm_mma_sync.cu).
+// gemm_sm103_f8.cu and gemm_sm103_mx.cu; gemm_mma_sync.cu).
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -26,6 +26,7 @@ struct TcgenLaunch {
     int epi_warps;            // 4 or 8 epilogue warps
     int tile_n;               // 256, or 64 for the narrow single-CTA tiles
     int f8;                   // 1: E4M3 / E5M2 operands (kind::f8f6f4), K-major only
+    int mx;                   // 1: and MX block-scaled (kind::mxf8f6f4), 128 x 192 tiles
     int pdl;                  // 1: launch with programmatic stream serialisation
 };
 
@@ -82,6 +83,18 @@ cudaError_t prepare_kernels_on_current_device();
 cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream);
 cudaError_t prepare_kernels_f8();                                          // gemm_sm103_f8.cu
 cudaError_t launch_tcgen05_f8(const TcgenLaunch& L, cudaStream_t stream);  // gemm_sm103_f8.cu
+cudaError_t prepare_kernels_mx();                                          // gemm_sm103_mx.cu
+cudaError_t launch_tcgen05_mx(const TcgenLaunch& L, cudaStream_t stream);  // gemm_sm103_mx.cu
+// MX scales of one operand, [rows, kblocks] bytes with row stride ld, into
+// the block-scaled kernel's per-stage chunks (GemmParams::sfa_tiles /
+// sfb_tiles) for tiles of tile_rows rows (columns) and kchunks 128-K stages;
+// rows and blocks outside the matrix get the scale 1 (byte 127).
+cudaError_t launch_sf_tiles(uint8_t* out, const uint8_t* in, int64_t ld, int64_t rows, int64_t kblocks,
+                            int tile_rows, int64_t tiles, int64_t kchunks, cudaStream_t stream);
+int64_t sf_tiles_bytes(int tile_rows, int64_t tiles, int64_t kchunks);
+int tcgen05_mx_tile_n();           // D columns per block-scaled tile
+int tcgen05_mx_smem_bytes();
+int tcgen05_mx_stages();
 cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,
                       float beta, int has_c, int num_sms, cudaStream_t stream);
 

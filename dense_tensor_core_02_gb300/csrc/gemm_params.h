@@ -34,7 +34,7 @@ struct GemmParams {
     int32_t num_m_tiles, num_n_tiles, num_k_blocks, num_tiles;
     int32_t group_m;        // rasterisation: M tiles per group
     float alpha, beta;
-    uint32_t idesc;         // tcgen05 instruction descriptor (kind::f16)
+    uint32_t idesc;         // tcgen05 instruction descriptor (kind::f16, f8f6f4 or mxf8f6f4)
     int32_t a_mn_major;     // A stored [K, M] (transA): M contiguous
     int32_t b_mn_major;     // B stored [K, N] (no transB): N contiguous
     int32_t has_c;          // beta != 0: C is read
@@ -64,6 +64,14 @@ struct GemmParams {
     int32_t pad2;           // keeps ws_counters 8-byte aligned
     uint32_t* ws_counters;    // [sk_tiles][2 CTA ranks] arrival counters
     void* ws_partials;        // [sk_tiles][ws_max_nc][2 ranks] x one CTA's fp32 accumulator (128 x tile N)
+    // MX block scales, rearranged for the kernel: for 128-K stage kb and M
+    // tile mb, 512 bytes at sfa_tiles + (kb * num_m_tiles + mb) * 512; for
+    // N tile nb, (tile N / 128) such chunks at sfb_tiles + (kb * num_n_tiles
+    // + nb) * (tile N / 128) * 512.  Within a chunk, byte (r % 32) * 16 +
+    // (r / 32) * 4 + j holds the scale of row (column) r of the 128, block
+    // 4 kb + j.  Unused (null) without block scaling.
+    const uint8_t* sfa_tiles;
+    const uint8_t* sfb_tiles;
 };
 
 // ---------------------------------------------------------------------------

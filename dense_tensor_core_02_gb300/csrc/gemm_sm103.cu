@@ -55,10 +55,12 @@ int noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
 
 cudaError_t prepare_kernels_on_current_device() {
     cudaError_t e = prepare_family<false>();
-    return e != cudaSuccess ? e : prepare_kernels_f8();
+    if (e == cudaSuccess) e = prepare_kernels_f8();
+    return e != cudaSuccess ? e : prepare_kernels_mx();
 }
 
 cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream) {
+    if (L.mx) return launch_tcgen05_mx(L, stream);
     return L.f8 ? launch_tcgen05_f8(L, stream) : launch_family<false>(L, stream);
 }
 

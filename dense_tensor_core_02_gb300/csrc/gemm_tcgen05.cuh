@@ -57,6 +57,15 @@ constexpr int kAtomBytes = 1024;     // 8 rows x 128 bytes: one 128B-swizzle ato
 constexpr int kMnChunkBytes = 64 * kBK * 2;   // one 64-wide MN-major box (64 x 64 x 2 B)
 constexpr int kSmemBudget = 232448;  // dynamic shared memory per CTA on sm_103
 static_assert(kBK / kUK == 4, "the MMA loop issues four K slices per stage");
+// MX block-scaled 8-bit operands: one UE8M0 scale per 32 K elements of each
+// row of A and column of B.  A 128-K stage spans four scale blocks, so each
+// row's scales of a stage are one 32-bit word.  Tiles are 128 x 192 on one
+// SM: two accumulators take 384 TMEM columns, the scale slots 64 more.
+constexpr int kMxBlock = 32;         // K elements per scale
+constexpr int kMxTileN = 192;        // accumulator columns of the block-scaled tiles
+constexpr int kSfChunkBytes = 512;   // scales of 128 rows x 4 blocks, in tcgen05.cp order
+constexpr int kSfSlotCols = 16;      // TMEM columns per stage's scales: SFA 4, SFB 4 per 128 columns of N
+static_assert(kBK8 == 4 * kMxBlock, "one scale word per row and stage");
 
 // kEpiW epilogue warps: 4 (one per TMEM lane quadrant, each storing all
 // columns of its 32 rows) for K-heavy shapes, or 8 (two per quadrant, half
@@ -66,9 +75,13 @@ static_assert(kBK / kUK == 4, "the MMA loop issues four K slices per stage");
 // single CTA) or 64 (128 x 64 single-CTA tiles for problems too small to
 // fill the GPU with wide tiles: four times as many CTAs, each with a
 // quarter of the epilogue).
-template <bool kPair, int kEpiW, int kTileN_ = kBNMax>
+// kMX: the block-scaled variant (one CTA, 8-bit K-major operands): each
+// stage also carries the scales of its 128 rows of A and its kTileN columns
+// of B, and two accumulators plus the scale slots share the 512 TMEM columns.
+template <bool kPair, int kEpiW, int kTileN_ = kBNMax, bool kMX_ = false>
 struct Cfg {
     static constexpr int kTileN = kTileN_;                 // D columns per tile
+    static constexpr bool kMX = kMX_;
     static constexpr int kCtaGroup = kPair ? 2 : 1;
     static constexpr int kTileM = kPair ? 2 * kBM : kBM;   // D rows per tile
     static constexpr int kLoadN = kPair ? kTileN / 2 : kTileN;   // B rows (N) each CTA stages
@@ -91,10 +104,14 @@ struct Cfg {
     // more D bytes in flight per SM
     static constexpr int kEpiBufs = kEpiW == 8 ? 3 : 2;
     static constexpr int kEpiBytes = kEpiW * kEpiBufs * kEpiBufBytes;
-    static constexpr int kStages = (kSmemBudget - kEpiBytes - 2048) / kStageBytes;
+    // scales of one stage (kMX): SFA of 128 rows, then SFB in 128-column groups
+    static constexpr int kSfbChunks = (kTileN + 127) / 128;
+    static constexpr int kSfBytes = kMX ? (1 + kSfbChunks) * kSfChunkBytes : 0;
+    static constexpr int kStages = (kSmemBudget - kEpiBytes - 2048 - (kMX ? 1024 : 0)) / (kStageBytes + kSfBytes);
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
-    static constexpr int kOffEpi = kOffB + kStages * kBBytes;
+    static constexpr int kOffSf = kOffB + kStages * kBBytes;
+    static constexpr int kOffEpi = kOffSf + (kStages * kSfBytes + 1023) / 1024 * 1024;
     static constexpr int kOffBar = kOffEpi + kEpiBytes;
     // full[S], empty[S], tmem_full[2], tmem_empty[2], c_ready[epilogue warps][kEpiBufs]
     static constexpr int kNumBars = 2 * kStages + 4 + kEpiBufs * kEpiW;
@@ -104,6 +121,10 @@ struct Cfg {
     static constexpr int kSmemBytes = kOffSkFlag + 4 + 1024;   // + base alignment slack
     static_assert(kStages >= 2, "at least two operand stages");
     static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
+    // One TMEM scale slot per operand stage (see the MMA issuer).
+    static_assert(!kMX || (!kPair && 2 * kTileN + kStages * kSfSlotCols <= kTmemCols &&
+                           4 + 4 * kSfbChunks <= kSfSlotCols),
+                  "block-scaled tiles: one CTA, accumulators and scale slots within the TMEM allocation");
 };
 
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand:
@@ -124,6 +145,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 __device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int mn_major, int kk) {
     return mn_major ? sw128_desc(tile + kk * (kUK * 128), kMnChunkBytes, kAtomBytes)
                     : sw128_desc(tile + kk * (kUK * 2), 16, kAtomBytes);
+}
+
+// Descriptor of one 512-byte scale chunk for tcgen05.cp (no swizzle): 32
+// rows of 16 bytes, 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
+           (1ull << 46);
 }
 
 static __device__ __noinline__ void report_timeout(const GemmParams& p, int site, int detail) {
@@ -237,12 +265,13 @@ __device__ __forceinline__ float2 unpack2(uint32_t u, int out) {
     return __bfloat1622float2(h);
 }
 
-template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN, bool kF8>
-__global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN>::kNumThreads, 1)
+template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN, bool kF8, bool kMX = false>
+__global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const GemmParams p) {
-    using Cf = Cfg<kPair, kEpiW, kTileN>;
+    using Cf = Cfg<kPair, kEpiW, kTileN, kMX>;
+    static_assert(!kMX || kF8, "block scaling applies to 8-bit operands");
     constexpr int kBN = kTileN;
     // K elements per 128-byte operand row; an MMA's K slice is 32 bytes of
     // it either way, so descriptors advance alike (8-bit operands are only
@@ -322,7 +351,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN>::kNumThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            const uint32_t stage_tx = (kPair ? 2 : 1) * Cf::kStageBytes;
+            const uint32_t stage_tx = (kPair ? 2 : 1) * Cf::kStageBytes + Cf::kSfBytes;
             const uint64_t pol_a = ptx::l2_policy(p.hint_a);
             const uint64_t pol_b = ptx::l2_policy(p.hint_b);
             UnitIter units;
@@ -351,6 +380,18 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN>::kNumThreads, 1)
                                                 p.a_mn_major, a_row0, kBM, k0, fb, pol_a);
                             load_operand<kPair>(base + Cf::kOffB + stage * Cf::kBBytes + sub * Cf::kBSubBytes, &tmB,
                                                 p.b_mn_major, b_row0, Cf::kLoadN, k0, fb, pol_b);
+                        }
+                        if constexpr (kMX) {
+                            // this stage's scales, laid out by the host in the
+                            // order tcgen05.cp reads them: the 128 rows of A,
+                            // then the tile's columns of B
+                            const uint32_t sdst = base + Cf::kOffSf + stage * Cf::kSfBytes;
+                            ptx::bulk_load(sdst, p.sfa_tiles + ((int64_t)kb * p.num_m_tiles + mb) * kSfChunkBytes,
+                                           kSfChunkBytes, fb);
+                            ptx::bulk_load(sdst + kSfChunkBytes,
+                                           p.sfb_tiles + ((int64_t)kb * p.num_n_tiles + nb) *
+                                                             (Cf::kSfbChunks * kSfChunkBytes),
+                                           Cf::kSfbChunks * kSfChunkBytes, fb);
                         }
                     }
                     if (++stage == Cf::kStages) {
@@ -406,17 +447,43 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN>::kNumThreads, 1)
                     ptx::tc_fence_after_sync();
                     const uint64_t ad = a_desc0 + (uint64_t)(stage * (Cf::kABytes >> 4));
                     const uint64_t bd = b_desc0 + (uint64_t)(stage * (Cf::kBBytes >> 4));
+                    if constexpr (kMX) {
+                        // The stage's scales into its own TMEM slot behind the
+                        // accumulators, then its four K = 32 slices, slice kk
+                        // taking byte kk of every row's and column's scale
+                        // word.  A copy and the later MMAs of this thread run
+                        // in issue order.  The slot's previous readers, the
+                        // MMAs of this stage's last round, have completed: the
+                        // producer refilled the stage only after their commit
+                        // released it, and the full barrier waited on above
+                        // follows that refill.
+                        const uint32_t slot = tmem_base + (uint32_t)(2 * kBN + stage * kSfSlotCols);
+                        const uint32_t ssrc = base + Cf::kOffSf + stage * Cf::kSfBytes;
+                        ptx::tmem_cp_32x128b_warpx4(slot, sf_desc(ssrc));
 #pragma unroll
-                    for (int sub = 0; sub < Cf::kSub; ++sub) {
-                        const uint64_t as = ad + (uint64_t)(sub * (Cf::kASubBytes >> 4));
-                        const uint64_t bs = bd + (uint64_t)(sub * (Cf::kBSubBytes >> 4));
+                        for (int c = 0; c < Cf::kSfbChunks; ++c)
+                            ptx::tmem_cp_32x128b_warpx4(slot + 4 + 4 * c, sf_desc(ssrc + (1 + c) * kSfChunkBytes));
 #pragma unroll
                         for (int kk = 0; kk < kBK / kUK; ++kk) {
-                            const uint32_t accumulate = ((kb - u.kb) | sub | kk) != 0;
-                            if constexpr (kF8)
-                                ptx::mma_f8f6f4<kCG>(d_tmem, as + kk * a_kstep, bs + kk * b_kstep, idesc, accumulate);
-                            else
-                                ptx::mma_f16<kCG>(d_tmem, as + kk * a_kstep, bs + kk * b_kstep, idesc, accumulate);
+                            const uint32_t accumulate = ((kb - u.kb) | kk) != 0;
+                            ptx::mma_mxf8f6f4(d_tmem, ad + kk * a_kstep, bd + kk * b_kstep,
+                                              idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), slot, slot + 4,
+                                              accumulate);
+                        }
+                    } else {
+#pragma unroll
+                        for (int sub = 0; sub < Cf::kSub; ++sub) {
+                            const uint64_t as = ad + (uint64_t)(sub * (Cf::kASubBytes >> 4));
+                            const uint64_t bs = bd + (uint64_t)(sub * (Cf::kBSubBytes >> 4));
+#pragma unroll
+                            for (int kk = 0; kk < kBK / kUK; ++kk) {
+                                const uint32_t accumulate = ((kb - u.kb) | sub | kk) != 0;
+                                if constexpr (kF8)
+                                    ptx::mma_f8f6f4<kCG>(d_tmem, as + kk * a_kstep, bs + kk * b_kstep, idesc,
+                                                         accumulate);
+                                else
+                                    ptx::mma_f16<kCG>(d_tmem, as + kk * a_kstep, bs + kk * b_kstep, idesc, accumulate);
+                            }
                         }
                     }
                     if constexpr (kPair)
@@ -685,13 +752,13 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN>::kNumThreads, 1)
                 if (pace) __nanosleep((unsigned)p.epi_pace_ns);
                 ++chunk_iter;
             };
-            static_assert(kChunks % 2 == 0 || kChunks == 1, "chunks are taken in pairs");
+            static_assert(kChunks >= 1, "at least one staging chunk per warp and tile");
             __syncwarp();
             tmem_load(0, va);
 #pragma unroll
             for (int c = 0; c < kChunks; c += 2) {
                 chunk(c, va, vb);
-                if constexpr (kChunks > 1) chunk(c + 1, vb, va);
+                if (c + 1 < kChunks) chunk(c + 1, vb, va);
             }
             __syncwarp();
             ptx::tmem_wait_ld();   // a prefetch cut short by `stop` must land before the release
@@ -725,11 +792,11 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN>::kNumThreads, 1)
 // 256-wide tiles with 4 epilogue warps for each output type, and with 8
 // epilogue warps for f32 output (the store-bound configuration); the 64-wide
 // single-CTA tiles with 4 epilogue warps for each output type.
-template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN, bool kF8>
+template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN, bool kF8, bool kMX = false>
 static cudaError_t prepare_one() {
-    return cudaFuncSetAttribute(gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC, kTileN, kF8>,
+    return cudaFuncSetAttribute(gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC, kTileN, kF8, kMX>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg<kPair, kEpiW, kTileN>::kSmemBytes);
+                                Cfg<kPair, kEpiW, kTileN, kMX>::kSmemBytes);
 }
 
 template <bool kPair, bool kHasC, bool kF8>
@@ -749,9 +816,9 @@ static cudaError_t prepare_narrow() {
     return prepare_one<false, kOutBF16, 4, kHasC, kNarrowN, kF8>();
 }
 
-template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN, bool kF8>
+template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN, bool kF8, bool kMX = false>
 static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
-    using Cf = Cfg<kPair, kEpiW, kTileN>;
+    using Cf = Cfg<kPair, kEpiW, kTileN, kMX>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.grid, 1, 1);
     cfg.blockDim = dim3(Cf::kNumThreads, 1, 1);
@@ -773,8 +840,8 @@ static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
     }
     cfg.attrs = n ? attr : nullptr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC, kTileN, kF8>, L.a, L.b, L.c, L.d,
-                              L.p);
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC, kTileN, kF8, kMX>, L.a, L.b, L.c,
+                              L.d, L.p);
 }
 
 template <bool kPair, bool kHasC, bool kF8>
@@ -814,6 +881,23 @@ static cudaError_t launch_family(const TcgenLaunch& L, cudaStream_t stream) {
         return has_c ? launch_narrow<true, kF8>(L, stream) : launch_narrow<false, kF8>(L, stream);
     if (L.pair) return has_c ? launch_group<true, true, kF8>(L, stream) : launch_group<true, false, kF8>(L, stream);
     return has_c ? launch_group<false, true, kF8>(L, stream) : launch_group<false, false, kF8>(L, stream);
+}
+
+// The block-scaled kernels: 128 x 192 single-CTA tiles, 4 epilogue warps,
+// every output type, with and without C.
+template <bool kHasC>
+static cudaError_t prepare_mx_group() {
+    cudaError_t e;
+    if ((e = prepare_one<false, kOutF32, 4, kHasC, kMxTileN, true, true>()) != cudaSuccess) return e;
+    if ((e = prepare_one<false, kOutF16, 4, kHasC, kMxTileN, true, true>()) != cudaSuccess) return e;
+    return prepare_one<false, kOutBF16, 4, kHasC, kMxTileN, true, true>();
+}
+
+template <bool kHasC>
+static cudaError_t launch_mx_group(const TcgenLaunch& L, cudaStream_t stream) {
+    if (L.out == kOutF32) return launch_one<false, kOutF32, 4, kHasC, kMxTileN, true, true>(L, stream);
+    if (L.out == kOutF16) return launch_one<false, kOutF16, 4, kHasC, kMxTileN, true, true>(L, stream);
+    return launch_one<false, kOutBF16, 4, kHasC, kMxTileN, true, true>(L, stream);
 }
 
 }  // namespace gb300

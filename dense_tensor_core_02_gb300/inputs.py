@@ -41,6 +41,9 @@ class GemmCase:
     beta: float = 0.0
     c_dist: str = "normal"         # distribution of C when beta != 0
     seed: int = 0
+    mx: bool = False               # MX block-scaled operands (UE8M0 scale per 32 K elements)
+    sf_lo: int = 120               # scale bytes uniform on [sf_lo, sf_hi] (2^(e - 127))
+    sf_hi: int = 134
 
     @property
     def a_shape(self):
@@ -59,7 +62,9 @@ class GemmCase:
         """Each operand read once, C read once when beta != 0, D written once."""
         isz = _ELEM_BYTES[self.in_dtype]
         osz = _ELEM_BYTES[self.out_dtype]
-        return isz * (self.M * self.K + self.K * self.N) + osz * self.M * self.N * (1 + (self.beta != 0))
+        scale_bytes = (self.M + self.N) * ((self.K + 31) // 32) if self.mx else 0
+        return (isz * (self.M * self.K + self.K * self.N) + osz * self.M * self.N * (1 + (self.beta != 0)) +
+                scale_bytes)
 
 
 def _draw(gen, shape, dist, std):
@@ -85,6 +90,17 @@ def make_inputs(case: GemmCase):
     if case.beta != 0.0:
         C = _draw(gen, (case.M, case.N), case.c_dist, 1.0).to(_TORCH_DTYPE[case.out_dtype])
     return A, B, C
+
+
+def make_scales(case: GemmCase):
+    """CPU uint8 tensors (SFA [M, ceil(K/32)], SFB [N, ceil(K/32)]) of MX
+    scale bytes for ``case``, uniform on [sf_lo, sf_hi], drawn in that order
+    from ``torch.Generator().manual_seed(case.seed + 1000000)``."""
+    gen = torch.Generator().manual_seed(case.seed + 1000000)
+    kb = (case.K + 31) // 32
+    SFA = torch.randint(case.sf_lo, case.sf_hi + 1, (case.M, kb), generator=gen, dtype=torch.int32)
+    SFB = torch.randint(case.sf_lo, case.sf_hi + 1, (case.N, kb), generator=gen, dtype=torch.int32)
+    return SFA.to(torch.uint8), SFB.to(torch.uint8)
 
 
 def integer_matrix(shape, lo, hi, seed, dtype="f16"):
@@ -118,6 +134,11 @@ def _cases():
         GemmCase("gemm_8192_e4m3_transB", k8192, k8192, k8192, "e4m3", transB=1),
         GemmCase("gemm_4096_e5m2_transB_beta1", 4096, 4096, 4096, "e5m2", dist="uniform",
                  transB=1, alpha=1.0, beta=1.0, c_dist="uniform"),
+        # MX block-scaled 8-bit operands (the SFA / SFB block scaling of the
+        # same section), scales 2^-7 .. 2^7
+        GemmCase("gemm_8192_mxe4m3_transB", k8192, k8192, k8192, "e4m3", transB=1, mx=True),
+        GemmCase("gemm_4096_mxe5m2_transB_beta1", 4096, 4096, 4096, "e5m2", dist="uniform",
+                 transB=1, alpha=1.0, beta=1.0, c_dist="uniform", mx=True),
     ]
     return [dataclasses.replace(c, seed=1000 + i + 1) for i, c in enumerate(rows)]
 

@@ -131,6 +131,47 @@ GEMM_API int gemm(void* D, const void* A, const void* B, const void* C,
          int transA, int transB, float alpha, float beta,
          int in_dtype, int out_dtype, struct CUstream_st* stream);
 
+/*
+ * gemm_mx -- gemm() with MX block-scaled 8-bit operands:
+ *
+ *   D[i][j] = alpha * sum_k (sa(i, k) * op(A)[i][k]) * (sb(j, k) * op(B)[k][j])
+ *             + beta * C[i][j],
+ *   sa(i, k) = 2^(SFA[i * ld_sfa + k / 32] - 127),
+ *   sb(j, k) = 2^(SFB[j * ld_sfb + k / 32] - 127).
+ *
+ * The TIRx gemm guide (section 七) lists block scaling with separate A and
+ * B scale factors ("SFA/SFB") among the tcgen05 path's modes without
+ * defining it; this is the OCP Microscaling (MX) reading: every 32
+ * consecutive K elements of a row of op(A) share one UE8M0 scale byte, and
+ * likewise every 32 of a column of op(B).  A scale byte e stands for
+ * 2^(e - 127); e = 255 is NaN and makes its 32 products NaN.
+ *
+ *   SFA, SFB         device pointers: SFA row-major [M, ceil(K/32)] bytes with
+ *                    row stride ld_sfa, SFB row-major [N, ceil(K/32)] with row
+ *                    stride ld_sfb (rows of SFB are columns of op(B),
+ *                    whatever transB says).  Any byte alignment.  Not read
+ *                    when K == 0 (may then be NULL).
+ *   ld_sfa, ld_sfb   >= ceil(K/32) when K > 0.
+ *   in_dtype         GEMM_E4M3 or GEMM_E5M2 (else GEMM_ERR_UNSUPPORTED_DTYPE).
+ *   everything else  as for gemm().
+ *
+ * Kernel: tcgen05.mma kind::mxf8f6f4 with 128 x 192 tiles on one SM; each
+ * call first rearranges the scales into per-stage chunks in a workspace of
+ * this (device, stream) (about (M + 1.33 N) * K / 128 bytes), then runs the
+ * product.  Layouts that are not K-major 16-byte aligned go through the same
+ * repacking as gemm()'s 8-bit operands.  D must not overlap SFA or SFB
+ * (GEMM_ERR_ALIAS).  Under CUDA graph capture nothing is allocated: the
+ * workspaces must exist from an earlier call of at least the same size on
+ * the stream, else GEMM_ERR_CUDA.
+ */
+GEMM_API int gemm_mx(void* D, const void* A, const void* B, const void* C,
+                     const void* SFA, const void* SFB,
+                     int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd,
+                     int64_t ld_sfa, int64_t ld_sfb,
+                     int transA, int transB, float alpha, float beta,
+                     int in_dtype, int out_dtype, struct CUstream_st* stream);
+
 /* A static, human-readable name for a gemm_status_t value (never NULL). */
 GEMM_API const char* gemm_status_string(int status);
 

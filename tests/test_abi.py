@@ -300,3 +300,49 @@ def test_schedule_rejects_bad_arguments(lib):
     for args in [(0, 1, 1, 0, 0), (4, 0, 1, 0, 0), (4, 4, 2, 5, 0), (4, 4, 2, 1, 2)]:
         with pytest.raises(binding.GemmError):
             binding.gemm_schedule_units(*args)
+
+
+# ---- gemm_mx: MX block-scaled 8-bit operands --------------------------------
+
+SA_ = 0x50000000
+SB_ = 0x60000000
+MX_OK = dict(OK_ARGS, in_dtype=3, transB=1, SFA=SA_, SFB=SB_, ld_sfa=2, ld_sfb=2)
+
+
+def _call_mx(**kw):
+    a = dict(MX_OK)
+    a.update(kw)
+    return binding.gemm_mx(a["D"], a["A"], a["B"], a["C"], a["SFA"], a["SFB"], a["M"], a["N"], a["K"],
+                           a["lda"], a["ldb"], a["ldc"], a["ldd"], a["ld_sfa"], a["ld_sfb"], a["transA"],
+                           a["transB"], a["alpha"], a["beta"], a["in_dtype"], a["out_dtype"], 0)
+
+
+MX_REJECTIONS = [
+    (dict(in_dtype=0), -2),                 # block scaling is for 8-bit operands
+    (dict(in_dtype=1), -2),
+    (dict(in_dtype=2), -2),
+    (dict(SFA=0), -1),
+    (dict(SFB=0), -1),
+    (dict(ld_sfa=1), -1),                   # K = 64: two scales per row
+    (dict(ld_sfb=1), -1),
+    (dict(K=65, lda=80, ldb=80), -1),       # K = 65: three scales per row
+    (dict(D=SA_), -4),                      # D overlaps SFA
+    (dict(SFB=D_ + 100), -4),               # SFB inside D
+    (dict(lda=63), -1),                     # the operand rules of gemm() still apply
+    (dict(C=D_ + 4096), -4),
+]
+
+
+@pytest.mark.parametrize("kw,code", MX_REJECTIONS, ids=[str(r[0]) for r in MX_REJECTIONS])
+def test_mx_rejected_before_any_device_work(lib, kw, code):
+    assert _call_mx(**kw) == code
+
+
+def test_mx_valid_calls_reach_the_device(lib):
+    # unaligned scales, padded scale rows, K = 0 with NULL scales, every
+    # transpose form: all pass validation and fail only on a CPU-only box.
+    for kw in (dict(), dict(SFA=SA_ + 3, SFB=SB_ + 1), dict(ld_sfa=7, ld_sfb=3), dict(K=0, SFA=0, SFB=0),
+               dict(transA=1, transB=0), dict(in_dtype=4, out_dtype=1)):
+        rc = _call_mx(**kw)
+        assert rc in (0, -7, -5), (kw, rc)
+    assert _call_mx(M=0) == 0 and _call_mx(N=0) == 0
