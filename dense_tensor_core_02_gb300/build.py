@@ -42,7 +42,17 @@ def _stale(out: str, deps) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile what is stale and link the library.  Concurrent callers (test
+    workers) take turns on a lock file, so no object is written twice at
+    once."""
+    import fcntl
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        return _build_locked(force, verbose)
+
+
+def _build_locked(force: bool, verbose: bool) -> str:
     headers = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "gemm_gb300.h")]
     jobs = []
     objs = []

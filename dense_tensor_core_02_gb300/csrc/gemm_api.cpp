@@ -244,6 +244,25 @@ int encode_2d(CUtensorMap* map, int dt, const void* ptr, int64_t dim0, int64_t d
     return GEMM_OK;
 }
 
+// The rearranged MX scales (see GemmParams::sf_a_groups) as a 2-D tensor of
+// 32-bit words: rows of 128 words (one 512-byte chunk), `box_rows` chunks
+// per copy, no swizzle.
+int encode_sf(CUtensorMap* map, const void* ptr, int64_t chunks, uint32_t box_rows) {
+    cuuint64_t dims[2] = {128, (cuuint64_t)chunks};
+    cuuint64_t strides[1] = {512};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        GEMM_LOGF("cuTensorMapEncodeTiled failed (%d) for the scales: %lld chunks, box %u", (int)r, (long long)chunks,
+                  box_rows);
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
 struct Plan {
     int pair;
     int tile_m, tile_n;
@@ -360,11 +379,12 @@ int epi_warps_for(int64_t K, int pair, int out_dtype, int tile_n, int f8) {
     return (K + stage_k - 1) / stage_k <= 4 ? 8 : 4;
 }
 
-// mx: the block-scaled kernel, which has one tile shape (128 x 192 on one
-// SM, 4 epilogue warps); stream-K applies to it as to the others.
+// mx: the block-scaled kernel, whose tiles are 192 wide (256 x 192 on a CTA
+// pair, 128 x 192 on one SM; no narrow tiles), with 4 epilogue warps;
+// stream-K applies to it as to the others.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk, int out_dtype, int f8, int mx = 0) {
     Plan pl{};
-    const int ov = mx ? kSingle : variant_override();
+    const int ov = (mx && variant_override() == kNarrow) ? kAuto : variant_override();
     pl.pair = ov == kPairV || (ov == kAuto && M > gb300::tcgen05_tile_m(0)) ? 1 : 0;
     pl.tile_m = gb300::tcgen05_tile_m(pl.pair);
     pl.tile_n = mx ? gb300::tcgen05_mx_tile_n() : gb300::tcgen05_wide_n();
@@ -415,8 +435,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
     }
     if (mx) {
         pl.epi_warps = 4;
-        pl.smem = gb300::tcgen05_mx_smem_bytes();
-        pl.stages = gb300::tcgen05_mx_stages();
+        pl.smem = gb300::tcgen05_mx_smem_bytes(pl.pair);
+        pl.stages = gb300::tcgen05_mx_stages(pl.pair);
         return pl;
     }
     pl.epi_warps = epi_warps_for(K, pl.pair, out_dtype, pl.tile_n, f8);
@@ -930,10 +950,15 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
     }
 
     Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, 1, 1);
-    // The scales, rearranged into per-stage chunks (gemm_sm103_mx.cu).
+    // The scales, rearranged into 512-byte chunks (gemm_sm103_mx.cu): one per
+    // 128-K sub-block and 128-row group of A (each CTA of a pair has its
+    // own), and (tile N / 128) per sub-block and N tile.
     const int64_t kblocks = (K + 31) / 32;
-    const int64_t sfa_bytes = gb300::sf_tiles_bytes(pl.tile_m, pl.num_m, pl.iters);
-    const int64_t sfb_bytes = gb300::sf_tiles_bytes(pl.tile_n, pl.num_n, pl.iters);
+    const int64_t kchunks = (int64_t)pl.iters * (gb300::tcgen05_stage_k(pl.pair, 1) / 128);
+    const int64_t a_groups = (int64_t)pl.num_m * (pl.pair ? 2 : 1);
+    const int sfb_chunks = (pl.tile_n + 127) / 128;
+    const int64_t sfa_bytes = gb300::sf_tiles_bytes(128, a_groups, kchunks);
+    const int64_t sfb_bytes = gb300::sf_tiles_bytes(pl.tile_n, pl.num_n, kchunks);
     void* sws = nullptr;
     uint32_t sepoch = 0;
     if (workspace_for(kWsScales, dev, s, sfa_bytes + sfb_bytes, &sws, &sepoch, !in_capture) != GEMM_OK)
@@ -961,8 +986,10 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
     const uint32_t fmt = in_dtype == GEMM_E5M2 ? 1u : 0u;
     p.idesc = (fmt << 7) | (fmt << 10) | (((uint32_t)pl.tile_n >> 3) << 17) | (1u << 23) |
               (((uint32_t)pl.tile_m >> 4) << 24);
-    p.sfa_tiles = sfa_tiles;
-    p.sfb_tiles = sfb_tiles;
+    if ((rc = encode_sf(&L.sfa, sfa_tiles, sfa_bytes / 512, 1)) != GEMM_OK ||
+        (rc = encode_sf(&L.sfb, sfb_tiles, sfb_bytes / 512, (uint32_t)sfb_chunks)) != GEMM_OK)
+        return reject(rc, "scale tensor maps");
+    p.sf_a_groups = (int32_t)a_groups;
     L.mx = 1;
     p.status = ds->d_status;
     p.skip_first_stage = skip_first_stage_setting();
@@ -973,19 +1000,20 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
         p.ws_counters = static_cast<uint32_t*>(ws);
         p.ws_partials = static_cast<char*>(ws) + ((int64_t)pl.sk_tiles * 2 * 4 + 255) / 256 * 256;
     }
-    cudaError_t e = gb300::launch_sf_tiles(sfa_tiles, static_cast<const uint8_t*>(SFA), ld_sfa, M, kblocks,
-                                           pl.tile_m, pl.num_m, pl.iters, s);
+    cudaError_t e = gb300::launch_sf_tiles(sfa_tiles, static_cast<const uint8_t*>(SFA), ld_sfa, M, kblocks, 128,
+                                           a_groups, kchunks, s);
     if (e == cudaSuccess)
         e = gb300::launch_sf_tiles(sfb_tiles, static_cast<const uint8_t*>(SFB), ld_sfb, N, kblocks, pl.tile_n,
-                                   pl.num_n, pl.iters, s);
+                                   pl.num_n, kchunks, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));
     }
-    GEMM_LOGF("mx: M=%lld N=%lld K=%lld in=%d out=%d beta%s0: tiles %dx%d (%d), grid %d, smem %d, %d stages, "
+    GEMM_LOGF("mx: M=%lld N=%lld K=%lld in=%d out=%d beta%s0: %s tiles %dx%d (%d), grid %d, smem %d, %d stages, "
               "%d stream-K tiles",
-              (long long)M, (long long)N, (long long)K, in_dtype, out_dtype, has_c ? "!=" : "==", pl.tile_m,
-              pl.tile_n, pl.num_tiles, pl.grid, pl.smem, pl.stages, pl.sk_tiles);
+              (long long)M, (long long)N, (long long)K, in_dtype, out_dtype, has_c ? "!=" : "==",
+              pl.pair ? "cta-pair" : "1-cta", pl.tile_m, pl.tile_n, pl.num_tiles, pl.grid, pl.smem, pl.stages,
+              pl.sk_tiles);
     return launch_described(L, s);
 }
 

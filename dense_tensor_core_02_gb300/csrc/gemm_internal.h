@@ -19,6 +19,7 @@ constexpr int kDeviceErrTimeout = -8;
 
 struct TcgenLaunch {
     CUtensorMap a, b, c, d;   // TMA descriptors (c unused when beta == 0)
+    CUtensorMap sfa, sfb;     // block scales (mx only; see GemmParams::sf_a_groups)
     GemmParams p;
     int pair;                 // 1: CTA-pair (cta_group::2) kernel
     int out;                  // OutKind
@@ -26,7 +27,7 @@ struct TcgenLaunch {
     int epi_warps;            // 4 or 8 epilogue warps
     int tile_n;               // 256, or 64 for the narrow single-CTA tiles
     int f8;                   // 1: E4M3 / E5M2 operands (kind::f8f6f4), K-major only
-    int mx;                   // 1: and MX block-scaled (kind::mxf8f6f4), 128 x 192 tiles
+    int mx;                   // 1: and MX block-scaled (kind::mxf8f6f4), 192-wide tiles
     int pdl;                  // 1: launch with programmatic stream serialisation
 };
 
@@ -86,15 +87,15 @@ cudaError_t launch_tcgen05_f8(const TcgenLaunch& L, cudaStream_t stream);  // ge
 cudaError_t prepare_kernels_mx();                                          // gemm_sm103_mx.cu
 cudaError_t launch_tcgen05_mx(const TcgenLaunch& L, cudaStream_t stream);  // gemm_sm103_mx.cu
 // MX scales of one operand, [rows, kblocks] bytes with row stride ld, into
-// the block-scaled kernel's per-stage chunks (GemmParams::sfa_tiles /
-// sfb_tiles) for tiles of tile_rows rows (columns) and kchunks 128-K stages;
-// rows and blocks outside the matrix get the scale 1 (byte 127).
+// the block-scaled kernel's 512-byte chunks (see GemmParams::sf_a_groups)
+// for tiles of tile_rows rows (columns) and kchunks 128-K sub-blocks; rows
+// and blocks outside the matrix get the scale 1 (byte 127).
 cudaError_t launch_sf_tiles(uint8_t* out, const uint8_t* in, int64_t ld, int64_t rows, int64_t kblocks,
                             int tile_rows, int64_t tiles, int64_t kchunks, cudaStream_t stream);
 int64_t sf_tiles_bytes(int tile_rows, int64_t tiles, int64_t kchunks);
 int tcgen05_mx_tile_n();           // D columns per block-scaled tile
-int tcgen05_mx_smem_bytes();
-int tcgen05_mx_stages();
+int tcgen05_mx_smem_bytes(int pair);
+int tcgen05_mx_stages(int pair);
 cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,
                       float beta, int has_c, int num_sms, cudaStream_t stream);
 

@@ -64,14 +64,15 @@ struct GemmParams {
     int32_t pad2;           // keeps ws_counters 8-byte aligned
     uint32_t* ws_counters;    // [sk_tiles][2 CTA ranks] arrival counters
     void* ws_partials;        // [sk_tiles][ws_max_nc][2 ranks] x one CTA's fp32 accumulator (128 x tile N)
-    // MX block scales, rearranged for the kernel: for 128-K stage kb and M
-    // tile mb, 512 bytes at sfa_tiles + (kb * num_m_tiles + mb) * 512; for
-    // N tile nb, (tile N / 128) such chunks at sfb_tiles + (kb * num_n_tiles
-    // + nb) * (tile N / 128) * 512.  Within a chunk, byte (r % 32) * 16 +
-    // (r / 32) * 4 + j holds the scale of row (column) r of the 128, block
-    // 4 kb + j.  Unused (null) without block scaling.
-    const uint8_t* sfa_tiles;
-    const uint8_t* sfb_tiles;
+    // MX block scales (kernels with block scaling only), rearranged by the
+    // host into 512-byte chunks, the rows of the SFA / SFB tensor maps.  A
+    // chunk holds the scales of 128 rows (columns) for one 128-K sub-block:
+    // byte (r % 32) * 16 + (r / 32) * 4 + j is row r's scale of block 4 kc
+    // + j.  SFA chunk of 128-K sub-block kc and 128-row group g: row
+    // kc * sf_a_groups + g.  SFB chunks of sub-block kc and N tile nb: the
+    // (tile N / 128) rows from (kc * num_n_tiles + nb) * (tile N / 128) on.
+    int32_t sf_a_groups;      // 128-row groups per sub-block in the SFA map (M tiles x CTAs per tile)
+    int32_t pad3;
 };
 
 // ---------------------------------------------------------------------------

@@ -9,17 +9,25 @@
 namespace gb300 {
 
 cudaError_t prepare_kernels_mx() {
-    cudaError_t e = prepare_mx_group<false>();
-    return e != cudaSuccess ? e : prepare_mx_group<true>();
+    cudaError_t e;
+    if ((e = prepare_mx_group<false, false>()) != cudaSuccess) return e;
+    if ((e = prepare_mx_group<false, true>()) != cudaSuccess) return e;
+    if ((e = prepare_mx_group<true, false>()) != cudaSuccess) return e;
+    return prepare_mx_group<true, true>();
 }
 
 cudaError_t launch_tcgen05_mx(const TcgenLaunch& L, cudaStream_t stream) {
-    return L.p.has_c ? launch_mx_group<true>(L, stream) : launch_mx_group<false>(L, stream);
+    if (L.pair) return L.p.has_c ? launch_mx_group<true, true>(L, stream) : launch_mx_group<true, false>(L, stream);
+    return L.p.has_c ? launch_mx_group<false, true>(L, stream) : launch_mx_group<false, false>(L, stream);
 }
 
 int tcgen05_mx_tile_n() { return kMxTileN; }
-int tcgen05_mx_smem_bytes() { return Cfg<false, 4, kMxTileN, true>::kSmemBytes; }
-int tcgen05_mx_stages() { return Cfg<false, 4, kMxTileN, true>::kStages; }
+int tcgen05_mx_smem_bytes(int pair) {
+    return pair ? Cfg<true, 4, kMxTileN, true>::kSmemBytes : Cfg<false, 4, kMxTileN, true>::kSmemBytes;
+}
+int tcgen05_mx_stages(int pair) {
+    return pair ? Cfg<true, 4, kMxTileN, true>::kStages : Cfg<false, 4, kMxTileN, true>::kStages;
+}
 
 // One thread per (stage kc, tile, 128-row group g, row r of the group): the
 // row's four scales of the stage (blocks 4 kc .. 4 kc + 3) become one 32-bit

@@ -58,13 +58,14 @@ constexpr int kMnChunkBytes = 64 * kBK * 2;   // one 64-wide MN-major box (64 x 
 constexpr int kSmemBudget = 232448;  // dynamic shared memory per CTA on sm_103
 static_assert(kBK / kUK == 4, "the MMA loop issues four K slices per stage");
 // MX block-scaled 8-bit operands: one UE8M0 scale per 32 K elements of each
-// row of A and column of B.  A 128-K stage spans four scale blocks, so each
-// row's scales of a stage are one 32-bit word.  Tiles are 128 x 192 on one
-// SM: two accumulators take 384 TMEM columns, the scale slots 64 more.
+// row of A and column of B.  A 128-K sub-block spans four scale blocks, so
+// each row's scales of a sub-block are one 32-bit word.  Tiles are 192
+// columns wide (128 x 192 on one SM, 256 x 192 on a CTA pair): two
+// accumulators take 384 TMEM columns, the stages' scale slots the rest.
 constexpr int kMxBlock = 32;         // K elements per scale
 constexpr int kMxTileN = 192;        // accumulator columns of the block-scaled tiles
 constexpr int kSfChunkBytes = 512;   // scales of 128 rows x 4 blocks, in tcgen05.cp order
-constexpr int kSfSlotCols = 16;      // TMEM columns per stage's scales: SFA 4, SFB 4 per 128 columns of N
+constexpr int kSfSlotCols = 16;      // TMEM columns per sub-block's scales: SFA 4, SFB 4 per 128 columns of N
 static_assert(kBK8 == 4 * kMxBlock, "one scale word per row and stage");
 
 // kEpiW epilogue warps: 4 (one per TMEM lane quadrant, each storing all
@@ -75,9 +76,10 @@ static_assert(kBK8 == 4 * kMxBlock, "one scale word per row and stage");
 // single CTA) or 64 (128 x 64 single-CTA tiles for problems too small to
 // fill the GPU with wide tiles: four times as many CTAs, each with a
 // quarter of the epilogue).
-// kMX: the block-scaled variant (one CTA, 8-bit K-major operands): each
-// stage also carries the scales of its 128 rows of A and its kTileN columns
-// of B, and two accumulators plus the scale slots share the 512 TMEM columns.
+// kMX: the block-scaled variant (8-bit K-major operands): each sub-block of a
+// stage also carries the scales of the CTA's 128 rows of A and of all kTileN
+// columns of B (both CTAs of a pair need every column's scales), and two
+// accumulators plus the scale slots share the 512 TMEM columns.
 template <bool kPair, int kEpiW, int kTileN_ = kBNMax, bool kMX_ = false>
 struct Cfg {
     static constexpr int kTileN = kTileN_;                 // D columns per tile
@@ -88,7 +90,7 @@ struct Cfg {
     static constexpr int kEpiWarps = kEpiW;
     static constexpr int kNumThreads = 64 + 32 * kEpiW;    // producer, MMA, epilogue warps
     static constexpr int kEpiCols = kTileN / (kEpiW / 4);  // accumulator columns per epilogue warp
-    static_assert(kLoadN % 64 == 0, "MN-major operand boxes are 64 wide");
+    static_assert(kMX || kLoadN % 64 == 0, "MN-major operand boxes are 64 wide");
     static_assert(kTileN <= kBNMax && kTileN % 64 == 0, "tile width");
     // A pipeline stage holds kSub 64-wide K sub-blocks.  The MMA issuer pays a
     // fixed cost per stage (barrier wait, release commit) while the tensor
@@ -104,9 +106,12 @@ struct Cfg {
     // more D bytes in flight per SM
     static constexpr int kEpiBufs = kEpiW == 8 ? 3 : 2;
     static constexpr int kEpiBytes = kEpiW * kEpiBufs * kEpiBufBytes;
-    // scales of one stage (kMX): SFA of 128 rows, then SFB in 128-column groups
+    // scales of one stage (kMX): per sub-block, SFA of the CTA's 128 rows,
+    // then SFB in 128-column groups
     static constexpr int kSfbChunks = (kTileN + 127) / 128;
-    static constexpr int kSfBytes = kMX ? (1 + kSfbChunks) * kSfChunkBytes : 0;
+    static constexpr int kSfSubBytes = (1 + kSfbChunks) * kSfChunkBytes;
+    static constexpr int kSfBytes = kMX ? kSub * kSfSubBytes : 0;
+    static constexpr int kSfStageCols = kSub * kSfSlotCols;   // TMEM columns of one stage's scales
     static constexpr int kStages = (kSmemBudget - kEpiBytes - 2048 - (kMX ? 1024 : 0)) / (kStageBytes + kSfBytes);
     static constexpr int kOffA = 0;
     static constexpr int kOffB = kOffA + kStages * kABytes;
@@ -122,9 +127,8 @@ struct Cfg {
     static_assert(kStages >= 2, "at least two operand stages");
     static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
     // One TMEM scale slot per operand stage (see the MMA issuer).
-    static_assert(!kMX || (!kPair && 2 * kTileN + kStages * kSfSlotCols <= kTmemCols &&
-                           4 + 4 * kSfbChunks <= kSfSlotCols),
-                  "block-scaled tiles: one CTA, accumulators and scale slots within the TMEM allocation");
+    static_assert(!kMX || (2 * kTileN + kStages * kSfStageCols <= kTmemCols && 4 + 4 * kSfbChunks <= kSfSlotCols),
+                  "block-scaled tiles: accumulators and scale slots within the TMEM allocation");
 };
 
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand:
@@ -269,6 +273,7 @@ template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN, bool kF8, boo
 __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                        const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const GemmParams p) {
     using Cf = Cfg<kPair, kEpiW, kTileN, kMX>;
     static_assert(!kMX || kF8, "block scaling applies to 8-bit operands");
@@ -320,6 +325,10 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
         ptx::prefetch_tensormap(&tmB);
         ptx::prefetch_tensormap(&tmD);
         if constexpr (kHasC) ptx::prefetch_tensormap(&tmC);
+        if constexpr (kMX) {
+            ptx::prefetch_tensormap(&tmSFA);
+            ptx::prefetch_tensormap(&tmSFB);
+        }
     }
     if (warp == 1) {
         ptx::tmem_alloc<kCG>(ptx::smem_addr(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
@@ -351,9 +360,10 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            const uint32_t stage_tx = (kPair ? 2 : 1) * Cf::kStageBytes + Cf::kSfBytes;
+            const uint32_t stage_tx = (kPair ? 2 : 1) * (Cf::kStageBytes + Cf::kSfBytes);
             const uint64_t pol_a = ptx::l2_policy(p.hint_a);
             const uint64_t pol_b = ptx::l2_policy(p.hint_b);
+            const uint64_t pol_sf = ptx::l2_policy(2);   // scales: re-read by every tile of their row / column
             UnitIter units;
             units.start(sched, cluster_id);
             WorkUnit u;
@@ -383,15 +393,23 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                         }
                         if constexpr (kMX) {
                             // this stage's scales, laid out by the host in the
-                            // order tcgen05.cp reads them: the 128 rows of A,
-                            // then the tile's columns of B
-                            const uint32_t sdst = base + Cf::kOffSf + stage * Cf::kSfBytes;
-                            ptx::bulk_load(sdst, p.sfa_tiles + ((int64_t)kb * p.num_m_tiles + mb) * kSfChunkBytes,
-                                           kSfChunkBytes, fb);
-                            ptx::bulk_load(sdst + kSfChunkBytes,
-                                           p.sfb_tiles + ((int64_t)kb * p.num_n_tiles + nb) *
-                                                             (Cf::kSfbChunks * kSfChunkBytes),
-                                           Cf::kSfbChunks * kSfChunkBytes, fb);
+                            // order tcgen05.cp reads them (512-byte chunks, rows
+                            // of the SFA / SFB tensor maps): per sub-block the
+                            // CTA's 128 rows of A, then every column of the tile
+#pragma unroll
+                            for (int sub = 0; sub < Cf::kSub; ++sub) {
+                                const int kc = kb * Cf::kSub + sub;   // 128-K chunk
+                                const uint32_t sdst = base + Cf::kOffSf + stage * Cf::kSfBytes + sub * Cf::kSfSubBytes;
+                                const int a_chunk = kc * p.sf_a_groups + mb * (kPair ? 2 : 1) + (int)rank;
+                                const int b_chunk = (kc * p.num_n_tiles + nb) * Cf::kSfbChunks;
+                                if constexpr (kPair) {
+                                    ptx::tma_load_2d_pair_hint(sdst, &tmSFA, 0, a_chunk, fb, pol_sf);
+                                    ptx::tma_load_2d_pair_hint(sdst + kSfChunkBytes, &tmSFB, 0, b_chunk, fb, pol_sf);
+                                } else {
+                                    ptx::tma_load_2d_hint(sdst, &tmSFA, 0, a_chunk, fb, pol_sf);
+                                    ptx::tma_load_2d_hint(sdst + kSfChunkBytes, &tmSFB, 0, b_chunk, fb, pol_sf);
+                                }
+                            }
                         }
                     }
                     if (++stage == Cf::kStages) {
@@ -449,26 +467,38 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                     const uint64_t bd = b_desc0 + (uint64_t)(stage * (Cf::kBBytes >> 4));
                     if constexpr (kMX) {
                         // The stage's scales into its own TMEM slot behind the
-                        // accumulators, then its four K = 32 slices, slice kk
-                        // taking byte kk of every row's and column's scale
-                        // word.  A copy and the later MMAs of this thread run
-                        // in issue order.  The slot's previous readers, the
-                        // MMAs of this stage's last round, have completed: the
-                        // producer refilled the stage only after their commit
-                        // released it, and the full barrier waited on above
-                        // follows that refill.
-                        const uint32_t slot = tmem_base + (uint32_t)(2 * kBN + stage * kSfSlotCols);
-                        const uint32_t ssrc = base + Cf::kOffSf + stage * Cf::kSfBytes;
-                        ptx::tmem_cp_32x128b_warpx4(slot, sf_desc(ssrc));
+                        // accumulators (16 columns per sub-block), then its
+                        // MMAs, slice kk of a sub-block taking byte kk of every
+                        // row's and column's scale word.  A copy and the later
+                        // MMAs of this thread run in issue order.  The slot's
+                        // previous readers, the MMAs of this stage's last
+                        // round, have completed: the producer refilled the
+                        // stage only after their commit released it, and the
+                        // full barrier waited on above follows that refill.
+                        const uint32_t slot0 = tmem_base + (uint32_t)(2 * kBN + stage * Cf::kSfStageCols);
+                        const uint32_t ssrc0 = base + Cf::kOffSf + stage * Cf::kSfBytes;
 #pragma unroll
-                        for (int c = 0; c < Cf::kSfbChunks; ++c)
-                            ptx::tmem_cp_32x128b_warpx4(slot + 4 + 4 * c, sf_desc(ssrc + (1 + c) * kSfChunkBytes));
+                        for (int sub = 0; sub < Cf::kSub; ++sub) {
+                            const uint32_t slot = slot0 + sub * kSfSlotCols;
+                            const uint32_t ssrc = ssrc0 + sub * Cf::kSfSubBytes;
+                            ptx::tmem_cp_32x128b_warpx4<kCG>(slot, sf_desc(ssrc));
 #pragma unroll
-                        for (int kk = 0; kk < kBK / kUK; ++kk) {
-                            const uint32_t accumulate = ((kb - u.kb) | kk) != 0;
-                            ptx::mma_mxf8f6f4(d_tmem, ad + kk * a_kstep, bd + kk * b_kstep,
-                                              idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), slot, slot + 4,
-                                              accumulate);
+                            for (int c = 0; c < Cf::kSfbChunks; ++c)
+                                ptx::tmem_cp_32x128b_warpx4<kCG>(slot + 4 + 4 * c,
+                                                                 sf_desc(ssrc + (1 + c) * kSfChunkBytes));
+                        }
+#pragma unroll
+                        for (int sub = 0; sub < Cf::kSub; ++sub) {
+                            const uint64_t as = ad + (uint64_t)(sub * (Cf::kASubBytes >> 4));
+                            const uint64_t bs = bd + (uint64_t)(sub * (Cf::kBSubBytes >> 4));
+                            const uint32_t slot = slot0 + sub * kSfSlotCols;
+#pragma unroll
+                            for (int kk = 0; kk < kBK / kUK; ++kk) {
+                                const uint32_t accumulate = ((kb - u.kb) | sub | kk) != 0;
+                                ptx::mma_mxf8f6f4<kCG>(d_tmem, as + kk * a_kstep, bs + kk * b_kstep,
+                                                       idesc | ((uint32_t)kk << 4) | ((uint32_t)kk << 29), slot,
+                                                       slot + 4, accumulate);
+                            }
                         }
                     } else {
 #pragma unroll
@@ -841,7 +871,7 @@ static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
     cfg.attrs = n ? attr : nullptr;
     cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC, kTileN, kF8, kMX>, L.a, L.b, L.c,
-                              L.d, L.p);
+                              L.d, L.sfa, L.sfb, L.p);
 }
 
 template <bool kPair, bool kHasC, bool kF8>
@@ -883,21 +913,21 @@ static cudaError_t launch_family(const TcgenLaunch& L, cudaStream_t stream) {
     return has_c ? launch_group<false, true, kF8>(L, stream) : launch_group<false, false, kF8>(L, stream);
 }
 
-// The block-scaled kernels: 128 x 192 single-CTA tiles, 4 epilogue warps,
-// every output type, with and without C.
-template <bool kHasC>
+// The block-scaled kernels: 192-wide tiles on one SM or a CTA pair, 4
+// epilogue warps, every output type, with and without C.
+template <bool kPair, bool kHasC>
 static cudaError_t prepare_mx_group() {
     cudaError_t e;
-    if ((e = prepare_one<false, kOutF32, 4, kHasC, kMxTileN, true, true>()) != cudaSuccess) return e;
-    if ((e = prepare_one<false, kOutF16, 4, kHasC, kMxTileN, true, true>()) != cudaSuccess) return e;
-    return prepare_one<false, kOutBF16, 4, kHasC, kMxTileN, true, true>();
+    if ((e = prepare_one<kPair, kOutF32, 4, kHasC, kMxTileN, true, true>()) != cudaSuccess) return e;
+    if ((e = prepare_one<kPair, kOutF16, 4, kHasC, kMxTileN, true, true>()) != cudaSuccess) return e;
+    return prepare_one<kPair, kOutBF16, 4, kHasC, kMxTileN, true, true>();
 }
 
-template <bool kHasC>
+template <bool kPair, bool kHasC>
 static cudaError_t launch_mx_group(const TcgenLaunch& L, cudaStream_t stream) {
-    if (L.out == kOutF32) return launch_one<false, kOutF32, 4, kHasC, kMxTileN, true, true>(L, stream);
-    if (L.out == kOutF16) return launch_one<false, kOutF16, 4, kHasC, kMxTileN, true, true>(L, stream);
-    return launch_one<false, kOutBF16, 4, kHasC, kMxTileN, true, true>(L, stream);
+    if (L.out == kOutF32) return launch_one<kPair, kOutF32, 4, kHasC, kMxTileN, true, true>(L, stream);
+    if (L.out == kOutF16) return launch_one<kPair, kOutF16, 4, kHasC, kMxTileN, true, true>(L, stream);
+    return launch_one<kPair, kOutBF16, 4, kHasC, kMxTileN, true, true>(L, stream);
 }
 
 }  // namespace gb300

@@ -155,10 +155,10 @@ GEMM_API int gemm(void* D, const void* A, const void* B, const void* C,
  *   in_dtype         GEMM_E4M3 or GEMM_E5M2 (else GEMM_ERR_UNSUPPORTED_DTYPE).
  *   everything else  as for gemm().
  *
- * Kernel: tcgen05.mma kind::mxf8f6f4 with 128 x 192 tiles on one SM; each
- * call first rearranges the scales into per-stage chunks in a workspace of
- * this (device, stream) (about (M + 1.33 N) * K / 128 bytes), then runs the
- * product.  Layouts that are not K-major 16-byte aligned go through the same
+ * Kernel: tcgen05.mma kind::mxf8f6f4 with 256 x 192 tiles on a CTA pair
+ * (128 x 192 on one SM when M <= 128); each call first rearranges the
+ * scales into 512-byte chunks in a workspace of this (device, stream)
+ * (about (M + 1.33 N) * K / 128 bytes), then runs the product.  Layouts that are not K-major 16-byte aligned go through the same
  * repacking as gemm()'s 8-bit operands.  D must not overlap SFA or SFB
  * (GEMM_ERR_ALIAS).  Under CUDA graph capture nothing is allocated: the
  * workspaces must exist from an earlier call of at least the same size on

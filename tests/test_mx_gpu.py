@@ -6,7 +6,8 @@ The TIRx gemm guide lists block scaling with separate A and B scale factors
 is the OCP Microscaling one: one UE8M0 scale byte per 32 K elements of each
 row of op(A) (SFA [M, ceil(K/32)]) and of each column of op(B) (SFB
 [N, ceil(K/32)]).  The kernel is tcgen05.mma kind::mxf8f6f4 with the scales
-copied into tensor memory, 128 x 192 tiles on one SM.
+copied into tensor memory, 256 x 192 tiles on a CTA pair or 128 x 192 on
+one SM.
 
 Integer operands in [-8, 8] with scales within 2^+-1 keep every fp32
 partial sum exact, so those cases are compared bit for bit; wider scale
@@ -33,6 +34,14 @@ def _device():
     yield
     rc, info = H.poll()
     assert rc == 0, ("device status after the module", rc, info)
+
+
+@pytest.fixture(params=["pair", "single"])
+def variant(request):
+    """256 x 192 tiles on a CTA pair (the default when M > 128) or 128 x 192
+    tiles on one SM."""
+    with H.env(GEMM_VARIANT=request.param, GEMM_PATH=None):
+        yield request.param
 
 
 def scales(rows, K, lo, hi, seed, pad=0):
@@ -86,7 +95,7 @@ SHAPES = [(128, 192, 128), (16, 8, 32), (1, 1, 1), (257, 200, 160), (300, 400, 5
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("dtype", FP8)
 @pytest.mark.parametrize("beta", [0.0, 1.0])
-def test_integers_exact(shape, dtype, beta):
+def test_integers_exact(variant, shape, dtype, beta):
     M, N, K = shape
     seed = 5 * M + 3 * N + K + (dtype == "e5m2") + 2 * int(beta)
     A = H.int_matrix((M, K), -8, 8, dtype, seed)
@@ -102,7 +111,7 @@ def test_integers_exact(shape, dtype, beta):
 
 
 @pytest.mark.parametrize("dtype", FP8)
-def test_each_block_takes_its_own_scale(dtype):
+def test_each_block_takes_its_own_scale(variant, dtype):
     """One distinct power of two per (row, block) and (column, block): a
     scale applied to the wrong block, row or column shows at once."""
     M, N, K = 256, 384, 256
@@ -120,7 +129,7 @@ def test_each_block_takes_its_own_scale(dtype):
 
 @pytest.mark.parametrize("dtype", FP8)
 @pytest.mark.parametrize("out_dtype", ["f32", "f16", "bf16"])
-def test_random_wide_scales(dtype, out_dtype):
+def test_random_wide_scales(variant, dtype, out_dtype):
     M, N, K = 520, 392, 776
     seed = 41 + (dtype == "e5m2") + 2 * ["f32", "f16", "bf16"].index(out_dtype)
     A = H.normal_matrix((M, K), dtype, seed)
@@ -182,7 +191,7 @@ def test_unaligned_scales_and_operands():
 
 
 @pytest.mark.parametrize("dtype", FP8)
-def test_streamk_split(dtype):
+def test_streamk_split(variant, dtype):
     M, N, K = 1024, 768, 2080
     A = H.int_matrix((M, K), -4, 4, dtype, 91)
     B = H.int_matrix((N, K), -4, 4, dtype, 92)
