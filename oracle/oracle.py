@@ -18,6 +18,11 @@ With ``sfa`` / ``sfb`` given, the 8-bit operands are MX block-scaled: every
 [N, ceil(K/32)], uint8; 255 is NaN) -- the OCP Microscaling reading of the
 "block scaling (SFA / SFB)" the TIRx gemm guide lists in section 七.
 
+E2M1 (the OCP 4-bit format; fp4 in the guide's list of precisions) is
+stored packed, two elements per byte, element e of a row-major array
+(e = row * ld + col) in the low nibble of byte e // 2 when e is even and in
+the high nibble when it is odd; its leading dimensions count elements.
+
 Inputs are numpy arrays or torch CPU tensors: A and B hold fp16 / bf16
 bits, or E4M3 / E5M2 bits (one byte each; the 8-bit precisions of the
 tcgen05 path the TIRx gemm guide lists in section 七); C holds fp32 (or
@@ -34,8 +39,9 @@ import threading
 
 import numpy as np
 
-F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
+F16, BF16, F32, E4M3, E5M2, E2M1 = 0, 1, 2, 3, 4, 5
 FP8 = (E4M3, E5M2)
+PACKED = (E2M1,)   # two elements per byte, even elements in the low nibble
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "oracle_gemm.c")
@@ -87,7 +93,14 @@ def _bits8(x):
 
 
 def _operand(x, in_dtype):
-    return _bits8(x) if in_dtype in FP8 else _bits16(x)
+    return _bits8(x) if (in_dtype in FP8 or in_dtype in PACKED) else _bits16(x)
+
+
+def _ld_operand(arr, default, in_dtype):
+    """Leading dimension in elements (a packed byte row holds two)."""
+    if arr is not None and arr.ndim == 2 and in_dtype in PACKED:
+        return 2 * arr.shape[1]
+    return _ld(arr, default)
 
 
 def _c_array(c, c_dtype):
@@ -146,6 +159,8 @@ class Oracle:
         lib.oracle_gemm_entries.restype = i32
         lib.oracle_gemm_entries.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, i64, i64, i64,
                                             i64, i64, i64, i32, i32, dbl, dbl, i32, i32]
+        lib.oracle_decode_e2m1.restype = dbl
+        lib.oracle_decode_e2m1.argtypes = [ctypes.c_uint8]
         lib.oracle_decode_ue8m0.restype = dbl
         lib.oracle_decode_ue8m0.argtypes = [ctypes.c_uint8]
         lib.oracle_gemm_mx.restype = i32
@@ -170,6 +185,9 @@ class Oracle:
     def decode_e5m2(self, bits: int) -> float:
         return self.lib.oracle_decode_e5m2(int(bits))
 
+    def decode_e2m1(self, bits: int) -> float:
+        return self.lib.oracle_decode_e2m1(int(bits))
+
     def decode_ue8m0(self, bits: int) -> float:
         return self.lib.oracle_decode_ue8m0(int(bits))
 
@@ -186,8 +204,8 @@ class Oracle:
         mx = _mx_args(sfa, sfb, ld_sfa, ld_sfb, K)
         Ab, Bb = _operand(A, in_dtype), _operand(B, in_dtype)
         C_ = _c_array(C, c_dtype) if beta != 0.0 else None
-        lda = lda if lda is not None else _ld(Ab, M if transA else K)
-        ldb = ldb if ldb is not None else _ld(Bb, K if transB else N)
+        lda = lda if lda is not None else _ld_operand(Ab, M if transA else K, in_dtype)
+        ldb = ldb if ldb is not None else _ld_operand(Bb, K if transB else N, in_dtype)
         ldc = ldc if ldc is not None else _ld(C_, N)
         D = np.full((M, N), np.nan)
         bound = np.full((M, N), np.nan)
@@ -223,8 +241,8 @@ class Oracle:
         mx = _mx_args(sfa, sfb, ld_sfa, ld_sfb, K)
         Ab, Bb = _operand(A, in_dtype), _operand(B, in_dtype)
         C_ = _c_array(C, c_dtype) if beta != 0.0 else None
-        lda = lda if lda is not None else _ld(Ab, M if transA else K)
-        ldb = ldb if ldb is not None else _ld(Bb, K if transB else N)
+        lda = lda if lda is not None else _ld_operand(Ab, M if transA else K, in_dtype)
+        ldb = ldb if ldb is not None else _ld_operand(Bb, K if transB else N, in_dtype)
         ldc = ldc if ldc is not None else _ld(C_, N)
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         cols = np.ascontiguousarray(cols, dtype=np.int64)
@@ -313,3 +331,7 @@ def decode_e5m2(bits):
 
 def decode_ue8m0(bits):
     return default().decode_ue8m0(bits)
+
+
+def decode_e2m1(bits):
+    return default().decode_e2m1(bits)

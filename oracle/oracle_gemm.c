@@ -41,7 +41,13 @@
  * sum of |products| is kept alongside, so the caller can form the
  * per-element error bound  |alpha| * sum|a*b| + |beta| * |c|.
  *
- * Block-scaled 8-bit operands (oracle_gemm_mx*): the TIRx gemm guide lists
+ * 4-bit operands: E2M1, the OCP 4-bit floating-point format (the guide lists
+ * fp4 among gemm_async's precisions, same section), stored packed, two
+ * elements per byte: element e of a row-major array (e = row * ld + col, ld
+ * in elements) is the low nibble of byte e / 2 when e is even, the high
+ * nibble when it is odd.  E2M1 is used block-scaled (below).
+ *
+ * Block-scaled 8-bit and 4-bit operands (oracle_gemm_mx*): the TIRx gemm guide lists
  * block scaling with separate A and B scale factors ("SFA/SFB") among the
  * asynchronous path's modes (section 七) without defining it.  The reading
  * taken is the OCP Microscaling (MX) one: each run of 32 consecutive K
@@ -64,7 +70,7 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2, ORACLE_E4M3 = 3, ORACLE_E5M2 = 4 };
+enum { ORACLE_F16 = 0, ORACLE_BF16 = 1, ORACLE_F32 = 2, ORACLE_E4M3 = 3, ORACLE_E5M2 = 4, ORACLE_E2M1 = 5 };
 
 /* ---- exact element decoders -------------------------------------------- */
 
@@ -136,6 +142,19 @@ double oracle_decode_e5m2(uint8_t b)
     return sign ? -v : v;
 }
 
+/* E2M1: 1 sign bit, 2 exponent bits (bias 1), 1 fraction bit; no
+ * infinities or NaNs, so the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6. */
+double oracle_decode_e2m1(uint8_t c)
+{
+    const int sign = (c >> 3) & 1, e = (c >> 1) & 3, f = c & 1;
+    double v;
+    if (e == 0)
+        v = 0.5 * f;                              /* subnormal: 0.f * 2^0 */
+    else
+        v = ldexp((double)(2 + f), e - 2);       /* 1.f * 2^(e-1) */
+    return sign ? -v : v;
+}
+
 /* UE8M0, the MX shared scale: 8 exponent bits (bias 127), no sign and no
  * fraction, so the value is 2^(e - 127); the all-ones pattern is NaN. */
 double oracle_decode_ue8m0(uint8_t e)
@@ -161,6 +180,7 @@ static double g_f16_table[65536];
 static double g_bf16_table[65536];
 static double g_e4m3_table[256];
 static double g_e5m2_table[256];
+static double g_e2m1_table[16];
 static pthread_once_t g_tables_once = PTHREAD_ONCE_INIT;
 
 static void fill_tables(void)
@@ -173,6 +193,7 @@ static void fill_tables(void)
         g_e4m3_table[b] = oracle_decode_e4m3((uint8_t)b);
         g_e5m2_table[b] = oracle_decode_e5m2((uint8_t)b);
     }
+    for (uint32_t c = 0; c < 16u; ++c) g_e2m1_table[c] = oracle_decode_e2m1((uint8_t)c);
 }
 
 static const double* table_for(int dtype)
@@ -182,6 +203,7 @@ static const double* table_for(int dtype)
     case ORACLE_F16: return g_f16_table;
     case ORACLE_BF16: return g_bf16_table;
     case ORACLE_E4M3: return g_e4m3_table;
+    case ORACLE_E2M1: return g_e2m1_table;
     default: return g_e5m2_table;
     }
 }
@@ -196,16 +218,21 @@ typedef struct {
     int transA, transB;
     double alpha, beta;
     const double* in_table;   /* decoder for A and B */
-    int in_bytes;             /* bytes per A / B element: 2 (fp16, bf16) or 1 (fp8) */
+    int in_bytes;             /* bytes per A / B element: 2 (fp16, bf16), 1 (fp8), 0 (packed fp4) */
     int c_dtype;
     const uint8_t* SFA;       /* MX scales of Ahat's rows, or NULL (no block scaling) */
     const uint8_t* SFB;       /* MX scales of Bhat's columns */
     int64_t ld_sfa, ld_sfb;
 } problem_t;
 
-/* The bit pattern of operand element `idx` (elements of in_bytes bytes). */
+/* The bit pattern of operand element `idx` (elements of in_bytes bytes, or
+ * nibbles when in_bytes is 0: even elements in the low nibble). */
 static unsigned operand_bits(const problem_t* p, const void* X, int64_t idx)
 {
+    if (p->in_bytes == 0) {
+        const uint8_t b = ((const uint8_t*)X)[idx / 2];
+        return (idx % 2 == 0) ? (b & 0xFu) : (b >> 4);
+    }
     return p->in_bytes == 1 ? ((const uint8_t*)X)[idx] : ((const uint16_t*)X)[idx];
 }
 
@@ -264,7 +291,7 @@ static int setup(problem_t* p, const void* A, const void* B, const void* C,
 {
     if (M < 0 || N < 0 || K < 0) return -1;
     if (in_dtype != ORACLE_F16 && in_dtype != ORACLE_BF16 && in_dtype != ORACLE_E4M3 &&
-        in_dtype != ORACLE_E5M2)
+        in_dtype != ORACLE_E5M2 && in_dtype != ORACLE_E2M1)
         return -1;
     if (c_dtype != ORACLE_F16 && c_dtype != ORACLE_BF16 && c_dtype != ORACLE_F32) return -1;
     if ((M > 0 && K > 0 && A == NULL) || (K > 0 && N > 0 && B == NULL)) return -1;
@@ -281,7 +308,7 @@ static int setup(problem_t* p, const void* A, const void* B, const void* C,
     p->transA = transA != 0; p->transB = transB != 0;
     p->alpha = alpha; p->beta = beta;
     p->in_table = table_for(in_dtype);
-    p->in_bytes = (in_dtype == ORACLE_E4M3 || in_dtype == ORACLE_E5M2) ? 1 : 2;
+    p->in_bytes = (in_dtype == ORACLE_E4M3 || in_dtype == ORACLE_E5M2) ? 1 : in_dtype == ORACLE_E2M1 ? 0 : 2;
     p->c_dtype = c_dtype;
     p->SFA = NULL;
     p->SFB = NULL;
@@ -294,7 +321,7 @@ static int setup(problem_t* p, const void* A, const void* B, const void* C,
 static int setup_mx(problem_t* p, const void* SFA, const void* SFB, int64_t ld_sfa, int64_t ld_sfb)
 {
     const int64_t kb = (p->K + MX_BLOCK - 1) / MX_BLOCK;
-    if (p->in_bytes != 1) return -1;
+    if (p->in_bytes > 1) return -1;
     if ((p->M > 0 && p->K > 0 && SFA == NULL) || (p->N > 0 && p->K > 0 && SFB == NULL)) return -1;
     if (p->K > 0 && (ld_sfa < kb || ld_sfb < kb)) return -1;
     p->SFA = (const uint8_t*)SFA;

@@ -24,7 +24,10 @@ plain mathematics fix:
   blocks of 32 along K (ragged last block, padded scale rows), unit scales
   reducing to the unscaled product, exact doubling of a row / column when
   its scales go up by one, invariance when a block's scale moves from A to
-  B, a closed form at a block boundary and NaN scales.
+  B, a closed form at a block boundary and NaN scales;
+* packed E2M1 (fp4): the format's 16 values (OCP: magnitudes 0, 0.5, 1, 1.5,
+  2, 3, 4, 6), the nibble order of the packing (even elements low), and
+  exact rational brute force of block-scaled fp4 products.
 
 ``tests/test_oracle_mutants.py`` runs the same pins against deliberately
 broken builds of the oracle and requires each break to be caught.
@@ -34,7 +37,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from oracle.oracle import BF16, E4M3, E5M2, F16, F32
+from oracle.oracle import BF16, E2M1, E4M3, E5M2, F16, F32
 
 F16_NAN = 0x7E00
 BF16_NAN = 0x7FC0
@@ -549,6 +552,70 @@ def pin_mx_numpy_float64(orc):
         assert np.all(np.abs(D - ref) <= 1e-12 * bound), "MX numpy float64 mismatch (dtype=%d)" % dtype
 
 
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]   # the OCP E2M1 magnitudes, codes 0..7
+
+
+def pin_e2m1_decoder(orc):
+    got = [orc.decode_e2m1(c) for c in range(16)]
+    assert got[:8] == E2M1_VALUES, "E2M1 positive codes"
+    assert got[8:] == [-v for v in E2M1_VALUES], "E2M1 sign bit"
+    assert np.signbit(got[8]), "code 8 is -0"
+
+
+def pin_e2m1_packing(orc):
+    """Byte 0x71 holds element 0 = code 1 (0.5) in the low nibble and element
+    1 = code 7 (6.0) in the high nibble."""
+    A = np.array([[0x71]], dtype=np.uint8)            # [1, K = 2]
+    one = np.array([[127]], dtype=np.uint8)
+    for b, want in ((0x02, 0.5), (0x20, 6.0), (0x22, 6.5)):
+        B = np.array([[b]], dtype=np.uint8)           # stored [N = 1, K = 2]
+        D, _ = orc.gemm(A, B, None, 1, 1, 2, transB=1, in_dtype=E2M1, sfa=one, sfb=one)
+        assert D[0, 0] == want, "E2M1 nibble order (byte 0x%02x)" % b
+    # a row of 3 elements with ld 4: the second row starts at byte 2
+    A2 = np.array([[0x21, 0x03], [0x54, 0x06]], dtype=np.uint8)   # rows (1.0, 0.5, 1.5), (2.0, 3.0, 4.0)
+    B2 = np.array([[0x22, 0x02]], dtype=np.uint8)                 # (1, 1, 1)
+    D2, _ = orc.gemm(A2, B2, None, 2, 1, 3, lda=4, ldb=4, transB=1, in_dtype=E2M1,
+                     sfa=np.full((2, 1), 127, np.uint8), sfb=one)
+    assert D2[:, 0].tolist() == [3.0, 9.0], "packed rows with a leading dimension"
+
+
+def _unpack_e2m1(packed, rows, cols, ld):
+    """Element values of a packed row-major fp4 array, in Python floats."""
+    flat = packed.reshape(-1)
+    out = []
+    for r in range(rows):
+        row = []
+        for c in range(cols):
+            e = r * ld + c
+            code = (int(flat[e // 2]) >> (4 * (e % 2))) & 0xF
+            v = E2M1_VALUES[code & 7]
+            row.append(-v if code & 8 else v)
+        out.append(row)
+    return out
+
+
+def pin_mx_fp4_brute_force(orc):
+    from fractions import Fraction
+    rng = np.random.default_rng(79)
+    for (M, N, K) in ((3, 4, 70), (2, 3, 64), (5, 2, 2)):
+        lda, ldb = K + 6, K + 2
+        A = rng.integers(0, 256, size=(M, lda // 2), dtype=np.uint8)
+        B = rng.integers(0, 256, size=(N, ldb // 2), dtype=np.uint8)
+        kb = (K + 31) // 32
+        sfa = rng.integers(124, 131, size=(M, kb)).astype(np.uint8)
+        sfb = rng.integers(124, 131, size=(N, kb)).astype(np.uint8)
+        D, _ = orc.gemm(A, B, None, M, N, K, lda=lda, ldb=ldb, transB=1, in_dtype=E2M1, sfa=sfa, sfb=sfb)
+        a = _unpack_e2m1(A, M, K, lda)
+        b = _unpack_e2m1(B, N, K, ldb)
+        for i in range(M):
+            for j in range(N):
+                acc = Fraction(0)
+                for k in range(K):
+                    e = int(sfa[i, k // 32]) + int(sfb[j, k // 32]) - 254
+                    acc += Fraction(a[i][k]) * Fraction(b[j][k]) * Fraction(2) ** e
+                assert D[i, j] == float(acc), "fp4 brute force %s at (%d, %d)" % ((M, N, K), i, j)
+
+
 def pin_mx_rejects_bad_arguments(orc):
     A8 = torch.zeros((4, 64), dtype=torch.float8_e4m3fn)
     A16 = torch.zeros((4, 64), dtype=torch.float16)
@@ -594,4 +661,7 @@ ALL_PINS = [
     pin_mx_nan_scale,
     pin_mx_numpy_float64,
     pin_mx_rejects_bad_arguments,
+    pin_e2m1_decoder,
+    pin_e2m1_packing,
+    pin_mx_fp4_brute_force,
 ]

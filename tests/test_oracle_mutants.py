@@ -57,7 +57,13 @@ MUTANTS = {
     "mx_scale_bias_128": ("ldexp(1.0, (int)e - 127)", "ldexp(1.0, (int)e - 128)"),
     "mx_nan_scale_missing": ("e == 0xFFu ? NAN :", "0 ? NAN :"),
     "mx_scale_row_check_missing": ("if (p->K > 0 && (ld_sfa < kb || ld_sfb < kb)) return -1;", ""),
-    "mx_16bit_accepted": ("if (p->in_bytes != 1) return -1;", ""),
+    "mx_16bit_accepted": ("if (p->in_bytes > 1) return -1;", ""),
+    "e2m1_exponent_bias": ("v = ldexp((double)(2 + f), e - 2);", "v = ldexp((double)(2 + f), e - 1);"),
+    "e2m1_subnormal_dropped": ("v = 0.5 * f;", "v = 0.0 * f;"),
+    "e2m1_nibbles_swapped": ("return (idx % 2 == 0) ? (b & 0xFu) : (b >> 4);",
+                             "return (idx % 2 == 0) ? (b >> 4) : (b & 0xFu);"),
+    "e2m1_byte_index": ("const uint8_t b = ((const uint8_t*)X)[idx / 2];",
+                        "const uint8_t b = ((const uint8_t*)X)[idx / 2 + (idx % 4 == 3)];"),
     "entries_use_col_as_row": ("D[e] = one_element(p, rows[e], cols[e], &bound[e]);",
                                "D[e] = one_element(p, rows[e], cols[e] % (p->N > 1 ? p->N - 1 : 1), &bound[e]);"),
 }
