@@ -179,7 +179,8 @@ def _args():
 
 def _workload_config(case, n_gpus):
     from dense_tensor_core_02_gb300.inputs import CASES
-    dist = ("N(0,%g)" % case.std) if case.dist == "normal" else "U[-1,1]"
+    dist = ("uniform random E2M1 codes, packed" if case.in_dtype == "e2m1" else
+            ("N(0,%g)" % case.std) if case.dist == "normal" else "U[-1,1]")
     mx = (", MX block scales (UE8M0 per 32 K, bytes U{%d..%d})" % (case.sf_lo, case.sf_hi)) if case.mx else ""
     return {
         "workload": "%s: M=%d N=%d K=%d, %s A/B %s%s, %s D, alpha=%g beta=%g, transA=%d transB=%d" % (
@@ -210,7 +211,7 @@ def _oracle_sampler(case):
     sf = dict(zip(("sfa", "sfb"), (x.numpy() for x in make_scales(case)))) if case.mx else {}
     threads = len(os.sched_getaffinity(0))
     rng = np.random.default_rng(case.seed)
-    code = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4}
+    code = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
 
     def run(n):
         rows = rng.integers(0, case.M, size=n)
@@ -293,7 +294,8 @@ def run_ours(args, case):
     binding.load_library()
 
     code = {"f16": binding.F16, "bf16": binding.BF16, "f32": binding.F32, "e4m3": binding.E4M3,
-            "e5m2": binding.E5M2}
+            "e5m2": binding.E5M2, "e2m1": binding.E2M1}
+    epu = 2 if case.in_dtype == "e2m1" else 1   # operand elements per stored byte (packed fp4)
     A, B, C = make_inputs(case)
     Ad, Bd = A.to(dev), B.to(dev)
     Cd = C.to(dev) if C is not None else None
@@ -312,7 +314,8 @@ def run_ours(args, case):
 
     def call(D_, A_, B_, C_, SFA_, SFB_, s_ptr):
         if case.mx:
-            rc = binding.gemm_mx(D_, A_, B_, C_, SFA_, SFB_, case.M, case.N, case.K, A_.stride(0), B_.stride(0),
+            rc = binding.gemm_mx(D_, A_, B_, C_, SFA_, SFB_, case.M, case.N, case.K, A_.stride(0) * epu,
+                                 B_.stride(0) * epu,
                                  C_.stride(0) if C_ is not None else case.N, D_.stride(0), SFA_.stride(0),
                                  SFB_.stride(0), case.transA, case.transB, case.alpha, case.beta,
                                  code[case.in_dtype], code[case.out_dtype], s_ptr)
@@ -464,7 +467,9 @@ def run_ours(args, case):
     achieved = case.flops / (per_launch_ms * 1e-3) / 1e12
     # 8-bit operands: no measured fp8 peak exists, so the measured bf16 figures
     # are scaled by the nominal dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s).
-    rate = FP8_RATE if case.in_dtype in ("e4m3", "e5m2") else 1.0
+    # Packed 4-bit operands run on the same kind::mxf8f6f4 instruction as the
+    # 8-bit ones (K = 32 per instruction), so their peak is the 8-bit one.
+    rate = FP8_RATE if case.in_dtype in ("e4m3", "e5m2", "e2m1") else 1.0
     peak = float(peaks["bf16_tflops"]) * rate
     src = ("%s bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json); f16 runs at the bf16 rate" % peak_src
            if rate == 1.0 else
@@ -495,7 +500,9 @@ def run_ours(args, case):
     roofline["burst"] = dict(burst, launches=BURST_STEPS, best_of=3, ms_per_launch=burst_ms)
     if case.mx:
         roofline["note"] = ("block-scaled: the time per launch is that of the whole gemm_mx step, the two small "
-                            "scale-rearranging launches included")
+                            "scale-rearranging launches included" +
+                            ("; packed E2M1 runs on kind::mxf8f6f4 at the 8-bit instruction rate, so the peak is "
+                             "the 8-bit one" if case.in_dtype == "e2m1" else ""))
     if clocks and clocks.get("sm_mhz") and roofline["bound"] == "tensor":
         clk_peak = num_sms * FLOP_PER_CLK_PER_SM * rate * clocks["sm_mhz"] * 1e6 / 1e12
         roofline["frac_of_clock_peak"] = achieved / clk_peak

@@ -13,7 +13,7 @@ import ctypes
 import os
 import threading
 
-F16, BF16, F32, E4M3, E5M2 = 0, 1, 2, 3, 4
+F16, BF16, F32, E4M3, E5M2, E2M1 = 0, 1, 2, 3, 4, 5
 GEMM_OK = 0
 GEMM_ERR_DEVICE_TIMEOUT = -8
 GEMM_ERR_UNSUPPORTED_LAYOUT = -10
@@ -120,9 +120,9 @@ def gemm_host(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, be
 def gemm_mx(D, A, B, C, SFA, SFB, M, N, K, lda, ldb, ldc, ldd, ld_sfa, ld_sfb, transA, transB, alpha, beta,
             in_dtype, out_dtype, stream=None) -> int:
     """The C entry point ``gemm_mx``: ``gemm`` with MX block-scaled E4M3 /
-    E5M2 operands (one UE8M0 scale byte per 32 K elements of each row of
-    op(A), SFA [M, ceil(K/32)], and of each column of op(B), SFB
-    [N, ceil(K/32)]).  Returns its status."""
+    E5M2 / packed E2M1 operands (one UE8M0 scale byte per 32 K elements of
+    each row of op(A), SFA [M, ceil(K/32)], and of each column of op(B),
+    SFB [N, ceil(K/32)]).  Returns its status."""
     lib = load_library()
     return lib.gemm_mx(_addr(D), _addr(A), _addr(B), _addr(C), _addr(SFA), _addr(SFB), int(M), int(N), int(K),
                        int(lda), int(ldb), int(ldc), int(ldd), int(ld_sfa), int(ld_sfb), int(transA), int(transB),

@@ -145,7 +145,11 @@ void tuning(GemmParams& p, int tile_n) {
 }
 
 bool is_f8(int dtype) { return dtype == GEMM_E4M3 || dtype == GEMM_E5M2; }
-int elem_size(int dtype) { return dtype == GEMM_F32 ? 4 : is_f8(dtype) ? 1 : 2; }
+// Bytes per element; packed E2M1 (two per byte) counts as 1 where a byte
+// granularity is asked (alignment), and its rows are addressed through
+// row_bytes().
+int elem_size(int dtype) { return dtype == GEMM_F32 ? 4 : (is_f8(dtype) || dtype == GEMM_E2M1) ? 1 : 2; }
+int64_t row_bytes(int dtype, int64_t elems) { return dtype == GEMM_E2M1 ? elems / 2 : elems * elem_size(dtype); }
 int out_kind_of(int out_dtype) {
     return out_dtype == GEMM_F32 ? gb300::kOutF32 : out_dtype == GEMM_F16 ? gb300::kOutF16 : gb300::kOutBF16;
 }
@@ -221,6 +225,9 @@ CUtensorMapDataType tma_dtype(int dt) {
         case GEMM_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
         case GEMM_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
         case GEMM_F32: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+        // packed E2M1: each 16-element (8-byte) group lands in 16 bytes of
+        // shared memory, the layout kind::mxf8f6f4 reads 4-bit operands in
+        case GEMM_E2M1: return CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
         default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
     }
 }
@@ -230,7 +237,7 @@ CUtensorMapDataType tma_dtype(int dt) {
 int encode_2d(CUtensorMap* map, int dt, const void* ptr, int64_t dim0, int64_t dim1, int64_t ld, uint32_t box0,
               uint32_t box1) {
     cuuint64_t dims[2] = {(cuuint64_t)dim0, (cuuint64_t)dim1};
-    cuuint64_t strides[1] = {(cuuint64_t)(ld * elem_size(dt))};
+    cuuint64_t strides[1] = {(cuuint64_t)row_bytes(dt, ld)};
     cuuint32_t box[2] = {box0, box1};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, tma_dtype(dt), 2, const_cast<void*>(ptr), dims, strides, box, estr,
@@ -450,8 +457,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
 // ones.  Grown on demand (freeing the old one synchronises the device) and
 // kept until the process exits.  `epoch` numbers the launches that use it.
 // Kinds: the stream-K partial sums and arrival counters, the repacked
-// operands / outputs of gemm_repacked, and gemm_mx's rearranged scales.
-enum WorkspaceKind { kWsStreamK = 0, kWsRepack = 1, kWsScales = 2 };
+// operands / outputs of gemm_repacked, gemm_mx's rearranged scales, and its
+// copies of 4-bit operands padded to TMA's 4-bit rules.
+enum WorkspaceKind { kWsStreamK = 0, kWsRepack = 1, kWsScales = 2, kWsFp4 = 3 };
 struct Workspace {
     int kind;
     int dev;
@@ -570,7 +578,7 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
                      int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA,
                      int transB, float alpha, float beta, int in_dtype, int out_dtype) {
     const bool has_c = beta != 0.0f;
-    const bool f8 = is_f8(in_dtype);
+    const bool f8 = is_f8(in_dtype) || in_dtype == GEMM_E2M1;   // 128 K elements per 128-byte shared row
     const int osz = elem_size(out_dtype);
     int rc;
     if ((rc = get_encoder()) != GEMM_OK) return rc;
@@ -690,14 +698,21 @@ int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t 
                   int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA, int transB, float alpha,
                   float beta, int in_dtype, int out_dtype, int dev, cudaStream_t s, bool may_grow,
                   const void* SFA = nullptr, const void* SFB = nullptr, int64_t ld_sfa = 0, int64_t ld_sfb = 0) {
-    const int isz = elem_size(in_dtype);
+    // Packed 4-bit operands (K-major, K and the leading dimensions even) are
+    // moved as rows of K / 2 bytes.
+    const bool fp4 = in_dtype == GEMM_E2M1;
+    const int64_t epu = fp4 ? 2 : 1;   // elements per copied unit
+    const int64_t Ku = K / epu;
+    lda /= epu;
+    ldb /= epu;
+    const int isz = fp4 ? 1 : elem_size(in_dtype);
     const int osz = elem_size(out_dtype);
     const bool has_c = beta != 0.0f;
-    const bool f8 = is_f8(in_dtype);
+    const bool f8 = is_f8(in_dtype) || fp4;
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
     auto round_up = [](int64_t x, int64_t m) { return (x + m - 1) / m * m; };
-    const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
-    const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
+    const int64_t a_rows = transA ? Ku : M, a_cols = transA ? M : Ku;
+    const int64_t b_rows = transB ? N : Ku, b_cols = transB ? Ku : N;
     // 8-bit operands end up K-major: A as [M, K] (transA2 = 0), B as [N, K] (transB2 = 1)
     const int transA2 = f8 ? 0 : transA;
     const int transB2 = f8 ? 1 : transB;
@@ -750,8 +765,8 @@ int gemm_repacked(void* D, const void* A, const void* B, const void* C, int64_t 
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
-    const int rc = SFA ? gemm_mx(D2, A2, B2, C2, SFA, SFB, M, N, K, lda2, ldb2, ldc2, ldd2, ld_sfa, ld_sfb, transA2,
-                                 transB2, alpha, beta, in_dtype, out_dtype, s)
+    const int rc = SFA ? gemm_mx(D2, A2, B2, C2, SFA, SFB, M, N, K, lda2 * epu, ldb2 * epu, ldc2, ldd2, ld_sfa, ld_sfb,
+                                 transA2, transB2, alpha, beta, in_dtype, out_dtype, s)
                        : gemm(D2, A2, B2, C2, M, N, K, lda2, ldb2, ldc2, ldd2, transA2, transB2, alpha, beta,
                               in_dtype, out_dtype, s);
     if (rc != GEMM_OK || d_ok) return rc;
@@ -919,8 +934,19 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
             int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int64_t ld_sfa, int64_t ld_sfb,
             int transA, int transB, float alpha, float beta, int in_dtype, int out_dtype,
             struct CUstream_st* stream) {
-    if (!is_f8(in_dtype)) return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "block scaling needs E4M3 / E5M2 operands");
-    int rc = validate(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, beta, in_dtype, out_dtype);
+    const bool fp4 = in_dtype == GEMM_E2M1;
+    if (!is_f8(in_dtype) && !fp4)
+        return reject(GEMM_ERR_UNSUPPORTED_DTYPE, "block scaling needs E4M3 / E5M2 / E2M1 operands");
+    // Packed 4-bit operands: K-major only (A [M, K], B [N, K]), whole bytes
+    // per row (K and the leading dimensions even).  Validated as the byte
+    // matrices they are: A [M, K / 2], B [N, K / 2].
+    if (fp4 && (transA != 0 || transB != 1) && M > 0 && N > 0 && K > 0)
+        return reject(GEMM_ERR_UNSUPPORTED_LAYOUT, "4-bit operands must be K-major (transA = 0, transB = 1)");
+    if (fp4 && K > 0 && M > 0 && N > 0 && ((K | lda | ldb) & 1))
+        return reject(GEMM_ERR_INVALID_ARG, "4-bit operands: K, lda and ldb must be even");
+    const int64_t epu = fp4 ? 2 : 1;   // elements per byte of A and B
+    const int vdt = fp4 ? GEMM_E4M3 : in_dtype;
+    int rc = validate(D, A, B, C, M, N, K / epu, lda / epu, ldb / epu, ldc, ldd, transA, transB, beta, vdt, out_dtype);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
     if ((rc = validate_scales(D, SFA, SFB, M, N, K, ld_sfa, ld_sfb, ldd, out_dtype)) != GEMM_OK) return rc;
 
@@ -937,9 +963,16 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
     if ((rc = device_state(dev, &ds)) != GEMM_OK) return reject(rc, "device set-up");
     const bool has_c = beta != 0.0f;
     if (K == 0) return launch_k0_or_reject(out_dtype, D, C, M, N, ldc, ldd, alpha, beta, ds->num_sms, s);
-    const bool direct_ok =
-        tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, elem_size(in_dtype), elem_size(out_dtype), has_c) &&
-        operand_majors_ok(in_dtype, transA, transB);
+    // Packed 4-bit operands reach shared memory through TMA's 16U4_ALIGN16B
+    // type, which wants 32-byte-aligned rows of a multiple of 128 elements;
+    // the other layouts are copied below into rows of K rounded up to 128,
+    // zero-padded.  D and C follow gemm()'s rules.
+    auto a32 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 31u) == 0; };
+    const bool fp4_ops_ok = !fp4 || (a32(A) && a32(B) && lda % 64 == 0 && ldb % 64 == 0 && K % 128 == 0);
+    const bool direct_ok = fp4 ? tma_layout_ok(D, nullptr, nullptr, C, 0, 0, 0, ldc, ldd, 1, elem_size(out_dtype), has_c)
+                               : tma_layout_ok(D, A, B, C, K, lda, ldb, ldc, ldd, elem_size(in_dtype),
+                                               elem_size(out_dtype), has_c) &&
+                                     operand_majors_ok(in_dtype, transA, transB);
     if (!direct_ok) {
         GEMM_LOGF("mx: M=%lld N=%lld K=%lld: layout the tcgen05 kernel cannot take as it is, repacked", (long long)M,
                   (long long)N, (long long)K);
@@ -947,6 +980,29 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
                            dev, s, !in_capture, SFA, SFB, ld_sfa, ld_sfb);
         if (rc != kNoWorkspace) return rc == GEMM_OK ? GEMM_OK : reject(rc, "repacked call");
         return reject(GEMM_ERR_UNSUPPORTED_LAYOUT, "8-bit operands: no workspace for repacking");
+    }
+
+    int64_t k_map = K;   // the K extent of the operand tensor maps
+    if (!fp4_ops_ok) {
+        const int64_t kp = (K + 127) / 128 * 128;
+        const int64_t a_bytes = (M * (kp / 2) + 255) / 256 * 256;
+        const int64_t b_bytes = (N * (kp / 2) + 255) / 256 * 256;
+        void* fws = nullptr;
+        uint32_t fepoch = 0;
+        if (workspace_for(kWsFp4, dev, s, a_bytes + b_bytes, &fws, &fepoch, !in_capture) != GEMM_OK)
+            return reject(GEMM_ERR_CUDA, "4-bit operand workspace");
+        uint8_t* a2 = static_cast<uint8_t*>(fws);
+        uint8_t* b2 = a2 + a_bytes;
+        GEMM_LOGF("mx: 4-bit operands copied into 32-byte-aligned rows of %lld elements", (long long)kp);
+        if (cudaMemsetAsync(fws, 0, (size_t)(a_bytes + b_bytes), s) != cudaSuccess ||
+            gb300::launch_copy2d(a2, kp / 2, A, lda / 2, M, K / 2, 1, s) != cudaSuccess ||
+            gb300::launch_copy2d(b2, kp / 2, B, ldb / 2, N, K / 2, 1, s) != cudaSuccess) {
+            cudaGetLastError();
+            return reject(GEMM_ERR_LAUNCH, "4-bit operand copies");
+        }
+        A = a2;
+        B = b2;
+        lda = ldb = k_map = kp;
     }
 
     Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, 1, 1);
@@ -974,22 +1030,27 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
         pl = make_plan(M, N, K, ds->num_sms, false, out_dtype, 1, 1);   // whole tiles: no workspace
     }
     TcgenLaunch L;
-    if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
+    // (packed 4-bit operands: maps of k_map elements per row; 128 of them
+    // fill a 128-byte shared-memory row, as 8-bit ones do)
+    if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, k_map, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
                                in_dtype, out_dtype)) != GEMM_OK)
         return reject(rc, "tensor maps");
     GemmParams& p = L.p;
+    p.K = (int32_t)K;
+    p.num_k_blocks = pl.iters;
     // tcgen05 instruction descriptor, kind::mxf8f6f4: A / B format (bits 7-9,
-    // 10-12: 0 = E4M3, 1 = E5M2), both K-major (bits 15, 16 = 0), N >> 3
+    // 10-12: 0 = E4M3, 1 = E5M2, 5 = E2M1), both K-major (bits 15, 16 = 0), N >> 3
     // (bits 17-22), scale type UE8M0 (bit 23), M >> 4 (bits 24-28); the
     // kernel adds the scale-byte IDs of each K slice (bits 4-5 for B, 29-30
     // for A).  The accumulator is f32 by definition of the kind.
-    const uint32_t fmt = in_dtype == GEMM_E5M2 ? 1u : 0u;
+    const uint32_t fmt = fp4 ? 5u : in_dtype == GEMM_E5M2 ? 1u : 0u;
     p.idesc = (fmt << 7) | (fmt << 10) | (((uint32_t)pl.tile_n >> 3) << 17) | (1u << 23) |
               (((uint32_t)pl.tile_m >> 4) << 24);
     if ((rc = encode_sf(&L.sfa, sfa_tiles, sfa_bytes / 512, 1)) != GEMM_OK ||
         (rc = encode_sf(&L.sfb, sfb_tiles, sfb_bytes / 512, (uint32_t)sfb_chunks)) != GEMM_OK)
         return reject(rc, "scale tensor maps");
     p.sf_a_groups = (int32_t)a_groups;
+    p.operands_packed4 = fp4 ? 1 : 0;
     L.mx = 1;
     p.status = ds->d_status;
     p.skip_first_stage = skip_first_stage_setting();

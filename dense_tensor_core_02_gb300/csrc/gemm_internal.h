@@ -27,7 +27,7 @@ struct TcgenLaunch {
     int epi_warps;            // 4 or 8 epilogue warps
     int tile_n;               // 256, or 64 for the narrow single-CTA tiles
     int f8;                   // 1: E4M3 / E5M2 operands (kind::f8f6f4), K-major only
-    int mx;                   // 1: and MX block-scaled (kind::mxf8f6f4), 192-wide tiles
+    int mx;                   // 1: MX block-scaled (kind::mxf8f6f4; 8-bit or packed E2M1 operands), 192-wide tiles
     int pdl;                  // 1: launch with programmatic stream serialisation
 };
 

@@ -72,7 +72,10 @@ struct GemmParams {
     // kc * sf_a_groups + g.  SFB chunks of sub-block kc and N tile nb: the
     // (tile N / 128) rows from (kc * num_n_tiles + nb) * (tile N / 128) on.
     int32_t sf_a_groups;      // 128-row groups per sub-block in the SFA map (M tiles x CTAs per tile)
-    int32_t pad3;
+    // 1: packed E2M1 operands.  TMA's 16U4_ALIGN16B copies fill each 128-byte
+    // shared row with 64 bytes of data (8 bytes per 16-byte group) and count
+    // only those toward the barrier's transaction bytes.
+    int32_t operands_packed4;
 };
 
 // ---------------------------------------------------------------------------

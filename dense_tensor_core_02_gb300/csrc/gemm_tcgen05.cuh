@@ -360,7 +360,8 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            const uint32_t stage_tx = (kPair ? 2 : 1) * (Cf::kStageBytes + Cf::kSfBytes);
+            const uint32_t stage_tx =
+                (kPair ? 2 : 1) * ((kMX && p.operands_packed4 ? Cf::kStageBytes / 2 : Cf::kStageBytes) + Cf::kSfBytes);
             const uint64_t pol_a = ptx::l2_policy(p.hint_a);
             const uint64_t pol_b = ptx::l2_policy(p.hint_b);
             const uint64_t pol_sf = ptx::l2_policy(2);   // scales: re-read by every tile of their row / column

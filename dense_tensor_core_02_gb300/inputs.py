@@ -21,7 +21,7 @@ import torch
 
 _TORCH_DTYPE = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
                 "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
-_ELEM_BYTES = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}
+_ELEM_BYTES = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1, "e2m1": 0.5}
 
 
 @dataclasses.dataclass(frozen=True)
@@ -31,7 +31,7 @@ class GemmCase:
     M: int
     N: int
     K: int
-    in_dtype: str = "f16"          # dtype of A and B
+    in_dtype: str = "f16"          # dtype of A and B ("e2m1": packed fp4, uniform random codes)
     out_dtype: str = "f32"         # dtype of C and D
     dist: str = "normal"           # "normal" (mean 0, std) or "uniform" on [-1, 1]
     std: float = 1.0
@@ -63,8 +63,8 @@ class GemmCase:
         isz = _ELEM_BYTES[self.in_dtype]
         osz = _ELEM_BYTES[self.out_dtype]
         scale_bytes = (self.M + self.N) * ((self.K + 31) // 32) if self.mx else 0
-        return (isz * (self.M * self.K + self.K * self.N) + osz * self.M * self.N * (1 + (self.beta != 0)) +
-                scale_bytes)
+        return int(isz * (self.M * self.K + self.K * self.N) + osz * self.M * self.N * (1 + (self.beta != 0)) +
+                   scale_bytes)
 
 
 def _draw(gen, shape, dist, std):
@@ -76,16 +76,30 @@ def _draw(gen, shape, dist, std):
     raise ValueError(dist)
 
 
+def packed_fp4(gen, shape):
+    """Uniform random E2M1 codes for a row-major [rows, cols] operand (cols
+    even), packed two to a byte, even columns in the low nibble: uint8
+    [rows, cols / 2]."""
+    rows, cols = shape
+    codes = torch.randint(0, 16, (rows, cols), generator=gen, dtype=torch.int32)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).to(torch.uint8)
+
+
 def make_inputs(case: GemmCase):
     """CPU tensors (A, B, C) for ``case``; C is None when beta == 0.
 
     The generator is ``torch.Generator().manual_seed(case.seed)``; A, B
-    and C are drawn from it in that order.
+    and C are drawn from it in that order.  Packed E2M1 operands are uint8
+    tensors of uniform random codes (``packed_fp4``).
     """
     gen = torch.Generator().manual_seed(case.seed)
-    dt = _TORCH_DTYPE[case.in_dtype]
-    A = _draw(gen, case.a_shape, case.dist, case.std).to(dt)
-    B = _draw(gen, case.b_shape, case.dist, case.std).to(dt)
+    if case.in_dtype == "e2m1":
+        A = packed_fp4(gen, case.a_shape)
+        B = packed_fp4(gen, case.b_shape)
+    else:
+        dt = _TORCH_DTYPE[case.in_dtype]
+        A = _draw(gen, case.a_shape, case.dist, case.std).to(dt)
+        B = _draw(gen, case.b_shape, case.dist, case.std).to(dt)
     C = None
     if case.beta != 0.0:
         C = _draw(gen, (case.M, case.N), case.c_dist, 1.0).to(_TORCH_DTYPE[case.out_dtype])
@@ -139,6 +153,8 @@ def _cases():
         GemmCase("gemm_8192_mxe4m3_transB", k8192, k8192, k8192, "e4m3", transB=1, mx=True),
         GemmCase("gemm_4096_mxe5m2_transB_beta1", 4096, 4096, 4096, "e5m2", dist="uniform",
                  transB=1, alpha=1.0, beta=1.0, c_dist="uniform", mx=True),
+        # packed fp4 (E2M1, the guide's other gemm_async precision), block-scaled
+        GemmCase("gemm_8192_mxe2m1_transB", k8192, k8192, k8192, "e2m1", transB=1, mx=True),
     ]
     return [dataclasses.replace(c, seed=1000 + i + 1) for i, c in enumerate(rows)]
 

@@ -66,7 +66,10 @@ typedef enum {
     GEMM_BF16 = 1, /* bfloat16 */
     GEMM_F32 = 2,  /* IEEE binary32 (outputs only) */
     GEMM_E4M3 = 3, /* 8-bit float, 1-4-3, bias 7, no infinities, S.1111.111 = NaN (operands only) */
-    GEMM_E5M2 = 4  /* 8-bit float, 1-5-2, bias 15, with infinities and NaNs (operands only) */
+    GEMM_E5M2 = 4, /* 8-bit float, 1-5-2, bias 15, with infinities and NaNs (operands only) */
+    GEMM_E2M1 = 5  /* 4-bit float, 1-2-1, bias 1 (0, 0.5, 1, 1.5, 2, 3, 4, 6), packed two per byte,
+                      even elements in the low nibble; leading dimensions count elements
+                      (gemm_mx operands only) */
 } gemm_dtype_t;
 
 typedef enum {
@@ -152,7 +155,15 @@ GEMM_API int gemm(void* D, const void* A, const void* B, const void* C,
  *                    whatever transB says).  Any byte alignment.  Not read
  *                    when K == 0 (may then be NULL).
  *   ld_sfa, ld_sfb   >= ceil(K/32) when K > 0.
- *   in_dtype         GEMM_E4M3 or GEMM_E5M2 (else GEMM_ERR_UNSUPPORTED_DTYPE).
+ *   in_dtype         GEMM_E4M3, GEMM_E5M2 or GEMM_E2M1 (else
+ *                    GEMM_ERR_UNSUPPORTED_DTYPE).  E2M1 (fp4, the guide's
+ *                    other gemm_async precision) is packed: element e of a
+ *                    row-major operand (e = row * ld + col) is the low nibble
+ *                    of byte e / 2 when e is even, the high nibble when odd.
+ *                    It must be K-major (A stored [M, K], transA = 0; B
+ *                    stored [N, K], transB = 1; else
+ *                    GEMM_ERR_UNSUPPORTED_LAYOUT) with K, lda and ldb even
+ *                    (else GEMM_ERR_INVALID_ARG).
  *   everything else  as for gemm().
  *
  * Kernel: tcgen05.mma kind::mxf8f6f4 with 256 x 192 tiles on a CTA pair

@@ -18,7 +18,7 @@ import torch
 import oracle.oracle as oracle
 from dense_tensor_core_02_gb300 import binding
 
-CODE = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4}
+CODE = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
 TORCH = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32, "e4m3": torch.float8_e4m3fn,
          "e5m2": torch.float8_e5m2}
 ORACLE_THREADS = max(1, min(16, len(os.sched_getaffinity(0))))

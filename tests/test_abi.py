@@ -346,3 +346,17 @@ def test_mx_valid_calls_reach_the_device(lib):
         rc = _call_mx(**kw)
         assert rc in (0, -7, -5), (kw, rc)
     assert _call_mx(M=0) == 0 and _call_mx(N=0) == 0
+
+
+def test_fp4_only_through_gemm_mx(lib):
+    assert _call(in_dtype=5) == -2                        # gemm() has no 4-bit operands
+    assert _call_mx(in_dtype=5, transA=1) == -10          # packed fp4 is K-major only
+    assert _call_mx(in_dtype=5, transB=0) == -10
+    assert _call_mx(in_dtype=5, K=63, lda=64, ldb=64) == -1   # whole bytes per row
+    assert _call_mx(in_dtype=5, lda=65, ldb=66) == -1
+    assert _call_mx(in_dtype=5, lda=62) == -1             # lda >= K
+    assert _call_mx(in_dtype=5, D=A_ + 16) == -4          # D overlaps A's bytes ([64, 32] bytes from A_)
+    assert _call_mx(in_dtype=5, D=A_ + 64 * 32) in (0, -7, -5)   # just past A's last byte: no overlap
+    for kw in (dict(), dict(A=A_ + 3, lda=70), dict(K=2, lda=2, ldb=2)):
+        rc = _call_mx(in_dtype=5, **kw)
+        assert rc in (0, -7, -5), (kw, rc)

@@ -72,8 +72,9 @@ def run_mx(A, B, C, SFA, SFB, M, N, K, *, transA=0, transB=1, alpha=1.0, beta=0.
         view.copy_(S.to(dev))
         sf.append((view, S.stride(0)))
     D = torch.full((M, N), float("nan"), dtype=H.TORCH[out_dtype], device=dev)
-    lda = Ad.stride(0) if Ad is not None else 0
-    ldb = Bd.stride(0) if Bd is not None else 0
+    epu = 2 if in_dtype == "e2m1" else 1   # packed fp4: leading dimensions count elements
+    lda = Ad.stride(0) * epu if Ad is not None else 0
+    ldb = Bd.stride(0) * epu if Bd is not None else 0
     ldc = Cd.stride(0) if Cd is not None else N
     rc = binding.gemm_mx(D, Ad, Bd, Cd, sf[0][0], sf[1][0], M, N, K, lda, ldb, ldc, D.stride(0), sf[0][1],
                          sf[1][1], transA, transB, alpha, beta, H.CODE[in_dtype], H.CODE[out_dtype], None)
@@ -270,3 +271,112 @@ def test_workload_sampled(case):
                                      alpha=case.alpha, beta=case.beta, in_dtype=H.CODE[case.in_dtype],
                                      c_dtype=H.CODE[case.out_dtype])
     H.assert_close(D.double().numpy()[rows, cols], ref, bound, case.out_dtype, case.name)
+
+
+# ---- packed E2M1 (fp4) operands ----------------------------------------------
+
+
+def fp4_matrix(rows, K, seed, lo_code=0, hi_code=15, pad=0):
+    """Random E2M1 codes in [lo_code, hi_code], packed two per byte (even
+    columns low): uint8 [rows, (K + pad) / 2], the padding all-ones codes."""
+    g = torch.Generator().manual_seed(seed)
+    codes = torch.full((rows, K + pad), 0xF, dtype=torch.int32)
+    codes[:, :K] = torch.randint(lo_code, hi_code + 1, (rows, K), generator=g, dtype=torch.int32)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).to(torch.uint8)
+
+
+FP4_SHAPES = [(128, 192, 256), (16, 8, 64), (1, 1, 2), (257, 200, 160), (300, 400, 544), (640, 520, 1040),
+              (129, 385, 48)]
+
+
+@pytest.mark.parametrize("shape", FP4_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("beta", [0.0, 1.0])
+def test_fp4_exact(variant, shape, beta):
+    """E2M1 products are multiples of 1/4 and the scales stay within 2^+-1,
+    so every fp32 partial sum is exact: bit for bit."""
+    M, N, K = shape
+    seed = 7 * M + 5 * N + K + 2 * int(beta)
+    A = fp4_matrix(M, K, seed)
+    B = fp4_matrix(N, K, seed + 1)
+    C = H.int_matrix((M, N), -100, 100, "f32", seed + 2) if beta else None
+    SFA = scales(M, K, 126, 128, seed + 3, pad=1)
+    SFB = scales(N, K, 126, 128, seed + 4, pad=2)
+    kw = dict(beta=beta, in_dtype="e2m1")
+    D, rc = run_mx(A, B, C, SFA, SFB, M, N, K, **kw)
+    assert rc == 0
+    ref, _ = oracle_mx(A, B, C, SFA, SFB, M, N, K, **kw)
+    H.assert_exact(D.numpy(), ref, "fp4 %s beta=%s" % (shape, beta))
+
+
+def test_fp4_each_block_takes_its_own_scale(variant):
+    M, N, K = 256, 384, 512
+    A = fp4_matrix(M, K, 131, 2, 2)      # all 1.0
+    B = fp4_matrix(N, K, 132, 2, 2)
+    kb = K // 32
+    SFA = torch.tensor([[124 + (i + 3 * b) % 8 for b in range(kb)] for i in range(M)], dtype=torch.uint8)
+    SFB = torch.tensor([[124 + (j * 5 + b) % 7 for b in range(kb)] for j in range(N)], dtype=torch.uint8)
+    D, rc = run_mx(A, B, None, SFA, SFB, M, N, K, in_dtype="e2m1")
+    assert rc == 0
+    ref, _ = oracle_mx(A, B, None, SFA, SFB, M, N, K, in_dtype="e2m1")
+    H.assert_exact(D.numpy(), ref, "fp4 per-block scales")
+
+
+@pytest.mark.parametrize("out_dtype", ["f32", "f16", "bf16"])
+def test_fp4_random_wide_scales(variant, out_dtype):
+    M, N, K = 520, 392, 776
+    seed = 141 + ["f32", "f16", "bf16"].index(out_dtype)
+    A = fp4_matrix(M, K, seed)
+    B = fp4_matrix(N, K, seed + 1)
+    C = H.normal_matrix((M, N), out_dtype, seed + 2)
+    # (for f16 D the scales stay small enough that |D| < 65504: an overflow
+    # would round to infinity, correctly, and say nothing about the product)
+    hi = 129 if out_dtype == "f16" else 135
+    SFA = scales(M, K, 115, hi, seed + 3)
+    SFB = scales(N, K, 118, hi - 4, seed + 4)
+    kw = dict(alpha=-0.625, beta=0.75, in_dtype="e2m1", out_dtype=out_dtype)
+    D, rc = run_mx(A, B, C, SFA, SFB, M, N, K, **kw)
+    assert rc == 0
+    ref, bound = oracle_mx(A, B, C, SFA, SFB, M, N, K, **kw)
+    H.assert_close(D.double().numpy(), ref, bound, out_dtype, "fp4 random -> %s" % out_dtype)
+
+
+def test_fp4_padded_and_offset_rows():
+    """Leading dimensions off the 16-byte grid and an odd byte offset: the
+    rows are copied into aligned workspace first; the padding (all-ones
+    codes, -6.0) must never be read."""
+    M, N, K = 200, 136, 102
+    A = fp4_matrix(M, K, 151, pad=6)     # lda = 108 elements = 54 bytes
+    B = fp4_matrix(N, K, 152, pad=2)     # ldb = 104 = 52 bytes
+    SFA = scales(M, K, 126, 128, 153)
+    SFB = scales(N, K, 126, 128, 154)
+    D, rc = run_mx(A, B, None, SFA, SFB, M, N, K, in_dtype="e2m1")
+    assert rc == 0
+    ref, _ = oracle.gemm(A, B, None, M, N, K, transB=1, in_dtype=H.CODE["e2m1"], lda=K + 6, ldb=K + 2,
+                         threads=H.ORACLE_THREADS, sfa=SFA.numpy(), sfb=SFB.numpy())
+    H.assert_exact(D.numpy(), ref, "fp4 padded rows")
+    dev = torch.device("cuda", 0)
+    buf = torch.zeros(A.numel() + 1 + 64, dtype=torch.uint8, device=dev)
+    Av = buf[1:1 + A.numel()].view(A.shape)   # odd byte offset
+    Av.copy_(A.to(dev))
+    Bd, sa, sb = B.to(dev), SFA.to(dev), SFB.to(dev)
+    Dd = torch.full((M, N), float("nan"), device=dev)
+    rc = binding.gemm_mx(Dd, Av, Bd, None, sa, sb, M, N, K, K + 6, K + 2, N, N, sa.stride(0), sb.stride(0), 0, 1,
+                         1.0, 0.0, H.CODE["e2m1"], H.CODE["f32"], None)
+    torch.cuda.synchronize()
+    assert rc == 0
+    H.assert_exact(Dd.cpu().numpy(), ref, "fp4 odd byte offset")
+
+
+def test_fp4_streamk_split(variant):
+    M, N, K = 1024, 768, 4160
+    A = fp4_matrix(M, K, 161)
+    B = fp4_matrix(N, K, 162)
+    SFA = scales(M, K, 126, 128, 163)
+    SFB = scales(N, K, 126, 128, 164)
+    with H.env(GEMM_SK_MIN_ITERS="1"):
+        D, rc = run_mx(A, B, None, SFA, SFB, M, N, K, in_dtype="e2m1")
+    assert rc == 0
+    rows, cols = H.sample_positions(M, N, per_block=8, seed=29)
+    ref, _ = oracle.gemm_entries(A, B, None, M, N, K, rows, cols, transB=1, in_dtype=H.CODE["e2m1"],
+                                 threads=H.ORACLE_THREADS, sfa=SFA.numpy(), sfb=SFB.numpy())
+    H.assert_exact(D.numpy()[rows, cols], ref, "fp4 stream-K")
