@@ -39,6 +39,8 @@ E2E_STREAMS = 2                      # streams the end-to-end steps alternate be
 BURST_STEPS = 10                     # launches per burst measurement
 KERNEL_SOURCES = ["dense_tensor_core_02_gb300/csrc/gemm_tcgen05.cuh",
                   "dense_tensor_core_02_gb300/csrc/gemm_sm103.cu",
+                  "dense_tensor_core_02_gb300/csrc/gemm_sm103_f8.cu",
+                  "dense_tensor_core_02_gb300/csrc/gemm_sm103_mx.cu",
                   "dense_tensor_core_02_gb300/csrc/ptx.cuh",
                   "dense_tensor_core_02_gb300/csrc/gemm_params.h"]
 
