@@ -115,3 +115,75 @@ def test_captured_noalloc_and_host():
     ref, _ = H.oracle_full(A, B, None, M, N, K)
     H.assert_exact(Dd.cpu().numpy(), 2.0 * ref, "captured no-alloc")
     H.assert_exact(hD.numpy(), -ref, "captured gemm_host")
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "e2m1"])
+def test_captured_gemm_mx_replays(dtype):
+    """gemm_mx in a graph, after a call of the same size on the stream made
+    its workspaces (rearranged scales; for 4-bit rows off TMA's grid, the
+    padded operand copies, whose memset and copies are captured too).
+    Replays with new operands and new scales in the same buffers."""
+    import oracle.oracle as oracle
+    from tests.test_mx_gpu import fp4_matrix, scales
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream()
+    M, N, K = 512, 384, (1000 if dtype == "e2m1" else 1024)
+    epu = 2 if dtype == "e2m1" else 1
+
+    def operands(seed):
+        if dtype == "e2m1":
+            return fp4_matrix(M, K, seed), fp4_matrix(N, K, seed + 1)
+        return H.int_matrix((M, K), -8, 8, dtype, seed), H.int_matrix((N, K), -8, 8, dtype, seed + 1)
+
+    A, B = operands(201)
+    SFA, SFB = scales(M, K, 126, 128, 203), scales(N, K, 126, 128, 204)
+    Ad, Bd, sa, sb = A.to(dev), B.to(dev), SFA.to(dev), SFB.to(dev)
+    Dd = torch.empty((M, N), device=dev)
+
+    def call():
+        rc = binding.gemm_mx(Dd, Ad, Bd, None, sa, sb, M, N, K, Ad.stride(0) * epu, Bd.stride(0) * epu, N, N,
+                             sa.stride(0), sb.stride(0), 0, 1, 1.0, 0.0, H.CODE[dtype], H.CODE["f32"], s)
+        assert rc == 0
+
+    with torch.cuda.stream(s):
+        call()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for rep in range(2):
+        if rep == 1:
+            A, B = operands(301)
+            SFA = scales(M, K, 126, 128, 303)
+            Ad.copy_(A)
+            Bd.copy_(B)
+            sa.copy_(SFA)
+        Dd.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref, _ = oracle.gemm(A, B, None, M, N, K, transB=1, in_dtype=H.CODE[dtype], threads=H.ORACLE_THREADS,
+                             sfa=SFA.numpy(), sfb=SFB.numpy())
+        H.assert_exact(Dd.cpu().numpy(), ref, "gemm_mx replay %d (%s)" % (rep, dtype))
+
+
+def test_captured_gemm_mx_without_workspace_is_refused():
+    """On a stream with no earlier gemm_mx call the scale workspace does not
+    exist, and a capture may not allocate it: the call is refused before it
+    enqueues anything (GEMM_ERR_CUDA) and the capture stays valid."""
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream()
+    M, N, K = 256, 192, 256
+    A = H.int_matrix((M, K), -8, 8, "e4m3", 211).to(dev)
+    B = H.int_matrix((N, K), -8, 8, "e4m3", 212).to(dev)
+    sa = torch.full((M, K // 32), 127, dtype=torch.uint8, device=dev)
+    sb = torch.full((N, K // 32), 127, dtype=torch.uint8, device=dev)
+    Dd = torch.full((M, N), 3.0, device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        rc = binding.gemm_mx(Dd, A, B, None, sa, sb, M, N, K, K, K, N, N, K // 32, K // 32, 0, 1, 1.0, 0.0,
+                             H.CODE["e4m3"], H.CODE["f32"], s)
+        Dd.add_(1.0)
+    assert rc == -7
+    g.replay()
+    torch.cuda.synchronize()
+    assert bool((Dd == 4.0).all()), "the refused call must not have written D"

@@ -380,3 +380,74 @@ def test_fp4_streamk_split(variant):
     ref, _ = oracle.gemm_entries(A, B, None, M, N, K, rows, cols, transB=1, in_dtype=H.CODE["e2m1"],
                                  threads=H.ORACLE_THREADS, sfa=SFA.numpy(), sfb=SFB.numpy())
     H.assert_exact(D.numpy()[rows, cols], ref, "fp4 stream-K")
+
+
+# ---- seeded sweep over gemm_mx's argument space ------------------------------
+
+
+def _mx_case(seed):
+    rng = np.random.default_rng(seed)
+    pick = lambda xs: xs[int(rng.integers(len(xs)))]
+    dtype = pick(["e4m3", "e5m2", "e2m1"])
+    dims = [1, 7, 16, 33, 128, 129, 192, 255, 300, 513]
+    kdims = [0, 2, 16, 32, 64, 100, 128, 256, 300, 640] + ([] if dtype == "e2m1" else [1, 7, 33, 129])
+    c = dict(M=pick(dims), N=pick(dims), K=pick(kdims), dtype=dtype, out=pick(["f32", "f16", "bf16"]),
+             transA=0 if dtype == "e2m1" else int(rng.integers(2)),
+             transB=1 if dtype == "e2m1" else int(rng.integers(2)),
+             beta=pick([0.0, 1.0, -0.5]), alpha=pick([1.0, 2.0, -0.75]),
+             pad=pick([0, 0, 2, 6]), off=pick([0, 0, 1, 3]), sf_pad=pick([0, 1, 5]), sf_off=pick([0, 1]),
+             variant=pick([None, None, "single"]))
+    c["exact"] = c["out"] == "f32" and c["alpha"] in (1.0, 2.0) and c["beta"] in (0.0, 1.0)
+    return c
+
+
+def _place(host_u8, off, dev):
+    """A uint8 [rows, cols] matrix at byte offset `off` of a device buffer."""
+    buf = torch.full((host_u8.numel() + off + 64,), 0xFF, dtype=torch.uint8, device=dev)
+    v = buf[off:off + host_u8.numel()].view(host_u8.shape)
+    v.copy_(host_u8.to(dev))
+    return v
+
+
+@pytest.mark.parametrize("seed", range(60))
+def test_mx_fuzz(seed):
+    c = _mx_case(3000 + seed)
+    M, N, K, dt = c["M"], c["N"], c["K"], c["dtype"]
+    dev = torch.device("cuda", 0)
+    epu = 2 if dt == "e2m1" else 1
+    pad = c["pad"] if dt != "e2m1" else 2 * (c["pad"] // 2)
+    # operands as stored (padded rows), then viewed as bytes
+    ra, ca = (K, M) if c["transA"] else (M, K)
+    rb, cb = (N, K) if c["transB"] else (K, N)
+    if dt == "e2m1":
+        A = fp4_matrix(ra, ca, seed, pad=pad)
+        B = fp4_matrix(rb, cb, seed + 1, pad=pad)
+    else:
+        A = H.int_matrix((ra, ca + pad), -8, 8, dt, seed).view(torch.uint8)
+        B = H.int_matrix((rb, cb + pad), -8, 8, dt, seed + 1).view(torch.uint8)
+    lda, ldb = (ca + pad), (cb + pad)
+    C = H.int_matrix((M, N), -50, 50, c["out"], seed + 2) if c["beta"] else None
+    # (f16 D: scales small enough that |D| stays below the f16 maximum)
+    lo, hi = (126, 128) if c["exact"] else (118, 126) if c["out"] == "f16" else (118, 134)
+    SFA = scales(M, K, lo, hi, seed + 3, pad=c["sf_pad"])
+    SFB = scales(N, K, lo, hi, seed + 4, pad=c["sf_pad"])
+    Av, Bv = _place(A, c["off"], dev), _place(B, c["off"] * 2, dev)
+    sav, sbv = _place(SFA, c["sf_off"], dev), _place(SFB, c["sf_off"], dev)
+    Cd = C.to(dev) if C is not None else None
+    D = torch.full((M, N), float("nan"), dtype=H.TORCH[c["out"]], device=dev)
+    with H.env(GEMM_VARIANT=c["variant"]):
+        rc = binding.gemm_mx(D, Av if K else None, Bv if K else None, Cd, sav if K else None, sbv if K else None,
+                             M, N, K, lda, ldb, N, N, SFA.shape[1], SFB.shape[1], c["transA"], c["transB"],
+                             c["alpha"], c["beta"], H.CODE[dt], H.CODE[c["out"]], None)
+    torch.cuda.synchronize()
+    assert rc == 0, (c, binding.gemm_status_string(rc))
+    Ao = A if dt == "e2m1" else A.view(H.TORCH[dt])
+    Bo = B if dt == "e2m1" else B.view(H.TORCH[dt])
+    ref, bound = oracle.gemm(Ao, Bo, C, M, N, K, transA=c["transA"], transB=c["transB"], alpha=c["alpha"],
+                             beta=c["beta"], in_dtype=H.CODE[dt], c_dtype=H.CODE[c["out"]], lda=lda, ldb=ldb,
+                             threads=H.ORACLE_THREADS, sfa=SFA.numpy(), sfb=SFB.numpy())
+    got = D.cpu().double().numpy()
+    if c["exact"]:
+        H.assert_exact(got, ref, "mx fuzz %s" % c)
+    else:
+        H.assert_close(got, ref, bound, c["out"], "mx fuzz %s" % c)
