@@ -88,7 +88,8 @@ struct Cfg {
     static constexpr int kTileM = kPair ? 2 * kBM : kBM;   // D rows per tile
     static constexpr int kLoadN = kPair ? kTileN / 2 : kTileN;   // B rows (N) each CTA stages
     static constexpr int kEpiWarps = kEpiW;
-    static constexpr int kNumThreads = 64 + 32 * kEpiW;    // producer, MMA, epilogue warps
+    // producer, MMA, epilogue warps (+ kMX: the warp that copies the scales)
+    static constexpr int kNumThreads = 64 + 32 * kEpiW + (kMX ? 32 : 0);
     static constexpr int kEpiCols = kTileN / (kEpiW / 4);  // accumulator columns per epilogue warp
     static_assert(kMX || kLoadN % 64 == 0, "MN-major operand boxes are 64 wide");
     static_assert(kTileN <= kBNMax && kTileN % 64 == 0, "tile width");
@@ -118,8 +119,9 @@ struct Cfg {
     static constexpr int kOffSf = kOffB + kStages * kBBytes;
     static constexpr int kOffEpi = kOffSf + (kStages * kSfBytes + 1023) / 1024 * 1024;
     static constexpr int kOffBar = kOffEpi + kEpiBytes;
-    // full[S], empty[S], tmem_full[2], tmem_empty[2], c_ready[epilogue warps][kEpiBufs]
-    static constexpr int kNumBars = 2 * kStages + 4 + kEpiBufs * kEpiW;
+    // full[S], empty[S], tmem_full[2], tmem_empty[2], c_ready[epilogue warps][kEpiBufs],
+    // kMX: scales_ready[S]
+    static constexpr int kNumBars = 2 * kStages + 4 + kEpiBufs * kEpiW + (kMX ? kStages : 0);
     static constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
     static constexpr int kOffAbort = kOffTmemSlot + 4;
     static constexpr int kOffSkFlag = kOffAbort + 4;    // "this CTA finishes the stream-K tile"
@@ -304,6 +306,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
     auto tfull_bar = [&](int a) { return bars + 8u * (2 * Cf::kStages + a); };
     auto tempty_bar = [&](int a) { return bars + 8u * (2 * Cf::kStages + 2 + a); };
     auto c_bar = [&](int w, int b) { return bars + 8u * (2 * Cf::kStages + 4 + Cf::kEpiBufs * w + b); };
+    auto sf_bar = [&](int s) { return bars + 8u * (2 * Cf::kStages + 4 + Cf::kEpiBufs * kEpiWarps + s); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cf::kOffAbort);
     volatile int* sk_flag = reinterpret_cast<volatile int*>(smem + Cf::kOffSkFlag);
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(smem + Cf::kOffTmemSlot);
@@ -319,6 +322,8 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
         }
         for (int w = 0; w < kEpiWarps; ++w)
             for (int b = 0; b < Cf::kEpiBufs; ++b) ptx::mbar_init(c_bar(w, b), 1);
+        if constexpr (kMX)
+            for (int s = 0; s < Cf::kStages; ++s) ptx::mbar_init(sf_bar(s), 1);
         *abort_flag = 0;
         ptx::fence_mbarrier_init();
         ptx::prefetch_tensormap(&tmA);
@@ -467,27 +472,17 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                     const uint64_t ad = a_desc0 + (uint64_t)(stage * (Cf::kABytes >> 4));
                     const uint64_t bd = b_desc0 + (uint64_t)(stage * (Cf::kBBytes >> 4));
                     if constexpr (kMX) {
-                        // The stage's scales into its own TMEM slot behind the
-                        // accumulators (16 columns per sub-block), then its
-                        // MMAs, slice kk of a sub-block taking byte kk of every
-                        // row's and column's scale word.  A copy and the later
-                        // MMAs of this thread run in issue order.  The slot's
-                        // previous readers, the MMAs of this stage's last
-                        // round, have completed: the producer refilled the
-                        // stage only after their commit released it, and the
-                        // full barrier waited on above follows that refill.
-                        const uint32_t slot0 = tmem_base + (uint32_t)(2 * kBN + stage * Cf::kSfStageCols);
-                        const uint32_t ssrc0 = base + Cf::kOffSf + stage * Cf::kSfBytes;
-#pragma unroll
-                        for (int sub = 0; sub < Cf::kSub; ++sub) {
-                            const uint32_t slot = slot0 + sub * kSfSlotCols;
-                            const uint32_t ssrc = ssrc0 + sub * Cf::kSfSubBytes;
-                            ptx::tmem_cp_32x128b_warpx4<kCG>(slot, sf_desc(ssrc));
-#pragma unroll
-                            for (int c = 0; c < Cf::kSfbChunks; ++c)
-                                ptx::tmem_cp_32x128b_warpx4<kCG>(slot + 4 + 4 * c,
-                                                                 sf_desc(ssrc + (1 + c) * kSfChunkBytes));
+                        // The scale warp has copied the stage's scales into the
+                        // stage's TMEM slot behind the accumulators (16 columns
+                        // per sub-block) and committed that to scales_ready;
+                        // slice kk of a sub-block takes byte kk of every row's
+                        // and column's scale word.
+                        if (!wait_bounded(sf_bar(stage), phase, abort_flag, p, kSiteMmaFull, t)) {
+                            ok = false;
+                            break;
                         }
+                        ptx::tc_fence_after_sync();
+                        const uint32_t slot0 = tmem_base + (uint32_t)(2 * kBN + stage * Cf::kSfStageCols);
 #pragma unroll
                         for (int sub = 0; sub < Cf::kSub; ++sub) {
                             const uint64_t as = ad + (uint64_t)(sub * (Cf::kASubBytes >> 4));
@@ -531,6 +526,56 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                     ptx::mma_commit_pair(tfull_bar(acc), 0x3);
                 else
                     ptx::mma_commit(tfull_bar(acc));
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2 + kEpiWarps) {
+        // ---------------- kMX: scale copies (the pair's leader CTA only) ----------------
+        // For each stage the MMA issuer will use, in the same order: wait for
+        // its data, copy its scales from shared memory into the stage's TMEM
+        // slot (tcgen05.cp, in both CTAs of a pair), commit to scales_ready.
+        // Taking the copies off the MMA issuer shortens its per-stage work.
+        // The slot's previous readers, the MMAs of this stage's last round,
+        // have completed: the producer refilled the stage only after their
+        // commit released it, and the full barrier waited on here follows
+        // that refill.
+        if constexpr (kMX) {
+            if (leader && lane == 0) {
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                UnitIter units;
+                units.start(sched, cluster_id);
+                WorkUnit u;
+                while (ok && units.next(sched, cluster_id, &u)) {
+                    for (int kb = u.kb; kb < u.ke; ++kb) {
+                        if (!wait_bounded(full_bar(stage), phase, abort_flag, p, kSiteMmaFull, u.tile)) {
+                            ok = false;
+                            break;
+                        }
+                        ptx::tc_fence_after_sync();
+                        const uint32_t slot0 = tmem_base + (uint32_t)(2 * kBN + stage * Cf::kSfStageCols);
+                        const uint32_t ssrc0 = base + Cf::kOffSf + stage * Cf::kSfBytes;
+#pragma unroll
+                        for (int sub = 0; sub < Cf::kSub; ++sub) {
+                            const uint32_t slot = slot0 + sub * kSfSlotCols;
+                            const uint32_t ssrc = ssrc0 + sub * Cf::kSfSubBytes;
+                            ptx::tmem_cp_32x128b_warpx4<kCG>(slot, sf_desc(ssrc));
+#pragma unroll
+                            for (int c = 0; c < Cf::kSfbChunks; ++c)
+                                ptx::tmem_cp_32x128b_warpx4<kCG>(slot + 4 + 4 * c,
+                                                                 sf_desc(ssrc + (1 + c) * kSfChunkBytes));
+                        }
+                        if constexpr (kPair)
+                            ptx::mma_commit_pair(sf_bar(stage), 0x1);
+                        else
+                            ptx::mma_commit(sf_bar(stage));
+                        if (++stage == Cf::kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                }
             }
         }
         __syncwarp();
