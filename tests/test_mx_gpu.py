@@ -451,3 +451,27 @@ def test_mx_fuzz(seed):
         H.assert_exact(got, ref, "mx fuzz %s" % c)
     else:
         H.assert_close(got, ref, bound, c["out"], "mx fuzz %s" % c)
+
+
+@pytest.mark.parametrize("dtype", ["e4m3", "e2m1"])
+def test_bounded_wait_reports_and_recovers(variant, dtype):
+    """Failure detection without a fault: the test hook leaves the first
+    stage of the first tile unfilled, so the MMA issuer's and the scale
+    warp's waits on it run out (bounded), the kernel unwinds and records
+    GEMM_ERR_DEVICE_TIMEOUT; the next call on the same context is correct."""
+    M, N, K = 384, 448, 512
+    if dtype == "e2m1":
+        A, B = fp4_matrix(M, K, 171), fp4_matrix(N, K, 172)
+    else:
+        A, B = H.int_matrix((M, K), -8, 8, dtype, 171), H.int_matrix((N, K), -8, 8, dtype, 172)
+    SFA, SFB = scales(M, K, 126, 128, 173), scales(N, K, 126, 128, 174)
+    with H.env(GEMM_TEST_SKIP_FIRST_STAGE="1", GEMM_WAIT_TIMEOUT_NS="300000000"):
+        _, rc = run_mx(A, B, None, SFA, SFB, M, N, K, in_dtype=dtype)
+    assert rc == 0
+    status, info = H.poll()
+    assert status == binding.GEMM_ERR_DEVICE_TIMEOUT, (status, info)
+    assert H.poll()[0] == 0
+    D, rc = run_mx(A, B, None, SFA, SFB, M, N, K, in_dtype=dtype)
+    assert rc == 0 and H.poll()[0] == 0
+    ref, _ = oracle_mx(A, B, None, SFA, SFB, M, N, K, in_dtype=dtype)
+    H.assert_exact(D.numpy(), ref, "after recovery (%s)" % dtype)
