@@ -386,15 +386,15 @@ int epi_warps_for(int64_t K, int pair, int out_dtype, int tile_n, int f8) {
     return (K + stage_k - 1) / stage_k <= 4 ? 8 : 4;
 }
 
-// mx: the block-scaled kernel, whose tiles are 192 wide (256 x 192 on a CTA
-// pair, 128 x 192 on one SM; no narrow tiles), with 4 epilogue warps;
-// stream-K applies to it as to the others.
+// mx: the block-scaled kernel, whose tiles are 224 wide for f32 D and 192
+// for 16-bit D (on a CTA pair or one SM; no narrow tiles), with 4 epilogue
+// warps; stream-K applies to it as to the others.
 Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk, int out_dtype, int f8, int mx = 0) {
     Plan pl{};
     const int ov = (mx && variant_override() == kNarrow) ? kAuto : variant_override();
     pl.pair = ov == kPairV || (ov == kAuto && M > gb300::tcgen05_tile_m(0)) ? 1 : 0;
     pl.tile_m = gb300::tcgen05_tile_m(pl.pair);
-    pl.tile_n = mx ? gb300::tcgen05_mx_tile_n() : gb300::tcgen05_wide_n();
+    pl.tile_n = mx ? gb300::tcgen05_mx_tile_n(out_dtype == GEMM_F32) : gb300::tcgen05_wide_n();
     // Narrow 128 x 64 tiles when the wide ones would keep at most a quarter
     // of the SMs busy (the time then goes into latency and into each CTA's
     // epilogue, which a narrow tile cuts by four), or when N fits one.
@@ -442,8 +442,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
     }
     if (mx) {
         pl.epi_warps = 4;
-        pl.smem = gb300::tcgen05_mx_smem_bytes(pl.pair);
-        pl.stages = gb300::tcgen05_mx_stages(pl.pair);
+        pl.smem = gb300::tcgen05_mx_smem_bytes(pl.pair, out_dtype == GEMM_F32);
+        pl.stages = gb300::tcgen05_mx_stages(pl.pair, out_dtype == GEMM_F32);
         return pl;
     }
     pl.epi_warps = epi_warps_for(K, pl.pair, out_dtype, pl.tile_n, f8);

@@ -93,9 +93,9 @@ cudaError_t launch_tcgen05_mx(const TcgenLaunch& L, cudaStream_t stream);  // ge
 cudaError_t launch_sf_tiles(uint8_t* out, const uint8_t* in, int64_t ld, int64_t rows, int64_t kblocks,
                             int tile_rows, int64_t tiles, int64_t kchunks, cudaStream_t stream);
 int64_t sf_tiles_bytes(int tile_rows, int64_t tiles, int64_t kchunks);
-int tcgen05_mx_tile_n();           // D columns per block-scaled tile
-int tcgen05_mx_smem_bytes(int pair);
-int tcgen05_mx_stages(int pair);
+int tcgen05_mx_tile_n(int f32_out);   // D columns per block-scaled tile
+int tcgen05_mx_smem_bytes(int pair, int f32_out);
+int tcgen05_mx_stages(int pair, int f32_out);
 cudaError_t launch_k0(int out, void* D, const void* C, int M, int N, int64_t ldc, int64_t ldd, float alpha,
                       float beta, int has_c, int num_sms, cudaStream_t stream);
 

@@ -21,11 +21,14 @@ cudaError_t launch_tcgen05_mx(const TcgenLaunch& L, cudaStream_t stream) {
     return L.p.has_c ? launch_mx_group<false, true>(L, stream) : launch_mx_group<false, false>(L, stream);
 }
 
-int tcgen05_mx_tile_n() { return kMxTileN; }
-int tcgen05_mx_smem_bytes(int pair) {
+int tcgen05_mx_tile_n(int f32_out) { return f32_out ? kMxTileNF32 : kMxTileN; }
+int tcgen05_mx_smem_bytes(int pair, int f32_out) {
+    if (f32_out)
+        return pair ? Cfg<true, 4, kMxTileNF32, true>::kSmemBytes : Cfg<false, 4, kMxTileNF32, true>::kSmemBytes;
     return pair ? Cfg<true, 4, kMxTileN, true>::kSmemBytes : Cfg<false, 4, kMxTileN, true>::kSmemBytes;
 }
-int tcgen05_mx_stages(int pair) {
+int tcgen05_mx_stages(int pair, int f32_out) {
+    if (f32_out) return pair ? Cfg<true, 4, kMxTileNF32, true>::kStages : Cfg<false, 4, kMxTileNF32, true>::kStages;
     return pair ? Cfg<true, 4, kMxTileN, true>::kStages : Cfg<false, 4, kMxTileN, true>::kStages;
 }
 

@@ -59,11 +59,12 @@ constexpr int kSmemBudget = 232448;  // dynamic shared memory per CTA on sm_103
 static_assert(kBK / kUK == 4, "the MMA loop issues four K slices per stage");
 // MX block-scaled 8-bit operands: one UE8M0 scale per 32 K elements of each
 // row of A and column of B.  A 128-K sub-block spans four scale blocks, so
-// each row's scales of a sub-block are one 32-bit word.  Tiles are 192
-// columns wide (128 x 192 on one SM, 256 x 192 on a CTA pair): two
-// accumulators take 384 TMEM columns, the stages' scale slots the rest.
+// each row's scales of a sub-block are one 32-bit word.  Tiles are 224
+// columns wide for f32 D and 192 for 16-bit D (on one SM or a CTA pair):
+// two accumulators take 448 or 384 TMEM columns, scale slots the rest.
 constexpr int kMxBlock = 32;         // K elements per scale
-constexpr int kMxTileN = 192;        // accumulator columns of the block-scaled tiles
+constexpr int kMxTileN = 192;        // accumulator columns of the block-scaled tiles (16-bit D)
+constexpr int kMxTileNF32 = 224;     // the same for f32 D, whose 32-column epilogue chunks allow it
 constexpr int kSfChunkBytes = 512;   // scales of 128 rows x 4 blocks, in tcgen05.cp order
 constexpr int kSfSlotCols = 16;      // TMEM columns per sub-block's scales: SFA 4, SFB 4 per 128 columns of N
 static_assert(kBK8 == 4 * kMxBlock, "one scale word per row and stage");
@@ -92,7 +93,7 @@ struct Cfg {
     static constexpr int kNumThreads = 64 + 32 * kEpiW + (kMX ? 32 : 0);
     static constexpr int kEpiCols = kTileN / (kEpiW / 4);  // accumulator columns per epilogue warp
     static_assert(kMX || kLoadN % 64 == 0, "MN-major operand boxes are 64 wide");
-    static_assert(kTileN <= kBNMax && kTileN % 64 == 0, "tile width");
+    static_assert(kTileN <= kBNMax && kTileN % (kMX ? 32 : 64) == 0, "tile width");
     // A pipeline stage holds kSub 64-wide K sub-blocks.  The MMA issuer pays a
     // fixed cost per stage (barrier wait, release commit) while the tensor
     // core queues only a few MMAs, so the pair kernel puts 8 MMAs (2 sub-
@@ -129,7 +130,13 @@ struct Cfg {
     static_assert(kStages >= 2, "at least two operand stages");
     static_assert(kSmemBytes <= kSmemBudget, "shared memory budget");
     // One TMEM scale slot per operand stage (see the MMA issuer).
-    static_assert(!kMX || (2 * kTileN + kStages * kSfStageCols <= kTmemCols && 4 + 4 * kSfbChunks <= kSfSlotCols),
+    // TMEM scale slots (one stage's scales each) beside the two accumulators:
+    // one per stage when they fit, else a ring the scale warp reuses once the
+    // MMAs that read a slot have committed.
+    static constexpr int kSfSlotsFit = kMX ? (kTmemCols - 2 * kTileN) / kSfStageCols : 1;
+    static constexpr int kSfSlots = kSfSlotsFit < kStages ? kSfSlotsFit : kStages;
+    static_assert(!kMX || (kSfSlots >= 2 && 2 * kTileN + kSfSlots * kSfStageCols <= kTmemCols &&
+                           4 + 4 * kSfbChunks <= kSfSlotCols),
                   "block-scaled tiles: accumulators and scale slots within the TMEM allocation");
 };
 
@@ -451,6 +458,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
             const uint64_t b_kstep = (uint64_t)((p.b_mn_major ? kUK * 128 : kUK * 2) >> 4);
             int stage = 0;
             uint32_t phase = 0;
+            uint32_t gstage = 0;   // stages consumed so far (kMX: picks the scale slot)
             int it = 0;
             bool ok = true;
             UnitIter units;
@@ -482,7 +490,8 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                             break;
                         }
                         ptx::tc_fence_after_sync();
-                        const uint32_t slot0 = tmem_base + (uint32_t)(2 * kBN + stage * Cf::kSfStageCols);
+                        const uint32_t slot0 =
+                            tmem_base + (uint32_t)(2 * kBN + (int)(gstage % Cf::kSfSlots) * Cf::kSfStageCols);
 #pragma unroll
                         for (int sub = 0; sub < Cf::kSub; ++sub) {
                             const uint64_t as = ad + (uint64_t)(sub * (Cf::kASubBytes >> 4));
@@ -516,6 +525,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                         ptx::mma_commit_pair(empty_bar(stage), 0x3);
                     else
                         ptx::mma_commit(empty_bar(stage));
+                    ++gstage;
                     if (++stage == Cf::kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -532,17 +542,21 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
     } else if (warp == 2 + kEpiWarps) {
         // ---------------- kMX: scale copies (the pair's leader CTA only) ----------------
         // For each stage the MMA issuer will use, in the same order: wait for
-        // its data, copy its scales from shared memory into the stage's TMEM
-        // slot (tcgen05.cp, in both CTAs of a pair), commit to scales_ready.
-        // Taking the copies off the MMA issuer shortens its per-stage work.
-        // The slot's previous readers, the MMAs of this stage's last round,
-        // have completed: the producer refilled the stage only after their
-        // commit released it, and the full barrier waited on here follows
-        // that refill.
+        // its data, copy its scales from shared memory into a TMEM scale slot
+        // (slot g mod kSfSlots for the g-th stage; tcgen05.cp, in both CTAs of
+        // a pair), commit to scales_ready.  Taking the copies off the MMA
+        // issuer shortens its per-stage work.  The slot's previous readers,
+        // the MMAs of stage g - kSfSlots, have completed: with one slot per
+        // stage, because the producer refilled this stage only after their
+        // commit released it and the full barrier waited on here follows that
+        // refill; with fewer slots than stages, by waiting for that commit on
+        // its stage's empty barrier (whose next phase cannot complete before
+        // this warp has copied stage g + 1, so the parity test is unambiguous).
         if constexpr (kMX) {
             if (leader && lane == 0) {
                 int stage = 0;
                 uint32_t phase = 0;
+                uint32_t gstage = 0;
                 bool ok = true;
                 UnitIter units;
                 units.start(sched, cluster_id);
@@ -553,8 +567,19 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                             ok = false;
                             break;
                         }
+                        if constexpr (Cf::kSfSlots < Cf::kStages) {
+                            if (gstage >= (uint32_t)Cf::kSfSlots) {
+                                const uint32_t prev = gstage - Cf::kSfSlots;
+                                if (!wait_bounded(empty_bar((int)(prev % Cf::kStages)), (prev / Cf::kStages) & 1u,
+                                                  abort_flag, p, kSiteMmaFull, u.tile)) {
+                                    ok = false;
+                                    break;
+                                }
+                            }
+                        }
                         ptx::tc_fence_after_sync();
-                        const uint32_t slot0 = tmem_base + (uint32_t)(2 * kBN + stage * Cf::kSfStageCols);
+                        const uint32_t slot0 =
+                            tmem_base + (uint32_t)(2 * kBN + (int)(gstage % Cf::kSfSlots) * Cf::kSfStageCols);
                         const uint32_t ssrc0 = base + Cf::kOffSf + stage * Cf::kSfBytes;
 #pragma unroll
                         for (int sub = 0; sub < Cf::kSub; ++sub) {
@@ -570,6 +595,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                             ptx::mma_commit_pair(sf_bar(stage), 0x1);
                         else
                             ptx::mma_commit(sf_bar(stage));
+                        ++gstage;
                         if (++stage == Cf::kStages) {
                             stage = 0;
                             phase ^= 1u;
@@ -959,19 +985,19 @@ static cudaError_t launch_family(const TcgenLaunch& L, cudaStream_t stream) {
     return has_c ? launch_group<false, true, kF8>(L, stream) : launch_group<false, false, kF8>(L, stream);
 }
 
-// The block-scaled kernels: 192-wide tiles on one SM or a CTA pair, 4
-// epilogue warps, every output type, with and without C.
+// The block-scaled kernels: 224-wide (f32 D) or 192-wide (16-bit D) tiles on
+// one SM or a CTA pair, 4 epilogue warps, with and without C.
 template <bool kPair, bool kHasC>
 static cudaError_t prepare_mx_group() {
     cudaError_t e;
-    if ((e = prepare_one<kPair, kOutF32, 4, kHasC, kMxTileN, true, true>()) != cudaSuccess) return e;
+    if ((e = prepare_one<kPair, kOutF32, 4, kHasC, kMxTileNF32, true, true>()) != cudaSuccess) return e;
     if ((e = prepare_one<kPair, kOutF16, 4, kHasC, kMxTileN, true, true>()) != cudaSuccess) return e;
     return prepare_one<kPair, kOutBF16, 4, kHasC, kMxTileN, true, true>();
 }
 
 template <bool kPair, bool kHasC>
 static cudaError_t launch_mx_group(const TcgenLaunch& L, cudaStream_t stream) {
-    if (L.out == kOutF32) return launch_one<kPair, kOutF32, 4, kHasC, kMxTileN, true, true>(L, stream);
+    if (L.out == kOutF32) return launch_one<kPair, kOutF32, 4, kHasC, kMxTileNF32, true, true>(L, stream);
     if (L.out == kOutF16) return launch_one<kPair, kOutF16, 4, kHasC, kMxTileN, true, true>(L, stream);
     return launch_one<kPair, kOutBF16, 4, kHasC, kMxTileN, true, true>(L, stream);
 }
