@@ -946,6 +946,7 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
         return reject(GEMM_ERR_INVALID_ARG, "4-bit operands: K, lda and ldb must be even");
     const int64_t epu = fp4 ? 2 : 1;   // elements per byte of A and B
     const int vdt = fp4 ? GEMM_E4M3 : in_dtype;
+    const int64_t lda_in = lda, ldb_in = ldb;   // the caller's strides (lda / ldb may be redirected below)
     int rc = validate(D, A, B, C, M, N, K / epu, lda / epu, ldb / epu, ldc, ldd, transA, transB, beta, vdt, out_dtype);
     if (rc != GEMM_OK || M == 0 || N == 0) return rc;
     if ((rc = validate_scales(D, SFA, SFB, M, N, K, ld_sfa, ld_sfb, ldd, out_dtype)) != GEMM_OK) return rc;
@@ -982,29 +983,9 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
         return reject(GEMM_ERR_UNSUPPORTED_LAYOUT, "8-bit operands: no workspace for repacking");
     }
 
-    int64_t k_map = K;   // the K extent of the operand tensor maps
-    if (!fp4_ops_ok) {
-        const int64_t kp = (K + 127) / 128 * 128;
-        const int64_t a_bytes = (M * (kp / 2) + 255) / 256 * 256;
-        const int64_t b_bytes = (N * (kp / 2) + 255) / 256 * 256;
-        void* fws = nullptr;
-        uint32_t fepoch = 0;
-        if (workspace_for(kWsFp4, dev, s, a_bytes + b_bytes, &fws, &fepoch, !in_capture) != GEMM_OK)
-            return reject(GEMM_ERR_CUDA, "4-bit operand workspace");
-        uint8_t* a2 = static_cast<uint8_t*>(fws);
-        uint8_t* b2 = a2 + a_bytes;
-        GEMM_LOGF("mx: 4-bit operands copied into 32-byte-aligned rows of %lld elements", (long long)kp);
-        if (cudaMemsetAsync(fws, 0, (size_t)(a_bytes + b_bytes), s) != cudaSuccess ||
-            gb300::launch_copy2d(a2, kp / 2, A, lda / 2, M, K / 2, 1, s) != cudaSuccess ||
-            gb300::launch_copy2d(b2, kp / 2, B, ldb / 2, N, K / 2, 1, s) != cudaSuccess) {
-            cudaGetLastError();
-            return reject(GEMM_ERR_LAUNCH, "4-bit operand copies");
-        }
-        A = a2;
-        B = b2;
-        lda = ldb = k_map = kp;
-    }
-
+    // Every workspace is acquired before anything is enqueued, so a refusal
+    // (for instance inside a stream capture, which cannot allocate) leaves
+    // the stream as it was.
     Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, 1, 1);
     // The scales, rearranged into 512-byte chunks (gemm_sm103_mx.cu): one per
     // 128-K sub-block and 128-row group of A (each CTA of a pair has its
@@ -1029,11 +1010,33 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
         if (!in_capture) return reject(GEMM_ERR_CUDA, "stream-K workspace");
         pl = make_plan(M, N, K, ds->num_sms, false, out_dtype, 1, 1);   // whole tiles: no workspace
     }
+    // 4-bit operands off TMA's 4-bit grid: copied into zero-padded rows of K
+    // rounded up to 128 elements.
+    int64_t k_map = K;   // the K extent of the operand tensor maps
+    uint8_t* a2 = nullptr;
+    uint8_t* b2 = nullptr;
+    const int64_t kp = (K + 127) / 128 * 128;
+    const int64_t a2_bytes = (M * (kp / 2) + 255) / 256 * 256;
+    const int64_t b2_bytes = (N * (kp / 2) + 255) / 256 * 256;
+    if (!fp4_ops_ok) {
+        void* fws = nullptr;
+        uint32_t fepoch = 0;
+        if (workspace_for(kWsFp4, dev, s, a2_bytes + b2_bytes, &fws, &fepoch, !in_capture) != GEMM_OK)
+            return reject(GEMM_ERR_CUDA, "4-bit operand workspace");
+        a2 = static_cast<uint8_t*>(fws);
+        b2 = a2 + a2_bytes;
+    }
+    const void* A_op = a2 ? a2 : A;
+    const void* B_op = b2 ? b2 : B;
+    if (a2) {
+        lda = ldb = k_map = kp;
+    }
+
     TcgenLaunch L;
     // (packed 4-bit operands: maps of k_map elements per row; 128 of them
     // fill a 128-byte shared-memory row, as 8-bit ones do)
-    if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, k_map, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
-                               in_dtype, out_dtype)) != GEMM_OK)
+    if ((rc = describe_tcgen05(&L, pl, D, A_op, B_op, C, M, N, k_map, lda, ldb, ldc, ldd, transA, transB, alpha,
+                               beta, in_dtype, out_dtype)) != GEMM_OK)
         return reject(rc, "tensor maps");
     GemmParams& p = L.p;
     p.K = (int32_t)K;
@@ -1061,8 +1064,18 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
         p.ws_counters = static_cast<uint32_t*>(ws);
         p.ws_partials = static_cast<char*>(ws) + ((int64_t)pl.sk_tiles * 2 * 4 + 255) / 256 * 256;
     }
-    cudaError_t e = gb300::launch_sf_tiles(sfa_tiles, static_cast<const uint8_t*>(SFA), ld_sfa, M, kblocks, 128,
-                                           a_groups, kchunks, s);
+    // ---- enqueue: the 4-bit operand copies, the scale rearranging, the product ----
+    cudaError_t e = cudaSuccess;
+    if (a2) {
+        GEMM_LOGF("mx: 4-bit operands copied into 32-byte-aligned rows of %lld elements", (long long)kp);
+        if (cudaMemsetAsync(a2, 0, (size_t)(a2_bytes + b2_bytes), s) != cudaSuccess)
+            e = cudaErrorUnknown;
+        if (e == cudaSuccess) e = gb300::launch_copy2d(a2, kp / 2, A, lda_in / 2, M, K / 2, 1, s);
+        if (e == cudaSuccess) e = gb300::launch_copy2d(b2, kp / 2, B, ldb_in / 2, N, K / 2, 1, s);
+    }
+    if (e == cudaSuccess)
+        e = gb300::launch_sf_tiles(sfa_tiles, static_cast<const uint8_t*>(SFA), ld_sfa, M, kblocks, 128, a_groups,
+                                   kchunks, s);
     if (e == cudaSuccess)
         e = gb300::launch_sf_tiles(sfb_tiles, static_cast<const uint8_t*>(SFB), ld_sfb, N, kblocks, pl.tile_n,
                                    pl.num_n, kchunks, s);
