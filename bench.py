@@ -10,6 +10,12 @@ region is exactly K steps between CUDA events on the launching stream,
 bracketed by a barrier and a device synchronisation; with N > 1 (torchrun)
 every rank runs its own replica and the slowest rank's time is used.
 
+The roofline's tensor peak is the measured cuBLAS bf16 figure (x 2 for
+8-bit operands) in the power state the timed loop ran in: the sustained
+figure for a loop long enough to meet the power cap (the default 1000
+launches of the 8192^3 workload), the burst figure for a short loop and for
+the separate burst measurement (best of three 10-launch runs).
+
 --impl reference times the CPU oracle instead (the only other
 implementation of this operation in the repository), on bounded samples
 of the same workload, on the host cores.
@@ -472,28 +478,39 @@ def run_ours(args, case):
     # Packed 4-bit operands run on the same kind::mxf8f6f4 instruction as the
     # 8-bit ones (K = 32 per instruction), so their peak is the 8-bit one.
     rate = FP8_RATE if case.in_dtype in ("e4m3", "e5m2", "e2m1") else 1.0
-    peak = float(peaks["bf16_tflops"]) * rate
-    src = ("%s bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json); f16 runs at the bf16 rate" % peak_src
-           if rate == 1.0 else
-           "%s bf16 burst (cuBLAS 8192^3, MEASURED_PEAKS.json) x 2, the nominal dense fp8 / bf16 ratio" % peak_src)
+    peak_burst = float(peaks["bf16_tflops"]) * rate
+    peak_sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * rate
+    # The measured peaks come as a burst (a short cuBLAS run, clocks up) and a
+    # sustained figure (seconds of back-to-back cuBLAS under the power cap).
+    # The timed loop is held to the same condition as its denominator: a loop
+    # that ran long enough to meet the power cap (>= 0.5 s, or sw_power_cap
+    # seen while it ran) is compared with the sustained peak; a short loop, and
+    # the burst figure, with the burst peak.
+    power_capped = elapsed_ms >= 500.0 or bool(clocks and "sw_power_cap" in clocks.get("reasons", []))
+    peak = peak_sustained if power_capped else peak_burst
+    kind = "sustained" if power_capped else "burst"
+    src = ("%s bf16 %s (cuBLAS 8192^3, MEASURED_PEAKS.json)%s; this loop: %d launches in %.0f ms%s" % (
+        peak_src, kind, "; f16 runs at the bf16 rate" if rate == 1.0 else
+        " x 2, the nominal dense fp8 / bf16 ratio", args.steps, elapsed_ms,
+        ", sw_power_cap active" if clocks and "sw_power_cap" in clocks.get("reasons", []) else ""))
     achieved_gbs = case.algorithmic_bytes / (per_launch_ms * 1e-3) / 1e9
     hbm = float(peaks["hbm_gbs"])
     # the bound: below the ridge (peak flop/s / copy bandwidth) the algorithmic
     # bytes limit the launch, above it the tensor cores do
     intensity = case.flops / case.algorithmic_bytes
-    ridge = peak * 1e12 / (hbm * 1e9)
+    ridge = peak_burst * 1e12 / (hbm * 1e9)
     burst_tflops = case.flops / (burst_ms * 1e-3) / 1e12
     if intensity >= ridge:
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                    "frac": achieved / peak, "peak_source": src,
-                    "frac_of_sustained": achieved / (float(peaks.get("bf16_tflops_sustained", peak / rate)) * rate),
+                    "frac": achieved / peak, "peak_kind": kind, "peak_source": src,
+                    "frac_of_burst": achieved / peak_burst, "frac_of_sustained": achieved / peak_sustained,
                     "frac_of_nominal": achieved / (NOMINAL_DENSE_TFLOPS * rate)}
-        burst = {"achieved": burst_tflops, "frac": burst_tflops / peak}
+        burst = {"achieved": burst_tflops, "frac": burst_tflops / peak_burst, "peak": peak_burst}
     else:
         roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s",
                     "frac": achieved_gbs / hbm,
                     "peak_source": "%s copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" % peak_src,
-                    "achieved_tflops": achieved, "tensor_peak_tflops": peak}
+                    "achieved_tflops": achieved, "tensor_peak_tflops": peak_burst}
         burst_gbs = case.algorithmic_bytes / (burst_ms * 1e-3) / 1e9
         burst = {"achieved": burst_gbs, "frac": burst_gbs / hbm}
     roofline.update({"traffic": _profiled_traffic(case.name), "arithmetic_intensity": intensity,
