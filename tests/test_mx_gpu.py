@@ -475,3 +475,43 @@ def test_bounded_wait_reports_and_recovers(variant, dtype):
     assert rc == 0 and H.poll()[0] == 0
     ref, _ = oracle_mx(A, B, None, SFA, SFB, M, N, K, in_dtype=dtype)
     H.assert_exact(D.numpy(), ref, "after recovery (%s)" % dtype)
+
+
+def test_in_place_and_alpha_zero():
+    """D = C in place (beta = 1), and alpha = 0 (D = beta * C exactly)."""
+    dev = torch.device("cuda", 0)
+    M, N, K = 300, 280, 192
+    A = H.int_matrix((M, K), -8, 8, "e4m3", 181).to(dev)
+    B = H.int_matrix((N, K), -8, 8, "e4m3", 182).to(dev)
+    SFA, SFB = scales(M, K, 126, 128, 183), scales(N, K, 126, 128, 184)
+    sa, sb = SFA.to(dev), SFB.to(dev)
+    C = H.int_matrix((M, N), -50, 50, "f32", 185)
+    D = C.to(dev).clone()
+    rc = binding.gemm_mx(D, A, B, D, sa, sb, M, N, K, K, K, N, N, sa.stride(0), sb.stride(0), 0, 1, 1.0, 1.0,
+                         H.CODE["e4m3"], H.CODE["f32"], None)
+    torch.cuda.synchronize()
+    assert rc == 0
+    ref, _ = oracle_mx(A.cpu(), B.cpu(), C, SFA, SFB, M, N, K, beta=1.0)
+    H.assert_exact(D.cpu().numpy(), ref, "in place")
+    D2 = torch.full((M, N), float("nan"), device=dev)
+    rc = binding.gemm_mx(D2, A, B, C.to(dev), sa, sb, M, N, K, K, K, N, N, sa.stride(0), sb.stride(0), 0, 1, 0.0,
+                         -2.0, H.CODE["e4m3"], H.CODE["f32"], None)
+    torch.cuda.synchronize()
+    assert rc == 0
+    H.assert_exact(D2.cpu().numpy(), -2.0 * C.double().numpy(), "alpha = 0")
+
+
+@pytest.mark.parametrize("e", [0, 1, 253])
+def test_extreme_scale_exponents(e):
+    """Every scale 2^(e - 127) with tiny operands: the smallest scales (2^-127,
+    2^-126: the products lie far below the fp32 normal range) and a large one
+    (2^126 x 2^-126 on B keeps the products representable)."""
+    M, N, K = 128, 192, 128
+    A = H.int_matrix((M, K), -2, 2, "e4m3", 191)
+    B = H.int_matrix((N, K), -2, 2, "e4m3", 192)
+    SFA = torch.full((M, K // 32), e, dtype=torch.uint8)
+    SFB = torch.full((N, K // 32), 254 - e if e == 253 else 127, dtype=torch.uint8)
+    D, rc = run_mx(A, B, None, SFA, SFB, M, N, K)
+    assert rc == 0
+    ref, bound = oracle_mx(A, B, None, SFA, SFB, M, N, K)
+    H.assert_close(D.double().numpy(), ref, bound, "f32", "scale exponent %d" % e)
