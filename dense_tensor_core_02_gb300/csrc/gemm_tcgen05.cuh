@@ -780,9 +780,26 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                 if (lane == 0) ptx::bulk_wait_group_read<Cf::kEpiBufs - 1>();
                 __syncwarp();
                 if constexpr (kHasC) {   // this chunk of C, by TMA, into the staging box
-                    if (lane == 0 && !(prefetch_c && c < kPrefetchC)) {
+                    // C runs kAhead chunks ahead of its use: chunk c's C was
+                    // prefetched with the tile or issued by chunk c - kAhead;
+                    // only the first chunks of a tile without the prefetch
+                    // load their own.  Then this chunk issues the C of chunk
+                    // c + kAhead into the buffer of chunk c - 1, once that
+                    // chunk's D store has read it, so the load's latency hides
+                    // behind this chunk's work.
+                    constexpr int kAhead = Cf::kEpiBufs - 1;
+                    if (lane == 0 && !((prefetch_c && c < kPrefetchC) || c >= kAhead)) {
                         ptx::mbar_arrive_expect_tx(c_bar(ew, buf), kEpiBufBytes);
                         ptx::tma_load_2d(sbuf, &tmC, col0, row0, c_bar(ew, buf));
+                    }
+                    const int cn = c + kAhead;
+                    if (kAhead > 0 && cn < kChunks && !(prefetch_c && cn < kPrefetchC) &&
+                        col0 + kAhead * kChunkCols < p.N && lane == 0) {
+                        ptx::bulk_wait_group_read<0>();
+                        const uint32_t bn = (chunk_iter + kAhead) % Cf::kEpiBufs;
+                        ptx::mbar_arrive_expect_tx(c_bar(ew, bn), kEpiBufBytes);
+                        ptx::tma_load_2d(epi + bn * kEpiBufBytes, &tmC, col0 + kAhead * kChunkCols, row0,
+                                         c_bar(ew, bn));
                     }
                     ok = wait_bounded(c_bar(ew, buf), (chunk_iter / Cf::kEpiBufs) & 1u, abort_flag, p,
                                       kSiteEpilogueC, t);
