@@ -122,7 +122,8 @@ int group_m_setting() {
 //    (>= 24 stages, ~0.7 us each) each store chunk is followed by a pause of
 //    20 ns per stage (a quarter of the main loop spread over a warp's 8
 //    chunks), at most 2 us.  Measured (8192 x 8192, K = 4096 / 8192 / 16384):
-//    +2 % / +1 % / +0.7 %; shorter tiles are store-bound and get no pause.
+//    +2 % / +1 % / +0.7 %; block-scaled 8192^3 (224-wide tiles): +2.7 % E4M3,
+//    +2 % E2M1; shorter tiles are store-bound and get no pause.
 void tuning(GemmParams& p, int tile_n) {
     p.hint_a = p.num_n_tiles == 1 ? 1 : 2;
     p.hint_b = p.num_m_tiles == 1 ? 1 : 2;
@@ -136,7 +137,7 @@ void tuning(GemmParams& p, int tile_n) {
         p.hint_d = d;
     }
     p.epi_pace_ns = 0;
-    if (tile_n == 256 && p.num_k_blocks >= 24) p.epi_pace_ns = std::min(2000, p.num_k_blocks * 20);
+    if (tile_n >= 192 && p.num_k_blocks >= 24) p.epi_pace_ns = std::min(2000, p.num_k_blocks * 20);
     const char* pv = std::getenv("GEMM_EPI_PACE_NS");
     if (pv && *pv) {
         const int ns = std::atoi(pv);
