@@ -65,6 +65,7 @@ struct Pipe {
     cudaEvent_t b_loaded[kFirstBlocks] = {};    // column block j of B is on the device
     cudaEvent_t b_computed[kFirstBlocks] = {};  // column block j of the first panel's D is on the device
     cudaEvent_t entry = nullptr;             // this call's place in the caller's stream
+    cudaEvent_t copied_in = nullptr;         // the copy-in stream's work so far (failed calls)
     cudaEvent_t copied_out = nullptr;        // this call's D is on the host
     char* buf = nullptr;
     int64_t bytes = 0;
@@ -99,6 +100,7 @@ int pipe_for(int dev, cudaStream_t user, bool may_create, Pipe** out) {
     bool ok = cudaStreamCreateWithFlags(&p->in, cudaStreamNonBlocking) == cudaSuccess &&
               cudaStreamCreateWithFlags(&p->out, cudaStreamNonBlocking) == cudaSuccess &&
               cudaEventCreateWithFlags(&p->entry, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&p->copied_in, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&p->copied_out, cudaEventDisableTiming) == cudaSuccess;
     for (int i = 0; ok && i < kMaxPanels; ++i)
         ok = cudaEventCreateWithFlags(&p->loaded[i], cudaEventDisableTiming) == cudaSuccess &&
@@ -171,6 +173,19 @@ int validate_host(const void* D, const void* A, const void* B, const void* C, in
 int copy_error() {
     cudaGetLastError();
     return GEMM_ERR_CUDA;
+}
+
+// A call that fails part-way, after some copies were enqueued on the side
+// streams: the caller's stream is made to wait for them all the same, so
+// that they stay inside "the stream has completed this call" (the host
+// buffers must stay unchanged until then) and the next call's copies into
+// the staging buffers cannot overtake them.
+int fail_joined(Pipe* p, cudaStream_t user, int rc) {
+    cudaGetLastError();
+    if (cudaEventRecord(p->copied_in, p->in) == cudaSuccess) cudaStreamWaitEvent(user, p->copied_in, 0);
+    if (cudaEventRecord(p->copied_out, p->out) == cudaSuccess) cudaStreamWaitEvent(user, p->copied_out, 0);
+    cudaGetLastError();
+    return rc;
 }
 
 }  // namespace
@@ -259,28 +274,35 @@ extern "C" GEMM_API int gemm_host(void* D, const void* A, const void* B, const v
         return (int)GEMM_OK;
     };
 
-    // copy-in: B's first column block, the first panel's A and C, B's other blocks
-    if (K > 0 && copy_b(0, std::min(bcols, N)) != cudaSuccess) return copy_error();
-    if (!copy_panel_inputs(0)) return copy_error();
-    for (int j = 1; j < blocks; ++j) {
-        const int64_t n0 = j * bcols;
-        if (copy_b(n0, std::min(bcols, N - n0)) != cudaSuccess || cudaEventRecord(p->b_loaded[j], p->in) != cudaSuccess)
+    auto enqueue = [&]() -> int {
+        // copy-in: B's first column block, the first panel's A and C, B's other blocks
+        if (K > 0 && copy_b(0, std::min(bcols, N)) != cudaSuccess) return copy_error();
+        if (!copy_panel_inputs(0)) return copy_error();
+        for (int j = 1; j < blocks; ++j) {
+            const int64_t n0 = j * bcols;
+            if (copy_b(n0, std::min(bcols, N - n0)) != cudaSuccess ||
+                cudaEventRecord(p->b_loaded[j], p->in) != cudaSuccess)
+                return copy_error();
+        }
+        // the first panel, block by block
+        int r;
+        for (int j = 0; j < blocks; ++j) {
+            const int64_t n0 = j * bcols;
+            if ((r = compute_and_return(0, n0, std::min(bcols, N - n0), j == 0 ? p->loaded[0] : p->b_loaded[j],
+                                        p->b_computed[j])) != GEMM_OK)
+                return r;
+        }
+        // the other panels, whole
+        for (int q = 1; q < panels; ++q) {
+            if (!copy_panel_inputs(q)) return copy_error();
+            if ((r = compute_and_return(q, 0, N, p->loaded[q], p->computed[q])) != GEMM_OK) return r;
+        }
+        // D is on the host when the caller's stream reaches this point.
+        if (cudaEventRecord(p->copied_out, p->out) != cudaSuccess ||
+            cudaStreamWaitEvent(user, p->copied_out, 0) != cudaSuccess)
             return copy_error();
-    }
-    // the first panel, block by block
-    for (int j = 0; j < blocks; ++j) {
-        const int64_t n0 = j * bcols;
-        if ((rc = compute_and_return(0, n0, std::min(bcols, N - n0), j == 0 ? p->loaded[0] : p->b_loaded[j],
-                                     p->b_computed[j])) != GEMM_OK)
-            return rc;
-    }
-    // the other panels, whole
-    for (int q = 1; q < panels; ++q) {
-        if (!copy_panel_inputs(q)) return copy_error();
-        if ((rc = compute_and_return(q, 0, N, p->loaded[q], p->computed[q])) != GEMM_OK) return rc;
-    }
-    // D is on the host when the caller's stream reaches this point.
-    if (cudaEventRecord(p->copied_out, p->out) != cudaSuccess || cudaStreamWaitEvent(user, p->copied_out, 0) != cudaSuccess)
-        return copy_error();
+        return GEMM_OK;
+    };
+    if ((rc = enqueue()) != GEMM_OK) return fail_joined(p, user, rc);
     return GEMM_OK;
 }

@@ -293,7 +293,11 @@ GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, const void* C,
  *     (else GEMM_ERR_CUDA); the captured copies then read and write the
  *     same host buffers on every replay.
  * Returns GEMM_OK or a GEMM_ERR_* code; argument errors (including host
- * buffers that overlap) are detected before anything is enqueued.
+ * buffers that overlap) are detected before anything is enqueued.  An
+ * error from a later step (a CUDA call, or gemm() refusing a panel) leaves
+ * the copies already enqueued ordered before the rest of `stream`, as on
+ * success: the host buffers must stay unchanged until `stream` has
+ * completed; D is then partly written.
  */
 GEMM_API int gemm_host(void* D, const void* A, const void* B, const void* C,
                        int64_t M, int64_t N, int64_t K,
