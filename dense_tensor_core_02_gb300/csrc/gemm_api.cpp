@@ -383,7 +383,7 @@ int epi_warps_for(int64_t K, int pair, int out_dtype, int tile_n, int f8) {
     if (out_dtype != GEMM_F32 || tile_n == gb300::tcgen05_narrow_n()) return 4;
     const char* v = std::getenv("GEMM_EPI_WARPS");
     if (v && (std::strcmp(v, "4") == 0 || std::strcmp(v, "8") == 0)) return std::atoi(v);
-    const int64_t stage_k = gb300::tcgen05_stage_k(pair, f8);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pair, f8, 4);
     return (K + stage_k - 1) / stage_k <= 4 ? 8 : 4;
 }
 
@@ -408,7 +408,8 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
     pl.num_m = (int)((M + pl.tile_m - 1) / pl.tile_m);
     pl.num_n = (int)((N + pl.tile_n - 1) / pl.tile_n);
     pl.num_tiles = pl.num_m * pl.num_n;
-    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8);
+    pl.epi_warps = mx ? 4 : epi_warps_for(K, pl.pair, out_dtype, pl.tile_n, f8);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps);
     pl.iters = (int)((K + stage_k - 1) / stage_k);
     const int units = pl.pair ? num_sms / 2 : num_sms;   // clusters that fit at once
     int clusters = pl.num_tiles < units ? pl.num_tiles : units;
@@ -442,12 +443,10 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
         pl.ws_bytes = counters + (int64_t)pl.sk_tiles * pl.max_nc * 2 * kPartialBytes;
     }
     if (mx) {
-        pl.epi_warps = 4;
         pl.smem = gb300::tcgen05_mx_smem_bytes(pl.pair, out_dtype == GEMM_F32);
         pl.stages = gb300::tcgen05_mx_stages(pl.pair, out_dtype == GEMM_F32);
         return pl;
     }
-    pl.epi_warps = epi_warps_for(K, pl.pair, out_dtype, pl.tile_n, f8);
     pl.smem = gb300::tcgen05_smem_bytes(pl.pair, pl.epi_warps, pl.tile_n);
     pl.stages = gb300::tcgen05_stages(pl.pair, pl.epi_warps, pl.tile_n);
     return pl;
@@ -611,7 +610,7 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     p.K = (int32_t)K;
     p.num_m_tiles = pl.num_m;
     p.num_n_tiles = pl.num_n;
-    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps);
     p.num_k_blocks = (int32_t)((K + stage_k - 1) / stage_k);   // pipeline stages per tile
     p.num_tiles = pl.num_tiles;
     p.group_m = group_m_setting();
@@ -992,7 +991,7 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
     // 128-K sub-block and 128-row group of A (each CTA of a pair has its
     // own), and (tile N / 128) per sub-block and N tile.
     const int64_t kblocks = (K + 31) / 32;
-    const int64_t kchunks = (int64_t)pl.iters * (gb300::tcgen05_stage_k(pl.pair, 1) / 128);
+    const int64_t kchunks = (int64_t)pl.iters * (gb300::tcgen05_stage_k(pl.pair, 1, pl.epi_warps) / 128);
     const int64_t a_groups = (int64_t)pl.num_m * (pl.pair ? 2 : 1);
     const int sfb_chunks = (pl.tile_n + 127) / 128;
     const int64_t sfa_bytes = gb300::sf_tiles_bytes(128, a_groups, kchunks);

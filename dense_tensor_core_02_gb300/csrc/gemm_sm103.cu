@@ -68,7 +68,8 @@ int tcgen05_tile_m(int pair) { return pair ? Cfg<true, 4>::kTileM : Cfg<false, 4
 int tcgen05_wide_n() { return kBNMax; }
 int tcgen05_narrow_n() { return kNarrowN; }
 int tcgen05_block_k(int f8) { return f8 ? kBK8 : kBK; }
-int tcgen05_stage_k(int pair, int f8) {
+int tcgen05_stage_k(int pair, int f8, int epi_warps) {
+    if (epi_warps == 8) return tcgen05_block_k(f8) * (pair ? Cfg<true, 8>::kSub : Cfg<false, 8>::kSub);
     return tcgen05_block_k(f8) * (pair ? Cfg<true, 4>::kSub : Cfg<false, 4>::kSub);
 }
 int tcgen05_load_rows_b(int pair, int tile_n) { return pair ? tile_n / 2 : tile_n; }

@@ -97,8 +97,11 @@ struct Cfg {
     // A pipeline stage holds kSub 64-wide K sub-blocks.  The MMA issuer pays a
     // fixed cost per stage (barrier wait, release commit) while the tensor
     // core queues only a few MMAs, so the pair kernel puts 8 MMAs (2 sub-
-    // blocks) behind each wait: 64 KiB stages instead of 32 KiB ones.
-    static constexpr int kSub = kPair ? 2 : 1;
+    // blocks) behind each wait: 64 KiB stages instead of 32 KiB ones.  The
+    // 8-epilogue-warp kernel (tiles of a few stages, bound by the D stores)
+    // keeps 32 KiB stages: beside its staging boxes that makes four stages
+    // instead of two, so the loads of the next tile start sooner.
+    static constexpr int kSub = (kPair && kEpiW == 4) ? 2 : 1;
     static constexpr int kASubBytes = kBM * kBK * 2;
     static constexpr int kBSubBytes = kLoadN * kBK * 2;
     static constexpr int kABytes = kSub * kASubBytes;
