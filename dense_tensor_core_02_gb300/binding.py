@@ -52,6 +52,8 @@ def load_library():
             lib.gemm_tile_coords.argtypes = [i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
             lib.gemm_plan.restype = i32
             lib.gemm_plan.argtypes = [i64, i64, i64, i32, ctypes.POINTER(i64)]
+            lib.gemm_plan_layout.restype = i32
+            lib.gemm_plan_layout.argtypes = [i64, i64, i64, i32, i32, i32, i32, ctypes.POINTER(i64)]
             lib.gemm_noalloc.restype = i32
             lib.gemm_noalloc.argtypes = list(lib.gemm.argtypes)
             lib.gemm_host.restype = i32
@@ -150,14 +152,26 @@ def gemm_tile_coords(tile, num_m, num_n, group_m):
     return m.value, n.value
 
 
+_PLAN_KEYS = ("cta_pair", "tile_m", "tile_n", "num_tiles", "grid", "smem_bytes", "epi_warps", "stages",
+              "sk_tiles", "workspace_bytes")
+
+
 def gemm_plan(M, N, K, num_sms):
     out = (ctypes.c_int64 * 10)()
     rc = load_library().gemm_plan(int(M), int(N), int(K), int(num_sms), out)
     if rc != GEMM_OK:
         raise GemmError(rc, "gemm_plan")
-    keys = ("cta_pair", "tile_m", "tile_n", "num_tiles", "grid", "smem_bytes", "epi_warps", "stages",
-            "sk_tiles", "workspace_bytes")
-    return dict(zip(keys, list(out)))
+    return dict(zip(_PLAN_KEYS, list(out)))
+
+
+def gemm_plan_layout(M, N, K, transB, in_dtype, out_dtype, num_sms):
+    """The configuration gemm() would choose for this layout and these types."""
+    out = (ctypes.c_int64 * 10)()
+    rc = load_library().gemm_plan_layout(int(M), int(N), int(K), int(transB), int(in_dtype), int(out_dtype),
+                                         int(num_sms), out)
+    if rc != GEMM_OK:
+        raise GemmError(rc, "gemm_plan_layout")
+    return dict(zip(_PLAN_KEYS, list(out)))
 
 
 def gemm_schedule_units(num_tiles, iters, workers, sk_tiles, worker):

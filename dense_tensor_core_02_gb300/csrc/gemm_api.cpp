@@ -295,6 +295,15 @@ struct Plan {
 // whole waves; the default does the same.  A stream-K range shorter than
 // GEMM_SK_MIN_ITERS stages (default 24) is not worth a partial: for small
 // problems fewer clusters are used instead.
+// Wave-fitted 224-wide tiles (see make_plan): GEMM_FIT_TILES=0 never takes
+// them, 1 takes them wherever they apply, unset chooses by wave count.
+int fit_setting() {
+    const char* v = std::getenv("GEMM_FIT_TILES");
+    if (v && std::strcmp(v, "0") == 0) return 0;
+    if (v && std::strcmp(v, "1") == 0) return 2;
+    return 1;
+}
+
 int streamk_setting() {
     const char* v = std::getenv("GEMM_STREAMK");
     return (v && std::strcmp(v, "0") == 0) ? 0 : 1;
@@ -395,8 +404,10 @@ int epi_warps_for(int64_t K, int pair, int out_dtype, int tile_n, int f8) {
 
 // mx: the block-scaled kernel, whose tiles are 224 wide for f32 D and 192
 // for 16-bit D (on a CTA pair or one SM; no narrow tiles), with 4 epilogue
-// warps; stream-K applies to it as to the others.
-Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk, int out_dtype, int f8, int mx = 0) {
+// warps; stream-K applies to it as to the others.  b_kmajor: B is stored
+// [N, K] (transB), which the 224-wide wave-fitted tiles need.
+Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk, int out_dtype, int f8, int mx = 0,
+               int b_kmajor = 0) {
     Plan pl{};
     const int ov = (mx && variant_override() == kNarrow) ? kAuto : variant_override();
     pl.pair = ov == kPairV || (ov == kAuto && M > gb300::tcgen05_tile_m(0)) ? 1 : 0;
@@ -418,6 +429,30 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
     const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps);
     pl.iters = (int)((K + stage_k - 1) / stage_k);
     const int units = pl.pair ? num_sms / 2 : num_sms;   // clusters that fit at once
+    // Wave-fitted tiles: a persistent launch takes about (waves) x (time of
+    // one tile), which grows with the tile width.  When the 256-wide tiles
+    // leave the last wave partly empty and stream-K would not split it,
+    // 224-wide ones can take fewer tile-widths in all (4096^2: 4 waves of
+    // 256 columns, or 4 waves of 224).  CTA pairs with f32 D, K-major B and
+    // the 4-warp epilogue; taken when that saves at least 5 %.
+    const int fit = fit_setting();
+    if (!mx && fit && pl.pair && b_kmajor && out_dtype == GEMM_F32 && pl.epi_warps == 4 &&
+        pl.tile_n == gb300::tcgen05_wide_n()) {
+        const int fit_n = gb300::tcgen05_fit_n();
+        const int64_t n_fit = (N + fit_n - 1) / fit_n;
+        const int64_t tiles_fit = (int64_t)pl.num_m * n_fit;
+        const int64_t rem = pl.num_tiles % units;
+        const bool sk_fills = allow_streamk && streamk_setting() && pl.iters > 0 && rem != 0 &&
+                              pl.num_tiles > units && rem * pl.iters / units >= sk_min_iters_setting();
+        const double cost_wide = (sk_fills ? (double)pl.num_tiles / units : (double)((pl.num_tiles + units - 1) / units)) *
+                                 gb300::tcgen05_wide_n();
+        const double cost_fit = (double)((tiles_fit + units - 1) / units) * fit_n;
+        if (fit == 2 || cost_fit < 0.95 * cost_wide) {
+            pl.tile_n = fit_n;
+            pl.num_n = (int)n_fit;
+            pl.num_tiles = (int)tiles_fit;
+        }
+    }
     int clusters = pl.num_tiles < units ? pl.num_tiles : units;
     if (clusters < 1) clusters = 1;
     // Stream-K when the whole tiles leave the last wave partly empty.
@@ -589,6 +624,8 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     int rc;
     if ((rc = get_encoder()) != GEMM_OK) return rc;
     std::memset(L, 0, sizeof(*L));
+    // 224-wide tiles (wave-fitted or block-scaled) stage B K-major only
+    if (pl.tile_n == gb300::tcgen05_fit_n() && !transB) return GEMM_ERR_INVALID_ARG;
     const uint32_t bk = (uint32_t)gb300::tcgen05_block_k(f8);   // K elements per 128-byte row
     // A: K-major (transA = 0) as [M rows][K], else MN-major as [K rows][M]
     if (!transA)
@@ -844,9 +881,19 @@ int gemm_schedule_units(int num_tiles, int iters, int workers, int sk_tiles, int
 }
 
 int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out) {
-    if (M < 1 || N < 1 || K < 0 || num_sms < 2 || !out) return GEMM_ERR_INVALID_ARG;
+    return gemm_plan_layout(M, N, K, 0, GEMM_F16, GEMM_F32, num_sms, out);
+}
+
+int gemm_plan_layout(int64_t M, int64_t N, int64_t K, int transB, int in_dtype, int out_dtype, int num_sms,
+                     int64_t* out) {
+    if (M < 1 || N < 1 || K < 0 || num_sms < 2 || !out || (transB != 0 && transB != 1)) return GEMM_ERR_INVALID_ARG;
     if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_TOO_LARGE;
-    Plan pl = make_plan(M, N, K, num_sms, true, GEMM_F32, 0);
+    if ((in_dtype != GEMM_F16 && in_dtype != GEMM_BF16 && !is_f8(in_dtype)) ||
+        (out_dtype != GEMM_F32 && out_dtype != GEMM_F16 && out_dtype != GEMM_BF16))
+        return GEMM_ERR_UNSUPPORTED_DTYPE;
+    // 8-bit operands always reach the kernel K-major (repacked if needed)
+    const int f8 = is_f8(in_dtype) ? 1 : 0;
+    Plan pl = make_plan(M, N, K, num_sms, true, out_dtype, f8, 0, f8 ? 1 : transB);
     out[0] = pl.pair;
     out[1] = pl.tile_m;
     out[2] = pl.tile_n;
@@ -907,12 +954,12 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
                                      out_dtype, s);
     }
 
-    Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, f8 ? 1 : 0);
+    Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, f8 ? 1 : 0, 0, transB);
     void* ws = nullptr;
     uint32_t epoch = 0;
     if (pl.sk_tiles > 0 && workspace_for(kWsStreamK, dev, s, pl.ws_bytes, &ws, &epoch, !in_capture) != GEMM_OK) {
         if (!in_capture) return reject(GEMM_ERR_CUDA, "stream-K workspace");
-        pl = make_plan(M, N, K, ds->num_sms, false, out_dtype, f8 ? 1 : 0);   // whole tiles: no workspace
+        pl = make_plan(M, N, K, ds->num_sms, false, out_dtype, f8 ? 1 : 0, 0, transB);   // whole tiles: no workspace
     }
     TcgenLaunch L;
     if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
@@ -1218,7 +1265,7 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
     if (route == kRouteSync)   // needs no scratch either
         return launch_sync_or_reject(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype,
                                      out_dtype, s);
-    const Plan pl = make_plan(M, N, K, ns->num_sms, false, out_dtype, f8 ? 1 : 0);   // no workspace: data-parallel
+    const Plan pl = make_plan(M, N, K, ns->num_sms, false, out_dtype, f8 ? 1 : 0, 0, transB);   // no workspace: data-parallel
     TcgenLaunch L;
     if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
                                in_dtype, out_dtype)) != GEMM_OK)

@@ -67,6 +67,7 @@ cudaError_t launch_tcgen05(const TcgenLaunch& L, cudaStream_t stream) {
 int tcgen05_tile_m(int pair) { return pair ? Cfg<true, 4>::kTileM : Cfg<false, 4>::kTileM; }
 int tcgen05_wide_n() { return kBNMax; }
 int tcgen05_narrow_n() { return kNarrowN; }
+int tcgen05_fit_n() { return kFitN; }
 int tcgen05_block_k(int f8) { return f8 ? kBK8 : kBK; }
 int tcgen05_stage_k(int pair, int f8, int epi_warps) {
     if (epi_warps == 8) return tcgen05_block_k(f8) * (pair ? Cfg<true, 8>::kSub : Cfg<false, 8>::kSub);
@@ -76,11 +77,13 @@ int tcgen05_load_rows_b(int pair, int tile_n) { return pair ? tile_n / 2 : tile_
 int tcgen05_load_rows_a() { return kBM; }
 int tcgen05_smem_bytes(int pair, int epi_warps, int tile_n) {
     if (tile_n == kNarrowN) return Cfg<false, 4, kNarrowN>::kSmemBytes;
+    if (tile_n == kFitN) return Cfg<true, 4, kFitN>::kSmemBytes;
     if (pair) return epi_warps == 8 ? Cfg<true, 8>::kSmemBytes : Cfg<true, 4>::kSmemBytes;
     return epi_warps == 8 ? Cfg<false, 8>::kSmemBytes : Cfg<false, 4>::kSmemBytes;
 }
 int tcgen05_stages(int pair, int epi_warps, int tile_n) {
     if (tile_n == kNarrowN) return Cfg<false, 4, kNarrowN>::kStages;
+    if (tile_n == kFitN) return Cfg<true, 4, kFitN>::kStages;
     if (pair) return epi_warps == 8 ? Cfg<true, 8>::kStages : Cfg<true, 4>::kStages;
     return epi_warps == 8 ? Cfg<false, 8>::kStages : Cfg<false, 4>::kStages;
 }

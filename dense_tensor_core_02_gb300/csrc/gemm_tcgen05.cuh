@@ -47,6 +47,7 @@ namespace gb300 {
 constexpr int kBM = 128;             // accumulator rows per CTA (= TMEM lanes)
 constexpr int kBNMax = 256;          // accumulator columns of the throughput tiles
 constexpr int kNarrowN = 64;         // accumulator columns of the narrow (small-problem) tiles
+constexpr int kFitN = 224;           // wave-fitted CTA-pair tiles: f32 D, K-major B only
 constexpr int kBK = 64;              // K per sub-block: one 128-byte swizzle row of 16-bit elements
 constexpr int kUK = 16;              // K per tcgen05.mma kind::f16
 constexpr int kBK8 = 128;            // the same for 8-bit elements
@@ -74,9 +75,12 @@ static_assert(kBK8 == 4 * kMxBlock, "one scale word per row and stage");
 // the columns each) for shapes whose time goes into storing D; the operand
 // ring gets whatever shared memory the staging boxes leave.
 // kTileN: 256 (the throughput tiles: 256 x 256 per CTA pair, 128 x 256 per
-// single CTA) or 64 (128 x 64 single-CTA tiles for problems too small to
-// fill the GPU with wide tiles: four times as many CTAs, each with a
-// quarter of the epilogue).
+// single CTA), 224 (256 x 224 CTA-pair tiles, f32 D and K-major B, for
+// shapes whose 256-wide tiles leave the last wave mostly empty: 4096^2
+// gives 256 tiles = 3.4 waves of 76 pairs at 256 wide, 304 = 4.0 at 224)
+// or 64 (128 x 64 single-CTA tiles for problems too small to fill the GPU
+// with wide tiles: four times as many CTAs, each with a quarter of the
+// epilogue).
 // kMX: the block-scaled variant (8-bit K-major operands): each sub-block of a
 // stage also carries the scales of the CTA's 128 rows of A and of all kTileN
 // columns of B (both CTAs of a pair need every column's scales), and two
@@ -92,8 +96,10 @@ struct Cfg {
     // producer, MMA, epilogue warps (+ kMX: the warp that copies the scales)
     static constexpr int kNumThreads = 64 + 32 * kEpiW + (kMX ? 32 : 0);
     static constexpr int kEpiCols = kTileN / (kEpiW / 4);  // accumulator columns per epilogue warp
-    static_assert(kMX || kLoadN % 64 == 0, "MN-major operand boxes are 64 wide");
-    static_assert(kTileN <= kBNMax && kTileN % (kMX ? 32 : 64) == 0, "tile width");
+    // MN-major B is staged in 64-wide boxes; the 224-wide and block-scaled
+    // tiles (112 or 96 B rows per CTA) are launched for K-major B only.
+    static_assert(kMX || kTileN == kFitN || kLoadN % 64 == 0, "MN-major operand boxes are 64 wide");
+    static_assert(kTileN <= kBNMax && kTileN % ((kMX || kTileN == kFitN) ? 32 : 64) == 0, "tile width");
     // A pipeline stage holds kSub 64-wide K sub-blocks.  The MMA issuer pays a
     // fixed cost per stage (barrier wait, release commit) while the tensor
     // core queues only a few MMAs, so the pair kernel puts 8 MMAs (2 sub-
@@ -912,7 +918,8 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
 
 // Instantiated configurations: every (pair, beta != 0) combination of the
 // 256-wide tiles with 4 epilogue warps for each output type, and with 8
-// epilogue warps for f32 output (the store-bound configuration); the 64-wide
+// epilogue warps for f32 output (the store-bound configuration); the
+// 224-wide CTA-pair tiles with 4 epilogue warps for f32 output; the 64-wide
 // single-CTA tiles with 4 epilogue warps for each output type.
 template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN, bool kF8, bool kMX = false>
 static cudaError_t prepare_one() {
@@ -926,6 +933,8 @@ static cudaError_t prepare_group() {
     cudaError_t e;
     if ((e = prepare_one<kPair, kOutF32, 4, kHasC, kBNMax, kF8>()) != cudaSuccess) return e;
     if ((e = prepare_one<kPair, kOutF32, 8, kHasC, kBNMax, kF8>()) != cudaSuccess) return e;
+    if constexpr (kPair)
+        if ((e = prepare_one<kPair, kOutF32, 4, kHasC, kFitN, kF8>()) != cudaSuccess) return e;
     if ((e = prepare_one<kPair, kOutF16, 4, kHasC, kBNMax, kF8>()) != cudaSuccess) return e;
     return prepare_one<kPair, kOutBF16, 4, kHasC, kBNMax, kF8>();
 }
@@ -968,6 +977,11 @@ static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
 
 template <bool kPair, bool kHasC, bool kF8>
 static cudaError_t launch_group(const TcgenLaunch& L, cudaStream_t stream) {
+    if (L.tile_n == kFitN) {   // f32 D, 4 epilogue warps, CTA pairs (the host's plan guarantees it)
+        if constexpr (kPair)
+            if (L.out == kOutF32 && L.epi_warps == 4) return launch_one<kPair, kOutF32, 4, kHasC, kFitN, kF8>(L, stream);
+        return cudaErrorInvalidConfiguration;
+    }
     if (L.out == kOutF32)
         return L.epi_warps == 8 ? launch_one<kPair, kOutF32, 8, kHasC, kBNMax, kF8>(L, stream)
                                 : launch_one<kPair, kOutF32, 4, kHasC, kBNMax, kF8>(L, stream);

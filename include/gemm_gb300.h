@@ -205,7 +205,8 @@ GEMM_API int gemm_tile_coords(int tile, int num_m, int num_n, int group_m, int* 
 
 /*
  * Host-only query (no GPU needed): the kernel configuration gemm() would
- * choose for these sizes on a GPU with num_sms SMs.  out[0..9] receive:
+ * choose for these sizes on a GPU with num_sms SMs (fp16 operands, B stored
+ * [K, N], f32 D; gemm_plan_layout below takes the others).  out[0..9] receive:
  * cta_pair (1 = 2-SM tiles), tile_m, tile_n, number of tiles, grid size
  * (CTAs), dynamic shared memory bytes, epilogue warps, operand pipeline
  * stages, stream-K tiles (trailing tiles split along K; 0 = every tile
@@ -213,6 +214,21 @@ GEMM_API int gemm_tile_coords(int tile, int num_m, int num_n, int group_m, int* 
  * need.  Returns GEMM_OK or an error code.
  */
 GEMM_API int gemm_plan(int64_t M, int64_t N, int64_t K, int num_sms, int64_t* out);
+
+/*
+ * Host-only query (no GPU needed): gemm_plan() for a layout and types --
+ * transB (1: B stored [N, K]), in_dtype (GEMM_F16, GEMM_BF16, GEMM_E4M3 or
+ * GEMM_E5M2) and out_dtype (GEMM_F32, GEMM_F16 or GEMM_BF16) -- with the
+ * same out[0..9].  8-bit operands are planned K-major, the layout gemm()
+ * runs them in.  The plan can differ with the layout: with f32 D and
+ * K-major B, tiles 224 columns wide are chosen when they fill the last wave
+ * better than 256-wide ones.  gemm_plan(M, N, K, num_sms, out) equals
+ * gemm_plan_layout(M, N, K, 0, GEMM_F16, GEMM_F32, num_sms, out).  Returns
+ * GEMM_OK, GEMM_ERR_INVALID_ARG, GEMM_ERR_TOO_LARGE or
+ * GEMM_ERR_UNSUPPORTED_DTYPE.
+ */
+GEMM_API int gemm_plan_layout(int64_t M, int64_t N, int64_t K, int transB, int in_dtype, int out_dtype,
+                              int num_sms, int64_t* out);
 
 /*
  * Host-only query (no GPU needed): the work of one persistent worker

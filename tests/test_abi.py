@@ -33,7 +33,7 @@ def _declared_functions():
 
 def test_header_declares_the_abi():
     assert {"gemm", "gemm_status_string", "gemm_poll_device_error", "gemm_tile_coords",
-            "gemm_plan"} <= _declared_functions()
+            "gemm_plan", "gemm_plan_layout"} <= _declared_functions()
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -294,6 +294,46 @@ def test_plan_tile_width(lib, M, N, K, tile_n):
     assert p["tile_n"] == tile_n
     if tile_n == 64:
         assert p["cta_pair"] == 0 and p["tile_m"] == 128 and p["epi_warps"] == 4
+
+
+@pytest.mark.parametrize("M,N,K,transB,in_dtype,out_dtype,tile_n,num_tiles", [
+    (4096, 4096, 4096, 1, binding.BF16, binding.F32, 224, 16 * 19),   # 3.4 waves of 256 -> 4.0 of 224
+    (4096, 4096, 4096, 1, binding.E5M2, binding.F32, 224, 16 * 19),
+    (4096, 4096, 4096, 0, binding.E4M3, binding.F32, 224, 16 * 19),   # 8-bit: planned K-major
+    (4096, 4096, 4096, 0, binding.BF16, binding.F32, 256, 256),       # MN-major B: 64-wide boxes
+    (4096, 4096, 4096, 1, binding.BF16, binding.BF16, 256, 256),      # 16-bit D: 64-column chunks
+    (8192, 8192, 8192, 1, binding.F16, binding.F32, 256, 1024),       # stream-K fills the last wave
+    (8192, 8192, 4096, 1, binding.F16, binding.F32, 256, 1024),       # 14 waves of 256 = 16 of 224
+    (8192, 8192, 256, 1, binding.F16, binding.F32, 256, 1024),        # store-bound: 8 epilogue warps
+    (32768, 256, 4096, 1, binding.F16, binding.F32, 256, 128),        # N = 256: one column of tiles
+])
+def test_plan_wave_fitted_tiles(lib, M, N, K, transB, in_dtype, out_dtype, tile_n, num_tiles):
+    """224-wide CTA-pair tiles exactly where they fill the waves better
+    (f32 D and K-major B only)."""
+    p = binding.gemm_plan_layout(M, N, K, transB, in_dtype, out_dtype, 152)
+    assert (p["tile_n"], p["num_tiles"]) == (tile_n, num_tiles)
+    if tile_n == 224:
+        assert p["cta_pair"] == 1 and p["epi_warps"] == 4 and p["sk_tiles"] == 0 and p["grid"] == 152
+
+
+def test_plan_layout_defaults_and_rejections(lib):
+    for M, N, K in [(512, 512, 512), (4096, 4096, 4096), (8192, 8192, 8192), (1000, 1000, 1000)]:
+        assert binding.gemm_plan(M, N, K, 152) == binding.gemm_plan_layout(M, N, K, 0, binding.F16, binding.F32, 152)
+    for args, code in [((64, 64, 64, 2, binding.F16, binding.F32, 152), -1),
+                       ((64, 64, 64, 0, binding.F32, binding.F32, 152), -2),
+                       ((64, 64, 64, 0, binding.F16, binding.E4M3, 152), -2),
+                       ((0, 64, 64, 0, binding.F16, binding.F32, 152), -1)]:
+        with pytest.raises(binding.GemmError) as e:
+            binding.gemm_plan_layout(*args)
+        assert e.value.status == code
+
+
+def test_plan_wave_fitted_tiles_switch(lib, monkeypatch):
+    monkeypatch.setenv("GEMM_FIT_TILES", "0")
+    assert binding.gemm_plan_layout(4096, 4096, 4096, 1, binding.BF16, binding.F32, 152)["tile_n"] == 256
+    monkeypatch.setenv("GEMM_FIT_TILES", "1")
+    assert binding.gemm_plan_layout(8192, 8192, 8192, 1, binding.F16, binding.F32, 152)["tile_n"] == 224
+    assert binding.gemm_plan_layout(8192, 8192, 8192, 0, binding.F16, binding.F32, 152)["tile_n"] == 256
 
 
 def test_schedule_rejects_bad_arguments(lib):
