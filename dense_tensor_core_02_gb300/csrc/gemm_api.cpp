@@ -1127,11 +1127,10 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
         if (e == cudaSuccess) e = gb300::launch_copy2d(b2, kp / 2, B, ldb_in / 2, N, K / 2, 1, s);
     }
     if (e == cudaSuccess)
-        e = gb300::launch_sf_tiles(sfa_tiles, static_cast<const uint8_t*>(SFA), ld_sfa, M, kblocks, 128, a_groups,
-                                   kchunks, s);
-    if (e == cudaSuccess)
-        e = gb300::launch_sf_tiles(sfb_tiles, static_cast<const uint8_t*>(SFB), ld_sfb, N, kblocks, pl.tile_n,
-                                   pl.num_n, kchunks, s);
+        e = gb300::launch_sf_tiles(
+            gb300::sf_job(sfa_tiles, static_cast<const uint8_t*>(SFA), ld_sfa, M, kblocks, 128, a_groups, kchunks),
+            gb300::sf_job(sfb_tiles, static_cast<const uint8_t*>(SFB), ld_sfb, N, kblocks, pl.tile_n, pl.num_n, kchunks),
+            s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return reject(GEMM_ERR_LAUNCH, cudaGetErrorString(e));

@@ -90,8 +90,18 @@ cudaError_t launch_tcgen05_mx(const TcgenLaunch& L, cudaStream_t stream);  // ge
 // the block-scaled kernel's 512-byte chunks (see GemmParams::sf_a_groups)
 // for tiles of tile_rows rows (columns) and kchunks 128-K sub-blocks; rows
 // and blocks outside the matrix get the scale 1 (byte 127).
-cudaError_t launch_sf_tiles(uint8_t* out, const uint8_t* in, int64_t ld, int64_t rows, int64_t kblocks,
-                            int tile_rows, int64_t tiles, int64_t kchunks, cudaStream_t stream);
+// One operand's block scales for sf_tiles_kernel (see gemm_sm103_mx.cu).
+struct SfJob {
+    uint32_t* out;          // rearranged chunks (sf_tiles_bytes)
+    const uint8_t* in;      // the caller's scales, [rows][ld] bytes
+    int64_t ld, rows, kblocks;
+    int32_t tile_rows, groups;
+    int64_t tiles, kchunks;
+    int64_t blocks;         // thread blocks of this job
+};
+SfJob sf_job(uint8_t* out, const uint8_t* in, int64_t ld, int64_t rows, int64_t kblocks, int tile_rows, int64_t tiles,
+             int64_t kchunks);
+cudaError_t launch_sf_tiles(const SfJob& a, const SfJob& b, cudaStream_t stream);   // both in one launch
 int64_t sf_tiles_bytes(int tile_rows, int64_t tiles, int64_t kchunks);
 int tcgen05_mx_tile_n(int f32_out);   // D columns per block-scaled tile
 int tcgen05_mx_smem_bytes(int pair, int f32_out);

@@ -32,33 +32,54 @@ int tcgen05_mx_stages(int pair, int f32_out) {
     return pair ? Cfg<true, 4, kMxTileN, true>::kStages : Cfg<false, 4, kMxTileN, true>::kStages;
 }
 
-// One thread per (stage kc, tile, 128-row group g, row r of the group): the
-// row's four scales of the stage (blocks 4 kc .. 4 kc + 3) become one 32-bit
-// word at byte (r % 32) * 16 + (r / 32) * 4 of the group's 512-byte chunk,
-// block 4 kc + j in byte j.  That is the layout tcgen05.cp .32x128b.warpx4
-// reads: 32 rows of 16 bytes, row r % 32 holding rows r % 32 + 32 q of the
-// group in its four words q.
-__global__ void sf_tiles_kernel(uint32_t* out, const uint8_t* in, int64_t ld, int64_t rows, int64_t kblocks,
-                                int tile_rows, int groups, int64_t tiles, int64_t total) {
+// The block scales in the order the main kernel loads them.  For each
+// 128-K sub-block kc, tile and 128-row group g of the tile, a 512-byte chunk
+// whose 32-bit word (r % 32) * 4 + r / 32 holds row r's four scales of the
+// sub-block (blocks 4 kc .. 4 kc + 3, block 4 kc + j in byte j): the layout
+// tcgen05.cp .32x128b.warpx4 reads, 32 rows of 16 bytes, row r % 32 holding
+// rows r % 32 + 32 q of the group in its four words q.  Rows past the
+// operand or the tile, and blocks past K, get 127 (a scale of 1).
+//
+// A thread block takes one group and a run of kSfRun sub-blocks: it gathers
+// the run's scales row by row (each row's bytes are contiguous in the
+// caller's array) into shared memory, then writes the run's chunks whole.
+// Both operands' scales go in one launch: blocks [0, a.blocks) take SFA.
+constexpr int kSfRun = 8;
+
+__global__ void __launch_bounds__(256) sf_tiles_kernel(SfJob a, SfJob b) {
     ptx::grid_dependency_wait();   // the previous kernel's writes are visible (programmatic launch)
     ptx::launch_dependents();
-    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (int64_t)gridDim.x * blockDim.x) {
-        const int r = (int)(idx % 128);
-        const int64_t chunk = idx / 128;   // ((kc * tiles + tile) * groups + g)
-        const int g = (int)(chunk % groups);
-        const int64_t tile = (chunk / groups) % tiles;
-        const int64_t kc = chunk / groups / tiles;
+    __shared__ uint32_t words[128 * (kSfRun + 1)];   // [row][sub-block of the run], one word of padding per row
+    const int64_t bid = (int64_t)blockIdx.x;
+    const bool is_a = bid < a.blocks;
+    const SfJob& j = is_a ? a : b;
+    const int64_t blk = is_a ? bid : bid - a.blocks;
+    const int64_t runs = (j.kchunks + kSfRun - 1) / kSfRun;
+    const int64_t run = blk % runs;
+    const int g = (int)((blk / runs) % j.groups);
+    const int64_t tile = blk / runs / j.groups;
+    const int64_t kc0 = run * kSfRun;
+    for (int i = threadIdx.x; i < 128 * kSfRun; i += blockDim.x) {
+        const int r = i / kSfRun, c = i % kSfRun;
         const int in_tile = g * 128 + r;
-        const int64_t row = tile * tile_rows + in_tile;
+        const int64_t row = tile * j.tile_rows + in_tile;
+        const bool row_ok = in_tile < j.tile_rows && row < j.rows;
         uint32_t word = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int64_t kb = kc * 4 + j;
-            const uint32_t v = (in_tile < tile_rows && row < rows && kb < kblocks) ? in[row * ld + kb] : 127u;
-            word |= v << (8 * j);
+        for (int q = 0; q < 4; ++q) {
+            const int64_t kb = (kc0 + c) * 4 + q;
+            const uint32_t v = (row_ok && kb < j.kblocks) ? j.in[row * j.ld + kb] : 127u;
+            word |= v << (8 * q);
         }
-        out[chunk * (kSfChunkBytes / 4) + (r % 32) * 4 + r / 32] = word;
+        words[r * (kSfRun + 1) + c] = word;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 128 * kSfRun; i += blockDim.x) {
+        const int c = i / 128, p = i % 128;
+        const int64_t kc = kc0 + c;
+        if (kc >= j.kchunks) break;   // c only grows along a thread's loop
+        const int r = (p & 3) * 32 + (p >> 2);
+        j.out[((kc * j.tiles + tile) * j.groups + g) * 128 + p] = words[r * (kSfRun + 1) + c];
     }
 }
 
@@ -67,15 +88,27 @@ int64_t sf_tiles_bytes(int tile_rows, int64_t tiles, int64_t kchunks) {
     return kchunks * tiles * groups * kSfChunkBytes;
 }
 
-cudaError_t launch_sf_tiles(uint8_t* out, const uint8_t* in, int64_t ld, int64_t rows, int64_t kblocks,
-                            int tile_rows, int64_t tiles, int64_t kchunks, cudaStream_t stream) {
-    const int groups = (tile_rows + 127) / 128;
-    const int64_t total = kchunks * tiles * groups * 128;
-    if (total <= 0) return cudaSuccess;
-    int64_t blocks = (total + 255) / 256;
-    if (blocks > 4096) blocks = 4096;
-    return launch_with_pdl(sf_tiles_kernel, dim3((unsigned)blocks), dim3(256), stream,
-                           reinterpret_cast<uint32_t*>(out), in, ld, rows, kblocks, tile_rows, groups, tiles, total);
+SfJob sf_job(uint8_t* out, const uint8_t* in, int64_t ld, int64_t rows, int64_t kblocks, int tile_rows, int64_t tiles,
+             int64_t kchunks) {
+    SfJob j{};
+    j.out = reinterpret_cast<uint32_t*>(out);
+    j.in = in;
+    j.ld = ld;
+    j.rows = rows;
+    j.kblocks = kblocks;
+    j.tile_rows = tile_rows;
+    j.groups = (tile_rows + 127) / 128;
+    j.tiles = tiles;
+    j.kchunks = kchunks;
+    j.blocks = kchunks > 0 ? tiles * j.groups * ((kchunks + kSfRun - 1) / kSfRun) : 0;
+    return j;
+}
+
+cudaError_t launch_sf_tiles(const SfJob& a, const SfJob& b, cudaStream_t stream) {
+    const int64_t blocks = a.blocks + b.blocks;
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    return launch_with_pdl(sf_tiles_kernel, dim3((unsigned)blocks), dim3(256), stream, a, b);
 }
 
 }  // namespace gb300
