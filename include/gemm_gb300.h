@@ -166,10 +166,12 @@ GEMM_API int gemm(void* D, const void* A, const void* B, const void* C,
  *                    (else GEMM_ERR_INVALID_ARG).
  *   everything else  as for gemm().
  *
- * Kernel: tcgen05.mma kind::mxf8f6f4 with 256 x 192 tiles on a CTA pair
- * (128 x 192 on one SM when M <= 128); each call first rearranges the
- * scales into 512-byte chunks in a workspace of this (device, stream)
- * (about (M + 1.33 N) * K / 128 bytes), then runs the product.  Layouts that are not K-major 16-byte aligned go through the same
+ * Kernel: tcgen05.mma kind::mxf8f6f4 with 256 x 224 tiles on a CTA pair
+ * for f32 D and 256 x 192 for 16-bit D (128-row tiles on one SM when
+ * M <= 128); each call first rearranges the scales into 512-byte chunks in
+ * a workspace of this (device, stream) (about (M + 1.14 N) * K / 32 bytes
+ * for f32 D, (M + 1.33 N) * K / 32 for 16-bit D), then runs the product.
+ * Layouts that are not K-major 16-byte aligned go through the same
  * repacking as gemm()'s 8-bit operands.  D must not overlap SFA or SFB
  * (GEMM_ERR_ALIAS).  Under CUDA graph capture nothing is allocated: the
  * workspaces must exist from an earlier call of at least the same size on
