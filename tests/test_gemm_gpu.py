@@ -267,6 +267,28 @@ def test_non_default_stream():
     H.assert_close(D.numpy(), ref, bound, what="side stream")
 
 
+def test_default_stream_argument_is_torchs_current_stream():
+    """stream=None means torch's current stream, also inside a stream context:
+    the call is ordered after work queued there and before work queued later."""
+    from dense_tensor_core_02_gb300.binding import _stream
+    assert _stream(None) == torch.cuda.current_stream().cuda_stream
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        assert _stream(None) == s.cuda_stream != torch.cuda.default_stream().cuda_stream
+        M, N, K = 384, 320, 256
+        dev = torch.device("cuda", 0)
+        A = H.int_matrix((M, K), -4, 4, "f16", 53).to(dev)
+        B = H.int_matrix((K, N), -4, 4, "f16", 54).to(dev)
+        torch.cuda._sleep(1000000)   # the call must wait for this on s
+        D = torch.full((M, N), float("nan"), device=dev)
+        assert binding.gemm(D, A, B, None, M, N, K, K, N, N, N, 0, 0, 1.0, 0.0, 0, 2) == 0
+        out = D.clone()   # queued on s after the product
+    torch.cuda.synchronize()
+    ref, _ = H.oracle_full(A.cpu(), B.cpu(), None, M, N, K)
+    H.assert_exact(out.cpu().numpy(), ref, "stream=None inside a stream context")
+    assert _stream(None) == torch.cuda.current_stream().cuda_stream
+
+
 def test_repeatable_bitwise():
     """The same call twice gives the same bits (fixed accumulation order)."""
     case = CASE_BY_NAME["gemm_512_f16_alpha1.5_beta0.5"]
