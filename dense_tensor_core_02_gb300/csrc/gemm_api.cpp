@@ -508,35 +508,46 @@ struct Workspace {
     void* base;
     int64_t bytes;
     uint32_t epoch;
+    bool captured;   // a CUDA graph captured a launch that uses `base`
 };
 std::vector<Workspace> g_workspaces;
+// Buffers replaced while a captured graph may still use them: kept (not
+// freed) until the process exits, so that replaying that graph stays safe.
+std::vector<void*> g_retired;
 
 // `may_grow` false (the stream is being captured into a CUDA graph, where
 // allocating is not allowed): only an existing workspace that is large
-// enough is returned; otherwise GEMM_ERR_CUDA, with nothing changed.
+// enough is returned; otherwise GEMM_ERR_CUDA, with nothing changed.  A
+// workspace a capture has used is never freed when it grows later (graph
+// replays keep using its address); others are freed (which synchronises
+// the device, so no launch still uses them).
 int workspace_for(int kind, int dev, cudaStream_t s, int64_t bytes, void** base, uint32_t* epoch, bool may_grow) {
     std::lock_guard<std::mutex> lock(g_mutex);
     Workspace* w = nullptr;
     for (auto& x : g_workspaces)
         if (x.kind == kind && x.dev == dev && x.stream == s) w = &x;
     if (!w) {
-        g_workspaces.push_back(Workspace{kind, dev, s, nullptr, 0, 0});
+        g_workspaces.push_back(Workspace{kind, dev, s, nullptr, 0, 0, false});
         w = &g_workspaces.back();
     }
     if (w->bytes < bytes) {
         if (!may_grow) return GEMM_ERR_CUDA;
-        if (w->base && cudaFree(w->base) != cudaSuccess) {
+        if (w->base && w->captured) {
+            g_retired.push_back(w->base);
+        } else if (w->base && cudaFree(w->base) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
         w->base = nullptr;
         w->bytes = 0;
+        w->captured = false;
         if (cudaMalloc(&w->base, (size_t)bytes) != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
         w->bytes = bytes;
     }
+    if (!may_grow) w->captured = true;
     w->epoch = (w->epoch + 1) & 0xFFFFFFu;
     *base = w->base;
     *epoch = w->epoch;

@@ -69,11 +69,13 @@ struct Pipe {
     cudaEvent_t copied_out = nullptr;        // this call's D is on the host
     char* buf = nullptr;
     int64_t bytes = 0;
+    bool captured = false;   // a CUDA graph captured copies into `buf`
     bool ready = false;
 };
 
 std::mutex g_mutex;
 std::vector<Pipe*> g_pipes;
+std::vector<char*> g_retired;   // replaced staging that captured graphs may still use
 
 // True while `s` is being captured into a CUDA graph: nothing may be
 // created or allocated then.
@@ -116,16 +118,25 @@ int pipe_for(int dev, cudaStream_t user, bool may_create, Pipe** out) {
 }
 
 // Grows the pipe's staging buffer.  Freeing the old one synchronises the
-// device, so no copy or product still uses it.
+// device, so no copy or product still uses it; one that a captured graph
+// has used is kept instead (until the process exits), since replays of
+// that graph keep using its address.  `may_grow` false: inside a capture.
 int ensure_buffer(Pipe* p, int64_t bytes, bool may_grow) {
-    if (p->bytes >= bytes) return GEMM_OK;
+    if (p->bytes >= bytes) {
+        if (!may_grow) p->captured = true;
+        return GEMM_OK;
+    }
     if (!may_grow) return GEMM_ERR_CUDA;
-    if (p->buf && cudaFree(p->buf) != cudaSuccess) {
+    if (p->buf && p->captured) {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        g_retired.push_back(p->buf);
+    } else if (p->buf && cudaFree(p->buf) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
     p->buf = nullptr;
     p->bytes = 0;
+    p->captured = false;
     if (cudaMalloc(&p->buf, (size_t)bytes) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;

@@ -123,7 +123,9 @@ typedef enum {
  * long as an earlier call (outside the capture) has run on the device; it
  * then allocates nothing: stream-K splitting and the repacking route are
  * used only where this stream's workspace from earlier calls is large
- * enough (otherwise whole tiles, respectively the mma.sync kernel).
+ * enough (otherwise whole tiles, respectively the mma.sync kernel).  A
+ * workspace that a capture used stays allocated when a later call outgrows
+ * it, so the graph can be replayed after any number of other calls.
  * Returns GEMM_OK or a GEMM_ERR_* code (see gemm_status_t).
  * Setting the environment variable GEMM_LOG=1 prints each call's plan or
  * rejection reason to stderr.
@@ -309,7 +311,8 @@ GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, const void* C,
  *   - CUDA graphs: a call inside a capture of `stream` needs the staging
  *     set up by an earlier call on that stream with at least these sizes
  *     (else GEMM_ERR_CUDA); the captured copies then read and write the
- *     same host buffers on every replay.
+ *     same host buffers on every replay.  Staging that a capture used
+ *     stays allocated when later calls outgrow it, so replays stay valid.
  * Returns GEMM_OK or a GEMM_ERR_* code; argument errors (including host
  * buffers that overlap) are detected before anything is enqueued.  An
  * error from a later step (a CUDA call, or gemm() refusing a panel) leaves

@@ -71,6 +71,46 @@ def test_captured_gemm_replays(warm):
             H.assert_exact(Dd.cpu().numpy(), ref, "replay %d %s" % (rep, (M, N, K)))
 
 
+def test_replay_after_the_workspace_grew():
+    """A graph captured with the stream-K workspace of one size, then an
+    eager call on the same stream that needs a larger one: the library keeps
+    the captured buffer (it does not free what a graph refers to), so later
+    replays still compute into valid memory and give exact results."""
+    dev = torch.device("cuda", 0)
+    s = torch.cuda.Stream()
+    small, large = (256, 256, 1024), (1024, 1024, 2048)   # stream-K workspaces of 34 and 101 MB
+    A, B, Ad, Bd, Dd = _problem(*small, 31, dev)
+    A2, B2, Ad2, Bd2, Dd2 = _problem(*large, 41, dev)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def call(prob, shape):
+        M, N, K = shape
+        assert binding.gemm(prob[2], prob[0], prob[1], None, M, N, K, K, N, N, N, 0, 0, 1.0, 0.0, 0, 2, s) == 0
+
+    with H.env(GEMM_SK_MIN_ITERS="1"):
+        p_small, p_large = binding.gemm_plan(*small, sms), binding.gemm_plan(*large, sms)
+        assert 0 < p_small["workspace_bytes"] < p_large["workspace_bytes"]
+        with torch.cuda.stream(s):
+            call((Ad, Bd, Dd), small)   # creates the workspace at the small size
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            call((Ad, Bd, Dd), small)
+        with torch.cuda.stream(s):
+            call((Ad2, Bd2, Dd2), large)   # grows the workspace
+        s.synchronize()
+        for _ in range(2):
+            Dd.fill_(float("nan"))
+            g.replay()
+            torch.cuda.synchronize()
+            ref, _ = H.oracle_full(A, B, None, *small)
+            H.assert_exact(Dd.cpu().numpy(), ref, "replay after growth")
+    rows = list(range(0, large[0], 61))
+    ref2, _ = H.oracle_at(A2, B2, None, *large, [r for r in rows for _ in range(large[1])],
+                          [c for _ in rows for c in range(large[1])])
+    H.assert_exact(Dd2.cpu().numpy()[rows].ravel(), ref2, "the eager call that grew the workspace")
+
+
 def test_captured_misaligned_call_without_workspace():
     """A layout off the 16-byte grid, large enough for the repacking route,
     captured on a fresh stream: no repack workspace exists, so the captured
