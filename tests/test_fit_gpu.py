@@ -82,6 +82,21 @@ def test_fit_8bit_exact(fit, dtype, beta):
     H.assert_exact(D.numpy(), ref, "224-wide %s beta %g" % (dtype, beta))
 
 
+@pytest.mark.parametrize("dtype", ["e4m3", "e5m2"])
+def test_fit_8bit_b_stored_k_by_n(fit, dtype):
+    """8-bit B stored [K, N]: the call copies it K-major into a workspace
+    first, then runs the 224-wide tiles on the copy."""
+    M, N, K = 520, 900, 1408   # more than 4 stages of 256: the 4-warp kernel
+    assert _plan(M, N, K, dtype)["tile_n"] == FIT_N   # planned K-major whatever the stored layout
+    A = H.int_matrix((M, K), -4, 4, dtype, 45)
+    B = H.int_matrix((K, N), -4, 4, dtype, 46)
+    C = H.int_matrix((M, N), -50, 50, "f32", 47)
+    D, rc = H.run_gemm(A, B, C, M, N, K, transB=0, beta=1.0, in_dtype=dtype)
+    assert rc == 0
+    ref, _ = H.oracle_full(A, B, C, M, N, K, transB=0, beta=1.0, in_dtype=dtype)
+    H.assert_exact(D.numpy(), ref, "224-wide %s, B stored [K, N]" % dtype)
+
+
 @pytest.mark.parametrize("shape", [(1000, 1000, 1000), (256, 672, 4096), (600, 520, 2000)],
                          ids=lambda s: "x".join(map(str, s)))
 def test_fit_streamk_exact(fit, shape):
