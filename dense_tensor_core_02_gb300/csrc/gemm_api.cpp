@@ -291,10 +291,6 @@ struct Plan {
     int64_t ws_bytes;  // workspace the stream-K fixup needs
 };
 
-// Stream-K policy: GEMM_STREAMK=0 never, 1 whenever the tiles do not fill
-// whole waves; the default does the same.  A stream-K range shorter than
-// GEMM_SK_MIN_ITERS stages (default 24) is not worth a partial: for small
-// problems fewer clusters are used instead.
 // Wave-fitted 224-wide tiles (see make_plan): GEMM_FIT_TILES=0 never takes
 // them, 1 takes them wherever they apply, unset chooses by wave count.
 int fit_setting() {
@@ -304,6 +300,10 @@ int fit_setting() {
     return 1;
 }
 
+// Stream-K policy: GEMM_STREAMK=0 never, 1 whenever the tiles do not fill
+// whole waves; the default does the same.  A stream-K range shorter than
+// GEMM_SK_MIN_ITERS stages (default 24) is not worth a partial: for small
+// problems fewer clusters are used instead.
 int streamk_setting() {
     const char* v = std::getenv("GEMM_STREAMK");
     return (v && std::strcmp(v, "0") == 0) ? 0 : 1;
@@ -444,8 +444,9 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
         const int64_t rem = pl.num_tiles % units;
         const bool sk_fills = allow_streamk && streamk_setting() && pl.iters > 0 && rem != 0 &&
                               pl.num_tiles > units && rem * pl.iters / units >= sk_min_iters_setting();
-        const double cost_wide = (sk_fills ? (double)pl.num_tiles / units : (double)((pl.num_tiles + units - 1) / units)) *
-                                 gb300::tcgen05_wide_n();
+        const double waves_wide =
+            sk_fills ? (double)pl.num_tiles / units : (double)((pl.num_tiles + units - 1) / units);
+        const double cost_wide = waves_wide * gb300::tcgen05_wide_n();
         const double cost_fit = (double)((tiles_fit + units - 1) / units) * fit_n;
         if (fit == 2 || cost_fit < 0.95 * cost_wide) {
             pl.tile_n = fit_n;
