@@ -73,3 +73,28 @@ def test_noalloc_matches_gemm_twice(prob):
     for i, D in enumerate(outs):
         got = D.double().cpu().numpy()
         H.assert_close(got, want, bound, ot, "gemm_noalloc call %d vs gemm" % (i + 1))
+
+
+def test_noalloc_wave_fitted_tiles():
+    """gemm_noalloc() on the 224-wide tiles (taken by force on this shape) gives
+    the same bits as gemm() on integer inputs, and the oracle's."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    M, N, K = 1024, 1120, 1408
+    dev = torch.device("cuda", 0)
+    A = H.int_matrix((M, K), -4, 4, "bf16", 71)
+    B = H.int_matrix((N, K), -4, 4, "bf16", 72)
+    C = H.int_matrix((M, N), -50, 50, "f32", 73)
+    Ad, Bd, Cd = A.to(dev), B.to(dev), C.to(dev)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    with H.env(GEMM_FIT_TILES="1", GEMM_VARIANT="pair", GEMM_PATH="tcgen05"):
+        assert binding.gemm_plan_layout(M, N, K, 1, binding.BF16, binding.F32, sms)["tile_n"] == 224
+        D = torch.full((M, N), float("nan"), device=dev)
+        ref = torch.full((M, N), float("nan"), device=dev)
+        assert _call(binding.gemm_noalloc, D, Ad, Bd, Cd, M, N, K, "bf16", "f32", 0, 1, 1.0, 1.0) == 0
+        assert _call(binding.gemm, ref, Ad, Bd, Cd, M, N, K, "bf16", "f32", 0, 1, 1.0, 1.0) == 0
+    torch.cuda.synchronize()
+    assert binding.gemm_poll_device_error()[0] == 0
+    assert torch.equal(D, ref)
+    want, _ = H.oracle_full(A, B, C, M, N, K, transB=1, beta=1.0, in_dtype="bf16")
+    H.assert_exact(D.cpu().numpy(), want, "gemm_noalloc on 224-wide tiles")
