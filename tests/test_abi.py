@@ -400,3 +400,30 @@ def test_fp4_only_through_gemm_mx(lib):
     for kw in (dict(), dict(A=A_ + 3, lda=70), dict(K=2, lda=2, ldb=2)):
         rc = _call_mx(in_dtype=5, **kw)
         assert rc in (0, -7, -5), (kw, rc)
+
+
+def test_plan_layout_invariants(lib):
+    """Every plan, over a seeded spread of shapes, layouts and types: the tile
+    count covers the output, the grid fits the GPU, 224-wide tiles appear only
+    for f32 D with K-major B on CTA pairs, and a workspace exists exactly when
+    tiles are split along K."""
+    import numpy as np
+    rng = np.random.default_rng(2024)
+    sms = 152
+    for _ in range(3000):
+        M, N = (int(x) for x in np.exp(rng.uniform(0, np.log(40000), 2)).astype(int) + 1)
+        K = int(np.exp(rng.uniform(0, np.log(70000)))) if rng.random() > 0.05 else 0
+        tb = int(rng.integers(0, 2))
+        it = int(rng.choice([binding.F16, binding.BF16, binding.E4M3, binding.E5M2]))
+        ot = int(rng.choice([binding.F32, binding.F16, binding.BF16]))
+        p = binding.gemm_plan_layout(M, N, K, tb, it, ot, sms)
+        tm, tn = p["tile_m"], p["tile_n"]
+        assert tn in (64, 224, 256) and tm in (128, 256), p
+        assert p["num_tiles"] == -(-M // tm) * -(-N // tn), (M, N, K, p)
+        assert 1 <= p["grid"] <= sms and (p["grid"] % 2 == 0 or not p["cta_pair"]), p
+        if tn == 224:
+            assert p["cta_pair"] and ot == binding.F32 and p["epi_warps"] == 4, (M, N, K, tb, it, ot, p)
+            assert tb == 1 or it in (binding.E4M3, binding.E5M2), (M, N, K, tb, it, p)
+        assert 0 <= p["sk_tiles"] <= p["num_tiles"]
+        assert (p["workspace_bytes"] > 0) == (p["sk_tiles"] > 0), p
+        assert p["stages"] >= 2 and p["smem_bytes"] <= 232448, p
