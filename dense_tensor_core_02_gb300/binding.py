@@ -136,7 +136,10 @@ def gemm_status_string(status: int) -> str:
 
 
 def gemm_poll_device_error(stream=None):
-    """Synchronise ``stream``; return (status, [code, block, site, detail])."""
+    """Synchronise ``stream``; read and clear one status record of the
+    current device (gemm()'s or gemm_noalloc()'s, whichever holds an error;
+    nothing is created or allocated); return (status, [code, block, site,
+    detail])."""
     info = (ctypes.c_int * 4)()
     rc = load_library().gemm_poll_device_error(_stream(stream), info)
     return rc, list(info)

@@ -212,6 +212,17 @@ int device_state(int dev, DeviceState** out) {
     return st.status;
 }
 
+// gemm()'s status record on `dev` if its set-up has run and succeeded,
+// else NULL (nothing is created).
+DeviceStatus* gemm_status_record(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    const DeviceState& st = g_devices[dev];
+    return st.ready && st.status == GEMM_OK ? st.d_status : nullptr;
+}
+
+DeviceStatus* noalloc_status_record(int dev);   // gemm_noalloc()'s, defined with it below
+
 int get_encoder() {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
@@ -1161,26 +1172,33 @@ int gemm_poll_device_error(struct CUstream_st* stream, int* info) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
-    DeviceState* ds = nullptr;
-    int rc = device_state(dev, &ds);
-    if (rc != GEMM_OK) return rc;
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_CUDA;
     }
-    DeviceStatus st{};
-    if (cudaMemcpy(&st, ds->d_status, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) {
-        cudaGetLastError();
-        return GEMM_ERR_CUDA;
-    }
-    if (info) {
-        info[0] = st.code;
-        info[1] = st.block;
-        info[2] = st.site;
-        info[3] = st.detail;
-    }
-    if (st.code != 0) {
-        if (cudaMemset(ds->d_status, 0, sizeof(DeviceStatus)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    // The two records this device may have: gemm()'s (cudaMalloc'd at its
+    // first call) and gemm_noalloc()'s (the static array).  Only records
+    // whose set-up has succeeded are read; none is created here, so a
+    // caller that never lets the library allocate can poll too.
+    DeviceStatus* records[2] = {gemm_status_record(dev), noalloc_status_record(dev)};
+    if (info) info[0] = info[1] = info[2] = info[3] = 0;
+    for (DeviceStatus* rec : records) {
+        if (rec == nullptr) continue;
+        DeviceStatus st{};
+        if (cudaMemcpy(&st, rec, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        if (st.code == 0) continue;
+        if (info) {
+            info[0] = st.code;
+            info[1] = st.block;
+            info[2] = st.site;
+            info[3] = st.detail;
+        }
+        // Clear the record that is reported; a second one, if it also
+        // holds an error, is reported by the next poll.
+        if (cudaMemset(rec, 0, sizeof(DeviceStatus)) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
             cudaGetLastError();
             return GEMM_ERR_CUDA;
         }
@@ -1196,46 +1214,57 @@ int gemm_poll_device_error(struct CUstream_st* stream, int* info) {
 // device memory.  Its set-up (once per device) only queries attributes, sets
 // the kernels' shared-memory limit and looks up the static scratch's device
 // address; each call then validates, encodes the TMA maps on the host
-// stack, clears the status record with a stream-ordered memset and
-// launches.  Nothing on this path calls cudaMalloc, cudaFree or any other
-// allocating routine.
+// stack and launches.  The kernel's status record is the static array's
+// first 16 bytes: zero when the library is loaded, it keeps the first wait
+// that gave up until gemm_poll_device_error() reads and clears it.  Nothing
+// on this path calls cudaMalloc, cudaFree or any other allocating routine.
 
 namespace {
 
 struct NoAllocState {
-    bool ready = false;
-    int status = GEMM_OK;
+    bool ready = false;                       // set-up done and succeeded
     int num_sms = 0;
     DeviceStatus* scratch_status = nullptr;   // device address of the static scratch
 };
 
 NoAllocState g_noalloc[kMaxDevices];
 
+// The one-time set-up of `dev` (the current device).  Only a successful
+// set-up is kept: after a failure the next call tries again.
 int noalloc_device_state(int dev, NoAllocState** out) {
     if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
     NoAllocState& st = g_noalloc[dev];
     if (!st.ready) {
-        st.ready = true;
-        int major = 0, minor = 0;
+        int major = 0, minor = 0, sms = 0, status = GEMM_OK;
         void* scratch = nullptr;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            st.status = GEMM_ERR_CUDA;
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            status = GEMM_ERR_CUDA;
         } else if (major != 10 || minor != 3) {
-            st.status = GEMM_ERR_ARCH;
+            status = GEMM_ERR_ARCH;
         } else if (gb300::prepare_kernels_on_current_device() != cudaSuccess) {
-            st.status = GEMM_ERR_CUDA;
+            status = GEMM_ERR_CUDA;
         } else if (gb300::noalloc_scratch_address(&scratch) != cudaSuccess || scratch == nullptr) {
-            st.status = GEMM_ERR_CUDA;
-        } else {
-            st.scratch_status = static_cast<DeviceStatus*>(scratch);
+            status = GEMM_ERR_CUDA;
         }
-        if (st.status != GEMM_OK) cudaGetLastError();
+        if (status != GEMM_OK) {
+            cudaGetLastError();
+            return status;
+        }
+        st.num_sms = sms;
+        st.scratch_status = static_cast<DeviceStatus*>(scratch);
+        st.ready = true;
     }
     *out = &st;
-    return st.status;
+    return GEMM_OK;
+}
+
+DeviceStatus* noalloc_status_record(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    return g_noalloc[dev].ready ? g_noalloc[dev].scratch_status : nullptr;
 }
 
 }  // namespace
@@ -1281,14 +1310,11 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
     if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
                                in_dtype, out_dtype)) != GEMM_OK)
         return reject(rc, "tensor maps");
+    // The status record keeps the first wait that gave up since the last
+    // gemm_poll_device_error(), which reads and clears it; it is zero when
+    // the library is loaded.
     L.p.status = ns->scratch_status;
-    L.p.skip_first_stage = 0;
-    // The status record must start each call at zero (the kernel records
-    // only the first wait that gives up); stream-ordered, allocates nothing.
-    if (cudaMemsetAsync(L.p.status, 0, sizeof(DeviceStatus), s) != cudaSuccess) {
-        cudaGetLastError();
-        return reject(GEMM_ERR_CUDA, "clearing the static status record");
-    }
+    L.p.skip_first_stage = skip_first_stage_setting();
     GEMM_LOGF("no-alloc: M=%lld N=%lld K=%lld: %s tiles %dx%d (%d), grid %d", (long long)M, (long long)N,
               (long long)K, pl.pair ? "cta-pair" : "1-cta", pl.tile_m, pl.tile_n, pl.num_tiles, pl.grid);
     return launch_described(L, s);

@@ -43,6 +43,14 @@
  * argument error is detected before anything is enqueued, and D is then
  * untouched.  A failure inside the kernel (a pipeline wait that exceeded
  * its time bound) is reported by gemm_poll_device_error().
+ *
+ * Naming: the header is gemm_gb300.h, after the library it declares
+ * (libgemm_gb300.so), rather than a bare gemm.h, so that it cannot be
+ * shadowed by, or shadow, another library's gemm.h on an include path.
+ * The calls, their argument order and the status convention are those of
+ * the planned boundary; the additions are marked where they are declared
+ * (the `info` argument of gemm_poll_device_error, and gemm_mx,
+ * gemm_noalloc, gemm_host and the host-only queries).
  */
 #ifndef GEMM_GB300_H
 #define GEMM_GB300_H
@@ -187,20 +195,50 @@ GEMM_API int gemm_mx(void* D, const void* A, const void* B, const void* C,
                      int transA, int transB, float alpha, float beta,
                      int in_dtype, int out_dtype, struct CUstream_st* stream);
 
-/* A static, human-readable name for a gemm_status_t value (never NULL). */
+/*
+ * A static, human-readable name for a gemm_status_t value (never NULL).
+ *
+ * The status convention stands in for the error path of the TIRx gemm
+ * guide (section 二, "What it accepts", its closing paragraph on dispatch
+ * failure: a variant that cannot take the call raises DispatchFail, and
+ * when no variant can, the reasons are collected into one RuntimeError).  Across a C ABI there are no exceptions, so each
+ * reason the guide gives for refusing a call becomes a negative code,
+ * returned before anything is enqueued, and this call names it.
+ */
 GEMM_API const char* gemm_status_string(int status);
 
 /*
- * Synchronises `stream`, then reads and clears the current device's status
- * block.  Returns GEMM_OK, GEMM_ERR_DEVICE_TIMEOUT when a kernel's pipeline
- * wait exceeded its bound (GEMM_WAIT_TIMEOUT_NS, default 2 s) since the last
- * poll, or GEMM_ERR_CUDA when the stream reports a CUDA error.  When
- * `info` is not NULL it receives four ints: code, block, wait site, detail.
+ * Synchronises `stream`, then reads and clears a status record of the
+ * current device.  The device has up to two: gemm()'s (gemm_mx() and
+ * gemm_host() share it), created by the first gemm() call on the device,
+ * and gemm_noalloc()'s, the static array set up by its first call.  Only
+ * records that exist are read: this call creates nothing and allocates
+ * nothing, so callers of gemm_noalloc() may use it too.  Each record keeps
+ * the first in-kernel wait that gave up (GEMM_WAIT_TIMEOUT_NS, default
+ * 2 s) since it was last cleared; a kernel that gave up stopped early and
+ * left its D partly written.
+ *
+ * Returns GEMM_OK (no record holds an error), GEMM_ERR_DEVICE_TIMEOUT
+ * (one record held a timeout; that record is cleared -- when both hold
+ * one, gemm()'s is reported first and the other by the next poll), or
+ * GEMM_ERR_CUDA when the stream reports a CUDA error.  When `info` is not
+ * NULL it receives four ints: code, block, wait site, detail (all zero
+ * when GEMM_OK is returned).
+ *
+ * Source: the TIRx gemm guide's error path (see gemm_status_string) turns
+ * dispatch failures into errors the caller sees; an asynchronous kernel
+ * can only report after the fact, so this poll is how its failures reach
+ * the caller.  The `info` argument is this library's addition: the
+ * single-argument poll(stream) planned for the boundary gives the code
+ * alone.
  */
 GEMM_API int gemm_poll_device_error(struct CUstream_st* stream, int* info);
 
 /*
  * Host-only query (no GPU needed): the persistent kernel's tile order.
+ * The pages have no counterpart of the host-only queries (this one and the
+ * three below); they expose this library's scheduler and planner so that
+ * tests and callers can check what a call will run without a GPU.
  * For a grid of num_m x num_n output tiles rasterised in groups of group_m
  * tile rows, writes the (m, n) tile coordinates of tile index `tile`.
  * Returns GEMM_OK, or GEMM_ERR_INVALID_ARG for out-of-range arguments.
@@ -273,12 +311,16 @@ GEMM_API int gemm_schedule_units(int num_tiles, int iters, int workers, int sk_t
  *     the kernels' shared-memory limit, and the device address of the
  *     static array via cudaGetSymbolAddress).  Make that first call before
  *     any stream capture.
- *   - All gemm_noalloc() calls on a device share the one status record; each
- *     call clears it (a stream-ordered memset) before its kernel starts.
- *     Calls whose kernels overlap on the GPU (different streams) race on it.
- *   - A pipeline wait that exceeds its time bound stops the kernel early and
- *     is recorded only in that static record: gemm_poll_device_error()
- *     reports the errors of gemm(), not of this call.
+ *   - All gemm_noalloc() calls on a device share the one status record.
+ *     It is zero when the library is loaded and keeps the first pipeline
+ *     wait that gave up (the kernel then stops early, leaving D partly
+ *     written) until gemm_poll_device_error() reads and clears it; no
+ *     gemm_noalloc() call clears it.  Calls whose kernels overlap on the
+ *     GPU (different streams) race on it: a timeout in either is reported,
+ *     but the record says which call's kernel wrote first, not which call
+ *     the caller meant to check.
+ *   - gemm_poll_device_error() reads this record without allocating, so it
+ *     is the way to learn whether a gemm_noalloc() call completed.
  */
 GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, const void* C,
                           int64_t M, int64_t N, int64_t K,

@@ -1,15 +1,32 @@
 """gemm_noalloc(): the allocation-free entry point, against gemm().
 
-Some callers cannot let a library allocate device memory (they own the
-device's memory through their own pool, or run where allocation calls are
-not allowed).  gemm_noalloc() keeps its kernel's scratch in a fixed static
-array instead.  Here it is called through the C ABI twice in a row for each
-problem and both results are compared with gemm()'s on the same inputs,
-within the parity tolerance the other tests use.  gemm_noalloc() is called
-first, so that in a fresh process its one-time per-device set-up runs too.
+Some callers cannot let a library allocate device memory: they own the
+device's memory through their own pool or budget, or they run where CUDA
+allocation calls are not allowed.  gemm_noalloc() keeps its kernel's only
+scratch, the 16-byte status record, in a fixed static array instead of a
+cudaMalloc'd block.  The tests here:
+
+- call it through the C ABI twice in a row for each problem and compare
+  both results with gemm()'s on the same inputs, within the parity
+  tolerance the other tests use (in this pytest process, after the other
+  test files, so gemm() has set the device up long before);
+- run it in a fresh interpreter before any gemm() call, so that its own
+  one-time set-up is what runs, check the result against the oracle, and
+  count with a CUPTI callback every allocation call that reaches the CUDA
+  driver while it runs: none (gemm()'s first call, made afterwards as a
+  control, is seen allocating its status record);
+- make a pipeline wait run out inside a gemm_noalloc() launch (a host-set
+  test hook that leaves one stage unfilled: no fault) and check that
+  gemm_poll_device_error() reports it, clears it, and that the next call
+  is bit-exact.
 
 The file name makes pytest collect it last.
 """
+import json
+import os
+import subprocess
+import sys
+
 import numpy as np
 import pytest
 import torch
@@ -18,6 +35,8 @@ from dense_tensor_core_02_gb300 import binding
 from tests import gpu_helpers as H
 
 pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 PROBLEMS = [
     # (M, N, K, in, out, transA, transB, alpha, beta)
@@ -98,3 +117,197 @@ def test_noalloc_wave_fitted_tiles():
     assert torch.equal(D, ref)
     want, _ = H.oracle_full(A, B, C, M, N, K, transB=1, beta=1.0, in_dtype="bf16")
     H.assert_exact(D.cpu().numpy(), want, "gemm_noalloc on 224-wide tiles")
+
+
+# ---------------------------------------------------------------------------
+# A fresh process: gemm_noalloc() before any gemm().  The child holds its
+# buffers through the CUDA runtime's shared library (not torch), and counts
+# every device-memory allocation call that reaches the CUDA driver with a
+# CUPTI callback (tests/alloc_counter.c, loaded before any CUDA call), so
+# that the library's statically linked runtime is seen too.  gemm()'s first
+# call, which allocates its status record, is the control that shows the
+# counter sees the library's allocations.
+
+_CHILD = r"""
+import ctypes, json, os, sys
+import numpy as np
+sys.path.insert(0, os.environ["REPO_ROOT"])
+out = {}
+counter = None
+if os.environ.get("ALLOC_COUNTER"):
+    counter = ctypes.CDLL(os.environ["ALLOC_COUNTER"])
+    counter.alloc_counter_allocs.restype = ctypes.c_long
+    counter.alloc_counter_frees.restype = ctypes.c_long
+    out["counter_rc"] = counter.alloc_counter_start()
+from dense_tensor_core_02_gb300 import binding
+
+def counts():
+    if counter is None or out.get("counter_rc"):
+        return None
+    return [counter.alloc_counter_allocs(), counter.alloc_counter_frees()]
+
+def cudart():
+    home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    for name in (os.path.join(home, "lib64", "libcudart.so"), "libcudart.so.13", "libcudart.so"):
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            pass
+    raise RuntimeError("the CUDA runtime library was not found")
+
+rt = cudart()
+rt.cudaMalloc.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t]
+rt.cudaMemcpy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+H2D, D2H = 1, 2
+
+def check(rc, what):
+    if rc != 0:
+        raise RuntimeError("%s: CUDA error %d" % (what, rc))
+
+def device_copy(host):
+    p = ctypes.c_void_p()
+    check(rt.cudaMalloc(ctypes.byref(p), host.nbytes), "cudaMalloc")
+    check(rt.cudaMemcpy(p, host.ctypes.data, host.nbytes, H2D), "cudaMemcpy H2D")
+    return p.value
+
+check(rt.cudaSetDevice(0), "cudaSetDevice")
+args = json.loads(sys.argv[1])
+M, N, K = args["M"], args["N"], args["K"]
+A = np.load(args["A"]); B = np.load(args["B"]); C = np.load(args["C"])
+dA, dB, dC = device_copy(A), device_copy(B), device_copy(C)
+D_init = np.full((M, N), np.nan, dtype=np.float32)
+dDs = [device_copy(D_init) for _ in range(4)]
+check(rt.cudaDeviceSynchronize(), "cudaDeviceSynchronize")
+
+# three gemm_noalloc() calls and a poll, before any gemm(); allocation
+# calls counted from just before the first to just after the poll
+out["counts_before"] = counts()
+out["rc"] = []
+for dD in dDs[:3]:
+    out["rc"].append(binding.gemm_noalloc(
+        dD, dA, dB, dC, M, N, K, K, N, N, N, 0, 0, 1.0, 1.0, binding.F16, binding.F32, 0))
+out["poll"] = binding.gemm_poll_device_error(0)[0]
+out["counts_after"] = counts()
+for i, dD in enumerate(dDs[:3]):
+    D = np.empty((M, N), dtype=np.float32)
+    check(rt.cudaMemcpy(D.ctypes.data, dD, D.nbytes, D2H), "cudaMemcpy D2H")
+    np.save(os.path.join(args["out"], "D%d.npy" % i), D)
+# the control: gemm()'s first call on the device allocates its status record
+out["gemm_rc"] = binding.gemm(dDs[3], dA, dB, dC, M, N, K, K, N, N, N, 0, 0, 1.0, 1.0, binding.F16,
+                              binding.F32, 0)
+check(rt.cudaDeviceSynchronize(), "cudaDeviceSynchronize")
+out["counts_after_gemm"] = counts()
+print(json.dumps(out))
+"""
+
+_FRESH_SHAPE = (384, 520, 264)
+
+
+@pytest.fixture(scope="module")
+def fresh_process(tmp_path_factory):
+    """Runs the child once: gemm_noalloc() three times in a fresh
+    interpreter, then the gemm() control.  Returns (report, integer inputs,
+    output directory)."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tmp = tmp_path_factory.mktemp("noalloc_fresh")
+    M, N, K = _FRESH_SHAPE
+    A = H.int_matrix((M, K), -4, 4, "f16", 81)
+    B = H.int_matrix((K, N), -4, 4, "f16", 82)
+    C = H.int_matrix((M, N), -50, 50, "f32", 83)
+    paths = {}
+    for name, x in (("A", A.view(torch.int16)), ("B", B.view(torch.int16)), ("C", C)):
+        paths[name] = str(tmp / ("%s.npy" % name))
+        np.save(paths[name], x.numpy())
+    env = dict(os.environ, REPO_ROOT=ROOT)
+    for k in ("GEMM_TEST_SKIP_FIRST_STAGE", "GEMM_PATH", "GEMM_VARIANT", "ALLOC_COUNTER"):
+        env.pop(k, None)
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    counter = str(tmp / "liballoc_counter.so")
+    build = subprocess.run(["gcc", "-shared", "-fPIC", "-O2", "-std=c99", "-I" + os.path.join(cuda, "include"),
+                            "-o", counter, os.path.join(ROOT, "tests", "alloc_counter.c"),
+                            "-L" + os.path.join(cuda, "lib64"), "-lcupti",
+                            "-Wl,-rpath," + os.path.join(cuda, "lib64")], capture_output=True, text=True)
+    if build.returncode == 0:
+        env["ALLOC_COUNTER"] = counter
+    proc = subprocess.run([sys.executable, "-c", _CHILD, json.dumps(dict(M=M, N=N, K=K, out=str(tmp), **paths))],
+                          env=env, capture_output=True, text=True, timeout=300)
+    assert proc.returncode == 0, proc.stderr[-3000:]
+    report = json.loads(proc.stdout.strip().splitlines()[-1])
+    report["counter_build"] = build.returncode == 0 or build.stderr[-500:]
+    return report, (A, B, C), tmp
+
+
+def test_noalloc_first_in_fresh_process(fresh_process):
+    """In a fresh interpreter, gemm_noalloc() runs before any gemm(): its own
+    one-time set-up runs, the poll reads its record without creating
+    gemm()'s, and the three results are the oracle's bit for bit (integer
+    inputs)."""
+    report, (A, B, C), tmp = fresh_process
+    assert report["rc"] == [0, 0, 0], report
+    assert report["poll"] == 0 and report["gemm_rc"] == 0, report
+    M, N, K = _FRESH_SHAPE
+    want, _ = H.oracle_full(A, B, C, M, N, K, beta=1.0)
+    for i in range(3):
+        H.assert_exact(np.load(str(tmp / ("D%d.npy" % i))), want, "fresh-process gemm_noalloc call %d" % i)
+
+
+def test_noalloc_makes_no_allocation_call(fresh_process):
+    """CUPTI sees no device-memory allocation or release call from the first
+    gemm_noalloc() call (with its set-up) through the third and the poll,
+    and does see the one gemm()'s first call makes."""
+    report, _, _ = fresh_process
+    if report["counter_build"] is not True:
+        pytest.skip("the CUPTI allocation counter did not build: %s" % report["counter_build"])
+    if report.get("counter_rc"):
+        pytest.skip("CUPTI refused the subscription (CUptiResult %d)" % report["counter_rc"])
+    before, after, control = report["counts_before"], report["counts_after"], report["counts_after_gemm"]
+    assert after == before, "gemm_noalloc() made allocation / release calls: %s -> %s" % (before, after)
+    assert control[0] > after[0], "the counter did not see gemm()'s first allocation: %s" % report
+
+
+def test_noalloc_wait_bound_reported_and_cleared():
+    """A stage that is never filled (test hook) makes a wait inside a
+    gemm_noalloc() launch run out: gemm_poll_device_error() reports the
+    timeout from the static record and clears it, and the next call is
+    bit-exact."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    M, N, K = 256, 256, 512
+    dev = torch.device("cuda", 0)
+    A = H.int_matrix((M, K), -4, 4, "f16", 91)
+    B = H.int_matrix((K, N), -4, 4, "f16", 92)
+    Ad, Bd = A.to(dev), B.to(dev)
+    assert H.poll()[0] == 0
+    D = torch.full((M, N), float("nan"), device=dev)
+    with H.env(GEMM_TEST_SKIP_FIRST_STAGE="1", GEMM_WAIT_TIMEOUT_NS="300000000", GEMM_PATH="tcgen05"):
+        assert _call(binding.gemm_noalloc, D, Ad, Bd, None, M, N, K, "f16", "f32", 0, 0, 1.0, 0.0) == 0
+    status, info = H.poll()
+    assert status == binding.GEMM_ERR_DEVICE_TIMEOUT, (status, info)
+    assert info[0] == binding.GEMM_ERR_DEVICE_TIMEOUT and info[2] in (1, 2, 3, 4, 5, 6), info
+    assert H.poll() == (0, [0, 0, 0, 0])      # cleared by the first poll
+    want, _ = H.oracle_full(A, B, None, M, N, K)
+    for i in range(2):
+        D = torch.full((M, N), float("nan"), device=dev)
+        assert _call(binding.gemm_noalloc, D, Ad, Bd, None, M, N, K, "f16", "f32", 0, 0, 1.0, 0.0) == 0
+        assert H.poll()[0] == 0
+        H.assert_exact(D.cpu().numpy(), want, "gemm_noalloc after the timeout, call %d" % (i + 1))
+
+
+def test_both_records_reported_one_per_poll():
+    """A timeout in gemm() and one in gemm_noalloc(), both unpolled: the
+    first poll reports one, the second the other, the third finds none."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    M, N, K = 256, 256, 512
+    dev = torch.device("cuda", 0)
+    Ad = H.int_matrix((M, K), -4, 4, "f16", 93).to(dev)
+    Bd = H.int_matrix((K, N), -4, 4, "f16", 94).to(dev)
+    assert H.poll()[0] == 0
+    D = torch.empty((M, N), device=dev)
+    with H.env(GEMM_TEST_SKIP_FIRST_STAGE="1", GEMM_WAIT_TIMEOUT_NS="300000000", GEMM_PATH="tcgen05"):
+        assert _call(binding.gemm, D, Ad, Bd, None, M, N, K, "f16", "f32", 0, 0, 1.0, 0.0) == 0
+        assert _call(binding.gemm_noalloc, D, Ad, Bd, None, M, N, K, "f16", "f32", 0, 0, 1.0, 0.0) == 0
+    assert H.poll()[0] == binding.GEMM_ERR_DEVICE_TIMEOUT
+    assert H.poll()[0] == binding.GEMM_ERR_DEVICE_TIMEOUT
+    assert H.poll()[0] == 0
