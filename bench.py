@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--case NAME] [--no-e2e] [--no-cpu-baseline]
+                    [--no-per-config] [--no-clock-study] [--cpu-budget SECONDS]
 
 A step is one GEMM call through the C ABI over the resident, seeded
 synthetic inputs of the workload (default: M = N = K = 8192, fp16
@@ -12,9 +13,25 @@ every rank runs its own replica and the slowest rank's time is used.
 
 The roofline's tensor peak is the measured cuBLAS bf16 figure (x 2 for
 8-bit operands) in the power state the timed loop ran in: the sustained
-figure for a loop long enough to meet the power cap (the default 1000
-launches of the 8192^3 workload), the burst figure for a short loop and for
-the separate burst measurement (best of three 10-launch runs).
+figure for a loop long enough to meet the power cap, the burst figure for a
+short loop and for the separate burst measurement (best of three 10-launch
+runs).
+
+At N = 1 the line also carries, outside the timed region:
+  clock_study  the headline workload for >= 1.5 s in chunks of launches,
+               each chunk preceded by a clock probe (a one-block kernel
+               that spins a fixed number of SM clock cycles, timed with
+               CUDA events): launch time against the SM clock it ran at;
+  per_config   every BASELINE workload (10 warm-ups, then >= 50 launches
+               and >= 200 ms, each launch between its own events): median
+               and min per launch, throughput, bound and fraction of the
+               measured peak, and the probed SM clock;
+  cpu_baseline the oracle as it stands on the host cores, single-threaded
+               and on all cores, for every workload: the full problem for
+               the small ones (and 4096^3), a tile-covering sample (one
+               full row per 128-row block, one full column per 256-column
+               block) for the others, with the full time extrapolated from
+               the measured rate and labelled so.
 
 --impl reference times the CPU oracle instead (the only other
 implementation of this operation in the repository), on bounded samples
@@ -124,7 +141,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.QUERY,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -180,8 +197,14 @@ def _args():
     ap.add_argument("--case", default=None, help="workload name (default: the 8192^3 fp16 headline)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--no-clock-study", action="store_true", help="skip the clock study")
+    ap.add_argument("--clock-study-seconds", type=float, default=1.5)
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target wall time of the CPU-baseline sample")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target wall time of the reference arm's per-step samples")
+    ap.add_argument("--cpu-budget", type=float, default=100.0,
+                    help="target wall time of the whole CPU oracle table (all workloads, both thread counts)")
     return ap.parse_args()
 
 
@@ -204,7 +227,81 @@ def _workload_config(case, n_gpus):
 
 
 # ----------------------------------------------------------------------------
+# host-side arithmetic of the measurements (no GPU; tested on the CPU)
+
+
+def tile_covering_entries(M, N, row_block=128, col_block=256):
+    """The tile-covering sample of an M x N output: one full row in every
+    row_block-row block and one full column in every col_block-column block
+    (the row's position within its block varies from block to block, as
+    does the column's), each output element listed once.  Every
+    row_block x col_block output tile holds sampled elements.  Returns
+    (rows, cols) int64 arrays."""
+    import numpy as np
+    pick_r = np.array(sorted({min(M - 1, b * row_block + (b * 53 + 17) % row_block)
+                              for b in range((M + row_block - 1) // row_block)}), dtype=np.int64)
+    pick_c = np.array(sorted({min(N - 1, b * col_block + (b * 97 + 31) % col_block)
+                              for b in range((N + col_block - 1) // col_block)}), dtype=np.int64)
+    r1 = np.repeat(pick_r, N)
+    c1 = np.tile(np.arange(N, dtype=np.int64), len(pick_r))
+    others = np.setdiff1d(np.arange(M, dtype=np.int64), pick_r)
+    r2 = np.tile(others, len(pick_c))
+    c2 = np.repeat(pick_c, len(others))
+    return np.concatenate([r1, r2]), np.concatenate([c1, c2])
+
+
+def every_nth(n_total, n_keep):
+    """Indices of n_keep entries spread evenly over n_total (all when
+    n_keep >= n_total)."""
+    import numpy as np
+    if n_keep >= n_total:
+        return np.arange(n_total, dtype=np.int64)
+    return np.unique(np.linspace(0, n_total - 1, max(1, n_keep)).round().astype(np.int64))
+
+
+def clock_bins(chunks, width_mhz=50.0):
+    """Chunks of launches grouped by the SM clock they ran at.  ``chunks``
+    are dicts with ``mhz`` (probed clock), ``launches`` and ``ms`` (device
+    time of the chunk).  Returns one dict per occupied bin: its clock range,
+    chunk and launch counts, and the mean time per launch in the bin."""
+    bins = {}
+    for c in chunks:
+        b = int(c["mhz"] // width_mhz)
+        e = bins.setdefault(b, {"chunks": 0, "launches": 0, "ms": 0.0, "mhz_sum": 0.0})
+        e["chunks"] += 1
+        e["launches"] += c["launches"]
+        e["ms"] += c["ms"]
+        e["mhz_sum"] += c["mhz"] * c["launches"]
+    out = []
+    for b in sorted(bins):
+        e = bins[b]
+        out.append({"mhz_lo": b * width_mhz, "mhz_hi": (b + 1) * width_mhz, "chunks": e["chunks"],
+                    "launches": e["launches"], "ms_per_launch": e["ms"] / e["launches"],
+                    "mhz_mean": e["mhz_sum"] / e["launches"]})
+    return out
+
+
+def roofline_of(flops, nbytes, seconds, tensor_peak_tflops, hbm_gbs):
+    """The bound of one launch of `flops` flops moving `nbytes` algorithmic
+    bytes, and the fraction of that bound reached in `seconds`: "tensor"
+    when the arithmetic intensity is at or above the ridge point (peak flop/s
+    over copy bandwidth), else "hbm"; "latency" is added as the limit when
+    the roofline time is under 3 us (launch latency dominates)."""
+    t_tensor = flops / (tensor_peak_tflops * 1e12)
+    t_hbm = nbytes / (hbm_gbs * 1e9)
+    bound = "tensor" if t_tensor >= t_hbm else "hbm"
+    ideal = max(t_tensor, t_hbm)
+    out = {"bound": bound, "frac": ideal / seconds if seconds > 0 else None, "ideal_us": ideal * 1e6}
+    if ideal < 3e-6:
+        out["limited_by"] = "latency"
+    return out
+
+
+# ----------------------------------------------------------------------------
 # CPU oracle timing (the cpu_baseline leg and the reference arm)
+
+
+_CODE = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
 
 
 def _oracle_sampler(case):
@@ -219,7 +316,6 @@ def _oracle_sampler(case):
     sf = dict(zip(("sfa", "sfb"), (x.numpy() for x in make_scales(case)))) if case.mx else {}
     threads = len(os.sched_getaffinity(0))
     rng = np.random.default_rng(case.seed)
-    code = {"f16": 0, "bf16": 1, "f32": 2, "e4m3": 3, "e5m2": 4, "e2m1": 5}
 
     def run(n):
         rows = rng.integers(0, case.M, size=n)
@@ -227,7 +323,7 @@ def _oracle_sampler(case):
         t0 = time.perf_counter()
         oracle.gemm_entries(A, B, C, case.M, case.N, case.K, rows, cols, transA=case.transA,
                             transB=case.transB, alpha=case.alpha, beta=case.beta,
-                            in_dtype=code[case.in_dtype], c_dtype=code[case.out_dtype], threads=threads, **sf)
+                            in_dtype=_CODE[case.in_dtype], c_dtype=_CODE[case.out_dtype], threads=threads, **sf)
         return time.perf_counter() - t0
 
     return run, threads
@@ -242,7 +338,76 @@ def _calibrate(run, threads, target_s):
         n *= 4
 
 
+# Workloads whose full problem the CPU table times (BASELINE order, 1-based):
+# the single atom, 512^3, 4096^3 and 1000^3; the others are timed on the
+# tile-covering sample.
+CPU_FULL_PROBLEM = (1, 2, 3, 10)
+
+
+def cpu_oracle_timings(case, index, A, B, C, threads, budget_s):
+    """The oracle as it stands on this workload, on one thread and on
+    `threads` threads: the full problem (CPU_FULL_PROBLEM) or the
+    tile-covering sample.  A run whose projected time exceeds its share of
+    `budget_s` is cut to an evenly spread subset (rows of the full problem,
+    entries of the sample); the full problem's time is then extrapolated
+    from the measured rate and labelled "extrapolated"."""
+    import numpy as np
+
+    import oracle.oracle as oracle
+    kw = dict(transA=case.transA, transB=case.transB, alpha=case.alpha, beta=case.beta,
+              in_dtype=_CODE[case.in_dtype], c_dtype=_CODE[case.out_dtype])
+    full = index in CPU_FULL_PROBLEM
+    flop_per_entry = 2.0 * case.K
+    full_flops = float(case.flops)
+    # single-threaded calibration on a few entries: the per-thread rate
+    rng = np.random.default_rng(case.seed)
+    n_cal = int(max(16, min(case.M * case.N, 2e7 / max(flop_per_entry, 1.0))))
+    cr, cc = rng.integers(0, case.M, n_cal), rng.integers(0, case.N, n_cal)
+    t0 = time.perf_counter()
+    oracle.gemm_entries(A, B, C, case.M, case.N, case.K, cr, cc, threads=1, **kw)
+    rate1 = n_cal * flop_per_entry / max(time.perf_counter() - t0, 1e-9)
+    # shares of the budget per run: the full 4096^3 problem on all cores
+    # 40 %, the other all-core runs 6 % each; one thread: 8 % for a full
+    # problem, 2 % for a sample
+    caps = {"all": budget_s * (0.40 if index == 3 else 0.06), "single": budget_s * (0.08 if full else 0.02)}
+    if not full:
+        rows_s, cols_s = tile_covering_entries(case.M, case.N)
+        sample_desc = ("tile-covering sample: one full row per 128-row block and one full column per "
+                       "256-column block (%d output elements)" % len(rows_s))
+    out = {"workload": case.name, "index": index, "threads_all": threads,
+           "work": "full problem" if full else sample_desc}
+    for label, nthr in (("single_thread", 1), ("all_cores", threads)):
+        rate_guess = rate1 * (nthr if nthr == 1 else 0.8 * nthr)
+        if full:
+            rows_needed = case.M
+            flops_row = 2.0 * case.N * case.K
+            keep = int(min(rows_needed, max(1, caps["all" if nthr > 1 else "single"] * rate_guess / flops_row)))
+            t0 = time.perf_counter()
+            oracle.gemm(A, B, C, case.M, case.N, case.K, rows=(0, keep), threads=nthr, **kw)
+            sec = time.perf_counter() - t0
+            done = keep * flops_row
+            what = "the full problem" if keep == rows_needed else "rows 0..%d of %d of the full problem" % (
+                keep, rows_needed)
+        else:
+            n_all = len(rows_s)
+            keep = int(min(n_all, max(nthr * 4, caps["all" if nthr > 1 else "single"] * rate_guess /
+                                      flop_per_entry)))
+            idx = every_nth(n_all, keep)
+            t0 = time.perf_counter()
+            oracle.gemm_entries(A, B, C, case.M, case.N, case.K, rows_s[idx], cols_s[idx], threads=nthr, **kw)
+            sec = time.perf_counter() - t0
+            done = len(idx) * flop_per_entry
+            what = "the whole sample" if len(idx) == n_all else "%d of its elements, evenly spread" % len(idx)
+        rate = done / sec
+        out[label] = {"threads": nthr, "measured_on": what, "seconds": sec, "gflops": rate / 1e9,
+                      "full_problem_seconds": full_flops / rate,
+                      "full_problem_seconds_kind": "measured" if (full and done == full_flops) else "extrapolated"}
+    return out
+
+
 def cpu_baseline(case, target_s):
+    """The reference-arm style figure: random output elements of `case` on
+    all host cores for about target_s seconds."""
     run, threads = _oracle_sampler(case)
     n, _ = _calibrate(run, threads, target_s)
     t = run(n)
@@ -284,12 +449,223 @@ def run_reference(args, case):
 # ----------------------------------------------------------------------------
 # the CUDA path
 
+CLOCK_PROBE_CYCLES = 200000     # SM clock cycles one probe spins (about 0.1 ms)
+CLOCK_CHUNK = 16                # launches between two probes in the clock study
+FLUSH_BYTES = 256 << 20         # the L2 flush write (L2 is 129 MB)
+
+
+def _probe_pair(torch):
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def _probe(torch, stream, pair):
+    """Enqueue a clock probe: one block spinning CLOCK_PROBE_CYCLES SM
+    cycles between the two events of `pair`."""
+    pair[0].record(stream)
+    torch.cuda._sleep(CLOCK_PROBE_CYCLES)
+    pair[1].record(stream)
+
+
+def _probe_mhz(pair):
+    ms = pair[0].elapsed_time(pair[1])
+    return CLOCK_PROBE_CYCLES / (ms * 1e3) if ms > 0 else None
+
+
+class _Workload:
+    """One workload's device buffers and its launch through the C ABI."""
+
+    def __init__(self, case, dev, host=None):
+        import torch
+
+        from dense_tensor_core_02_gb300 import binding
+        from dense_tensor_core_02_gb300.inputs import make_inputs, make_scales
+        self.case, self.binding = case, binding
+        self.code = {"f16": binding.F16, "bf16": binding.BF16, "f32": binding.F32, "e4m3": binding.E4M3,
+                     "e5m2": binding.E5M2, "e2m1": binding.E2M1}
+        self.epu = 2 if case.in_dtype == "e2m1" else 1   # operand elements per stored byte (packed fp4)
+        self.A, self.B, self.C = host if host is not None else make_inputs(case)
+        self.SFA, self.SFB = make_scales(case) if case.mx else (None, None)
+        self.Ad, self.Bd = self.A.to(dev), self.B.to(dev)
+        self.Cd = self.C.to(dev) if self.C is not None else None
+        self.SFAd = self.SFA.to(dev) if self.SFA is not None else None
+        self.SFBd = self.SFB.to(dev) if self.SFB is not None else None
+        self.otype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[case.out_dtype]
+        self.Dd = torch.empty((case.M, case.N), dtype=self.otype, device=dev)
+        # launches per step: gemm_mx rearranges both operands' scales first (one launch)
+        self.launches_per_step = 2 if case.mx else 1
+
+    def call(self, D_, A_, B_, C_, SFA_, SFB_, s_ptr):
+        case, b = self.case, self.binding
+        if case.mx:
+            rc = b.gemm_mx(D_, A_, B_, C_, SFA_, SFB_, case.M, case.N, case.K, A_.stride(0) * self.epu,
+                           B_.stride(0) * self.epu, C_.stride(0) if C_ is not None else case.N, D_.stride(0),
+                           SFA_.stride(0), SFB_.stride(0), case.transA, case.transB, case.alpha, case.beta,
+                           self.code[case.in_dtype], self.code[case.out_dtype], s_ptr)
+        else:
+            rc = b.gemm(D_, A_, B_, C_, case.M, case.N, case.K, A_.stride(0), B_.stride(0),
+                        C_.stride(0) if C_ is not None else case.N, D_.stride(0), case.transA, case.transB,
+                        case.alpha, case.beta, self.code[case.in_dtype], self.code[case.out_dtype], s_ptr)
+        if rc != 0:
+            raise RuntimeError("gemm: %s" % b.gemm_status_string(rc))
+
+    def step(self, s_ptr):
+        self.call(self.Dd, self.Ad, self.Bd, self.Cd, self.SFAd, self.SFBd, s_ptr)
+
+
+def clock_study(torch, wl, stream, dev, seconds, num_sms, rate):
+    """The workload back to back for about `seconds`, in chunks of
+    CLOCK_CHUNK launches, each chunk preceded by a clock probe: per chunk the
+    device time per launch and the SM clock it ran at (the mean of the probes
+    before and after it).  Returns the chunk table's summary and bins."""
+    sptr = stream.cuda_stream
+    # estimate the chunk count from one chunk
+    e0, e1 = _probe_pair(torch)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(CLOCK_CHUNK):
+            wl.step(sptr)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    chunk_ms = max(e0.elapsed_time(e1), 1e-3)
+    n_chunks = max(8, min(4000, int(seconds * 1e3 / chunk_ms)))
+    probes = [_probe_pair(torch) for _ in range(n_chunks + 1)]
+    spans = [_probe_pair(torch) for _ in range(n_chunks)]
+    with torch.cuda.stream(stream):
+        for c in range(n_chunks):
+            _probe(torch, stream, probes[c])
+            spans[c][0].record(stream)
+            for _ in range(CLOCK_CHUNK):
+                wl.step(sptr)
+            spans[c][1].record(stream)
+        _probe(torch, stream, probes[n_chunks])
+    torch.cuda.synchronize(dev)
+    chunks = []
+    for c in range(n_chunks):
+        f0, f1 = _probe_mhz(probes[c]), _probe_mhz(probes[c + 1])
+        if f0 is None or f1 is None:
+            continue
+        chunks.append({"mhz": 0.5 * (f0 + f1), "launches": CLOCK_CHUNK, "ms": spans[c][0].elapsed_time(spans[c][1])})
+    flops = wl.case.flops
+    ideal_cycles = flops / (num_sms * FLOP_PER_CLK_PER_SM * rate)
+    total_ms = sum(c["ms"] for c in chunks)
+    launches = sum(c["launches"] for c in chunks)
+    mhz = [c["mhz"] for c in chunks]
+    cyc = [c["ms"] / c["launches"] * 1e-3 * c["mhz"] * 1e6 for c in chunks]
+    med_mhz = statistics.median(mhz)
+    ms_per_launch = total_ms / launches
+    achieved = flops / (ms_per_launch * 1e-3) / 1e12
+    bins = clock_bins(chunks)
+    for b in bins:
+        t = b["ms_per_launch"] * 1e-3
+        b["tflops"] = flops / t / 1e12
+        b["cycles_per_launch"] = t * b["mhz_mean"] * 1e6
+        b["frac_of_clock_peak"] = ideal_cycles / b["cycles_per_launch"]
+    first = chunks[0]
+    return {
+        "launches": launches, "chunks": len(chunks), "seconds": total_ms * 1e-3,
+        "probe": "torch.cuda._sleep(%d cycles) on one block between chunks of %d launches, timed by CUDA events "
+                 "on the launching stream; a chunk's clock is the mean of the probes around it" % (
+                     CLOCK_PROBE_CYCLES, CLOCK_CHUNK),
+        "ms_per_launch": ms_per_launch, "tflops": achieved,
+        "sm_mhz_median": med_mhz, "sm_mhz_min": min(mhz), "sm_mhz_max": max(mhz),
+        "clock_peak_tflops_at_median": num_sms * FLOP_PER_CLK_PER_SM * rate * med_mhz * 1e6 / 1e12,
+        "frac_of_clock_peak": achieved / (num_sms * FLOP_PER_CLK_PER_SM * rate * med_mhz * 1e6 / 1e12),
+        "cycles_per_launch_median": statistics.median(cyc), "ideal_cycles_per_launch": ideal_cycles,
+        "first_chunk": {"sm_mhz": first["mhz"], "ms_per_launch": first["ms"] / first["launches"],
+                        "frac_of_clock_peak": ideal_cycles / (first["ms"] / first["launches"] * 1e-3 *
+                                                              first["mhz"] * 1e6)},
+        "bins": bins,
+    }
+
+
+def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, cpu=None):
+    """One BASELINE workload: 10 warm-ups, then >= 50 launches and >= 200 ms.
+    Workloads larger than L2 run back to back in 5 groups between events
+    (median and min over the groups' time per launch); workloads that fit
+    in L2 get an L2 flush before every launch, each launch between its own
+    events (median and min over launches).  A clock probe before and after."""
+    wl = _Workload(case, dev)
+    sptr = stream.cuda_stream
+    fits_l2 = case.algorithmic_bytes <= 129e6
+    w0, w1 = _probe_pair(torch)
+    with torch.cuda.stream(stream):
+        w0.record(stream)
+        for _ in range(10):
+            wl.step(sptr)
+        w1.record(stream)
+    torch.cuda.synchronize(dev)
+    est_ms = max(w0.elapsed_time(w1) / 10, 1e-3)
+    n = int(min(5000, max(50, 200.0 / est_ms)))
+    p0, p1 = _probe_pair(torch), _probe_pair(torch)
+    with torch.cuda.stream(stream):
+        _probe(torch, stream, p0)
+        if fits_l2:
+            spans = [_probe_pair(torch) for _ in range(n)]
+            for a, b in spans:
+                flush.zero_()
+                a.record(stream)
+                wl.step(sptr)
+                b.record(stream)
+        else:
+            groups = 5
+            per = (n + groups - 1) // groups
+            spans = [_probe_pair(torch) for _ in range(groups)]
+            for a, b in spans:
+                a.record(stream)
+                for _ in range(per):
+                    wl.step(sptr)
+                b.record(stream)
+        _probe(torch, stream, p1)
+    torch.cuda.synchronize(dev)
+    status, info = wl.binding.gemm_poll_device_error(stream)
+    if status != 0:
+        raise RuntimeError("device status after %s: %s %s" % (case.name, wl.binding.gemm_status_string(status),
+                                                               info))
+    if fits_l2:
+        per_launch = [a.elapsed_time(b) for a, b in spans]
+        launches = n
+    else:
+        per_launch = [a.elapsed_time(b) / per for a, b in spans]
+        launches = per * len(spans)
+    med, mn = statistics.median(per_launch), min(per_launch)
+    rate = FP8_RATE if case.in_dtype in ("e4m3", "e5m2", "e2m1") else 1.0
+    peak_burst = float(peaks["bf16_tflops"]) * rate
+    hbm = float(peaks["hbm_gbs"])
+    roof = roofline_of(case.flops, case.algorithmic_bytes, med * 1e-3, peak_burst, hbm)
+    mhz = [m for m in (_probe_mhz(p0), _probe_mhz(p1)) if m]
+    row = {
+        "index": index, "workload": case.name,
+        "M": case.M, "N": case.N, "K": case.K, "in_dtype": case.in_dtype, "out_dtype": case.out_dtype,
+        "alpha": case.alpha, "beta": case.beta, "transA": case.transA, "transB": case.transB,
+        "launches": launches, "timing": ("each launch between its own events after a 256 MB L2 flush"
+                                         if fits_l2 else "5 groups of back-to-back launches between events"),
+        "us_median": med * 1e3, "us_min": mn * 1e3,
+        "tflops_median": case.flops / (med * 1e-3) / 1e12, "tflops_best": case.flops / (mn * 1e-3) / 1e12,
+        "gbs_median": case.algorithmic_bytes / (med * 1e-3) / 1e9,
+        "algorithmic_flops": case.flops, "algorithmic_bytes": case.algorithmic_bytes,
+        "bound": roof["bound"], "frac": roof["frac"], "roofline_ideal_us": roof["ideal_us"],
+        "peak": peak_burst if roof["bound"] == "tensor" else hbm,
+        "peak_unit": UNIT if roof["bound"] == "tensor" else "GB/s",
+        "peak_kind": ("measured bf16 burst (cuBLAS)" + ("" if rate == 1.0 else " x 2, nominal fp8 / bf16 ratio"))
+        if roof["bound"] == "tensor" else "measured HBM copy bandwidth",
+        "sm_mhz_probed": statistics.mean(mhz) if mhz else None,
+        "traffic": _profiled_traffic(case.name),
+    }
+    if "limited_by" in roof:
+        row["limited_by"] = roof["limited_by"]
+    if mhz and roof["bound"] == "tensor":
+        row["frac_of_clock_peak"] = row["tflops_median"] / (
+            num_sms * FLOP_PER_CLK_PER_SM * rate * statistics.mean(mhz) * 1e6 / 1e12)
+    host = (wl.A, wl.B, wl.C)
+    del wl
+    return row, host
+
 
 def run_ours(args, case):
     import torch
 
     from dense_tensor_core_02_gb300 import binding
-    from dense_tensor_core_02_gb300.inputs import make_inputs, make_scales
+    from dense_tensor_core_02_gb300.inputs import CASES
 
     rank, world, local_rank = _rank_info()
     dist = None
@@ -301,41 +677,16 @@ def run_ours(args, case):
     torch.cuda.set_device(dev)
     binding.load_library()
 
-    code = {"f16": binding.F16, "bf16": binding.BF16, "f32": binding.F32, "e4m3": binding.E4M3,
-            "e5m2": binding.E5M2, "e2m1": binding.E2M1}
-    epu = 2 if case.in_dtype == "e2m1" else 1   # operand elements per stored byte (packed fp4)
-    A, B, C = make_inputs(case)
-    Ad, Bd = A.to(dev), B.to(dev)
-    Cd = C.to(dev) if C is not None else None
-    SFA, SFB = make_scales(case) if case.mx else (None, None)
-    SFAd = SFA.to(dev) if SFA is not None else None
-    SFBd = SFB.to(dev) if SFB is not None else None
-    # launches per step: gemm_mx rearranges both operands' scales first (one launch)
-    launches_per_step = 2 if case.mx else 1
-    otype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[case.out_dtype]
-    Dd = torch.empty((case.M, case.N), dtype=otype, device=dev)
+    wl = _Workload(case, dev)
+    A, B, C, SFA, SFB = wl.A, wl.B, wl.C, wl.SFA, wl.SFB
+    Dd, otype = wl.Dd, wl.otype
     stream = torch.cuda.Stream(dev)
     sptr = stream.cuda_stream
-    ldc = Cd.stride(0) if Cd is not None else case.N
     small = case.algorithmic_bytes <= 129e6
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if small else None
-
-    def call(D_, A_, B_, C_, SFA_, SFB_, s_ptr):
-        if case.mx:
-            rc = binding.gemm_mx(D_, A_, B_, C_, SFA_, SFB_, case.M, case.N, case.K, A_.stride(0) * epu,
-                                 B_.stride(0) * epu,
-                                 C_.stride(0) if C_ is not None else case.N, D_.stride(0), SFA_.stride(0),
-                                 SFB_.stride(0), case.transA, case.transB, case.alpha, case.beta,
-                                 code[case.in_dtype], code[case.out_dtype], s_ptr)
-        else:
-            rc = binding.gemm(D_, A_, B_, C_, case.M, case.N, case.K, A_.stride(0), B_.stride(0),
-                              C_.stride(0) if C_ is not None else case.N, D_.stride(0), case.transA, case.transB,
-                              case.alpha, case.beta, code[case.in_dtype], code[case.out_dtype], s_ptr)
-        if rc != 0:
-            raise RuntimeError("gemm: %s" % binding.gemm_status_string(rc))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step():
-        call(Dd, Ad, Bd, Cd, SFAd, SFBd, sptr)
+        wl.step(sptr)
 
     def barrier():
         if dist is not None:
@@ -354,7 +705,7 @@ def run_ours(args, case):
         fit in L2 get a flush (a 256 MB write) before every launch, outside
         the timed spans: each launch is bracketed by its own event pair."""
         with torch.cuda.stream(stream):
-            if flush is None:
+            if not small:
                 e0.record(stream)
                 for _ in range(n):
                     step()
@@ -368,14 +719,21 @@ def run_ours(args, case):
                     step()
                     b.record(stream)
         torch.cuda.synchronize(dev)
-        return e0.elapsed_time(e1) if flush is None else sum(a.elapsed_time(b) for a, b in spans)
+        return e0.elapsed_time(e1) if not small else sum(a.elapsed_time(b) for a, b in spans)
 
     # burst: the best of three runs of BURST_STEPS launches, measured the way
-    # the burst peak is (a short run, before the power cap sets in); the
-    # headline is the long run below, reported against both peaks
+    # the burst peak is (a short run, before the power cap sets in), each
+    # with a clock probe before it; the headline is the run below
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    burst_ms = min(timed(BURST_STEPS) for _ in range(3)) / BURST_STEPS
+    burst_runs = []
+    for _ in range(3):
+        pp = _probe_pair(torch)
+        with torch.cuda.stream(stream):
+            _probe(torch, stream, pp)
+        burst_runs.append((timed(BURST_STEPS) / BURST_STEPS, _probe_mhz(pp)))
+        time.sleep(0.2)   # let the power state settle back between runs
+    burst_ms, burst_mhz = min(burst_runs, key=lambda r: r[0])
 
     sampler = ClockSampler(local_rank).start() if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
@@ -383,7 +741,17 @@ def run_ours(args, case):
     torch.cuda.synchronize(dev)
     elapsed_ms = timed(args.steps)
     barrier()
+    # the clock study runs right after the timed region, on rank 0 at N = 1,
+    # with the sampler still running (its samples then cover both)
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rate = FP8_RATE if case.in_dtype in ("e4m3", "e5m2", "e2m1") else 1.0
+    study = None
+    if world == 1 and not args.no_clock_study and not small:
+        study = clock_study(torch, wl, stream, dev, args.clock_study_seconds, num_sms, rate)
     clocks = sampler.stop() if sampler else None
+    if clocks is not None:
+        clocks["window"] = ("the timed region (%.0f ms)%s" % (
+            elapsed_ms, " and the clock study after it (%.1f s)" % study["seconds"] if study else ""))
     status, info = binding.gemm_poll_device_error(stream)
     if status != 0:
         raise RuntimeError("device status after timing: %s %s" % (binding.gemm_status_string(status), info))
@@ -422,13 +790,13 @@ def run_ours(args, case):
                     for d_, h_ in ((dA, hA), (dB, hB), (dC, hC), (dSA, hSFA), (dSB, hSFB)):
                         if d_ is not None:
                             d_.copy_(h_, non_blocking=True)
-                    call(dD, dA, dB, dC, dSA, dSB, s_i.cuda_stream)
+                    wl.call(dD, dA, dB, dC, dSA, dSB, s_i.cuda_stream)
                     hD.copy_(dD, non_blocking=True)
                 return
             rc = binding.gemm_host(hD, hA, hB, hC, case.M, case.N, case.K, hA.stride(0), hB.stride(0),
                                    hC.stride(0) if hC is not None else case.N, hD.stride(0), case.transA,
-                                   case.transB, case.alpha, case.beta, code[case.in_dtype],
-                                   code[case.out_dtype], s_i.cuda_stream)
+                                   case.transB, case.alpha, case.beta, wl.code[case.in_dtype],
+                                   wl.code[case.out_dtype], s_i.cuda_stream)
             if rc != 0:
                 raise RuntimeError("gemm_host: %s" % binding.gemm_status_string(rc))
 
@@ -464,6 +832,7 @@ def run_ours(args, case):
                        "alternating between %d streams" if case.mx else
                        "gemm_host (pinned host buffers; copies pipelined with the products over row panels; "
                        "steps alternate between %d streams)") % len(streams)}
+        del hA, hB, hC, hDs, streams
 
     if rank != 0:
         if dist is not None:
@@ -471,28 +840,25 @@ def run_ours(args, case):
         return 0
 
     peaks, peak_src = _measured_peaks()
-    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     achieved = case.flops / (per_launch_ms * 1e-3) / 1e12
     # 8-bit operands: no measured fp8 peak exists, so the measured bf16 figures
     # are scaled by the nominal dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s).
     # Packed 4-bit operands run on the same kind::mxf8f6f4 instruction as the
     # 8-bit ones (K = 32 per instruction), so their peak is the 8-bit one.
-    rate = FP8_RATE if case.in_dtype in ("e4m3", "e5m2", "e2m1") else 1.0
     peak_burst = float(peaks["bf16_tflops"]) * rate
     peak_sustained = float(peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])) * rate
     # The measured peaks come as a burst (a short cuBLAS run, clocks up) and a
     # sustained figure (seconds of back-to-back cuBLAS under the power cap).
     # The timed loop is held to the same condition as its denominator: a loop
-    # that ran long enough to meet the power cap (>= 0.5 s, or sw_power_cap
-    # seen while it ran) is compared with the sustained peak; a short loop, and
-    # the burst figure, with the burst peak.
-    power_capped = elapsed_ms >= 500.0 or bool(clocks and "sw_power_cap" in clocks.get("reasons", []))
+    # that ran long enough to meet the power cap (>= 0.5 s) is compared with
+    # the sustained peak; a short loop, and the burst figure, with the burst
+    # peak.
+    power_capped = elapsed_ms >= 500.0
     peak = peak_sustained if power_capped else peak_burst
     kind = "sustained" if power_capped else "burst"
-    src = ("%s bf16 %s (cuBLAS 8192^3, MEASURED_PEAKS.json)%s; this loop: %d launches in %.0f ms%s" % (
+    src = ("%s bf16 %s (cuBLAS 8192^3, MEASURED_PEAKS.json)%s; this loop: %d launches in %.0f ms" % (
         peak_src, kind, "; f16 runs at the bf16 rate" if rate == 1.0 else
-        " x 2, the nominal dense fp8 / bf16 ratio", args.steps, elapsed_ms,
-        ", sw_power_cap active" if clocks and "sw_power_cap" in clocks.get("reasons", []) else ""))
+        " x 2, the nominal dense fp8 / bf16 ratio", args.steps, elapsed_ms))
     achieved_gbs = case.algorithmic_bytes / (per_launch_ms * 1e-3) / 1e9
     hbm = float(peaks["hbm_gbs"])
     # the bound: below the ridge (peak flop/s / copy bandwidth) the algorithmic
@@ -516,26 +882,67 @@ def run_ours(args, case):
     roofline.update({"traffic": _profiled_traffic(case.name), "arithmetic_intensity": intensity,
                      "ridge_flop_per_byte": ridge, "algorithmic_flops_per_launch": case.flops,
                      "algorithmic_bytes_per_launch": case.algorithmic_bytes, "achieved_gbs": achieved_gbs})
-    roofline["burst"] = dict(burst, launches=BURST_STEPS, best_of=3, ms_per_launch=burst_ms)
+    roofline["burst"] = dict(burst, launches=BURST_STEPS, best_of=3, ms_per_launch=burst_ms, sm_mhz_probed=burst_mhz)
     if case.mx:
         roofline["note"] = ("block-scaled: the time per launch is that of the whole gemm_mx step, the two small "
                             "scale-rearranging launches included" +
                             ("; packed E2M1 runs on kind::mxf8f6f4 at the 8-bit instruction rate, so the peak is "
                              "the 8-bit one" if case.in_dtype == "e2m1" else ""))
-    if clocks and clocks.get("sm_mhz") and roofline["bound"] == "tensor":
-        clk_peak = num_sms * FLOP_PER_CLK_PER_SM * rate * clocks["sm_mhz"] * 1e6 / 1e12
-        roofline["frac_of_clock_peak"] = achieved / clk_peak
-        roofline["clock_peak_tflops"] = clk_peak
+    if roofline["bound"] == "tensor":
+        # the dense peak at the clock the launches ran at: n_SM x 8192 flop/clk x f
+        # (x 2 for 8-bit operands), with f from the clock probes -- the one before
+        # the burst runs for the burst figure, the clock study's median for the loop
+        if burst_mhz:
+            roofline["burst"]["frac_of_clock_peak"] = burst_tflops / (
+                num_sms * FLOP_PER_CLK_PER_SM * rate * burst_mhz * 1e6 / 1e12)
+        if study:
+            roofline["frac_of_clock_peak"] = study["frac_of_clock_peak"]
+            roofline["clock_peak_tflops"] = study["clock_peak_tflops_at_median"]
+            roofline["clock_source"] = "clock study median (%d chunks, %.0f MHz)" % (study["chunks"],
+                                                                                  study["sm_mhz_median"])
     roofline["max_clock_peak_tflops"] = num_sms * FLOP_PER_CLK_PER_SM * rate * 2070e6 / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": per_launch_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": case.in_dtype, "data": "synthetic",
         "config": _workload_config(case, world), "roofline": roofline,
-        "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps * launches_per_step, "num_sms": num_sms,
+        "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps * wl.launches_per_step, "num_sms": num_sms,
     }
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    if study:
+        line["clock_study"] = study
+    del wl
+
+    # every BASELINE workload, and the CPU oracle on the same inputs
+    per_config, cpu_rows = [], []
+    want_cpu = not args.no_cpu_baseline and world == 1
+    if world == 1 and not args.no_per_config:
+        for i, c in enumerate(CASES[:10]):
+            row, host = per_config_row(torch, c, i + 1, dev, stream, peaks, num_sms, flush)
+            per_config.append(row)
+            if want_cpu:
+                cpu_rows.append(cpu_oracle_timings(c, i + 1, *host, threads=len(os.sched_getaffinity(0)),
+                                                   budget_s=args.cpu_budget))
+            del host
+        line["per_config"] = per_config
+    if want_cpu:
+        head = next((r for r in cpu_rows if r["workload"] == case.name), None)
+        if head is None:
+            from dense_tensor_core_02_gb300.inputs import make_inputs
+            head = cpu_oracle_timings(case, CASES.index(case) + 1, *make_inputs(case),
+                                      threads=len(os.sched_getaffinity(0)), budget_s=args.cpu_budget)
+        allc, one = head["all_cores"], head["single_thread"]
+        line["cpu_baseline"] = {
+            "value": allc["gflops"] / 1e3, "unit": UNIT, "cores": allc["threads"], "kind": "oracle",
+            "sample": "%s of %s: %s, on %d threads (%.1f s)" % (head["work"], case.name, allc["measured_on"],
+                                                                 allc["threads"], allc["seconds"]),
+            "single_thread_value": one["gflops"] / 1e3,
+            "single_thread_sample": "%s, on 1 thread (%.1f s)" % (one["measured_on"], one["seconds"]),
+            "full_problem_seconds_all_cores": allc["full_problem_seconds"],
+            "full_problem_seconds_all_cores_kind": allc["full_problem_seconds_kind"],
+            "full_problem_seconds_single_thread": one["full_problem_seconds"],
+            "full_problem_seconds_single_thread_kind": one["full_problem_seconds_kind"],
+            "per_config": cpu_rows,
+        }
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
