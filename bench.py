@@ -450,25 +450,56 @@ def run_reference(args, case):
 # the CUDA path
 
 CLOCK_PROBE_CYCLES = 200000     # SM clock cycles one probe spins (about 0.1 ms)
+CLOCK_PROBE_SHORT = 50000       # the short probe of the overhead calibration
 CLOCK_CHUNK = 16                # launches between two probes in the clock study
 FLUSH_BYTES = 256 << 20         # the L2 flush write (L2 is 129 MB)
+
+# Launch overhead (ms) inside a probe's event pair, measured once on the idle
+# GPU by clock_probe_calibrate(); subtracted from every probe's time.
+_probe_overhead_ms = 0.0
 
 
 def _probe_pair(torch):
     return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
 
-def _probe(torch, stream, pair):
-    """Enqueue a clock probe: one block spinning CLOCK_PROBE_CYCLES SM
-    cycles between the two events of `pair`."""
+def _probe(torch, stream, pair, cycles=CLOCK_PROBE_CYCLES):
+    """Enqueue a clock probe: one block spinning `cycles` SM cycles between
+    the two events of `pair`."""
     pair[0].record(stream)
-    torch.cuda._sleep(CLOCK_PROBE_CYCLES)
+    torch.cuda._sleep(cycles)
     pair[1].record(stream)
 
 
-def _probe_mhz(pair):
-    ms = pair[0].elapsed_time(pair[1])
-    return CLOCK_PROBE_CYCLES / (ms * 1e3) if ms > 0 else None
+def _probe_mhz(pair, cycles=CLOCK_PROBE_CYCLES):
+    ms = pair[0].elapsed_time(pair[1]) - _probe_overhead_ms
+    return cycles / (ms * 1e3) if ms > 0 else None
+
+
+def clock_probe_calibrate(torch, stream, dev):
+    """A probe's event pair also holds the launch of its spin kernel.  On
+    the idle GPU (one clock) a long and a short probe give both terms:
+    t = overhead + cycles / f.  Sets the overhead the probes subtract and
+    returns it with the idle clock."""
+    global _probe_overhead_ms
+    fits = []
+    for _ in range(3):
+        lp, sp = _probe_pair(torch), _probe_pair(torch)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(1000000)   # bring the clock up first
+            _probe(torch, stream, lp, CLOCK_PROBE_CYCLES)
+            _probe(torch, stream, sp, CLOCK_PROBE_SHORT)
+        torch.cuda.synchronize(dev)
+        tl, ts = lp[0].elapsed_time(lp[1]), sp[0].elapsed_time(sp[1])
+        if tl > ts:
+            f_khz = (CLOCK_PROBE_CYCLES - CLOCK_PROBE_SHORT) / (tl - ts)   # cycles per ms
+            fits.append((tl - CLOCK_PROBE_CYCLES / f_khz, f_khz / 1e3))
+    if not fits:
+        return {"overhead_us": 0.0, "idle_mhz": None}
+    fits.sort()
+    over, mhz = fits[len(fits) // 2]
+    _probe_overhead_ms = max(0.0, over)
+    return {"overhead_us": _probe_overhead_ms * 1e3, "idle_mhz": mhz}
 
 
 class _Workload:
@@ -564,8 +595,10 @@ def clock_study(torch, wl, stream, dev, seconds, num_sms, rate):
     return {
         "launches": launches, "chunks": len(chunks), "seconds": total_ms * 1e-3,
         "probe": "torch.cuda._sleep(%d cycles) on one block between chunks of %d launches, timed by CUDA events "
-                 "on the launching stream; a chunk's clock is the mean of the probes around it" % (
-                     CLOCK_PROBE_CYCLES, CLOCK_CHUNK),
+                 "on the launching stream, minus the probe's own launch overhead (calibrated on the idle GPU); a "
+                 "chunk's clock is the mean of the probes around it.  A probe runs while the GPU is nearly idle, "
+                 "so it reads the clock the power controller has just set for the chunk, at most slightly "
+                 "raised" % (CLOCK_PROBE_CYCLES, CLOCK_CHUNK),
         "ms_per_launch": ms_per_launch, "tflops": achieved,
         "sm_mhz_median": med_mhz, "sm_mhz_min": min(mhz), "sm_mhz_max": max(mhz),
         "clock_peak_tflops_at_median": num_sms * FLOP_PER_CLK_PER_SM * rate * med_mhz * 1e6 / 1e12,
@@ -583,7 +616,8 @@ def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, cpu=N
     Workloads larger than L2 run back to back in 5 groups between events
     (median and min over the groups' time per launch); workloads that fit
     in L2 get an L2 flush before every launch, each launch between its own
-    events (median and min over launches).  A clock probe before and after."""
+    events (median and min over launches).  A clock probe right after the
+    loop reads the clock it ran at."""
     wl = _Workload(case, dev)
     sptr = stream.cuda_stream
     fits_l2 = case.algorithmic_bytes <= 129e6
@@ -596,9 +630,8 @@ def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, cpu=N
     torch.cuda.synchronize(dev)
     est_ms = max(w0.elapsed_time(w1) / 10, 1e-3)
     n = int(min(5000, max(50, 200.0 / est_ms)))
-    p0, p1 = _probe_pair(torch), _probe_pair(torch)
+    p1 = _probe_pair(torch)
     with torch.cuda.stream(stream):
-        _probe(torch, stream, p0)
         if fits_l2:
             spans = [_probe_pair(torch) for _ in range(n)]
             for a, b in spans:
@@ -632,7 +665,7 @@ def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, cpu=N
     peak_burst = float(peaks["bf16_tflops"]) * rate
     hbm = float(peaks["hbm_gbs"])
     roof = roofline_of(case.flops, case.algorithmic_bytes, med * 1e-3, peak_burst, hbm)
-    mhz = [m for m in (_probe_mhz(p0), _probe_mhz(p1)) if m]
+    mhz = [m for m in (_probe_mhz(p1),) if m]   # after the loop: the clock it ran at
     row = {
         "index": index, "workload": case.name,
         "M": case.M, "N": case.N, "K": case.K, "in_dtype": case.in_dtype, "out_dtype": case.out_dtype,
@@ -700,10 +733,13 @@ def run_ours(args, case):
     if status != 0:
         raise RuntimeError("device status after warm-up: %s %s" % (binding.gemm_status_string(status), info))
 
-    def timed(n):
+    def timed(n, probe_after=None):
         """Device time (ms) of n launches on the stream.  Working sets that
         fit in L2 get a flush (a 256 MB write) before every launch, outside
-        the timed spans: each launch is bracketed by its own event pair."""
+        the timed spans: each launch is bracketed by its own event pair.
+        With `probe_after`, a clock probe follows the last launch (outside
+        the timed span): it reads the clock the launches ran at, before the
+        idle GPU's clock comes back up."""
         with torch.cuda.stream(stream):
             if not small:
                 e0.record(stream)
@@ -718,28 +754,31 @@ def run_ours(args, case):
                     a.record(stream)
                     step()
                     b.record(stream)
+            if probe_after is not None:
+                _probe(torch, stream, probe_after)
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) if not small else sum(a.elapsed_time(b) for a, b in spans)
 
     # burst: the best of three runs of BURST_STEPS launches, measured the way
-    # the burst peak is (a short run, before the power cap sets in), each
-    # with a clock probe before it; the headline is the run below
+    # the burst peak is (a short run after an idle pause, before the power cap
+    # sets in), each followed by a clock probe; the headline is the run below
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    probe_cal = clock_probe_calibrate(torch, stream, dev)
     burst_runs = []
     for _ in range(3):
-        pp = _probe_pair(torch)
-        with torch.cuda.stream(stream):
-            _probe(torch, stream, pp)
-        burst_runs.append((timed(BURST_STEPS) / BURST_STEPS, _probe_mhz(pp)))
         time.sleep(0.2)   # let the power state settle back between runs
+        pp = _probe_pair(torch)
+        burst_runs.append((timed(BURST_STEPS, probe_after=pp) / BURST_STEPS, _probe_mhz(pp)))
     burst_ms, burst_mhz = min(burst_runs, key=lambda r: r[0])
 
     sampler = ClockSampler(local_rank).start() if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     barrier()
     torch.cuda.synchronize(dev)
-    elapsed_ms = timed(args.steps)
+    timed_probe = _probe_pair(torch)
+    elapsed_ms = timed(args.steps, probe_after=timed_probe)
+    timed_mhz = _probe_mhz(timed_probe)
     barrier()
     # the clock study runs right after the timed region, on rank 0 at N = 1,
     # with the sampler still running (its samples then cover both)
@@ -750,6 +789,7 @@ def run_ours(args, case):
         study = clock_study(torch, wl, stream, dev, args.clock_study_seconds, num_sms, rate)
     clocks = sampler.stop() if sampler else None
     if clocks is not None:
+        clocks["sm_mhz_probed_after_timed_region"] = timed_mhz
         clocks["window"] = ("the timed region (%.0f ms)%s" % (
             elapsed_ms, " and the clock study after it (%.1f s)" % study["seconds"] if study else ""))
     status, info = binding.gemm_poll_device_error(stream)
@@ -895,11 +935,14 @@ def run_ours(args, case):
         if burst_mhz:
             roofline["burst"]["frac_of_clock_peak"] = burst_tflops / (
                 num_sms * FLOP_PER_CLK_PER_SM * rate * burst_mhz * 1e6 / 1e12)
+        if timed_mhz:
+            # the timed loop against the dense peak at the clock it ran at
+            clk_peak = num_sms * FLOP_PER_CLK_PER_SM * rate * timed_mhz * 1e6 / 1e12
+            roofline["frac_of_clock_peak"] = achieved / clk_peak
+            roofline["clock_peak_tflops"] = clk_peak
+            roofline["clock_source"] = "probe right after the timed launches (%.0f MHz)" % timed_mhz
         if study:
-            roofline["frac_of_clock_peak"] = study["frac_of_clock_peak"]
-            roofline["clock_peak_tflops"] = study["clock_peak_tflops_at_median"]
-            roofline["clock_source"] = "clock study median (%d chunks, %.0f MHz)" % (study["chunks"],
-                                                                                  study["sm_mhz_median"])
+            roofline["frac_of_clock_peak_clock_study"] = study["frac_of_clock_peak"]
     roofline["max_clock_peak_tflops"] = num_sms * FLOP_PER_CLK_PER_SM * rate * 2070e6 / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -910,6 +953,7 @@ def run_ours(args, case):
     }
     if study:
         line["clock_study"] = study
+        study["probe_calibration"] = probe_cal
     del wl
 
     # every BASELINE workload, and the CPU oracle on the same inputs

@@ -112,6 +112,18 @@ int group_m_setting(int k_blocks) {
     return k_blocks <= 8 ? 2 : 8;
 }
 
+// SMs the persistent grid may use: all of the device's, or fewer when
+// GEMM_MAX_SMS is set (at least 2), leaving the rest to other work on the
+// GPU.
+int plan_sms(int device_sms) {
+    const char* v = std::getenv("GEMM_MAX_SMS");
+    if (v && *v) {
+        const int n = std::atoi(v);
+        if (n >= 2 && n < device_sms) return n;
+    }
+    return device_sms;
+}
+
 // Memory-system tuning of a launch (needs the tile counts set).
 //  * L2 eviction priorities of the A, B loads and D stores (0 normal, 1
 //    evict-first, 2 evict-last).  Operand panels are re-read by the other
@@ -977,12 +989,12 @@ int gemm(void* D, const void* A, const void* B, const void* C, int64_t M, int64_
                                      out_dtype, s);
     }
 
-    Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, f8 ? 1 : 0, 0, transB);
+    Plan pl = make_plan(M, N, K, plan_sms(ds->num_sms), true, out_dtype, f8 ? 1 : 0, 0, transB);
     void* ws = nullptr;
     uint32_t epoch = 0;
     if (pl.sk_tiles > 0 && workspace_for(kWsStreamK, dev, s, pl.ws_bytes, &ws, &epoch, !in_capture) != GEMM_OK) {
         if (!in_capture) return reject(GEMM_ERR_CUDA, "stream-K workspace");
-        pl = make_plan(M, N, K, ds->num_sms, false, out_dtype, f8 ? 1 : 0, 0, transB);   // whole tiles: no workspace
+        pl = make_plan(M, N, K, plan_sms(ds->num_sms), false, out_dtype, f8 ? 1 : 0, 0, transB);   // whole tiles: no workspace
     }
     TcgenLaunch L;
     if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
@@ -1062,7 +1074,7 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
     // Every workspace is acquired before anything is enqueued, so a refusal
     // (for instance inside a stream capture, which cannot allocate) leaves
     // the stream as it was.
-    Plan pl = make_plan(M, N, K, ds->num_sms, true, out_dtype, 1, 1);
+    Plan pl = make_plan(M, N, K, plan_sms(ds->num_sms), true, out_dtype, 1, 1);
     // The scales, rearranged into 512-byte chunks (gemm_sm103_mx.cu): one per
     // 128-K sub-block and 128-row group of A (each CTA of a pair has its
     // own), and (tile N / 128) per sub-block and N tile.
@@ -1084,7 +1096,7 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
     uint32_t epoch = 0;
     if (pl.sk_tiles > 0 && workspace_for(kWsStreamK, dev, s, pl.ws_bytes, &ws, &epoch, !in_capture) != GEMM_OK) {
         if (!in_capture) return reject(GEMM_ERR_CUDA, "stream-K workspace");
-        pl = make_plan(M, N, K, ds->num_sms, false, out_dtype, 1, 1);   // whole tiles: no workspace
+        pl = make_plan(M, N, K, plan_sms(ds->num_sms), false, out_dtype, 1, 1);   // whole tiles: no workspace
     }
     // 4-bit operands off TMA's 4-bit grid: copied into zero-padded rows of K
     // rounded up to 128 elements.
@@ -1305,7 +1317,7 @@ extern "C" GEMM_API int gemm_noalloc(void* D, const void* A, const void* B, cons
     if (route == kRouteSync)   // needs no scratch either
         return launch_sync_or_reject(D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta, in_dtype,
                                      out_dtype, s);
-    const Plan pl = make_plan(M, N, K, ns->num_sms, false, out_dtype, f8 ? 1 : 0, 0, transB);   // no workspace: data-parallel
+    const Plan pl = make_plan(M, N, K, plan_sms(ns->num_sms), false, out_dtype, f8 ? 1 : 0, 0, transB);   // no workspace: data-parallel
     TcgenLaunch L;
     if ((rc = describe_tcgen05(&L, pl, D, A, B, C, M, N, K, lda, ldb, ldc, ldd, transA, transB, alpha, beta,
                                in_dtype, out_dtype)) != GEMM_OK)

@@ -136,7 +136,8 @@ typedef enum {
  * it, so the graph can be replayed after any number of other calls.
  * Returns GEMM_OK or a GEMM_ERR_* code (see gemm_status_t).
  * Setting the environment variable GEMM_LOG=1 prints each call's plan or
- * rejection reason to stderr.
+ * rejection reason to stderr; GEMM_MAX_SMS=n (n >= 2) plans the persistent
+ * grid for at most n SMs, leaving the others to other work on the GPU.
  */
 GEMM_API int gemm(void* D, const void* A, const void* B, const void* C,
          int64_t M, int64_t N, int64_t K,
