@@ -18,14 +18,21 @@ short loop and for the separate burst measurement (best of three 10-launch
 runs).
 
 At N = 1 the line also carries, outside the timed region:
+  clocks       the SM clock the timed loop ran at: the same loop run again
+               with the grid planned for 2 fewer SMs while a one-thread
+               probe kernel (compiled by this script) samples %globaltimer
+               and %clock64 on a free SM.  Neither a probe between launches
+               nor NVML sees it: the power limiter lets the clock back up
+               within ~0.1 ms of the load stopping, and NVML reports the
+               clock the controller asks for (2070 MHz during a burst that
+               runs at ~1.6-1.7 GHz);
   clock_study  the headline workload for >= 1.5 s in chunks of launches,
-               each chunk preceded by a clock probe (a one-block kernel
-               that spins a fixed number of SM clock cycles, timed with
-               CUDA events): launch time against the SM clock it ran at;
+               clocked the same way: launch time against the SM clock it
+               ran at, binned by clock;
   per_config   every BASELINE workload (10 warm-ups, then >= 50 launches
-               and >= 200 ms, each launch between its own events): median
-               and min per launch, throughput, bound and fraction of the
-               measured peak, and the probed SM clock;
+               and >= 200 ms): median and min per launch, throughput,
+               bound and fraction of the measured peak, and the SM clock
+               during the loop (measured as above);
   cpu_baseline the oracle as it stands on the host cores, single-threaded
                and on all cores, for every workload: the full problem for
                the small ones (and 4096^3), a tile-covering sample (one
@@ -449,57 +456,171 @@ def run_reference(args, case):
 # ----------------------------------------------------------------------------
 # the CUDA path
 
-CLOCK_PROBE_CYCLES = 200000     # SM clock cycles one probe spins (about 0.1 ms)
-CLOCK_PROBE_SHORT = 50000       # the short probe of the overhead calibration
-CLOCK_CHUNK = 16                # launches between two probes in the clock study
+CLOCK_CHUNK = 16                # launches per chunk of the clock study
 FLUSH_BYTES = 256 << 20         # the L2 flush write (L2 is 129 MB)
+SPARE_SMS = 2                   # SMs a clock measurement leaves free for its probe
+PROBE_INTERVAL_NS = 20000       # one clock sample every 20 us
 
-# Launch overhead (ms) inside a probe's event pair, measured once on the idle
-# GPU by clock_probe_calibrate(); subtracted from every probe's time.
-_probe_overhead_ms = 0.0
+# Measurement helper compiled by this script (not part of the library): a
+# one-thread kernel that samples (%globaltimer, %clock64, %smid) every
+# interval_ns, n times (so it ends after n * interval_ns), and a one-thread
+# kernel that writes %globaltimer once, to mark where a loop starts and ends
+# on the same clock.  An SM's clock64 advances at that SM's clock, so the
+# ratio of the two counters between samples is the clock the SMs ran at.
+_CLOCK_PROBE_SRC = r"""
+#include <cuda_runtime.h>
+__global__ void gb_clock_probe(unsigned long long* out, int n, unsigned long long interval_ns) {
+    unsigned long long t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (int i = 0; i < n; ++i) {
+        unsigned long long t;
+        do {
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        } while (t < t0 + (unsigned long long)i * interval_ns);
+        unsigned long long c = clock64();
+        unsigned int sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        out[3 * i] = t;
+        out[3 * i + 1] = c;
+        out[3 * i + 2] = sm;
+    }
+}
+__global__ void gb_stamp(unsigned long long* out) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    *out = t;
+}
+extern "C" int launch_clock_probe(void* out, int n, unsigned long long interval_ns, void* stream) {
+    gb_clock_probe<<<1, 1, 0, (cudaStream_t)stream>>>((unsigned long long*)out, n, interval_ns);
+    return (int)cudaGetLastError();
+}
+extern "C" int launch_stamp(void* out, void* stream) {
+    gb_stamp<<<1, 1, 0, (cudaStream_t)stream>>>((unsigned long long*)out);
+    return (int)cudaGetLastError();
+}
+"""
 
 
-def _probe_pair(torch):
-    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+def load_clock_probe():
+    """Compiles the measurement helper above with nvcc into a temporary
+    directory and loads it; None if that fails (the clock is then not
+    reported)."""
+    import ctypes
+    import shutil
+    import tempfile
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    d = tempfile.mkdtemp(prefix="gemm_bench_probe_")
+    src, lib = os.path.join(d, "probe.cu"), os.path.join(d, "libprobe.so")
+    with open(src, "w") as f:
+        f.write(_CLOCK_PROBE_SRC)
+    r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-shared", "-Xcompiler", "-fPIC",
+                        "-o", lib, src], capture_output=True, text=True)
+    if r.returncode != 0:
+        return None
+    probe = ctypes.CDLL(lib)
+    probe.launch_clock_probe.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong, ctypes.c_void_p]
+    probe.launch_stamp.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    # Launch both kernels once now: the first launch of a kernel loads it,
+    # and that load would wait for a probe already running on the GPU.
+    import torch
+    scratch = torch.zeros(8, dtype=torch.int64, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    if probe.launch_clock_probe(scratch.data_ptr(), 1, 1000, s) != 0 or probe.launch_stamp(scratch.data_ptr(), s) != 0:
+        return None
+    torch.cuda.synchronize()
+    return probe
 
 
-def _probe(torch, stream, pair, cycles=CLOCK_PROBE_CYCLES):
-    """Enqueue a clock probe: one block spinning `cycles` SM cycles between
-    the two events of `pair`."""
-    pair[0].record(stream)
-    torch.cuda._sleep(cycles)
-    pair[1].record(stream)
+def clock_series(samples):
+    """(time ns, MHz) between consecutive probe samples taken on one SM."""
+    out = []
+    for (t0, c0, s0), (t1, c1, s1) in zip(samples, samples[1:]):
+        if t1 > t0 and s0 == s1 and c1 >= c0:
+            out.append((0.5 * (t0 + t1), (c1 - c0) / (t1 - t0) * 1e3))
+    return out
 
 
-def _probe_mhz(pair, cycles=CLOCK_PROBE_CYCLES):
-    ms = pair[0].elapsed_time(pair[1]) - _probe_overhead_ms
-    return cycles / (ms * 1e3) if ms > 0 else None
+def clock_between(series, t0, t1):
+    """The clock readings whose interval centre lies in [t0, t1] (ns)."""
+    return [m for t, m in series if t0 <= t <= t1]
 
 
-def clock_probe_calibrate(torch, stream, dev):
-    """A probe's event pair also holds the launch of its spin kernel.  On
-    the idle GPU (one clock) a long and a short probe give both terms:
-    t = overhead + cycles / f.  Sets the overhead the probes subtract and
-    returns it with the idle clock."""
-    global _probe_overhead_ms
-    fits = []
-    for _ in range(3):
-        lp, sp = _probe_pair(torch), _probe_pair(torch)
-        with torch.cuda.stream(stream):
-            torch.cuda._sleep(1000000)   # bring the clock up first
-            _probe(torch, stream, lp, CLOCK_PROBE_CYCLES)
-            _probe(torch, stream, sp, CLOCK_PROBE_SHORT)
-        torch.cuda.synchronize(dev)
-        tl, ts = lp[0].elapsed_time(lp[1]), sp[0].elapsed_time(sp[1])
-        if tl > ts:
-            f_khz = (CLOCK_PROBE_CYCLES - CLOCK_PROBE_SHORT) / (tl - ts)   # cycles per ms
-            fits.append((tl - CLOCK_PROBE_CYCLES / f_khz, f_khz / 1e3))
-    if not fits:
-        return {"overhead_us": 0.0, "idle_mhz": None}
-    fits.sort()
-    over, mhz = fits[len(fits) // 2]
-    _probe_overhead_ms = max(0.0, over)
-    return {"overhead_us": _probe_overhead_ms * 1e3, "idle_mhz": mhz}
+class ClockProbe:
+    """Runs loops of a workload with the persistent grid planned for
+    SPARE_SMS fewer SMs while the probe kernel samples the clock on a free SM
+    (a probe between launches cannot see the clock a loop runs at: the
+    power limiter lets it back up within ~0.1 ms of the load stopping).
+    Each loop is bracketed by timestamp kernels on its stream."""
+
+    def __init__(self, torch, dev, num_sms, lib):
+        self.torch, self.dev, self.num_sms, self.lib = torch, dev, num_sms, lib
+
+    def run(self, wl, segments, launches_per_segment, fits_l2=False, flush=None):
+        """`segments` back-to-back segments of `launches_per_segment` launches
+        after an idle pause of 0.5 s.  Returns (per-segment list of (device
+        ms per launch, median MHz, readings)) or None."""
+        torch = self.torch
+        old = os.environ.get("GEMM_MAX_SMS")
+        os.environ["GEMM_MAX_SMS"] = str(self.num_sms - SPARE_SMS)
+        try:
+            s1, s2 = torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev)
+            sptr = s1.cuda_stream
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s1):
+                for _ in range(3):
+                    wl.step(sptr)
+                e0.record(s1)
+                wl.step(sptr)
+                e1.record(s1)
+            torch.cuda.synchronize(self.dev)
+            est_ms = max(e0.elapsed_time(e1), 1e-3) * (2.0 if fits_l2 else 1.0)
+            total_ms = est_ms * segments * launches_per_segment * 1.5 + 20.0
+            n = int(total_ms * 1e6 / PROBE_INTERVAL_NS) + 10
+            buf = torch.zeros(3 * n, dtype=torch.int64, device=self.dev)
+            stamps = torch.zeros(segments + 1, dtype=torch.int64, device=self.dev)
+            spans = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(segments)]
+            time.sleep(0.5)
+            if self.lib.launch_clock_probe(buf.data_ptr(), n, PROBE_INTERVAL_NS, s2.cuda_stream) != 0:
+                return None
+            time.sleep(0.002)   # the probe is running before the loop starts
+            with torch.cuda.stream(s1):
+                for k, (a, b) in enumerate(spans):
+                    if self.lib.launch_stamp(stamps[k:].data_ptr(), sptr) != 0:
+                        return None
+                    a.record(s1)
+                    for _ in range(launches_per_segment):
+                        if fits_l2:
+                            flush.zero_()
+                        wl.step(sptr)
+                    b.record(s1)
+                if self.lib.launch_stamp(stamps[segments:].data_ptr(), sptr) != 0:
+                    return None
+            torch.cuda.synchronize(self.dev)
+            series = clock_series([tuple(x) for x in buf.view(-1, 3).cpu().tolist()])
+            st = stamps.cpu().tolist()
+            out = []
+            for k, (a, b) in enumerate(spans):
+                inside = clock_between(series, st[k], st[k + 1])
+                out.append((a.elapsed_time(b) / launches_per_segment,
+                            statistics.median(inside) if inside else None, len(inside)))
+            return out
+        finally:
+            if old is None:
+                os.environ.pop("GEMM_MAX_SMS", None)
+            else:
+                os.environ["GEMM_MAX_SMS"] = old
+
+
+def clock_during(probe, wl, launches, fits_l2=False, flush=None):
+    """The SM clock during a loop of `launches` launches (the loop run again
+    beside the clock probe after an idle pause): (median MHz, readings)."""
+    if probe is None:
+        return None, 0
+    res = probe.run(wl, 1, launches, fits_l2, flush)
+    if not res or res[0][1] is None:
+        return None, 0
+    return res[0][1], res[0][2]
 
 
 class _Workload:
@@ -543,41 +664,37 @@ class _Workload:
         self.call(self.Dd, self.Ad, self.Bd, self.Cd, self.SFAd, self.SFBd, s_ptr)
 
 
-def clock_study(torch, wl, stream, dev, seconds, num_sms, rate):
-    """The workload back to back for about `seconds`, in chunks of
-    CLOCK_CHUNK launches, each chunk preceded by a clock probe: per chunk the
-    device time per launch and the SM clock it ran at (the mean of the probes
-    before and after it).  Returns the chunk table's summary and bins."""
-    sptr = stream.cuda_stream
-    # estimate the chunk count from one chunk
-    e0, e1 = _probe_pair(torch)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(CLOCK_CHUNK):
-            wl.step(sptr)
-        e1.record(stream)
+def _event_pair(torch):
+    return torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+
+def clock_study(torch, probe, wl, dev, seconds, num_sms, rate):
+    """The workload back to back for about `seconds` after an idle pause, in
+    chunks of CLOCK_CHUNK launches between CUDA events, beside the clock
+    probe (ClockProbe): per chunk the device time per launch and the median
+    clock inside it.  Returns the chunk table's summary and its bins by
+    clock, or None without the probe."""
+    if probe is None:
+        return None
+    sptr = torch.cuda.current_stream(dev).cuda_stream
+    e0, e1 = _event_pair(torch)
+    e0.record()
+    for _ in range(CLOCK_CHUNK):
+        wl.step(sptr)
+    e1.record()
     torch.cuda.synchronize(dev)
     chunk_ms = max(e0.elapsed_time(e1), 1e-3)
-    n_chunks = max(8, min(4000, int(seconds * 1e3 / chunk_ms)))
-    probes = [_probe_pair(torch) for _ in range(n_chunks + 1)]
-    spans = [_probe_pair(torch) for _ in range(n_chunks)]
-    with torch.cuda.stream(stream):
-        for c in range(n_chunks):
-            _probe(torch, stream, probes[c])
-            spans[c][0].record(stream)
-            for _ in range(CLOCK_CHUNK):
-                wl.step(sptr)
-            spans[c][1].record(stream)
-        _probe(torch, stream, probes[n_chunks])
-    torch.cuda.synchronize(dev)
-    chunks = []
-    for c in range(n_chunks):
-        f0, f1 = _probe_mhz(probes[c]), _probe_mhz(probes[c + 1])
-        if f0 is None or f1 is None:
-            continue
-        chunks.append({"mhz": 0.5 * (f0 + f1), "launches": CLOCK_CHUNK, "ms": spans[c][0].elapsed_time(spans[c][1])})
+    n_chunks = max(8, min(2000, int(seconds * 1e3 / chunk_ms)))
+    res = probe.run(wl, n_chunks, CLOCK_CHUNK)
+    if not res:
+        return None
+    chunks = [{"mhz": m, "launches": CLOCK_CHUNK, "ms": ms * CLOCK_CHUNK, "readings": r}
+              for ms, m, r in res if m]
+    if not chunks:
+        return None
+    sms = num_sms - SPARE_SMS
     flops = wl.case.flops
-    ideal_cycles = flops / (num_sms * FLOP_PER_CLK_PER_SM * rate)
+    ideal_cycles = flops / (sms * FLOP_PER_CLK_PER_SM * rate)
     total_ms = sum(c["ms"] for c in chunks)
     launches = sum(c["launches"] for c in chunks)
     mhz = [c["mhz"] for c in chunks]
@@ -585,24 +702,23 @@ def clock_study(torch, wl, stream, dev, seconds, num_sms, rate):
     med_mhz = statistics.median(mhz)
     ms_per_launch = total_ms / launches
     achieved = flops / (ms_per_launch * 1e-3) / 1e12
+    clk_peak = sms * FLOP_PER_CLK_PER_SM * rate * med_mhz * 1e6 / 1e12
     bins = clock_bins(chunks)
-    for b in bins:
-        t = b["ms_per_launch"] * 1e-3
-        b["tflops"] = flops / t / 1e12
-        b["cycles_per_launch"] = t * b["mhz_mean"] * 1e6
-        b["frac_of_clock_peak"] = ideal_cycles / b["cycles_per_launch"]
+    for bn in bins:
+        t = bn["ms_per_launch"] * 1e-3
+        bn["tflops"] = flops / t / 1e12
+        bn["cycles_per_launch"] = t * bn["mhz_mean"] * 1e6
+        bn["frac_of_clock_peak"] = ideal_cycles / bn["cycles_per_launch"]
     first = chunks[0]
     return {
-        "launches": launches, "chunks": len(chunks), "seconds": total_ms * 1e-3,
-        "probe": "torch.cuda._sleep(%d cycles) on one block between chunks of %d launches, timed by CUDA events "
-                 "on the launching stream, minus the probe's own launch overhead (calibrated on the idle GPU); a "
-                 "chunk's clock is the mean of the probes around it.  A probe runs while the GPU is nearly idle, "
-                 "so it reads the clock the power controller has just set for the chunk, at most slightly "
-                 "raised" % (CLOCK_PROBE_CYCLES, CLOCK_CHUNK),
+        "launches": launches, "chunks": len(chunks), "seconds": total_ms * 1e-3, "sms": sms,
+        "clock_readings": sum(c["readings"] for c in chunks),
+        "method": "a one-thread probe kernel samples %%globaltimer and %%clock64 every %d us on one of the %d SMs "
+                  "the grid leaves free; timestamp kernels between chunks place them on the same clock; a "
+                  "chunk's clock is the median reading inside it" % (PROBE_INTERVAL_NS // 1000, SPARE_SMS),
         "ms_per_launch": ms_per_launch, "tflops": achieved,
         "sm_mhz_median": med_mhz, "sm_mhz_min": min(mhz), "sm_mhz_max": max(mhz),
-        "clock_peak_tflops_at_median": num_sms * FLOP_PER_CLK_PER_SM * rate * med_mhz * 1e6 / 1e12,
-        "frac_of_clock_peak": achieved / (num_sms * FLOP_PER_CLK_PER_SM * rate * med_mhz * 1e6 / 1e12),
+        "clock_peak_tflops_at_median": clk_peak, "frac_of_clock_peak": achieved / clk_peak,
         "cycles_per_launch_median": statistics.median(cyc), "ideal_cycles_per_launch": ideal_cycles,
         "first_chunk": {"sm_mhz": first["mhz"], "ms_per_launch": first["ms"] / first["launches"],
                         "frac_of_clock_peak": ideal_cycles / (first["ms"] / first["launches"] * 1e-3 *
@@ -611,17 +727,17 @@ def clock_study(torch, wl, stream, dev, seconds, num_sms, rate):
     }
 
 
-def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, cpu=None):
+def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, probe=None):
     """One BASELINE workload: 10 warm-ups, then >= 50 launches and >= 200 ms.
     Workloads larger than L2 run back to back in 5 groups between events
     (median and min over the groups' time per launch); workloads that fit
     in L2 get an L2 flush before every launch, each launch between its own
-    events (median and min over launches).  A clock probe right after the
-    loop reads the clock it ran at."""
+    events (median and min over launches).  The clock the loop ran at is
+    measured while it runs again beside the clock probe (clock_during)."""
     wl = _Workload(case, dev)
     sptr = stream.cuda_stream
     fits_l2 = case.algorithmic_bytes <= 129e6
-    w0, w1 = _probe_pair(torch)
+    w0, w1 = _event_pair(torch)
     with torch.cuda.stream(stream):
         w0.record(stream)
         for _ in range(10):
@@ -630,10 +746,9 @@ def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, cpu=N
     torch.cuda.synchronize(dev)
     est_ms = max(w0.elapsed_time(w1) / 10, 1e-3)
     n = int(min(5000, max(50, 200.0 / est_ms)))
-    p1 = _probe_pair(torch)
     with torch.cuda.stream(stream):
         if fits_l2:
-            spans = [_probe_pair(torch) for _ in range(n)]
+            spans = [_event_pair(torch) for _ in range(n)]
             for a, b in spans:
                 flush.zero_()
                 a.record(stream)
@@ -642,13 +757,12 @@ def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, cpu=N
         else:
             groups = 5
             per = (n + groups - 1) // groups
-            spans = [_probe_pair(torch) for _ in range(groups)]
+            spans = [_event_pair(torch) for _ in range(groups)]
             for a, b in spans:
                 a.record(stream)
                 for _ in range(per):
                     wl.step(sptr)
                 b.record(stream)
-        _probe(torch, stream, p1)
     torch.cuda.synchronize(dev)
     status, info = wl.binding.gemm_poll_device_error(stream)
     if status != 0:
@@ -665,7 +779,8 @@ def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, cpu=N
     peak_burst = float(peaks["bf16_tflops"]) * rate
     hbm = float(peaks["hbm_gbs"])
     roof = roofline_of(case.flops, case.algorithmic_bytes, med * 1e-3, peak_burst, hbm)
-    mhz = [m for m in (_probe_mhz(p1),) if m]   # after the loop: the clock it ran at
+    during, n_samples = clock_during(probe, wl, launches, fits_l2, flush)
+    mhz = [during] if during else []
     row = {
         "index": index, "workload": case.name,
         "M": case.M, "N": case.N, "K": case.K, "in_dtype": case.in_dtype, "out_dtype": case.out_dtype,
@@ -681,7 +796,8 @@ def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, cpu=N
         "peak_unit": UNIT if roof["bound"] == "tensor" else "GB/s",
         "peak_kind": ("measured bf16 burst (cuBLAS)" + ("" if rate == 1.0 else " x 2, nominal fp8 / bf16 ratio"))
         if roof["bound"] == "tensor" else "measured HBM copy bandwidth",
-        "sm_mhz_probed": statistics.mean(mhz) if mhz else None,
+        "sm_mhz_during": statistics.mean(mhz) if mhz else None,
+        "clock_samples": n_samples,
         "traffic": _profiled_traffic(case.name),
     }
     if "limited_by" in roof:
@@ -733,13 +849,10 @@ def run_ours(args, case):
     if status != 0:
         raise RuntimeError("device status after warm-up: %s %s" % (binding.gemm_status_string(status), info))
 
-    def timed(n, probe_after=None):
+    def timed(n):
         """Device time (ms) of n launches on the stream.  Working sets that
         fit in L2 get a flush (a 256 MB write) before every launch, outside
-        the timed spans: each launch is bracketed by its own event pair.
-        With `probe_after`, a clock probe follows the last launch (outside
-        the timed span): it reads the clock the launches ran at, before the
-        idle GPU's clock comes back up."""
+        the timed spans: each launch is bracketed by its own event pair."""
         with torch.cuda.stream(stream):
             if not small:
                 e0.record(stream)
@@ -754,44 +867,48 @@ def run_ours(args, case):
                     a.record(stream)
                     step()
                     b.record(stream)
-            if probe_after is not None:
-                _probe(torch, stream, probe_after)
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) if not small else sum(a.elapsed_time(b) for a, b in spans)
 
     # burst: the best of three runs of BURST_STEPS launches, measured the way
     # the burst peak is (a short run after an idle pause, before the power cap
-    # sets in), each followed by a clock probe; the headline is the run below
+    # sets in); the headline is the run below
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    probe_cal = clock_probe_calibrate(torch, stream, dev)
     burst_runs = []
     for _ in range(3):
         time.sleep(0.2)   # let the power state settle back between runs
-        pp = _probe_pair(torch)
-        burst_runs.append((timed(BURST_STEPS, probe_after=pp) / BURST_STEPS, _probe_mhz(pp)))
-    burst_ms, burst_mhz = min(burst_runs, key=lambda r: r[0])
+        burst_runs.append(timed(BURST_STEPS) / BURST_STEPS)
+    burst_ms = min(burst_runs)
 
     sampler = ClockSampler(local_rank).start() if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     barrier()
     torch.cuda.synchronize(dev)
-    timed_probe = _probe_pair(torch)
-    elapsed_ms = timed(args.steps, probe_after=timed_probe)
-    timed_mhz = _probe_mhz(timed_probe)
+    elapsed_ms = timed(args.steps)
     barrier()
-    # the clock study runs right after the timed region, on rank 0 at N = 1,
-    # with the sampler still running (its samples then cover both)
+    # after the timed region, on rank 0 at N = 1, with the sampler still
+    # running (its samples then cover all of it): the clock the timed loop
+    # ran at (the same loop again, its clock read by NVML while it runs),
+    # the same for a burst, then the clock study
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     rate = FP8_RATE if case.in_dtype in ("e4m3", "e5m2", "e2m1") else 1.0
     study = None
-    if world == 1 and not args.no_clock_study and not small:
-        study = clock_study(torch, wl, stream, dev, args.clock_study_seconds, num_sms, rate)
+    timed_mhz, timed_samples, burst_mhz = None, 0, None
+    probe = None
+    if world == 1 and not args.no_clock_study:
+        lib = load_clock_probe()
+        probe = ClockProbe(torch, dev, num_sms, lib) if lib is not None else None
+        timed_mhz, timed_samples = clock_during(probe, wl, args.steps, small, flush)
+        burst_mhz, _ = clock_during(probe, wl, BURST_STEPS, small, flush)
+        if not small:
+            study = clock_study(torch, probe, wl, dev, args.clock_study_seconds, num_sms, rate)
     clocks = sampler.stop() if sampler else None
     if clocks is not None:
-        clocks["sm_mhz_probed_after_timed_region"] = timed_mhz
+        clocks["sm_mhz_during_timed_loop"] = timed_mhz
+        clocks["sm_mhz_during_timed_loop_samples"] = timed_samples
         clocks["window"] = ("the timed region (%.0f ms)%s" % (
-            elapsed_ms, " and the clock study after it (%.1f s)" % study["seconds"] if study else ""))
+            elapsed_ms, " and the clock measurements after it (%.1f s)" % (study["seconds"] if study else 0.0)))
     status, info = binding.gemm_poll_device_error(stream)
     if status != 0:
         raise RuntimeError("device status after timing: %s %s" % (binding.gemm_status_string(status), info))
@@ -922,7 +1039,7 @@ def run_ours(args, case):
     roofline.update({"traffic": _profiled_traffic(case.name), "arithmetic_intensity": intensity,
                      "ridge_flop_per_byte": ridge, "algorithmic_flops_per_launch": case.flops,
                      "algorithmic_bytes_per_launch": case.algorithmic_bytes, "achieved_gbs": achieved_gbs})
-    roofline["burst"] = dict(burst, launches=BURST_STEPS, best_of=3, ms_per_launch=burst_ms, sm_mhz_probed=burst_mhz)
+    roofline["burst"] = dict(burst, launches=BURST_STEPS, best_of=3, ms_per_launch=burst_ms, sm_mhz_during=burst_mhz)
     if case.mx:
         roofline["note"] = ("block-scaled: the time per launch is that of the whole gemm_mx step, the two small "
                             "scale-rearranging launches included" +
@@ -940,7 +1057,9 @@ def run_ours(args, case):
             clk_peak = num_sms * FLOP_PER_CLK_PER_SM * rate * timed_mhz * 1e6 / 1e12
             roofline["frac_of_clock_peak"] = achieved / clk_peak
             roofline["clock_peak_tflops"] = clk_peak
-            roofline["clock_source"] = "probe right after the timed launches (%.0f MHz)" % timed_mhz
+            roofline["clock_source"] = (
+                "median of %d in-kernel clock readings on a spare SM during a repeat of the timed loop planned "
+                "for %d SMs (%.0f MHz)" % (timed_samples, num_sms - SPARE_SMS, timed_mhz))
         if study:
             roofline["frac_of_clock_peak_clock_study"] = study["frac_of_clock_peak"]
     roofline["max_clock_peak_tflops"] = num_sms * FLOP_PER_CLK_PER_SM * rate * 2070e6 / 1e12
@@ -953,7 +1072,6 @@ def run_ours(args, case):
     }
     if study:
         line["clock_study"] = study
-        study["probe_calibration"] = probe_cal
     del wl
 
     # every BASELINE workload, and the CPU oracle on the same inputs
@@ -961,7 +1079,7 @@ def run_ours(args, case):
     want_cpu = not args.no_cpu_baseline and world == 1
     if world == 1 and not args.no_per_config:
         for i, c in enumerate(CASES[:10]):
-            row, host = per_config_row(torch, c, i + 1, dev, stream, peaks, num_sms, flush)
+            row, host = per_config_row(torch, c, i + 1, dev, stream, peaks, num_sms, flush, probe)
             per_config.append(row)
             if want_cpu:
                 cpu_rows.append(cpu_oracle_timings(c, i + 1, *host, threads=len(os.sched_getaffinity(0)),

@@ -67,3 +67,16 @@ def test_roofline_classification():
     # the single atom: latency
     r = bench.roofline_of(2 * 16 * 8 * 16, 2 * (16 * 16 + 16 * 8) + 4 * 16 * 8, 8e-6, 1882.7, 6772.2)
     assert r["limited_by"] == "latency"
+
+
+def test_clock_series_from_probe_samples():
+    """Consecutive (globaltimer ns, clock64, smid) samples give the clock in
+    MHz between them; pairs across a change of SM (the counters are per SM)
+    or with a non-advancing timer are skipped."""
+    samples = [(1000, 5000, 7), (21000, 5000 + 40000, 7), (41000, 45000 + 33800, 7),
+               (61000, 10, 9), (81000, 10 + 20700 * 2, 9), (81000, 99999, 9)]
+    series = bench.clock_series(samples)
+    assert [round(m) for _, m in series] == [2000, 1690, 2070]
+    assert [t for t, _ in series] == [11000.0, 31000.0, 71000.0]
+    assert bench.clock_between(series, 10000, 40000) == [series[0][1], series[1][1]]
+    assert bench.clock_between(series, 72000, 90000) == []

@@ -334,3 +334,21 @@ def test_arch_is_sm103():
     major, minor = torch.cuda.get_device_capability(0)
     assert (major, minor) == (10, 3)
 
+
+
+@pytest.mark.parametrize("sms", [100, 38, 2])
+def test_max_sms_limits_the_grid_and_stays_exact(sms):
+    """GEMM_MAX_SMS plans the persistent grid for fewer SMs (more tiles per
+    CTA, other stream-K splits); the result is the oracle's bit for bit on
+    integer inputs."""
+    M, N, K = 1280, 1536, 1152
+    A = H.int_matrix((M, K), -4, 4, "f16", 301)
+    B = H.int_matrix((K, N), -4, 4, "f16", 302)
+    C = H.int_matrix((M, N), -50, 50, "f32", 303)
+    with H.env(GEMM_MAX_SMS=str(sms)):
+        plan = binding.gemm_plan(M, N, K, sms)
+        assert plan["grid"] <= sms
+        D, rc = H.run_gemm(A, B, C, M, N, K, beta=1.0)
+    assert rc == 0 and H.poll()[0] == 0
+    want, _ = H.oracle_full(A, B, C, M, N, K, beta=1.0)
+    H.assert_exact(D.numpy(), want, "GEMM_MAX_SMS=%d" % sms)
