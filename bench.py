@@ -208,8 +208,6 @@ def _args():
     ap.add_argument("--no-clock-study", action="store_true", help="skip the clock study")
     ap.add_argument("--clock-study-seconds", type=float, default=1.5)
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0,
-                    help="target wall time of the reference arm's per-step samples")
     ap.add_argument("--cpu-budget", type=float, default=100.0,
                     help="target wall time of the whole CPU oracle table (all workloads, both thread counts)")
     return ap.parse_args()
@@ -410,18 +408,6 @@ def cpu_oracle_timings(case, index, A, B, C, threads, budget_s):
                       "full_problem_seconds": full_flops / rate,
                       "full_problem_seconds_kind": "measured" if (full and done == full_flops) else "extrapolated"}
     return out
-
-
-def cpu_baseline(case, target_s):
-    """The reference-arm style figure: random output elements of `case` on
-    all host cores for about target_s seconds."""
-    run, threads = _oracle_sampler(case)
-    n, _ = _calibrate(run, threads, target_s)
-    t = run(n)
-    flops = 2.0 * case.K * n
-    return {"value": flops / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": "%d output elements of %s (random positions, each the full K=%d dot product), "
-                      "%.1f s on %d threads" % (n, case.name, case.K, t, threads)}
 
 
 def run_reference(args, case):

@@ -141,7 +141,9 @@ int plan_sms(int device_sms) {
 //    20 ns per stage (a quarter of the main loop spread over a warp's 8
 //    chunks), at most 2 us.  Measured (8192 x 8192, K = 4096 / 8192 / 16384):
 //    +2 % / +1 % / +0.7 %; block-scaled 8192^3 (224-wide tiles): +2.7 % E4M3,
-//    +2 % E2M1; shorter tiles are store-bound and get no pause.
+//    +2 % E2M1.  Tiles of 8 to 23 stages get 30 ns per stage (8192^2 x 1024,
+//    8 stages: 240 ns, +1.5 %; 480 ns +0.9 %, 960 ns -29 %); shorter tiles
+//    are store-bound and lose with any pause (K = 256: 150 ns -4 %).
 void tuning(GemmParams& p, int tile_n) {
     p.hint_a = p.num_n_tiles == 1 ? 1 : 2;
     p.hint_b = p.num_m_tiles == 1 ? 1 : 2;
@@ -155,7 +157,8 @@ void tuning(GemmParams& p, int tile_n) {
         p.hint_d = d;
     }
     p.epi_pace_ns = 0;
-    if (tile_n >= 192 && p.num_k_blocks >= 24) p.epi_pace_ns = std::min(2000, p.num_k_blocks * 20);
+    if (tile_n >= 192 && p.num_k_blocks >= 8)
+        p.epi_pace_ns = std::min(2000, p.num_k_blocks * (p.num_k_blocks >= 24 ? 20 : 30));
     const char* pv = std::getenv("GEMM_EPI_PACE_NS");
     if (pv && *pv) {
         const int ns = std::atoi(pv);

@@ -624,6 +624,10 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
         const float beta = p.beta;
         constexpr int kVec = 16 / kOutBytes;   // elements per 16-byte piece
         const uint64_t pol_d = ptx::l2_policy(p.hint_d);
+        // C is read exactly once: evict-first, so that it does not push the
+        // operand panels the other tiles still read out of L2 (4096^3 E5M2
+        // beta = 1: +1.8 %, bf16: +0.3 %).
+        const uint64_t pol_c = ptx::l2_policy(1);
         uint32_t chunk_iter = 0;
         int it = 0;
         bool ok = true;
@@ -651,7 +655,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                     if (col0 < p.N) {
                         const uint32_t buf = (chunk_iter + c) % Cf::kEpiBufs;
                         ptx::mbar_arrive_expect_tx(c_bar(ew, buf), kEpiBufBytes);
-                        ptx::tma_load_2d(epi + buf * kEpiBufBytes, &tmC, col0, row0, c_bar(ew, buf));
+                        ptx::tma_load_2d_hint(epi + buf * kEpiBufBytes, &tmC, col0, row0, c_bar(ew, buf), pol_c);
                     }
                 }
             }
@@ -799,7 +803,7 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                     constexpr int kAhead = Cf::kEpiBufs - 1;
                     if (lane == 0 && !((prefetch_c && c < kPrefetchC) || c >= kAhead)) {
                         ptx::mbar_arrive_expect_tx(c_bar(ew, buf), kEpiBufBytes);
-                        ptx::tma_load_2d(sbuf, &tmC, col0, row0, c_bar(ew, buf));
+                        ptx::tma_load_2d_hint(sbuf, &tmC, col0, row0, c_bar(ew, buf), pol_c);
                     }
                     const int cn = c + kAhead;
                     if (kAhead > 0 && cn < kChunks && !(prefetch_c && cn < kPrefetchC) &&
@@ -807,8 +811,8 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                         ptx::bulk_wait_group_read<0>();
                         const uint32_t bn = (chunk_iter + kAhead) % Cf::kEpiBufs;
                         ptx::mbar_arrive_expect_tx(c_bar(ew, bn), kEpiBufBytes);
-                        ptx::tma_load_2d(epi + bn * kEpiBufBytes, &tmC, col0 + kAhead * kChunkCols, row0,
-                                         c_bar(ew, bn));
+                        ptx::tma_load_2d_hint(epi + bn * kEpiBufBytes, &tmC, col0 + kAhead * kChunkCols, row0,
+                                         c_bar(ew, bn), pol_c);
                     }
                     ok = wait_bounded(c_bar(ew, buf), (chunk_iter / Cf::kEpiBufs) & 1u, abort_flag, p,
                                       kSiteEpilogueC, t);
