@@ -502,8 +502,10 @@ def load_clock_probe():
     r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-shared", "-Xcompiler", "-fPIC",
                         "-o", lib, src], capture_output=True, text=True)
     if r.returncode != 0:
+        shutil.rmtree(d, ignore_errors=True)
         return None
     probe = ctypes.CDLL(lib)
+    shutil.rmtree(d, ignore_errors=True)   # the loaded library stays mapped
     probe.launch_clock_probe.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_ulonglong, ctypes.c_void_p]
     probe.launch_stamp.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
     # Launch both kernels once now: the first launch of a kernel loads it,
