@@ -31,8 +31,7 @@ constexpr int64_t kMaxDim = 2147483647;           // TMA coordinates are signed 
 constexpr int64_t kMaxStrideBytes = 1ll << 40;    // TMA global stride limit
 
 struct DeviceState {
-    bool ready = false;
-    int status = GEMM_OK;     // sticky result of the set-up
+    bool ready = false;       // set-up done and succeeded
     int num_sms = 0;
     DeviceStatus* d_status = nullptr;
 };
@@ -83,6 +82,14 @@ uint64_t wait_timeout_ns() {
 int skip_first_stage_setting() {
     const char* v = std::getenv("GEMM_TEST_SKIP_FIRST_STAGE");
     return (v && std::strcmp(v, "1") == 0) ? 1 : 0;
+}
+
+// Test hook (GEMM_TEST_FAIL_SETUP=1): a device's one-time set-up fails
+// before any CUDA call, as a transient failure would, so that tests can
+// check that the failure is not cached and the next call sets up.
+bool fail_setup_setting() {
+    const char* v = std::getenv("GEMM_TEST_FAIL_SETUP");
+    return v && std::strcmp(v, "1") == 0;
 }
 
 // Kernel variant: "pair" (256 x 256 tiles on 2 SMs), "single" (128 x 256),
@@ -201,30 +208,42 @@ bool device_ready(int dev) {
     return g_devices[dev].ready;
 }
 
+// The one-time set-up of `dev` (the current device).  Only a successful
+// set-up is kept: after a failure (reported to that call) the next call
+// tries again.
 int device_state(int dev, DeviceState** out) {
     if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState& st = g_devices[dev];
     if (!st.ready) {
-        st.ready = true;
-        int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        int major = 0, minor = 0, sms = 0, status = GEMM_OK;
+        DeviceStatus* d_status = nullptr;
+        if (fail_setup_setting()) {
+            status = GEMM_ERR_CUDA;
+        } else if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            st.status = GEMM_ERR_CUDA;
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            status = GEMM_ERR_CUDA;
         } else if (major != 10 || minor != 3) {
             GEMM_LOGF("device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
-            st.status = GEMM_ERR_ARCH;
+            status = GEMM_ERR_ARCH;
         } else if (gb300::prepare_kernels_on_current_device() != cudaSuccess) {
-            st.status = GEMM_ERR_CUDA;
-        } else if (cudaMalloc(&st.d_status, sizeof(DeviceStatus)) != cudaSuccess ||
-                   cudaMemset(st.d_status, 0, sizeof(DeviceStatus)) != cudaSuccess) {
-            st.status = GEMM_ERR_CUDA;
+            status = GEMM_ERR_CUDA;
+        } else if (cudaMalloc(&d_status, sizeof(DeviceStatus)) != cudaSuccess ||
+                   cudaMemset(d_status, 0, sizeof(DeviceStatus)) != cudaSuccess) {
+            status = GEMM_ERR_CUDA;
         }
-        if (st.status != GEMM_OK) cudaGetLastError();   // do not leave a sticky-free error behind
+        if (status != GEMM_OK) {
+            if (d_status) cudaFree(d_status);
+            cudaGetLastError();   // do not leave a sticky-free error behind
+            return status;
+        }
+        st.num_sms = sms;
+        st.d_status = d_status;
+        st.ready = true;
     }
     *out = &st;
-    return st.status;
+    return GEMM_OK;
 }
 
 // gemm()'s status record on `dev` if its set-up has run and succeeded,
@@ -233,7 +252,7 @@ DeviceStatus* gemm_status_record(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_mutex);
     const DeviceState& st = g_devices[dev];
-    return st.ready && st.status == GEMM_OK ? st.d_status : nullptr;
+    return st.ready ? st.d_status : nullptr;
 }
 
 DeviceStatus* noalloc_status_record(int dev);   // gemm_noalloc()'s, defined with it below
@@ -1253,7 +1272,9 @@ int noalloc_device_state(int dev, NoAllocState** out) {
     if (!st.ready) {
         int major = 0, minor = 0, sms = 0, status = GEMM_OK;
         void* scratch = nullptr;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        if (fail_setup_setting()) {
+            status = GEMM_ERR_CUDA;
+        } else if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
             status = GEMM_ERR_CUDA;

@@ -34,7 +34,8 @@
  * are device pointers valid on the current device.  gemm() enqueues its
  * work on `stream` and returns without synchronising.  The library keeps
  * one small device status block per device (allocated on the first call on
- * that device) and, per (device, stream), workspaces for stream-K partial
+ * that device; a set-up that fails is reported by that call and tried again
+ * by the next) and, per (device, stream), workspaces for stream-K partial
  * sums and repacked operands, allocated when a call first needs them and
  * grown on demand (growing one synchronises the device).  Calls are
  * thread-safe.

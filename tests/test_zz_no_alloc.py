@@ -311,3 +311,50 @@ def test_both_records_reported_one_per_poll():
     assert H.poll()[0] == binding.GEMM_ERR_DEVICE_TIMEOUT
     assert H.poll()[0] == binding.GEMM_ERR_DEVICE_TIMEOUT
     assert H.poll()[0] == 0
+
+
+_CHILD_RETRY = r"""
+import json, os, sys
+sys.path.insert(0, os.environ["REPO_ROOT"])
+import torch
+from dense_tensor_core_02_gb300 import binding
+M, N, K = 256, 264, 192
+g = torch.Generator().manual_seed(5)
+A = torch.randint(-4, 5, (M, K), generator=g).half().cuda()
+B = torch.randint(-4, 5, (K, N), generator=g).half().cuda()
+out = {}
+def run(fn):
+    D = torch.full((M, N), float("nan"), device="cuda")
+    rc = fn(D, A, B, None, M, N, K, K, N, N, N, 0, 0, 1.0, 0.0, binding.F16, binding.F32, None)
+    torch.cuda.synchronize()
+    return rc, D
+want = (A.float().cpu() @ B.float().cpu())
+for name, fn in (("noalloc", binding.gemm_noalloc), ("gemm", binding.gemm)):
+    os.environ["GEMM_TEST_FAIL_SETUP"] = "1"
+    out[name + "_failed"] = run(fn)[0]
+    del os.environ["GEMM_TEST_FAIL_SETUP"]
+    rc, D = run(fn)
+    out[name + "_retried"] = rc
+    out[name + "_exact"] = bool(torch.equal(D.cpu(), want))
+out["poll"] = binding.gemm_poll_device_error()[0]
+print(json.dumps(out))
+"""
+
+
+def test_failed_setup_is_retried():
+    """A device set-up that fails (host test hook, before any CUDA call) is
+    reported by that call and not remembered: the next call on the device
+    sets up and computes the exact result.  For gemm_noalloc() and gemm(),
+    in a fresh interpreter where neither has set the device up."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    env = dict(os.environ, REPO_ROOT=ROOT)
+    env.pop("GEMM_TEST_FAIL_SETUP", None)
+    proc = subprocess.run([sys.executable, "-c", _CHILD_RETRY], env=env, capture_output=True, text=True,
+                          timeout=300)
+    assert proc.returncode == 0, proc.stderr[-3000:]
+    out = json.loads(proc.stdout.strip().splitlines()[-1])
+    for name in ("noalloc", "gemm"):
+        assert out[name + "_failed"] == -7, out            # GEMM_ERR_CUDA, nothing enqueued
+        assert out[name + "_retried"] == 0 and out[name + "_exact"], out
+    assert out["poll"] == 0, out
