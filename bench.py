@@ -112,12 +112,12 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic(case_name):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
+def _profiled(case_name):
+    """The committed ncu figures of a workload (profiles/traffic_<case>.txt)
+    if they were taken on the current kernel source, else {}."""
     path = os.path.join(ROOT, "profiles", "traffic_%s.txt" % case_name)
     if not os.path.exists(path):
-        return None
+        return {}
     vals = {}
     with open(path) as f:
         for line in f:
@@ -125,9 +125,24 @@ def _profiled_traffic(case_name):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
     if vals.get("kernel_source_sha256_16") != kernel_source_hash():
-        return None
+        return {}
+    return vals
+
+
+def _profiled_traffic(case_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
     try:
-        return int(float(vals["dram_bytes_per_launch"]))
+        return int(float(_profiled(case_name)["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+def _profiled_duration_us(case_name):
+    """The ncu launch duration (us) in the committed summary, on the current
+    kernel source; else None."""
+    try:
+        return float(_profiled(case_name)["ncu_duration_ns"]) / 1e3
     except (KeyError, ValueError):
         return None
 
@@ -787,7 +802,11 @@ def per_config_row(torch, case, index, dev, stream, peaks, num_sms, flush, probe
         "sm_mhz_during": statistics.mean(mhz) if mhz else None,
         "clock_samples": n_samples,
         "traffic": _profiled_traffic(case.name),
+        "ncu_us": _profiled_duration_us(case.name),
     }
+    if row["ncu_us"] and roof["bound"] == "tensor":
+        # the committed ncu launch (one serialised launch) against the same peak
+        row["frac_ncu"] = case.flops / (row["ncu_us"] * 1e-6) / 1e12 / peak_burst
     if "limited_by" in roof:
         row["limited_by"] = roof["limited_by"]
     if mhz and roof["bound"] == "tensor":
