@@ -387,11 +387,24 @@ int64_t env_int64(const char* name, int64_t dflt) {
     return (v && *v) ? std::strtoll(v, nullptr, 10) : dflt;
 }
 
+// Aligned fp16 / bf16 problems with a short K and a small D run soonest on
+// the mma.sync route's atom kernel.  Graph-replayed device time per launch
+// on GB300 (atom kernel vs tcgen05 kernel, us): 16x8x16 1.9 vs 2.8, 64x64x8
+// 1.8 vs 3.1, 256x256x32 2.9 vs 3.1, 512x512x16 2.4 vs 3.2; from K = 64 on
+// the tcgen05 kernel is as fast or faster (64^3 3.6 vs 3.0, 8x8x512 14.1 vs
+// 4.6, 2048^2 x 8 14.4 vs 6.7).  GEMM_SYNC_MAX_WORK replaces the rule by
+// M*N*K <= its value.
+bool sync_pays(int64_t M, int64_t N, int64_t K) {
+    const int64_t bound = env_int64("GEMM_SYNC_MAX_WORK", -1);
+    if (bound >= 0) return M * N * K <= bound;
+    return K <= 32 && M * N <= (int64_t)1 << 18;
+}
+
 // Which kernel:
 //  * the tcgen05 kernel on the caller's buffers when it can take them as
 //    they are (TMA's alignment rule; 8-bit operands K-major), except for
-//    fp16 / bf16 problems so small that its set-up dominates
-//    (M*N*K <= GEMM_SYNC_MAX_WORK, default 2^15 = 32^3);
+//    fp16 / bf16 problems so small that the mma.sync route's atom kernel
+//    finishes sooner (sync_pays);
 //  * otherwise, when the caller may allocate and the problem pays for the
 //    copies (M*N*K > GEMM_REPACK_MIN_WORK, default 2^22; always for 8-bit
 //    operands), the tcgen05 kernel on repacked copies (gemm_repacked);
@@ -405,10 +418,21 @@ Route route_for(bool direct_ok, bool f8, bool can_allocate, int64_t M, int64_t N
     const int64_t work = M * N * K;
     if (!f8 && v && std::strcmp(v, "mma_sync") == 0) return kRouteSync;
     const bool force_tc = v && std::strcmp(v, "tcgen05") == 0;
-    if (direct_ok)
-        return (!f8 && !force_tc && work <= env_int64("GEMM_SYNC_MAX_WORK", 1 << 15)) ? kRouteSync : kRouteTcgen05;
+    if (direct_ok) return (!f8 && !force_tc && sync_pays(M, N, K)) ? kRouteSync : kRouteTcgen05;
     if (can_allocate && (f8 || force_tc || work > env_int64("GEMM_REPACK_MIN_WORK", 1 << 22))) return kRouteRepack;
     return f8 ? kRouteNone : kRouteSync;
+}
+
+// Which kernel of the mma.sync route.  Graph-replayed device time per launch
+// on GB300 (us; the one-warp-per-16x8-block atom kernel vs the tiled one):
+// 16x8x16 1.6 vs 4.0, 128^3 5.9 vs 12.1, 256^3 10.9 vs 20.2, 1000x64x64 3.8 vs
+// 6.8; the tiled kernel's shared-memory reuse wins once D is large
+// (2048^2 x 8: 40.5 vs 11.1; 512^3: 42.8 vs 36.7).  GEMM_SYNC_ATOM_MAX_WORK
+// replaces the rule by M*N*K <= its value.
+bool sync_atom_kernel(int64_t M, int64_t N, int64_t K) {
+    const int64_t bound = env_int64("GEMM_SYNC_ATOM_MAX_WORK", -1);
+    if (bound >= 0) return M * N * K <= bound;
+    return M * N <= (int64_t)1 << 18 && M * N * K <= (int64_t)1 << 24;
 }
 
 cudaError_t launch_sync(void* D, const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
@@ -433,6 +457,7 @@ cudaError_t launch_sync(void* D, const void* A, const void* B, const void* C, in
     sp.in_bf16 = in_dtype == GEMM_BF16 ? 1 : 0;
     sp.out = out_kind;
     sp.has_c = has_c ? 1 : 0;
+    sp.atom = sync_atom_kernel(M, N, K) ? 1 : 0;
     return gb300::launch_mma_sync(sp, s);
 }
 

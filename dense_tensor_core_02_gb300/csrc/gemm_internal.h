@@ -44,6 +44,7 @@ struct SyncParams {
     int in_bf16;   // A and B are bf16 (else f16)
     int out;       // OutKind of C and D
     int has_c;     // beta != 0
+    int atom;      // 1: the one-warp-per-16x8-block kernel (tiny problems), 0: the tiled one
 };
 
 cudaError_t launch_mma_sync(const SyncParams& p, cudaStream_t stream);

@@ -25,9 +25,17 @@
 // atom, as the lowering does for K = 8 (mod 16).  Staged columns past K are
 // zero, so the last k16 atom of a ragged K adds nothing for them.
 //
-// CTA tile 128 x 128, 8 warps in a 2 x 4 grid of 64 x 32 warp tiles
-// (4 x 4 atoms each); K slabs of 32 double-buffered in shared memory with
-// padded rows, the next slab's loads in flight during the current MMAs.
+// Two kernels share this lowering:
+//  * gemm_mma_sync_kernel: CTA tile 128 x 128, 8 warps in a 2 x 4 grid of
+//    64 x 32 warp tiles (4 x 4 atoms each); K slabs of 32 double-buffered in
+//    shared memory with padded rows, the next slab's loads in flight during
+//    the current MMAs.  For layouts TMA cannot take, at any size.
+//  * gemm_mma_atom_kernel: one warp per 16 x 8 block of D (one atom wide),
+//    its fragments read straight from global memory into the slots above --
+//    the demonstration program's own shape, with no shared staging and no
+//    CTA barrier.  For tiny problems, whose time is the launch and a chain
+//    of memory latencies: a 16 x 8 x 16 product takes 1.6 us per launch
+//    (graph-replayed) against 4.1 us for the tiled kernel's 256-thread CTA.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -252,8 +260,100 @@ __global__ void __launch_bounds__(kSThreads) gemm_mma_sync_kernel(SyncParams p) 
     }
 }
 
+constexpr int kAtomWarps = 4;   // warps per CTA of the atom kernel
+// K steps (of 16) whose fragments the atom kernel loads together: 1 for
+// K <= 32, where the extra predicated loads of a longer group cost more than
+// they hide (16x8x16: 1.6 vs 2.1 us per launch), else 4 (16x16x4096: 139 vs
+// 183 us; 128^3: 5.9 vs 7.3 us)
+constexpr int kAtomStepsDeep = 4;
+constexpr int64_t kAtomShallowK = 32;
+
+// D = alpha * op(A) @ op(B) (+ beta * C) one 16 x 8 block per warp.  Lane
+// 4 g + t loads its A slots (rows g, g + 8; K columns 2 t, 2 t + 1 and
+// 8 more) and B slots (column g; the same K rows) from global memory,
+// out-of-range elements as 0, so a ragged M, N or K needs no other care;
+// a K remainder of at most 8 takes the m16n8k8 atom, as in the tiled kernel.
+template <int kIn, int kOut, bool kHasC, int kSteps>
+__global__ void __launch_bounds__(kAtomWarps * 32) gemm_mma_atom_kernel(SyncParams p) {
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
+    const int lane = threadIdx.x % 32;
+    const int g = lane / 4, tq = lane % 4;
+    const uint16_t* A = static_cast<const uint16_t*>(p.A);
+    const uint16_t* B = static_cast<const uint16_t*>(p.B);
+    const int64_t n_blocks = (p.N + 7) / 8;
+    const int64_t blocks = (p.M + 15) / 16 * n_blocks;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+    // element steps of op(A) along its rows (M) and along K, and of op(B)
+    // along K and its columns (N)
+    const int64_t a_sm = p.transA ? 1 : p.lda, a_sk = p.transA ? p.lda : 1;
+    const int64_t b_sk = p.transB ? 1 : p.ldb, b_sn = p.transB ? p.ldb : 1;
+    for (int64_t blk = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; blk < blocks; blk += warps) {
+        const int64_t m0 = blk / n_blocks * 16, n0 = blk % n_blocks * 8;
+        // this lane's rows of op(A) (g, g + 8) and column of op(B) (g)
+        const bool in_r0 = m0 + g < p.M, in_r1 = m0 + g + 8 < p.M, in_n = n0 + g < p.N;
+        const uint16_t* a_r0 = A + (in_r0 ? (m0 + g) * a_sm : 0);
+        const uint16_t* a_r1 = A + (in_r1 ? (m0 + g + 8) * a_sm : 0);
+        const uint16_t* b_n = B + (in_n ? (n0 + g) * b_sn : 0);
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // kSteps K steps at a time: all their fragment loads are issued
+        // (predicated, with no branch between them) before the first of
+        // their MMAs, so the steps share one memory latency instead of paying
+        // one each.  Steps past K load nothing.
+        for (int64_t kc = 0; kc < p.K; kc += 16 * kSteps) {
+            const int64_t left = p.K - kc;   // the same for the whole warp
+            uint32_t af[kSteps][4], bf[kSteps][2];
+#pragma unroll
+            for (int st = 0; st < kSteps; ++st) {
+#pragma unroll
+                for (int kHi = 0; kHi < 2; ++kHi) {
+                    const int64_t k = kc + 16 * st + 2 * tq + 8 * kHi;   // K columns k, k + 1
+                    const bool k0_in = k < p.K, k1_in = k + 1 < p.K;
+                    // A slots: w = 2 kHi + rM, as in the tiled kernel
+                    af[st][2 * kHi] = pack_halves(in_r0 && k0_in ? a_r0[k * a_sk] : (uint16_t)0,
+                                                  in_r0 && k1_in ? a_r0[(k + 1) * a_sk] : (uint16_t)0);
+                    af[st][2 * kHi + 1] = pack_halves(in_r1 && k0_in ? a_r1[k * a_sk] : (uint16_t)0,
+                                                      in_r1 && k1_in ? a_r1[(k + 1) * a_sk] : (uint16_t)0);
+                    bf[st][kHi] = pack_halves(in_n && k0_in ? b_n[k * b_sk] : (uint16_t)0,
+                                              in_n && k1_in ? b_n[(k + 1) * b_sk] : (uint16_t)0);
+                }
+            }
+#pragma unroll
+            for (int st = 0; st < kSteps; ++st) {
+                const int64_t k_left = left - 16 * st;
+                if (k_left <= 0) break;
+                if (k_left > 8)
+                    mma_16816<kIn>(acc, af[st], bf[st]);
+                else
+                    mma_1688<kIn>(acc, af[st][0], af[st][1], bf[st][0]);
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            const int64_t m = m0 + g + 8 * (s / 2);
+            const int64_t n = n0 + 2 * tq + s % 2;
+            if (m < p.M && n < p.N) {
+                float d;
+                if constexpr (kHasC)
+                    d = fmaf(p.alpha, acc[s], p.beta * load_out<kOut>(p.C, m * p.ldc + n));
+                else
+                    d = p.alpha * acc[s];
+                store_out<kOut>(p.D, m * p.ldd + n, d);
+            }
+        }
+    }
+}
+
 template <int kIn, int kOut, bool kHasC>
 cudaError_t launch_sync_one(const SyncParams& p, cudaStream_t stream) {
+    if (p.atom) {
+        const int64_t blocks = (p.M + 15) / 16 * ((p.N + 7) / 8);
+        const int64_t warps = blocks < kAtomWarps ? blocks : kAtomWarps;
+        const int64_t ctas = (blocks + warps - 1) / warps;
+        const dim3 grid((unsigned)(ctas < 65535 ? ctas : 65535)), block((unsigned)(32 * warps));
+        if (p.K <= kAtomShallowK) return launch_with_pdl(gemm_mma_atom_kernel<kIn, kOut, kHasC, 1>, grid, block, stream, p);
+        return launch_with_pdl(gemm_mma_atom_kernel<kIn, kOut, kHasC, kAtomStepsDeep>, grid, block, stream, p);
+    }
     const int64_t m_tiles = (p.M + kSBM - 1) / kSBM;
     const dim3 grid((unsigned)((p.N + kSBN - 1) / kSBN), (unsigned)(m_tiles < 65535 ? m_tiles : 65535));
     return launch_with_pdl(gemm_mma_sync_kernel<kIn, kOut, kHasC>, grid, dim3(kSThreads), stream, p);

@@ -118,14 +118,19 @@ typedef enum {
  *     ldc, ldd times their element sizes are multiples of 16 bytes (TMA's
  *     rule), and 8-bit operands are K-major (A stored [M, K], transA = 0;
  *     B stored [N, K], transB = 1);
- *   - fp16 / bf16 problems with M*N*K <= 2^15 (GEMM_SYNC_MAX_WORK): a
- *     warp-level mma.sync kernel, whose set-up is cheaper;
+ *   - aligned fp16 / bf16 problems with K <= 32 and M*N <= 2^18: the
+ *     warp-level mma.sync route, whose one-warp-per-16x8-block kernel
+ *     finishes a launch sooner (GEMM_SYNC_MAX_WORK=w replaces this rule
+ *     by M*N*K <= w);
  *   - other layouts with M*N*K > 2^22 (GEMM_REPACK_MIN_WORK), and every
  *     other 8-bit layout: the tcgen05 kernel on workspace copies (operands
  *     copied into 16-byte-aligned rows, 8-bit MN-major operands transposed
  *     to K-major, a misaligned D computed in workspace and copied back);
- *   - the remaining fp16 / bf16 layouts: the mma.sync kernel, which reads
- *     and writes element by element.
+ *   - the remaining fp16 / bf16 layouts: the mma.sync route, which reads
+ *     and writes element by element (one warp per 16 x 8 block of D while
+ *     M*N <= 2^18 and M*N*K <= 2^24, else 128 x 128 CTA tiles staged in
+ *     shared memory; GEMM_SYNC_ATOM_MAX_WORK=w replaces this rule by
+ *     M*N*K <= w).
  * All accumulate in fp32 and agree within the documented tolerance.
  * GEMM_PATH=tcgen05 or mma_sync forces a kernel where it can run.
  * CUDA graphs: gemm() may be called while `stream` is being captured, as

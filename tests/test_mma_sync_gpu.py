@@ -6,7 +6,10 @@ describe -- and tiny problems.  It runs every layout that gemm_noalloc()
 receives off the 16-byte grid, and gemm()'s small ones (larger ones are
 repacked for the tcgen05 kernel; see test_repack_gpu.py).  The tests here
 force it (GEMM_PATH=mma_sync) on those layouts and on the workloads the
-tcgen05 kernel is tested on.  The shared parity cases (golden atom, page
+tcgen05 kernel is tested on.  The route has two kernels, the tiled one and,
+for problems with M*N*K <= GEMM_SYNC_ATOM_MAX_WORK, the one-warp-per-16x8-
+block atom kernel; the layout tests run each of them on every layout by
+setting that bound to 0 or beyond the problem.  The shared parity cases (golden atom, page
 test matrix, transposes, ragged canaries, in place, 16-bit outputs,
 alpha/beta) run on it through the "mma_sync" variant of the main GPU test
 module.
@@ -44,11 +47,16 @@ ODD_LAYOUTS = [
 ]
 
 
+# GEMM_SYNC_ATOM_MAX_WORK for each of the route's two kernels
+SYNC_KERNELS = {"tiled": "0", "atom": str(1 << 62)}
+
+
+@pytest.mark.parametrize("kernel", list(SYNC_KERNELS))
 @pytest.mark.parametrize("transA", [0, 1])
 @pytest.mark.parametrize("transB", [0, 1])
 @pytest.mark.parametrize("layout", ODD_LAYOUTS, ids=lambda l: "%dx%dx%d_o%s" % (l[0], l[1], l[2],
                                                                                "".join(map(str, l[3]))))
-def test_odd_layouts_integers_exact(layout, transA, transB):
+def test_odd_layouts_integers_exact(layout, transA, transB, kernel):
     """Layouts TMA cannot take; integer-valued inputs, so the fp32 result is
     exact."""
     M, N, K, offs, lds = layout
@@ -60,7 +68,7 @@ def test_odd_layouts_integers_exact(layout, transA, transB):
     A = H.int_matrix((K, M) if transA else (M, K), -8, 8, "f16", seed)
     B = H.int_matrix((N, K) if transB else (K, N), -8, 8, "f16", seed + 1)
     C = H.int_matrix((M, N), -100, 100, "f32", seed + 2)
-    with H.env(GEMM_PATH="mma_sync"):
+    with H.env(GEMM_PATH="mma_sync", GEMM_SYNC_ATOM_MAX_WORK=SYNC_KERNELS[kernel]):
         D, Dbuf, rc = H.run_layout(A, B, C, M, N, K, offs=offs, lds=lds, transA=transA, transB=transB, beta=1.0)
     assert rc == 0
     ref, _ = H.oracle_full(A, B, C, M, N, K, transA=transA, transB=transB, beta=1.0)
@@ -69,16 +77,17 @@ def test_odd_layouts_integers_exact(layout, transA, transB):
     H.check_canaries(Dbuf, M, N, offs[3], ldd)
 
 
+@pytest.mark.parametrize("kernel", list(SYNC_KERNELS))
 @pytest.mark.parametrize("in_dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("out_dtype", ["f32", "f16", "bf16"])
-def test_odd_layouts_random(in_dtype, out_dtype):
+def test_odd_layouts_random(in_dtype, out_dtype, kernel):
     M, N, K = 333, 250, 517
     seed = 7 + 3 * (in_dtype == "bf16") + ["f32", "f16", "bf16"].index(out_dtype)
     A = H.normal_matrix((K, M), in_dtype, seed)
     B = H.normal_matrix((K, N), in_dtype, seed + 1)
     C = H.normal_matrix((M, N), out_dtype, seed + 2)
     kw = dict(transA=1, alpha=-1.25, beta=0.5, in_dtype=in_dtype, out_dtype=out_dtype)
-    with H.env(GEMM_PATH="mma_sync"):
+    with H.env(GEMM_PATH="mma_sync", GEMM_SYNC_ATOM_MAX_WORK=SYNC_KERNELS[kernel]):
         D, Dbuf, rc = H.run_layout(A, B, C, M, N, K, offs=(1, 1, 1, 1), lds=(M + 1, N + 3, N + 1, N + 5), **kw)
     assert rc == 0
     ref, bound = H.oracle_full(A, B, C, M, N, K, **kw)
@@ -121,8 +130,9 @@ TINY = [(1, 1, 1), (16, 8, 16), (8, 16, 8), (63, 65, 17), (64, 64, 64), (5, 300,
 
 @pytest.mark.parametrize("shape", TINY, ids=lambda s: "x".join(map(str, s)))
 def test_tiny_problems_default_routing(shape):
-    """Tiny problems through the default routing (the smallest take the
-    mma.sync kernel, the rest the tcgen05 kernel): exact on integers."""
+    """Tiny problems through the default routing (those with K <= 32 take
+    the mma.sync route's atom kernel, the rest the tcgen05 kernel): exact on
+    integers."""
     M, N, K = shape
     A = H.int_matrix((M, K), -8, 8, "bf16", M + N + K)
     B = H.int_matrix((N, K), -8, 8, "bf16", M * N + K)
@@ -131,6 +141,34 @@ def test_tiny_problems_default_routing(shape):
     assert rc == 0
     ref, _ = H.oracle_full(A, B, None, M, N, K, transB=1, in_dtype="bf16", alpha=2.0)
     H.assert_exact(D.numpy(), ref, "tiny %s" % (shape,))
+
+
+# (M, N, K, transA, transB, in_dtype, out_dtype, beta): tiny problems, each
+# kernel of the route forced; K remainders of 0, 1..8 (the k8 atom) and 9..15
+TINY_FORCED = [(16, 8, 16, 0, 0, "f16", "f32", 0.0), (1, 1, 1, 1, 1, "bf16", "f16", 1.0),
+               (15, 9, 8, 1, 0, "f16", "bf16", -0.5), (33, 17, 24, 0, 1, "bf16", "f32", 2.0),
+               (7, 40, 41, 1, 1, "f16", "f32", 1.0), (48, 24, 9, 0, 0, "bf16", "bf16", 0.0)]
+
+
+@pytest.mark.parametrize("kernel", list(SYNC_KERNELS))
+@pytest.mark.parametrize("shape", TINY_FORCED, ids=lambda s: "%dx%dx%d_t%d%d_%s_%s_b%g" % s)
+def test_tiny_problems_each_sync_kernel(shape, kernel):
+    """Both kernels of the mma.sync route on tiny problems, every transpose
+    pair, 16-bit and fp32 outputs, with and without C: exact on integers."""
+    M, N, K, transA, transB, in_dtype, out_dtype, beta = shape
+    seed = 1000 + M * 7 + N * 3 + K
+    A = H.int_matrix((K, M) if transA else (M, K), -8, 8, in_dtype, seed)
+    B = H.int_matrix((N, K) if transB else (K, N), -8, 8, in_dtype, seed + 1)
+    C = H.int_matrix((M, N), -50, 50, out_dtype, seed + 2) if beta else None
+    kw = dict(transA=transA, transB=transB, alpha=1.0, beta=beta, in_dtype=in_dtype, out_dtype=out_dtype)
+    with H.env(GEMM_PATH="mma_sync", GEMM_SYNC_ATOM_MAX_WORK=SYNC_KERNELS[kernel]):
+        D, rc = H.run_gemm(A, B, C, M, N, K, **kw)
+    assert rc == 0
+    ref, bound = H.oracle_full(A, B, C, M, N, K, **kw)
+    if out_dtype == "f32":
+        H.assert_exact(D.numpy(), ref, "tiny %s on the %s kernel" % (shape, kernel))
+    else:
+        H.assert_close(D.double().numpy(), ref, bound, out_dtype, "tiny %s on the %s kernel" % (shape, kernel))
 
 
 SMALL_CASES = [c for c in CASES if not c.mx and c.M * c.N * c.K <= 1024 ** 3]
