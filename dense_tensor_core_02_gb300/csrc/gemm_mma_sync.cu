@@ -263,8 +263,8 @@ __global__ void __launch_bounds__(kSThreads) gemm_mma_sync_kernel(SyncParams p) 
 constexpr int kAtomWarps = 4;   // warps per CTA of the atom kernel
 // K steps (of 16) whose fragments the atom kernel loads together: 1 for
 // K <= 32, where the extra predicated loads of a longer group cost more than
-// they hide (16x8x16: 1.6 vs 2.1 us per launch), else 4 (16x16x4096: 139 vs
-// 183 us; 128^3: 5.9 vs 7.3 us)
+// they hide (16x8x16: 1.6 vs 2.1 us per launch), else 4 (16x16x4096: 150 vs
+// 183 us; 128^3: 6.2 vs 7.3 us; graph-replayed on GB300)
 constexpr int kAtomStepsDeep = 4;
 constexpr int64_t kAtomShallowK = 32;
 
