@@ -3,6 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--case NAME] [--no-e2e] [--no-cpu-baseline]
                     [--no-per-config] [--no-clock-study] [--cpu-budget SECONDS]
+    python bench.py --library-peaks
 
 A step is one GEMM call through the C ABI over the resident, seeded
 synthetic inputs of the workload (default: M = N = K = 8192, fp16
@@ -43,6 +44,14 @@ At N = 1 the line also carries, outside the timed region:
 --impl reference times the CPU oracle instead (the only other
 implementation of this operation in the repository), on bounded samples
 of the same workload, on the host cores.
+
+--library-peaks measures, instead of this library, the vendor library's
+8192^3 throughput through torch (cuBLAS bf16, cuBLASLt E4M3 with per-tensor
+scales to bf16 and to fp32 D): the burst (best of three 10-launch runs after
+an idle second) and the sustained rate (median of the last half of a 3 s
+loop).  It gives the 8-bit peak that the tensor fractions of 8-bit
+workloads can be read against; the line's own fractions keep the measured
+bf16 figure x 2.
 """
 from __future__ import annotations
 
@@ -225,7 +234,67 @@ def _args():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=100.0,
                     help="target wall time of the whole CPU oracle table (all workloads, both thread counts)")
+    ap.add_argument("--library-peaks", action="store_true",
+                    help="measure the vendor library's bf16 and E4M3 8192^3 throughput instead (one JSON line)")
     return ap.parse_args()
+
+
+def library_peaks():
+    """cuBLAS / cuBLASLt 8192^3 throughput through torch, burst and
+    sustained (see the module docstring).  Measurement only: the library's
+    own path never calls them."""
+    import torch
+
+    n = 8192
+    flop = 2.0 * n ** 3
+    g = torch.Generator(device="cuda").manual_seed(3)
+    a16 = torch.randn(n, n, device="cuda", generator=g).to(torch.bfloat16)
+    b16 = torch.randn(n, n, device="cuda", generator=g).to(torch.bfloat16).t()
+    a8 = torch.randn(n, n, device="cuda", generator=g).to(torch.float8_e4m3fn)
+    b8 = torch.randn(n, n, device="cuda", generator=g).to(torch.float8_e4m3fn).t()   # column-major, as cuBLASLt wants
+    one = torch.ones((), device="cuda")
+    ops = {
+        "bf16_to_bf16": lambda: torch.mm(a16, b16),
+        "e4m3_to_bf16": lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one, out_dtype=torch.bfloat16),
+        "e4m3_to_f32": lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one, out_dtype=torch.float32),
+    }
+    out = {"workload": "M=N=K=8192, random operands", "unit": UNIT}
+    for name, fn in ops.items():
+        try:
+            fn()
+            torch.cuda.synchronize()
+        except Exception as e:   # an op this torch build or GPU does not offer
+            out[name] = {"unavailable": str(e).splitlines()[0][:200]}
+            continue
+        burst = []
+        for _ in range(3):
+            time.sleep(1.0)
+            e0, e1 = _event_pair(torch)
+            e0.record()
+            for _ in range(10):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            burst.append(flop * 10 / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+        time.sleep(1.0)
+        rates = []
+        t_end = time.time() + 3.0
+        while time.time() < t_end:
+            e0, e1 = _event_pair(torch)
+            e0.record()
+            for _ in range(20):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            rates.append(flop * 20 / (e0.elapsed_time(e1) * 1e-3) / 1e12)
+        tail = rates[len(rates) // 2:]
+        out[name] = {"burst": max(burst), "burst_runs": burst, "sustained": statistics.median(tail),
+                     "sustained_chunks": len(tail)}
+    for kind in ("burst", "sustained"):
+        if "burst" in out.get("bf16_to_bf16", {}) and "burst" in out.get("e4m3_to_f32", {}):
+            out["e4m3_to_f32_over_bf16_" + kind] = out["e4m3_to_f32"][kind] / out["bf16_to_bf16"][kind]
+    print(json.dumps(out), flush=True)
+    return 0
 
 
 def _workload_config(case, n_gpus):
@@ -1142,6 +1211,8 @@ def main():
     args = _args()
     from dense_tensor_core_02_gb300.inputs import CASE_BY_NAME, HEADLINE
     case = CASE_BY_NAME[args.case] if args.case else HEADLINE
+    if args.library_peaks:
+        return library_peaks()
     if args.impl == "reference":
         return run_reference(args, case)
     return run_ours(args, case)
