@@ -303,6 +303,54 @@ int encode_2d(CUtensorMap* map, int dt, const void* ptr, int64_t dim0, int64_t d
     return GEMM_OK;
 }
 
+// One pipeline stage of a K-major operand (stored [rows][K], K contiguous)
+// as a single box.  The K extent of each 128-byte shared row (bk elements)
+// is the map's first dimension and the K chunks its third: dims {bk, rows,
+// K / bk}, box {bk, box_rows, sub}; the box lands as `sub` consecutive
+// {bk, box_rows} slabs, the image of `sub` 2-D boxes.  K must be a multiple
+// of bk: a partial chunk would read on into the next row instead of reading
+// zeros.
+int encode_kmajor_stage(CUtensorMap* map, int dt, const void* ptr, int64_t K, int64_t rows, int64_t ld, uint32_t bk,
+                        uint32_t box_rows, uint32_t sub) {
+    cuuint64_t dims[3] = {(cuuint64_t)bk, (cuuint64_t)rows, (cuuint64_t)(K / bk)};
+    cuuint64_t strides[2] = {(cuuint64_t)row_bytes(dt, ld), (cuuint64_t)row_bytes(dt, bk)};
+    cuuint32_t box[3] = {bk, box_rows, sub};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, tma_dtype(dt), 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        GEMM_LOGF("cuTensorMapEncodeTiled failed (%d): K-major stage map, K %lld, rows %lld, ld %lld", (int)r,
+                  (long long)K, (long long)rows, (long long)ld);
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+// One pipeline stage of an MN-major operand (stored [K][mn], mn contiguous)
+// as a single box: dims {64, bk, mn / 64, K / bk} (64 MN elements of a K
+// row, the bk K rows of a sub-block, the 64-wide MN chunks, the sub-blocks),
+// box {64, bk, box_mn / 64, sub}, landing as [sub-block][MN chunk][K row]:
+// the image of the 2-D boxes {64, bk}.  mn and K must be multiples of 64 and
+// bk: partial chunks would read past the rows instead of reading zeros.
+int encode_mnmajor_stage(CUtensorMap* map, int dt, const void* ptr, int64_t mn, int64_t K, int64_t ld, uint32_t bk,
+                         uint32_t box_mn, uint32_t sub) {
+    cuuint64_t dims[4] = {64, (cuuint64_t)bk, (cuuint64_t)(mn / 64), (cuuint64_t)(K / bk)};
+    cuuint64_t strides[3] = {(cuuint64_t)row_bytes(dt, ld), (cuuint64_t)row_bytes(dt, 64),
+                             (cuuint64_t)row_bytes(dt, ld) * bk};
+    cuuint32_t box[4] = {64, bk, box_mn / 64, sub};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(map, tma_dtype(dt), 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        GEMM_LOGF("cuTensorMapEncodeTiled failed (%d): MN-major stage map, mn %lld, K %lld, ld %lld", (int)r,
+                  (long long)mn, (long long)K, (long long)ld);
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
 // The rearranged MX scales (see GemmParams::sf_a_groups) as a 2-D tensor of
 // 32-bit words: rows of 128 words (one 512-byte chunk), `box_rows` chunks
 // per copy, no swizzle.
@@ -699,7 +747,7 @@ int validate_scales(const void* D, const void* SFA, const void* SFB, int64_t M, 
 // record and, for stream-K, the workspace.
 int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, const void* B, const void* C,
                      int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA,
-                     int transB, float alpha, float beta, int in_dtype, int out_dtype) {
+                     int transB, float alpha, float beta, int in_dtype, int out_dtype, bool stage_boxes = true) {
     const bool has_c = beta != 0.0f;
     const bool f8 = is_f8(in_dtype) || in_dtype == GEMM_E2M1;   // 128 K elements per 128-byte shared row
     const int osz = elem_size(out_dtype);
@@ -709,17 +757,51 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     // 224-wide tiles (wave-fitted or block-scaled) stage B K-major only
     if (pl.tile_n == gb300::tcgen05_fit_n() && !transB) return GEMM_ERR_INVALID_ARG;
     const uint32_t bk = (uint32_t)gb300::tcgen05_block_k(f8);   // K elements per 128-byte row
+    // K sub-blocks per pipeline stage, and the rows of A and B one CTA stages
+    const uint32_t sub = (uint32_t)(gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps) / (int)bk);
+    const uint32_t rows_a = (uint32_t)gb300::tcgen05_load_rows_a();
+    const uint32_t rows_b = (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n);
+    // A whole stage in one box for the kernels whose stages hold two K
+    // sub-blocks, where the sizes allow it (GEMM_STAGE_BOXES=0: always the
+    // 2-D boxes).  A TMA copy costs the SM about the same time whatever its
+    // size up to 32 KB: on GB300 one 32 KB box moves 70 bytes per SM clock,
+    // two 16 KB boxes 64, four 8 KB boxes 54.  Measured against the 2-D
+    // boxes: 8192^3 +0.6 to +0.8 %, 4096^3 bf16 beta = 1 +1.0 %, 8192^2 x 4096
+    // +0.9 %.  The 8-epilogue-warp kernel (one sub-block per stage, bound by
+    // its D stores) lost 1.7 % with the MN-major chunks merged, and keeps them
+    // apart.
+    const char* sb = std::getenv("GEMM_STAGE_BOXES");
+    const bool boxes_ok = stage_boxes && sub > 1 && K % bk == 0 && !(sb && std::strcmp(sb, "0") == 0);
+    int a_dims = 2, b_dims = 2;
     // A: K-major (transA = 0) as [M rows][K], else MN-major as [K rows][M]
-    if (!transA)
-        rc = encode_2d(&L->a, in_dtype, A, K, M, lda, bk, (uint32_t)gb300::tcgen05_load_rows_a());
-    else
+    if (!transA) {
+        if (boxes_ok) {
+            rc = encode_kmajor_stage(&L->a, in_dtype, A, K, M, lda, bk, rows_a, sub);
+            a_dims = 3;
+        } else {
+            rc = encode_2d(&L->a, in_dtype, A, K, M, lda, bk, rows_a);
+        }
+    } else if (boxes_ok && M % 64 == 0) {
+        rc = encode_mnmajor_stage(&L->a, in_dtype, A, M, K, lda, bk, rows_a, sub);
+        a_dims = 4;
+    } else {
         rc = encode_2d(&L->a, in_dtype, A, M, K, lda, 64, bk);
+    }
     if (rc != GEMM_OK) return rc;
     // B: K-major (transB = 1) as [N rows][K], else MN-major as [K rows][N]
-    if (transB)
-        rc = encode_2d(&L->b, in_dtype, B, K, N, ldb, bk, (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n));
-    else
+    if (transB) {
+        if (boxes_ok) {
+            rc = encode_kmajor_stage(&L->b, in_dtype, B, K, N, ldb, bk, rows_b, sub);
+            b_dims = 3;
+        } else {
+            rc = encode_2d(&L->b, in_dtype, B, K, N, ldb, bk, rows_b);
+        }
+    } else if (boxes_ok && N % 64 == 0) {
+        rc = encode_mnmajor_stage(&L->b, in_dtype, B, N, K, ldb, bk, rows_b, sub);
+        b_dims = 4;
+    } else {
         rc = encode_2d(&L->b, in_dtype, B, N, K, ldb, 64, bk);
+    }
     if (rc != GEMM_OK) return rc;
     const uint32_t chunk_cols = 128u / (uint32_t)osz;
     // TMA stores write whole 16-byte pieces of a row, even past the tensor's
@@ -733,6 +815,8 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     p.M = (int32_t)M;
     p.N = (int32_t)N;
     p.K = (int32_t)K;
+    p.a_box_dims = a_dims;
+    p.b_box_dims = b_dims;
     p.num_m_tiles = pl.num_m;
     p.num_n_tiles = pl.num_n;
     const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps);
@@ -1171,7 +1255,7 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
     // (packed 4-bit operands: maps of k_map elements per row; 128 of them
     // fill a 128-byte shared-memory row, as 8-bit ones do)
     if ((rc = describe_tcgen05(&L, pl, D, A_op, B_op, C, M, N, k_map, lda, ldb, ldc, ldd, transA, transB, alpha,
-                               beta, in_dtype, out_dtype)) != GEMM_OK)
+                               beta, in_dtype, out_dtype, false)) != GEMM_OK)
         return reject(rc, "tensor maps");
     GemmParams& p = L.p;
     p.K = (int32_t)K;

@@ -76,6 +76,13 @@ struct GemmParams {
     // shared row with 64 bytes of data (8 bytes per 16-byte group) and count
     // only those toward the barrier's transaction bytes.
     int32_t operands_packed4;
+    // How the producer fetches one pipeline stage of A and of B: 2 = one 2-D
+    // TMA box per 64-wide K sub-block (and per 64-wide MN chunk of an
+    // MN-major operand); 3 = the whole stage of a K-major operand in one 3-D
+    // box; 4 = the whole stage of an MN-major operand in one 4-D box.  A TMA
+    // copy costs the SM about the same time whatever its size up to 32 KB,
+    // so fewer, larger boxes fetch operands faster.
+    int32_t a_box_dims, b_box_dims;
 };
 
 // ---------------------------------------------------------------------------

@@ -254,6 +254,34 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
     }
 }
 
+// One pipeline stage (kSub K sub-blocks) of an operand.  box_dims 3: a
+// K-major operand whose tensor map is {K in a 128-byte row, rows, K chunks}:
+// one box of all kSub chunks, whose shared image is the kSub sub-blocks one
+// after another.  box_dims 4: an MN-major operand whose map is {MN in a
+// 128-byte row, K rows of a chunk, MN chunks, K chunks}: one box, laid out
+// as [sub-block][64-wide MN chunk][K row], the same image as the 2-D boxes.
+// Otherwise one 2-D box per sub-block (and per MN chunk).
+template <bool kPair, int kSub>
+__device__ __forceinline__ void load_stage(uint32_t dst, uint32_t sub_bytes, const CUtensorMap* map, int mn_major,
+                                           int box_dims, int row0, int rows, int kb, int bke, uint32_t bar,
+                                           uint64_t policy) {
+    if (box_dims == 3) {
+        if constexpr (kPair)
+            ptx::tma_load_3d_pair_hint(dst, map, 0, row0, kb * kSub, bar, policy);
+        else
+            ptx::tma_load_3d_hint(dst, map, 0, row0, kb * kSub, bar, policy);
+    } else if (box_dims == 4) {
+        if constexpr (kPair)
+            ptx::tma_load_4d_pair_hint(dst, map, 0, 0, row0 / 64, kb * kSub, bar, policy);
+        else
+            ptx::tma_load_4d_hint(dst, map, 0, 0, row0 / 64, kb * kSub, bar, policy);
+    } else {
+#pragma unroll
+        for (int sub = 0; sub < kSub; ++sub)
+            load_operand<kPair>(dst + sub * sub_bytes, map, mn_major, row0, rows, (kb * kSub + sub) * bke, bar, policy);
+    }
+}
+
 template <int kOut>
 struct OutTraits;
 template <>
@@ -405,14 +433,11 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                     if (!skip) {
                         const uint32_t fb = kPair ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
                         if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), stage_tx);
-#pragma unroll
-                        for (int sub = 0; sub < Cf::kSub; ++sub) {
-                            const int k0 = (kb * Cf::kSub + sub) * kBKe;
-                            load_operand<kPair>(base + Cf::kOffA + stage * Cf::kABytes + sub * Cf::kASubBytes, &tmA,
-                                                p.a_mn_major, a_row0, kBM, k0, fb, pol_a);
-                            load_operand<kPair>(base + Cf::kOffB + stage * Cf::kBBytes + sub * Cf::kBSubBytes, &tmB,
-                                                p.b_mn_major, b_row0, Cf::kLoadN, k0, fb, pol_b);
-                        }
+                        load_stage<kPair, Cf::kSub>(base + Cf::kOffA + stage * Cf::kABytes, Cf::kASubBytes, &tmA,
+                                                    p.a_mn_major, p.a_box_dims, a_row0, kBM, kb, kBKe, fb, pol_a);
+                        load_stage<kPair, Cf::kSub>(base + Cf::kOffB + stage * Cf::kBBytes, Cf::kBSubBytes, &tmB,
+                                                    p.b_mn_major, p.b_box_dims, b_row0, Cf::kLoadN, kb, kBKe, fb,
+                                                    pol_b);
                         if constexpr (kMX) {
                             // this stage's scales, laid out by the host in the
                             // order tcgen05.cp reads them (512-byte chunks, rows

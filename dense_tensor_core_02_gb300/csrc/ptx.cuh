@@ -168,6 +168,44 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* 
         : "memory");
 }
 
+// 3-D and 4-D tile loads: one box of several 2-D slabs (the tensor map's
+// extra dimensions), one-CTA and CTA-pair forms.
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, int32_t c2,
+                                                 uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
+                                                      int32_t c2, uint32_t cluster_bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(cluster_bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const void* tmap, int32_t c0, int32_t c1, int32_t c2,
+                                                 int32_t c3, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair_hint(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
+                                                      int32_t c2, int32_t c3, uint32_t cluster_bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(cluster_bar), "l"(policy)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_store_2d_hint(const void* tmap, uint32_t src, int32_t c0, int32_t c1,
                                                   uint64_t policy) {
     asm volatile(

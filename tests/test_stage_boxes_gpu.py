@@ -1,0 +1,68 @@
+"""GPU parity of the whole-stage operand boxes.
+
+The CTA-pair kernel with four epilogue warps stages two 64-wide K sub-blocks
+per pipeline stage.  Where the sizes allow it, its producer fetches a stage
+of each operand with one TMA box: a 3-D box for a K-major operand (K a
+multiple of the sub-block width), a 4-D box for an MN-major one (also M or N
+a multiple of 64).  Elsewhere, and with GEMM_STAGE_BOXES=0, it issues one
+2-D box per sub-block and per 64-wide MN chunk.  Both fill shared memory
+with the same image, so on integer inputs both are exact against the oracle
+and equal to each other bit for bit.  The shapes below take each form for A
+and for B, with ragged M and N, an odd number of sub-blocks (the last stage's
+second sub-block lies past K and reads zeros) and 8-bit operands.
+"""
+import pytest
+import torch
+
+from dense_tensor_core_02_gb300 import binding
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load_library()
+    yield
+    rc, info = H.poll()
+    assert rc == 0, ("device status after the module", rc, info)
+
+
+# (M, N, K, transA, transB, in_dtype, out_dtype, integer range), on the pair
+# kernel (forced: the size rule would give these small problems narrow
+# one-SM tiles) with four epilogue warps: 16-bit D, or f32 D with more than
+# four stages (K > 512; > 1024 for 8-bit operands).  Those with K-major B and
+# f32 D run on the 224-wide tiles (112 B rows per CTA).
+SHAPES = [
+    (520, 392, 704, 0, 1, "f16", "f32", 8),     # A, B K-major: 3-D boxes; 11 sub-blocks
+    (520, 384, 640, 1, 0, "bf16", "f32", 8),    # A MN-major, M % 64 != 0: 2-D; B MN-major: 4-D
+    (512, 448, 576, 1, 0, "f16", "f32", 8),     # A, B MN-major: 4-D boxes; 9 sub-blocks
+    (300, 256, 128, 0, 0, "f16", "f16", 2),     # A K-major 3-D, B MN-major 4-D, one stage, f16 D
+    (384, 320, 1000, 0, 1, "f16", "f32", 8),    # K % 64 != 0: 2-D boxes for both
+    (520, 392, 1152, 0, 1, "e4m3", "f32", 8),   # 8-bit, K-major: 3-D boxes of 128-byte K rows; 9 sub-blocks
+    (264, 200, 704, 1, 1, "bf16", "bf16", 2),   # A MN-major 2-D (M % 64 != 0), B K-major 3-D, bf16 D
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "%dx%dx%d_t%d%d_%s_%s" % s[:7])
+def test_stage_boxes_match_2d_boxes_and_oracle(shape):
+    M, N, K, transA, transB, in_dtype, out_dtype, lim = shape
+    seed = 7 * M + 3 * N + K + transA + 2 * transB
+    A = H.int_matrix((K, M) if transA else (M, K), -lim, lim, in_dtype, seed)
+    B = H.int_matrix((N, K) if transB else (K, N), -lim, lim, in_dtype, seed + 1)
+    C = H.int_matrix((M, N), -20, 20, out_dtype, seed + 2)
+    kw = dict(transA=transA, transB=transB, alpha=1.0, beta=1.0, in_dtype=in_dtype, out_dtype=out_dtype)
+    out = []
+    for boxes in (None, "0"):
+        with H.env(GEMM_PATH="tcgen05", GEMM_VARIANT="pair", GEMM_STAGE_BOXES=boxes):
+            D, rc = H.run_gemm(A, B, C, M, N, K, **kw)
+        assert rc == 0, boxes
+        out.append(D)
+    assert torch.equal(out[0], out[1]), "whole-stage boxes and 2-D boxes disagree"
+    ref, bound = H.oracle_full(A, B, C, M, N, K, **kw)
+    if out_dtype == "f32":
+        H.assert_exact(out[0].numpy(), ref, "stage boxes %s" % (shape,))
+    else:   # one rounding to the 16-bit D
+        H.assert_close(out[0].double().numpy(), ref, bound, out_dtype, "stage boxes %s" % (shape,))
