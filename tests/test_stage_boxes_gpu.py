@@ -9,7 +9,8 @@ a multiple of 64).  Elsewhere, and with GEMM_STAGE_BOXES=0, it issues one
 with the same image, so on integer inputs both are exact against the oracle
 and equal to each other bit for bit.  The shapes below take each form for A
 and for B, with ragged M and N, an odd number of sub-blocks (the last stage's
-second sub-block lies past K and reads zeros) and 8-bit operands.
+second sub-block lies past K and reads zeros), 8-bit operands, and the
+block-scaled kernel's 8-bit operands.
 """
 import pytest
 import torch
@@ -66,3 +67,30 @@ def test_stage_boxes_match_2d_boxes_and_oracle(shape):
         H.assert_exact(out[0].numpy(), ref, "stage boxes %s" % (shape,))
     else:   # one rounding to the 16-bit D
         H.assert_close(out[0].double().numpy(), ref, bound, out_dtype, "stage boxes %s" % (shape,))
+
+
+# block-scaled 8-bit operands (gemm_mx): the same whole-stage operand boxes
+# (K a multiple of 128 here), scales per sub-block as before
+MX_SHAPES = [(640, 520, 1024, "e4m3", 0.0), (264, 448, 640, "e5m2", 1.0), (520, 392, 1000, "e4m3", 1.0)]
+
+
+@pytest.mark.parametrize("shape", MX_SHAPES, ids=lambda s: "%dx%dx%d_%s_b%g" % s)
+def test_mx_stage_boxes_match_2d_boxes_and_oracle(shape):
+    from tests.test_mx_gpu import oracle_mx, run_mx, scales
+    M, N, K, dtype, beta = shape
+    seed = 11 * M + N + K
+    A = H.int_matrix((M, K), -8, 8, dtype, seed)
+    B = H.int_matrix((N, K), -8, 8, dtype, seed + 1)
+    C = H.int_matrix((M, N), -100, 100, "f32", seed + 2) if beta else None
+    SFA = scales(M, K, 126, 128, seed + 3)
+    SFB = scales(N, K, 126, 128, seed + 4)
+    kw = dict(beta=beta, in_dtype=dtype)
+    out = []
+    for boxes in (None, "0"):
+        with H.env(GEMM_PATH=None, GEMM_VARIANT="pair", GEMM_STAGE_BOXES=boxes):
+            D, rc = run_mx(A, B, C, SFA, SFB, M, N, K, **kw)
+        assert rc == 0, boxes
+        out.append(D)
+    assert torch.equal(out[0], out[1]), "whole-stage boxes and 2-D boxes disagree"
+    ref, _ = oracle_mx(A, B, C, SFA, SFB, M, N, K, **kw)
+    H.assert_exact(out[0].numpy(), ref, "mx stage boxes %s" % (shape,))
