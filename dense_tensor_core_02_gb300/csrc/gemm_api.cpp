@@ -763,7 +763,7 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     const uint32_t rows_b = (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n);
     // A whole stage in one box for the kernels whose stages hold two K
     // sub-blocks, where the sizes allow it (GEMM_STAGE_BOXES=0: always the
-    // 2-D boxes; packed 4-bit operands keep them too).  A TMA copy costs the SM about the same time whatever its
+    // 2-D boxes).  A TMA copy costs the SM about the same time whatever its
     // size up to 32 KB: on GB300 one 32 KB box moves 70 bytes per SM clock,
     // two 16 KB boxes 64, four 8 KB boxes 54.  Measured against the 2-D
     // boxes: 8192^3 +0.6 to +0.8 %, 4096^3 bf16 beta = 1 +1.0 %, 8192^2 x 4096
@@ -1253,12 +1253,12 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
 
     TcgenLaunch L;
     // (packed 4-bit operands: maps of k_map elements per row; 128 of them
-    // fill a 128-byte shared-memory row, as 8-bit ones do.  8-bit operands
-    // take whole-stage boxes like the plain kernel's: 8192^3 MX E4M3 +1.7 to
-    // +2.6 %, 4096^3 MX E5M2 beta = 1 +1.2 %; the scale boxes stay per
-    // sub-block, merging them too gained nothing measurable.)
+    // fill a 128-byte shared-memory row, as 8-bit ones do.  The operands take
+    // whole-stage boxes like the plain kernel's: 8192^3 MX E4M3 +1.7 to
+    // +2.6 %, E2M1 +2.0 to +2.4 %, 4096^3 MX E5M2 beta = 1 +1.2 %; the scale
+    // boxes stay per sub-block, merging them too gained nothing measurable.)
     if ((rc = describe_tcgen05(&L, pl, D, A_op, B_op, C, M, N, k_map, lda, ldb, ldc, ldd, transA, transB, alpha,
-                               beta, in_dtype, out_dtype, !fp4)) != GEMM_OK)
+                               beta, in_dtype, out_dtype, true)) != GEMM_OK)
         return reject(rc, "tensor maps");
     GemmParams& p = L.p;
     p.K = (int32_t)K;

@@ -69,18 +69,23 @@ def test_stage_boxes_match_2d_boxes_and_oracle(shape):
         H.assert_close(out[0].double().numpy(), ref, bound, out_dtype, "stage boxes %s" % (shape,))
 
 
-# block-scaled 8-bit operands (gemm_mx): the same whole-stage operand boxes
-# (K a multiple of 128 here), scales per sub-block as before
-MX_SHAPES = [(640, 520, 1024, "e4m3", 0.0), (264, 448, 640, "e5m2", 1.0), (520, 392, 1000, "e4m3", 1.0)]
+# block-scaled operands (gemm_mx): the same whole-stage operand boxes (K a
+# multiple of 128 here; packed E2M1 through its 16U4_ALIGN16B maps), scales
+# per sub-block as before
+MX_SHAPES = [(640, 520, 1024, "e4m3", 0.0), (264, 448, 640, "e5m2", 1.0), (520, 392, 1000, "e4m3", 1.0),
+             (384, 392, 1152, "e2m1", 1.0)]
 
 
 @pytest.mark.parametrize("shape", MX_SHAPES, ids=lambda s: "%dx%dx%d_%s_b%g" % s)
 def test_mx_stage_boxes_match_2d_boxes_and_oracle(shape):
-    from tests.test_mx_gpu import oracle_mx, run_mx, scales
+    from tests.test_mx_gpu import fp4_matrix, oracle_mx, run_mx, scales
     M, N, K, dtype, beta = shape
     seed = 11 * M + N + K
-    A = H.int_matrix((M, K), -8, 8, dtype, seed)
-    B = H.int_matrix((N, K), -8, 8, dtype, seed + 1)
+    if dtype == "e2m1":   # packed codes, two per byte
+        A, B = fp4_matrix(M, K, seed), fp4_matrix(N, K, seed + 1)
+    else:
+        A = H.int_matrix((M, K), -8, 8, dtype, seed)
+        B = H.int_matrix((N, K), -8, 8, dtype, seed + 1)
     C = H.int_matrix((M, N), -100, 100, "f32", seed + 2) if beta else None
     SFA = scales(M, K, 126, 128, seed + 3)
     SFB = scales(N, K, 126, 128, seed + 4)
