@@ -516,7 +516,7 @@ int epi_warps_for(int64_t K, int pair, int out_dtype, int tile_n, int f8) {
     if (out_dtype != GEMM_F32 || tile_n == gb300::tcgen05_narrow_n()) return 4;
     const char* v = std::getenv("GEMM_EPI_WARPS");
     if (v && (std::strcmp(v, "4") == 0 || std::strcmp(v, "8") == 0)) return std::atoi(v);
-    const int64_t stage_k = gb300::tcgen05_stage_k(pair, f8, 4);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pair, f8, 4, tile_n);
     return (K + stage_k - 1) / stage_k <= 4 ? 8 : 4;
 }
 
@@ -544,7 +544,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int num_sms, bool allow_streamk,
     pl.num_n = (int)((N + pl.tile_n - 1) / pl.tile_n);
     pl.num_tiles = pl.num_m * pl.num_n;
     pl.epi_warps = mx ? 4 : epi_warps_for(K, pl.pair, out_dtype, pl.tile_n, f8);
-    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps, pl.tile_n);
     pl.iters = (int)((K + stage_k - 1) / stage_k);
     const int units = pl.pair ? num_sms / 2 : num_sms;   // clusters that fit at once
     // Wave-fitted tiles: a persistent launch takes about (waves) x (time of
@@ -758,7 +758,7 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     if (pl.tile_n == gb300::tcgen05_fit_n() && !transB) return GEMM_ERR_INVALID_ARG;
     const uint32_t bk = (uint32_t)gb300::tcgen05_block_k(f8);   // K elements per 128-byte row
     // K sub-blocks per pipeline stage, and the rows of A and B one CTA stages
-    const uint32_t sub = (uint32_t)(gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps) / (int)bk);
+    const uint32_t sub = (uint32_t)(gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps, pl.tile_n) / (int)bk);
     const uint32_t rows_a = (uint32_t)gb300::tcgen05_load_rows_a();
     const uint32_t rows_b = (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n);
     // A whole stage in one box for the kernels whose stages hold two K
@@ -819,7 +819,7 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     p.b_box_dims = b_dims;
     p.num_m_tiles = pl.num_m;
     p.num_n_tiles = pl.num_n;
-    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps);
+    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps, pl.tile_n);
     p.num_k_blocks = (int32_t)((K + stage_k - 1) / stage_k);   // pipeline stages per tile
     p.num_tiles = pl.num_tiles;
     p.group_m = group_m_setting(p.num_k_blocks);
@@ -1210,7 +1210,7 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
     // 128-K sub-block and 128-row group of A (each CTA of a pair has its
     // own), and (tile N / 128) per sub-block and N tile.
     const int64_t kblocks = (K + 31) / 32;
-    const int64_t kchunks = (int64_t)pl.iters * (gb300::tcgen05_stage_k(pl.pair, 1, pl.epi_warps) / 128);
+    const int64_t kchunks = (int64_t)pl.iters * (gb300::tcgen05_stage_k(pl.pair, 1, pl.epi_warps, pl.tile_n) / 128);
     const int64_t a_groups = (int64_t)pl.num_m * (pl.pair ? 2 : 1);
     const int sfb_chunks = (pl.tile_n + 127) / 128;
     const int64_t sfa_bytes = gb300::sf_tiles_bytes(128, a_groups, kchunks);

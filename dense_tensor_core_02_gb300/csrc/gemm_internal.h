@@ -120,7 +120,7 @@ int tcgen05_wide_n();              // D columns per throughput tile
 int tcgen05_narrow_n();            // D columns per narrow tile (single CTA, 4 epilogue warps)
 int tcgen05_fit_n();               // D columns per wave-fitted tile (CTA pair, f32 D, K-major B)
 int tcgen05_block_k(int f8);       // K of one TMA operand box (one 128-byte swizzle row)
-int tcgen05_stage_k(int pair, int f8, int epi_warps);   // K per pipeline stage
+int tcgen05_stage_k(int pair, int f8, int epi_warps, int tile_n);   // K per pipeline stage
 int tcgen05_load_rows_a();         // A rows (M) one CTA stages per stage
 int tcgen05_load_rows_b(int pair, int tile_n);   // B rows (N) one CTA stages per stage
 int tcgen05_smem_bytes(int pair, int epi_warps, int tile_n);

@@ -69,7 +69,8 @@ int tcgen05_wide_n() { return kBNMax; }
 int tcgen05_narrow_n() { return kNarrowN; }
 int tcgen05_fit_n() { return kFitN; }
 int tcgen05_block_k(int f8) { return f8 ? kBK8 : kBK; }
-int tcgen05_stage_k(int pair, int f8, int epi_warps) {
+int tcgen05_stage_k(int pair, int f8, int epi_warps, int tile_n) {
+    if (tile_n == kNarrowN) return tcgen05_block_k(f8) * Cfg<false, 4, kNarrowN>::kSub;
     if (epi_warps == 8) return tcgen05_block_k(f8) * (pair ? Cfg<true, 8>::kSub : Cfg<false, 8>::kSub);
     return tcgen05_block_k(f8) * (pair ? Cfg<true, 4>::kSub : Cfg<false, 4>::kSub);
 }

@@ -106,8 +106,11 @@ struct Cfg {
     // blocks) behind each wait: 64 KiB stages instead of 32 KiB ones.  The
     // 8-epilogue-warp kernel (tiles of a few stages, bound by the D stores)
     // keeps 32 KiB stages: beside its staging boxes that makes four stages
-    // instead of two, so the loads of the next tile start sooner.
-    static constexpr int kSub = (kPair && kEpiW == 4) ? 2 : 1;
+    // instead of two, so the loads of the next tile start sooner.  The
+    // narrow 128 x 64 tiles take two sub-blocks per stage too (four 48 KiB
+    // stages): their time goes into fetching operands, and a whole stage of
+    // each operand then arrives in one TMA copy instead of two.
+    static constexpr int kSub = (kEpiW == 4 && (kPair || kTileN == kNarrowN)) ? 2 : 1;
     static constexpr int kASubBytes = kBM * kBK * 2;
     static constexpr int kBSubBytes = kLoadN * kBK * 2;
     static constexpr int kABytes = kSub * kASubBytes;
