@@ -763,13 +763,13 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     const uint32_t rows_b = (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n);
     // A whole stage in one box for the kernels whose stages hold two K
     // sub-blocks, where the sizes allow it (GEMM_STAGE_BOXES=0: always the
-    // 2-D boxes).  A TMA copy costs the SM about the same time whatever its
-    // size up to 32 KB: on GB300 one 32 KB box moves 70 bytes per SM clock,
-    // two 16 KB boxes 64, four 8 KB boxes 54.  Measured against the 2-D
-    // boxes: 8192^3 +0.6 to +0.8 %, 4096^3 bf16 beta = 1 +1.0 %, 8192^2 x 4096
-    // +0.9 %.  The 8-epilogue-warp kernel (one sub-block per stage, bound by
-    // its D stores) lost 1.7 % with the MN-major chunks merged, and keeps them
-    // apart.
+    // 2-D boxes).  Measured against the 2-D boxes: 8192^3 +0.6 to +0.8 %,
+    // 4096^3 bf16 beta = 1 +1.0 %, 8192^2 x 4096 +0.9 %, 512^3 -11 % time.
+    // (The operand supply itself is not the limit: in this kernel's access
+    // pattern TMA delivers ~95 bytes per SM clock on every SM with either
+    // form, against the 64 the tensor pipe needs.)  The 8-epilogue-warp
+    // kernel (one sub-block per stage, bound by its D stores) lost 1.7 % with
+    // the MN-major chunks merged, and keeps them apart.
     const char* sb = std::getenv("GEMM_STAGE_BOXES");
     const bool boxes_ok = stage_boxes && sub > 1 && K % bk == 0 && !(sb && std::strcmp(sb, "0") == 0);
     int a_dims = 2, b_dims = 2;

@@ -79,9 +79,8 @@ struct GemmParams {
     // How the producer fetches one pipeline stage of A and of B: 2 = one 2-D
     // TMA box per 64-wide K sub-block (and per 64-wide MN chunk of an
     // MN-major operand); 3 = the whole stage of a K-major operand in one 3-D
-    // box; 4 = the whole stage of an MN-major operand in one 4-D box.  A TMA
-    // copy costs the SM about the same time whatever its size up to 32 KB,
-    // so fewer, larger boxes fetch operands faster.
+    // box; 4 = the whole stage of an MN-major operand in one 4-D box.  Fewer
+    // copies per stage measured 0.6 to 1 % faster on the tensor-bound shapes.
     int32_t a_box_dims, b_box_dims;
 };
 
