@@ -747,7 +747,7 @@ int validate_scales(const void* D, const void* SFA, const void* SFB, int64_t M, 
 // record and, for stream-K, the workspace.
 int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, const void* B, const void* C,
                      int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd, int transA,
-                     int transB, float alpha, float beta, int in_dtype, int out_dtype, bool stage_boxes = true) {
+                     int transB, float alpha, float beta, int in_dtype, int out_dtype) {
     const bool has_c = beta != 0.0f;
     const bool f8 = is_f8(in_dtype) || in_dtype == GEMM_E2M1;   // 128 K elements per 128-byte shared row
     const int osz = elem_size(out_dtype);
@@ -771,7 +771,7 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     // kernel (one sub-block per stage, bound by its D stores) lost 1.7 % with
     // the MN-major chunks merged, and keeps them apart.
     const char* sb = std::getenv("GEMM_STAGE_BOXES");
-    const bool boxes_ok = stage_boxes && sub > 1 && K % bk == 0 && !(sb && std::strcmp(sb, "0") == 0);
+    const bool boxes_ok = sub > 1 && K % bk == 0 && !(sb && std::strcmp(sb, "0") == 0);
     int a_dims = 2, b_dims = 2;
     // A: K-major (transA = 0) as [M rows][K], else MN-major as [K rows][M]
     if (!transA) {
@@ -1258,7 +1258,7 @@ int gemm_mx(void* D, const void* A, const void* B, const void* C, const void* SF
     // +2.6 %, E2M1 +2.0 to +2.4 %, 4096^3 MX E5M2 beta = 1 +1.2 %; the scale
     // boxes stay per sub-block, merging them too gained nothing measurable.)
     if ((rc = describe_tcgen05(&L, pl, D, A_op, B_op, C, M, N, k_map, lda, ldb, ldc, ldd, transA, transB, alpha,
-                               beta, in_dtype, out_dtype, true)) != GEMM_OK)
+                               beta, in_dtype, out_dtype)) != GEMM_OK)
         return reject(rc, "tensor maps");
     GemmParams& p = L.p;
     p.K = (int32_t)K;
