@@ -307,9 +307,8 @@ int encode_2d(CUtensorMap* map, int dt, const void* ptr, int64_t dim0, int64_t d
 // as a single box.  The K extent of each 128-byte shared row (bk elements)
 // is the map's first dimension and the K chunks its third: dims {bk, rows,
 // K / bk}, box {bk, box_rows, sub}; the box lands as `sub` consecutive
-// {bk, box_rows} slabs, the image of `sub` 2-D boxes.  K must be a multiple
-// of bk: a partial chunk would read on into the next row instead of reading
-// zeros.
+// {bk, box_rows} slabs, the image of `sub` 2-D boxes.  K is a multiple of
+// bk (the caller's whole chunks).
 int encode_kmajor_stage(CUtensorMap* map, int dt, const void* ptr, int64_t K, int64_t rows, int64_t ld, uint32_t bk,
                         uint32_t box_rows, uint32_t sub) {
     cuuint64_t dims[3] = {(cuuint64_t)bk, (cuuint64_t)rows, (cuuint64_t)(K / bk)};
@@ -331,8 +330,8 @@ int encode_kmajor_stage(CUtensorMap* map, int dt, const void* ptr, int64_t K, in
 // as a single box: dims {64, bk, mn / 64, K / bk} (64 MN elements of a K
 // row, the bk K rows of a sub-block, the 64-wide MN chunks, the sub-blocks),
 // box {64, bk, box_mn / 64, sub}, landing as [sub-block][MN chunk][K row]:
-// the image of the 2-D boxes {64, bk}.  mn and K must be multiples of 64 and
-// bk: partial chunks would read past the rows instead of reading zeros.
+// the image of the 2-D boxes {64, bk}.  mn and K are multiples of 64 and bk
+// (the caller rounds mn up and K down; see describe_tcgen05).
 int encode_mnmajor_stage(CUtensorMap* map, int dt, const void* ptr, int64_t mn, int64_t K, int64_t ld, uint32_t bk,
                          uint32_t box_mn, uint32_t sub) {
     cuuint64_t dims[4] = {64, (cuuint64_t)bk, (cuuint64_t)(mn / 64), (cuuint64_t)(K / bk)};
@@ -762,45 +761,66 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     const uint32_t rows_a = (uint32_t)gb300::tcgen05_load_rows_a();
     const uint32_t rows_b = (uint32_t)gb300::tcgen05_load_rows_b(pl.pair, pl.tile_n);
     // A whole stage in one box for the kernels whose stages hold two K
-    // sub-blocks, where the sizes allow it (GEMM_STAGE_BOXES=0: always the
-    // 2-D boxes).  Measured against the 2-D boxes: 8192^3 +0.6 to +0.8 %,
-    // 4096^3 bf16 beta = 1 +1.0 %, 8192^2 x 4096 +0.9 %, 512^3 -11 % time.
+    // sub-blocks (GEMM_STAGE_BOXES=0: always the 2-D boxes).  Measured
+    // against the 2-D boxes: 8192^3 +0.6 to +0.8 %, 4096^3 bf16 beta = 1
+    // +1.0 %, 8192^2 x 4096 +0.9 %, 512^3 -11 % time, 1000^3 -3 % time.
     // (The operand supply itself is not the limit: in this kernel's access
     // pattern TMA delivers ~95 bytes per SM clock on every SM with either
     // form, against the 64 the tensor pipe needs.)  The 8-epilogue-warp
     // kernel (one sub-block per stage, bound by its D stores) lost 1.7 % with
     // the MN-major chunks merged, and keeps them apart.
+    //
+    // The whole-stage maps cover only complete stages.  A K-major map counts
+    // whole 128-byte K chunks, and a partial last stage takes the 2-D boxes:
+    // a partial chunk would read on into the next row instead of reading
+    // zeros.  An MN-major map counts 64-wide MN chunks; when M (or N) is not
+    // a multiple of 64 the last chunk reads up to 63 elements past the end of
+    // each K row, into the row after it.  Those elements only reach rows (or
+    // columns) of D that are never stored, and the last K row, which has no
+    // row after it, always comes through the 2-D boxes.  That takes an
+    // extent of at least 64, so that the overrun stays inside the next row.
     const char* sb = std::getenv("GEMM_STAGE_BOXES");
-    const bool boxes_ok = sub > 1 && K % bk == 0 && !(sb && std::strcmp(sb, "0") == 0);
+    const bool boxes_ok = sub > 1 && !(sb && std::strcmp(sb, "0") == 0);
+    const int64_t stage_k = (int64_t)bk * sub;
+    const int64_t full_stages = K / stage_k;               // stages with every K chunk complete
+    const int64_t all_stages = (K + stage_k - 1) / stage_k;
+    // whole-stage count of an MN-major operand of extent mn (0: 2-D boxes only)
+    auto mn_whole = [&](int64_t mn) -> int64_t {
+        if (mn % 64 == 0) return full_stages;
+        return mn >= 64 ? std::min(full_stages, all_stages - 1) : 0;
+    };
     int a_dims = 2, b_dims = 2;
+    int64_t a_whole = 0, b_whole = 0;
     // A: K-major (transA = 0) as [M rows][K], else MN-major as [K rows][M]
-    if (!transA) {
-        if (boxes_ok) {
-            rc = encode_kmajor_stage(&L->a, in_dtype, A, K, M, lda, bk, rows_a, sub);
-            a_dims = 3;
-        } else {
-            rc = encode_2d(&L->a, in_dtype, A, K, M, lda, bk, rows_a);
-        }
-    } else if (boxes_ok && M % 64 == 0) {
-        rc = encode_mnmajor_stage(&L->a, in_dtype, A, M, K, lda, bk, rows_a, sub);
-        a_dims = 4;
-    } else {
+    if (!transA)
+        rc = encode_2d(&L->a, in_dtype, A, K, M, lda, bk, rows_a);
+    else
         rc = encode_2d(&L->a, in_dtype, A, M, K, lda, 64, bk);
+    if (rc != GEMM_OK) return rc;
+    if (boxes_ok && !transA && full_stages > 0) {
+        a_dims = 3;
+        a_whole = full_stages;
+        rc = encode_kmajor_stage(&L->a_stage, in_dtype, A, K / bk * bk, M, lda, bk, rows_a, sub);
+    } else if (boxes_ok && transA && mn_whole(M) > 0) {
+        a_dims = 4;
+        a_whole = mn_whole(M);
+        rc = encode_mnmajor_stage(&L->a_stage, in_dtype, A, (M + 63) / 64 * 64, K / bk * bk, lda, bk, rows_a, sub);
     }
     if (rc != GEMM_OK) return rc;
     // B: K-major (transB = 1) as [N rows][K], else MN-major as [K rows][N]
-    if (transB) {
-        if (boxes_ok) {
-            rc = encode_kmajor_stage(&L->b, in_dtype, B, K, N, ldb, bk, rows_b, sub);
-            b_dims = 3;
-        } else {
-            rc = encode_2d(&L->b, in_dtype, B, K, N, ldb, bk, rows_b);
-        }
-    } else if (boxes_ok && N % 64 == 0) {
-        rc = encode_mnmajor_stage(&L->b, in_dtype, B, N, K, ldb, bk, rows_b, sub);
-        b_dims = 4;
-    } else {
+    if (transB)
+        rc = encode_2d(&L->b, in_dtype, B, K, N, ldb, bk, rows_b);
+    else
         rc = encode_2d(&L->b, in_dtype, B, N, K, ldb, 64, bk);
+    if (rc != GEMM_OK) return rc;
+    if (boxes_ok && transB && full_stages > 0) {
+        b_dims = 3;
+        b_whole = full_stages;
+        rc = encode_kmajor_stage(&L->b_stage, in_dtype, B, K / bk * bk, N, ldb, bk, rows_b, sub);
+    } else if (boxes_ok && !transB && mn_whole(N) > 0) {
+        b_dims = 4;
+        b_whole = mn_whole(N);
+        rc = encode_mnmajor_stage(&L->b_stage, in_dtype, B, (N + 63) / 64 * 64, K / bk * bk, ldb, bk, rows_b, sub);
     }
     if (rc != GEMM_OK) return rc;
     const uint32_t chunk_cols = 128u / (uint32_t)osz;
@@ -817,10 +837,11 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     p.K = (int32_t)K;
     p.a_box_dims = a_dims;
     p.b_box_dims = b_dims;
+    p.a_whole_stages = (int32_t)a_whole;
+    p.b_whole_stages = (int32_t)b_whole;
     p.num_m_tiles = pl.num_m;
     p.num_n_tiles = pl.num_n;
-    const int64_t stage_k = gb300::tcgen05_stage_k(pl.pair, f8, pl.epi_warps, pl.tile_n);
-    p.num_k_blocks = (int32_t)((K + stage_k - 1) / stage_k);   // pipeline stages per tile
+    p.num_k_blocks = (int32_t)all_stages;   // pipeline stages per tile
     p.num_tiles = pl.num_tiles;
     p.group_m = group_m_setting(p.num_k_blocks);
     p.alpha = alpha;

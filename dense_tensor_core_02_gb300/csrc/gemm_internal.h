@@ -20,6 +20,7 @@ constexpr int kDeviceErrTimeout = -8;
 struct TcgenLaunch {
     CUtensorMap a, b, c, d;   // TMA descriptors (c unused when beta == 0)
     CUtensorMap sfa, sfb;     // block scales (mx only; see GemmParams::sf_a_groups)
+    CUtensorMap a_stage, b_stage;   // whole-stage boxes (see GemmParams::a_box_dims)
     GemmParams p;
     int pair;                 // 1: CTA-pair (cta_group::2) kernel
     int out;                  // OutKind

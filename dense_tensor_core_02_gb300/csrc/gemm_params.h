@@ -81,7 +81,10 @@ struct GemmParams {
     // MN-major operand); 3 = the whole stage of a K-major operand in one 3-D
     // box; 4 = the whole stage of an MN-major operand in one 4-D box.  Fewer
     // copies per stage measured 0.6 to 1 % faster on the tensor-bound shapes.
+    // The whole-stage boxes serve stages [0, *_whole_stages) (their own
+    // maps); later stages (a partial last one) take the 2-D boxes.
     int32_t a_box_dims, b_box_dims;
+    int32_t a_whole_stages, b_whole_stages;
 };
 
 // ---------------------------------------------------------------------------

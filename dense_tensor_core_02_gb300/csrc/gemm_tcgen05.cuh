@@ -257,27 +257,32 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const CUtensorMap* ma
     }
 }
 
-// One pipeline stage (kSub K sub-blocks) of an operand.  box_dims 3: a
-// K-major operand whose tensor map is {K in a 128-byte row, rows, K chunks}:
-// one box of all kSub chunks, whose shared image is the kSub sub-blocks one
-// after another.  box_dims 4: an MN-major operand whose map is {MN in a
-// 128-byte row, K rows of a chunk, MN chunks, K chunks}: one box, laid out
-// as [sub-block][64-wide MN chunk][K row], the same image as the 2-D boxes.
-// Otherwise one 2-D box per sub-block (and per MN chunk).
+// One pipeline stage (kSub K sub-blocks) of an operand.  For stages below
+// `whole`, box_dims 3: a K-major operand whose stage map is {K in a 128-byte
+// row, rows, K chunks}: one box of all kSub chunks, whose shared image is
+// the kSub sub-blocks one after another; box_dims 4: an MN-major operand
+// whose stage map is {MN in a 128-byte row, K rows of a chunk, MN chunks,
+// K chunks}: one box, laid out as [sub-block][64-wide MN chunk][K row], the
+// same image as the 2-D boxes.  Otherwise one 2-D box of `map` per
+// sub-block (and per MN chunk).
 template <bool kPair, int kSub>
-__device__ __forceinline__ void load_stage(uint32_t dst, uint32_t sub_bytes, const CUtensorMap* map, int mn_major,
-                                           int box_dims, int row0, int rows, int kb, int bke, uint32_t bar,
-                                           uint64_t policy) {
-    if (box_dims == 3) {
-        if constexpr (kPair)
-            ptx::tma_load_3d_pair_hint(dst, map, 0, row0, kb * kSub, bar, policy);
-        else
-            ptx::tma_load_3d_hint(dst, map, 0, row0, kb * kSub, bar, policy);
-    } else if (box_dims == 4) {
-        if constexpr (kPair)
-            ptx::tma_load_4d_pair_hint(dst, map, 0, 0, row0 / 64, kb * kSub, bar, policy);
-        else
-            ptx::tma_load_4d_hint(dst, map, 0, 0, row0 / 64, kb * kSub, bar, policy);
+__device__ __forceinline__ void load_stage(uint32_t dst, uint32_t sub_bytes, const CUtensorMap* map,
+                                           const CUtensorMap* stage_map, int mn_major, int box_dims, int whole,
+                                           int row0, int rows, int kb, int bke, uint32_t bar, uint64_t policy) {
+    // The launch-wide 2-D test comes first: testing the stage index inside
+    // every branch cost the one-sub-block kernels 22 % at K = 256 (measured).
+    if (box_dims != 2 && kb < whole) {
+        if (box_dims == 3) {
+            if constexpr (kPair)
+                ptx::tma_load_3d_pair_hint(dst, stage_map, 0, row0, kb * kSub, bar, policy);
+            else
+                ptx::tma_load_3d_hint(dst, stage_map, 0, row0, kb * kSub, bar, policy);
+        } else {
+            if constexpr (kPair)
+                ptx::tma_load_4d_pair_hint(dst, stage_map, 0, 0, row0 / 64, kb * kSub, bar, policy);
+            else
+                ptx::tma_load_4d_hint(dst, stage_map, 0, 0, row0 / 64, kb * kSub, bar, policy);
+        }
     } else {
 #pragma unroll
         for (int sub = 0; sub < kSub; ++sub)
@@ -321,6 +326,7 @@ __device__ __forceinline__ float2 unpack2(uint32_t u, int out) {
 template <bool kPair, int kOut, int kEpiW, bool kHasC, int kTileN, bool kF8, bool kMX = false>
 __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmAs, const __grid_constant__ CUtensorMap tmBs,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                         const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                         const GemmParams p) {
@@ -375,6 +381,8 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
         ptx::fence_mbarrier_init();
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
+        if (p.a_box_dims > 2) ptx::prefetch_tensormap(&tmAs);
+        if (p.b_box_dims > 2) ptx::prefetch_tensormap(&tmBs);
         ptx::prefetch_tensormap(&tmD);
         if constexpr (kHasC) ptx::prefetch_tensormap(&tmC);
         if constexpr (kMX) {
@@ -437,10 +445,11 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
                         const uint32_t fb = kPair ? ptx::map_to_rank(full_bar(stage), 0) : full_bar(stage);
                         if (leader) ptx::mbar_arrive_expect_tx(full_bar(stage), stage_tx);
                         load_stage<kPair, Cf::kSub>(base + Cf::kOffA + stage * Cf::kABytes, Cf::kASubBytes, &tmA,
-                                                    p.a_mn_major, p.a_box_dims, a_row0, kBM, kb, kBKe, fb, pol_a);
+                                                    &tmAs, p.a_mn_major, p.a_box_dims, p.a_whole_stages, a_row0,
+                                                    kBM, kb, kBKe, fb, pol_a);
                         load_stage<kPair, Cf::kSub>(base + Cf::kOffB + stage * Cf::kBBytes, Cf::kBSubBytes, &tmB,
-                                                    p.b_mn_major, p.b_box_dims, b_row0, Cf::kLoadN, kb, kBKe, fb,
-                                                    pol_b);
+                                                    &tmBs, p.b_mn_major, p.b_box_dims, p.b_whole_stages, b_row0,
+                                                    Cf::kLoadN, kb, kBKe, fb, pol_b);
                         if constexpr (kMX) {
                             // this stage's scales, laid out by the host in the
                             // order tcgen05.cp reads them (512-byte chunks, rows
@@ -1003,8 +1012,8 @@ static cudaError_t launch_one(const TcgenLaunch& L, cudaStream_t stream) {
     }
     cfg.attrs = n ? attr : nullptr;
     cfg.numAttrs = n;
-    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC, kTileN, kF8, kMX>, L.a, L.b, L.c,
-                              L.d, L.sfa, L.sfb, L.p);
+    return cudaLaunchKernelEx(&cfg, gemm_tcgen05_kernel<kPair, kOut, kEpiW, kHasC, kTileN, kF8, kMX>, L.a, L.b,
+                              L.a_stage, L.b_stage, L.c, L.d, L.sfa, L.sfb, L.p);
 }
 
 template <bool kPair, bool kHasC, bool kF8>

@@ -1,16 +1,20 @@
 """GPU parity of the whole-stage operand boxes.
 
-The CTA-pair kernel with four epilogue warps stages two 64-wide K sub-blocks
-per pipeline stage.  Where the sizes allow it, its producer fetches a stage
-of each operand with one TMA box: a 3-D box for a K-major operand (K a
-multiple of the sub-block width), a 4-D box for an MN-major one (also M or N
-a multiple of 64).  Elsewhere, and with GEMM_STAGE_BOXES=0, it issues one
-2-D box per sub-block and per 64-wide MN chunk.  Both fill shared memory
-with the same image, so on integer inputs both are exact against the oracle
-and equal to each other bit for bit.  The shapes below take each form for A
-and for B, with ragged M and N, an odd number of sub-blocks (the last stage's
-second sub-block lies past K and reads zeros), 8-bit operands, and the
-block-scaled kernel's 8-bit operands.
+The CTA-pair kernel with four epilogue warps, and the narrow one, stage two
+64-wide K sub-blocks per pipeline stage.  Their producer fetches each
+complete stage of an operand with one TMA box: a 3-D box for a K-major
+operand, a 4-D box for an MN-major one.  A partial last stage (K not a
+multiple of the stage), and for an MN-major operand whose extent is not a
+multiple of 64 the last stage, take one 2-D box per sub-block and per 64-wide
+MN chunk, as every stage does with GEMM_STAGE_BOXES=0.  Both forms fill
+shared memory with the same image, so on integer inputs both are exact
+against the oracle and equal to each other bit for bit.  The shapes below
+take each form for A and for B: ragged M, N and K, an odd number of
+sub-blocks (the last stage's second sub-block lies past K and reads zeros),
+MN extents below and above 64 that are not multiples of 64 (whose last chunk
+reads past the row, into values that reach only unstored rows or columns of
+D), K shorter than one stage, 8-bit operands, and the block-scaled kernel's
+operands.
 """
 import pytest
 import torch
@@ -38,12 +42,15 @@ def _device():
 # f32 D run on the 224-wide tiles (112 B rows per CTA).
 SHAPES = [
     (520, 392, 704, 0, 1, "f16", "f32", 8),     # A, B K-major: 3-D boxes; 11 sub-blocks
-    (520, 384, 640, 1, 0, "bf16", "f32", 8),    # A MN-major, M % 64 != 0: 2-D; B MN-major: 4-D
+    (520, 384, 640, 1, 0, "bf16", "f32", 8),    # A MN-major, M % 64 != 0: 4-D but the last stage; B 4-D
     (512, 448, 576, 1, 0, "f16", "f32", 8),     # A, B MN-major: 4-D boxes; 9 sub-blocks
     (300, 256, 128, 0, 0, "f16", "f16", 2),     # A K-major 3-D, B MN-major 4-D, one stage, f16 D
-    (384, 320, 1000, 0, 1, "f16", "f32", 8),    # K % 64 != 0: 2-D boxes for both
+    (384, 320, 1000, 0, 1, "f16", "f32", 8),    # K % 64 != 0: 3-D boxes, the partial last stage 2-D
+    (520, 392, 1000, 0, 0, "f16", "f32", 8),    # ragged K, B MN-major with N % 64 != 0
+    (264, 40, 704, 1, 0, "bf16", "f32", 8),     # B MN-major with N < 64: 2-D boxes only
+    (300, 200, 100, 0, 1, "f16", "f32", 8),     # K shorter than one stage: 2-D boxes only
     (520, 392, 1152, 0, 1, "e4m3", "f32", 8),   # 8-bit, K-major: 3-D boxes of 128-byte K rows; 9 sub-blocks
-    (264, 200, 704, 1, 1, "bf16", "bf16", 2),   # A MN-major 2-D (M % 64 != 0), B K-major 3-D, bf16 D
+    (264, 200, 704, 1, 1, "bf16", "bf16", 2),   # A MN-major 4-D but the last stage (M % 64 != 0), B 3-D
 ]
 
 
@@ -69,11 +76,11 @@ def test_stage_boxes_match_2d_boxes_and_oracle(shape):
         H.assert_close(out[0].double().numpy(), ref, bound, out_dtype, "stage boxes %s" % (shape,))
 
 
-# block-scaled operands (gemm_mx): the same whole-stage operand boxes (K a
-# multiple of 128 here; packed E2M1 through its 16U4_ALIGN16B maps), scales
-# per sub-block as before
+# block-scaled operands (gemm_mx): the same whole-stage operand boxes (packed
+# E2M1 through its 16U4_ALIGN16B maps; K = 1000 has a partial last stage),
+# scales per sub-block as before
 MX_SHAPES = [(640, 520, 1024, "e4m3", 0.0), (264, 448, 640, "e5m2", 1.0), (520, 392, 1000, "e4m3", 1.0),
-             (384, 392, 1152, "e2m1", 1.0)]
+             (384, 392, 1152, "e2m1", 1.0), (264, 448, 1000, "e5m2", 0.0)]
 
 
 @pytest.mark.parametrize("shape", MX_SHAPES, ids=lambda s: "%dx%dx%d_%s_b%g" % s)
