@@ -763,7 +763,7 @@ int describe_tcgen05(TcgenLaunch* L, const Plan& pl, void* D, const void* A, con
     // A whole stage in one box for the kernels whose stages hold two K
     // sub-blocks (GEMM_STAGE_BOXES=0: always the 2-D boxes).  Measured
     // against the 2-D boxes: 8192^3 +0.6 to +0.8 %, 4096^3 bf16 beta = 1
-    // +1.0 %, 8192^2 x 4096 +0.9 %, 512^3 -11 % time, 1000^3 -3 % time.
+    // +1.0 %, 8192^2 x 4096 +0.9 %, 512^3 -11 % time, 1000^3 -4 % time.
     // (The operand supply itself is not the limit: in this kernel's access
     // pattern TMA delivers ~95 bytes per SM clock on every SM with either
     // form, against the 64 the tensor pipe needs.)  The 8-epilogue-warp

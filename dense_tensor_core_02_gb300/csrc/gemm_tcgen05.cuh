@@ -379,10 +379,12 @@ __global__ void __launch_bounds__(Cfg<kPair, kEpiW, kTileN, kMX>::kNumThreads, 1
             for (int s = 0; s < Cf::kStages; ++s) ptx::mbar_init(sf_bar(s), 1);
         *abort_flag = 0;
         ptx::fence_mbarrier_init();
-        ptx::prefetch_tensormap(&tmA);
-        ptx::prefetch_tensormap(&tmB);
+        // the maps the producer reads: the whole-stage ones first, the 2-D
+        // ones where some stage takes them
         if (p.a_box_dims > 2) ptx::prefetch_tensormap(&tmAs);
         if (p.b_box_dims > 2) ptx::prefetch_tensormap(&tmBs);
+        if (p.a_box_dims == 2 || p.a_whole_stages < p.num_k_blocks) ptx::prefetch_tensormap(&tmA);
+        if (p.b_box_dims == 2 || p.b_whole_stages < p.num_k_blocks) ptx::prefetch_tensormap(&tmB);
         ptx::prefetch_tensormap(&tmD);
         if constexpr (kHasC) ptx::prefetch_tensormap(&tmC);
         if constexpr (kMX) {
